@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark of the sharded mixed-precision AdamW step over a flat, padded buffer.
+
+One step = one pass of the hot path over one batch of synthetic gradients:
+reduce-scatter with averaging over N_d simulated ranks, AdamW on every rank's
+shard, all-gather of the bf16 parameters into every rank's replica - the
+fused single-launch kernel over the whole flat space (zs_fused_step).
+
+Default workload: Llama-style 1.3B flat buffer (24 layers, d 2048, SwiGLU
+5504, vocab 32000, untied), N_d = 8 simulated ranks, ZeRO-2, 25 MiB buckets,
+bf16 grads N(0, 5e-4) with 0.1% entries x100, fp32 master/m/v.  Inputs are
+59 GB, far larger than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--profile-case] [--no-e2e] [--no-cpu-baseline]
+
+With --gpus N > 1 (launched by torchrun) every rank runs an independent
+replica of the workload on its own GPU (the simulated ranks live inside one
+GPU, so there is no exchange between GPUs); value = all ranks' parameters
+updated / the slowest rank's time.  --impl reference times the CPU oracle on
+the host cores on a bounded sample of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sharded AdamW step params/sec and achieved HBM GB/s vs 8 TB/s (1 GB300)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def maybe_init_dist(ws, backend):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(dist, value, device):
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ peaks, clocks, profiles
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    csrc = os.path.join(ROOT, "fsdp_sharded_optimizer_flatparameter_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, kernel_key):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel_key, workload))
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if line.startswith("- ") and ":" in line:
+                    k, v = line[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("source_digest") != source_digest():
+            return None
+        return float(fields["traffic_bytes_per_full_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of the benchmarked GPU during the timed region."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.bus = None
+        try:
+            import torch
+
+            p = torch.cuda.get_device_properties(device_index)
+            self.bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            pass
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        rows = []
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.bus and parts[1].upper() != self.bus.upper():
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
+        power = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ workloads
+
+def bytes_per_padded_element(n_d, kernel):
+    """Algorithmic HBM bytes per padded element of one launch (each byte crosses HBM once)."""
+    if kernel == "fused":          # read N_d bf16 grads + master/m/v; write master/m/v + N_d bf16 replicas
+        return 2 * n_d + 12 + 12 + 2 * n_d
+    if kernel == "unfused":        # RS (N_d reads, 1 write) + AdamW (2 + 12 read, 12 + 2 write) + AG (2 read, N_d writes)
+        return (2 * n_d + 2) + (14 + 14) + (2 + 2 * n_d)
+    raise ValueError(kernel)
+
+
+def oracle_sample(n_d, sample_elems, sigma, outlier_p, seed):
+    """Inputs for the oracle's ZeRO step on a bounded sample of the flat buffer."""
+    import numpy as np
+    import torch
+
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    grads, _ = synth.rank_grads(n_d, sample_elems, [], seed=seed, step=1, sigma=sigma, outlier_p=outlier_p)
+    g_np = [g.contiguous().view(torch.int16).numpy().view(np.uint16).copy() for g in grads]
+    master = synth.master_init(sample_elems, [], seed).numpy().copy()
+    return g_np, master
+
+
+def time_oracle(n_d, sample_elems, sigma, outlier_p, seed, min_seconds, max_reps=1000, reps=None):
+    """Runs the oracle's ZeRO step (reduce-scatter with averaging, AdamW per rank, all-gather)
+    on a flat buffer of sample_elems elements; returns (seconds per step, steps)."""
+    import numpy as np
+
+    from oracle import layout, steps
+
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    plan = layout.make_plan([(sample_elems,)], n_d, bucket_bytes=25 << 20)
+    g_np, master = oracle_sample(n_d, plan.padded, sigma, outlier_p, seed)
+    om = [steps.shard_of(plan, r, master) for r in range(n_d)]
+    omm = [np.zeros(plan.shard_total, np.float32) for _ in range(n_d)]
+    ov = [np.zeros(plan.shard_total, np.float32) for _ in range(n_d)]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        _, om, omm, ov = steps.zero_step(plan, g_np, om, omm, ov, synth.HPARAMS, done + 1)
+        done += 1
+        el = time.perf_counter() - t0
+        if reps is not None and done >= reps:
+            break
+        if reps is None and (el >= min_seconds or done >= max_reps):
+            break
+    return el / done, done, plan.padded
+
+
+def cpu_threads_used():
+    # numpy element-wise ufuncs run on one thread
+    return 1
+
+
+# ------------------------------------------------------------------ reference arm: the CPU oracle
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    n_d = wl["n_d"]
+    sample = 1 << 20
+    for _ in range(args.warmup):
+        time_oracle(n_d, sample, wl["sigma"], wl["outlier_p"], wl["seed"], 0, reps=1)
+    per_step, done, padded = time_oracle(n_d, sample, wl["sigma"], wl["outlier_p"], wl["seed"], 0, reps=args.steps)
+    value = padded / per_step
+    desc = ("oracle ZeRO step (numpy fp32, reduce-scatter-mean + AdamW + all-gather) on a %d-element sample "
+            "of the %s flat buffer, N_d=%d, one sample per step" % (padded, wl["model"], n_d))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "sample_elems": padded, "n_d": n_d},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": cpu_threads_used(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = maybe_init_dist(ws, "nccl")
+
+    wl = dict(synth.WORKLOADS[args.workload])
+    shapes, units = synth.workload_params(wl["model"])
+    if args.profile_case:
+        # the same kernel on a smaller flat buffer (32 Mi elements, 1.9 GB at N_d = 8): for ncu captures
+        shapes, units = [(32 << 20,)], None
+    n_d = wl["n_d"]
+    plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"], unit_of_param=units)
+    P, pads = plan.padded, plan.pad_ranges()
+    hp = synth.HPARAMS
+    if wl["stage"] == 3:
+        raise SystemExit("the default step is the ZeRO-1/2 fused step; use bench_zero3 for ZeRO-3 workloads")
+
+    t_setup = time.perf_counter()
+    master = synth.master_init(P, pads, wl["seed"], device=dev)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    grads, gbase = synth.rank_buffers(n_d, P, torch.bfloat16, dev)
+    synth.fill_grads(grads, pads, wl["seed"], 1, wl["sigma"], wl["outlier_p"])
+    reps, rbase = synth.rank_buffers(n_d, P, torch.bfloat16, dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    log("setup %.1fs: %s, %d params (padded %d), N_d=%d, %.1f GB resident" % (
+        time.perf_counter() - t_setup, args.workload, plan.numel, P, n_d,
+        (gbase.numel() * 2 + rbase.numel() * 2 + 3 * master.numel() * 4) / 1e9))
+
+    step = [0]
+
+    def one_step():
+        step[0] += 1
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, step[0], stream=stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)                              # let the sampler see the start of the region
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        one_step()
+        ev[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(dist, total_ms, dev)
+    kernel_ms = statistics.mean(launch_ms)
+
+    value = ws * plan.numel * args.steps / (total_ms / 1e3)
+    bpe = bytes_per_padded_element(n_d, "fused")
+    algo_bytes = bpe * P
+    achieved = algo_bytes / (kernel_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # the unfused path on the same buffers, for comparison (not part of value)
+    unfused = None
+    if not args.profile_case and rank == 0 and args.unfused_steps > 0:
+        ghat = torch.empty(P, dtype=torch.bfloat16, device=dev)
+        shards = torch.empty(P, dtype=torch.bfloat16, device=dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for k in range(args.unfused_steps + 2):
+            if k == 2:
+                a.record(stream)
+            step[0] += 1
+            zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED, stream=stream)
+            zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, master, m, v, [shards], zs.ZS_SHARDED, hp,
+                                   step[0], stream=stream)
+            zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ums = a.elapsed_time(b) / args.unfused_steps
+        unfused = {"ms_per_step": ums, "params_per_s": plan.numel / (ums / 1e3),
+                   "algorithmic_gbs": bytes_per_padded_element(n_d, "unfused") * P / (ums / 1e3) / 1e9,
+                   "launches_per_step": 3}
+        del ghat, shards
+
+    # end to end through the C ABI with host buffers: H2D of every rank's gradients, the step, D2H of a replica
+    e2e = None
+    if not args.no_e2e and not args.profile_case:
+        host_g = torch.empty((n_d, P), dtype=torch.bfloat16, pin_memory=True)
+        for q in range(n_d):
+            host_g[q].copy_(grads[q], non_blocking=False)
+        host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+        hptrs = [host_g[q].data_ptr() for q in range(n_d)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(2, min(args.steps, 5))
+        for k in range(n_e2e + 1):
+            if k == 1:
+                a.record(stream)
+            step[0] += 1
+            zs.zs_fused_step_host(plan, hptrs, grads, master, m, v, reps, hp, step[0], host_out.data_ptr(),
+                                  stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = max_over_ranks(dist, a.elapsed_time(b) / n_e2e, dev)
+        e2e = {"value": ws * plan.numel / (ems / 1e3), "unit": "params/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": n_d * P * 2, "d2h_bytes_per_step": P * 2}
+        del host_g, host_out
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and not args.profile_case:
+        per_step, done, padded = time_oracle(n_d, 1 << 20, wl["sigma"], wl["outlier_p"], wl["seed"], 10.0)
+        cpu = {"value": padded / per_step, "unit": "params/s", "cores": cpu_threads_used(), "kind": "oracle",
+               "sample": "oracle ZeRO step (numpy fp32) on a %d-element sample of the %s flat buffer, N_d=%d, "
+                         "%d steps in %.1f s" % (padded, wl["model"], n_d, done, per_step * done)}
+
+    if rank == 0:
+        traffic = profiled_traffic(args.workload, "k_fused") if not args.profile_case else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload + ("-profile-case" if args.profile_case else ""),
+                       "model_shape": wl["model"], "params": plan.numel, "padded": P, "n_d": n_d,
+                       "stage": "zero%d" % wl["stage"], "bucket_bytes": wl["bucket_bytes"],
+                       "step": "fused reduce-scatter-mean + AdamW + all-gather, one launch",
+                       "storage": "bf16 params/grads, fp32 master/m/v",
+                       "l2": "inputs %.0f GB >> 129 MB L2, no flush" % ((4 * n_d + 24) * P / 1e9),
+                       "parallelism": "replicas" if ws > 1 else "1 GPU, %d simulated ranks" % n_d},
+            "hbm_gbs": achieved,
+            "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
+                         "bytes_per_padded_element": bpe, "kernel": "k_fused<%d,broadcast>" % n_d,
+                         "kernel_ms": kernel_ms},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "unfused": unfused,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama-1.3b-zero2")
+    ap.add_argument("--profile-case", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused-steps", type=int, default=10)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and not args.profile_case:
+        log("note: fewer than 3 warm-up steps")
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    return run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,337 @@
+"""Python binding of ``libzs.so``: the sharded mixed-precision AdamW step over a flat, padded buffer.
+
+The functions here carry the C ABI's names (``include/zs.h``) and only
+marshal arguments: torch tensors (or raw integer addresses) become pointers,
+the current CUDA stream becomes the stream argument, and a negative status
+becomes a :class:`ZsError`.  Every step of the method runs in the library's
+CUDA kernels; there is no Python or CPU fallback.  When the shared library
+is missing, importing this package raises an error that says how to build it.
+
+Before a device call the binding checks that each tensor argument is a CUDA
+tensor of the right element size holding at least the elements the call
+will touch, because the C ABI receives bare pointers and cannot.
+"""
+
+import ctypes
+import os
+
+from ._lib import LIB_PATH, load_library
+
+_lib = load_library()
+
+ZS_OK = 0
+ZS_ERR_INVALID = -1
+ZS_ERR_CUDA = -2
+ZS_ERR_OOM_HOST = -3
+ZS_ERR_UNSUPPORTED = -5
+
+ZS_STAGE_DP, ZS_STAGE_ZERO1, ZS_STAGE_ZERO2, ZS_STAGE_ZERO3 = 0, 1, 2, 3
+ZS_RANK_FULL, ZS_SHARDED, ZS_RANK_BUCKET, ZS_RANK_UNIT = 0, 1, 2, 3
+ZS_MAX_RANKS = 64
+
+c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+P_i64 = ctypes.POINTER(c_i64)
+P_i32 = ctypes.POINTER(c_i32)
+
+
+class ZsError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("zs status %d: %s" % (status, message))
+        self.status = status
+
+
+class zs_adamw_hparams(ctypes.Structure):
+    _fields_ = [("lr", c_f32), ("beta1", c_f32), ("beta2", c_f32), ("eps", c_f32), ("weight_decay", c_f32)]
+
+
+def _sig(name, args, res=c_i32):
+    f = getattr(_lib, name)
+    f.argtypes = args
+    f.restype = res
+    return f
+
+
+_sig("zs_plan_create", [c_i32, P_i32, P_i64, P_i32, c_i32, c_i32, c_i64, ctypes.POINTER(c_vp)])
+_sig("zs_plan_destroy", [c_vp], None)
+_sig("zs_plan_info", [c_vp, P_i64, P_i64, P_i64, P_i32, P_i32, P_i32, P_i32])
+_sig("zs_plan_unit", [c_vp, c_i32, P_i64, P_i64, P_i64, P_i64])
+_sig("zs_plan_bucket", [c_vp, c_i32, P_i32, P_i64, P_i64])
+_sig("zs_plan_bucket_rank_slice", [c_vp, c_i32, c_i32, P_i64, P_i64])
+_sig("zs_plan_param", [c_vp, c_i32, P_i32, P_i64, P_i64])
+_sig("zs_plan_param_segment", [c_vp, c_i32, c_i32, P_i64, P_i64, P_i64])
+_sig("zs_plan_memory_bytes", [c_vp, c_i32, P_i64])
+_sig("zs_plan_comm_bytes", [c_vp, c_i32, c_i32, P_i64])
+_sig("zs_adamw_scalars", [ctypes.POINTER(zs_adamw_hparams), c_i64, ctypes.POINTER(c_f32)])
+_sig("zs_last_error", [], ctypes.c_char_p)
+_sig("zs_accumulate_grad", [c_vp, c_vp, c_vp, c_f32, c_i32, c_vp])
+_sig("zs_reduce_scatter_mean", [c_vp, c_i32, c_vp, c_i32, c_vp, c_i32, c_vp])
+_sig("zs_adamw_shard_step", [c_vp, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32,
+                             ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
+_sig("zs_all_gather", [c_vp, c_vp, c_i32, c_vp, c_vp])
+_sig("zs_fused_step", [c_vp, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
+                       ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
+_sig("zs_fused_step_host", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                            ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp])
+_sig("zs_zero3_gather_unit", [c_vp, c_i32, c_vp, c_vp, c_vp])
+_sig("zs_zero3_rs_step_unit", [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                               ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
+
+EXPORTED = [
+    "zs_plan_create", "zs_plan_destroy", "zs_plan_info", "zs_plan_unit", "zs_plan_bucket",
+    "zs_plan_bucket_rank_slice", "zs_plan_param", "zs_plan_param_segment", "zs_plan_memory_bytes",
+    "zs_plan_comm_bytes", "zs_adamw_scalars", "zs_last_error", "zs_accumulate_grad",
+    "zs_reduce_scatter_mean", "zs_adamw_shard_step", "zs_all_gather", "zs_fused_step",
+    "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit",
+]
+
+
+def _check(status):
+    if status != ZS_OK:
+        raise ZsError(status, _lib.zs_last_error().decode())
+    return status
+
+
+def zs_last_error():
+    return _lib.zs_last_error().decode()
+
+
+# ------------------------------------------------------------------ plan
+
+class Plan:
+    """Owns a zs_plan_t.  Queries return plain Python integers."""
+
+    def __init__(self, shapes, n_d, stage=ZS_STAGE_ZERO1, bucket_bytes=0, unit_of_param=None):
+        self._h = None
+        shapes = [tuple(int(d) for d in s) for s in shapes]
+        n = len(shapes)
+        ndims = (c_i32 * max(n, 1))(*[len(s) for s in shapes])
+        flat = [d for s in shapes for d in s]
+        dims = (c_i64 * max(len(flat), 1))(*flat)
+        units = None
+        if unit_of_param is not None:
+            units = (c_i32 * max(n, 1))(*[int(u) for u in unit_of_param])
+        h = c_vp()
+        _check(_lib.zs_plan_create(n, ndims, dims, units, int(n_d), int(stage), int(bucket_bytes), ctypes.byref(h)))
+        self._h = h
+        info = self.info()
+        self.numel, self.padded, self.shard_per_rank = info["numel"], info["padded"], info["shard_per_rank"]
+        self.n_units, self.n_buckets, self.n_d, self.stage = (info["n_units"], info["n_buckets"],
+                                                              info["n_d"], info["stage"])
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _lib.zs_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def info(self):
+        a, b, c = c_i64(), c_i64(), c_i64()
+        d, e, f, g = c_i32(), c_i32(), c_i32(), c_i32()
+        _check(_lib.zs_plan_info(self._h, *(ctypes.byref(x) for x in (a, b, c, d, e, f, g))))
+        return {"numel": a.value, "padded": b.value, "shard_per_rank": c.value, "n_units": d.value,
+                "n_buckets": e.value, "n_d": f.value, "stage": g.value}
+
+    def unit(self, u):
+        a, b, c, d = c_i64(), c_i64(), c_i64(), c_i64()
+        _check(_lib.zs_plan_unit(self._h, int(u), *(ctypes.byref(x) for x in (a, b, c, d))))
+        return {"base": a.value, "numel": b.value, "padded": c.value, "shard": d.value}
+
+    def bucket(self, b):
+        u, lo, hi = c_i32(), c_i64(), c_i64()
+        _check(_lib.zs_plan_bucket(self._h, int(b), ctypes.byref(u), ctypes.byref(lo), ctypes.byref(hi)))
+        return u.value, lo.value, hi.value
+
+    def bucket_rank_slice(self, b, rank):
+        lo, hi = c_i64(), c_i64()
+        _check(_lib.zs_plan_bucket_rank_slice(self._h, int(b), int(rank), ctypes.byref(lo), ctypes.byref(hi)))
+        return lo.value, hi.value
+
+    def param(self, k):
+        u, off, n = c_i32(), c_i64(), c_i64()
+        _check(_lib.zs_plan_param(self._h, int(k), ctypes.byref(u), ctypes.byref(off), ctypes.byref(n)))
+        return u.value, off.value, n.value
+
+    def param_segment(self, k, rank):
+        a, b, c = c_i64(), c_i64(), c_i64()
+        _check(_lib.zs_plan_param_segment(self._h, int(k), int(rank), ctypes.byref(a), ctypes.byref(b),
+                                          ctypes.byref(c)))
+        return a.value, b.value, c.value
+
+    def memory_bytes(self, stage=None):
+        out = c_i64()
+        _check(_lib.zs_plan_memory_bytes(self._h, self.stage if stage is None else int(stage), ctypes.byref(out)))
+        return out.value
+
+    def comm_bytes(self, stage=None, reshard_after_forward=True):
+        out = c_i64()
+        _check(_lib.zs_plan_comm_bytes(self._h, self.stage if stage is None else int(stage),
+                                       1 if reshard_after_forward else 0, ctypes.byref(out)))
+        return out.value
+
+    def pad_ranges(self):
+        out = []
+        for u in range(self.n_units):
+            d = self.unit(u)
+            if d["padded"] > d["numel"]:
+                out.append((d["base"] + d["numel"], d["base"] + d["padded"]))
+        return out
+
+
+def zs_adamw_scalars(hp, step):
+    out = (c_f32 * 8)()
+    _check(_lib.zs_adamw_scalars(ctypes.byref(_hp(hp)), int(step), out))
+    return list(out)
+
+
+# ------------------------------------------------------------------ marshalling helpers
+
+def _hp(hp):
+    if isinstance(hp, zs_adamw_hparams):
+        return hp
+    return zs_adamw_hparams(float(hp["lr"]), float(hp["beta1"]), float(hp["beta2"]), float(hp["eps"]),
+                            float(hp["weight_decay"]))
+
+
+def _addr(x, min_elems=None, elem_size=None, what="buffer", device=True):
+    """Address of a tensor (size-checked) or an integer address (unchecked)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if device and not x.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % what)
+        if not x.is_contiguous():
+            raise ValueError("%s must be contiguous" % what)
+        if elem_size is not None and x.element_size() != elem_size:
+            raise ValueError("%s must have %d-byte elements" % (what, elem_size))
+        if min_elems is not None and x.numel() < min_elems:
+            raise ValueError("%s holds %d elements, the call touches %d" % (what, x.numel(), min_elems))
+        return x.data_ptr()
+    raise TypeError("%s: expected a tensor or an integer address" % what)
+
+
+def _ptr_array(xs, min_elems, elem_size, what, device=True):
+    if xs is None:
+        return None
+    vals = [_addr(x, min_elems, elem_size, "%s[%d]" % (what, i), device) for i, x in enumerate(xs)]
+    return (c_vp * max(len(vals), 1))(*vals)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _bf16_elems(plan, kind, bucket=-1, unit=0):
+    if kind in (ZS_RANK_FULL, ZS_SHARDED):
+        return plan.padded
+    if kind == ZS_RANK_BUCKET:
+        _, lo, hi = plan.bucket(bucket)
+        return hi - lo
+    if kind == ZS_RANK_UNIT:
+        return plan.unit(unit)["padded"]
+    raise ValueError("unknown buffer kind %r" % (kind,))
+
+
+def _n_ptrs(kind, xs, n_d, what):
+    want = 1 if kind == ZS_SHARDED else n_d
+    if xs is not None and len(xs) != want:
+        raise ValueError("%s: expected %d pointer(s), got %d" % (what, want, len(xs)))
+
+
+# ------------------------------------------------------------------ device operations
+
+def zs_accumulate_grad(plan, acc, micro, scale, first, stream=None):
+    _n_ptrs(ZS_RANK_FULL, acc, plan.n_d, "acc")
+    _n_ptrs(ZS_RANK_FULL, micro, plan.n_d, "micro")
+    return _check(_lib.zs_accumulate_grad(plan.handle, _ptr_array(acc, plan.padded, 2, "acc"),
+                                          _ptr_array(micro, plan.padded, 2, "micro"), float(scale),
+                                          1 if first else 0, _stream(stream)))
+
+
+def zs_reduce_scatter_mean(plan, bucket, grads, grads_kind, out, out_kind, stream=None):
+    _n_ptrs(grads_kind, grads, plan.n_d, "grads")
+    _n_ptrs(out_kind, out, plan.n_d, "out")
+    ng = _bf16_elems(plan, grads_kind, bucket)
+    no = _bf16_elems(plan, out_kind, bucket)
+    return _check(_lib.zs_reduce_scatter_mean(plan.handle, int(bucket), _ptr_array(grads, ng, 2, "grads"),
+                                              int(grads_kind), _ptr_array(out, no, 2, "out"), int(out_kind),
+                                              _stream(stream)))
+
+
+def zs_adamw_shard_step(plan, rank, grad, grad_kind, master, m, v, params, params_kind, hp, step, stream=None):
+    _n_ptrs(grad_kind, grad, plan.n_d, "grad")
+    _n_ptrs(params_kind, params, plan.n_d, "params")
+    n = plan.padded
+    return _check(_lib.zs_adamw_shard_step(
+        plan.handle, int(rank), _ptr_array(grad, n, 2, "grad"), int(grad_kind),
+        _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+        _ptr_array(params, n, 2, "params"), int(params_kind), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+def zs_all_gather(plan, src, src_kind, replicas, stream=None):
+    _n_ptrs(src_kind, src, plan.n_d, "src")
+    _n_ptrs(ZS_RANK_FULL, replicas, plan.n_d, "replicas")
+    n = plan.padded
+    return _check(_lib.zs_all_gather(plan.handle, _ptr_array(src, n, 2, "src"), int(src_kind),
+                                     _ptr_array(replicas, n, 2, "replicas"), _stream(stream)))
+
+
+def zs_fused_step(plan, bucket, grads, grads_kind, master, m, v, replicas, hp, step, stream=None):
+    _n_ptrs(grads_kind, grads, plan.n_d, "grads")
+    _n_ptrs(ZS_RANK_FULL, replicas, plan.n_d, "replicas")
+    n = plan.padded
+    ng = _bf16_elems(plan, grads_kind, bucket)
+    return _check(_lib.zs_fused_step(
+        plan.handle, int(bucket), _ptr_array(grads, ng, 2, "grads"), int(grads_kind),
+        _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+        _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+def zs_fused_step_host(plan, host_grads, dev_grads, master, m, v, replicas, hp, step, host_replica0=None,
+                       stream=None):
+    _n_ptrs(ZS_RANK_FULL, host_grads, plan.n_d, "host_grads")
+    _n_ptrs(ZS_RANK_FULL, dev_grads, plan.n_d, "dev_grads")
+    n = plan.padded
+    return _check(_lib.zs_fused_step_host(
+        plan.handle, _ptr_array(host_grads, n, 2, "host_grads", device=False),
+        _ptr_array(dev_grads, n, 2, "dev_grads"),
+        _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+        _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)), int(step),
+        _addr(host_replica0, n, 2, "host_replica0", device=False), _stream(stream)))
+
+
+def zs_zero3_gather_unit(plan, unit, shards, full, stream=None):
+    _n_ptrs(ZS_RANK_UNIT, full, plan.n_d, "full")
+    nu = plan.unit(unit)["padded"]
+    return _check(_lib.zs_zero3_gather_unit(plan.handle, int(unit), _addr(shards, plan.padded, 2, "shards"),
+                                            _ptr_array(full, nu, 2, "full"), _stream(stream)))
+
+
+def zs_zero3_rs_step_unit(plan, unit, grads, master, m, v, shards, hp, step, stream=None):
+    _n_ptrs(ZS_RANK_UNIT, grads, plan.n_d, "grads")
+    n = plan.padded
+    nu = plan.unit(unit)["padded"]
+    return _check(_lib.zs_zero3_rs_step_unit(
+        plan.handle, int(unit), _ptr_array(grads, nu, 2, "grads"),
+        _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+        _addr(shards, n, 2, "shards"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+__all__ = ["Plan", "ZsError", "zs_adamw_hparams", "LIB_PATH"] + EXPORTED + [
+    n for n in dir() if n.startswith("ZS_")]
+del os

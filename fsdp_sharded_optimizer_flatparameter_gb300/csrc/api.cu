@@ -1,0 +1,313 @@
+// C ABI of the device operations: argument checks, buffer-kind resolution and
+// launches.  Every check runs before anything is enqueued, so a rejected call
+// writes nothing.  The library never allocates device memory and never
+// synchronises; all work goes on the caller's stream.
+#include <cmath>
+#include <cstdio>
+#include <string>
+
+#include "launch.h"
+#include "plan.h"
+
+using zs::BView;
+using zs::Ptrs;
+using zs::Range;
+using zs::set_error;
+
+namespace {
+
+constexpr uintptr_t kAlign = 16;
+
+bool misaligned(const void* p) { return ((uintptr_t)p & (kAlign - 1)) != 0; }
+
+int fail(const char* fn, const std::string& what) {
+    set_error(std::string(fn) + ": " + what);
+    return ZS_ERR_INVALID;
+}
+
+int cuda_status(const char* fn, cudaError_t e) {
+    if (e == cudaSuccess) return ZS_OK;
+    set_error(std::string(fn) + ": " + cudaGetErrorString(e));
+    return ZS_ERR_CUDA;
+}
+
+// Checks a pointer array of `count` entries: present, non-NULL, 16-byte aligned.
+int check_ptrs(const char* fn, const char* name, const void* const* ptrs, int count) {
+    if (!ptrs) return fail(fn, std::string(name) + " is NULL");
+    for (int q = 0; q < count; ++q) {
+        if (!ptrs[q]) return fail(fn, std::string(name) + "[" + std::to_string(q) + "] is NULL (missing rank)");
+        if (misaligned(ptrs[q])) return fail(fn, std::string(name) + "[" + std::to_string(q) + "] is not 16-byte aligned");
+    }
+    return ZS_OK;
+}
+
+int check_one(const char* fn, const char* name, const void* p) {
+    if (!p) return fail(fn, std::string(name) + " is NULL");
+    if (misaligned(p)) return fail(fn, std::string(name) + " is not 16-byte aligned");
+    return ZS_OK;
+}
+
+// Resolves a bf16 buffer of the given kind into a view; `bucket_begin` and
+// `unit_base` give the origin of ZS_RANK_BUCKET and ZS_RANK_UNIT buffers.
+int make_view(const char* fn, const char* name, const void* const* ptrs, int32_t kind, int nd,
+              int64_t bucket_begin, int64_t unit_base, BView* out) {
+    int rc;
+    switch (kind) {
+        case ZS_SHARDED:
+            if ((rc = check_ptrs(fn, name, ptrs, 1)) != ZS_OK) return rc;
+            for (int q = 0; q < ZS_MAX_RANKS; ++q) out->ptr.p[q] = (uint16_t*)ptrs[0];
+            out->off = 0;
+            return ZS_OK;
+        case ZS_RANK_FULL:
+        case ZS_RANK_BUCKET:
+        case ZS_RANK_UNIT:
+            if ((rc = check_ptrs(fn, name, ptrs, nd)) != ZS_OK) return rc;
+            for (int q = 0; q < ZS_MAX_RANKS; ++q) out->ptr.p[q] = q < nd ? (uint16_t*)ptrs[q] : nullptr;
+            out->off = kind == ZS_RANK_FULL ? 0 : (kind == ZS_RANK_BUCKET ? bucket_begin : unit_base);
+            return ZS_OK;
+        default:
+            return fail(fn, std::string(name) + ": unknown buffer kind");
+    }
+}
+
+int check_hp(const char* fn, const zs_adamw_hparams* hp, int64_t step, zs::AdamScalars* s) {
+    if (!hp) return fail(fn, "hparams is NULL");
+    if (step < 1) return fail(fn, "step must be >= 1 (1-based)");
+    const float vals[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+    for (float x : vals)
+        if (!std::isfinite(x)) return fail(fn, "hyper-parameters must be finite");
+    if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f && hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+        return fail(fn, "betas must lie in [0, 1)");
+    float sc[8];
+    zs_adamw_scalars(hp, step, sc);
+    *s = {sc[0], sc[1], sc[2], sc[3], sc[4], sc[5], sc[6], sc[7]};
+    return ZS_OK;
+}
+
+int check_plan(const char* fn, zs_plan_t plan) {
+    if (!plan) return fail(fn, "plan is NULL");
+    return ZS_OK;
+}
+
+int check_bucket(const char* fn, zs_plan_t plan, int32_t bucket, bool allow_all) {
+    if (bucket == -1 && allow_all) return ZS_OK;
+    if (bucket < 0 || bucket >= (int32_t)plan->buckets.size()) return fail(fn, "bucket out of range");
+    return ZS_OK;
+}
+
+Range unit_range(const zs::Unit& u) { return {u.base, u.base + u.padded, u.base, u.shard}; }
+
+cudaStream_t as_stream(void* s) { return (cudaStream_t)s; }
+
+#define ZS_TRY(expr)                 \
+    do {                             \
+        int _rc = (expr);            \
+        if (_rc != ZS_OK) return _rc; \
+    } while (0)
+
+}  // namespace
+
+extern "C" int zs_accumulate_grad(zs_plan_t plan, void* const* acc, const void* const* micro, float scale,
+                                  int32_t first, void* stream) {
+    static const char* fn = "zs_accumulate_grad";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    ZS_TRY(check_ptrs(fn, "acc", (const void* const*)acc, plan->n_d));
+    ZS_TRY(check_ptrs(fn, "micro", micro, plan->n_d));
+    if (!std::isfinite(scale)) return fail(fn, "scale must be finite");
+    Ptrs a{}, mi{};
+    for (int q = 0; q < plan->n_d; ++q) {
+        a.p[q] = (uint16_t*)acc[q];
+        mi.p[q] = (uint16_t*)micro[q];
+    }
+    if (plan->padded == 0) return ZS_OK;
+    return cuda_status(fn, zs::launch_accumulate(a, mi, plan->n_d, plan->padded, scale, first ? 1 : 0,
+                                                 as_stream(stream)));
+}
+
+extern "C" int zs_reduce_scatter_mean(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
+                                      void* const* out, int32_t out_kind, void* stream) {
+    static const char* fn = "zs_reduce_scatter_mean";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    ZS_TRY(check_bucket(fn, plan, bucket, true));
+    if (grads_kind != ZS_RANK_FULL && grads_kind != ZS_RANK_BUCKET) return fail(fn, "grads_kind must be RANK_FULL or RANK_BUCKET");
+    if (grads_kind == ZS_RANK_BUCKET && bucket < 0) return fail(fn, "RANK_BUCKET gradients need a bucket index");
+    if (out_kind != ZS_RANK_FULL && out_kind != ZS_SHARDED) return fail(fn, "out_kind must be RANK_FULL or SHARDED");
+    const int nd = plan->n_d;
+    const int64_t bbeg = bucket >= 0 ? plan->buckets[bucket].begin : 0;
+    BView g, o;
+    ZS_TRY(make_view(fn, "grads", grads, grads_kind, nd, bbeg, 0, &g));
+    ZS_TRY(make_view(fn, "out", (const void* const*)out, out_kind, nd, 0, 0, &o));
+    const bool by_owner = out_kind == ZS_RANK_FULL;
+    if (bucket >= 0) {
+        const auto& bk = plan->buckets[bucket];
+        const auto& u = plan->units[bk.unit];
+        return cuda_status(fn, zs::launch_rs_mean(g, o, by_owner, {bk.begin, bk.end, u.base, u.shard}, nd,
+                                                  as_stream(stream)));
+    }
+    for (const auto& u : plan->units) {
+        if (u.padded == 0) continue;
+        ZS_TRY(cuda_status(fn, zs::launch_rs_mean(g, o, by_owner, unit_range(u), nd, as_stream(stream))));
+    }
+    return ZS_OK;
+}
+
+extern "C" int zs_adamw_shard_step(zs_plan_t plan, int32_t rank, const void* const* grad, int32_t grad_kind,
+                                   float* master, float* m, float* v, void* const* params, int32_t params_kind,
+                                   const zs_adamw_hparams* hp, int64_t step, void* stream) {
+    static const char* fn = "zs_adamw_shard_step";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    const int nd = plan->n_d;
+    if (rank < -1 || rank >= nd) return fail(fn, "rank out of range");
+    if (grad_kind != ZS_RANK_FULL && grad_kind != ZS_SHARDED) return fail(fn, "grad_kind must be RANK_FULL or SHARDED");
+    if (params_kind != ZS_RANK_FULL && params_kind != ZS_SHARDED) return fail(fn, "params_kind must be RANK_FULL or SHARDED");
+    ZS_TRY(check_one(fn, "master", master));
+    ZS_TRY(check_one(fn, "m", m));
+    ZS_TRY(check_one(fn, "v", v));
+    zs::AdamScalars s;
+    ZS_TRY(check_hp(fn, hp, step, &s));
+    BView g, pv;
+    ZS_TRY(make_view(fn, "grad", grad, grad_kind, nd, 0, 0, &g));
+    ZS_TRY(make_view(fn, "params", (const void* const*)params, params_kind, nd, 0, 0, &pv));
+    for (const auto& u : plan->units) {
+        Range r = unit_range(u);
+        if (rank >= 0) {
+            r.lo = u.base + (int64_t)rank * u.shard;
+            r.hi = r.lo + u.shard;
+        }
+        if (r.hi <= r.lo) continue;
+        ZS_TRY(cuda_status(fn, zs::launch_adamw(g, grad_kind == ZS_RANK_FULL, master, m, v, pv,
+                                                params_kind == ZS_RANK_FULL, r, s, as_stream(stream))));
+    }
+    return ZS_OK;
+}
+
+extern "C" int zs_all_gather(zs_plan_t plan, const void* const* src, int32_t src_kind, void* const* replicas,
+                             void* stream) {
+    static const char* fn = "zs_all_gather";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    const int nd = plan->n_d;
+    if (src_kind != ZS_RANK_FULL && src_kind != ZS_SHARDED) return fail(fn, "src_kind must be RANK_FULL or SHARDED");
+    BView sv, dv;
+    ZS_TRY(make_view(fn, "src", src, src_kind, nd, 0, 0, &sv));
+    ZS_TRY(make_view(fn, "replicas", (const void* const*)replicas, ZS_RANK_FULL, nd, 0, 0, &dv));
+    const bool in_place = src_kind == ZS_RANK_FULL;
+    if (in_place) {
+        for (int q = 0; q < nd; ++q)
+            if (src[q] != replicas[q]) return fail(fn, "RANK_FULL source must be the replicas themselves (in place)");
+    }
+    for (const auto& u : plan->units) {
+        if (u.padded == 0) continue;
+        ZS_TRY(cuda_status(fn, zs::launch_gather(sv, in_place, dv, in_place, unit_range(u), nd, as_stream(stream))));
+    }
+    return ZS_OK;
+}
+
+static int fused_common(const char* fn, zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
+                        float* master, float* m, float* v, void* const* replicas, const zs_adamw_hparams* hp,
+                        int64_t step, cudaStream_t st) {
+    ZS_TRY(check_plan(fn, plan));
+    ZS_TRY(check_bucket(fn, plan, bucket, true));
+    if (grads_kind != ZS_RANK_FULL && grads_kind != ZS_RANK_BUCKET) return fail(fn, "grads_kind must be RANK_FULL or RANK_BUCKET");
+    if (grads_kind == ZS_RANK_BUCKET && bucket < 0) return fail(fn, "RANK_BUCKET gradients need a bucket index");
+    const int nd = plan->n_d;
+    ZS_TRY(check_one(fn, "master", master));
+    ZS_TRY(check_one(fn, "m", m));
+    ZS_TRY(check_one(fn, "v", v));
+    zs::AdamScalars s;
+    ZS_TRY(check_hp(fn, hp, step, &s));
+    const int64_t bbeg = bucket >= 0 ? plan->buckets[bucket].begin : 0;
+    BView g, o;
+    ZS_TRY(make_view(fn, "grads", grads, grads_kind, nd, bbeg, 0, &g));
+    ZS_TRY(make_view(fn, "replicas", (const void* const*)replicas, ZS_RANK_FULL, nd, 0, 0, &o));
+    for (int q = 0; q < nd; ++q)
+        for (int j = 0; j < nd; ++j)
+            if (replicas[q] == grads[j]) return fail(fn, "replicas must not be the gradient buffers");
+    Range r;
+    if (bucket >= 0) {
+        const auto& bk = plan->buckets[bucket];
+        r = {bk.begin, bk.end, 0, 1};
+    } else {
+        r = {0, plan->padded, 0, 1};       // the fused step needs no owner: one pass over the flat space
+    }
+    if (r.hi <= r.lo) return ZS_OK;
+    return cuda_status(fn, zs::launch_fused(g, master, m, v, o, true, r, s, nd, st));
+}
+
+extern "C" int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
+                             float* master, float* m, float* v, void* const* replicas, const zs_adamw_hparams* hp,
+                             int64_t step, void* stream) {
+    zs::clear_error();
+    return fused_common("zs_fused_step", plan, bucket, grads, grads_kind, master, m, v, replicas, hp, step,
+                        as_stream(stream));
+}
+
+extern "C" int zs_fused_step_host(zs_plan_t plan, const void* const* host_grads, void* const* dev_grads,
+                                  float* master, float* m, float* v, void* const* replicas,
+                                  const zs_adamw_hparams* hp, int64_t step, void* host_replica0, void* stream) {
+    static const char* fn = "zs_fused_step_host";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    const int nd = plan->n_d;
+    if (!host_grads) return fail(fn, "host_grads is NULL");
+    for (int q = 0; q < nd; ++q)
+        if (!host_grads[q]) return fail(fn, "host_grads has a NULL entry (missing rank)");
+    ZS_TRY(check_ptrs(fn, "dev_grads", (const void* const*)dev_grads, nd));
+    ZS_TRY(check_ptrs(fn, "replicas", (const void* const*)replicas, nd));
+    // validate everything the fused step checks before the first copy is enqueued
+    {
+        ZS_TRY(check_one(fn, "master", master));
+        ZS_TRY(check_one(fn, "m", m));
+        ZS_TRY(check_one(fn, "v", v));
+        zs::AdamScalars s;
+        ZS_TRY(check_hp(fn, hp, step, &s));
+    }
+    cudaStream_t st = as_stream(stream);
+    const size_t bytes = (size_t)plan->padded * 2;
+    for (int q = 0; q < nd && bytes; ++q)
+        ZS_TRY(cuda_status(fn, cudaMemcpyAsync(dev_grads[q], host_grads[q], bytes, cudaMemcpyHostToDevice, st)));
+    ZS_TRY(fused_common(fn, plan, -1, (const void* const*)dev_grads, ZS_RANK_FULL, master, m, v, replicas, hp, step, st));
+    if (host_replica0 && bytes)
+        ZS_TRY(cuda_status(fn, cudaMemcpyAsync(host_replica0, replicas[0], bytes, cudaMemcpyDeviceToHost, st)));
+    return ZS_OK;
+}
+
+extern "C" int zs_zero3_gather_unit(zs_plan_t plan, int32_t unit, const void* shards, void* const* full,
+                                    void* stream) {
+    static const char* fn = "zs_zero3_gather_unit";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    if (unit < 0 || unit >= (int32_t)plan->units.size()) return fail(fn, "unit out of range");
+    const auto& u = plan->units[unit];
+    const void* sp[1] = {shards};
+    BView sv, dv;
+    ZS_TRY(make_view(fn, "shards", sp, ZS_SHARDED, plan->n_d, 0, 0, &sv));
+    ZS_TRY(make_view(fn, "full", (const void* const*)full, ZS_RANK_UNIT, plan->n_d, 0, u.base, &dv));
+    if (u.padded == 0) return ZS_OK;
+    return cuda_status(fn, zs::launch_gather(sv, false, dv, false, unit_range(u), plan->n_d, as_stream(stream)));
+}
+
+extern "C" int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads, float* master,
+                                     float* m, float* v, void* shards, const zs_adamw_hparams* hp, int64_t step,
+                                     void* stream) {
+    static const char* fn = "zs_zero3_rs_step_unit";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    if (unit < 0 || unit >= (int32_t)plan->units.size()) return fail(fn, "unit out of range");
+    const auto& u = plan->units[unit];
+    ZS_TRY(check_one(fn, "master", master));
+    ZS_TRY(check_one(fn, "m", m));
+    ZS_TRY(check_one(fn, "v", v));
+    zs::AdamScalars s;
+    ZS_TRY(check_hp(fn, hp, step, &s));
+    const void* sp[1] = {shards};
+    BView g, o;
+    ZS_TRY(make_view(fn, "grads", grads, ZS_RANK_UNIT, plan->n_d, 0, u.base, &g));
+    ZS_TRY(make_view(fn, "shards", sp, ZS_SHARDED, plan->n_d, 0, 0, &o));
+    if (u.padded == 0) return ZS_OK;
+    return cuda_status(fn, zs::launch_fused(g, master, m, v, o, false, unit_range(u), s, plan->n_d,
+                                            as_stream(stream)));
+}

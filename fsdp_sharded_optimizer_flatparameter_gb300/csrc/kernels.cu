@@ -1,0 +1,359 @@
+// Streaming kernels of the sharded optimizer step (sm_103a).
+//
+// Every step of the method is element-wise over the global flat index
+// ("Infra: Data Parallel", ZeRO section: AdamW is element-wise, so a rank can
+// update any part of the parameters from that part's mean gradient and
+// moments), so each kernel is a grid-stride loop over the index range of a
+// bucket or unit.  The body works on vectors of 8 elements (one 16-byte
+// access per bf16 rank slice, two per fp32 state array); a range whose ends
+// are not multiples of 8 has its at most 14 fringe elements done one by one
+// by block 0, and a range whose buffers cannot all be accessed in 16-byte
+// units (a bucket or unit base, or an owner boundary, off the 8-element grid)
+// runs element by element throughout.  The rank count N_d is a template
+// parameter for the common powers of two so the rank loops unroll; other
+// counts use the runtime value.  Nothing here waits on anything, so no kernel
+// can hang.
+#include <mutex>
+#include <unordered_map>
+
+#include "device.cuh"
+
+namespace zs {
+
+constexpr int kThreads = 256;
+
+// ------------------------------------------------------------------ launch geometry
+
+// Blocks for a grid-stride kernel: enough to cover the work, at most one
+// full wave of resident blocks on the current device.
+static int grid_for(const void* kernel, int64_t items) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cap_cache;     // (device, kernel) -> resident blocks
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t key = ((uint64_t)(uintptr_t)kernel) ^ ((uint64_t)dev << 56);
+    int cap;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cap_cache.find(key);
+        if (it == cap_cache.end()) {
+            int sms = 0, occ = 0;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+            cap = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
+            cap_cache.emplace(key, cap);
+        } else {
+            cap = it->second;
+        }
+    }
+    int64_t want = (items + kThreads - 1) / kThreads;
+    if (want < 1) want = 1;
+    return (int)(want < cap ? want : cap);
+}
+
+// Split [lo, hi) into an 8-aligned vector body and a scalar fringe.
+struct Split {
+    int64_t lo, hi;      // whole range
+    int64_t vlo;         // first element of the vector body
+    int64_t nvec;        // vectors of 8 in the body (0: run everything one by one)
+};
+
+static Split split_range(int64_t lo, int64_t hi, bool vec_ok) {
+    Split s{lo, hi, lo, 0};
+    if (!vec_ok) return s;
+    const int64_t vlo = (lo + 7) & ~int64_t(7);
+    const int64_t vhi = hi & ~int64_t(7);
+    if (vhi > vlo) {
+        s.vlo = vlo;
+        s.nvec = (vhi - vlo) >> 3;
+    }
+    return s;
+}
+
+// Runs op.template run<8>(i) over the body and op.template run<1>(i) over the fringe.
+template <class Op>
+__device__ __forceinline__ void for_range(const Split& sp, const Op& op) {
+    if (sp.nvec > 0) {
+        for (int64_t t = gtid(); t < sp.nvec; t += gstride()) op.template run<8>(sp.vlo + (t << 3));
+        const int64_t nhead = sp.vlo - sp.lo;
+        const int64_t tail0 = sp.vlo + (sp.nvec << 3);
+        const int64_t nfringe = nhead + (sp.hi - tail0);
+        if (blockIdx.x == 0 && (int64_t)threadIdx.x < nfringe) {
+            const int64_t j = threadIdx.x;
+            op.template run<1>(j < nhead ? sp.lo + j : tail0 + (j - nhead));
+        }
+    } else {
+        for (int64_t i = sp.lo + gtid(); i < sp.hi; i += gstride()) op.template run<1>(i);
+    }
+}
+
+__device__ __forceinline__ int owner_of(int64_t i, int64_t base, int64_t shard) { return (int)((i - base) / shard); }
+
+// ------------------------------------------------------------------ gradient accumulation
+
+struct AccumArgs {
+    Ptrs acc, micro;
+    float scale;
+    int first;
+};
+
+// One rank's buffers (blockIdx.y selects the rank).
+struct AccumOp {
+    uint16_t* acc;
+    const uint16_t* micro;
+    float scale;
+    int first;
+    template <int VEC>
+    __device__ __forceinline__ void run(int64_t i) const {
+        float g[VEC], prev[VEC];
+        unpack(ld_bf<VEC>(micro + i), g);
+        if (first) {
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) prev[k] = 0.0f;
+        } else {
+            unpack(ld_bf<VEC>(acc + i), prev);
+        }
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) prev[k] = __fadd_rn(prev[k], __fmul_rn(g[k], scale));
+        st_bf<VEC>(acc + i, pack(prev));
+    }
+};
+
+__global__ void __launch_bounds__(kThreads) k_accumulate(AccumArgs a, Split sp) {
+    const AccumOp op{a.acc.p[blockIdx.y], a.micro.p[blockIdx.y], a.scale, a.first};
+    for_range(sp, op);
+}
+
+cudaError_t launch_accumulate(const Ptrs& acc, const Ptrs& micro, int nd, int64_t n, float scale, int first,
+                              cudaStream_t st) {
+    AccumArgs a{acc, micro, scale, first};
+    Split sp = split_range(0, n, true);
+    dim3 grid(grid_for((const void*)k_accumulate, sp.nvec > 0 ? sp.nvec : n), nd);
+    k_accumulate<<<grid, kThreads, 0, st>>>(a, sp);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ reduce-scatter with averaging
+
+template <int ND>
+struct RsOp {
+    BView g, out;
+    int out_by_owner;
+    int nd;
+    float inv_nd;
+    int64_t base, shard;
+    template <int VEC>
+    __device__ __forceinline__ void run(int64_t i) const {
+        const int n = ND > 0 ? ND : nd;
+        float acc[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            float f[VEC];
+            unpack(ld_bf<VEC>(g.ptr.p[q] + (i - g.off)), f);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = mean_of_sum<ND>(acc[k], n, inv_nd);
+        const int qo = out_by_owner ? owner_of(i, base, shard) : 0;
+        st_bf<VEC>(out.ptr.p[qo] + (i - out.off), pack(acc));
+    }
+};
+
+template <int ND>
+__global__ void __launch_bounds__(kThreads) k_rs_mean(RsOp<ND> op, Split sp) { for_range(sp, op); }
+
+template <int ND>
+static cudaError_t rs_impl(const BView& g, const BView& out, bool by_owner, const Range& r, int nd, Split sp,
+                           cudaStream_t st) {
+    RsOp<ND> op{g, out, by_owner ? 1 : 0, nd, 1.0f / (float)nd, r.base, r.shard};
+    const int grid = grid_for((const void*)k_rs_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    k_rs_mean<ND><<<grid, kThreads, 0, st>>>(op, sp);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ AdamW on a shard
+
+struct AdamOp {
+    BView grad, par;
+    int grad_by_owner, par_by_owner;
+    float *master, *m, *v;
+    AdamScalars s;
+    int64_t base, shard;
+    template <int VEC>
+    __device__ __forceinline__ void run(int64_t i) const {
+        const int q = (grad_by_owner | par_by_owner) ? owner_of(i, base, shard) : 0;
+        float g[VEC], p[VEC], mm[VEC], vv[VEC];
+        unpack(ld_bf<VEC>(grad.ptr.p[grad_by_owner ? q : 0] + (i - grad.off)), g);
+        ld_f32<VEC>(master + i, p);
+        ld_f32<VEC>(m + i, mm);
+        ld_f32<VEC>(v + i, vv);
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) adamw_elem(g[k], p[k], mm[k], vv[k], s);
+        st_f32<VEC>(master + i, p);
+        st_f32<VEC>(m + i, mm);
+        st_f32<VEC>(v + i, vv);
+        st_bf<VEC>(par.ptr.p[par_by_owner ? q : 0] + (i - par.off), pack(p));
+    }
+};
+
+__global__ void __launch_bounds__(kThreads) k_adamw(AdamOp op, Split sp) { for_range(sp, op); }
+
+// ------------------------------------------------------------------ all-gather (copy to every rank)
+
+template <int ND>
+struct GatherOp {
+    BView src, dst;
+    int src_by_owner, skip_owner;
+    int nd;
+    int64_t base, shard;
+    template <int VEC>
+    __device__ __forceinline__ void run(int64_t i) const {
+        const int n = ND > 0 ? ND : nd;
+        const int o = (src_by_owner | skip_owner) ? owner_of(i, base, shard) : -1;
+        const BfVec<VEC> w = ld_bf<VEC>(src.ptr.p[src_by_owner ? o : 0] + (i - src.off));
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            if (skip_owner && q == o) continue;
+            st_bf<VEC>(dst.ptr.p[q] + (i - dst.off), w);
+        }
+    }
+};
+
+template <int ND>
+__global__ void __launch_bounds__(kThreads) k_gather(GatherOp<ND> op, Split sp) { for_range(sp, op); }
+
+template <int ND>
+static cudaError_t gather_impl(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
+                               const Range& r, int nd, Split sp, cudaStream_t st) {
+    GatherOp<ND> op{src, dst, src_by_owner ? 1 : 0, skip_owner ? 1 : 0, nd, r.base, r.shard};
+    const int grid = grid_for((const void*)k_gather<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    k_gather<ND><<<grid, kThreads, 0, st>>>(op, sp);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ fused: reduce-mean + AdamW + scatter
+
+template <int ND, bool BROADCAST>
+struct FusedOp {
+    BView g, out;
+    float *master, *m, *v;
+    AdamScalars s;
+    int nd;
+    float inv_nd;
+    template <int VEC>
+    __device__ __forceinline__ void run(int64_t i) const {
+        const int n = ND > 0 ? ND : nd;
+        float acc[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            float f[VEC];
+            unpack(ld_bf<VEC>(g.ptr.p[q] + (i - g.off)), f);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+        }
+        float p[VEC], mm[VEC], vv[VEC], gr[VEC];
+        ld_f32<VEC>(master + i, p);
+        ld_f32<VEC>(m + i, mm);
+        ld_f32<VEC>(v + i, vv);
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = mean_of_sum<ND>(acc[k], n, inv_nd);
+        unpack(pack(acc), gr);                  // the reduced gradient is a bf16 value
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) adamw_elem(gr[k], p[k], mm[k], vv[k], s);
+        st_f32<VEC>(master + i, p);
+        st_f32<VEC>(m + i, mm);
+        st_f32<VEC>(v + i, vv);
+        const BfVec<VEC> w = pack(p);
+        if constexpr (BROADCAST) {
+#pragma unroll
+            for (int q = 0; q < n; ++q) {
+                st_bf<VEC>(out.ptr.p[q] + (i - out.off), w);
+            }
+        } else {
+            st_bf<VEC>(out.ptr.p[0] + (i - out.off), w);
+        }
+    }
+};
+
+template <int ND, bool BROADCAST>
+__global__ void __launch_bounds__(kThreads) k_fused(FusedOp<ND, BROADCAST> op, Split sp) { for_range(sp, op); }
+
+template <int ND, bool BROADCAST>
+static cudaError_t fused_impl(const BView& g, float* master, float* m, float* v, const BView& out,
+                              const AdamScalars& s, int nd, Split sp, cudaStream_t st) {
+    FusedOp<ND, BROADCAST> op{g, out, master, m, v, s, nd, 1.0f / (float)nd};
+    const int grid = grid_for((const void*)k_fused<ND, BROADCAST>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    k_fused<ND, BROADCAST><<<grid, kThreads, 0, st>>>(op, sp);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dispatch
+
+static bool aligned8(int64_t x) { return (x & 7) == 0; }
+
+#define ZS_DISPATCH_ND(nd, CALL)            \
+    switch (nd) {                           \
+        case 1: return CALL(1);             \
+        case 2: return CALL(2);             \
+        case 4: return CALL(4);             \
+        case 8: return CALL(8);             \
+        case 16: return CALL(16);           \
+        case 32: return CALL(32);           \
+        default: return CALL(0);            \
+    }
+
+cudaError_t launch_rs_mean(const BView& g, const BView& out, bool out_by_owner, const Range& r, int nd,
+                           cudaStream_t st) {
+    const bool vec = aligned8(g.off) && aligned8(out.off) &&
+                     (!out_by_owner || (aligned8(r.base) && aligned8(r.shard)));
+    const Split sp = split_range(r.lo, r.hi, vec);
+#define ZS_RS(N) rs_impl<N>(g, out, out_by_owner, r, nd, sp, st)
+    ZS_DISPATCH_ND(nd, ZS_RS)
+#undef ZS_RS
+}
+
+cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, float* m, float* v,
+                         const BView& par, bool par_by_owner, const Range& r, const AdamScalars& s,
+                         cudaStream_t st) {
+    const bool by_owner = grad_by_owner || par_by_owner;
+    const bool vec = aligned8(grad.off) && aligned8(par.off) &&
+                     (!by_owner || (aligned8(r.base) && aligned8(r.shard)));
+    const Split sp = split_range(r.lo, r.hi, vec);
+    AdamOp op{grad, par, grad_by_owner ? 1 : 0, par_by_owner ? 1 : 0, master, m, v, s, r.base, r.shard};
+    const int grid = grid_for((const void*)k_adamw, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    k_adamw<<<grid, kThreads, 0, st>>>(op, sp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
+                          const Range& r, int nd, cudaStream_t st) {
+    const bool by_owner = src_by_owner || skip_owner;
+    const bool vec = aligned8(src.off) && aligned8(dst.off) &&
+                     (!by_owner || (aligned8(r.base) && aligned8(r.shard)));
+    const Split sp = split_range(r.lo, r.hi, vec);
+#define ZS_GA(N) gather_impl<N>(src, src_by_owner, dst, skip_owner, r, nd, sp, st)
+    ZS_DISPATCH_ND(nd, ZS_GA)
+#undef ZS_GA
+}
+
+cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
+    const bool vec = aligned8(g.off) && aligned8(out.off);
+    const Split sp = split_range(r.lo, r.hi, vec);
+    if (broadcast) {
+#define ZS_FB(N) fused_impl<N, true>(g, master, m, v, out, s, nd, sp, st)
+        ZS_DISPATCH_ND(nd, ZS_FB)
+#undef ZS_FB
+    } else {
+#define ZS_FS(N) fused_impl<N, false>(g, master, m, v, out, s, nd, sp, st)
+        ZS_DISPATCH_ND(nd, ZS_FS)
+#undef ZS_FS
+    }
+}
+
+}  // namespace zs

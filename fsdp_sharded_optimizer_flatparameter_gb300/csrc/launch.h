@@ -1,0 +1,47 @@
+// Host-side launchers of the step's kernels (internal; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zs.h"
+
+namespace zs {
+
+// N_d rank pointers to bf16 words.
+struct Ptrs {
+    uint16_t* p[ZS_MAX_RANKS];
+};
+
+// A bf16 buffer kind resolved to addresses: rank q's element at global flat
+// index i lives at ptr.p[q] + (i - off).  A ZS_SHARDED array repeats its one
+// pointer in every slot with off = 0.
+struct BView {
+    Ptrs ptr;
+    int64_t off;
+};
+
+// The step-dependent fp32 scalars of AdamW (see zs_adamw_scalars).
+struct AdamScalars {
+    float beta1, beta2, eps, decay, c1, c2, step_size, sqrt_bc2;
+};
+
+// A global range [lo, hi) inside one unit (base, shard); owner(i) = (i - base) / shard.
+struct Range {
+    int64_t lo, hi;
+    int64_t base, shard;
+};
+
+cudaError_t launch_accumulate(const Ptrs& acc, const Ptrs& micro, int nd, int64_t n, float scale, int first,
+                              cudaStream_t st);
+cudaError_t launch_rs_mean(const BView& g, const BView& out, bool out_by_owner, const Range& r, int nd,
+                           cudaStream_t st);
+cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, float* m, float* v,
+                         const BView& par, bool par_by_owner, const Range& r, const AdamScalars& s,
+                         cudaStream_t st);
+cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
+                          const Range& r, int nd, cudaStream_t st);
+cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st);
+
+}  // namespace zs

@@ -1,0 +1,259 @@
+/*
+ * zs.h - C ABI of the sharded mixed-precision AdamW step over a flat, padded
+ * parameter buffer (ZeRO-1/2/3, FSDP1 FlatParameter), for one sm_103a GPU on
+ * which the N_d data-parallel ranks are simulated as separate device buffers.
+ *
+ * The method is the one described in "Infra: Data Parallel" (F. Pu):
+ *   - section "Naive Data Parallelism": gradient buckets, gradient accumulation
+ *     over micro-batches with the loss divided by their number;
+ *   - section "Zero Redundancy Optimizer (ZeRO)": Reduce-Scatter with
+ *     averaging, an element-wise AdamW update of each rank's shard with fp32
+ *     master weights and moments (k = 12 bytes per parameter), All-Gather of
+ *     the updated 16-bit parameters; ZeRO-2 bucket-wise reduction; ZeRO-3
+ *     per-layer gather / reduce-scatter with no gather after the update;
+ *   - section "Fully Sharded Data Parallel (FSDP)", subsection "FSDP1": the
+ *     FlatParameter (flatten + concatenate the parameters of one unit, pad,
+ *     cut into N_d equal contiguous shards that may cross parameter
+ *     boundaries; a rank holding nothing of a parameter sees an empty view).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions (all entry points)
+ *
+ * Types.      Parameters and gradients are bf16 (16-bit, stored as 2-byte
+ *             words); master weights, m and v are fp32.
+ * Indices.    Every element has one GLOBAL FLAT INDEX i in [0, padded_numel):
+ *             the units' padded FlatParameters laid one after another in
+ *             unit order.  Unit u covers [base_u, base_u + padded_u); rank r
+ *             owns [base_u + r*S_u, base_u + (r+1)*S_u) of it, S_u =
+ *             padded_u / N_d.  Padding elements are zero in every buffer.
+ * Buffer kinds (how a pointer argument maps global index i of rank q):
+ *   ZS_RANK_FULL   N_d pointers; ptrs[q][i]              (whole flat space)
+ *   ZS_SHARDED     1 pointer;    ptrs[0][i]              (each rank's shard of
+ *                  every unit at its owned position: the concatenation of all
+ *                  ranks' shards; on separate GPUs each rank would hold only
+ *                  its own piece)
+ *   ZS_RANK_BUCKET N_d pointers; ptrs[q][i - bucket_begin] (one bucket)
+ *   ZS_RANK_UNIT   N_d pointers; ptrs[q][i - unit_base]    (one unit)
+ *             master, m and v are always ZS_SHARDED fp32 arrays of
+ *             padded_numel elements.
+ * Ownership.  The caller owns all device memory and all streams.  The library
+ *             never allocates device memory, never synchronises, and only
+ *             enqueues work on the given stream (a cudaStream_t; NULL is the
+ *             legacy default stream).  A plan owns host tables only.
+ * Alignment.  Every device pointer must be 16-byte aligned.
+ * Aliasing.   Inputs and outputs must not overlap unless a call says so.
+ * Step.       The AdamW step t is 1-based.
+ * Errors.     Every entry point returns ZS_OK or a negative status.  Argument
+ *             errors are found before anything is enqueued (nothing is
+ *             written); zs_last_error() then returns a message (thread-local,
+ *             valid until the next call on that thread).  Launch failures
+ *             return ZS_ERR_CUDA.  Faults inside kernels surface at the
+ *             caller's next synchronisation, as with any CUDA launch.
+ * Threads.    A plan is immutable after creation and may be shared by
+ *             threads; calls on different streams may run concurrently when
+ *             their buffers do not overlap.
+ */
+#ifndef ZS_H
+#define ZS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ codes */
+#define ZS_OK               0
+#define ZS_ERR_INVALID     (-1)   /* bad argument: nothing was enqueued              */
+#define ZS_ERR_CUDA        (-2)   /* a CUDA runtime call or launch failed            */
+#define ZS_ERR_OOM_HOST    (-3)   /* host allocation for plan tables failed          */
+#define ZS_ERR_UNSUPPORTED (-5)   /* valid request this build does not implement     */
+
+#define ZS_STAGE_DP     0         /* naive data parallel (no sharding)               */
+#define ZS_STAGE_ZERO1  1         /* optimizer state sharded                         */
+#define ZS_STAGE_ZERO2  2         /* + gradients sharded                             */
+#define ZS_STAGE_ZERO3  3         /* + parameters sharded (FSDP full shard)          */
+
+#define ZS_RANK_FULL    0
+#define ZS_SHARDED      1
+#define ZS_RANK_BUCKET  2
+#define ZS_RANK_UNIT    3
+
+#define ZS_MAX_RANKS    64        /* largest N_d accepted                            */
+
+typedef struct zs_plan_s* zs_plan_t;
+
+/* AdamW hyper-parameters, as fp32 values. */
+typedef struct {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+} zs_adamw_hparams;
+
+/* ------------------------------------------------------------------ plan (host only) */
+
+/* Build the FlatParameter plan.  "Infra: Data Parallel", FSDP section, FSDP1
+ * layout figure and subsection "FSDP1"; buckets from section "Naive Data
+ * Parallelism".
+ *   n_params        number of parameters (>= 1), in module order.
+ *   ndims[k]        rank of parameter k's shape (0..8; 0 = scalar, one element).
+ *   dims            all shapes concatenated (sum of ndims entries), each >= 1.
+ *   unit_of_param   unit id of each parameter, ids 0..U-1 all used; NULL puts
+ *                   every parameter in unit 0.  Parameters of a unit keep their
+ *                   relative order; unit u's FlatParameter is padded on its own
+ *                   with the fewest zeros that make its length a multiple of n_d.
+ *   n_d             number of data-parallel ranks, 1..ZS_MAX_RANKS.
+ *   stage           ZS_STAGE_* (recorded; used as the default for accounting).
+ *   bucket_bytes    gradient bucket size in bytes of bf16 gradients; a bucket is
+ *                   floor(bucket_bytes/2) consecutive elements of one unit (the
+ *                   last bucket of a unit is shorter).  <= 0 means one bucket per unit.
+ *   out             receives the plan; release it with zs_plan_destroy.
+ * Errors: ZS_ERR_INVALID for any out-of-range argument; ZS_ERR_OOM_HOST. */
+int zs_plan_create(int32_t n_params, const int32_t* ndims, const int64_t* dims,
+                   const int32_t* unit_of_param, int32_t n_d, int32_t stage,
+                   int64_t bucket_bytes, zs_plan_t* out);
+void zs_plan_destroy(zs_plan_t plan);
+
+/* Totals.  Any output pointer may be NULL. */
+int zs_plan_info(zs_plan_t plan, int64_t* numel, int64_t* padded_numel,
+                 int64_t* shard_numel_per_rank, int32_t* n_units, int32_t* n_buckets,
+                 int32_t* n_d, int32_t* stage);
+/* Unit u: global base index, real and padded element counts, shard size S_u. */
+int zs_plan_unit(zs_plan_t plan, int32_t u, int64_t* base, int64_t* numel,
+                 int64_t* padded_numel, int64_t* shard_numel);
+/* Bucket b (0..n_buckets-1, ordered by global index): its unit and global range [begin, end). */
+int zs_plan_bucket(zs_plan_t plan, int32_t b, int32_t* unit, int64_t* begin, int64_t* end);
+/* The part [begin, end) of bucket b that the reduce-scatter hands to rank r (begin == end: none). */
+int zs_plan_bucket_rank_slice(zs_plan_t plan, int32_t b, int32_t rank, int64_t* begin, int64_t* end);
+/* Parameter k: unit and global flat range [flat_offset, flat_offset + numel). */
+int zs_plan_param(zs_plan_t plan, int32_t k, int32_t* unit, int64_t* flat_offset, int64_t* numel);
+/* The view of parameter k on rank r ("use_orig_params", subsection "FSDP1"):
+ * global flat_begin, offset inside the rank's shard of the unit, and length.
+ * A rank holding no element of the parameter gets len = 0 and zeros for the
+ * other two (the empty view). */
+int zs_plan_param_segment(zs_plan_t plan, int32_t k, int32_t rank, int64_t* flat_begin,
+                          int64_t* shard_offset, int64_t* len);
+/* Model-state bytes one rank holds under `stage` ("Infra: Data Parallel", ZeRO
+ * memory figure): parameters and gradients at 2 bytes, master/m/v at 4 bytes
+ * each (k = 12); sharded stages hold the padded FlatParameter. */
+int zs_plan_memory_bytes(zs_plan_t plan, int32_t stage, int64_t* bytes_per_rank);
+/* Bytes one rank sends in one step under `stage` (ZeRO section, communication
+ * paragraphs; 16-bit elements, every bucket and unit summed): DP ring
+ * all-reduce, ZeRO-1/2 reduce-scatter + all-gather, ZeRO-3 reduce-scatter +
+ * one or two all-gathers (two when reshard_after_forward != 0, FSDP2
+ * subsection). */
+int zs_plan_comm_bytes(zs_plan_t plan, int32_t stage, int32_t reshard_after_forward,
+                       int64_t* bytes_sent_per_rank);
+
+/* The eight fp32 scalars AdamW uses at step t (host only), in this order:
+ * beta1, beta2, eps, decay = 1 - lr*wd, c1 = 1 - beta1, c2 = 1 - beta2,
+ * step_size = lr / (1 - beta1^t), sqrt_bc2 = sqrt(1 - beta2^t); each computed
+ * in double from the fp32 hyper-parameters, then rounded to fp32. */
+int zs_adamw_scalars(const zs_adamw_hparams* hp, int64_t step, float* out8);
+
+/* Message for the last non-OK return on this thread ("" if none). */
+const char* zs_last_error(void);
+
+/* ------------------------------------------------------------------ device operations */
+
+/* Gradient accumulation without synchronisation ("Infra: Data Parallel",
+ * section "Naive Data Parallelism", gradient-accumulation paragraph): for
+ * every rank q and element i,
+ *     acc[q][i] = bf16( fp32(acc[q][i]) + fp32(micro[q][i]) * scale )
+ * with acc taken as +0 when `first` != 0 (acc is then write-only).  `scale`
+ * is 1/n_micro for n_micro equal micro-batches whose losses are sample means.
+ * acc, micro: ZS_RANK_FULL bf16, N_d pointers each; acc may equal micro
+ * (in place). */
+int zs_accumulate_grad(zs_plan_t plan, void* const* acc, const void* const* micro,
+                       float scale, int32_t first, void* stream);
+
+/* Reduce-Scatter with averaging (ZeRO section, ZeRO-1 paragraph; ZeRO-1 and
+ * ZeRO-2 flow figures): for every element i of bucket `bucket` (or of every
+ * bucket when bucket = -1), owned by rank r,
+ *     out_r[i] = bf16( (sum over q = 0..N_d-1, ascending, of fp32 grads[q][i]) / N_d )
+ * The sum starts from +0 and is fp32.
+ *   grads_kind  ZS_RANK_FULL, or ZS_RANK_BUCKET (then bucket >= 0).
+ *   out_kind    ZS_RANK_FULL: out[r] is rank r's full buffer and only its
+ *               owned elements are written (ZeRO-1 keeps the full gradient
+ *               buffer; out may be the same array of pointers as grads, in
+ *               place);  ZS_SHARDED: out[0] is the sharded reduced gradient
+ *               (ZeRO-2). */
+int zs_reduce_scatter_mean(zs_plan_t plan, int32_t bucket, const void* const* grads,
+                           int32_t grads_kind, void* const* out, int32_t out_kind, void* stream);
+
+/* AdamW on shards (ZeRO section: AdamW is element-wise, each rank updates only
+ * its own shard with its own moments): for every element i owned by `rank`
+ * (every rank when rank = -1), with g = fp32(grad_r[i]) and the scalars of
+ * zs_adamw_scalars, each operation rounded once in fp32 and none fused:
+ *     p = master[i] * decay
+ *     m[i] = beta1*m[i] + c1*g
+ *     v[i] = beta2*v[i] + c2*(g*g)
+ *     p = p - step_size * (m[i] / (sqrt(v[i]) / sqrt_bc2 + eps))
+ *     master[i] = p;   param_r[i] = bf16(p)
+ *   grad_kind   ZS_SHARDED, or ZS_RANK_FULL (ZeRO-1: rank r's reduced slice in
+ *               its full gradient buffer).
+ *   params_kind ZS_RANK_FULL: written into rank r's replica at its owned
+ *               position (the source of an in-place all-gather);  ZS_SHARDED. */
+int zs_adamw_shard_step(zs_plan_t plan, int32_t rank, const void* const* grad, int32_t grad_kind,
+                        float* master, float* m, float* v, void* const* params,
+                        int32_t params_kind, const zs_adamw_hparams* hp, int64_t step,
+                        void* stream);
+
+/* All-Gather of the updated bf16 parameters (ZeRO section, ZeRO-1 paragraph
+ * and flow figure): every rank's replica receives every rank's shard.
+ *   src_kind  ZS_SHARDED: src[0] is the sharded parameter array;
+ *             ZS_RANK_FULL: in place, src must equal replicas and rank r's
+ *             shard is read from its own replica.
+ *   replicas  ZS_RANK_FULL, N_d pointers. */
+int zs_all_gather(zs_plan_t plan, const void* const* src, int32_t src_kind,
+                  void* const* replicas, void* stream);
+
+/* The three steps above in one pass over HBM: reduce-scatter with averaging,
+ * AdamW on the shard, all-gather into every replica.  Results are bit-identical
+ * to zs_reduce_scatter_mean + zs_adamw_shard_step + zs_all_gather (the reduced
+ * gradient is rounded to bf16 before the update as there).
+ *   bucket      -1 = the whole flat space, else one bucket (the update is
+ *               element-wise, so a bucket can be stepped as soon as its
+ *               gradients are complete).
+ *   grads_kind  ZS_RANK_FULL, or ZS_RANK_BUCKET (bucket >= 0; ZeRO-2 staging).
+ *   replicas    ZS_RANK_FULL; must not overlap grads. */
+int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
+                  float* master, float* m, float* v, void* const* replicas,
+                  const zs_adamw_hparams* hp, int64_t step, void* stream);
+
+/* zs_fused_step over the whole flat space with the gradients in HOST memory
+ * (pinned for overlap): enqueues one host-to-device copy per rank into
+ * dev_grads (ZS_RANK_FULL, caller-owned device staging), the fused step, and a
+ * device-to-host copy of rank 0's updated replica into host_replica0 (may be
+ * NULL to skip).  Same results as zs_fused_step. */
+int zs_fused_step_host(zs_plan_t plan, const void* const* host_grads, void* const* dev_grads,
+                       float* master, float* m, float* v, void* const* replicas,
+                       const zs_adamw_hparams* hp, int64_t step, void* host_replica0,
+                       void* stream);
+
+/* ZeRO-3 gather of one unit (ZeRO section, ZeRO-3 paragraph and flow figure:
+ * before forward, and again before backward, each rank borrows the unit's full
+ * parameters): full[q][j] = shards[0][base_u + j] for every rank q and j in
+ * [0, padded_u).
+ *   shards  ZS_SHARDED bf16 parameter shards (1 pointer).
+ *   full    ZS_RANK_UNIT, N_d pointers of padded_u elements. */
+int zs_zero3_gather_unit(zs_plan_t plan, int32_t unit, const void* shards, void* const* full,
+                         void* stream);
+
+/* ZeRO-3 reduce-scatter with averaging of one unit's gradients fused with the
+ * AdamW update of every rank's shard of that unit (same arithmetic as
+ * zs_reduce_scatter_mean then zs_adamw_shard_step); no gather follows.
+ *   grads   ZS_RANK_UNIT, N_d pointers of padded_u elements (each rank's
+ *           backward gradients for the unit).
+ *   shards  ZS_SHARDED bf16 parameter shards, updated in place. */
+int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads, float* master,
+                          float* m, float* v, void* shards, const zs_adamw_hparams* hp,
+                          int64_t step, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZS_H */

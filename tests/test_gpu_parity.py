@@ -1,0 +1,313 @@
+"""GPU parity: every device entry point of the C ABI against the CPU oracle.
+
+Small cases run the oracle on the whole buffer; the full-size model shapes
+(in the launch configuration the benchmark times) compare sampled chunks of
+the flat space, which is exact because every step is element-wise.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+import gpu_helpers as H
+from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+from oracle import layout, numerics, steps
+
+pytestmark = pytest.mark.gpu
+
+HP = synth.HPARAMS
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+
+def _plans(shapes, n_d, units=None, bucket_bytes=0, stage=1):
+    plan = zs.Plan(shapes, n_d, stage=stage, bucket_bytes=bucket_bytes, unit_of_param=units)
+    ref = layout.make_plan(shapes, n_d, unit_of_param=units, bucket_bytes=bucket_bytes if bucket_bytes > 0 else None)
+    return plan, ref
+
+
+class State:
+    """fp32 master/m/v (ZS_SHARDED) on the device."""
+
+    def __init__(self, master):
+        self.master = master.clone()
+        self.m = torch.zeros_like(master)
+        self.v = torch.zeros_like(master)
+
+    def args(self):
+        return self.master, self.m, self.v
+
+
+def _oracle_state(ref, master_np):
+    n_d = ref.n_d
+    return (H.reshard(ref, master_np), [np.zeros(ref.shard_total, np.float32) for _ in range(n_d)],
+            [np.zeros(ref.shard_total, np.float32) for _ in range(n_d)])
+
+
+def _check_state(ref, st, om, omm, ov, what):
+    H.check_f32(H.to_np_f32(st.master), H.unshard(ref, om), what + " master")
+    H.check_f32(H.to_np_f32(st.m), H.unshard(ref, omm), what + " m")
+    H.check_f32(H.to_np_f32(st.v), H.unshard(ref, ov), what + " v")
+
+
+# ---------------------------------------------------------------- the tiny MLP, every path, 10 steps
+
+@pytest.mark.parametrize("bucket_bytes", [0, 4096, 1000])
+def test_mlp_tiny_zero1_zero2_fused_ten_steps(bucket_bytes):
+    """W1 256x512, b1, W2 512x256, b2 on N_d = 4 ranks, 10 steps: the fused step,
+    ZeRO-1 (in-place reduce-scatter, AdamW, in-place all-gather) and ZeRO-2
+    (bucket-wise reduce-scatter from per-bucket staging into a sharded reduced
+    gradient, AdamW, all-gather) each against the oracle's ZeRO step."""
+    shapes, _ = synth.workload_params("mlp-tiny")
+    n_d = 4
+    plan, ref = _plans(shapes, n_d, bucket_bytes=bucket_bytes)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=0, device=DEV)
+    sts = {k: State(master0) for k in ("fused", "zero1", "zero2")}
+    reps = {k: synth.rank_buffers(n_d, P, BF16, DEV)[0] for k in sts}
+    om, omm, ov = _oracle_state(ref, H.to_np_f32(master0))
+    for t in range(1, 11):
+        grads, _ = synth.rank_grads(n_d, P, pads, seed=0, step=t, sigma=1e-3, device=DEV)
+        g_np = [H.to_np_bf16(g) for g in grads]
+        ref_reps, om, omm, ov = steps.zero_step(ref, g_np, om, omm, ov, HP, t)
+        reduced_ref = steps.reduce_scatter_mean(ref, g_np)
+
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *sts["fused"].args(), reps["fused"], HP, t)
+
+        g1 = [g.clone() for g in grads]
+        zs.zs_reduce_scatter_mean(plan, -1, g1, zs.ZS_RANK_FULL, g1, zs.ZS_RANK_FULL)
+        zs.zs_adamw_shard_step(plan, -1, g1, zs.ZS_RANK_FULL, *sts["zero1"].args(), reps["zero1"],
+                               zs.ZS_RANK_FULL, HP, t)
+        zs.zs_all_gather(plan, reps["zero1"], zs.ZS_RANK_FULL, reps["zero1"])
+
+        ghat = torch.zeros(P, dtype=BF16, device=DEV)
+        for b in reversed(range(plan.n_buckets)):          # backward makes buckets ready last-to-first
+            _, lo, hi = plan.bucket(b)
+            staging = [g[lo:hi].clone() for g in grads]
+            zs.zs_reduce_scatter_mean(plan, b, staging, zs.ZS_RANK_BUCKET, [ghat], zs.ZS_SHARDED)
+            del staging                                     # the bucket's non-owned gradients are freed
+        shards = torch.zeros(P, dtype=BF16, device=DEV)
+        zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, *sts["zero2"].args(), [shards],
+                               zs.ZS_SHARDED, HP, t)
+        zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps["zero2"])
+        torch.cuda.synchronize()
+
+        for k in sts:
+            _check_state(ref, sts[k], om, omm, ov, "%s t=%d" % (k, t))
+            for q in range(n_d):
+                H.check_bf16(H.to_np_bf16(reps[k][q]), ref_reps[q], "%s replica %d t=%d" % (k, q, t))
+        # ZeRO-1 keeps the full gradient buffer: owned slice reduced, the rest untouched local gradients
+        for r in range(n_d):
+            lo, hi = layout.shard_range(ref, 0, r)
+            g1r = H.to_np_bf16(g1[r])
+            H.check_bf16(g1r[lo:hi], reduced_ref[r], "zero1 reduced slice r=%d" % r)
+            assert np.array_equal(g1r[:lo], g_np[r][:lo]) and np.array_equal(g1r[hi:], g_np[r][hi:])
+        H.check_bf16(H.to_np_bf16(ghat), H.unshard(ref, reduced_ref), "zero2 reduced gradient t=%d" % t)
+
+
+# ---------------------------------------------------------------- gradient accumulation
+
+@pytest.mark.parametrize("n_d", [1, 3, 8])
+def test_accumulation_four_microbatches(n_d):
+    shapes = [(1000, 3), (77,), (5, 5, 5)]
+    plan, ref = _plans(shapes, n_d)
+    P, pads = plan.padded, plan.pad_ranges()
+    acc, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    ref_acc = [None] * n_d
+    for j in range(4):
+        micro, _ = synth.rank_grads(n_d, P, pads, seed=11, step=j, sigma=1e-3, device=DEV)
+        zs.zs_accumulate_grad(plan, acc, micro, 0.25, first=(j == 0))
+        for q in range(n_d):
+            ref_acc[q] = steps.accumulate(ref_acc[q], H.to_np_bf16(micro[q]), 0.25, first=(j == 0))
+    torch.cuda.synchronize()
+    for q in range(n_d):
+        H.check_bf16(H.to_np_bf16(acc[q]), ref_acc[q], "acc rank %d" % q)
+
+
+def test_accumulation_in_place_and_equal_microbatches():
+    """acc may be the micro buffer itself; four equal micro-batches give back the gradient."""
+    plan, _ = _plans([(4099,)], 2)
+    P, pads = plan.padded, plan.pad_ranges()
+    g, _ = synth.rank_grads(2, P, pads, seed=5, step=0, sigma=1e-3, device=DEV)
+    acc, _ = synth.rank_buffers(2, P, BF16, DEV)
+    for j in range(4):
+        zs.zs_accumulate_grad(plan, acc, g, 0.25, first=(j == 0))
+    same = [x.clone() for x in g]
+    zs.zs_accumulate_grad(plan, same, same, 1.0, first=True)
+    torch.cuda.synchronize()
+    for q in range(2):
+        assert torch.equal(acc[q], g[q])
+        assert torch.equal(same[q], g[q])
+
+
+# ---------------------------------------------------------------- ZeRO-3 per unit
+
+def _tiny_llama(n_layers=3, d=64, ffn=176, vocab=100):
+    shapes, units = [(vocab, d)], [n_layers]
+    for layer in range(n_layers):
+        ls = [(d,), (d, d), (d, d), (d, d), (d, d), (d,), (ffn, d), (ffn, d), (d, ffn)]
+        shapes += ls
+        units += [layer] * len(ls)
+    shapes += [(d,), (vocab, d)]
+    units += [n_layers, n_layers]
+    return shapes, units
+
+
+@pytest.mark.parametrize("n_d", [16, 5, 2])
+def test_zero3_units_two_steps(n_d):
+    """Per unit: gather for forward, gather again for backward (both equal the
+    shards before the update), reduce-scatter + AdamW on the shard; no gather after."""
+    shapes, units = _tiny_llama()
+    plan, ref = _plans(shapes, n_d, units=units, stage=3)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=3, device=DEV)
+    st = State(master0)
+    shards = torch.empty(P, dtype=BF16, device=DEV)
+    shards.copy_(master0.to(BF16))       # the initial bf16 shards: the cast of the fp32 masters
+    om, omm, ov = _oracle_state(ref, H.to_np_f32(master0))
+    osh = H.reshard(ref, H.to_np_bf16(shards))
+    for t in (1, 2):
+        for u in range(plan.n_units):                                   # forward: layer order
+            ud = plan.unit(u)
+            full, _ = synth.rank_buffers(n_d, ud["padded"], BF16, DEV)
+            zs.zs_zero3_gather_unit(plan, u, shards, full)
+            want = steps.all_gather_unit(ref, u, osh)
+            torch.cuda.synchronize()
+            for q in range(n_d):
+                H.check_bf16(H.to_np_bf16(full[q]), want[q], "fwd gather u=%d q=%d" % (u, q))
+        for u in reversed(range(plan.n_units)):                         # backward: reverse order
+            ud = plan.unit(u)
+            full, _ = synth.rank_buffers(n_d, ud["padded"], BF16, DEV)
+            zs.zs_zero3_gather_unit(plan, u, shards, full)
+            upads = [(ud["numel"], ud["padded"])] if ud["padded"] > ud["numel"] else []
+            grads, _ = synth.rank_grads(n_d, ud["padded"], upads, seed=30 + u, step=t, sigma=5e-4, device=DEV)
+            zs.zs_zero3_rs_step_unit(plan, u, grads, *st.args(), shards, HP, t)
+            fwd, bwd, osh, om, omm, ov = steps.zero3_unit_step(ref, u, osh, [H.to_np_bf16(g) for g in grads],
+                                                               om, omm, ov, HP, t)
+            torch.cuda.synchronize()
+            for q in range(n_d):
+                H.check_bf16(H.to_np_bf16(full[q]), bwd[q], "bwd gather u=%d q=%d" % (u, q))
+        _check_state(ref, st, om, omm, ov, "zero3 t=%d" % t)
+        H.check_bf16(H.to_np_bf16(shards), H.unshard(ref, osh), "zero3 shards t=%d" % t)
+
+
+# ---------------------------------------------------------------- edge cases
+
+EDGE = [
+    # (shapes, n_d, bucket_bytes)
+    ([(1,)], 1, 0),                         # one element, one rank
+    ([(7,)], 3, 0),                         # padding to 9, non-power-of-two ranks
+    ([(3,), (4,)], 8, 2),                   # more ranks than elements, one-element buckets
+    ([(65_541,)], 8, 1000),                 # ragged tail, buckets off the 8-element grid
+    ([(3 * 65_536 + 13,)], 5, 0),           # odd shard size (owner boundaries off the grid)
+    ([(100_003,), (17, 3)], 16, 4096),
+    ([(40_000,)], 32, 0),
+    ([(9_999,)], 64, 0),                    # the largest rank count
+    ([(123_457,)], 6, 2048),
+]
+
+
+@pytest.mark.parametrize("shapes,n_d,bucket_bytes", EDGE)
+def test_edge_cases_all_paths(shapes, n_d, bucket_bytes):
+    plan, ref = _plans(shapes, n_d, bucket_bytes=bucket_bytes)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=7, device=DEV)
+    om, omm, ov = _oracle_state(ref, H.to_np_f32(master0))
+    st_f, st_u, st_b = State(master0), State(master0), State(master0)
+    reps_f = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    reps_u = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    reps_b = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    for t in (1, 2, 3):
+        grads, _ = synth.rank_grads(n_d, P, pads, seed=7, step=t, sigma=1e-3, outlier_p=0.01, device=DEV)
+        g_np = [H.to_np_bf16(g) for g in grads]
+        ref_reps, om, omm, ov = steps.zero_step(ref, g_np, om, omm, ov, HP, t)
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *st_f.args(), reps_f, HP, t)
+        # fused, bucket by bucket from staging buffers (ZeRO-2 with the update as each bucket completes)
+        for b in reversed(range(plan.n_buckets)):
+            _, lo, hi = plan.bucket(b)
+            staging = [g[lo:hi].clone() for g in grads]
+            zs.zs_fused_step(plan, b, staging, zs.ZS_RANK_BUCKET, *st_b.args(), reps_b, HP, t)
+        # unfused ZeRO-1, one rank at a time for the update
+        g1 = [g.clone() for g in grads]
+        zs.zs_reduce_scatter_mean(plan, -1, g1, zs.ZS_RANK_FULL, g1, zs.ZS_RANK_FULL)
+        for r in range(n_d):
+            zs.zs_adamw_shard_step(plan, r, g1, zs.ZS_RANK_FULL, *st_u.args(), reps_u, zs.ZS_RANK_FULL, HP, t)
+        zs.zs_all_gather(plan, reps_u, zs.ZS_RANK_FULL, reps_u)
+        torch.cuda.synchronize()
+        for name, st, reps in (("fused", st_f, reps_f), ("bucketed", st_b, reps_b), ("unfused", st_u, reps_u)):
+            _check_state(ref, st, om, omm, ov, "%s t=%d" % (name, t))
+            for q in range(n_d):
+                H.check_bf16(H.to_np_bf16(reps[q]), ref_reps[q], "%s replica %d t=%d" % (name, q, t))
+        for lo, hi in pads:                                  # padding stays exactly zero
+            assert not st_f.master[lo:hi].any() and not reps_f[0][lo:hi].float().any()
+
+
+# ---------------------------------------------------------------- guard zones and rejected calls
+
+def _guarded(n_elems, dtype, guard=2048, fill=0x5A):
+    raw = torch.full(((n_elems + 2 * guard) * torch.tensor([], dtype=dtype).element_size(),), fill,
+                     dtype=torch.uint8, device=DEV)
+    t = raw.view(dtype)
+    return t[guard:guard + n_elems], raw, guard * t.element_size()
+
+
+def test_guard_zones_untouched():
+    """Sentinel bytes before and after every buffer must survive every call (no
+    out-of-bounds writes; compute-sanitizer is not available on this machine)."""
+    shapes, n_d, bb = [(5_003,), (11,)], 3, 998
+    plan, _ = _plans(shapes, n_d, bucket_bytes=bb)
+    P = plan.padded
+    bufs = []
+
+    def mk(dtype):
+        t, raw, g = _guarded(P, dtype)
+        t.zero_()
+        bufs.append((raw, g))
+        return t
+
+    grads = [mk(BF16) for _ in range(n_d)]
+    for g in grads:
+        g.normal_(0, 1e-3)
+    reps = [mk(BF16) for _ in range(n_d)]
+    master, m, v = mk(torch.float32), mk(torch.float32), mk(torch.float32)
+    ghat, shards = mk(BF16), mk(BF16)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED)
+    zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, master, m, v, [shards], zs.ZS_SHARDED, HP, 2)
+    zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps)
+    zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, grads, zs.ZS_RANK_FULL)
+    zs.zs_adamw_shard_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, zs.ZS_RANK_FULL, HP, 3)
+    zs.zs_all_gather(plan, reps, zs.ZS_RANK_FULL, reps)
+    zs.zs_accumulate_grad(plan, grads, reps, 0.5, first=False)
+    for b in range(plan.n_buckets):
+        zs.zs_fused_step(plan, b, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 4)
+    torch.cuda.synchronize()
+    for raw, g in bufs:
+        assert bool((raw[:g] == 0x5A).all()) and bool((raw[-g:] == 0x5A).all())
+
+
+def test_rejected_calls_write_nothing():
+    plan, _ = _plans([(4096,)], 4)
+    P = plan.padded
+    grads, _ = synth.rank_grads(4, P, [], seed=1, step=1, sigma=1e-3, device=DEV)
+    reps, _ = synth.rank_buffers(4, P, BF16, DEV)
+    master = synth.master_init(P, [], 1, device=DEV)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    before = master.clone()
+    misaligned = torch.zeros(P + 8, dtype=BF16, device=DEV)[1:P + 1]
+    with pytest.raises(zs.ZsError) as e:
+        zs.zs_fused_step(plan, -1, grads[:3] + [misaligned], zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    assert e.value.status == zs.ZS_ERR_INVALID and "aligned" in str(e.value)
+    with pytest.raises(zs.ZsError):
+        zs.zs_fused_step(plan, -1, grads[:3] + [0], zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    with pytest.raises(zs.ZsError):
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 0)
+    with pytest.raises(zs.ZsError):
+        zs.zs_adamw_shard_step(plan, 4, grads, zs.ZS_RANK_FULL, master, m, v, reps, zs.ZS_RANK_FULL, HP, 1)
+    with pytest.raises(zs.ZsError):
+        zs.zs_all_gather(plan, grads, zs.ZS_RANK_FULL, reps)          # in place needs src == replicas
+    with pytest.raises(ValueError):
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master[:100], m, v, reps, HP, 1)  # too small
+    torch.cuda.synchronize()
+    assert torch.equal(master, before) and not m.any() and not any(r.float().any() for r in reps)
