@@ -28,6 +28,8 @@ ZS_ERR_UNSUPPORTED = -5
 ZS_STAGE_DP, ZS_STAGE_ZERO1, ZS_STAGE_ZERO2, ZS_STAGE_ZERO3 = 0, 1, 2, 3
 ZS_RANK_FULL, ZS_SHARDED, ZS_RANK_BUCKET, ZS_RANK_UNIT = 0, 1, 2, 3
 ZS_MAX_RANKS = 64
+ZS_FUSED_AUTO, ZS_FUSED_LDG, ZS_FUSED_TMA = 0, 1, 2
+ZS_DEVERR_NONE, ZS_DEVERR_PRODUCER_WAIT, ZS_DEVERR_CONSUMER_WAIT, ZS_DEVERR_SELFTEST = 0, 1, 2, 3
 
 c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 P_i64 = ctypes.POINTER(c_i64)
@@ -75,13 +77,17 @@ _sig("zs_fused_step_host", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
 _sig("zs_zero3_gather_unit", [c_vp, c_i32, c_vp, c_vp, c_vp])
 _sig("zs_zero3_rs_step_unit", [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
+_sig("zs_set_fused_variant", [c_i32])
+_sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
+_sig("zs_selftest_wait_timeout", [c_i64, c_vp])
 
 EXPORTED = [
     "zs_plan_create", "zs_plan_destroy", "zs_plan_info", "zs_plan_unit", "zs_plan_bucket",
     "zs_plan_bucket_rank_slice", "zs_plan_param", "zs_plan_param_segment", "zs_plan_memory_bytes",
     "zs_plan_comm_bytes", "zs_adamw_scalars", "zs_last_error", "zs_accumulate_grad",
     "zs_reduce_scatter_mean", "zs_adamw_shard_step", "zs_all_gather", "zs_fused_step",
-    "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit",
+    "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit", "zs_set_fused_variant",
+    "zs_device_status", "zs_selftest_wait_timeout",
 ]
 
 
@@ -330,6 +336,20 @@ def zs_zero3_rs_step_unit(plan, unit, grads, master, m, v, shards, hp, step, str
         plan.handle, int(unit), _ptr_array(grads, nu, 2, "grads"),
         _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
         _addr(shards, n, 2, "shards"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+def zs_set_fused_variant(variant):
+    return _check(_lib.zs_set_fused_variant(int(variant)))
+
+
+def zs_device_status(clear=False):
+    code = ctypes.c_uint32()
+    _check(_lib.zs_device_status(ctypes.byref(code), 1 if clear else 0))
+    return code.value
+
+
+def zs_selftest_wait_timeout(limit_cycles, stream=None):
+    return _check(_lib.zs_selftest_wait_timeout(int(limit_cycles), _stream(stream)))
 
 
 __all__ = ["Plan", "ZsError", "zs_adamw_hparams", "LIB_PATH"] + EXPORTED + [

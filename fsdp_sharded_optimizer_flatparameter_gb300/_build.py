@@ -3,7 +3,7 @@
 Each translation unit under ``csrc/`` is compiled in parallel with nvcc into
 ``_build/``, then linked into the package directory against the shared CUDA
 runtime (the same ``libcudart.so`` PyTorch loads).  No cmake, one
-``-gencode``.  Run ``python -m fsdp_sharded_optimizer_flatparameter_gb300._build``.
+``-gencode``.  Run ``python fsdp_sharded_optimizer_flatparameter_gb300/_build.py``.
 """
 
 import concurrent.futures as cf

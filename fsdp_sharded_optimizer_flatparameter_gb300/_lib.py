@@ -10,7 +10,7 @@ def load_library():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             "libzs.so is not built (%s). Build it with "
-            "`python -m fsdp_sharded_optimizer_flatparameter_gb300._build` "
+            "`python fsdp_sharded_optimizer_flatparameter_gb300/_build.py` "
             "or `python -c 'import __graft_entry__ as g; g.build()'`; there is no fallback." % LIB_PATH)
     # torch first, so the CUDA runtime it ships is the one the library binds to
     try:

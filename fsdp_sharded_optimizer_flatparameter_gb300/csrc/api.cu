@@ -311,3 +311,28 @@ extern "C" int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* c
     return cuda_status(fn, zs::launch_fused(g, master, m, v, o, false, unit_range(u), s, plan->n_d,
                                             as_stream(stream)));
 }
+
+extern "C" int zs_set_fused_variant(int32_t variant) {
+    zs::clear_error();
+    if (variant != ZS_FUSED_AUTO && variant != ZS_FUSED_LDG && variant != ZS_FUSED_TMA)
+        return fail("zs_set_fused_variant", "unknown variant");
+    zs::set_fused_variant(variant);
+    return ZS_OK;
+}
+
+extern "C" int zs_device_status(uint32_t* code, int32_t clear) {
+    static const char* fn = "zs_device_status";
+    zs::clear_error();
+    if (!code) return fail(fn, "code is NULL");
+    unsigned int v = 0;
+    ZS_TRY(cuda_status(fn, zs::read_device_error(&v, clear != 0)));
+    *code = v;
+    return ZS_OK;
+}
+
+extern "C" int zs_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+    static const char* fn = "zs_selftest_wait_timeout";
+    zs::clear_error();
+    if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 32)) return fail(fn, "limit_cycles out of range");
+    return cuda_status(fn, zs::launch_wait_selftest((long long)limit_cycles, as_stream(stream)));
+}

@@ -341,10 +341,15 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
 #undef ZS_GA
 }
 
-cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
-    const bool vec = aligned8(g.off) && aligned8(out.off);
-    const Split sp = split_range(r.lo, r.hi, vec);
+static int g_fused_variant = ZS_FUSED_AUTO;
+void set_fused_variant(int v) { g_fused_variant = v; }
+int fused_variant() { return g_fused_variant; }
+
+// Smallest body worth a persistent staged launch (below it the register-streaming kernel is as fast).
+constexpr int64_t kTmaMinElems = int64_t(1) << 20;
+
+static cudaError_t launch_fused_ldg(const BView& g, float* master, float* m, float* v, const BView& out,
+                                    bool broadcast, const Split& sp, const AdamScalars& s, int nd, cudaStream_t st) {
     if (broadcast) {
 #define ZS_FB(N) fused_impl<N, true>(g, master, m, v, out, s, nd, sp, st)
         ZS_DISPATCH_ND(nd, ZS_FB)
@@ -354,6 +359,26 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
         ZS_DISPATCH_ND(nd, ZS_FS)
 #undef ZS_FS
     }
+}
+
+cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
+    const bool vec = aligned8(g.off) && aligned8(out.off);
+    const Split sp = split_range(r.lo, r.hi, vec);
+    const bool staged_nd = nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32;
+    const bool want_tma = g_fused_variant == ZS_FUSED_TMA ||
+                          (g_fused_variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
+    if (!(want_tma && staged_nd && sp.nvec > 0)) return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);
+    // staged body, then the at most 14 fringe elements one by one
+    const int64_t body_hi = sp.vlo + (sp.nvec << 3);
+    cudaError_t e = launch_fused_tma(g, master, m, v, out, broadcast, sp.vlo, sp.nvec << 3, s, nd, st);
+    if (e != cudaSuccess) return e;
+    if (sp.vlo > sp.lo) {
+        e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(sp.lo, sp.vlo, false), s, nd, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (sp.hi > body_hi) e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(body_hi, sp.hi, false), s, nd, st);
+    return e;
 }
 
 }  // namespace zs

@@ -1,0 +1,341 @@
+// Fused step with bulk-copy (TMA engine) staging of the inputs, sm_103a.
+//
+// Same arithmetic as the register-streaming fused kernel (reduce-mean over
+// ranks, AdamW, bf16 cast, store into every replica: "Infra: Data Parallel",
+// ZeRO section), different data movement.  The flat range is cut into tiles
+// of T elements.  Each CTA is persistent (one per SM) and owns a ring of
+// STAGES shared-memory stages; a stage holds one tile of every rank's bf16
+// gradients and of the fp32 master, m and v.  One producer thread issues the
+// N_d + 3 one-dimensional bulk copies of a tile (cp.async.bulk, completion
+// counted in bytes on the stage's "full" mbarrier, L2 evict-first); NCW
+// consumer warps wait for the stage, each thread computes VPT consecutive
+// elements from shared memory, streams its results straight to global memory
+// and the warp releases the stage on its "empty" mbarrier.  With up to
+// STAGES-1 tiles in flight per SM the loads keep ~200 KB of reads outstanding
+// per SM independent of register pressure.
+//
+// Every wait is bounded (clock64 budget).  A wait that runs out sets
+// g_zs_device_error, the CTA stops taking tiles, the producer waits (again
+// bounded) for the copies it still has in flight, and the kernel returns.
+#include "device.cuh"
+
+namespace zs {
+
+__device__ unsigned int g_zs_device_error;   // 0 = fine; otherwise a ZS_DEVERR_* code
+
+namespace {
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false once `limit` cycles have passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long long limit) {
+    if (mbar_try_wait(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(b, parity)) {
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// One-dimensional bulk copy global -> shared; bytes and both addresses multiples of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void flag_error(unsigned int code) { atomicCAS(&g_zs_device_error, 0u, code); }
+
+// VPT consecutive bf16 values from shared memory as fp32.
+template <int VPT>
+__device__ __forceinline__ void lds_bf(const uint16_t* p, float (&f)[VPT]) {
+    if constexpr (VPT == 8) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+        f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
+    } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    }
+}
+
+template <int VPT>
+__device__ __forceinline__ void lds_f32(const float* p, float (&f)[VPT]) {
+#pragma unroll
+    for (int k = 0; k < VPT; k += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(p + k);
+        f[k] = a.x; f[k + 1] = a.y; f[k + 2] = a.z; f[k + 3] = a.w;
+    }
+}
+
+template <int VPT>
+__device__ __forceinline__ void stg_f32(float* p, const float (&f)[VPT]) {
+#pragma unroll
+    for (int k = 0; k < VPT; k += 4) __stcs(reinterpret_cast<float4*>(p + k), make_float4(f[k], f[k + 1], f[k + 2], f[k + 3]));
+}
+
+}  // namespace
+
+struct TmaArgs {
+    Ptrs g;               // rank gradients; element i of rank q at g.p[q] + (i - g_off)
+    int64_t g_off;
+    Ptrs out;             // outputs; BROADCAST: every rank's replica, else out.p[0] only
+    int64_t out_off;
+    float *master, *m, *v;
+    AdamScalars s;
+    int64_t lo, n;        // body [lo, lo + n): lo, n and lo - g_off, lo - out_off multiples of 8
+    int nd;
+    float inv_nd;
+    long long wait_limit; // cycles a wait may take before the kernel gives up
+    long long drain_limit;// cycles to wait for copies still in flight after giving up
+};
+
+template <int ND, int NCW, int VPT>
+struct TmaShape {
+    static constexpr int kT = NCW * 32 * VPT;                           // elements per tile
+    static constexpr int kStageBytes = kT * (2 * ND + 12);
+    static constexpr int kBudget = 227 * 1024 - 256;
+    static constexpr int kStages = (kBudget / kStageBytes) > 8 ? 8 : (kBudget / kStageBytes);
+    static constexpr int kSmem = 256 + kStages * kStageBytes;
+    static_assert(kStages >= 2, "tile too large for a 2-stage ring");
+};
+
+template <int ND, int NCW, int VPT, bool BROADCAST>
+__global__ void __launch_bounds__(32 * (NCW + 1), 1) k_fused_tma(const __grid_constant__ TmaArgs a) {
+    using Sh = TmaShape<ND, NCW, VPT>;
+    constexpr int T = Sh::kT;
+    constexpr int S = Sh::kStages;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + S;
+    uint8_t* stages = smem + 256;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCW * 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int64_t ntiles = (a.n + T - 1) / T;
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            const uint64_t pol = evict_first_policy();
+            int64_t j = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+                const int s = (int)(j % S);
+                if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), a.wait_limit)) {
+                    flag_error(ZS_DEVERR_PRODUCER_WAIT);
+                    ok = false;
+                    break;
+                }
+                const int64_t i0 = a.lo + tile * T;
+                const int64_t rem = a.n - tile * T;
+                const uint32_t len = (uint32_t)(rem < T ? rem : T);
+                uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
+                mbar_expect_tx(&full[s], len * (2u * ND + 12u));
+#pragma unroll
+                for (int q = 0; q < ND; ++q)
+                    bulk_load(st + (size_t)q * T * 2, a.g.p[q] + (i0 - a.g_off), len * 2u, &full[s], pol);
+                float* sf = reinterpret_cast<float*>(st + (size_t)ND * T * 2);
+                bulk_load(sf, a.master + i0, len * 4u, &full[s], pol);
+                bulk_load(sf + T, a.m + i0, len * 4u, &full[s], pol);
+                bulk_load(sf + 2 * T, a.v + i0, len * 4u, &full[s], pol);
+            }
+            if (!ok) {
+                // drain: wait (bounded) for the copies issued into stages not yet consumed
+                const int64_t issued = j;
+                for (int64_t k = issued > S ? issued - S : 0; k < issued; ++k)
+                    mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int ct = threadIdx.x - 32;                  // 0 .. NCW*32-1
+    const int e = ct * VPT;                           // this thread's first element in a tile
+    const int n = ND;
+    int64_t j = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        const int s = (int)(j % S);
+        if (!mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
+            flag_error(ZS_DEVERR_CONSUMER_WAIT);
+            return;
+        }
+        const int64_t i0 = a.lo + tile * T;
+        const int64_t rem = a.n - tile * T;
+        const int len = (int)(rem < T ? rem : T);
+        if (e < len) {
+            const uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
+            const uint16_t* sg = reinterpret_cast<const uint16_t*>(st);
+            const float* sf = reinterpret_cast<const float*>(st + (size_t)ND * T * 2);
+            float acc[VPT];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) acc[k] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < n; ++q) {
+                float f[VPT];
+                lds_bf<VPT>(sg + (size_t)q * T + e, f);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+            }
+            float p[VPT], mm[VPT], vv[VPT];
+            lds_f32<VPT>(sf + e, p);
+            lds_f32<VPT>(sf + T + e, mm);
+            lds_f32<VPT>(sf + 2 * T + e, vv);
+            uint32_t gw[VPT / 2];
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2)
+                gw[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], n, a.inv_nd), mean_of_sum<ND>(acc[k + 1], n, a.inv_nd));
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2) {
+                adamw_elem(bf16_lo(gw[k / 2]), p[k], mm[k], vv[k], a.s);
+                adamw_elem(bf16_hi(gw[k / 2]), p[k + 1], mm[k + 1], vv[k + 1], a.s);
+            }
+            mbar_arrive(&empty[s]);                      // this thread is done with the stage
+            const int64_t i = i0 + e;
+            stg_f32<VPT>(a.master + i, p);
+            stg_f32<VPT>(a.m + i, mm);
+            stg_f32<VPT>(a.v + i, vv);
+            uint32_t pw[VPT / 2];
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2) pw[k / 2] = pack_bf16x2(p[k], p[k + 1]);
+            if constexpr (VPT == 8) {
+                const uint4 w = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                if constexpr (BROADCAST) {
+#pragma unroll
+                    for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint4*>(a.out.p[q] + (i - a.out_off)), w);
+                } else {
+                    __stcs(reinterpret_cast<uint4*>(a.out.p[0] + (i - a.out_off)), w);
+                }
+            } else {
+                const uint2 w = make_uint2(pw[0], pw[1]);
+                if constexpr (BROADCAST) {
+#pragma unroll
+                    for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint2*>(a.out.p[q] + (i - a.out_off)), w);
+                } else {
+                    __stcs(reinterpret_cast<uint2*>(a.out.p[0] + (i - a.out_off)), w);
+                }
+            }
+        } else {
+            mbar_arrive(&empty[s]);
+        }
+    }
+}
+
+namespace {
+
+template <int ND, int NCW, int VPT, bool BROADCAST>
+cudaError_t tma_impl(const TmaArgs& a, cudaStream_t st) {
+    using Sh = TmaShape<ND, NCW, VPT>;
+    auto kern = k_fused_tma<ND, NCW, VPT, BROADCAST>;
+    // set on every launch: the attribute belongs to the current device
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    kern<<<grid, 32 * (NCW + 1), Sh::kSmem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Returns cudaErrorNotSupported when no staged variant exists for this rank count.
+cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
+                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+    TmaArgs a;
+    a.g = g.ptr;
+    a.g_off = g.off;
+    a.out = out.ptr;
+    a.out_off = out.off;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.s = s;
+    a.lo = lo;
+    a.n = n;
+    a.nd = nd;
+    a.inv_nd = 1.0f / (float)nd;
+    a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
+    a.drain_limit = 4000000000LL;
+#define ZS_TMA(ND_, NCW_, VPT_)                                                          \
+    return broadcast ? tma_impl<ND_, NCW_, VPT_, true>(a, st) : tma_impl<ND_, NCW_, VPT_, false>(a, st)
+    switch (nd) {
+        case 2: ZS_TMA(2, 8, 8);
+        case 4: ZS_TMA(4, 8, 8);
+        case 8: ZS_TMA(8, 8, 8);
+        case 16: ZS_TMA(16, 8, 4);
+        case 32: ZS_TMA(32, 8, 4);
+        default: return cudaErrorNotSupported;
+    }
+#undef ZS_TMA
+}
+
+// Self-test of the bounded wait: waits on an mbarrier nothing arrives at, with
+// a budget of `limit` cycles, then records ZS_DEVERR_SELFTEST and returns.
+__global__ void k_wait_selftest(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit)) flag_error(ZS_DEVERR_SELFTEST);
+}
+
+cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
+    k_wait_selftest<<<1, 32, 0, st>>>(limit_cycles);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_error(unsigned int* out, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_zs_device_error, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_zs_device_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace zs

@@ -44,4 +44,15 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                          const Range& r, const AdamScalars& s, int nd, cudaStream_t st);
 
+// Bulk-copy staged fused kernel over the 8-aligned body [lo, lo + n); returns
+// cudaErrorNotSupported when no staged variant exists for this rank count.
+cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
+                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
+cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
+cudaError_t read_device_error(unsigned int* out, bool clear);
+
+// Which fused kernel zs_fused_step / zs_zero3_rs_step_unit use (ZS_FUSED_*).
+void set_fused_variant(int v);
+int fused_variant();
+
 }  // namespace zs

@@ -81,6 +81,15 @@ extern "C" {
 
 #define ZS_MAX_RANKS    64        /* largest N_d accepted                            */
 
+#define ZS_FUSED_AUTO   0         /* staged kernel for large 8-aligned ranges, else streaming */
+#define ZS_FUSED_LDG    1         /* register-streaming kernel (16-byte loads/stores)   */
+#define ZS_FUSED_TMA    2         /* bulk-copy staged kernel wherever it applies       */
+
+#define ZS_DEVERR_NONE          0u
+#define ZS_DEVERR_PRODUCER_WAIT 1u   /* a staged kernel's producer gave up waiting for a free stage */
+#define ZS_DEVERR_CONSUMER_WAIT 2u   /* a staged kernel's consumer gave up waiting for its data     */
+#define ZS_DEVERR_SELFTEST      3u   /* zs_selftest_wait_timeout ran its wait out (expected)         */
+
 typedef struct zs_plan_s* zs_plan_t;
 
 /* AdamW hyper-parameters, as fp32 values. */
@@ -155,6 +164,27 @@ int zs_adamw_scalars(const zs_adamw_hparams* hp, int64_t step, float* out8);
 
 /* Message for the last non-OK return on this thread ("" if none). */
 const char* zs_last_error(void);
+
+/* Selects the kernel behind zs_fused_step and zs_zero3_rs_step_unit for the
+ * whole process (ZS_FUSED_AUTO, ZS_FUSED_LDG or ZS_FUSED_TMA).  Every variant
+ * computes bit-identical results; they differ in how data reaches the SMs.  The
+ * staged kernel exists for N_d in {2, 4, 8, 16, 32} and needs the range's buffers
+ * on the 8-element grid; elsewhere the streaming kernel runs.  Set it before
+ * enqueueing work from other threads.  Errors: ZS_ERR_INVALID for an unknown value. */
+int zs_set_fused_variant(int32_t variant);
+
+/* Device-side status of the current device (ZS_DEVERR_*): a staged kernel whose
+ * bounded wait ran out records a code here, stops, waits (bounded) for its
+ * copies in flight and returns, leaving the context usable.  This call copies
+ * the word to the host, so it waits for the device's prior work; clear != 0
+ * resets it to ZS_DEVERR_NONE.  Errors: ZS_ERR_CUDA. */
+int zs_device_status(uint32_t* code, int32_t clear);
+
+/* Self-test of the bounded wait used by the staged kernels: one block waits on
+ * a barrier nothing will complete, gives up after limit_cycles SM cycles
+ * (1 .. 2^32) and records ZS_DEVERR_SELFTEST.  Nothing else is touched.
+ * Errors: ZS_ERR_INVALID for a limit out of range; ZS_ERR_CUDA. */
+int zs_selftest_wait_timeout(int64_t limit_cycles, void* stream);
 
 /* ------------------------------------------------------------------ device operations */
 

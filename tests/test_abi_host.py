@@ -171,3 +171,10 @@ def test_device_calls_reject_bad_arguments_before_launch():
                              ctypes.c_void_p(0)) == zs.ZS_ERR_INVALID
     assert lib.zs_fused_step(None, -1, arr(good), 0, None, None, None, arr(reps), ctypes.byref(hp),
                              ctypes.c_int64(1), None) == zs.ZS_ERR_INVALID
+
+
+def test_fused_variant_switch_validates():
+    assert zs.zs_set_fused_variant(zs.ZS_FUSED_LDG) == zs.ZS_OK
+    assert zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO) == zs.ZS_OK
+    with pytest.raises(zs.ZsError):
+        zs.zs_set_fused_variant(3)

@@ -311,3 +311,80 @@ def test_rejected_calls_write_nothing():
         zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master[:100], m, v, reps, HP, 1)  # too small
     torch.cuda.synchronize()
     assert torch.equal(master, before) and not m.any() and not any(r.float().any() for r in reps)
+
+
+# ---------------------------------------------------------------- staged (bulk-copy) kernel
+
+@pytest.fixture
+def variant():
+    yield zs.zs_set_fused_variant
+    zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+
+
+@pytest.mark.parametrize("n_d,numel,bucket_bytes", [
+    (2, 3 * 2048 * 8 + 5, 0), (4, 1_000_003, 0), (8, 262_912, 0), (8, 2_000_001, 1 << 20),
+    (16, 700_001, 0), (32, 300_007, 0), (3, 50_001, 0)])
+def test_staged_and_streaming_fused_kernels_agree_with_oracle(variant, n_d, numel, bucket_bytes):
+    """The bulk-copy staged kernel and the register-streaming kernel give the oracle's
+    results bit for bit, for whole-space and per-bucket launches with ragged tails."""
+    plan, ref = _plans([(numel,)], n_d, bucket_bytes=bucket_bytes)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=8, device=DEV)
+    om, omm, ov = _oracle_state(ref, H.to_np_f32(master0))
+    states = {v: State(master0) for v in (zs.ZS_FUSED_LDG, zs.ZS_FUSED_TMA)}
+    reps = {v: synth.rank_buffers(n_d, P, BF16, DEV)[0] for v in states}
+    for t in (1, 2):
+        grads, _ = synth.rank_grads(n_d, P, pads, seed=8, step=t, sigma=1e-3, outlier_p=0.001, device=DEV)
+        ref_reps, om, omm, ov = steps.zero_step(ref, [H.to_np_bf16(g) for g in grads], om, omm, ov, HP, t)
+        for v in states:
+            variant(v)
+            if bucket_bytes:
+                for b in reversed(range(plan.n_buckets)):
+                    zs.zs_fused_step(plan, b, grads, zs.ZS_RANK_FULL, *states[v].args(), reps[v], HP, t)
+            else:
+                zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *states[v].args(), reps[v], HP, t)
+        torch.cuda.synchronize()
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+        for v in states:
+            _check_state(ref, states[v], om, omm, ov, "variant %d t=%d" % (v, t))
+            for q in range(n_d):
+                H.check_bf16(H.to_np_bf16(reps[v][q]), ref_reps[q], "variant %d replica %d" % (v, q))
+
+
+def test_staged_zero3_rs_step_matches_streaming(variant):
+    shapes, units = _tiny_llama(n_layers=2, d=256, ffn=704, vocab=1000)
+    n_d = 16
+    plan, _ = _plans(shapes, n_d, units=units, stage=3)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=9, device=DEV)
+    out = {}
+    for v in (zs.ZS_FUSED_LDG, zs.ZS_FUSED_TMA):
+        variant(v)
+        st = State(master0)
+        shards = master0.to(BF16)
+        for u in reversed(range(plan.n_units)):
+            ud = plan.unit(u)
+            grads, _ = synth.rank_grads(n_d, ud["padded"], [], seed=90 + u, step=1, sigma=5e-4, device=DEV)
+            zs.zs_zero3_rs_step_unit(plan, u, grads, *st.args(), shards, HP, 1)
+        torch.cuda.synchronize()
+        out[v] = (st, shards)
+    a, b = out[zs.ZS_FUSED_LDG], out[zs.ZS_FUSED_TMA]
+    for x, y in zip(a[0].args(), b[0].args()):
+        assert torch.equal(x, y)
+    assert torch.equal(a[1], b[1])
+
+
+def test_bounded_wait_times_out_and_reports():
+    """A wait nothing completes gives up after its budget, records the status, and the
+    context stays usable."""
+    zs.zs_device_status(clear=True)
+    zs.zs_selftest_wait_timeout(200_000)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status(clear=True) == zs.ZS_DEVERR_SELFTEST
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    x = torch.ones(1024, device=DEV)
+    assert float(x.sum()) == 1024.0
+    with pytest.raises(zs.ZsError):
+        zs.zs_selftest_wait_timeout(0)
+    with pytest.raises(zs.ZsError):
+        zs.zs_set_fused_variant(7)
