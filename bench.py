@@ -278,6 +278,12 @@ def run_ours(args, ws, rank, local):
     plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"], unit_of_param=units)
     P, pads = plan.padded, plan.pad_ranges()
     hp = synth.HPARAMS
+    variant = {"auto": zs.ZS_FUSED_AUTO, "ldg": zs.ZS_FUSED_LDG, "tma": zs.ZS_FUSED_TMA}[args.fused_variant]
+    zs.zs_set_fused_variant(variant)
+    # the kernel the fused step runs for this workload (staged for large 8-aligned ranges)
+    staged = variant == zs.ZS_FUSED_TMA or (variant == zs.ZS_FUSED_AUTO and P >= (1 << 20))
+    staged = staged and n_d in (2, 4, 8, 16, 32)
+    kernel_name = ("k_fused_tma<%d>" if staged else "k_fused<%d,broadcast>") % n_d
     if wl["stage"] == 3:
         raise SystemExit("the default step is the ZeRO-1/2 fused step; use bench_zero3 for ZeRO-3 workloads")
 
@@ -386,12 +392,14 @@ def run_ours(args, ws, rank, local):
                          "%d steps in %.1f s" % (padded, wl["model"], n_d, done, per_step * done)}
 
     if rank == 0:
-        traffic = profiled_traffic(args.workload, "k_fused") if not args.profile_case else None
+        traffic = (profiled_traffic(args.workload, "k_fused_tma" if staged else "k_fused")
+                   if not args.profile_case else None)
         line = {
             "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": args.workload + ("-profile-case" if args.profile_case else ""),
+                       "fused_variant": args.fused_variant,
                        "model_shape": wl["model"], "params": plan.numel, "padded": P, "n_d": n_d,
                        "stage": "zero%d" % wl["stage"], "bucket_bytes": wl["bucket_bytes"],
                        "step": "fused reduce-scatter-mean + AdamW + all-gather, one launch",
@@ -403,7 +411,7 @@ def run_ours(args, ws, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
-                         "bytes_per_padded_element": bpe, "kernel": "k_fused<%d,broadcast>" % n_d,
+                         "bytes_per_padded_element": bpe, "kernel": kernel_name,
                          "kernel_ms": kernel_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -429,6 +437,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused-steps", type=int, default=10)
+    ap.add_argument("--fused-variant", choices=["auto", "ldg", "tma"], default="auto",
+                    help="kernel behind the fused step (all variants compute identical results)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.profile_case:
         log("note: fewer than 3 warm-up steps")

@@ -77,6 +77,8 @@ _sig("zs_fused_step_host", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
 _sig("zs_zero3_gather_unit", [c_vp, c_i32, c_vp, c_vp, c_vp])
 _sig("zs_zero3_rs_step_unit", [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
+_sig("zs_zero3_step", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
+                       ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp])
 _sig("zs_set_fused_variant", [c_i32])
 _sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
 _sig("zs_selftest_wait_timeout", [c_i64, c_vp])
@@ -87,7 +89,7 @@ EXPORTED = [
     "zs_plan_comm_bytes", "zs_adamw_scalars", "zs_last_error", "zs_accumulate_grad",
     "zs_reduce_scatter_mean", "zs_adamw_shard_step", "zs_all_gather", "zs_fused_step",
     "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit", "zs_set_fused_variant",
-    "zs_device_status", "zs_selftest_wait_timeout",
+    "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step",
 ]
 
 
@@ -336,6 +338,29 @@ def zs_zero3_rs_step_unit(plan, unit, grads, master, m, v, shards, hp, step, str
         plan.handle, int(unit), _ptr_array(grads, nu, 2, "grads"),
         _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
         _addr(shards, n, 2, "shards"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+def zs_zero3_step(plan, shards, master, m, v, unit_grads, pool, reshard_after_forward, hp, step,
+                  main_stream=None, side_stream=None):
+    """unit_grads: list (per unit) of N_d tensors; pool: list (per slot) of N_d tensors."""
+    n, nd = plan.padded, plan.n_d
+    if len(unit_grads) != plan.n_units:
+        raise ValueError("unit_grads needs one list of N_d buffers per unit")
+    biggest = max(plan.unit(u)["padded"] for u in range(plan.n_units))
+    flat_g = []
+    for u, per_rank in enumerate(unit_grads):
+        _n_ptrs(ZS_RANK_UNIT, per_rank, nd, "unit_grads[%d]" % u)
+        flat_g += [_addr(x, plan.unit(u)["padded"], 2, "unit_grads[%d]" % u) for x in per_rank]
+    flat_p = []
+    for k, per_rank in enumerate(pool):
+        _n_ptrs(ZS_RANK_UNIT, per_rank, nd, "pool[%d]" % k)
+        flat_p += [_addr(x, biggest, 2, "pool[%d]" % k) for x in per_rank]
+    main = _stream(main_stream)
+    side = main if side_stream is None else _stream(side_stream)
+    return _check(_lib.zs_zero3_step(
+        plan.handle, _addr(shards, n, 2, "shards"), _addr(master, n, 4, "master"), _addr(m, n, 4, "m"),
+        _addr(v, n, 4, "v"), (c_vp * max(len(flat_g), 1))(*flat_g), (c_vp * max(len(flat_p), 1))(*flat_p),
+        len(pool), 1 if reshard_after_forward else 0, ctypes.byref(_hp(hp)), int(step), main, side))
 
 
 def zs_set_fused_variant(variant):

@@ -1,0 +1,161 @@
+// ZeRO-3 / FSDP full-shard step over every unit, scheduled on two streams.
+//
+// "Infra: Data Parallel" (F. Pu), section "Zero Redundancy Optimizer (ZeRO)",
+// ZeRO-3 paragraph and flow figure: before a unit's forward its full
+// parameters are gathered and freed after use; in backward (reverse unit
+// order) they are gathered again, the unit's gradients are reduce-scattered
+// with averaging and each rank updates its own shard; nothing is gathered
+// after the update.  Subsection "FSDP2": with reshard_after_forward off the
+// gathered parameters are kept from forward to backward (one gather fewer).
+//
+// Communication (gathers, reduce-scatter + update) goes on `side`, the
+// compute stream `main` only records and waits on events (the place where a
+// model's forward and backward kernels would run).  Gathers go into a pool of
+// slots, each slot holding N_d unit-sized buffers; with two slots the gather
+// of the next unit overlaps the use of the current one (prefetch depth 1) and
+// a slot is reused only after `main` has released it.  The library creates
+// CUDA events (no device memory) and destroys them before returning; event
+// destruction is deferred by the runtime until the recorded work completes.
+#include <string>
+#include <vector>
+
+#include "launch.h"
+#include "plan.h"
+
+namespace {
+
+int fail(const char* fn, const std::string& what) {
+    zs::set_error(std::string(fn) + ": " + what);
+    return ZS_ERR_INVALID;
+}
+
+struct Events {
+    std::vector<cudaEvent_t> ev;
+    ~Events() {
+        for (auto e : ev) cudaEventDestroy(e);
+    }
+    cudaError_t make(size_t n) {
+        ev.reserve(n);
+        for (size_t i = 0; i < n; ++i) {
+            cudaEvent_t e;
+            cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+            if (r != cudaSuccess) return r;
+            ev.push_back(e);
+        }
+        return cudaSuccess;
+    }
+};
+
+}  // namespace
+
+extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float* m, float* v,
+                             const void* const* unit_grads, void* const* pool, int32_t pool_slots,
+                             int32_t reshard_after_forward, const zs_adamw_hparams* hp, int64_t step,
+                             void* main_stream, void* side_stream) {
+    static const char* fn = "zs_zero3_step";
+    zs::clear_error();
+    if (!plan) return fail(fn, "plan is NULL");
+    const int nd = plan->n_d;
+    const int U = (int)plan->units.size();
+    if (!unit_grads || !pool) return fail(fn, "unit_grads / pool is NULL");
+    const int need_slots = reshard_after_forward ? (U < 2 ? U : 2) : U;
+    if (pool_slots < need_slots)
+        return fail(fn, reshard_after_forward ? "pool needs 2 slots (1 for a single unit)"
+                                              : "pool needs one slot per unit when reshard_after_forward is off");
+    // argument checks of every launch first, so a bad pointer enqueues nothing
+    for (int u = 0; u < U; ++u) {
+        for (int q = 0; q < nd; ++q)
+            if (!unit_grads[(size_t)u * nd + q] || ((uintptr_t)unit_grads[(size_t)u * nd + q] & 15))
+                return fail(fn, "unit_grads entry NULL or not 16-byte aligned");
+    }
+    for (int s = 0; s < pool_slots * nd; ++s)
+        if (!pool[s] || ((uintptr_t)pool[s] & 15)) return fail(fn, "pool entry NULL or not 16-byte aligned");
+    if (!shards || ((uintptr_t)shards & 15) || !master || !m || !v || ((uintptr_t)master & 15) ||
+        ((uintptr_t)m & 15) || ((uintptr_t)v & 15))
+        return fail(fn, "state or shard pointer NULL or not 16-byte aligned");
+    if (!hp || step < 1) return fail(fn, "hparams NULL or step < 1");
+    float sc[8];
+    if (zs_adamw_scalars(hp, step, sc) != ZS_OK) return ZS_ERR_INVALID;
+    if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f && hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+        return fail(fn, "betas must lie in [0, 1)");
+    const zs::AdamScalars s{sc[0], sc[1], sc[2], sc[3], sc[4], sc[5], sc[6], sc[7]};
+
+    cudaStream_t mainS = (cudaStream_t)main_stream, sideS = (cudaStream_t)side_stream;
+    Events E;
+    // per unit: gathered (fwd), released (fwd), gathered (bwd), backward done, released (bwd)
+    cudaError_t err = E.make((size_t)U * 5 + 2);
+    if (err != cudaSuccess) {
+        zs::set_error(std::string(fn) + ": " + cudaGetErrorString(err));
+        return ZS_ERR_CUDA;
+    }
+    auto ev = [&](int u, int k) { return E.ev[(size_t)u * 5 + k]; };
+    cudaEvent_t start = E.ev[(size_t)U * 5];
+    cudaEvent_t done = E.ev[(size_t)U * 5 + 1];
+
+    zs::BView shard_view;
+    for (int q = 0; q < ZS_MAX_RANKS; ++q) shard_view.ptr.p[q] = (uint16_t*)shards;
+    shard_view.off = 0;
+    auto slot_view = [&](int slot, const zs::Unit& un) {
+        zs::BView b{};
+        for (int q = 0; q < nd; ++q) b.ptr.p[q] = (uint16_t*)pool[(size_t)slot * nd + q];
+        b.off = un.base;
+        return b;
+    };
+    auto grad_view = [&](int u) {
+        zs::BView b{};
+        for (int q = 0; q < nd; ++q) b.ptr.p[q] = (uint16_t*)unit_grads[(size_t)u * nd + q];
+        b.off = plan->units[u].base;
+        return b;
+    };
+    auto check = [&](cudaError_t e) {
+        if (e != cudaSuccess && err == cudaSuccess) err = e;
+    };
+
+    // the side stream starts after everything already enqueued on main
+    check(cudaEventRecord(start, mainS));
+    check(cudaStreamWaitEvent(sideS, start, 0));
+
+    // forward, unit order
+    cudaEvent_t slot_free[2] = {nullptr, nullptr};   // main's release of each slot's last user (reshard on)
+    for (int u = 0; u < U && err == cudaSuccess; ++u) {
+        const zs::Unit& un = plan->units[u];
+        const int slot = reshard_after_forward ? (u & 1) : u;
+        if (reshard_after_forward && slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
+        const zs::Range r{un.base, un.base + un.padded, un.base, un.shard};
+        check(zs::launch_gather(shard_view, false, slot_view(slot, un), false, r, nd, sideS));
+        check(cudaEventRecord(ev(u, 0), sideS));
+        check(cudaStreamWaitEvent(mainS, ev(u, 0), 0));
+        // forward(u) runs here on main; afterwards the gathered parameters are released
+        check(cudaEventRecord(ev(u, 1), mainS));
+        if (reshard_after_forward) slot_free[slot] = ev(u, 1);
+    }
+
+    // backward, reverse unit order
+    for (int u = U - 1; u >= 0 && err == cudaSuccess; --u) {
+        const zs::Unit& un = plan->units[u];
+        const zs::Range r{un.base, un.base + un.padded, un.base, un.shard};
+        if (reshard_after_forward) {
+            const int slot = u & 1;
+            if (slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
+            check(zs::launch_gather(shard_view, false, slot_view(slot, un), false, r, nd, sideS));
+            check(cudaEventRecord(ev(u, 2), sideS));
+            check(cudaStreamWaitEvent(mainS, ev(u, 2), 0));
+            // backward(u) runs here on main and produces unit_grads[u]; then the slot is released
+            check(cudaEventRecord(ev(u, 4), mainS));
+            slot_free[slot] = ev(u, 4);
+        } else {
+            check(cudaStreamWaitEvent(mainS, ev(u, 0), 0));   // still gathered from forward
+        }
+        check(cudaEventRecord(ev(u, 3), mainS));             // backward(u) done: its gradients exist
+        check(cudaStreamWaitEvent(sideS, ev(u, 3), 0));
+        check(zs::launch_fused(grad_view(u), master, m, v, shard_view, false, r, s, nd, sideS));
+    }
+    // main continues (the next step's forward) only after the last update
+    check(cudaEventRecord(done, sideS));
+    check(cudaStreamWaitEvent(mainS, done, 0));
+    if (err != cudaSuccess) {
+        zs::set_error(std::string(fn) + ": " + cudaGetErrorString(err));
+        return ZS_ERR_CUDA;
+    }
+    return ZS_OK;
+}

@@ -282,6 +282,31 @@ int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads
                           float* m, float* v, void* shards, const zs_adamw_hparams* hp,
                           int64_t step, void* stream);
 
+/* One ZeRO-3 step over every unit (ZeRO section, ZeRO-3 paragraph and flow
+ * figure; FSDP2 subsection for reshard_after_forward), scheduled on two streams:
+ * forward in unit order gathers each unit into a pool slot; backward in reverse
+ * order gathers it again (only when reshard_after_forward != 0), then reduce-
+ * scatters the unit's gradients with averaging and updates every rank's shard
+ * (zs_zero3_rs_step_unit).  Gathers and updates run on side_stream; main_stream
+ * (the compute stream, where a model's forward/backward would run) only waits
+ * for each gather and releases the slot, and at the end waits for the last
+ * update.  With two slots the next unit's gather overlaps the current unit's use.
+ * side_stream may equal main_stream (everything serialised; same results).
+ *   shards       ZS_SHARDED bf16 parameter shards (updated in place).
+ *   master,m,v   ZS_SHARDED fp32.
+ *   unit_grads   n_units * N_d pointers; unit u, rank q at [u*N_d + q], each
+ *                ZS_RANK_UNIT (padded_u elements).  Entries may repeat.
+ *   pool         pool_slots * N_d pointers; slot k, rank q at [k*N_d + q], each
+ *                at least the largest unit's padded size.  pool_slots >= 2 (1 for
+ *                a single unit) with reshard_after_forward, >= n_units without;
+ *                afterwards each slot holds the last unit gathered into it.
+ * The call creates and releases CUDA events (no device memory).
+ * Errors: ZS_ERR_INVALID (checked before anything is enqueued), ZS_ERR_CUDA. */
+int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float* m, float* v,
+                  const void* const* unit_grads, void* const* pool, int32_t pool_slots,
+                  int32_t reshard_after_forward, const zs_adamw_hparams* hp, int64_t step,
+                  void* main_stream, void* side_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -388,3 +388,70 @@ def test_bounded_wait_times_out_and_reports():
         zs.zs_selftest_wait_timeout(0)
     with pytest.raises(zs.ZsError):
         zs.zs_set_fused_variant(7)
+
+
+# ---------------------------------------------------------------- ZeRO-3 step on two streams
+
+@pytest.mark.parametrize("n_d,reshard", [(16, True), (5, True), (4, False), (2, True)])
+def test_zero3_step_two_streams_matches_oracle(n_d, reshard):
+    """The whole ZeRO-3 step (forward gathers, backward gathers, reduce-scatter + update per
+    unit) with communication on a side stream equals the oracle, and equals the same step
+    with everything serialised on one stream, bit for bit."""
+    shapes, units = _tiny_llama(n_layers=3, d=96, ffn=256, vocab=300)
+    plan, ref = _plans(shapes, n_d, units=units, stage=3)
+    P, pads = plan.padded, plan.pad_ranges()
+    U = plan.n_units
+    biggest = max(plan.unit(u)["padded"] for u in range(U))
+    master0 = synth.master_init(P, pads, seed=12, device=DEV)
+    om, omm, ov = _oracle_state(ref, H.to_np_f32(master0))
+    osh = H.reshard(ref, H.to_np_bf16(master0.to(BF16)))
+    runs = {}
+    for mode in ("overlap", "serial"):
+        st = State(master0)
+        shards = master0.to(BF16)
+        n_slots = 2 if reshard else U
+        pool = [synth.rank_buffers(n_d, biggest, BF16, DEV)[0] for _ in range(n_slots)]
+        main = torch.cuda.current_stream()
+        side = torch.cuda.Stream() if mode == "overlap" else main
+        for t in (1, 2):
+            ugrads = []
+            for u in range(U):
+                ud = plan.unit(u)
+                upads = [(ud["numel"], ud["padded"])] if ud["padded"] > ud["numel"] else []
+                ugrads.append(synth.rank_grads(n_d, ud["padded"], upads, seed=40 + u, step=t, sigma=5e-4,
+                                               device=DEV)[0])
+            zs.zs_zero3_step(plan, shards, *st.args(), ugrads, pool, reshard, HP, t, main_stream=main,
+                             side_stream=side)
+            torch.cuda.synchronize()
+            if mode == "overlap":
+                pre = [s_.copy() for s_ in osh]
+                for u in reversed(range(U)):
+                    _, _, osh, om, omm, ov = steps.zero3_unit_step(ref, u, osh, [H.to_np_bf16(g) for g in ugrads[u]],
+                                                                   om, omm, ov, HP, t)
+                _check_state(ref, st, om, omm, ov, "zero3_step t=%d" % t)
+                H.check_bf16(H.to_np_bf16(shards), H.unshard(ref, osh), "zero3_step shards t=%d" % t)
+                # the slots hold the last units gathered into them, from before the update
+                for u in ((0, 1) if reshard else range(U)):
+                    slot = (u & 1) if reshard else u
+                    want = steps.all_gather_unit(ref, u, pre)
+                    n_u = plan.unit(u)["padded"]
+                    for q in range(n_d):
+                        H.check_bf16(H.to_np_bf16(pool[slot][q][:n_u]), want[q], "pool slot %d q=%d" % (slot, q))
+        runs[mode] = (st, shards)
+    a, b = runs["overlap"], runs["serial"]
+    for x, y in zip(a[0].args(), b[0].args()):
+        assert torch.equal(x, y)
+    assert torch.equal(a[1], b[1])
+
+
+def test_zero3_step_rejects_small_pool():
+    shapes, units = _tiny_llama(n_layers=2)
+    plan, _ = _plans(shapes, 4, units=units, stage=3)
+    P = plan.padded
+    master = torch.zeros(P, device=DEV)
+    ug = [synth.rank_buffers(4, plan.unit(u)["padded"], BF16, DEV)[0] for u in range(plan.n_units)]
+    pool = [synth.rank_buffers(4, max(plan.unit(u)["padded"] for u in range(plan.n_units)), BF16, DEV)[0]]
+    with pytest.raises(zs.ZsError):
+        zs.zs_zero3_step(plan, master.to(BF16), master, master.clone(), master.clone(), ug, pool, True, HP, 1)
+    with pytest.raises(zs.ZsError):
+        zs.zs_zero3_step(plan, master.to(BF16), master, master.clone(), master.clone(), ug, pool * 2, False, HP, 1)
