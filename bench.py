@@ -84,13 +84,16 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("device.cuh", "launch.h", "kernels.cu", "kernels_tma.cu")
+
+
 def source_digest():
+    """Digest of the files that define the fused kernels (a profile is valid only for these sources)."""
     csrc = os.path.join(ROOT, "fsdp_sharded_optimizer_flatparameter_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -257,59 +260,125 @@ def run_reference(args, ws, rank):
 
 # ------------------------------------------------------------------ our arm
 
+class Workload:
+    """Device buffers and the timed step of one benchmarked workload."""
+
+    def __init__(self, args, dev, stream):
+        import torch
+
+        import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+        from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+        self.zs, self.torch = zs, torch
+        self.args, self.dev, self.stream = args, dev, stream
+        wl = self.wl = dict(synth.WORKLOADS[args.workload])
+        shapes, units = synth.workload_params(wl["model"])
+        if args.profile_case:
+            # the same kernel on a smaller flat buffer (32 Mi elements, 1.9 GB at N_d = 8): for ncu captures
+            shapes, units = [(32 << 20,)], None
+        self.n_d = n_d = wl["n_d"]
+        self.plan = plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"],
+                                   unit_of_param=units)
+        P, pads = plan.padded, plan.pad_ranges()
+        self.P, self.pads = P, pads
+        self.hp = synth.HPARAMS
+        self.t = 0
+        self.master = synth.master_init(P, pads, wl["seed"], device=dev)
+        self.m, self.v = torch.zeros_like(self.master), torch.zeros_like(self.master)
+        self.kind = "zero3" if wl["stage"] == 3 else ("accumulate+fused" if wl["micro"] > 1 else "fused")
+        bf16 = torch.bfloat16
+        if self.kind == "zero3":
+            U = plan.n_units
+            biggest = max(plan.unit(u)["padded"] for u in range(U))
+            self.shards = self.master.to(bf16)
+            # one set of per-rank gradient buffers, read as every unit's backward gradients
+            self.ugrads, self._gb = synth.rank_buffers(n_d, biggest, bf16, dev)
+            synth.fill_grads(self.ugrads, [], wl["seed"], 1, wl["sigma"], wl["outlier_p"])
+            self.pool = [synth.rank_buffers(n_d, biggest, bf16, dev)[0] for _ in range(2)]
+            self.side = torch.cuda.Stream(dev)
+            self.resident = (12 + 2) * P + 3 * n_d * biggest * 2
+        else:
+            self.grads, self._gb = synth.rank_buffers(n_d, P, bf16, dev)
+            synth.fill_grads(self.grads, pads, wl["seed"], 1, wl["sigma"], wl["outlier_p"])
+            self.reps, self._rb = synth.rank_buffers(n_d, P, bf16, dev)
+            self.resident = 12 * P + 2 * 2 * n_d * P
+            if self.kind == "accumulate+fused":
+                self.acc, self._ab = synth.rank_buffers(n_d, P, bf16, dev)
+                self.resident += 2 * n_d * P
+
+    # algorithmic HBM bytes of one step and the kernel launches it makes
+    def step_bytes(self):
+        n_d, P = self.n_d, self.P
+        if self.kind == "fused":
+            return bytes_per_padded_element(n_d, "fused") * P, 1
+        if self.kind == "accumulate+fused":
+            micro = self.wl["micro"]
+            acc = n_d * P * (4 + 6 * (micro - 1))       # first: read micro, write acc; then read both, write acc
+            return acc + bytes_per_padded_element(n_d, "fused") * P, micro + 1
+        # zero3: per unit two gathers (read shard, write N_d copies) + reduce-scatter with update
+        return P * (2 * (2 + 2 * n_d) + (2 * n_d + 12 + 12 + 2)), 3 * self.plan.n_units
+
+    def staged(self):
+        zs = self.zs
+        v = zs.fused_variant_setting
+        big = (self.P >= (1 << 20)) if self.kind != "zero3" else True
+        return self.n_d in (2, 4, 8, 16, 32) and (v == zs.ZS_FUSED_TMA or (v == zs.ZS_FUSED_AUTO and big))
+
+    def kernel_label(self):
+        fused = ("k_fused_tma<%d>" if self.staged() else "k_fused<%d>") % self.n_d
+        if self.kind == "fused":
+            return fused
+        if self.kind == "accumulate+fused":
+            return "%d x k_accumulate + %s" % (self.wl["micro"], fused)
+        return "2 x k_gather<%d> + %s per unit" % (self.n_d, fused)
+
+    def step(self):
+        zs, plan, hp = self.zs, self.plan, self.hp
+        self.t += 1
+        t, st = self.t, self.stream
+        if self.kind == "fused":
+            zs.zs_fused_step(plan, -1, self.grads, zs.ZS_RANK_FULL, self.master, self.m, self.v, self.reps, hp, t,
+                             stream=st)
+        elif self.kind == "accumulate+fused":
+            micro = self.wl["micro"]
+            for j in range(micro):
+                zs.zs_accumulate_grad(plan, self.acc, self.grads, 1.0 / micro, first=(j == 0), stream=st)
+            zs.zs_fused_step(plan, -1, self.acc, zs.ZS_RANK_FULL, self.master, self.m, self.v, self.reps, hp, t,
+                             stream=st)
+        else:
+            ug = [self.ugrads] * plan.n_units
+            zs.zs_zero3_step(plan, self.shards, self.master, self.m, self.v, ug, self.pool, True, hp, t,
+                             main_stream=st, side_stream=self.side)
+
+
 def run_ours(args, ws, rank, local):
     import torch
 
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = maybe_init_dist(ws, "nccl")
-
-    wl = dict(synth.WORKLOADS[args.workload])
-    shapes, units = synth.workload_params(wl["model"])
-    if args.profile_case:
-        # the same kernel on a smaller flat buffer (32 Mi elements, 1.9 GB at N_d = 8): for ncu captures
-        shapes, units = [(32 << 20,)], None
-    n_d = wl["n_d"]
-    plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"], unit_of_param=units)
-    P, pads = plan.padded, plan.pad_ranges()
-    hp = synth.HPARAMS
     variant = {"auto": zs.ZS_FUSED_AUTO, "ldg": zs.ZS_FUSED_LDG, "tma": zs.ZS_FUSED_TMA}[args.fused_variant]
     zs.zs_set_fused_variant(variant)
-    # the kernel the fused step runs for this workload (staged for large 8-aligned ranges)
-    staged = variant == zs.ZS_FUSED_TMA or (variant == zs.ZS_FUSED_AUTO and P >= (1 << 20))
-    staged = staged and n_d in (2, 4, 8, 16, 32)
-    kernel_name = ("k_fused_tma<%d>" if staged else "k_fused<%d,broadcast>") % n_d
-    if wl["stage"] == 3:
-        raise SystemExit("the default step is the ZeRO-1/2 fused step; use bench_zero3 for ZeRO-3 workloads")
+    zs.fused_variant_setting = variant
 
-    t_setup = time.perf_counter()
-    master = synth.master_init(P, pads, wl["seed"], device=dev)
-    m, v = torch.zeros_like(master), torch.zeros_like(master)
-    grads, gbase = synth.rank_buffers(n_d, P, torch.bfloat16, dev)
-    synth.fill_grads(grads, pads, wl["seed"], 1, wl["sigma"], wl["outlier_p"])
-    reps, rbase = synth.rank_buffers(n_d, P, torch.bfloat16, dev)
     stream = torch.cuda.current_stream(dev)
+    t_setup = time.perf_counter()
+    W = Workload(args, dev, stream)
+    plan, n_d, P = W.plan, W.n_d, W.P
     torch.cuda.synchronize(dev)
     log("setup %.1fs: %s, %d params (padded %d), N_d=%d, %.1f GB resident" % (
-        time.perf_counter() - t_setup, args.workload, plan.numel, P, n_d,
-        (gbase.numel() * 2 + rbase.numel() * 2 + 3 * master.numel() * 4) / 1e9))
-
-    step = [0]
-
-    def one_step():
-        step[0] += 1
-        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, step[0], stream=stream)
+        time.perf_counter() - t_setup, args.workload, plan.numel, P, n_d, W.resident / 1e9))
 
     for _ in range(args.warmup):
-        one_step()
+        W.step()
     torch.cuda.synchronize(dev)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    steps = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     sampler = ClockSampler(local)
     if dist is not None:
         dist.barrier()
@@ -319,40 +388,37 @@ def run_ours(args, ws, rank, local):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for k in range(args.steps):
+    for k in range(steps):
         ev[k][0].record(stream)
-        one_step()
+        W.step()
         ev[k][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms = t0.elapsed_time(t1)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = max_over_ranks(dist, total_ms, dev)
-    kernel_ms = statistics.mean(launch_ms)
+    total_ms = max_over_ranks(dist, t0.elapsed_time(t1), dev)
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
-    value = ws * plan.numel * args.steps / (total_ms / 1e3)
-    bpe = bytes_per_padded_element(n_d, "fused")
-    algo_bytes = bpe * P
-    achieved = algo_bytes / (kernel_ms / 1e3) / 1e9
+    value = ws * plan.numel * steps / (total_ms / 1e3)
+    algo_bytes, launches = W.step_bytes()
+    achieved = algo_bytes / (step_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
 
     # the unfused path on the same buffers, for comparison (not part of value)
     unfused = None
-    if not args.profile_case and rank == 0 and args.unfused_steps > 0:
+    if W.kind == "fused" and not args.profile_case and rank == 0 and args.unfused_steps > 0:
         ghat = torch.empty(P, dtype=torch.bfloat16, device=dev)
         shards = torch.empty(P, dtype=torch.bfloat16, device=dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for k in range(args.unfused_steps + 2):
             if k == 2:
                 a.record(stream)
-            step[0] += 1
-            zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED, stream=stream)
-            zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, master, m, v, [shards], zs.ZS_SHARDED, hp,
-                                   step[0], stream=stream)
-            zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps, stream=stream)
+            W.t += 1
+            zs.zs_reduce_scatter_mean(plan, -1, W.grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED, stream=stream)
+            zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, W.master, W.m, W.v, [shards], zs.ZS_SHARDED,
+                                   W.hp, W.t, stream=stream)
+            zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, W.reps, stream=stream)
         b.record(stream)
         torch.cuda.synchronize(dev)
         ums = a.elapsed_time(b) / args.unfused_steps
@@ -361,61 +427,70 @@ def run_ours(args, ws, rank, local):
                    "launches_per_step": 3}
         del ghat, shards
 
-    # end to end through the C ABI with host buffers: H2D of every rank's gradients, the step, D2H of a replica
+    # end to end through the C ABI with host buffers: every rank's gradients come from pinned host
+    # memory bucket by bucket through a two-slot device staging ring (copies overlap the per-bucket
+    # fused update) and rank 0's updated replica goes back to the host, all inside the timed region
     e2e = None
-    if not args.no_e2e and not args.profile_case:
+    if W.kind == "fused" and not args.no_e2e and not args.profile_case:
         host_g = torch.empty((n_d, P), dtype=torch.bfloat16, pin_memory=True)
         for q in range(n_d):
-            host_g[q].copy_(grads[q], non_blocking=False)
+            host_g[q].copy_(W.grads[q])
         host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
         hptrs = [host_g[q].data_ptr() for q in range(n_d)]
+        biggest = max(hi - lo for _, lo, hi in (plan.bucket(b) for b in range(plan.n_buckets)))
+        staging = [zs_synth_buffers(n_d, biggest, dev) for _ in range(2)]
+        copy_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_e2e = max(2, min(args.steps, 5))
+        n_e2e = max(2, min(steps, 5))
         for k in range(n_e2e + 1):
             if k == 1:
                 a.record(stream)
-            step[0] += 1
-            zs.zs_fused_step_host(plan, hptrs, grads, master, m, v, reps, hp, step[0], host_out.data_ptr(),
-                                  stream=stream)
+            W.t += 1
+            zs.zs_zero2_step_host(plan, hptrs, staging, W.master, W.m, W.v, W.reps, W.hp, W.t,
+                                  host_replica0=host_out.data_ptr(), stream=stream, copy_stream=copy_s,
+                                  d2h_stream=d2h_s)
         b.record(stream)
         torch.cuda.synchronize(dev)
         ems = max_over_ranks(dist, a.elapsed_time(b) / n_e2e, dev)
         e2e = {"value": ws * plan.numel / (ems / 1e3), "unit": "params/s", "ms_per_step": ems,
-               "h2d_bytes_per_step": n_d * P * 2, "d2h_bytes_per_step": P * 2}
-        del host_g, host_out
+               "h2d_bytes_per_step": n_d * P * 2, "d2h_bytes_per_step": P * 2,
+               "path": "zs_zero2_step_host: bucket-wise H2D through a 2-slot staging ring, fused update per "
+                       "bucket, D2H of rank 0's replica"}
+        del host_g, host_out, staging
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.profile_case:
-        per_step, done, padded = time_oracle(n_d, 1 << 20, wl["sigma"], wl["outlier_p"], wl["seed"], 10.0)
+        per_step, done, padded = time_oracle(n_d, 1 << 20, W.wl["sigma"], W.wl["outlier_p"], W.wl["seed"], 10.0)
         cpu = {"value": padded / per_step, "unit": "params/s", "cores": cpu_threads_used(), "kind": "oracle",
                "sample": "oracle ZeRO step (numpy fp32) on a %d-element sample of the %s flat buffer, N_d=%d, "
-                         "%d steps in %.1f s" % (padded, wl["model"], n_d, done, per_step * done)}
+                         "%d steps in %.1f s" % (padded, W.wl["model"], n_d, done, per_step * done)}
 
     if rank == 0:
-        traffic = (profiled_traffic(args.workload, "k_fused_tma" if staged else "k_fused")
-                   if not args.profile_case else None)
+        staged = W.staged()
+        traffic = None
+        if W.kind == "fused" and not args.profile_case:
+            traffic = profiled_traffic(args.workload, "k_fused_tma" if staged else "k_fused")
         line = {
-            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": args.workload + ("-profile-case" if args.profile_case else ""),
-                       "fused_variant": args.fused_variant,
-                       "model_shape": wl["model"], "params": plan.numel, "padded": P, "n_d": n_d,
-                       "stage": "zero%d" % wl["stage"], "bucket_bytes": wl["bucket_bytes"],
-                       "step": "fused reduce-scatter-mean + AdamW + all-gather, one launch",
+                       "fused_variant": args.fused_variant, "model_shape": W.wl["model"], "params": plan.numel,
+                       "padded": P, "n_d": n_d, "stage": "zero%d" % W.wl["stage"],
+                       "bucket_bytes": W.wl["bucket_bytes"], "step": W.kind,
                        "storage": "bf16 params/grads, fp32 master/m/v",
-                       "l2": "inputs %.0f GB >> 129 MB L2, no flush" % ((4 * n_d + 24) * P / 1e9),
+                       "l2": "step moves %.0f GB >> 129 MB L2, no flush" % (algo_bytes / 1e9),
                        "parallelism": "replicas" if ws > 1 else "1 GPU, %d simulated ranks" % n_d},
             "hbm_gbs": achieved,
             "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
-                         "bytes_per_padded_element": bpe, "kernel": kernel_name,
-                         "kernel_ms": kernel_ms},
+                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": algo_bytes if launches == 1 else None,
+                         "algorithmic_bytes_per_step": algo_bytes, "kernel": W.kernel_label(),
+                         "kernel_ms": step_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": launches * steps,
             "clocks": clocks,
             "unfused": unfused,
         }
@@ -426,10 +501,19 @@ def run_ours(args, ws, rank, local):
     return 0
 
 
+def zs_synth_buffers(n_d, n, dev):
+    import torch
+
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    return synth.rank_buffers(n_d, n, torch.bfloat16, dev)[0]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 200; 20 for the ZeRO-3 workload)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-1.3b-zero2")
@@ -442,6 +526,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.profile_case:
         log("note: fewer than 3 warm-up steps")
+    if args.steps is None:
+        args.steps = 20 if "zero3" in args.workload else 200
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, ws, rank)

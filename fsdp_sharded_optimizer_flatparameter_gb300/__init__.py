@@ -79,6 +79,8 @@ _sig("zs_zero3_rs_step_unit", [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
 _sig("zs_zero3_step", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                        ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp])
+_sig("zs_zero2_step_host", [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_vp, c_vp,
+                            ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp, c_vp, c_vp])
 _sig("zs_set_fused_variant", [c_i32])
 _sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
 _sig("zs_selftest_wait_timeout", [c_i64, c_vp])
@@ -89,7 +91,7 @@ EXPORTED = [
     "zs_plan_comm_bytes", "zs_adamw_scalars", "zs_last_error", "zs_accumulate_grad",
     "zs_reduce_scatter_mean", "zs_adamw_shard_step", "zs_all_gather", "zs_fused_step",
     "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit", "zs_set_fused_variant",
-    "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step",
+    "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step", "zs_zero2_step_host",
 ]
 
 
@@ -361,6 +363,28 @@ def zs_zero3_step(plan, shards, master, m, v, unit_grads, pool, reshard_after_fo
         plan.handle, _addr(shards, n, 2, "shards"), _addr(master, n, 4, "master"), _addr(m, n, 4, "m"),
         _addr(v, n, 4, "v"), (c_vp * max(len(flat_g), 1))(*flat_g), (c_vp * max(len(flat_p), 1))(*flat_p),
         len(pool), 1 if reshard_after_forward else 0, ctypes.byref(_hp(hp)), int(step), main, side))
+
+
+def zs_zero2_step_host(plan, host_grads, staging, master, m, v, replicas, hp, step, host_replica0=None,
+                       stream=None, copy_stream=None, d2h_stream=None):
+    """host_grads: N_d host tensors/addresses; staging: 2 lists of N_d device tensors (bucket-sized)."""
+    n, nd = plan.padded, plan.n_d
+    _n_ptrs(ZS_RANK_FULL, host_grads, nd, "host_grads")
+    if len(staging) != 2:
+        raise ValueError("staging needs 2 slots of N_d buffers")
+    biggest = max(hi - lo for _, lo, hi in (plan.bucket(b) for b in range(plan.n_buckets)))
+    flat_s = []
+    for k, per_rank in enumerate(staging):
+        _n_ptrs(ZS_RANK_BUCKET, per_rank, nd, "staging[%d]" % k)
+        flat_s += [_addr(x, biggest, 2, "staging[%d]" % k) for x in per_rank]
+    main = _stream(stream)
+    cp = _stream(copy_stream) if copy_stream is not None else main
+    d2 = _stream(d2h_stream) if d2h_stream is not None else None
+    return _check(_lib.zs_zero2_step_host(
+        plan.handle, _ptr_array(host_grads, n, 2, "host_grads", device=False), (c_vp * len(flat_s))(*flat_s),
+        biggest, _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+        _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)), int(step),
+        _addr(host_replica0, n, 2, "host_replica0", device=False), main, cp, d2))
 
 
 def zs_set_fused_variant(variant):

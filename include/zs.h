@@ -282,6 +282,27 @@ int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads
                           float* m, float* v, void* shards, const zs_adamw_hparams* hp,
                           int64_t step, void* stream);
 
+/* ZeRO-2 step fed from host memory ("Infra: Data Parallel", ZeRO section,
+ * ZeRO-2 paragraph and flow figure: gradients are reduced bucket by bucket and
+ * no rank keeps a full gradient buffer).  For each bucket, in descending order:
+ * one host-to-device copy per rank of the bucket's gradients into one slot of a
+ * two-slot staging ring (copy_stream), the fused step on that bucket (stream),
+ * which frees the slot, and, when host_replica0 is given, a device-to-host copy
+ * of the bucket's slice of rank 0's updated replica (d2h_stream, or copy_stream
+ * when NULL).  Copies of the next bucket overlap the update of this one.  Same
+ * results as zs_fused_step over the whole flat space.  `stream` waits for all
+ * of it at the end; the caller synchronises before reading host_replica0.
+ *   host_grads     N_d host pointers (pinned for asynchronous copies), each
+ *                  holding the rank's padded_numel gradients.
+ *   staging        2 * N_d device pointers; slot k, rank q at [k*N_d + q], each
+ *                  at least staging_elems >= the largest bucket's elements.
+ *   replicas       ZS_RANK_FULL; master/m/v ZS_SHARDED.
+ * Errors: ZS_ERR_INVALID (before anything is enqueued), ZS_ERR_CUDA. */
+int zs_zero2_step_host(zs_plan_t plan, const void* const* host_grads, void* const* staging,
+                       int64_t staging_elems, float* master, float* m, float* v, void* const* replicas,
+                       const zs_adamw_hparams* hp, int64_t step, void* host_replica0, void* stream,
+                       void* copy_stream, void* d2h_stream);
+
 /* One ZeRO-3 step over every unit (ZeRO section, ZeRO-3 paragraph and flow
  * figure; FSDP2 subsection for reshard_after_forward), scheduled on two streams:
  * forward in unit order gathers each unit into a pool slot; backward in reverse

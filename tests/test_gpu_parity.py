@@ -455,3 +455,38 @@ def test_zero3_step_rejects_small_pool():
         zs.zs_zero3_step(plan, master.to(BF16), master, master.clone(), master.clone(), ug, pool, True, HP, 1)
     with pytest.raises(zs.ZsError):
         zs.zs_zero3_step(plan, master.to(BF16), master, master.clone(), master.clone(), ug, pool * 2, False, HP, 1)
+
+
+# ---------------------------------------------------------------- host-fed steps
+
+@pytest.mark.parametrize("n_d,numel,bucket_bytes", [(8, 1_000_003, 1 << 18), (4, 262_912, 0), (3, 77_777, 10_000)])
+def test_host_fed_steps_match_device_fused_step(n_d, numel, bucket_bytes):
+    """zs_zero2_step_host (bucket-wise copies through a two-slot staging ring on a copy
+    stream, overlapped with the per-bucket update) and zs_fused_step_host equal
+    zs_fused_step on device-resident gradients, bit for bit, including the host copy of
+    rank 0's replica."""
+    plan, _ = _plans([(numel,)], n_d, bucket_bytes=bucket_bytes)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=13, device=DEV)
+    sts = [State(master0) for _ in range(3)]
+    reps = [synth.rank_buffers(n_d, P, BF16, DEV)[0] for _ in range(3)]
+    biggest = max(hi - lo for _, lo, hi in (plan.bucket(b) for b in range(plan.n_buckets)))
+    staging = [synth.rank_buffers(n_d, biggest, BF16, DEV)[0] for _ in range(2)]
+    dev_grads = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    copy_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    for t in (1, 2, 3):
+        grads, _ = synth.rank_grads(n_d, P, pads, seed=13, step=t, sigma=1e-3, device=DEV)
+        host = [g.cpu().pin_memory() for g in grads]
+        out1 = torch.empty(P, dtype=BF16).pin_memory()
+        out2 = torch.empty(P, dtype=BF16).pin_memory()
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *sts[0].args(), reps[0], HP, t)
+        zs.zs_zero2_step_host(plan, host, staging, *sts[1].args(), reps[1], HP, t, host_replica0=out1,
+                              copy_stream=copy_stream, d2h_stream=d2h_stream)
+        zs.zs_fused_step_host(plan, host, dev_grads, *sts[2].args(), reps[2], HP, t, host_replica0=out2)
+        torch.cuda.synchronize()
+        for k in (1, 2):
+            for x, y in zip(sts[0].args(), sts[k].args()):
+                assert torch.equal(x, y)
+            for q in range(n_d):
+                assert torch.equal(reps[0][q], reps[k][q])
+        assert torch.equal(out1, reps[0][0].cpu()) and torch.equal(out2, reps[0][0].cpu())
