@@ -81,6 +81,8 @@ _sig("zs_zero3_step", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                        ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp])
 _sig("zs_zero2_step_host", [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_vp, c_vp,
                             ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp, c_vp, c_vp])
+_sig("zs_checkpoint_save", [c_vp, ctypes.c_char_p, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp])
+_sig("zs_checkpoint_load", [c_vp, ctypes.c_char_p, c_vp, c_vp, c_vp, c_vp, P_i64, c_vp])
 _sig("zs_set_fused_variant", [c_i32])
 _sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
 _sig("zs_selftest_wait_timeout", [c_i64, c_vp])
@@ -92,6 +94,7 @@ EXPORTED = [
     "zs_reduce_scatter_mean", "zs_adamw_shard_step", "zs_all_gather", "zs_fused_step",
     "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit", "zs_set_fused_variant",
     "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step", "zs_zero2_step_host",
+    "zs_checkpoint_save", "zs_checkpoint_load",
 ]
 
 
@@ -387,6 +390,23 @@ def zs_zero2_step_host(plan, host_grads, staging, master, m, v, replicas, hp, st
         _addr(host_replica0, n, 2, "host_replica0", device=False), main, cp, d2))
 
 
+def zs_checkpoint_save(plan, directory, shards, master, m, v, step, stream=None):
+    n = plan.padded
+    return _check(_lib.zs_checkpoint_save(plan.handle, os.fsencode(directory), _addr(shards, n, 2, "shards"),
+                                          _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+                                          int(step), _stream(stream)))
+
+
+def zs_checkpoint_load(plan, directory, shards, master, m, v, stream=None):
+    """Returns the saved step."""
+    n = plan.padded
+    step = c_i64()
+    _check(_lib.zs_checkpoint_load(plan.handle, os.fsencode(directory), _addr(shards, n, 2, "shards"),
+                                   _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+                                   ctypes.byref(step), _stream(stream)))
+    return step.value
+
+
 def zs_set_fused_variant(variant):
     return _check(_lib.zs_set_fused_variant(int(variant)))
 
@@ -403,4 +423,3 @@ def zs_selftest_wait_timeout(limit_cycles, stream=None):
 
 __all__ = ["Plan", "ZsError", "zs_adamw_hparams", "LIB_PATH"] + EXPORTED + [
     n for n in dir() if n.startswith("ZS_")]
-del os

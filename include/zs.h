@@ -282,6 +282,28 @@ int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads
                           float* m, float* v, void* shards, const zs_adamw_hparams* hp,
                           int64_t step, void* stream);
 
+/* Sharded checkpoint ("Infra: Data Parallel", FSDP section, subsection
+ * "Checkpoint": each rank writes the shards it owns plus the metadata needed to
+ * restore them; loading follows the target layout, so the rank count may differ;
+ * optimizer state is saved with the weights).
+ * zs_checkpoint_save writes dir/meta.txt (format tag, N_d, step, parameter
+ * element counts and units, per-unit numel/padded/shard) and one file per
+ * simulated rank, dir/rank-NNNNN.bin, holding that rank's shard of the bf16
+ * parameters, then master, m and v (each the rank's piece of every unit, units in
+ * order).  zs_checkpoint_load reads such a directory into the ZS_SHARDED arrays of
+ * `plan`, which must describe the same parameters and units but may have another
+ * N_d: each unit's real elements keep their order, the new padding is zeroed.
+ * `dir` must exist.  Arrays are ZS_SHARDED device arrays of plan's padded_numel
+ * elements.  Both calls copy through a 64 MiB host buffer with cudaMemcpyAsync on
+ * `stream` and synchronise it (they return after the data is in place).
+ * Errors: ZS_ERR_INVALID (NULL argument, I/O failure, a checkpoint of another
+ * model or a malformed one: nothing is written to the device before the metadata
+ * and file sizes are checked), ZS_ERR_CUDA. */
+int zs_checkpoint_save(zs_plan_t plan, const char* dir, const void* shards, const float* master,
+                       const float* m, const float* v, int64_t step, void* stream);
+int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards, float* master, float* m,
+                       float* v, int64_t* step, void* stream);
+
 /* ZeRO-2 step fed from host memory ("Infra: Data Parallel", ZeRO section,
  * ZeRO-2 paragraph and flow figure: gradients are reduced bucket by bucket and
  * no rank keeps a full gradient buffer).  For each bucket, in descending order:
