@@ -83,6 +83,8 @@ _sig("zs_zero2_step_host", [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_vp, c_vp,
                             ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp, c_vp, c_vp])
 _sig("zs_checkpoint_save", [c_vp, ctypes.c_char_p, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp])
 _sig("zs_checkpoint_load", [c_vp, ctypes.c_char_p, c_vp, c_vp, c_vp, c_vp, P_i64, c_vp])
+_sig("zs_zero2_step_host_noalloc", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(zs_adamw_hparams), c_i64,
+                                    c_vp, c_vp])
 _sig("zs_set_fused_variant", [c_i32])
 _sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
 _sig("zs_selftest_wait_timeout", [c_i64, c_vp])
@@ -94,7 +96,7 @@ EXPORTED = [
     "zs_reduce_scatter_mean", "zs_adamw_shard_step", "zs_all_gather", "zs_fused_step",
     "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit", "zs_set_fused_variant",
     "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step", "zs_zero2_step_host",
-    "zs_checkpoint_save", "zs_checkpoint_load",
+    "zs_checkpoint_save", "zs_checkpoint_load", "zs_zero2_step_host_noalloc",
 ]
 
 
@@ -405,6 +407,17 @@ def zs_checkpoint_load(plan, directory, shards, master, m, v, stream=None):
                                    _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
                                    ctypes.byref(step), _stream(stream)))
     return step.value
+
+
+def zs_zero2_step_host_noalloc(plan, host_grads, master, m, v, replicas, hp, step, host_replica0=None,
+                               stream=None):
+    """zs_zero2_step_host with the staging ring inside the library: allocates nothing."""
+    n = plan.padded
+    _n_ptrs(ZS_RANK_FULL, host_grads, plan.n_d, "host_grads")
+    return _check(_lib.zs_zero2_step_host_noalloc(
+        plan.handle, _ptr_array(host_grads, n, 2, "host_grads", device=False), _addr(master, n, 4, "master"),
+        _addr(m, n, 4, "m"), _addr(v, n, 4, "v"), _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)),
+        int(step), _addr(host_replica0, n, 2, "host_replica0", device=False), _stream(stream)))
 
 
 def zs_set_fused_variant(variant):

@@ -325,6 +325,33 @@ int zs_zero2_step_host(zs_plan_t plan, const void* const* host_grads, void* cons
                        const zs_adamw_hparams* hp, int64_t step, void* host_replica0, void* stream,
                        void* copy_stream, void* d2h_stream);
 
+/* zs_zero2_step_host without caller-provided staging: a variant for callers
+ * that cannot allocate device memory when they run the step (a framework that
+ * owns all device memory through its own pool, a latency-critical thread that
+ * must not pay cudaMalloc's implicit device synchronisation, a plug-in handed only
+ * stream and buffer pointers).  The pages have no counterpart: this is a
+ * property of the library, not of the method.
+ * The two-slot staging ring is a fixed device array inside the library image,
+ * ZS_NOALLOC_STAGING_BYTES (32 MiB) per GPU, held by every GPU that loads the
+ * library until the process exits; the call itself allocates nothing (no
+ * cudaMalloc, no events).  The first call on a device looks up the array's device
+ * address with that device current (cudaGetSymbolAddress) and caches it; make
+ * that first call before any stream capture begins.  Copies, updates and the
+ * copy-back of rank 0's replica all run in order on `stream` (no overlap).
+ * Every call on a device shares the one array and leaves its last contents in
+ * it; nothing in it has to start at zero because each bucket is copied in before
+ * it is read.  Calls whose work overlaps on the GPU (other streams, other host
+ * threads) race on the array: serialise them.
+ * Same arguments and results as zs_zero2_step_host minus the staging.  Plans
+ * whose 2 x N_d x largest bucket (rounded up to 8 elements) x 2 bytes exceed
+ * ZS_NOALLOC_STAGING_BYTES are rejected with ZS_ERR_INVALID and a message that
+ * states the limit.  Errors: ZS_ERR_INVALID (before anything is enqueued),
+ * ZS_ERR_CUDA. */
+#define ZS_NOALLOC_STAGING_BYTES (32ll << 20)
+int zs_zero2_step_host_noalloc(zs_plan_t plan, const void* const* host_grads, float* master, float* m,
+                               float* v, void* const* replicas, const zs_adamw_hparams* hp, int64_t step,
+                               void* host_replica0, void* stream);
+
 /* One ZeRO-3 step over every unit (ZeRO section, ZeRO-3 paragraph and flow
  * figure; FSDP2 subsection for reshard_after_forward), scheduled on two streams:
  * forward in unit order gathers each unit into a pool slot; backward in reverse
