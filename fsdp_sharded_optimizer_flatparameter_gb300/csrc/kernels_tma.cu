@@ -10,9 +10,12 @@
 // counted in bytes on the stage's "full" mbarrier, L2 evict-first); NCW
 // consumer warps wait for the stage, each thread computes VPT consecutive
 // elements from shared memory, streams its results straight to global memory
-// and the warp releases the stage on its "empty" mbarrier.  With up to
-// STAGES-1 tiles in flight per SM the loads keep ~200 KB of reads outstanding
-// per SM independent of register pressure.
+// and releases the stage on its "empty" mbarrier.  With up to STAGES-1 tiles
+// in flight per CTA the loads keep up to ~200 KB of reads outstanding per SM
+// independent of register pressure.  The tile shape per rank count (warps,
+// elements per thread, ring depth, one or two CTAs per SM) was picked by
+// measurement; ring depth is not monotone in benefit on GB300 (for N_d = 8,
+// 8 stages of 1024 elements beat both 6-7 and 16 stages).
 //
 // Every wait is bounded (clock64 budget).  A wait that runs out sets
 // g_zs_device_error, the CTA stops taking tiles, the producer waits (again
@@ -122,19 +125,22 @@ struct TmaArgs {
     long long drain_limit;// cycles to wait for copies still in flight after giving up
 };
 
-template <int ND, int NCW, int VPT>
+// Tile and ring geometry: T elements per tile, as many stages as fit in
+// BUDGET bytes of shared memory (at most MAXST), 256 bytes of barriers first.
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
 struct TmaShape {
     static constexpr int kT = NCW * 32 * VPT;                           // elements per tile
     static constexpr int kStageBytes = kT * (2 * ND + 12);
-    static constexpr int kBudget = 227 * 1024 - 256;
-    static constexpr int kStages = (kBudget / kStageBytes) > 8 ? 8 : (kBudget / kStageBytes);
+    static constexpr int kFit = (BUDGET - 256) / kStageBytes;
+    static constexpr int kStages = kFit > MAXST ? MAXST : kFit;
     static constexpr int kSmem = 256 + kStages * kStageBytes;
     static_assert(kStages >= 2, "tile too large for a 2-stage ring");
+    static_assert(2 * kStages * 8 <= 256, "barriers must fit in the first 256 bytes");
 };
 
-template <int ND, int NCW, int VPT, bool BROADCAST>
-__global__ void __launch_bounds__(32 * (NCW + 1), 1) k_fused_tma(const __grid_constant__ TmaArgs a) {
-    using Sh = TmaShape<ND, NCW, VPT>;
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_constant__ TmaArgs a) {
+    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -265,18 +271,21 @@ __global__ void __launch_bounds__(32 * (NCW + 1), 1) k_fused_tma(const __grid_co
 
 namespace {
 
-template <int ND, int NCW, int VPT, bool BROADCAST>
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
 cudaError_t tma_impl(const TmaArgs& a, cudaStream_t st) {
-    using Sh = TmaShape<ND, NCW, VPT>;
-    auto kern = k_fused_tma<ND, NCW, VPT, BROADCAST>;
+    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
+    auto kern = k_fused_tma<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>;
     // set on every launch: the attribute belongs to the current device
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
+    int dev = 0, sms = 0, per_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), Sh::kSmem);
+    if (per_sm < 1) per_sm = 1;
     const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
-    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
+    const int grid = (int)(ntiles < cap ? ntiles : cap);
     kern<<<grid, 32 * (NCW + 1), Sh::kSmem, st>>>(a);
     return cudaGetLastError();
 }
@@ -301,14 +310,17 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
     a.inv_nd = 1.0f / (float)nd;
     a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
     a.drain_limit = 4000000000LL;
-#define ZS_TMA(ND_, NCW_, VPT_)                                                          \
-    return broadcast ? tma_impl<ND_, NCW_, VPT_, true>(a, st) : tma_impl<ND_, NCW_, VPT_, false>(a, st)
+// Shapes per rank count, chosen by measurement on GB300 (1.3B-element buffers): consumer warps,
+// elements per thread, stage cap, shared-memory budget (115712 bytes lets two CTAs share an SM).
+#define ZS_TMA(ND_, NCW_, VPT_, MAXST_, BUDGET_)                                                        \
+    return broadcast ? tma_impl<ND_, NCW_, VPT_, true, MAXST_, BUDGET_>(a, st)                          \
+                     : tma_impl<ND_, NCW_, VPT_, false, MAXST_, BUDGET_>(a, st)
     switch (nd) {
-        case 2: ZS_TMA(2, 8, 8);
-        case 4: ZS_TMA(4, 8, 8);
-        case 8: ZS_TMA(8, 8, 8);
-        case 16: ZS_TMA(16, 8, 4);
-        case 32: ZS_TMA(32, 8, 4);
+        case 2: ZS_TMA(2, 8, 8, 4, 232448);     // T 2048, 4 stages, 1 CTA/SM
+        case 4: ZS_TMA(4, 8, 4, 5, 115712);     // T 1024, 5 stages, 2 CTAs/SM
+        case 8: ZS_TMA(8, 4, 8, 8, 232448);     // T 1024, 8 stages, 1 CTA/SM
+        case 16: ZS_TMA(16, 4, 4, 5, 115712);   // T 512, 5 stages, 2 CTAs/SM
+        case 32: ZS_TMA(32, 4, 4, 2, 115712);   // T 512, 2 stages, 2 CTAs/SM
         default: return cudaErrorNotSupported;
     }
 #undef ZS_TMA
