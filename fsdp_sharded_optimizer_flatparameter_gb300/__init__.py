@@ -217,13 +217,18 @@ def _hp(hp):
 
 
 def _addr(x, min_elems=None, elem_size=None, what="buffer", device=True):
-    """Address of a tensor (size-checked) or an integer address (unchecked)."""
+    """Address of a tensor (size-checked) or an integer address (unchecked).
+
+    device=True: a CUDA tensor; "pinned_ok": a CUDA tensor or a pinned host tensor; False: any."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
     if hasattr(x, "data_ptr"):
-        if device and not x.is_cuda:
+        if device == "pinned_ok":
+            if not (x.is_cuda or x.is_pinned()):
+                raise ValueError("%s must be a CUDA tensor or pinned host memory" % what)
+        elif device and not x.is_cuda:
             raise ValueError("%s must be a CUDA tensor" % what)
         if not x.is_contiguous():
             raise ValueError("%s must be contiguous" % what)
@@ -311,10 +316,11 @@ def zs_fused_step(plan, bucket, grads, grads_kind, master, m, v, replicas, hp, s
     _n_ptrs(ZS_RANK_FULL, replicas, plan.n_d, "replicas")
     n = plan.padded
     ng = _bf16_elems(plan, grads_kind, bucket)
+    # gradients and replicas may be pinned host memory (read / written by the kernel over the host link)
     return _check(_lib.zs_fused_step(
-        plan.handle, int(bucket), _ptr_array(grads, ng, 2, "grads"), int(grads_kind),
+        plan.handle, int(bucket), _ptr_array(grads, ng, 2, "grads", "pinned_ok"), int(grads_kind),
         _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
-        _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+        _ptr_array(replicas, n, 2, "replicas", "pinned_ok"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
 
 
 def zs_fused_step_host(plan, host_grads, dev_grads, master, m, v, replicas, hp, step, host_replica0=None,

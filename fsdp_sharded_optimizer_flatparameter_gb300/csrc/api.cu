@@ -97,6 +97,7 @@ int check_bucket(const char* fn, zs_plan_t plan, int32_t bucket, bool allow_all)
 
 Range unit_range(const zs::Unit& u) { return {u.base, u.base + u.padded, u.base, u.shard}; }
 
+
 cudaStream_t as_stream(void* s) { return (cudaStream_t)s; }
 
 #define ZS_TRY(expr)                 \
@@ -234,6 +235,7 @@ static int fused_common(const char* fn, zs_plan_t plan, int32_t bucket, const vo
         r = {0, plan->padded, 0, 1};       // the fused step needs no owner: one pass over the flat space
     }
     if (r.hi <= r.lo) return ZS_OK;
+    // gradients or replicas may be pinned host memory: launch_fused then keeps to the streaming kernel
     return cuda_status(fn, zs::launch_fused(g, master, m, v, o, true, r, s, nd, st));
 }
 

@@ -361,11 +361,36 @@ static cudaError_t launch_fused_ldg(const BView& g, float* master, float* m, flo
     }
 }
 
+// True when every pointer is device memory of this context.  The staged kernel's bulk copies are
+// only ever pointed at device memory; host (pinned, mapped) or unknown pointers take the streaming
+// kernel, whose plain loads and stores reach pinned host memory under unified addressing.
+static bool all_device(const void* const* ps, int n) {
+    for (int i = 0; i < n; ++i) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ps[i]) != cudaSuccess) {
+            cudaGetLastError();                   // unregistered pointer: clear the error, refuse staging
+            return false;
+        }
+        if (at.type != cudaMemoryTypeDevice) return false;
+    }
+    return true;
+}
+
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st, bool allow_staged) {
     const bool vec = aligned8(g.off) && aligned8(out.off);
     const Split sp = split_range(r.lo, r.hi, vec);
-    const bool staged_nd = nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32;
+    bool staged_nd = allow_staged && (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
+    if (staged_nd) {
+        const void* ps[2 * ZS_MAX_RANKS + 3];
+        int n = 0;
+        for (int q = 0; q < nd; ++q) ps[n++] = g.ptr.p[q];
+        for (int q = 0; q < (broadcast ? nd : 1); ++q) ps[n++] = out.ptr.p[q];
+        ps[n++] = master;
+        ps[n++] = m;
+        ps[n++] = v;
+        staged_nd = all_device(ps, n);
+    }
     const bool want_tma = g_fused_variant == ZS_FUSED_TMA ||
                           (g_fused_variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
     if (!(want_tma && staged_nd && sp.nvec > 0)) return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);

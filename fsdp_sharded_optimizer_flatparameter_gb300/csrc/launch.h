@@ -41,8 +41,10 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
                          cudaStream_t st);
 cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
                           const Range& r, int nd, cudaStream_t st);
+// The staged kernel runs only for 8-aligned ranges of supported rank counts whose buffers are all
+// device memory; allow_staged = false forces the register-streaming kernel.
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st);
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st, bool allow_staged = true);
 
 // Bulk-copy staged fused kernel over the 8-aligned body [lo, lo + n); returns
 // cudaErrorNotSupported when no staged variant exists for this rank count.

@@ -244,6 +244,10 @@ int zs_all_gather(zs_plan_t plan, const void* const* src, int32_t src_kind,
  * AdamW on the shard, all-gather into every replica.  Results are bit-identical
  * to zs_reduce_scatter_mean + zs_adamw_shard_step + zs_all_gather (the reduced
  * gradient is rounded to bf16 before the update as there).
+ * Gradient and replica buffers may also be pinned host memory (cudaHostAlloc /
+ * cudaMallocHost, reachable from the device under unified addressing): the kernel
+ * then reads or writes them over the host link directly, with no copy-engine
+ * transfer (the register-streaming kernel is used for such calls).
  *   bucket      -1 = the whole flat space, else one bucket (the update is
  *               element-wise, so a bucket can be stepped as soon as its
  *               gradients are complete).

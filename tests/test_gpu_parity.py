@@ -490,3 +490,33 @@ def test_host_fed_steps_match_device_fused_step(n_d, numel, bucket_bytes):
             for q in range(n_d):
                 assert torch.equal(reps[0][q], reps[k][q])
         assert torch.equal(out1, reps[0][0].cpu()) and torch.equal(out2, reps[0][0].cpu())
+
+
+@pytest.mark.parametrize("variant", [zs.ZS_FUSED_AUTO, zs.ZS_FUSED_TMA])
+def test_fused_step_reads_and_writes_pinned_host_memory(variant):
+    """Gradients in pinned host memory and rank 0's replica in pinned host memory: the kernel
+    reads and writes them over the host link; results equal the all-device step bit for bit
+    (the staged kernel is never used for such calls, whatever variant is selected)."""
+    zs.zs_set_fused_variant(variant)
+    try:
+        plan, _ = _plans([(2_000_003,)], 8)
+        P, pads = plan.padded, plan.pad_ranges()
+        master0 = synth.master_init(P, pads, seed=14, device=DEV)
+        a, b = State(master0), State(master0)
+        reps_a = synth.rank_buffers(8, P, BF16, DEV)[0]
+        reps_b = synth.rank_buffers(8, P, BF16, DEV)[0]
+        host_rep0 = torch.empty(P, dtype=BF16).pin_memory()
+        for t in (1, 2):
+            grads, _ = synth.rank_grads(8, P, pads, seed=14, step=t, sigma=1e-3, device=DEV)
+            host = [g.cpu().pin_memory() for g in grads]
+            zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *a.args(), reps_a, HP, t)
+            zs.zs_fused_step(plan, -1, host, zs.ZS_RANK_FULL, *b.args(), [host_rep0] + reps_b[1:], HP, t)
+            torch.cuda.synchronize()
+            for x, y in zip(a.args(), b.args()):
+                assert torch.equal(x, y)
+            assert torch.equal(host_rep0, reps_a[0].cpu())
+            for q in range(1, 8):
+                assert torch.equal(reps_a[q], reps_b[q])
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
