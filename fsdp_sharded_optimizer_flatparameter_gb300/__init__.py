@@ -85,6 +85,8 @@ _sig("zs_checkpoint_save", [c_vp, ctypes.c_char_p, c_vp, c_vp, c_vp, c_vp, c_i64
 _sig("zs_checkpoint_load", [c_vp, ctypes.c_char_p, c_vp, c_vp, c_vp, c_vp, P_i64, c_vp])
 _sig("zs_zero2_step_host_noalloc", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(zs_adamw_hparams), c_i64,
                                     c_vp, c_vp])
+_sig("zs_all_reduce_mean", [c_vp, c_i32, c_vp, c_vp])
+_sig("zs_dp_step", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
 _sig("zs_set_fused_variant", [c_i32])
 _sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
 _sig("zs_selftest_wait_timeout", [c_i64, c_vp])
@@ -96,7 +98,8 @@ EXPORTED = [
     "zs_reduce_scatter_mean", "zs_adamw_shard_step", "zs_all_gather", "zs_fused_step",
     "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit", "zs_set_fused_variant",
     "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step", "zs_zero2_step_host",
-    "zs_checkpoint_save", "zs_checkpoint_load", "zs_zero2_step_host_noalloc",
+    "zs_checkpoint_save", "zs_checkpoint_load", "zs_zero2_step_host_noalloc", "zs_all_reduce_mean",
+    "zs_dp_step",
 ]
 
 
@@ -424,6 +427,23 @@ def zs_zero2_step_host_noalloc(plan, host_grads, master, m, v, replicas, hp, ste
         plan.handle, _ptr_array(host_grads, n, 2, "host_grads", device=False), _addr(master, n, 4, "master"),
         _addr(m, n, 4, "m"), _addr(v, n, 4, "v"), _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)),
         int(step), _addr(host_replica0, n, 2, "host_replica0", device=False), _stream(stream)))
+
+
+def zs_all_reduce_mean(plan, bucket, grads, stream=None):
+    _n_ptrs(ZS_RANK_FULL, grads, plan.n_d, "grads")
+    return _check(_lib.zs_all_reduce_mean(plan.handle, int(bucket), _ptr_array(grads, plan.padded, 2, "grads"),
+                                          _stream(stream)))
+
+
+def zs_dp_step(plan, grads, master, m, v, replicas, hp, step, stream=None):
+    """master, m, v, replicas: lists of N_d per-rank full buffers (each rank's own copy)."""
+    n, nd = plan.padded, plan.n_d
+    for name, xs in (("grads", grads), ("master", master), ("m", m), ("v", v), ("replicas", replicas)):
+        _n_ptrs(ZS_RANK_FULL, xs, nd, name)
+    return _check(_lib.zs_dp_step(
+        plan.handle, _ptr_array(grads, n, 2, "grads"), _ptr_array(master, n, 4, "master"),
+        _ptr_array(m, n, 4, "m"), _ptr_array(v, n, 4, "v"), _ptr_array(replicas, n, 2, "replicas"),
+        ctypes.byref(_hp(hp)), int(step), _stream(stream)))
 
 
 def zs_set_fused_variant(variant):

@@ -338,3 +338,38 @@ extern "C" int zs_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
     if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 32)) return fail(fn, "limit_cycles out of range");
     return cuda_status(fn, zs::launch_wait_selftest((long long)limit_cycles, as_stream(stream)));
 }
+
+extern "C" int zs_all_reduce_mean(zs_plan_t plan, int32_t bucket, void* const* grads, void* stream) {
+    static const char* fn = "zs_all_reduce_mean";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    ZS_TRY(check_bucket(fn, plan, bucket, true));
+    BView g;
+    ZS_TRY(make_view(fn, "grads", (const void* const*)grads, ZS_RANK_FULL, plan->n_d, 0, 0, &g));
+    Range r = bucket >= 0 ? Range{plan->buckets[bucket].begin, plan->buckets[bucket].end, 0, 1}
+                          : Range{0, plan->padded, 0, 1};
+    if (r.hi <= r.lo) return ZS_OK;
+    return cuda_status(fn, zs::launch_all_reduce_mean(g, r, plan->n_d, as_stream(stream)));
+}
+
+extern "C" int zs_dp_step(zs_plan_t plan, const void* const* grads, float* const* master, float* const* m,
+                          float* const* v, void* const* replicas, const zs_adamw_hparams* hp, int64_t step,
+                          void* stream) {
+    static const char* fn = "zs_dp_step";
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    const int nd = plan->n_d;
+    zs::AdamScalars s;
+    ZS_TRY(check_hp(fn, hp, step, &s));
+    ZS_TRY(check_ptrs(fn, "master", (const void* const*)master, nd));
+    ZS_TRY(check_ptrs(fn, "m", (const void* const*)m, nd));
+    ZS_TRY(check_ptrs(fn, "v", (const void* const*)v, nd));
+    BView g, o;
+    ZS_TRY(make_view(fn, "grads", grads, ZS_RANK_FULL, nd, 0, 0, &g));
+    ZS_TRY(make_view(fn, "replicas", (const void* const*)replicas, ZS_RANK_FULL, nd, 0, 0, &o));
+    for (int q = 0; q < nd; ++q)
+        for (int j = 0; j < nd; ++j)
+            if (replicas[q] == grads[j]) return fail(fn, "replicas must not be the gradient buffers");
+    if (plan->padded == 0) return ZS_OK;
+    return cuda_status(fn, zs::launch_dp_step(g, o, master, m, v, {0, plan->padded, 0, 1}, s, nd, as_stream(stream)));
+}

@@ -407,3 +407,129 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
 }
 
 }  // namespace zs
+
+namespace zs {
+
+// ------------------------------------------------------------------ naive data parallelism
+// "Infra: Data Parallel", section "Naive Data Parallelism": every rank keeps a full replica of
+// parameters, gradients and optimizer state; the gradients are all-reduced to their mean and every
+// rank applies the same update to its own copy.
+
+template <int ND>
+struct AllReduceOp {
+    BView g;
+    int nd;
+    float inv_nd;
+    template <int VEC>
+    __device__ __forceinline__ void run(int64_t i) const {
+        const int n = ND > 0 ? ND : nd;
+        float acc[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            float f[VEC];
+            unpack(ld_bf<VEC>(g.ptr.p[q] + (i - g.off)), f);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = mean_of_sum<ND>(acc[k], n, inv_nd);
+        const BfVec<VEC> w = pack(acc);
+#pragma unroll
+        for (int q = 0; q < n; ++q) st_bf<VEC>(g.ptr.p[q] + (i - g.off), w);
+    }
+};
+
+template <int ND>
+__global__ void __launch_bounds__(kThreads) k_all_reduce_mean(AllReduceOp<ND> op, Split sp) { for_range(sp, op); }
+
+struct FPtrs {
+    float* p[ZS_MAX_RANKS];
+};
+
+template <int ND>
+struct DpStepOp {
+    BView g, out;
+    FPtrs master, m, v;
+    AdamScalars s;
+    int nd;
+    float inv_nd;
+    template <int VEC>
+    __device__ __forceinline__ void run(int64_t i) const {
+        const int n = ND > 0 ? ND : nd;
+        float acc[VEC], gr[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            float f[VEC];
+            unpack(ld_bf<VEC>(g.ptr.p[q] + (i - g.off)), f);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) acc[k] = mean_of_sum<ND>(acc[k], n, inv_nd);
+        unpack(pack(acc), gr);                  // every rank receives the same bf16 mean
+#pragma unroll 1
+        for (int q = 0; q < n; ++q) {           // and runs the same update on its own full state
+            float p[VEC], mm[VEC], vv[VEC];
+            ld_f32<VEC>(master.p[q] + i, p);
+            ld_f32<VEC>(m.p[q] + i, mm);
+            ld_f32<VEC>(v.p[q] + i, vv);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) adamw_elem(gr[k], p[k], mm[k], vv[k], s);
+            st_f32<VEC>(master.p[q] + i, p);
+            st_f32<VEC>(m.p[q] + i, mm);
+            st_f32<VEC>(v.p[q] + i, vv);
+            st_bf<VEC>(out.ptr.p[q] + (i - out.off), pack(p));
+        }
+    }
+};
+
+template <int ND>
+__global__ void __launch_bounds__(kThreads) k_dp_step(DpStepOp<ND> op, Split sp) { for_range(sp, op); }
+
+template <int ND>
+static cudaError_t all_reduce_impl(const BView& g, int nd, Split sp, cudaStream_t st) {
+    AllReduceOp<ND> op{g, nd, 1.0f / (float)nd};
+    const int grid = grid_for((const void*)k_all_reduce_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    k_all_reduce_mean<ND><<<grid, kThreads, 0, st>>>(op, sp);
+    return cudaGetLastError();
+}
+
+template <int ND>
+static cudaError_t dp_step_impl(const BView& g, const BView& out, float* const* master, float* const* m,
+                                float* const* v, const AdamScalars& s, int nd, Split sp, cudaStream_t st) {
+    DpStepOp<ND> op{};
+    op.g = g;
+    op.out = out;
+    for (int q = 0; q < nd; ++q) {
+        op.master.p[q] = master[q];
+        op.m.p[q] = m[q];
+        op.v.p[q] = v[q];
+    }
+    op.s = s;
+    op.nd = nd;
+    op.inv_nd = 1.0f / (float)nd;
+    const int grid = grid_for((const void*)k_dp_step<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    k_dp_step<ND><<<grid, kThreads, 0, st>>>(op, sp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st) {
+    const Split sp = split_range(r.lo, r.hi, aligned8(g.off));
+#define ZS_AR(N) all_reduce_impl<N>(g, nd, sp, st)
+    ZS_DISPATCH_ND(nd, ZS_AR)
+#undef ZS_AR
+}
+
+cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,
+                           const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
+    const Split sp = split_range(r.lo, r.hi, aligned8(g.off) && aligned8(out.off));
+#define ZS_DP(N) dp_step_impl<N>(g, out, master, m, v, s, nd, sp, st)
+    ZS_DISPATCH_ND(nd, ZS_DP)
+#undef ZS_DP
+}
+
+}  // namespace zs

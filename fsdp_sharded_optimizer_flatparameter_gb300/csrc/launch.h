@@ -51,6 +51,9 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                              int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
+cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);
+cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,
+                           const Range& r, const AdamScalars& s, int nd, cudaStream_t st);
 cudaError_t read_device_error(unsigned int* out, bool clear);
 
 // Which fused kernel zs_fused_step / zs_zero3_rs_step_unit use (ZS_FUSED_*).

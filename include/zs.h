@@ -240,6 +240,23 @@ int zs_adamw_shard_step(zs_plan_t plan, int32_t rank, const void* const* grad, i
 int zs_all_gather(zs_plan_t plan, const void* const* src, int32_t src_kind,
                   void* const* replicas, void* stream);
 
+/* Naive data parallelism ("Infra: Data Parallel", section "Naive Data
+ * Parallelism": every rank keeps a full replica of parameters, gradients and
+ * optimizer state, all-reduces the gradients to their mean and applies the same
+ * update; per-rank model-state memory 16 bytes per parameter, ~4 Psi bytes sent).
+ * zs_all_reduce_mean: in place, every rank's buffer (ZS_RANK_FULL) gets
+ *   bf16((sum over q ascending of fp32 grads[q][i]) / N_d) for every element of
+ *   bucket `bucket` (-1: all).
+ * zs_dp_step: the all-reduce and each rank's full AdamW in one pass: master, m,
+ *   v are N_d full fp32 arrays (one per rank, padded_numel elements each, the
+ *   rank's own replicated state); replicas[q] receives bf16 of rank q's master.
+ *   Same arithmetic as zs_fused_step; every rank's copy ends bit-identical.
+ * Errors: ZS_ERR_INVALID (before anything is enqueued), ZS_ERR_CUDA. */
+int zs_all_reduce_mean(zs_plan_t plan, int32_t bucket, void* const* grads, void* stream);
+int zs_dp_step(zs_plan_t plan, const void* const* grads, float* const* master, float* const* m,
+               float* const* v, void* const* replicas, const zs_adamw_hparams* hp, int64_t step,
+               void* stream);
+
 /* The three steps above in one pass over HBM: reduce-scatter with averaging,
  * AdamW on the shard, all-gather into every replica.  Results are bit-identical
  * to zs_reduce_scatter_mean + zs_adamw_shard_step + zs_all_gather (the reduced

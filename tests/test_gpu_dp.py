@@ -1,0 +1,66 @@
+"""Naive data parallelism on the GPU: all-reduce with averaging and the replicated update.
+
+Against the oracle's naive-DP step, and the method's central identity: the
+sharded ZeRO step gives every rank the same parameters as naive DP, bit for bit.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+import gpu_helpers as H
+from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+from oracle import layout, steps
+
+pytestmark = pytest.mark.gpu
+
+HP = synth.HPARAMS
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+
+@pytest.mark.parametrize("n_d,numel,bucket_bytes", [(1, 1000, 0), (3, 70_001, 0), (4, 262_912, 4096), (8, 500_007, 0)])
+def test_all_reduce_mean(n_d, numel, bucket_bytes):
+    plan = zs.Plan([(numel,)], n_d, stage=0, bucket_bytes=bucket_bytes)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads, _ = synth.rank_grads(n_d, P, pads, seed=50, step=1, sigma=1e-3, outlier_p=0.01, device=DEV)
+    want = steps.reduce_mean([H.to_np_bf16(g) for g in grads])
+    if plan.n_buckets > 1:
+        for b in range(plan.n_buckets):
+            zs.zs_all_reduce_mean(plan, b, grads)
+    else:
+        zs.zs_all_reduce_mean(plan, -1, grads)
+    torch.cuda.synchronize()
+    for q in range(n_d):
+        H.check_bf16(H.to_np_bf16(grads[q]), want, "rank %d" % q)
+
+
+@pytest.mark.parametrize("n_d", [1, 3, 4, 8])
+def test_dp_step_matches_oracle_and_zero(n_d):
+    shapes = [(300, 96), (96,), (257, 96), (5,)]
+    plan = zs.Plan(shapes, n_d, stage=0)
+    ref = layout.make_plan(shapes, n_d)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=51, device=DEV)
+    dp_master = [master0.clone() for _ in range(n_d)]
+    dp_m = [torch.zeros_like(master0) for _ in range(n_d)]
+    dp_v = [torch.zeros_like(master0) for _ in range(n_d)]
+    dp_reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    z_master, z_m, z_v = master0.clone(), torch.zeros_like(master0), torch.zeros_like(master0)
+    z_reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    om, omm, ov = H.to_np_f32(master0), np.zeros(P, np.float32), np.zeros(P, np.float32)
+    for t in (1, 2, 3):
+        grads, _ = synth.rank_grads(n_d, P, pads, seed=52, step=t, sigma=1e-3, device=DEV)
+        reps_ref, om, omm, ov = steps.dp_step([H.to_np_bf16(g) for g in grads], om, omm, ov, HP, t)
+        zs.zs_dp_step(plan, grads, dp_master, dp_m, dp_v, dp_reps, HP, t)
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, z_master, z_m, z_v, z_reps, HP, t)
+        torch.cuda.synchronize()
+        for q in range(n_d):
+            H.check_f32(H.to_np_f32(dp_master[q]), om, "dp master rank %d t=%d" % (q, t))
+            H.check_f32(H.to_np_f32(dp_v[q]), ov, "dp v rank %d t=%d" % (q, t))
+            H.check_bf16(H.to_np_bf16(dp_reps[q]), reps_ref[q], "dp replica %d t=%d" % (q, t))
+            # sharded ZeRO == naive DP
+            assert torch.equal(z_reps[q], dp_reps[q])
+        assert torch.equal(z_master, dp_master[0]) and torch.equal(z_m, dp_m[0]) and torch.equal(z_v, dp_v[0])
+    assert plan.memory_bytes(0) == 16 * plan.numel
