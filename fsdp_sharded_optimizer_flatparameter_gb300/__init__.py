@@ -29,6 +29,7 @@ ZS_STAGE_DP, ZS_STAGE_ZERO1, ZS_STAGE_ZERO2, ZS_STAGE_ZERO3 = 0, 1, 2, 3
 ZS_RANK_FULL, ZS_SHARDED, ZS_RANK_BUCKET, ZS_RANK_UNIT = 0, 1, 2, 3
 ZS_MAX_RANKS = 64
 ZS_FUSED_AUTO, ZS_FUSED_LDG, ZS_FUSED_TMA = 0, 1, 2
+ZS_LAYOUT_FSDP1, ZS_LAYOUT_FSDP2 = 0, 1
 ZS_DEVERR_NONE, ZS_DEVERR_PRODUCER_WAIT, ZS_DEVERR_CONSUMER_WAIT, ZS_DEVERR_SELFTEST = 0, 1, 2, 3
 
 c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
@@ -55,6 +56,12 @@ def _sig(name, args, res=c_i32):
 
 _sig("zs_plan_create", [c_i32, P_i32, P_i64, P_i32, c_i32, c_i32, c_i64, ctypes.POINTER(c_vp)])
 _sig("zs_plan_destroy", [c_vp], None)
+_sig("zs_plan_create_fsdp2", [c_i32, P_i32, P_i64, P_i32, c_i32, c_i32, c_i64, ctypes.POINTER(c_vp)])
+_sig("zs_plan_layout", [c_vp, P_i32])
+_sig("zs_plan_param_rows", [c_vp, c_i32, c_i32, P_i64, P_i64, P_i64, P_i64])
+_sig("zs_plan_pad_ranges", [c_vp, P_i64, P_i64, c_i64, P_i64])
+_sig("zs_fsdp2_chunk_cat", [c_vp, c_i32, c_vp, c_vp, c_vp])
+_sig("zs_fsdp2_copy_out", [c_vp, c_i32, c_vp, c_vp, c_vp])
 _sig("zs_plan_info", [c_vp, P_i64, P_i64, P_i64, P_i32, P_i32, P_i32, P_i32])
 _sig("zs_plan_unit", [c_vp, c_i32, P_i64, P_i64, P_i64, P_i64])
 _sig("zs_plan_bucket", [c_vp, c_i32, P_i32, P_i64, P_i64])
@@ -99,7 +106,8 @@ EXPORTED = [
     "zs_fused_step_host", "zs_zero3_gather_unit", "zs_zero3_rs_step_unit", "zs_set_fused_variant",
     "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step", "zs_zero2_step_host",
     "zs_checkpoint_save", "zs_checkpoint_load", "zs_zero2_step_host_noalloc", "zs_all_reduce_mean",
-    "zs_dp_step",
+    "zs_dp_step", "zs_plan_create_fsdp2", "zs_plan_layout", "zs_plan_param_rows", "zs_plan_pad_ranges",
+    "zs_fsdp2_chunk_cat", "zs_fsdp2_copy_out",
 ]
 
 
@@ -118,8 +126,9 @@ def zs_last_error():
 class Plan:
     """Owns a zs_plan_t.  Queries return plain Python integers."""
 
-    def __init__(self, shapes, n_d, stage=ZS_STAGE_ZERO1, bucket_bytes=0, unit_of_param=None):
+    def __init__(self, shapes, n_d, stage=ZS_STAGE_ZERO1, bucket_bytes=0, unit_of_param=None, layout=ZS_LAYOUT_FSDP1):
         self._h = None
+        self.shapes = [tuple(int(d) for d in s) for s in shapes]
         shapes = [tuple(int(d) for d in s) for s in shapes]
         n = len(shapes)
         ndims = (c_i32 * max(n, 1))(*[len(s) for s in shapes])
@@ -129,7 +138,8 @@ class Plan:
         if unit_of_param is not None:
             units = (c_i32 * max(n, 1))(*[int(u) for u in unit_of_param])
         h = c_vp()
-        _check(_lib.zs_plan_create(n, ndims, dims, units, int(n_d), int(stage), int(bucket_bytes), ctypes.byref(h)))
+        create = _lib.zs_plan_create_fsdp2 if layout == ZS_LAYOUT_FSDP2 else _lib.zs_plan_create
+        _check(create(n, ndims, dims, units, int(n_d), int(stage), int(bucket_bytes), ctypes.byref(h)))
         self._h = h
         info = self.info()
         self.numel, self.padded, self.shard_per_rank = info["numel"], info["padded"], info["shard_per_rank"]
@@ -195,13 +205,23 @@ class Plan:
                                        1 if reshard_after_forward else 0, ctypes.byref(out)))
         return out.value
 
+    def layout(self):
+        out = c_i32()
+        _check(_lib.zs_plan_layout(self._h, ctypes.byref(out)))
+        return out.value
+
+    def param_rows(self, k, rank):
+        a, b, c, d = c_i64(), c_i64(), c_i64(), c_i64()
+        _check(_lib.zs_plan_param_rows(self._h, int(k), int(rank), *(ctypes.byref(x) for x in (a, b, c, d))))
+        return {"row_begin": a.value, "nrows": b.value, "rows_per_rank": c.value, "row_elems": d.value}
+
     def pad_ranges(self):
-        out = []
-        for u in range(self.n_units):
-            d = self.unit(u)
-            if d["padded"] > d["numel"]:
-                out.append((d["base"] + d["numel"], d["base"] + d["padded"]))
-        return out
+        count = c_i64()
+        _check(_lib.zs_plan_pad_ranges(self._h, None, None, 0, ctypes.byref(count)))
+        n = count.value
+        begins, ends = (c_i64 * max(n, 1))(), (c_i64 * max(n, 1))()
+        _check(_lib.zs_plan_pad_ranges(self._h, begins, ends, n, ctypes.byref(count)))
+        return [(begins[i], ends[i]) for i in range(n)]
 
 
 def zs_adamw_scalars(hp, step):
@@ -444,6 +464,29 @@ def zs_dp_step(plan, grads, master, m, v, replicas, hp, step, stream=None):
         plan.handle, _ptr_array(grads, n, 2, "grads"), _ptr_array(master, n, 4, "master"),
         _ptr_array(m, n, 4, "m"), _ptr_array(v, n, 4, "v"), _ptr_array(replicas, n, 2, "replicas"),
         ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+def _unit_params(plan, unit):
+    return [k for k in range(len(plan.shapes)) if plan.param(k)[0] == unit]
+
+
+def zs_fsdp2_chunk_cat(plan, unit, params, flat, stream=None):
+    """params: the unit's parameters (bf16 tensors in their own layout), in order; flat: padded_u elements."""
+    members = _unit_params(plan, unit)
+    if len(params) != len(members):
+        raise ValueError("expected %d parameters for unit %d" % (len(members), unit))
+    ptrs = [_addr(x, plan.param(k)[2], 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
+    return _check(_lib.zs_fsdp2_chunk_cat(plan.handle, int(unit), (c_vp * max(len(ptrs), 1))(*ptrs),
+                                          _addr(flat, plan.unit(unit)["padded"], 2, "flat"), _stream(stream)))
+
+
+def zs_fsdp2_copy_out(plan, unit, flat, params, stream=None):
+    members = _unit_params(plan, unit)
+    if len(params) != len(members):
+        raise ValueError("expected %d parameters for unit %d" % (len(members), unit))
+    ptrs = [_addr(x, plan.param(k)[2], 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
+    return _check(_lib.zs_fsdp2_copy_out(plan.handle, int(unit), _addr(flat, plan.unit(unit)["padded"], 2, "flat"),
+                                         (c_vp * max(len(ptrs), 1))(*ptrs), _stream(stream)))
 
 
 def zs_set_fused_variant(variant):

@@ -56,6 +56,7 @@ extern "C" int zs_checkpoint_save(zs_plan_t plan, const char* dir, const void* s
     static const char* fn = "zs_checkpoint_save";
     zs::clear_error();
     if (!plan || !dir || !shards || !master || !m || !v) return fail(fn, "NULL argument");
+    if (plan->layout != ZS_LAYOUT_FSDP1) return fail(fn, "only FSDP1-layout plans are supported", ZS_ERR_UNSUPPORTED);
     cudaStream_t st = (cudaStream_t)stream;
     const std::string d(dir);
     {
@@ -109,6 +110,7 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
     static const char* fn = "zs_checkpoint_load";
     zs::clear_error();
     if (!plan || !dir || !shards || !master || !m || !v) return fail(fn, "NULL argument");
+    if (plan->layout != ZS_LAYOUT_FSDP1) return fail(fn, "only FSDP1-layout plans are supported", ZS_ERR_UNSUPPORTED);
     cudaStream_t st = (cudaStream_t)stream;
     const std::string d(dir);
 

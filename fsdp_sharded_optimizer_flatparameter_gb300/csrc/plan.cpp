@@ -10,6 +10,7 @@
 // Accounting: section "Zero Redundancy Optimizer (ZeRO)", memory figure
 // (bytes of model states one GPU holds, k = 12) and communication paragraphs
 // (bytes one rank sends per step, 16-bit elements).
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -29,9 +30,8 @@ using zs::set_error;
 
 extern "C" const char* zs_last_error(void) { return zs::g_last_error.c_str(); }
 
-extern "C" int zs_plan_create(int32_t n_params, const int32_t* ndims, const int64_t* dims,
-                              const int32_t* unit_of_param, int32_t n_d, int32_t stage,
-                              int64_t bucket_bytes, zs_plan_t* out) {
+static int plan_create(int32_t n_params, const int32_t* ndims, const int64_t* dims, const int32_t* unit_of_param,
+                       int32_t n_d, int32_t stage, int64_t bucket_bytes, int32_t layout, zs_plan_t* out) {
     zs::clear_error();
     if (!out) { set_error("zs_plan_create: out is NULL"); return ZS_ERR_INVALID; }
     *out = nullptr;
@@ -45,7 +45,12 @@ extern "C" int zs_plan_create(int32_t n_params, const int32_t* ndims, const int6
     try {
         p->n_d = n_d;
         p->stage = stage;
+        p->layout = layout;
         p->param_numel.resize(n_params);
+        p->param_d0.assign(n_params, 1);
+        p->param_row.assign(n_params, 1);
+        p->param_chunk.assign(n_params, 1);
+        p->param_piece_off.assign(n_params, 0);
         p->param_offset.resize(n_params);
         p->param_unit.resize(n_params);
 
@@ -58,8 +63,11 @@ extern "C" int zs_plan_create(int32_t n_params, const int32_t* ndims, const int6
                 if (dims[d] < 1) { set_error("zs_plan_create: every dimension must be >= 1"); delete p; return ZS_ERR_INVALID; }
                 if (n > (int64_t(1) << 50) / dims[d]) { set_error("zs_plan_create: parameter too large"); delete p; return ZS_ERR_INVALID; }
                 n *= dims[d];
+                if (j == 0) p->param_d0[k] = dims[d];
             }
             p->param_numel[k] = n;
+            p->param_row[k] = n / p->param_d0[k];       // a 0-d parameter is one row of one element
+            p->param_chunk[k] = (p->param_d0[k] + n_d - 1) / n_d;
         }
 
         // units
@@ -80,19 +88,31 @@ extern "C" int zs_plan_create(int32_t n_params, const int32_t* ndims, const int6
         }
         int64_t base = 0;
         for (int32_t u = 0; u < n_units; ++u) {
-            int64_t off = base;
+            int64_t off = base, piece = 0;
             for (int32_t k = 0; k < n_params; ++k) {
                 int32_t ku = unit_of_param ? unit_of_param[k] : 0;
                 if (ku != u) continue;
                 p->param_unit[k] = u;
-                p->param_offset[k] = off;
+                if (layout == ZS_LAYOUT_FSDP2) {
+                    // each parameter cut along dim 0: its rank-r piece sits at base + r*S + piece
+                    p->param_piece_off[k] = piece;
+                    p->param_offset[k] = base + piece;
+                    piece += p->param_chunk[k] * p->param_row[k];
+                } else {
+                    p->param_offset[k] = off;
+                }
                 off += p->param_numel[k];
             }
             zs::Unit un;
             un.base = base;
             un.numel = off - base;
-            un.padded = ((un.numel + n_d - 1) / n_d) * n_d;
-            un.shard = un.padded / n_d;
+            if (layout == ZS_LAYOUT_FSDP2) {
+                un.shard = piece;
+                un.padded = piece * n_d;
+            } else {
+                un.padded = ((un.numel + n_d - 1) / n_d) * n_d;
+                un.shard = un.padded / n_d;
+            }
             p->units.push_back(un);
             p->numel += un.numel;
             p->shard_per_rank += un.shard;
@@ -119,6 +139,41 @@ extern "C" int zs_plan_create(int32_t n_params, const int32_t* ndims, const int6
         return ZS_ERR_OOM_HOST;
     }
     *out = p;
+    return ZS_OK;
+}
+
+extern "C" int zs_plan_create(int32_t n_params, const int32_t* ndims, const int64_t* dims,
+                              const int32_t* unit_of_param, int32_t n_d, int32_t stage,
+                              int64_t bucket_bytes, zs_plan_t* out) {
+    return plan_create(n_params, ndims, dims, unit_of_param, n_d, stage, bucket_bytes, ZS_LAYOUT_FSDP1, out);
+}
+
+extern "C" int zs_plan_create_fsdp2(int32_t n_params, const int32_t* ndims, const int64_t* dims,
+                                    const int32_t* unit_of_param, int32_t n_d, int32_t stage,
+                                    int64_t bucket_bytes, zs_plan_t* out) {
+    return plan_create(n_params, ndims, dims, unit_of_param, n_d, stage, bucket_bytes, ZS_LAYOUT_FSDP2, out);
+}
+
+extern "C" int zs_plan_layout(zs_plan_t p, int32_t* layout) {
+    zs::clear_error();
+    if (!p || !layout) { set_error("zs_plan_layout: NULL argument"); return ZS_ERR_INVALID; }
+    *layout = p->layout;
+    return ZS_OK;
+}
+
+extern "C" int zs_plan_param_rows(zs_plan_t p, int32_t k, int32_t rank, int64_t* row_begin, int64_t* nrows,
+                                  int64_t* rows_per_rank, int64_t* row_elems) {
+    zs::clear_error();
+    if (!p || k < 0 || k >= (int32_t)p->param_numel.size() || rank < 0 || rank >= p->n_d) {
+        set_error("zs_plan_param_rows: bad plan, parameter or rank");
+        return ZS_ERR_INVALID;
+    }
+    const int64_t c = p->param_chunk[k], d0 = p->param_d0[k];
+    const int64_t b = std::min<int64_t>((int64_t)rank * c, d0), e = std::min<int64_t>(((int64_t)rank + 1) * c, d0);
+    if (row_begin) *row_begin = b;
+    if (nrows) *nrows = e - b;
+    if (rows_per_rank) *rows_per_rank = c;
+    if (row_elems) *row_elems = p->param_row[k];
     return ZS_OK;
 }
 
@@ -194,6 +249,16 @@ extern "C" int zs_plan_param_segment(zs_plan_t p, int32_t k, int32_t rank, int64
         return ZS_ERR_INVALID;
     }
     const auto& un = p->units[p->param_unit[k]];
+    if (p->layout == ZS_LAYOUT_FSDP2) {
+        // rank r's piece: rows [r*c, min((r+1)*c, d0)) at base + r*S + piece offset
+        const int64_t c = p->param_chunk[k], d0 = p->param_d0[k];
+        const int64_t b = std::min<int64_t>((int64_t)rank * c, d0), e = std::min<int64_t>(((int64_t)rank + 1) * c, d0);
+        const int64_t n = (e - b) * p->param_row[k];
+        if (flat_begin) *flat_begin = n ? un.base + (int64_t)rank * un.shard + p->param_piece_off[k] : 0;
+        if (shard_offset) *shard_offset = n ? p->param_piece_off[k] : 0;
+        if (len) *len = n;
+        return ZS_OK;
+    }
     int64_t lo = p->param_offset[k], hi = lo + p->param_numel[k];
     int64_t s_lo = un.base + (int64_t)rank * un.shard, s_hi = s_lo + un.shard;
     int64_t a = lo > s_lo ? lo : s_lo;
@@ -253,5 +318,40 @@ extern "C" int zs_adamw_scalars(const zs_adamw_hparams* hp, int64_t step, float*
     out8[5] = (float)(1.0 - b2);
     out8[6] = (float)(lr / (1.0 - std::pow(b1, (double)step)));
     out8[7] = (float)std::sqrt(1.0 - std::pow(b2, (double)step));
+    return ZS_OK;
+}
+
+extern "C" int zs_plan_pad_ranges(zs_plan_t p, int64_t* begins, int64_t* ends, int64_t capacity, int64_t* count) {
+    zs::clear_error();
+    if (!p || !count || capacity < 0 || (capacity > 0 && (!begins || !ends))) {
+        set_error("zs_plan_pad_ranges: bad argument");
+        return ZS_ERR_INVALID;
+    }
+    int64_t n = 0;
+    auto emit = [&](int64_t b, int64_t e) {
+        if (e <= b) return;
+        if (n < capacity) {
+            begins[n] = b;
+            ends[n] = e;
+        }
+        ++n;
+    };
+    for (size_t u = 0; u < p->units.size(); ++u) {
+        const auto& un = p->units[u];
+        if (p->layout != ZS_LAYOUT_FSDP2) {
+            emit(un.base + un.numel, un.base + un.padded);
+            continue;
+        }
+        for (int32_t r = 0; r < p->n_d; ++r) {
+            for (size_t k = 0; k < p->param_numel.size(); ++k) {
+                if (p->param_unit[k] != (int32_t)u) continue;
+                const int64_t c = p->param_chunk[k], d0 = p->param_d0[k], row = p->param_row[k];
+                const int64_t b = std::min<int64_t>((int64_t)r * c, d0), e = std::min<int64_t>(((int64_t)r + 1) * c, d0);
+                const int64_t start = un.base + (int64_t)r * un.shard + p->param_piece_off[k];
+                emit(start + (e - b) * row, start + c * row);
+            }
+        }
+    }
+    *count = n;
     return ZS_OK;
 }

@@ -33,6 +33,7 @@ struct Bucket {
 struct zs_plan_s {
     int32_t n_d = 0;
     int32_t stage = 0;
+    int32_t layout = 0;                         // ZS_LAYOUT_FSDP1 or ZS_LAYOUT_FSDP2
     int64_t bucket_elems = 0;
     int64_t numel = 0;
     int64_t padded = 0;
@@ -40,6 +41,8 @@ struct zs_plan_s {
     std::vector<int64_t> param_numel;
     std::vector<int64_t> param_offset;          // global flat index of the first element
     std::vector<int32_t> param_unit;
+    // FSDP2 only: dim-0 rows, elements per row, rows per rank, offset of the piece in a rank's shard
+    std::vector<int64_t> param_d0, param_row, param_chunk, param_piece_off;
     std::vector<zs::Unit> units;
     std::vector<zs::Bucket> buckets;
 };

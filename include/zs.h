@@ -81,6 +81,9 @@ extern "C" {
 
 #define ZS_MAX_RANKS    64        /* largest N_d accepted                            */
 
+#define ZS_LAYOUT_FSDP1 0         /* FlatParameter: units flattened, padded, cut evenly   */
+#define ZS_LAYOUT_FSDP2 1         /* per-parameter Shard(0), rank-major group buffer      */
+
 #define ZS_FUSED_AUTO   0         /* staged kernel for large 8-aligned ranges, else streaming */
 #define ZS_FUSED_LDG    1         /* register-streaming kernel (16-byte loads/stores)   */
 #define ZS_FUSED_TMA    2         /* bulk-copy staged kernel wherever it applies       */
@@ -124,6 +127,39 @@ int zs_plan_create(int32_t n_params, const int32_t* ndims, const int64_t* dims,
                    const int32_t* unit_of_param, int32_t n_d, int32_t stage,
                    int64_t bucket_bytes, zs_plan_t* out);
 void zs_plan_destroy(zs_plan_t plan);
+
+/* Same arguments as zs_plan_create, FSDP2 layout ("Infra: Data Parallel", FSDP
+ * section, FSDP2 layout figure and subsection "FSDP2": every parameter keeps its
+ * global shape and is cut along dimension 0; a group's parameters are still
+ * gathered and reduce-scattered together).  Parameter k (d0 rows of `row`
+ * elements; a 0-d parameter is one row of one element) gives rank r the rows
+ * [r*c_k, min((r+1)*c_k, d0)), c_k = ceil(d0 / N_d).  Rank r's shard of a unit is
+ * its pieces of the unit's parameters in order, each padded with zero rows to c_k
+ * rows, so S_u = sum of c_k * row_k and the unit's flat range is the N_d shards one
+ * after another (padded_u = N_d * S_u).  Every other call of this header works on
+ * such a plan unchanged (the step is element-wise); zs_fsdp2_chunk_cat and
+ * zs_fsdp2_copy_out convert to and from the parameters' own layout.  For an FSDP2
+ * plan zs_plan_param's flat_offset is rank 0's piece; zs_plan_param_segment gives
+ * each rank's piece (real rows only).  Errors as zs_plan_create. */
+int zs_plan_create_fsdp2(int32_t n_params, const int32_t* ndims, const int64_t* dims,
+                         const int32_t* unit_of_param, int32_t n_d, int32_t stage,
+                         int64_t bucket_bytes, zs_plan_t* out);
+
+/* ZS_LAYOUT_FSDP1 or ZS_LAYOUT_FSDP2. */
+int zs_plan_layout(zs_plan_t plan, int32_t* layout);
+
+/* Dimension-0 split of parameter k on rank r (FSDP2 subsection: local shape =
+ * (nrows, rest of the global shape)): first row, number of rows (0 when the rank
+ * holds none), rows per rank c_k, elements per row.  Valid for both layouts (the
+ * FSDP1 layout does not use it). */
+int zs_plan_param_rows(zs_plan_t plan, int32_t k, int32_t rank, int64_t* row_begin, int64_t* nrows,
+                       int64_t* rows_per_rank, int64_t* row_elems);
+
+/* Global flat ranges [begin, end) that hold padding (zeros in every buffer), in
+ * increasing order: the tail of each unit for FSDP1, the padding rows of every
+ * rank's piece for FSDP2.  Writes at most `capacity` ranges and sets *count to the
+ * total number (call with capacity 0 to size the arrays). */
+int zs_plan_pad_ranges(zs_plan_t plan, int64_t* begins, int64_t* ends, int64_t capacity, int64_t* count);
 
 /* Totals.  Any output pointer may be NULL. */
 int zs_plan_info(zs_plan_t plan, int64_t* numel, int64_t* padded_numel,
@@ -240,6 +276,21 @@ int zs_adamw_shard_step(zs_plan_t plan, int32_t rank, const void* const* grad, i
 int zs_all_gather(zs_plan_t plan, const void* const* src, int32_t src_kind,
                   void* const* replicas, void* stream);
 
+/* FSDP2 layout conversions for one unit of an FSDP2 plan (see
+ * zs_plan_create_fsdp2).  `params` holds one pointer per parameter of the unit,
+ * in parameter order, each the parameter in its own (row-major, natural) layout
+ * as bf16; `flat` is the unit's flat buffer of padded_u bf16 elements (rank-major,
+ * e.g. a ZS_RANK_UNIT buffer, or a ZS_RANK_FULL buffer advanced to the unit's base).
+ * zs_fsdp2_chunk_cat: params -> flat, padding rows written as zeros (building one
+ *   rank's reduce-scatter input from its gradients).
+ * zs_fsdp2_copy_out: flat -> params (after a gather: each rank's rows back into the
+ *   full parameters).
+ * Pointers must be 2-byte aligned; runs that share their 16-byte phase move 16
+ * bytes per access.  Errors: ZS_ERR_INVALID (not an FSDP2 plan, bad unit, NULL or
+ * misaligned pointer; nothing enqueued), ZS_ERR_CUDA. */
+int zs_fsdp2_chunk_cat(zs_plan_t plan, int32_t unit, const void* const* params, void* flat, void* stream);
+int zs_fsdp2_copy_out(zs_plan_t plan, int32_t unit, const void* flat, void* const* params, void* stream);
+
 /* Naive data parallelism ("Infra: Data Parallel", section "Naive Data
  * Parallelism": every rank keeps a full replica of parameters, gradients and
  * optimizer state, all-reduces the gradients to their mean and applies the same
@@ -317,6 +368,7 @@ int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads
  * `dir` must exist.  Arrays are ZS_SHARDED device arrays of plan's padded_numel
  * elements.  Both calls copy through a 64 MiB host buffer with cudaMemcpyAsync on
  * `stream` and synchronise it (they return after the data is in place).
+ * Plans with the FSDP2 layout are not supported (ZS_ERR_UNSUPPORTED).
  * Errors: ZS_ERR_INVALID (NULL argument, I/O failure, a checkpoint of another
  * model or a malformed one: nothing is written to the device before the metadata
  * and file sizes are checked), ZS_ERR_CUDA. */
