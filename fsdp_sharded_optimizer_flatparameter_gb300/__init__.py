@@ -31,6 +31,7 @@ ZS_MAX_RANKS = 64
 ZS_FUSED_AUTO, ZS_FUSED_LDG, ZS_FUSED_TMA = 0, 1, 2
 ZS_LAYOUT_FSDP1, ZS_LAYOUT_FSDP2 = 0, 1
 ZS_DEVERR_NONE, ZS_DEVERR_PRODUCER_WAIT, ZS_DEVERR_CONSUMER_WAIT, ZS_DEVERR_SELFTEST = 0, 1, 2, 3
+ZS_DEVERR_GATHER_WAIT = 4
 
 c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 P_i64 = ctypes.POINTER(c_i64)

@@ -330,12 +330,35 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
     return cudaGetLastError();
 }
 
+static bool all_device(const void* const* ps, int n);
+constexpr int64_t kBulkGatherMinElems = int64_t(1) << 20;
+
 cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
                           const Range& r, int nd, cudaStream_t st) {
     const bool by_owner = src_by_owner || skip_owner;
     const bool vec = aligned8(src.off) && aligned8(dst.off) &&
                      (!by_owner || (aligned8(r.base) && aligned8(r.shard)));
     const Split sp = split_range(r.lo, r.hi, vec);
+    // one source for every destination: the bulk-store kernel moves the 8-aligned body
+    if (!by_owner && (sp.nvec << 3) >= kBulkGatherMinElems) {
+        const void* ps[ZS_MAX_RANKS + 1];
+        ps[0] = src.ptr.p[0];
+        for (int q = 0; q < nd; ++q) ps[q + 1] = dst.ptr.p[q];
+        if (all_device(ps, nd + 1)) {
+            const int64_t body_hi = sp.vlo + (sp.nvec << 3);
+            cudaError_t e = launch_gather_bulk(src.ptr.p[0], src.off, dst.ptr, dst.off, sp.vlo, sp.nvec << 3, nd, st);
+            if (e != cudaSuccess) return e;
+            Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
+            for (const Split& f : rest) {
+                if (f.hi <= f.lo) continue;
+#define ZS_GF(N) gather_impl<N>(src, false, dst, false, r, nd, f, st)
+                e = [&]() -> cudaError_t { ZS_DISPATCH_ND(nd, ZS_GF) }();
+#undef ZS_GF
+                if (e != cudaSuccess) return e;
+            }
+            return cudaSuccess;
+        }
+    }
 #define ZS_GA(N) gather_impl<N>(src, src_by_owner, dst, skip_owner, r, nd, sp, st)
     ZS_DISPATCH_ND(nd, ZS_GA)
 #undef ZS_GA

@@ -81,6 +81,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 __device__ __forceinline__ void flag_error(unsigned int code) { atomicCAS(&g_zs_device_error, 0u, code); }
 
+// One-dimensional bulk copy shared -> global, tracked in this thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(su32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's committed bulk stores have finished reading shared memory / have completed.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // VPT consecutive bf16 values from shared memory as fp32.
 template <int VPT>
 __device__ __forceinline__ void lds_bf(const uint16_t* p, float (&f)[VPT]) {
@@ -269,6 +279,81 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
     }
 }
 
+// ------------------------------------------------------------------ gather with bulk stores
+// One source, N_d destinations (the all-gather from shards and the ZeRO-3 unit gather:
+// "Infra: Data Parallel", ZeRO section).  Each CTA is one warp with a ring of S shared-memory
+// stages of T bf16 elements: lane 0 loads a tile with one bulk copy, then lanes 0..31 issue the
+// N_d bulk stores of that tile (shared -> each destination) in parallel; a stage is refilled once
+// every lane's stores have read it.  Many small CTAs per SM keep many store streams in flight,
+// which is what a write-heavy (1 read : N_d writes) stream needs.
+
+struct GatherBulkArgs {
+    const uint16_t* src;
+    int64_t src_off;      // element i of the source at src + (i - src_off)
+    Ptrs dst;
+    int64_t dst_off;      // element i of destination q at dst.p[q] + (i - dst_off)
+    int64_t lo, n;        // body [lo, lo + n): multiples of 8, and lo - src_off, lo - dst_off too
+    int nd;
+    int T;                // elements per tile (multiple of 8)
+    long long wait_limit, drain_limit;
+};
+
+template <int S>
+__global__ void __launch_bounds__(32) k_gather_bulk(const __grid_constant__ GatherBulkArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    uint16_t* buf = reinterpret_cast<uint16_t*>(smem + 128);
+    const int lane = threadIdx.x;
+    const int T = a.T;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const int64_t ntiles = (a.n + T - 1) / T;
+    auto tile_len = [&](int64_t tl) -> uint32_t {
+        const int64_t rem = a.n - tl * T;
+        return (uint32_t)(rem < T ? rem : T);
+    };
+    auto load = [&](int64_t tl, int64_t j) {             // lane 0 only
+        const int s = (int)(j % S);
+        const uint32_t len = tile_len(tl);
+        mbar_expect_tx(&bar[s], len * 2u);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         su32(buf + (size_t)s * T)),
+                     "l"(a.src + (a.lo + tl * T - a.src_off)), "r"(len * 2u), "r"(su32(&bar[s]))
+                     : "memory");
+    };
+    int64_t issued = 0, next = blockIdx.x;
+    for (; issued < S && next < ntiles; ++issued, next += gridDim.x)
+        if (lane == 0) load(next, issued);
+    int64_t j = 0;
+    bool ok = true;
+    for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x, ++j) {
+        const int s = (int)(j % S);
+        if (!mbar_wait(&bar[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
+            flag_error(ZS_DEVERR_GATHER_WAIT);
+            ok = false;
+            break;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const int64_t i = a.lo + tl * T;
+        const uint32_t bytes = tile_len(tl) * 2u;
+        for (int q = lane; q < a.nd; q += 32) bulk_store(a.dst.p[q] + (i - a.dst_off), buf + (size_t)s * T, bytes);
+        bulk_commit();
+        if (next < ntiles) {
+            bulk_wait_read_all();                        // every lane's stores have read the stage
+            __syncwarp();
+            if (lane == 0) load(next, issued);
+            ++issued;
+            next += gridDim.x;
+        }
+    }
+    if (!ok && lane == 0)                                // loads still in flight into the ring
+        for (int64_t k = j; k < issued; ++k) mbar_wait(&bar[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
+    bulk_wait_all();
+}
+
 namespace {
 
 template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
@@ -340,6 +425,35 @@ __global__ void k_wait_selftest(long long limit) {
 
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
     k_wait_selftest<<<1, 32, 0, st>>>(limit_cycles);
+    return cudaGetLastError();
+}
+
+// Bulk-store gather over the 8-aligned body [lo, lo + n): tiles of 8192 elements, a 2-stage ring
+// (32.9 KB) per one-warp CTA, about 16 CTAs per SM (chosen by measurement on GB300).
+cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
+                               int64_t n, int nd, cudaStream_t st) {
+    GatherBulkArgs a{};
+    a.src = src;
+    a.src_off = src_off;
+    a.dst = dst;
+    a.dst_off = dst_off;
+    a.lo = lo;
+    a.n = n;
+    a.nd = nd;
+    a.T = 8192;
+    a.wait_limit = 4000000000LL;
+    a.drain_limit = 4000000000LL;
+    constexpr int S = 2;
+    const int smem = 128 + S * a.T * 2;
+    cudaError_t e = cudaFuncSetAttribute(k_gather_bulk<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t ntiles = (n + a.T - 1) / a.T;
+    const int64_t cap = (int64_t)sms * 16;
+    const int grid = (int)(ntiles < cap ? ntiles : cap);
+    k_gather_bulk<S><<<grid, 32, smem, st>>>(a);
     return cudaGetLastError();
 }
 

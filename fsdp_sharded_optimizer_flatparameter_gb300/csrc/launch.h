@@ -51,6 +51,9 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                              int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
+// One source to N_d destinations with bulk stores, over the 8-aligned body [lo, lo + n).
+cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
+                               int64_t n, int nd, cudaStream_t st);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);
 cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,
                            const Range& r, const AdamScalars& s, int nd, cudaStream_t st);

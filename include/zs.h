@@ -92,6 +92,7 @@ extern "C" {
 #define ZS_DEVERR_PRODUCER_WAIT 1u   /* a staged kernel's producer gave up waiting for a free stage */
 #define ZS_DEVERR_CONSUMER_WAIT 2u   /* a staged kernel's consumer gave up waiting for its data     */
 #define ZS_DEVERR_SELFTEST      3u   /* zs_selftest_wait_timeout ran its wait out (expected)         */
+#define ZS_DEVERR_GATHER_WAIT   4u   /* a bulk-store gather gave up waiting for its tile             */
 
 typedef struct zs_plan_s* zs_plan_t;
 

@@ -520,3 +520,33 @@ def test_fused_step_reads_and_writes_pinned_host_memory(variant):
         assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
     finally:
         zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+
+
+# ---------------------------------------------------------------- bulk-store gather
+
+@pytest.mark.parametrize("n_d,numel", [(2, 3_000_001), (3, 1_500_007), (8, 4_194_305), (16, 2_100_003), (64, 1_048_583)])
+def test_bulk_store_gathers_match_oracle(n_d, numel):
+    """Gathers large enough for the bulk-store kernel (one source, N_d destinations): the
+    all-gather from shards into full replicas, and the ZeRO-3 unit gather at a unit base that is
+    not zero; ragged ends go through the element-wise fringe."""
+    shapes = [(numel,), (1_048_576 + 24,)]
+    plan, ref = _plans(shapes, n_d, units=[0, 1], stage=3)
+    P, pads = plan.padded, plan.pad_ranges()
+    shards = synth.master_init(P, pads, seed=60, device=DEV).to(BF16)
+    osh = H.reshard(ref, H.to_np_bf16(shards))
+    reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps)
+    full_units = []
+    for u in range(plan.n_units):
+        full, _ = synth.rank_buffers(n_d, plan.unit(u)["padded"], BF16, DEV)
+        zs.zs_zero3_gather_unit(plan, u, shards, full)
+        full_units.append(full)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    want = steps.all_gather(ref, osh)
+    for q in range(n_d):
+        assert np.array_equal(H.to_np_bf16(reps[q]), want[q])
+    for u in range(plan.n_units):
+        want_u = steps.all_gather_unit(ref, u, osh)
+        for q in (0, n_d // 2, n_d - 1):
+            assert np.array_equal(H.to_np_bf16(full_units[u][q]), want_u[q])
