@@ -408,23 +408,37 @@ def run_ours(args, ws, rank, local):
     # the unfused path on the same buffers, for comparison (not part of value)
     unfused = None
     if W.kind == "fused" and not args.profile_case and rank == 0 and args.unfused_steps > 0:
+        # the unfused ZeRO-2 step on the same buffers, each kernel timed on its own (not part of value)
         ghat = torch.empty(P, dtype=torch.bfloat16, device=dev)
         shards = torch.empty(P, dtype=torch.bfloat16, device=dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        names = ("reduce_scatter_mean", "adamw_shard_step", "all_gather")
+        per = {k: [] for k in names}
+        total = []
         for k in range(args.unfused_steps + 2):
-            if k == 2:
-                a.record(stream)
             W.t += 1
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            evs[0].record(stream)
             zs.zs_reduce_scatter_mean(plan, -1, W.grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED, stream=stream)
+            evs[1].record(stream)
             zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, W.master, W.m, W.v, [shards], zs.ZS_SHARDED,
                                    W.hp, W.t, stream=stream)
+            evs[2].record(stream)
             zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, W.reps, stream=stream)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        ums = a.elapsed_time(b) / args.unfused_steps
+            evs[3].record(stream)
+            torch.cuda.synchronize(dev)
+            if k >= 2:
+                for j, name in enumerate(names):
+                    per[name].append(evs[j].elapsed_time(evs[j + 1]))
+                total.append(evs[0].elapsed_time(evs[3]))
+        ums = statistics.mean(total)
+        kb = {"reduce_scatter_mean": 2 * n_d + 2, "adamw_shard_step": 28, "all_gather": 2 + 2 * n_d}
         unfused = {"ms_per_step": ums, "params_per_s": plan.numel / (ums / 1e3),
                    "algorithmic_gbs": bytes_per_padded_element(n_d, "unfused") * P / (ums / 1e3) / 1e9,
-                   "launches_per_step": 3}
+                   "launches_per_step": 3,
+                   "kernels": {name: {"ms": statistics.mean(per[name]), "bytes_per_element": kb[name],
+                                      "gbs": kb[name] * P / (statistics.mean(per[name]) / 1e3) / 1e9,
+                                      "frac_of_peak": kb[name] * P / (statistics.mean(per[name]) / 1e3) / 1e9 / peak}
+                               for name in names}}
         del ghat, shards
 
     # end to end through the C ABI with host buffers, all inside the timed region, two ways:

@@ -295,6 +295,10 @@ static cudaError_t fused_impl(const BView& g, float* master, float* m, float* v,
 // ------------------------------------------------------------------ dispatch
 
 static bool aligned8(int64_t x) { return (x & 7) == 0; }
+static bool all_device(const void* const* ps, int n);
+static int g_fused_variant = ZS_FUSED_AUTO;
+// Smallest body worth a persistent staged launch (below it the register-streaming kernel is as fast).
+constexpr int64_t kTmaMinElems = int64_t(1) << 20;
 
 #define ZS_DISPATCH_ND(nd, CALL)            \
     switch (nd) {                           \
@@ -324,13 +328,34 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
     const bool vec = aligned8(grad.off) && aligned8(par.off) &&
                      (!by_owner || (aligned8(r.base) && aligned8(r.shard)));
     const Split sp = split_range(r.lo, r.hi, vec);
+    // reduced gradient and parameters both one array (ZeRO-2): the staged kernel with one rank is
+    // exactly this update (the mean of one bf16 value is that value; a -0 gradient reads as +0,
+    // which changes neither moment nor parameter)
+    if (!by_owner && (sp.nvec << 3) >= kTmaMinElems && g_fused_variant != ZS_FUSED_LDG) {
+        const void* ps[5] = {grad.ptr.p[0], par.ptr.p[0], master, m, v};
+        if (all_device(ps, 5)) {
+            const int64_t body_hi = sp.vlo + (sp.nvec << 3);
+            cudaError_t e = launch_fused_tma(grad, master, m, v, par, false, sp.vlo, sp.nvec << 3, s, 1, st);
+            if (e != cudaErrorNotSupported) {
+                if (e != cudaSuccess) return e;
+                AdamOp op{grad, par, 0, 0, master, m, v, s, r.base, r.shard};
+                Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
+                for (const Split& f : rest) {
+                    if (f.hi <= f.lo) continue;
+                    k_adamw<<<grid_for((const void*)k_adamw, f.hi - f.lo), kThreads, 0, st>>>(op, f);
+                    e = cudaGetLastError();
+                    if (e != cudaSuccess) return e;
+                }
+                return cudaSuccess;
+            }
+        }
+    }
     AdamOp op{grad, par, grad_by_owner ? 1 : 0, par_by_owner ? 1 : 0, master, m, v, s, r.base, r.shard};
     const int grid = grid_for((const void*)k_adamw, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
     k_adamw<<<grid, kThreads, 0, st>>>(op, sp);
     return cudaGetLastError();
 }
 
-static bool all_device(const void* const* ps, int n);
 constexpr int64_t kBulkGatherMinElems = int64_t(1) << 20;
 
 cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
@@ -364,12 +389,8 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
 #undef ZS_GA
 }
 
-static int g_fused_variant = ZS_FUSED_AUTO;
 void set_fused_variant(int v) { g_fused_variant = v; }
 int fused_variant() { return g_fused_variant; }
-
-// Smallest body worth a persistent staged launch (below it the register-streaming kernel is as fast).
-constexpr int64_t kTmaMinElems = int64_t(1) << 20;
 
 static cudaError_t launch_fused_ldg(const BView& g, float* master, float* m, float* v, const BView& out,
                                     bool broadcast, const Split& sp, const AdamScalars& s, int nd, cudaStream_t st) {

@@ -229,3 +229,43 @@ def test_flat_2p28_plus_7_sweep(n_d):
         H.check_f32(_np(_snap(master, *c)), p, "zero3 master %s" % (c,))
         H.check_f32(_np(_snap(m, *c)), m1, "zero3 m %s" % (c,))
         H.check_bf16(_np(_snap(shards, *c)), bits, "zero3 shards %s" % (c,))
+
+
+def test_llama7b_zero3_step_two_streams_full_size():
+    """The whole ZeRO-3 step exactly as the benchmark runs it (all 33 units, side stream, 2-slot
+    pool, one set of per-rank gradient buffers read as every unit's gradients), sampled chunks of
+    three units against the oracle."""
+    wl = synth.WORKLOADS["llama-7b-zero3"]
+    shapes, units = synth.workload_params(wl["model"])
+    n_d = wl["n_d"]
+    plan = zs.Plan(shapes, n_d, stage=3, unit_of_param=units)
+    P, pads = plan.padded, plan.pad_ranges()
+    master = synth.master_init(P, pads, wl["seed"], device=DEV)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    shards = master.to(BF16)
+    biggest = max(plan.unit(u)["padded"] for u in range(plan.n_units))
+    ugrads, _ = synth.rank_buffers(n_d, biggest, BF16, DEV)
+    synth.fill_grads(ugrads, [], wl["seed"], 1, wl["sigma"])
+    pool = [synth.rank_buffers(n_d, biggest, BF16, DEV)[0] for _ in range(2)]
+    side = torch.cuda.Stream()
+    probe = {}
+    for u in (0, 17, 32):
+        ud = plan.unit(u)
+        for lo, hi in _chunks(ud["padded"], [r * ud["shard"] for r in (1, n_d - 1)], seed=70 + u, n_random=2):
+            gb = ud["base"]
+            probe[(u, lo, hi)] = ([_np(_snap(g, lo, hi)) for g in ugrads], _np(_snap(master, gb + lo, gb + hi)))
+    zs.zs_zero3_step(plan, shards, master, m, v, [ugrads] * plan.n_units, pool, True, HP, 1, side_stream=side)
+    torch.cuda.synchronize()
+    for (u, lo, hi), (gc_, p0) in probe.items():
+        gb = plan.unit(u)["base"]
+        z = np.zeros(hi - lo, np.float32)
+        _, p, m1, v1, bits = H.chunk_oracle(gc_, p0, z, z, HP, 1)
+        # units whose padding falls in the chunk: pad gradients are whatever the buffer holds beyond the
+        # unit's real elements, but pad master/m/v are 0 and stay 0 only if the gradient there is 0
+        real = min(hi, plan.unit(u)["numel"]) - lo
+        what = "u=%d [%d,%d)" % (u, lo, hi)
+        H.check_f32(_np(_snap(master, gb + lo, gb + lo + real)), p[:real], "master " + what)
+        H.check_f32(_np(_snap(v, gb + lo, gb + lo + real)), v1[:real], "v " + what)
+        H.check_bf16(_np(_snap(shards, gb + lo, gb + lo + real)), bits[:real], "shards " + what)
+    # after backward, slot u & 1 holds unit 1 and unit 0 gathered before their update
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE

@@ -550,3 +550,36 @@ def test_bulk_store_gathers_match_oracle(n_d, numel):
         want_u = steps.all_gather_unit(ref, u, osh)
         for q in (0, n_d // 2, n_d - 1):
             assert np.array_equal(H.to_np_bf16(full_units[u][q]), want_u[q])
+
+
+@pytest.mark.parametrize("n_d,numel", [(8, 3_000_005), (3, 2_500_001)])
+def test_staged_adamw_on_sharded_buffers(variant, n_d, numel):
+    """zs_adamw_shard_step with the reduced gradient and the parameters in ZS_SHARDED arrays runs
+    through the staged kernel with one rank; whole-unit and per-rank calls (ragged shard bounds)
+    equal the oracle and the streaming kernel bit for bit."""
+    plan, ref = _plans([(numel,)], n_d)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=61, device=DEV)
+    ghat_np = numerics.bf16_rne((np.random.default_rng(61).standard_normal(P) * 1e-3).astype(np.float32))
+    for lo, hi in pads:
+        ghat_np[lo:hi] = 0
+    ghat = H.from_np_bf16(ghat_np)
+    z = np.zeros(P, np.float32)
+    want_p, want_m, want_v, want_bits = steps.adamw(H.to_np_f32(master0), z, z, ghat_np, HP, 3)
+    results = {}
+    for v_, per_rank in ((zs.ZS_FUSED_AUTO, False), (zs.ZS_FUSED_AUTO, True), (zs.ZS_FUSED_LDG, False)):
+        variant(v_)
+        st = State(master0)
+        params = torch.zeros(P, dtype=BF16, device=DEV)
+        if per_rank:
+            for r in range(n_d):
+                zs.zs_adamw_shard_step(plan, r, [ghat], zs.ZS_SHARDED, *st.args(), [params], zs.ZS_SHARDED, HP, 3)
+        else:
+            zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, *st.args(), [params], zs.ZS_SHARDED, HP, 3)
+        torch.cuda.synchronize()
+        H.check_f32(H.to_np_f32(st.master), want_p, "master %d %s" % (v_, per_rank))
+        H.check_f32(H.to_np_f32(st.m), want_m, "m %d %s" % (v_, per_rank))
+        H.check_f32(H.to_np_f32(st.v), want_v, "v %d %s" % (v_, per_rank))
+        H.check_bf16(H.to_np_bf16(params), want_bits, "params %d %s" % (v_, per_rank))
+        results[(v_, per_rank)] = st
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
