@@ -450,48 +450,11 @@ def run_ours(args, ws, rank, local):
     # e2e reports the faster; the other is kept under e2e_alt.
     e2e = e2e_alt = None
     if W.kind == "fused" and not args.no_e2e and not args.profile_case:
-        host_g = torch.empty((n_d, P), dtype=torch.bfloat16, pin_memory=True)
-        for q in range(n_d):
-            host_g[q].copy_(W.grads[q])
-        host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
-        hrows = [host_g[q] for q in range(n_d)]
-        n_e2e = max(2, min(steps, 5))
-
-        def timed(fn):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            for k in range(n_e2e + 1):
-                if k == 1:
-                    a.record(stream)
-                W.t += 1
-                fn()
-            b.record(stream)
+        try:
+            e2e, e2e_alt = measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws)
+        except (RuntimeError, MemoryError) as exc:        # e.g. pinned host memory exhausted
+            e2e = {"value": None, "unit": "params/s", "error": str(exc)[:200]}
             torch.cuda.synchronize(dev)
-            return max_over_ranks(dist, a.elapsed_time(b) / n_e2e, dev)
-
-        zc_ms = timed(lambda: zs.zs_fused_step(plan, -1, hrows, zs.ZS_RANK_FULL, W.master, W.m, W.v,
-                                               [host_out] + W.reps[1:], W.hp, W.t, stream=stream))
-        biggest = max(hi - lo for _, lo, hi in (plan.bucket(b) for b in range(plan.n_buckets)))
-        staging = [zs_synth_buffers(n_d, biggest, dev) for _ in range(2)]
-        copy_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        st_ms = timed(lambda: zs.zs_zero2_step_host(plan, hrows, staging, W.master, W.m, W.v, W.reps, W.hp, W.t,
-                                                    host_replica0=host_out, stream=stream, copy_stream=copy_s,
-                                                    d2h_stream=d2h_s))
-        paths = {
-            "zero-copy": (zc_ms, "zs_fused_step on pinned host gradients, rank 0's replica written to pinned "
-                                 "host memory by the kernel over the host link"),
-            "staged": (st_ms, "zs_zero2_step_host: bucket-wise H2D through a 2-slot device staging ring on a "
-                              "copy stream, fused update per bucket, D2H of rank 0's replica on a third stream"),
-        }
-        order = sorted(paths, key=lambda k: paths[k][0])
-        for i, key in enumerate(order):
-            ms_, desc = paths[key]
-            rec = {"value": ws * plan.numel / (ms_ / 1e3), "unit": "params/s", "ms_per_step": ms_,
-                   "h2d_bytes_per_step": n_d * P * 2, "d2h_bytes_per_step": P * 2, "path": desc}
-            if i == 0:
-                e2e = rec
-            else:
-                e2e_alt = rec
-        del host_g, host_out, hrows, staging
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.profile_case:
@@ -535,6 +498,54 @@ def run_ours(args, ws, rank, local):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws):
+    """Both host-fed paths; returns (faster, other)."""
+    host_g = torch.empty((n_d, P), dtype=torch.bfloat16, pin_memory=True)
+    for q in range(n_d):
+        host_g[q].copy_(W.grads[q])
+    host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+    hrows = [host_g[q] for q in range(n_d)]
+    n_e2e = max(2, min(steps, 5))
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for k in range(n_e2e + 1):
+            if k == 1:
+                a.record(stream)
+            W.t += 1
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(dist, a.elapsed_time(b) / n_e2e, dev)
+
+    zc_ms = timed(lambda: zs.zs_fused_step(plan, -1, hrows, zs.ZS_RANK_FULL, W.master, W.m, W.v,
+                                           [host_out] + W.reps[1:], W.hp, W.t, stream=stream))
+    biggest = max(hi - lo for _, lo, hi in (plan.bucket(b) for b in range(plan.n_buckets)))
+    staging = [zs_synth_buffers(n_d, biggest, dev) for _ in range(2)]
+    copy_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    st_ms = timed(lambda: zs.zs_zero2_step_host(plan, hrows, staging, W.master, W.m, W.v, W.reps, W.hp, W.t,
+                                                host_replica0=host_out, stream=stream, copy_stream=copy_s,
+                                                d2h_stream=d2h_s))
+    e2e = e2e_alt = None
+    paths = {
+        "zero-copy": (zc_ms, "zs_fused_step on pinned host gradients, rank 0's replica written to pinned "
+                             "host memory by the kernel over the host link"),
+        "staged": (st_ms, "zs_zero2_step_host: bucket-wise H2D through a 2-slot device staging ring on a "
+                          "copy stream, fused update per bucket, D2H of rank 0's replica on a third stream"),
+    }
+    order = sorted(paths, key=lambda k: paths[k][0])
+    for i, key in enumerate(order):
+        ms_, desc = paths[key]
+        rec = {"value": ws * plan.numel / (ms_ / 1e3), "unit": "params/s", "ms_per_step": ms_,
+               "h2d_bytes_per_step": n_d * P * 2, "d2h_bytes_per_step": P * 2, "path": desc}
+        if i == 0:
+            e2e = rec
+        else:
+            e2e_alt = rec
+    del host_g, host_out, hrows, staging
+    return e2e, e2e_alt
 
 
 def zs_synth_buffers(n_d, n, dev):

@@ -8,6 +8,7 @@
 
 #include "launch.h"
 #include "plan.h"
+#include "trace.h"
 
 using zs::BView;
 using zs::Ptrs;
@@ -111,6 +112,7 @@ cudaStream_t as_stream(void* s) { return (cudaStream_t)s; }
 extern "C" int zs_accumulate_grad(zs_plan_t plan, void* const* acc, const void* const* micro, float scale,
                                   int32_t first, void* stream) {
     static const char* fn = "zs_accumulate_grad";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     ZS_TRY(check_ptrs(fn, "acc", (const void* const*)acc, plan->n_d));
@@ -129,6 +131,7 @@ extern "C" int zs_accumulate_grad(zs_plan_t plan, void* const* acc, const void* 
 extern "C" int zs_reduce_scatter_mean(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
                                       void* const* out, int32_t out_kind, void* stream) {
     static const char* fn = "zs_reduce_scatter_mean";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     ZS_TRY(check_bucket(fn, plan, bucket, true));
@@ -158,6 +161,7 @@ extern "C" int zs_adamw_shard_step(zs_plan_t plan, int32_t rank, const void* con
                                    float* master, float* m, float* v, void* const* params, int32_t params_kind,
                                    const zs_adamw_hparams* hp, int64_t step, void* stream) {
     static const char* fn = "zs_adamw_shard_step";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     const int nd = plan->n_d;
@@ -188,6 +192,7 @@ extern "C" int zs_adamw_shard_step(zs_plan_t plan, int32_t rank, const void* con
 extern "C" int zs_all_gather(zs_plan_t plan, const void* const* src, int32_t src_kind, void* const* replicas,
                              void* stream) {
     static const char* fn = "zs_all_gather";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     const int nd = plan->n_d;
@@ -242,6 +247,7 @@ static int fused_common(const char* fn, zs_plan_t plan, int32_t bucket, const vo
 extern "C" int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
                              float* master, float* m, float* v, void* const* replicas, const zs_adamw_hparams* hp,
                              int64_t step, void* stream) {
+    zs::TraceRange trace_("zs_fused_step");
     zs::clear_error();
     return fused_common("zs_fused_step", plan, bucket, grads, grads_kind, master, m, v, replicas, hp, step,
                         as_stream(stream));
@@ -251,6 +257,7 @@ extern "C" int zs_fused_step_host(zs_plan_t plan, const void* const* host_grads,
                                   float* master, float* m, float* v, void* const* replicas,
                                   const zs_adamw_hparams* hp, int64_t step, void* host_replica0, void* stream) {
     static const char* fn = "zs_fused_step_host";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     const int nd = plan->n_d;
@@ -280,6 +287,7 @@ extern "C" int zs_fused_step_host(zs_plan_t plan, const void* const* host_grads,
 extern "C" int zs_zero3_gather_unit(zs_plan_t plan, int32_t unit, const void* shards, void* const* full,
                                     void* stream) {
     static const char* fn = "zs_zero3_gather_unit";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     if (unit < 0 || unit >= (int32_t)plan->units.size()) return fail(fn, "unit out of range");
@@ -296,6 +304,7 @@ extern "C" int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* c
                                      float* m, float* v, void* shards, const zs_adamw_hparams* hp, int64_t step,
                                      void* stream) {
     static const char* fn = "zs_zero3_rs_step_unit";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     if (unit < 0 || unit >= (int32_t)plan->units.size()) return fail(fn, "unit out of range");
@@ -341,6 +350,7 @@ extern "C" int zs_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
 
 extern "C" int zs_all_reduce_mean(zs_plan_t plan, int32_t bucket, void* const* grads, void* stream) {
     static const char* fn = "zs_all_reduce_mean";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     ZS_TRY(check_bucket(fn, plan, bucket, true));
@@ -356,6 +366,7 @@ extern "C" int zs_dp_step(zs_plan_t plan, const void* const* grads, float* const
                           float* const* v, void* const* replicas, const zs_adamw_hparams* hp, int64_t step,
                           void* stream) {
     static const char* fn = "zs_dp_step";
+    zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     const int nd = plan->n_d;

@@ -15,6 +15,7 @@
 
 #include "launch.h"
 #include "plan.h"
+#include "trace.h"
 
 namespace {
 
@@ -73,8 +74,10 @@ extern "C" int zs_zero2_step_host(zs_plan_t plan, const void* const* host_grads,
         check(cudaStreamWaitEvent(h2d, start, 0));
         if (d2h != h2d) check(cudaStreamWaitEvent(d2h, start, 0));
     }
+    zs::TraceRange step_range("zs_zero2_step_host");
     int k = 0;
     for (int b = (int)plan->buckets.size() - 1; b >= 0 && err == cudaSuccess; --b, ++k) {
+        zs::TraceRange r_("zero2 bucket %lld", (long long)b);
         const auto& bk = plan->buckets[b];
         const int slot = k & 1;
         const size_t bytes = (size_t)(bk.end - bk.begin) * 2;

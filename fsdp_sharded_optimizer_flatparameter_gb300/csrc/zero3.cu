@@ -21,6 +21,7 @@
 
 #include "launch.h"
 #include "plan.h"
+#include "trace.h"
 
 namespace {
 
@@ -115,9 +116,11 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
     check(cudaEventRecord(start, mainS));
     check(cudaStreamWaitEvent(sideS, start, 0));
 
+    zs::TraceRange step_range("zs_zero3_step");
     // forward, unit order
     cudaEvent_t slot_free[2] = {nullptr, nullptr};   // main's release of each slot's last user (reshard on)
     for (int u = 0; u < U && err == cudaSuccess; ++u) {
+        zs::TraceRange r_("zero3 forward gather unit %lld", (long long)u);
         const zs::Unit& un = plan->units[u];
         const int slot = reshard_after_forward ? (u & 1) : u;
         if (reshard_after_forward && slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
@@ -132,6 +135,7 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
 
     // backward, reverse unit order
     for (int u = U - 1; u >= 0 && err == cudaSuccess; --u) {
+        zs::TraceRange r_("zero3 backward gather + reduce-scatter/update unit %lld", (long long)u);
         const zs::Unit& un = plan->units[u];
         const zs::Range r{un.base, un.base + un.padded, un.base, un.shard};
         if (reshard_after_forward) {

@@ -583,3 +583,42 @@ def test_staged_adamw_on_sharded_buffers(variant, n_d, numel):
         H.check_bf16(H.to_np_bf16(params), want_bits, "params %d %s" % (v_, per_rank))
         results[(v_, per_rank)] = st
     assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+
+
+def test_guard_zones_untouched_large_kernels():
+    """Sentinels around every buffer of the large-range kernels (staged fused step, staged AdamW,
+    bulk-store gathers, FSDP2 copies): nothing is written outside the buffers."""
+    n_d, numel = 8, 2_097_165
+    plan, _ = _plans([(numel,)], n_d, stage=3)
+    P = plan.padded
+    bufs = []
+
+    def mk(n, dtype):
+        t, raw, g = _guarded(n, dtype)
+        t.zero_()
+        bufs.append((raw, g))
+        return t
+
+    grads = [mk(P, BF16) for _ in range(n_d)]
+    for g in grads:
+        g.normal_(0, 1e-3)
+    reps = [mk(P, BF16) for _ in range(n_d)]
+    full = [mk(P, BF16) for _ in range(n_d)]
+    master, m, v = mk(P, torch.float32), mk(P, torch.float32), mk(P, torch.float32)
+    ghat, shards = mk(P, BF16), mk(P, BF16)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)        # staged, broadcast
+    zs.zs_zero3_rs_step_unit(plan, 0, grads, master, m, v, shards, HP, 2)               # staged, single output
+    zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED)
+    zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, master, m, v, [shards], zs.ZS_SHARDED, HP, 3)
+    zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps)                               # bulk gather
+    zs.zs_zero3_gather_unit(plan, 0, shards, full)                                      # bulk gather
+    p2 = zs.Plan([(1023, 2048), (5,)], n_d, layout=zs.ZS_LAYOUT_FSDP2)
+    params = [mk(1023 * 2048, BF16), mk(5, BF16)]
+    params[0].normal_()
+    flat = mk(p2.unit(0)["padded"], BF16)
+    zs.zs_fsdp2_chunk_cat(p2, 0, params, flat)
+    zs.zs_fsdp2_copy_out(p2, 0, flat, params)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    for raw, g in bufs:
+        assert bool((raw[:g] == 0x5A).all()) and bool((raw[-g:] == 0x5A).all())
