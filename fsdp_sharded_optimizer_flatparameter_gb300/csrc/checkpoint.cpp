@@ -1,27 +1,31 @@
-// Sharded checkpoint: every simulated rank writes its own shards, loading re-cuts
-// them for any rank count.
+// Sharded checkpoint: every simulated rank writes its own shards; loading lays
+// them out for any target plan - another rank count, unit grouping or layout.
 //
 // "Infra: Data Parallel" (F. Pu), section "Fully Sharded Data Parallel (FSDP)",
 // subsection "Checkpoint": ranks write the shards they own plus the metadata
-// needed to restore them; loading follows the target run's sharding layout,
-// so save and load may use different numbers of ranks; optimizer state is
-// saved with the weights.  An element is identified across layouts by its
-// position among its unit's real elements (padding is dropped and re-made).
+// needed to restore them; loading follows the target run's sharding layout, so
+// save and load may use different numbers of ranks; optimizer state is saved
+// with the weights; FSDP1 and FSDP2 layouts both support this.
+//
+// An element is identified by (parameter k, position e in the parameter's own
+// row-major order); no layout, rank count or unit grouping changes that.  Each
+// parameter's elements lie in a few runs that are contiguous both in one saved
+// rank file and in the target's flat space (a run ends where either side moves
+// to another rank); loading copies run by run and zeroes the target's padding.
 //
 // Files in `dir` (which must exist):
-//   meta.txt          text: format tag, N_d, step, parameter shapes and units,
-//                     per-unit (numel, padded, shard), the arrays and their types
-//   rank-NNNNN.bin    rank r's shard of each array in the order params (bf16),
-//                     master, m, v (fp32); each array is the rank's piece of every
-//                     unit, units in order
-// Both calls copy through a bounded host buffer with cudaMemcpyAsync on the
-// given stream and synchronise that stream.
+//   meta.txt          text: format tag and version, N_d, step, layout, per parameter
+//                     (numel, rows of dim 0, unit), per unit (numel, padded, shard),
+//                     the arrays and their element types
+//   rank-NNNNN.bin    rank r's shard of params (bf16), master, m, v (fp32), one after
+//                     another; each is the rank's piece of every unit, units in order
+// Both calls copy through a 64 MiB host buffer with cudaMemcpyAsync on the given
+// stream and synchronise that stream.
 #include <algorithm>
 #include <cerrno>
 #include <cstdio>
 #include <cstring>
 #include <fstream>
-#include <sstream>
 #include <string>
 #include <vector>
 
@@ -45,9 +49,67 @@ std::string rank_file(const std::string& dir, int r) {
     return dir + "/" + name;
 }
 
-struct SavedUnit {
-    int64_t numel, padded, shard;
+// Where element e of parameter k lives in a layout: the rank, the position inside that rank's
+// shard (all units concatenated), and how many following elements stay contiguous there.
+struct Layout {
+    int32_t n_d = 0, layout = 0;
+    std::vector<int64_t> numel, d0, row, chunk, unit, off_in_unit;   // per parameter
+    std::vector<int64_t> u_shard, u_local, u_base;                   // per unit
+    void finish() {
+        const size_t K = numel.size(), U = u_shard.size();
+        row.resize(K);
+        chunk.resize(K);
+        off_in_unit.assign(K, 0);
+        std::vector<int64_t> acc(U, 0);
+        for (size_t k = 0; k < K; ++k) {
+            row[k] = numel[k] / d0[k];
+            chunk[k] = (d0[k] + n_d - 1) / n_d;
+            off_in_unit[k] = acc[unit[k]];
+            acc[unit[k]] += layout == ZS_LAYOUT_FSDP2 ? chunk[k] * row[k] : numel[k];
+        }
+        u_local.assign(U, 0);
+        u_base.assign(U, 0);
+        for (size_t u = 1; u < U; ++u) {
+            u_local[u] = u_local[u - 1] + u_shard[u - 1];
+            u_base[u] = u_base[u - 1] + u_shard[u - 1] * n_d;
+        }
+    }
+    // (rank, position in the rank's shard, contiguous run length)
+    void locate(size_t k, int64_t e, int32_t* rank, int64_t* pos, int64_t* run) const {
+        const int64_t u = unit[k], S = u_shard[u];
+        if (layout == ZS_LAYOUT_FSDP2) {
+            const int64_t i = e / row[k], j = e % row[k];
+            const int64_t r = i / chunk[k];
+            *rank = (int32_t)r;
+            *pos = u_local[u] + off_in_unit[k] + (i - r * chunk[k]) * row[k] + j;
+            const int64_t rows_end = std::min((r + 1) * chunk[k], d0[k]);
+            *run = rows_end * row[k] - e;
+        } else {
+            const int64_t x = off_in_unit[k] + e;           // index inside the unit's flat range
+            const int64_t r = x / S;
+            *rank = (int32_t)r;
+            *pos = u_local[u] + (x - r * S);
+            *run = std::min((r + 1) * S - x, numel[k] - e);
+        }
+    }
+    // global flat index of (rank, position in the rank's shard)
+    int64_t global(size_t k, int32_t rank, int64_t pos) const {
+        const int64_t u = unit[k];
+        return u_base[u] + (int64_t)rank * u_shard[u] + (pos - u_local[u]);
+    }
 };
+
+Layout layout_of(zs_plan_t p) {
+    Layout L;
+    L.n_d = p->n_d;
+    L.layout = p->layout;
+    L.numel = p->param_numel;
+    L.d0 = p->param_d0;
+    L.unit.assign(p->param_unit.begin(), p->param_unit.end());
+    for (const auto& u : p->units) L.u_shard.push_back(u.shard);
+    L.finish();
+    return L;
+}
 
 }  // namespace
 
@@ -56,18 +118,18 @@ extern "C" int zs_checkpoint_save(zs_plan_t plan, const char* dir, const void* s
     static const char* fn = "zs_checkpoint_save";
     zs::clear_error();
     if (!plan || !dir || !shards || !master || !m || !v) return fail(fn, "NULL argument");
-    if (plan->layout != ZS_LAYOUT_FSDP1) return fail(fn, "only FSDP1-layout plans are supported", ZS_ERR_UNSUPPORTED);
     cudaStream_t st = (cudaStream_t)stream;
     const std::string d(dir);
     {
         std::ofstream meta(d + "/meta.txt");
         if (!meta) return fail(fn, "cannot write " + d + "/meta.txt: " + std::strerror(errno));
-        meta << "zs-checkpoint 1\n";
+        meta << "zs-checkpoint 2\n";
         meta << "n_d " << plan->n_d << "\n";
         meta << "step " << step << "\n";
+        meta << "layout " << plan->layout << "\n";
         meta << "params " << plan->param_numel.size() << "\n";
         for (size_t k = 0; k < plan->param_numel.size(); ++k)
-            meta << "p " << plan->param_numel[k] << " unit " << plan->param_unit[k] << "\n";
+            meta << "p " << plan->param_numel[k] << " d0 " << plan->param_d0[k] << " unit " << plan->param_unit[k] << "\n";
         meta << "units " << plan->units.size() << "\n";
         for (const auto& u : plan->units) meta << "u " << u.numel << " " << u.padded << " " << u.shard << "\n";
         meta << "arrays params:bf16 master:f32 m:f32 v:f32\n";
@@ -110,61 +172,69 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
     static const char* fn = "zs_checkpoint_load";
     zs::clear_error();
     if (!plan || !dir || !shards || !master || !m || !v) return fail(fn, "NULL argument");
-    if (plan->layout != ZS_LAYOUT_FSDP1) return fail(fn, "only FSDP1-layout plans are supported", ZS_ERR_UNSUPPORTED);
     cudaStream_t st = (cudaStream_t)stream;
     const std::string d(dir);
 
-    // ---- metadata
+    // ---- metadata of the save
     std::ifstream meta(d + "/meta.txt");
     if (!meta) return fail(fn, "cannot read " + d + "/meta.txt");
-    std::string tag;
-    int version = 0, saved_nd = 0;
+    std::string tag, key;
+    int version = 0;
     int64_t saved_step = 0;
     size_t n_params = 0, n_units = 0;
-    std::string key;
+    Layout S;
     meta >> tag >> version;
-    if (tag != "zs-checkpoint" || version != 1) return fail(fn, "not a zs checkpoint (meta.txt)");
-    meta >> key >> saved_nd;
-    if (key != "n_d" || saved_nd < 1 || saved_nd > ZS_MAX_RANKS) return fail(fn, "bad n_d in meta.txt");
+    if (tag != "zs-checkpoint" || version != 2) return fail(fn, "not a zs checkpoint of format 2 (meta.txt)");
+    meta >> key >> S.n_d;
+    if (key != "n_d" || S.n_d < 1 || S.n_d > ZS_MAX_RANKS) return fail(fn, "bad n_d in meta.txt");
     meta >> key >> saved_step;
     if (key != "step") return fail(fn, "bad step in meta.txt");
+    meta >> key >> S.layout;
+    if (key != "layout" || (S.layout != ZS_LAYOUT_FSDP1 && S.layout != ZS_LAYOUT_FSDP2)) return fail(fn, "bad layout in meta.txt");
     meta >> key >> n_params;
     if (key != "params" || n_params != plan->param_numel.size())
         return fail(fn, "the checkpoint holds another model (parameter count differs)");
+    S.numel.resize(n_params);
+    S.d0.resize(n_params);
+    S.unit.resize(n_params);
     for (size_t k = 0; k < n_params; ++k) {
-        std::string p, unit_kw;
-        int64_t numel = -1;
-        int unit = -1;
-        meta >> p >> numel >> unit_kw >> unit;
-        if (p != "p" || unit_kw != "unit") return fail(fn, "bad parameter line in meta.txt");
-        if (numel != plan->param_numel[k] || unit != plan->param_unit[k])
+        std::string p, d0_kw, unit_kw;
+        meta >> p >> S.numel[k] >> d0_kw >> S.d0[k] >> unit_kw >> S.unit[k];
+        if (p != "p" || d0_kw != "d0" || unit_kw != "unit") return fail(fn, "bad parameter line in meta.txt");
+        if (S.numel[k] != plan->param_numel[k] || S.d0[k] != plan->param_d0[k])
             return fail(fn, "the checkpoint holds another model (parameter " + std::to_string(k) + " differs)");
     }
     meta >> key >> n_units;
-    if (key != "units" || n_units != plan->units.size()) return fail(fn, "the checkpoint holds another unit layout");
-    std::vector<SavedUnit> su(n_units);
+    if (key != "units" || n_units < 1 || n_units > n_params) return fail(fn, "bad unit count in meta.txt");
+    for (size_t k = 0; k < n_params; ++k)
+        if (S.unit[k] < 0 || S.unit[k] >= (int64_t)n_units) return fail(fn, "bad unit id in meta.txt");
+    S.u_shard.resize(n_units);
     for (size_t u = 0; u < n_units; ++u) {
         std::string tagu;
-        meta >> tagu >> su[u].numel >> su[u].padded >> su[u].shard;
-        if (tagu != "u" || su[u].numel != plan->units[u].numel || su[u].shard * saved_nd != su[u].padded)
-            return fail(fn, "bad unit line in meta.txt");
+        int64_t numel = 0, padded = 0;
+        meta >> tagu >> numel >> padded >> S.u_shard[u];
+        if (tagu != "u" || S.u_shard[u] * S.n_d != padded) return fail(fn, "bad unit line in meta.txt");
     }
     if (!meta) return fail(fn, "truncated meta.txt");
-    int64_t saved_shard_total = 0;
-    std::vector<int64_t> unit_off(n_units);
-    for (size_t u = 0; u < n_units; ++u) {
-        unit_off[u] = saved_shard_total;
-        saved_shard_total += su[u].shard;
+    S.finish();
+    // the saved layout must place every element inside its rank's unit piece
+    for (size_t k = 0; k < n_params; ++k) {
+        int64_t need = S.layout == ZS_LAYOUT_FSDP2 ? S.off_in_unit[k] + S.chunk[k] * S.row[k]
+                                                   : (S.off_in_unit[k] + S.numel[k] + S.n_d - 1) / S.n_d;
+        int64_t have = S.layout == ZS_LAYOUT_FSDP2 ? S.u_shard[S.unit[k]] : S.u_shard[S.unit[k]];
+        if (need > have) return fail(fn, "meta.txt shard sizes do not fit its parameters");
     }
+    int64_t saved_shard_total = 0;
+    for (auto x : S.u_shard) saved_shard_total += x;
+    const Layout D = layout_of(plan);
 
-    // ---- data
-    void* dst[4] = {shards, master, m, v};
-    std::vector<FILE*> files(saved_nd, nullptr);
+    // ---- files
+    std::vector<FILE*> files(S.n_d, nullptr);
     auto close_all = [&]() {
         for (auto f : files)
             if (f) std::fclose(f);
     };
-    for (int r = 0; r < saved_nd; ++r) {
+    for (int r = 0; r < S.n_d; ++r) {
         files[r] = std::fopen(rank_file(d, r).c_str(), "rb");
         if (!files[r]) {
             close_all();
@@ -178,37 +248,48 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
             return fail(fn, rank_file(d, r) + " has the wrong size");
         }
     }
+
+    // ---- data: padding of the target first, then every parameter run by run
+    void* dst[4] = {shards, master, m, v};
+    std::vector<int64_t> pad_b, pad_e;
+    {
+        int64_t count = 0;
+        zs_plan_pad_ranges(plan, nullptr, nullptr, 0, &count);
+        pad_b.resize(count + 1);
+        pad_e.resize(count + 1);
+        zs_plan_pad_ranges(plan, pad_b.data(), pad_e.data(), count, &count);
+        pad_b.resize(count);
+        pad_e.resize(count);
+    }
     std::vector<char> buf(kChunk);
     int64_t section = 0;                                   // byte offset of array a inside a rank file
     for (int a = 0; a < 4; ++a) {
         const int eb = kElemBytes[a];
-        for (size_t u = 0; u < n_units; ++u) {
-            const zs::Unit& du = plan->units[u];
-            char* base = (char*)dst[a] + (size_t)du.base * eb;
-            // the target's padding is zero
-            if (du.padded > du.numel) {
-                cudaError_t e = cudaMemsetAsync(base + (size_t)du.numel * eb, 0, (size_t)(du.padded - du.numel) * eb, st);
-                if (e != cudaSuccess) {
-                    close_all();
-                    return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
-                }
+        for (size_t i = 0; i < pad_b.size(); ++i) {
+            cudaError_t e = cudaMemsetAsync((char*)dst[a] + (size_t)pad_b[i] * eb, 0, (size_t)(pad_e[i] - pad_b[i]) * eb, st);
+            if (e != cudaSuccess) {
+                close_all();
+                return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
             }
-            // unit-local real element j sits in saved rank j / S_u at position j % S_u of its piece
-            for (int r = 0; r < saved_nd; ++r) {
-                const int64_t lo = (int64_t)r * su[u].shard;
-                const int64_t hi = std::min(lo + su[u].shard, su[u].numel);
-                if (hi <= lo) continue;
-                if (std::fseek(files[r], (long)(section + unit_off[u] * eb), SEEK_SET) != 0) {
+        }
+        for (size_t k = 0; k < n_params; ++k) {
+            for (int64_t e0 = 0; e0 < S.numel[k];) {
+                int32_t rs, rd;
+                int64_t ps, pd, ls, ld;
+                S.locate(k, e0, &rs, &ps, &ls);
+                D.locate(k, e0, &rd, &pd, &ld);
+                int64_t len = std::min(ls, ld);
+                if (std::fseek(files[rs], (long)(section + ps * eb), SEEK_SET) != 0) {
                     close_all();
-                    return fail(fn, "seek failed in " + rank_file(d, r));
+                    return fail(fn, "seek failed in " + rank_file(d, rs));
                 }
-                size_t left = (size_t)(hi - lo) * eb;
-                char* to = base + (size_t)lo * eb;
+                char* to = (char*)dst[a] + (size_t)D.global(k, rd, pd) * eb;
+                size_t left = (size_t)len * eb;
                 while (left) {
                     const size_t n = left < kChunk ? left : kChunk;
-                    if (std::fread(buf.data(), 1, n, files[r]) != n) {
+                    if (std::fread(buf.data(), 1, n, files[rs]) != n) {
                         close_all();
-                        return fail(fn, "short read from " + rank_file(d, r));
+                        return fail(fn, "short read from " + rank_file(d, rs));
                     }
                     cudaError_t e = cudaMemcpyAsync(to, buf.data(), n, cudaMemcpyHostToDevice, st);
                     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -219,6 +300,7 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
                     to += n;
                     left -= n;
                 }
+                e0 += len;
             }
         }
         section += saved_shard_total * eb;

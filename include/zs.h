@@ -358,18 +358,19 @@ int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads
 /* Sharded checkpoint ("Infra: Data Parallel", FSDP section, subsection
  * "Checkpoint": each rank writes the shards it owns plus the metadata needed to
  * restore them; loading follows the target layout, so the rank count may differ;
- * optimizer state is saved with the weights).
- * zs_checkpoint_save writes dir/meta.txt (format tag, N_d, step, parameter
- * element counts and units, per-unit numel/padded/shard) and one file per
- * simulated rank, dir/rank-NNNNN.bin, holding that rank's shard of the bf16
- * parameters, then master, m and v (each the rank's piece of every unit, units in
- * order).  zs_checkpoint_load reads such a directory into the ZS_SHARDED arrays of
- * `plan`, which must describe the same parameters and units but may have another
- * N_d: each unit's real elements keep their order, the new padding is zeroed.
- * `dir` must exist.  Arrays are ZS_SHARDED device arrays of plan's padded_numel
- * elements.  Both calls copy through a 64 MiB host buffer with cudaMemcpyAsync on
- * `stream` and synchronise it (they return after the data is in place).
- * Plans with the FSDP2 layout are not supported (ZS_ERR_UNSUPPORTED).
+ * optimizer state is saved with the weights; FSDP1 and FSDP2 both support it).
+ * zs_checkpoint_save writes dir/meta.txt (format tag, N_d, step, layout, per
+ * parameter its element count, dim-0 rows and unit, per unit numel/padded/shard)
+ * and one file per simulated rank, dir/rank-NNNNN.bin, holding that rank's shard
+ * of the bf16 parameters, then master, m and v (each the rank's piece of every
+ * unit, units in order).  zs_checkpoint_load reads such a directory into the
+ * ZS_SHARDED arrays of `plan`, which must list the same parameters (element counts
+ * and dim-0 sizes) but may use another N_d, another unit grouping and the other
+ * layout: every element keeps its place in its parameter, the target's padding is
+ * zeroed.  `dir` must exist.  Arrays are ZS_SHARDED device arrays of plan's
+ * padded_numel elements.  Both calls copy through a 64 MiB host buffer with
+ * cudaMemcpyAsync on `stream` and synchronise it (they return after the data is
+ * in place).
  * Errors: ZS_ERR_INVALID (NULL argument, I/O failure, a checkpoint of another
  * model or a malformed one: nothing is written to the device before the metadata
  * and file sizes are checked), ZS_ERR_CUDA. */

@@ -72,3 +72,63 @@ def param_values(plan, rank_shards, k, name):
             ui = plan.param_unit[k]
             vals.append(rank_shards[r][name][offs[ui] + shard_off:offs[ui] + shard_off + length])
     return np.concatenate(vals) if vals else np.zeros(0)
+
+
+# ---------------------------------------------------------------- any layout to any layout
+# An element is identified by (parameter, position in the parameter's own row-major order),
+# which neither the rank count, the unit grouping nor the layout changes.  Saving keeps each
+# rank's shard of its layout; loading reads every parameter back element by element and lays it
+# out for the target plan.
+
+def save_any(plan, kind, rank_shards):
+    """kind: "fsdp1" (a layout.Plan) or "fsdp2" (an fsdp2.Plan2); rank_shards[r][name] rank-local."""
+    return {"kind": kind, "plan": plan, "ranks": [{k: np.array(v, copy=True) for k, v in rank_shards[r].items()}
+                                                  for r in range(plan.n_d)]}
+
+
+def param_values_any(saved, k, name):
+    """Parameter k's values (row-major) from a save of either layout."""
+    from . import fsdp2
+
+    plan, ranks = saved["plan"], saved["ranks"]
+    if saved["kind"] == "fsdp1":
+        return param_values(plan, ranks, k, name)
+    p = plan.params[k]
+    offs, acc = [], 0
+    for u in plan.units:
+        offs.append(acc)
+        acc += u.shard
+    rows = []
+    for r in range(plan.n_d):
+        begin, count = fsdp2.local_rows(plan, k, r)
+        if count:
+            start = offs[p.unit] + p.off
+            rows.append(ranks[r][name][start:start + count * p.row])
+    return np.concatenate(rows)
+
+
+def load_any(saved, plan, kind, name, n_params):
+    """Rank-local shards of `name` for `plan` (kind "fsdp1" or "fsdp2") from a save of either layout."""
+    from . import fsdp2
+
+    values = [param_values_any(saved, k, name) for k in range(n_params)]
+    full = []
+    for ui in range(len(plan.units)):
+        if kind == "fsdp2":
+            full.append(fsdp2.chunk_cat(plan, ui, values))
+        else:
+            u = plan.units[ui]
+            flat = np.zeros(u.padded, dtype=values[0].dtype)
+            for k in range(n_params):
+                if plan.param_unit[k] == ui:
+                    off = plan.param_offset[k] - u.base
+                    flat[off:off + values[k].size] = values[k]
+            full.append(flat)
+    out = []
+    for r in range(plan.n_d):
+        pieces = []
+        for ui, u in enumerate(plan.units):
+            shard = u.shard
+            pieces.append(full[ui][r * shard:(r + 1) * shard])
+        out.append(np.concatenate(pieces))
+    return out

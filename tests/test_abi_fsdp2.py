@@ -2,8 +2,6 @@
 
 import random
 
-import pytest
-
 import fsdp_sharded_optimizer_flatparameter_gb300 as zs
 from oracle import fsdp2
 
@@ -61,10 +59,3 @@ def test_memory_accounting_counts_the_padded_rows():
     assert p.shard_per_rank == 11
     assert p.memory_bytes(3) == 16 * 11
     assert p.comm_bytes(1) == 2 * 2 * 3 * 11
-
-
-def test_checkpoint_refuses_fsdp2_plans(tmp_path):
-    p = zs.Plan([(4, 2)], 2, layout=zs.ZS_LAYOUT_FSDP2)
-    with pytest.raises(zs.ZsError) as e:
-        zs.zs_checkpoint_save(p, str(tmp_path), 16, 16, 16, 16, 1, stream=0)
-    assert e.value.status == zs.ZS_ERR_UNSUPPORTED

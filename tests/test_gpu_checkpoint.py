@@ -14,7 +14,7 @@ import torch
 import fsdp_sharded_optimizer_flatparameter_gb300 as zs
 import gpu_helpers as H
 from fsdp_sharded_optimizer_flatparameter_gb300 import synth
-from oracle import checkpoint, layout, steps
+from oracle import checkpoint, layout, numerics, steps
 
 pytestmark = pytest.mark.gpu
 
@@ -101,3 +101,83 @@ def test_load_refuses_other_model_and_broken_files(tmp_path):
     assert "wrong size" in str(e.value)
     with pytest.raises(zs.ZsError):
         zs.zs_checkpoint_load(plan, str(tmp_path / "missing"), *[torch.zeros_like(a) for a in arrays])
+
+
+@pytest.mark.parametrize("src_layout,n_src,src_units,dst_layout,n_dst,dst_units", [
+    ("fsdp1", 8, True, "fsdp2", 3, False),
+    ("fsdp2", 4, True, "fsdp1", 5, True),
+    ("fsdp2", 6, False, "fsdp2", 16, True),
+    ("fsdp1", 2, False, "fsdp1", 7, True),
+])
+def test_load_into_another_layout_and_grouping(tmp_path, src_layout, n_src, src_units, dst_layout, n_dst, dst_units):
+    """A save in one layout (FSDP1 FlatParameter or FSDP2 Shard(0)), rank count and unit grouping
+    loads into another; every array equals the oracle's element-identity reload, bit for bit."""
+    from oracle import fsdp2
+
+    shapes, units = _model()
+    lay = {"fsdp1": zs.ZS_LAYOUT_FSDP1, "fsdp2": zs.ZS_LAYOUT_FSDP2}
+
+    def plans(kind, n_d, grouped):
+        u = units if grouped else None
+        ours = zs.Plan(shapes, n_d, stage=3 if grouped else 1, unit_of_param=u, layout=lay[kind])
+        ref = layout.make_plan(shapes, n_d, unit_of_param=u) if kind == "fsdp1" else \
+            fsdp2.make_plan(shapes, n_d, unit_of_param=u)
+        return ours, ref
+
+    src, ref_src = plans(src_layout, n_src, src_units)
+    dst, ref_dst = plans(dst_layout, n_dst, dst_units)
+    # inputs in the source layout, built on the host by the oracle from per-parameter values
+    nrng = np.random.default_rng(n_src * 31 + n_dst)
+    nat = {name: [(nrng.standard_normal(int(np.prod(s))) * sc).astype(np.float32) for s in shapes]
+           for name, sc in (("master", 0.02), ("m", 1e-4), ("v", 1e-6))}
+    nat["v"] = [np.abs(x) for x in nat["v"]]
+
+    def lay_out(kind, ref, values):
+        if kind == "fsdp2":
+            return np.concatenate([fsdp2.chunk_cat(ref, u, values) for u in range(len(ref.units))])
+        full = np.zeros(ref.padded, np.float32)
+        for k, x in enumerate(values):
+            full[ref.param_offset[k]:ref.param_offset[k] + x.size] = x
+        return full
+
+    host = {name: lay_out(src_layout, ref_src, nat[name]) for name in nat}
+    params_bits = numerics.bf16_rne(host["master"])
+    dev_arrays = [H.from_np_bf16(params_bits)] + [torch.from_numpy(host[n]).to(DEV) for n in ("master", "m", "v")]
+    zs.zs_checkpoint_save(src, str(tmp_path), *dev_arrays, step=4)
+
+    P = dst.padded
+    out = [torch.full((P,), 3, dtype=BF16, device=DEV)] + [torch.full((P,), 3.0, device=DEV) for _ in range(3)]
+    assert zs.zs_checkpoint_load(dst, str(tmp_path), *out) == 4
+    saved = checkpoint.save_any(ref_src, src_layout, [
+        {"params": _rank_slice(ref_src, src_layout, r, params_bits),
+         **{n: _rank_slice(ref_src, src_layout, r, host[n]) for n in ("master", "m", "v")}}
+        for r in range(n_src)])
+    n_params = len(shapes)
+    for i, name in enumerate(("params", "master", "m", "v")):
+        want = checkpoint.load_any(saved, ref_dst, dst_layout, name, n_params)
+        got = H.to_np_bf16(out[0]) if i == 0 else H.to_np_f32(out[i])
+        full_want = np.concatenate([_unshard_any(ref_dst, dst_layout, want)])
+        assert np.array_equal(got.view(np.uint16 if i == 0 else np.uint32),
+                              full_want.view(np.uint16 if i == 0 else np.uint32)), name
+
+
+def _rank_slice(ref, kind, r, full):
+    """Rank r's shard (all units) of a flat array laid out by `ref`."""
+    pieces = []
+    for u in ref.units:
+        shard = u.shard
+        base = u.base
+        pieces.append(full[base + r * shard:base + (r + 1) * shard])
+    return np.concatenate(pieces)
+
+
+def _unshard_any(ref, kind, rank_arrays):
+    full = np.zeros(ref.padded, dtype=rank_arrays[0].dtype)
+    offs, acc = [], 0
+    for u in ref.units:
+        offs.append(acc)
+        acc += u.shard
+    for ui, u in enumerate(ref.units):
+        for r in range(ref.n_d):
+            full[u.base + r * u.shard:u.base + (r + 1) * u.shard] = rank_arrays[r][offs[ui]:offs[ui] + u.shard]
+    return full

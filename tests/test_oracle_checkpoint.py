@@ -86,3 +86,46 @@ def test_load_rejects_another_model():
     saved = checkpoint.save(p, [{"master": np.zeros(p.shard_total, np.float32)} for _ in range(2)])
     with pytest.raises(ValueError):
         checkpoint.load(layout.make_plan([(4,), (7,)], 2), saved, "master")
+
+
+def _fsdp2_shards(plan2, params):
+    from oracle import fsdp2
+    out = [[] for _ in range(plan2.n_d)]
+    for ui, u in enumerate(plan2.units):
+        flat = fsdp2.chunk_cat(plan2, ui, [p.reshape(-1) for p in params])
+        for r in range(plan2.n_d):
+            out[r].append(flat[r * u.shard:(r + 1) * u.shard])
+    return [np.concatenate(x) for x in out]
+
+
+def test_any_layout_to_any_layout():
+    """Save in FSDP1 or FSDP2 with one rank count and unit grouping, load into the other layout with
+    another rank count and grouping: every parameter reads back unchanged, padding is zero."""
+    from oracle import fsdp2
+
+    rng = random.Random(9)
+    for _ in range(40):
+        n = rng.randint(1, 6)
+        shapes = [tuple(rng.randint(1, 6) for _ in range(rng.randint(1, 3))) for _ in range(n)]
+        params = [np.random.default_rng(rng.randint(0, 10 ** 6)).standard_normal(s).astype(np.float32) + 3
+                  for s in shapes]
+        state = None
+        for step in range(4):
+            kind = rng.choice(["fsdp1", "fsdp2"])
+            n_d = rng.randint(1, 7)
+            units = sorted(rng.randint(0, 2) for _ in range(n))
+            remap = {u: i for i, u in enumerate(sorted(set(units)))}
+            units = [remap[u] for u in units]
+            plan = layout.make_plan(shapes, n_d, unit_of_param=units) if kind == "fsdp1" else \
+                fsdp2.make_plan(shapes, n_d, unit_of_param=units)
+            if state is None:
+                shards = _shard_params(plan, params) if kind == "fsdp1" else _fsdp2_shards(plan, params)
+            else:
+                shards = checkpoint.load_any(state, plan, kind, "x", n)
+            for k, p in enumerate(params):
+                saved_now = checkpoint.save_any(plan, kind, [{"x": s} for s in shards])
+                assert np.array_equal(checkpoint.param_values_any(saved_now, k, "x"), p.reshape(-1))
+            total = sum(s.size for s in shards)
+            assert total == plan.padded
+            assert np.count_nonzero(np.concatenate(shards)) == sum(p.size for p in params)   # padding is zero
+            state = checkpoint.save_any(plan, kind, [{"x": s} for s in shards])
