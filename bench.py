@@ -500,12 +500,30 @@ def run_ours(args, ws, rank, local):
     return 0
 
 
+def all_ranks_ok(dist, ok, device):
+    """True when every rank reports ok (so no rank enters a collective the others skip)."""
+    if dist is None:
+        return ok
+    import torch
+
+    t = torch.tensor([1.0 if ok else 0.0], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return t.item() > 0.5
+
+
 def measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws):
     """Both host-fed paths; returns (faster, other)."""
-    host_g = torch.empty((n_d, P), dtype=torch.bfloat16, pin_memory=True)
+    try:
+        host_g = torch.empty((n_d, P), dtype=torch.bfloat16, pin_memory=True)
+        host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+        ok, why = True, ""
+    except (RuntimeError, MemoryError) as exc:          # e.g. pinned host memory exhausted
+        host_g = host_out = None
+        ok, why = False, str(exc)[:200]
+    if not all_ranks_ok(dist, ok, dev):
+        raise RuntimeError("pinned host buffers unavailable on some rank" + (": " + why if why else ""))
     for q in range(n_d):
         host_g[q].copy_(W.grads[q])
-    host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
     hrows = [host_g[q] for q in range(n_d)]
     n_e2e = max(2, min(steps, 5))
 
