@@ -34,8 +34,10 @@ def _worker(rank, world, port, out):
     try:
         # each rank's elapsed time differs; every rank must see the slowest one
         got = bench.max_over_ranks(dist, 10.0 + 5.0 * rank, "cpu")
+        # a rank that cannot take part makes every rank skip the collective-bearing section
+        agree = (bench.all_ranks_ok(dist, True, "cpu"), bench.all_ranks_ok(dist, rank == 0, "cpu"))
         dist.barrier()
-        out[rank] = got
+        out[rank] = (got, agree)
     finally:
         dist.destroy_process_group()
 
@@ -45,7 +47,7 @@ def test_max_over_ranks_gloo_world_size_2():
     manager = mp.Manager()
     out = manager.dict()
     mp.start_processes(_worker, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
-    assert dict(out) == {0: 15.0, 1: 15.0}
+    assert dict(out) == {0: (15.0, (True, False)), 1: (15.0, (True, False))}
 
 
 def test_reference_arm_under_torchrun_prints_once():
