@@ -351,6 +351,95 @@ class Workload:
                              main_stream=st, side_stream=self.side)
 
 
+def run_sweep(args, ws, rank, local):
+    """The 2^28+7-element flat buffer: the fused step for every N_d of the sweep, and the bucket-wise
+    ZeRO-2 step (one fused launch per bucket, descending) for every bucket size at N_d = 8."""
+    import torch
+
+    import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = maybe_init_dist(ws, "nccl")
+    stream = torch.cuda.current_stream(dev)
+    wl = synth.WORKLOADS["flat-sweep"]
+    shapes, _ = synth.workload_params(wl["model"])
+    hp = synth.HPARAMS
+    peak, peak_kind = hbm_peak()
+    steps = max(3, args.steps)
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(dist, a.elapsed_time(b) / n, dev)
+
+    points, launches = [], 0
+    sampler = ClockSampler(local)
+    sampler.start()
+    for n_d in wl["sweep_n_d"]:
+        plan = zs.Plan(shapes, n_d, stage=2, bucket_bytes=wl["bucket_bytes"])
+        P, pads = plan.padded, plan.pad_ranges()
+        master = synth.master_init(P, pads, wl["seed"], device=dev)
+        m, v = torch.zeros_like(master), torch.zeros_like(master)
+        grads, _ = synth.rank_buffers(n_d, P, torch.bfloat16, dev)
+        synth.fill_grads(grads, pads, wl["seed"], 1, wl["sigma"])
+        reps, _ = synth.rank_buffers(n_d, P, torch.bfloat16, dev)
+        t = [0]
+
+        def fused():
+            t[0] += 1
+            zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, t[0], stream=stream)
+
+        ms = timed(fused, steps)
+        launches += steps
+        gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
+        points.append({"n_d": n_d, "padding": P - plan.numel, "step": "fused, whole buffer", "ms": ms,
+                       "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
+        if n_d == 8:
+            for mib in wl["sweep_bucket_mib"]:
+                bp = zs.Plan(shapes, n_d, stage=2, bucket_bytes=mib << 20)
+
+                def bucketwise(bp=bp):
+                    t[0] += 1
+                    for b in reversed(range(bp.n_buckets)):
+                        zs.zs_fused_step(bp, b, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, t[0], stream=stream)
+
+                ms = timed(bucketwise, steps)
+                launches += steps * bp.n_buckets
+                gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
+                points.append({"n_d": n_d, "bucket_mib": mib, "buckets": bp.n_buckets,
+                               "step": "fused, bucket by bucket (descending)", "ms": ms,
+                               "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
+        del master, m, v, grads, reps
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
+    head = next(p for p in points if p["n_d"] == 8 and "bucket_mib" not in p)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": ws * head["params_per_s"], "unit": "params/s", "n_gpus": ws, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": head["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "flat-sweep", "params": 2 ** 28 + 7, "n_d": 8,
+                       "l2": "every step moves >= 10 GB >> 129 MB L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": head["gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
+            "sweep": points, "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def run_ours(args, ws, rank, local):
     import torch
 
@@ -592,10 +681,12 @@ def main():
     if args.warmup < 3 and args.impl == "ours" and not args.profile_case:
         log("note: fewer than 3 warm-up steps")
     if args.steps is None:
-        args.steps = 20 if "zero3" in args.workload else 200
+        args.steps = 20 if "zero3" in args.workload else (10 if args.workload == "flat-sweep" else 200)
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, ws, rank)
+    if args.workload == "flat-sweep":
+        return run_sweep(args, ws, rank, local)
     return run_ours(args, ws, rank, local)
 
 

@@ -130,6 +130,9 @@ WORKLOADS = {
                              outlier_p=1e-3, seed=2, steps=1, micro=1),
     "llama-7b-zero3": dict(model="llama-7b", n_d=16, stage=3, bucket_bytes=0, sigma=5e-4, outlier_p=0.0,
                            seed=3, steps=1, micro=1),
+    "flat-sweep": dict(model="flat-2^28+7", n_d=8, stage=2, bucket_bytes=1 << 20, sigma=1e-3, outlier_p=0.0,
+                       seed=4, steps=1, micro=1, sweep_n_d=(2, 4, 8, 16, 32),
+                       sweep_bucket_mib=(1, 4, 16, 64, 256, 1024)),
 }
 
 HPARAMS = {"lr": 1e-3, "beta1": 0.9, "beta2": 0.95, "eps": 1e-8, "weight_decay": 0.1}
