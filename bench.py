@@ -407,16 +407,17 @@ def run_sweep(args, ws, rank, local):
             for mib in wl["sweep_bucket_mib"]:
                 bp = zs.Plan(shapes, n_d, stage=2, bucket_bytes=mib << 20)
 
-                def bucketwise(bp=bp):
+                order = list(reversed(range(bp.n_buckets)))
+
+                def bucketwise(bp=bp, order=order):
                     t[0] += 1
-                    for b in reversed(range(bp.n_buckets)):
-                        zs.zs_fused_step(bp, b, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, t[0], stream=stream)
+                    zs.zs_fused_step_buckets(bp, order, grads, master, m, v, reps, hp, t[0], stream=stream)
 
                 ms = timed(bucketwise, steps)
                 launches += steps * bp.n_buckets
                 gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
                 points.append({"n_d": n_d, "bucket_mib": mib, "buckets": bp.n_buckets,
-                               "step": "fused, bucket by bucket (descending)", "ms": ms,
+                               "step": "fused, one launch per bucket (descending), zs_fused_step_buckets", "ms": ms,
                                "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
         del master, m, v, grads, reps
         torch.cuda.empty_cache()

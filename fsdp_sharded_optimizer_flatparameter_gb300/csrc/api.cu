@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdio>
 #include <string>
+#include <vector>
 
 #include "launch.h"
 #include "plan.h"
@@ -251,6 +252,42 @@ extern "C" int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* 
     zs::clear_error();
     return fused_common("zs_fused_step", plan, bucket, grads, grads_kind, master, m, v, replicas, hp, step,
                         as_stream(stream));
+}
+
+extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buckets,
+                                     const void* const* grads, float* master, float* m, float* v,
+                                     void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream) {
+    static const char* fn = "zs_fused_step_buckets";
+    zs::TraceRange trace_(fn);
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    if (n_buckets < 0 || (n_buckets > 0 && !buckets)) return fail(fn, "bad bucket list");
+    std::vector<char> seen(plan->buckets.size(), 0);
+    for (int32_t i = 0; i < n_buckets; ++i) {
+        ZS_TRY(check_bucket(fn, plan, buckets[i], false));
+        if (seen[buckets[i]]) return fail(fn, "a bucket appears twice (it would be updated twice)");
+        seen[buckets[i]] = 1;
+    }
+    // validate everything once through the single-bucket path's checks, then launch bucket by bucket
+    const int nd = plan->n_d;
+    ZS_TRY(check_one(fn, "master", master));
+    ZS_TRY(check_one(fn, "m", m));
+    ZS_TRY(check_one(fn, "v", v));
+    zs::AdamScalars s;
+    ZS_TRY(check_hp(fn, hp, step, &s));
+    BView g, o;
+    ZS_TRY(make_view(fn, "grads", grads, ZS_RANK_FULL, nd, 0, 0, &g));
+    ZS_TRY(make_view(fn, "replicas", (const void* const*)replicas, ZS_RANK_FULL, nd, 0, 0, &o));
+    for (int q = 0; q < nd; ++q)
+        for (int j = 0; j < nd; ++j)
+            if (replicas[q] == grads[j]) return fail(fn, "replicas must not be the gradient buffers");
+    for (int32_t i = 0; i < n_buckets; ++i) {
+        const auto& bk = plan->buckets[buckets[i]];
+        if (bk.end <= bk.begin) continue;
+        ZS_TRY(cuda_status(fn, zs::launch_fused(g, master, m, v, o, true, {bk.begin, bk.end, 0, 1}, s, nd,
+                                                as_stream(stream))));
+    }
+    return ZS_OK;
 }
 
 extern "C" int zs_fused_step_host(zs_plan_t plan, const void* const* host_grads, void* const* dev_grads,

@@ -424,8 +424,11 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
                          const Range& r, const AdamScalars& s, int nd, cudaStream_t st, bool allow_staged) {
     const bool vec = aligned8(g.off) && aligned8(out.off);
     const Split sp = split_range(r.lo, r.hi, vec);
-    bool staged_nd = allow_staged && (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
-    if (staged_nd) {
+    const bool want_tma = g_fused_variant == ZS_FUSED_TMA ||
+                          (g_fused_variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
+    bool staged = want_tma && sp.nvec > 0 && allow_staged &&
+                  (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
+    if (staged) {                       // only a staged candidate pays for the pointer queries
         const void* ps[2 * ZS_MAX_RANKS + 3];
         int n = 0;
         for (int q = 0; q < nd; ++q) ps[n++] = g.ptr.p[q];
@@ -433,11 +436,9 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
         ps[n++] = master;
         ps[n++] = m;
         ps[n++] = v;
-        staged_nd = all_device(ps, n);
+        staged = all_device(ps, n);
     }
-    const bool want_tma = g_fused_variant == ZS_FUSED_TMA ||
-                          (g_fused_variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
-    if (!(want_tma && staged_nd && sp.nvec > 0)) return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);
+    if (!staged) return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);
     // staged body, then the at most 14 fringe elements one by one
     const int64_t body_hi = sp.vlo + (sp.nvec << 3);
     cudaError_t e = launch_fused_tma(g, master, m, v, out, broadcast, sp.vlo, sp.nvec << 3, s, nd, st);

@@ -326,6 +326,16 @@ int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int3
                   float* master, float* m, float* v, void* const* replicas,
                   const zs_adamw_hparams* hp, int64_t step, void* stream);
 
+/* zs_fused_step for a list of buckets (ZS_RANK_FULL gradients), one launch per
+ * bucket in the order given - e.g. the buckets whose gradients became ready
+ * together, last layer first.  Same results as calling zs_fused_step once per
+ * bucket, with the argument checks and the per-call overhead paid once.
+ * Errors: ZS_ERR_INVALID (bad or repeated bucket index, or any check of
+ * zs_fused_step; nothing enqueued), ZS_ERR_CUDA. */
+int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buckets,
+                          const void* const* grads, float* master, float* m, float* v,
+                          void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream);
+
 /* zs_fused_step over the whole flat space with the gradients in HOST memory
  * (pinned for overlap): enqueues one host-to-device copy per rank into
  * dev_grads (ZS_RANK_FULL, caller-owned device staging), the fused step, and a

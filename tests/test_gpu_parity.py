@@ -622,3 +622,26 @@ def test_guard_zones_untouched_large_kernels():
     assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
     for raw, g in bufs:
         assert bool((raw[:g] == 0x5A).all()) and bool((raw[-g:] == 0x5A).all())
+
+
+def test_fused_step_buckets_equals_whole_range():
+    """zs_fused_step_buckets (all buckets, descending, one launch each) equals the whole-range step; a
+    repeated bucket is refused before anything runs."""
+    plan, _ = _plans([(3_000_011,)], 8, bucket_bytes=1 << 20)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=62, device=DEV)
+    a, b = State(master0), State(master0)
+    ra = synth.rank_buffers(8, P, BF16, DEV)[0]
+    rb = synth.rank_buffers(8, P, BF16, DEV)[0]
+    grads, _ = synth.rank_grads(8, P, pads, seed=62, step=1, sigma=1e-3, device=DEV)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *a.args(), ra, HP, 1)
+    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), grads, *b.args(), rb, HP, 1)
+    torch.cuda.synchronize()
+    for x, y in zip(a.args(), b.args()):
+        assert torch.equal(x, y)
+    assert all(torch.equal(x, y) for x, y in zip(ra, rb))
+    before = b.master.clone()
+    with pytest.raises(zs.ZsError):
+        zs.zs_fused_step_buckets(plan, [0, 1, 0], grads, *b.args(), rb, HP, 2)
+    torch.cuda.synchronize()
+    assert torch.equal(b.master, before)
