@@ -395,29 +395,32 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
     a.inv_nd = 1.0f / (float)nd;
     a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
     a.drain_limit = 4000000000LL;
-// Shapes per rank count, chosen by measurement on GB300 (1.3B-element buffers): consumer warps,
-// elements per thread, stage cap, shared-memory budget (115712 bytes lets two CTAs share an SM).
-// The single-output form (ZeRO-3 update, standalone AdamW with N_d = 1) is read-heavy and prefers
-// wider tiles with a shallow ring.
+// Shapes per rank count, chosen by measurement on GB300 (a grid of warps x elements per thread x
+// ring depth per rank count and output form, on 2^28-element buffers, then the leaders re-timed
+// three times interleaved): consumer warps, elements per thread, stage cap, shared-memory budget
+// (the ring takes min(cap, what fits); 115712 bytes lets two CTAs share an SM).  The single-output
+// form (ZeRO-3 update, standalone AdamW with N_d = 1) is read-heavy: at N_d = 8 the broadcast
+// shape reaches only ~74 % there, while three small CTAs per SM (2 warps x 512, 4 stages) stream
+// at the copy rate.
 #define ZS_TMA(ND_, NCW_, VPT_, MAXST_, BUDGET_, BROADCAST_) \
     return tma_impl<ND_, NCW_, VPT_, BROADCAST_, MAXST_, BUDGET_>(a, st)
     if (broadcast) {
         switch (nd) {
             case 2: ZS_TMA(2, 8, 8, 4, 232448, true);     // T 2048, 4 stages, 1 CTA/SM
-            case 4: ZS_TMA(4, 8, 4, 5, 115712, true);     // T 1024, 5 stages, 2 CTAs/SM
+            case 4: ZS_TMA(4, 8, 8, 3, 232448, true);     // T 2048, 3 stages, 1 CTA/SM
             case 8: ZS_TMA(8, 4, 8, 8, 232448, true);     // T 1024, 8 stages, 1 CTA/SM
-            case 16: ZS_TMA(16, 4, 4, 5, 115712, true);   // T 512, 5 stages, 2 CTAs/SM
-            case 32: ZS_TMA(32, 4, 4, 2, 115712, true);   // T 512, 2 stages, 2 CTAs/SM
+            case 16: ZS_TMA(16, 8, 4, 3, 232448, true);   // T 1024, 3 stages, 1 CTA/SM
+            case 32: ZS_TMA(32, 2, 8, 3, 232448, true);   // T 512, 3 stages, 1 CTA/SM
             default: return cudaErrorNotSupported;
         }
     }
     switch (nd) {
         case 1: ZS_TMA(1, 4, 8, 8, 115712, false);        // T 1024, 8 stages, 2 CTAs/SM
-        case 2: ZS_TMA(2, 8, 8, 4, 232448, false);
-        case 4: ZS_TMA(4, 8, 4, 5, 115712, false);
-        case 8: ZS_TMA(8, 4, 8, 8, 232448, false);
+        case 2: ZS_TMA(2, 8, 8, 4, 232448, false);        // T 2048, 4 stages, 1 CTA/SM
+        case 4: ZS_TMA(4, 8, 8, 3, 232448, false);        // T 2048, 3 stages, 1 CTA/SM
+        case 8: ZS_TMA(8, 2, 8, 4, 232448, false);        // T 512, 4 stages, 3 CTAs/SM
         case 16: ZS_TMA(16, 4, 8, 2, 115712, false);      // T 1024, 2 stages, 2 CTAs/SM
-        case 32: ZS_TMA(32, 4, 4, 2, 115712, false);
+        case 32: ZS_TMA(32, 4, 4, 2, 115712, false);      // T 512, 2 stages, 2 CTAs/SM
         default: return cudaErrorNotSupported;
     }
 #undef ZS_TMA
