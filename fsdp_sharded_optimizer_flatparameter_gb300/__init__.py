@@ -131,6 +131,7 @@ class Plan:
 
     def __init__(self, shapes, n_d, stage=ZS_STAGE_ZERO1, bucket_bytes=0, unit_of_param=None, layout=ZS_LAYOUT_FSDP1):
         self._h = None
+        self._members = self._param_numel = None
         self.shapes = [tuple(int(d) for d in s) for s in shapes]
         shapes = [tuple(int(d) for d in s) for s in shapes]
         n = len(shapes)
@@ -196,6 +197,22 @@ class Plan:
         _check(_lib.zs_plan_param_segment(self._h, int(k), int(rank), ctypes.byref(a), ctypes.byref(b),
                                           ctypes.byref(c)))
         return a.value, b.value, c.value
+
+    def unit_members(self, u):
+        """Indices of the parameters of unit u, in order (tabulated on first use; the plan is immutable)."""
+        if self._members is None:
+            members, numel = [[] for _ in range(self.n_units)], []
+            for k in range(len(self.shapes)):
+                unit, _, n = self.param(k)
+                members[unit].append(k)
+                numel.append(n)
+            self._members, self._param_numel = members, numel
+        return self._members[int(u)]
+
+    def param_numel(self, k):
+        if self._param_numel is None:
+            self.unit_members(0)
+        return self._param_numel[int(k)]
 
     def memory_bytes(self, stage=None):
         out = c_i64()
@@ -470,7 +487,9 @@ def zs_dp_step(plan, grads, master, m, v, replicas, hp, step, stream=None):
 
 
 def _unit_params(plan, unit):
-    return [k for k in range(len(plan.shapes)) if plan.param(k)[0] == unit]
+    if not 0 <= int(unit) < plan.n_units:
+        raise ZsError(ZS_ERR_INVALID, "unit %d out of range" % int(unit))
+    return plan.unit_members(unit)
 
 
 def zs_fsdp2_chunk_cat(plan, unit, params, flat, stream=None):
@@ -478,7 +497,7 @@ def zs_fsdp2_chunk_cat(plan, unit, params, flat, stream=None):
     members = _unit_params(plan, unit)
     if len(params) != len(members):
         raise ValueError("expected %d parameters for unit %d" % (len(members), unit))
-    ptrs = [_addr(x, plan.param(k)[2], 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
+    ptrs = [_addr(x, plan.param_numel(k), 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
     return _check(_lib.zs_fsdp2_chunk_cat(plan.handle, int(unit), (c_vp * max(len(ptrs), 1))(*ptrs),
                                           _addr(flat, plan.unit(unit)["padded"], 2, "flat"), _stream(stream)))
 
@@ -487,7 +506,7 @@ def zs_fsdp2_copy_out(plan, unit, flat, params, stream=None):
     members = _unit_params(plan, unit)
     if len(params) != len(members):
         raise ValueError("expected %d parameters for unit %d" % (len(members), unit))
-    ptrs = [_addr(x, plan.param(k)[2], 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
+    ptrs = [_addr(x, plan.param_numel(k), 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
     return _check(_lib.zs_fsdp2_copy_out(plan.handle, int(unit), _addr(flat, plan.unit(unit)["padded"], 2, "flat"),
                                          (c_vp * max(len(ptrs), 1))(*ptrs), _stream(stream)))
 

@@ -15,9 +15,13 @@
 // zs_fsdp2_chunk_cat builds the buffer from the parameters (the reduce-scatter
 // input built from each rank's gradients); zs_fsdp2_copy_out writes the
 // gathered buffer back into the parameters.  A launch covers up to kPerLaunch
-// parameters; blockIdx.y picks the parameter, blockIdx.z the rank and
-// blockIdx.x / threadIdx.x stride over the run.  Runs whose two ends share
-// their 16-byte phase move 8 bf16 values per access after a short scalar head.
+// parameters.  Every (parameter, rank) piece is cut into tasks of kTask
+// elements of the buffer side and each CTA takes one task, so the work is
+// balanced whatever the mix of parameter sizes (a 2-element norm next to a
+// 65M-element embedding); the CTA finds its piece by binary search over the
+// launch's prefix of task counts.  Runs whose two ends share their 16-byte
+// phase move 8 bf16 values per access, every thread issuing all of its loads
+// before its stores; other runs copy element by element.
 #include <string>
 
 #include "launch.h"
@@ -29,20 +33,25 @@ namespace {
 
 constexpr int kPerLaunch = 64;
 constexpr int kCopyThreads = 256;
+constexpr int kBatch = 8;                                   // 16-byte accesses in flight per thread
+constexpr int64_t kTask = (int64_t)kCopyThreads * kBatch * 8;  // 16384 elements per CTA
 
 struct Piece {
     uint16_t* param;        // the parameter's own layout (d0 x row elements)
     int64_t d0, row, chunk, off;
+    int64_t tasks;          // tasks per rank: ceil(chunk * row / kTask)
 };
 
 struct CopyArgs {
     Piece p[kPerLaunch];
+    int64_t first[kPerLaunch + 1];  // first[j] = sum over pieces before j of tasks * N_d
+    int n;                  // pieces in this launch
     uint16_t* flat;         // the group's buffer (N_d * shard elements)
     int64_t shard;
     int to_flat;            // 1: parameters -> buffer (zero padding rows), 0: buffer -> parameters
 };
 
-__device__ __forceinline__ void copy_run(uint16_t* dst, const uint16_t* src, int64_t n, int64_t t, int64_t stride) {
+__device__ __forceinline__ void copy_run(uint16_t* dst, const uint16_t* src, int64_t n, int t, int stride) {
     if ((((uintptr_t)dst ^ (uintptr_t)src) & 15) == 0) {
         const int64_t head = (int64_t)(((16 - ((uintptr_t)dst & 15)) & 15) >> 1);
         const int64_t h = head < n ? head : n;
@@ -50,32 +59,56 @@ __device__ __forceinline__ void copy_run(uint16_t* dst, const uint16_t* src, int
         const int64_t nv = (n - h) >> 3;
         const uint4* s4 = reinterpret_cast<const uint4*>(src + h);
         uint4* d4 = reinterpret_cast<uint4*>(dst + h);
-        for (int64_t i = t; i < nv; i += stride) __stcs(d4 + i, __ldcs(s4 + i));
+        for (int64_t b = t; b < nv; b += (int64_t)kBatch * stride) {
+            uint4 r[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int64_t i = b + (int64_t)k * stride;
+                if (i < nv) r[k] = __ldcs(s4 + i);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int64_t i = b + (int64_t)k * stride;
+                if (i < nv) __stcs(d4 + i, r[k]);
+            }
+        }
         for (int64_t i = h + (nv << 3) + t; i < n; i += stride) dst[i] = src[i];
     } else {
         for (int64_t i = t; i < n; i += stride) dst[i] = src[i];
     }
 }
 
-__device__ __forceinline__ void zero_run(uint16_t* dst, int64_t n, int64_t t, int64_t stride) {
+__device__ __forceinline__ void zero_run(uint16_t* dst, int64_t n, int t, int stride) {
     for (int64_t i = t; i < n; i += stride) dst[i] = 0;
 }
 
 __global__ void __launch_bounds__(kCopyThreads) k_fsdp2_copy(const __grid_constant__ CopyArgs a) {
-    const Piece& pc = a.p[blockIdx.y];
-    const int64_t r = blockIdx.z;
+    const int64_t task = blockIdx.x;
+    int lo = 0, hi = a.n - 1;                                 // last j with first[j] <= task
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.first[mid] <= task) lo = mid; else hi = mid - 1;
+    }
+    const Piece& pc = a.p[lo];
+    const int64_t k = task - a.first[lo];
+    const int64_t r = k / pc.tasks;                           // rank
+    const int64_t tk = k - r * pc.tasks;                      // task within the piece
     const int64_t begin = r * pc.chunk < pc.d0 ? r * pc.chunk : pc.d0;
     const int64_t end = (r + 1) * pc.chunk < pc.d0 ? (r + 1) * pc.chunk : pc.d0;
     const int64_t n = (end - begin) * pc.row;                 // real elements of this piece
+    const int64_t len = pc.chunk * pc.row;                    // buffer elements of this piece
+    const int64_t x0 = tk * kTask;
+    const int64_t x1 = x0 + kTask < len ? x0 + kTask : len;
     uint16_t* buf = a.flat + r * a.shard + pc.off;
     uint16_t* par = pc.param + begin * pc.row;
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t c1 = x1 < n ? x1 : n;                       // [x0, c1) real, [max(x0, n), x1) padding
+    const int t = threadIdx.x, stride = blockDim.x;
     if (a.to_flat) {
-        copy_run(buf, par, n, t, stride);
-        zero_run(buf + n, pc.chunk * pc.row - n, t, stride);  // padding rows
-    } else {
-        copy_run(par, buf, n, t, stride);
+        if (c1 > x0) copy_run(buf + x0, par + x0, c1 - x0, t, stride);
+        const int64_t z0 = x0 > n ? x0 : n;
+        if (x1 > z0) zero_run(buf + z0, x1 - z0, t, stride);
+    } else if (c1 > x0) {
+        copy_run(par + x0, buf + x0, c1 - x0, t, stride);
     }
 }
 
@@ -98,28 +131,25 @@ int fsdp2_copy(const char* fn, zs_plan_t plan, int32_t unit, void* const* params
         if (!params[j] || ((uintptr_t)params[j] & 1)) return fail(fn, "a parameter pointer is NULL or not 2-byte aligned");
     if ((uintptr_t)flat & 1) return fail(fn, "flat is not 2-byte aligned");
     const zs::Unit& un = plan->units[unit];
-    int sms = 0, dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     for (size_t first = 0; first < members.size(); first += kPerLaunch) {
         const size_t cnt = members.size() - first < (size_t)kPerLaunch ? members.size() - first : (size_t)kPerLaunch;
         CopyArgs a{};
-        int64_t longest = 1;
+        a.first[0] = 0;
         for (size_t j = 0; j < cnt; ++j) {
             const int32_t k = members[first + j];
+            const int64_t len = plan->param_chunk[k] * plan->param_row[k];
+            const int64_t tasks = std::max<int64_t>(1, (len + kTask - 1) / kTask);
             a.p[j] = {(uint16_t*)params[first + j], plan->param_d0[k], plan->param_row[k], plan->param_chunk[k],
-                      plan->param_piece_off[k]};
-            longest = std::max<int64_t>(longest, plan->param_chunk[k] * plan->param_row[k]);
+                      plan->param_piece_off[k], tasks};
+            a.first[j + 1] = a.first[j] + tasks * plan->n_d;
         }
+        a.n = (int)cnt;
         a.flat = (uint16_t*)flat;
         a.shard = un.shard;
         a.to_flat = to_flat;
-        // enough blocks along x for the longest run, about two waves over the whole grid
-        int64_t bx = (longest / 8 + kCopyThreads - 1) / kCopyThreads;
-        const int64_t cap = std::max<int64_t>(1, (int64_t)sms * 16 / (int64_t)(cnt * plan->n_d));
-        bx = std::max<int64_t>(1, std::min(bx, cap));
-        dim3 grid((unsigned)bx, (unsigned)cnt, (unsigned)plan->n_d);
-        k_fsdp2_copy<<<grid, kCopyThreads, 0, st>>>(a);
+        const int64_t total = a.first[cnt];
+        if (total > 0x7fffffffLL) return fail(fn, "unit too large for one launch");
+        k_fsdp2_copy<<<(unsigned)total, kCopyThreads, 0, st>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error(std::string(fn) + ": " + cudaGetErrorString(e));
