@@ -351,9 +351,24 @@ class Workload:
                              main_stream=st, side_stream=self.side)
 
 
+def timed_on_stream(torch, fn, steps, warmup, stream, dev, dist):
+    """Mean ms per call over `steps` calls after `warmup`, CUDA events on `stream`, max over ranks."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return max_over_ranks(dist, a.elapsed_time(b) / steps, dev)
+
+
 def run_sweep(args, ws, rank, local):
-    """The 2^28+7-element flat buffer: the fused step for every N_d of the sweep, and the bucket-wise
-    ZeRO-2 step (one fused launch per bucket, descending) for every bucket size at N_d = 8."""
+    """The 2^28+7-element flat buffer: the fused ZeRO-1/2 step and the ZeRO-3 step for every N_d of
+    the sweep, and the bucket-wise ZeRO-2 step (one fused launch per bucket, descending) for every
+    bucket size at N_d = 8."""
     import torch
 
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
@@ -370,16 +385,7 @@ def run_sweep(args, ws, rank, local):
     steps = max(3, args.steps)
 
     def timed(fn, n):
-        for _ in range(args.warmup):
-            fn()
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return max_over_ranks(dist, a.elapsed_time(b) / n, dev)
+        return timed_on_stream(torch, fn, n, args.warmup, stream, dev, dist)
 
     points, launches = [], 0
     sampler = ClockSampler(local)
@@ -403,6 +409,23 @@ def run_sweep(args, ws, rank, local):
         gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
         points.append({"n_d": n_d, "padding": P - plan.numel, "step": "fused, whole buffer", "ms": ms,
                        "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
+        # ZeRO-3 on the same buffer (one unit): forward gather, backward gather, reduce-scatter + update
+        p3 = zs.Plan(shapes, n_d, stage=3, bucket_bytes=wl["bucket_bytes"])
+        shards = master.to(torch.bfloat16)
+        extra, _ = synth.rank_buffers(n_d, P, torch.bfloat16, dev)
+        side = torch.cuda.Stream(dev)
+
+        def zero3():
+            t[0] += 1
+            zs.zs_zero3_step(p3, shards, master, m, v, [grads], [reps, extra], True, hp, t[0],
+                             main_stream=stream, side_stream=side)
+
+        ms = timed(zero3, steps)
+        launches += 3 * steps
+        gbs = P * (2 * (2 + 2 * n_d) + (2 * n_d + 26)) / (ms / 1e3) / 1e9
+        points.append({"n_d": n_d, "stage": 3, "step": "ZeRO-3: 2 gathers + reduce-scatter/update (one unit)",
+                       "ms": ms, "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
+        del shards, extra
         if n_d == 8:
             for mib in wl["sweep_bucket_mib"]:
                 bp = zs.Plan(shapes, n_d, stage=2, bucket_bytes=mib << 20)
@@ -422,7 +445,7 @@ def run_sweep(args, ws, rank, local):
         del master, m, v, grads, reps
         torch.cuda.empty_cache()
     clocks = sampler.stop()
-    head = next(p for p in points if p["n_d"] == 8 and "bucket_mib" not in p)
+    head = next(p for p in points if p["n_d"] == 8 and p["step"] == "fused, whole buffer")
     if rank == 0:
         line = {
             "metric": METRIC, "value": ws * head["params_per_s"], "unit": "params/s", "n_gpus": ws, "steps": steps,
@@ -433,6 +456,202 @@ def run_sweep(args, ws, rank, local):
             "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": head["gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
             "sweep": points, "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_next(args, ws, rank, local):
+    """The widening rows on their own shapes, each against its algorithmic bytes:
+    naive DP (all-reduce-mean, replicated update) on GPT-2-small at N_d = 8; ZeRO-3 with and
+    without reshard_after_forward on Llama-1.3B (one unit per layer + root) at N_d = 8; the FSDP2
+    Shard(0) layout on the same grouping (gradient chunk-cat, fused step, copy-out); and a sharded
+    checkpoint of GPT-2-small saved at N_d = 8 and reloaded at N_d = 8 and N_d = 4."""
+    import shutil
+    import tempfile
+
+    import torch
+
+    import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = maybe_init_dist(ws, "nccl")
+    stream = torch.cuda.current_stream(dev)
+    hp = synth.HPARAMS
+    peak, peak_kind = hbm_peak()
+    steps = max(3, args.steps)
+    bf16 = torch.bfloat16
+    rows, launches = [], 0
+
+    def timed(fn):
+        return timed_on_stream(torch, fn, steps, args.warmup, stream, dev, dist)
+
+    def row(name, ms, numel, nbytes, n_launch, **extra):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        rows.append(dict(row=name, ms=ms, params_per_s=numel / (ms / 1e3), algorithmic_bytes=nbytes, gbs=gbs,
+                         frac=gbs / peak, launches_per_step=n_launch, **extra))
+
+    sampler = ClockSampler(local)
+    sampler.start()
+
+    # naive DP on GPT-2-small, N_d = 8: every rank holds and updates the whole fp32 state
+    n_d = 8
+    shapes, _ = synth.workload_params("gpt2-small")
+    plan = zs.Plan(shapes, n_d, stage=0)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads, _ = synth.rank_buffers(n_d, P, bf16, dev)
+    synth.fill_grads(grads, pads, 1, 1, 1e-3)
+    reps, _ = synth.rank_buffers(n_d, P, bf16, dev)
+    master0 = synth.master_init(P, pads, 1, device=dev)
+    master = [master0.clone() for _ in range(n_d)]
+    mm = [torch.zeros_like(master0) for _ in range(n_d)]
+    vv = [torch.zeros_like(master0) for _ in range(n_d)]
+    t = [0]
+
+    def dp():
+        t[0] += 1
+        zs.zs_dp_step(plan, grads, master, mm, vv, reps, hp, t[0], stream=stream)
+
+    row("naive DP step (k_dp_step: all-reduce-mean + replicated AdamW), GPT-2-small, N_d=8", timed(dp), plan.numel,
+        28 * n_d * P, 1)
+    launches += steps
+
+    def ar():
+        zs.zs_all_reduce_mean(plan, -1, grads, stream=stream)
+
+    row("naive DP all-reduce-mean alone (k_all_reduce_mean), GPT-2-small, N_d=8", timed(ar), plan.numel,
+        4 * n_d * P, 1)
+    launches += steps
+    z_master, z_m, z_v = master0.clone(), torch.zeros_like(master0), torch.zeros_like(master0)
+
+    def zero():
+        t[0] += 1
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, z_master, z_m, z_v, reps, hp, t[0], stream=stream)
+
+    row("ZeRO-1/2 fused step on the same buffers, for comparison", timed(zero), plan.numel,
+        bytes_per_padded_element(n_d, "fused") * P, 1)
+    launches += steps
+    state_dp, state_zero = plan.memory_bytes(0), plan.memory_bytes(2)
+    del grads, reps, master, mm, vv, z_master, z_m, z_v
+
+    # sharded checkpoint of GPT-2-small: save at N_d = 8, reload at N_d = 8 and (resharded) N_d = 4
+    plan8 = zs.Plan(shapes, 8, stage=1)
+    plan4 = zs.Plan(shapes, 4, stage=1)
+    sh = master0.to(bf16)
+    cm, cv = torch.zeros_like(master0), torch.zeros_like(master0)
+    tmp = tempfile.mkdtemp(prefix="zs_ckpt_")
+    try:
+        def wall(fn):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            return (time.perf_counter() - t0) * 1e3
+        ckpt_bytes = 14 * plan8.numel
+        ms = min(wall(lambda: zs.zs_checkpoint_save(plan8, tmp, sh, master0, cm, cv, 7, stream=stream))
+                 for _ in range(3))
+        row("checkpoint save (N_d=8 shards -> files), GPT-2-small", ms, plan8.numel, ckpt_bytes, 0, timing="wall clock")
+        ms = min(wall(lambda: zs.zs_checkpoint_load(plan8, tmp, sh, master0, cm, cv, stream=stream))
+                 for _ in range(3))
+        row("checkpoint load, same N_d=8", ms, plan8.numel, ckpt_bytes, 0, timing="wall clock")
+        P4 = plan4.padded
+        sh4 = torch.empty(P4, dtype=bf16, device=dev)
+        m4, c4m, c4v = (torch.empty(P4, dtype=torch.float32, device=dev) for _ in range(3))
+        ms = min(wall(lambda: zs.zs_checkpoint_load(plan4, tmp, sh4, m4, c4m, c4v, stream=stream))
+                 for _ in range(3))
+        row("checkpoint load resharded to N_d=4", ms, plan4.numel, ckpt_bytes, 0, timing="wall clock")
+        del sh4, m4, c4m, c4v
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    del sh, cm, cv, master0
+
+    # ZeRO-3 on Llama-1.3B (24 layer units + root), N_d = 8, with and without resharding after forward
+    shapes, units = synth.workload_params("llama-1.3b-units")
+    plan = zs.Plan(shapes, n_d, stage=3, unit_of_param=units)
+    P, U = plan.padded, plan.n_units
+    biggest = max(plan.unit(u)["padded"] for u in range(U))
+    master = synth.master_init(P, plan.pad_ranges(), 2, device=dev)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    shards = master.to(bf16)
+    ugrads, _ = synth.rank_buffers(n_d, biggest, bf16, dev)
+    synth.fill_grads(ugrads, [], 2, 1, 5e-4)
+    side = torch.cuda.Stream(dev)
+    pool = [synth.rank_buffers(n_d, biggest, bf16, dev)[0] for _ in range(U)]
+    for reshard in (True, False):
+        slots = pool[:2] if reshard else pool
+
+        def z3(slots=slots, reshard=reshard):
+            t[0] += 1
+            zs.zs_zero3_step(plan, shards, master, m, v, [ugrads] * U, slots, reshard, hp, t[0],
+                             main_stream=stream, side_stream=side)
+
+        gathers = 2 if reshard else 1
+        row("ZeRO-3 step, Llama-1.3B, N_d=8, reshard_after_forward=%s" % reshard, timed(z3), plan.numel,
+            P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), (gathers + 1) * U,
+            comm_bytes_per_rank=plan.comm_bytes(3, reshard))
+        launches += steps * (gathers + 1) * U
+    del master, m, v, shards, ugrads, pool
+
+    # FSDP2 Shard(0) layout on the same grouping: per rank gradient chunk-cat, fused step, copy-out
+    plan = zs.Plan(shapes, n_d, stage=2, unit_of_param=units, layout=zs.ZS_LAYOUT_FSDP2)
+    P, pads = plan.padded, plan.pad_ranges()
+    master = synth.master_init(P, pads, 2, device=dev)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    grads, _ = synth.rank_buffers(n_d, P, bf16, dev)
+    reps, _ = synth.rank_buffers(n_d, P, bf16, dev)
+    params = [torch.empty(s, dtype=bf16, device=dev).normal_(0, 1e-3) for s in shapes]
+    members = [[k for k in range(len(shapes)) if units[k] == u] for u in range(plan.n_units)]
+    unit_base = [plan.unit(u)["base"] for u in range(plan.n_units)]
+    unit_pad = [plan.unit(u)["padded"] for u in range(plan.n_units)]
+
+    def chunk_cat(q=0):
+        for u in range(plan.n_units):
+            zs.zs_fsdp2_chunk_cat(plan, u, [params[k] for k in members[u]],
+                                  grads[q][unit_base[u]:unit_base[u] + unit_pad[u]], stream=stream)
+
+    def copy_out(q=0):
+        for u in range(plan.n_units):
+            zs.zs_fsdp2_copy_out(plan, u, reps[q][unit_base[u]:unit_base[u] + unit_pad[u]],
+                                 [params[k] for k in members[u]], stream=stream)
+
+    for q in range(n_d):
+        chunk_cat(q)
+    layout_launches = sum((len(mem) + 63) // 64 for mem in members)
+    row("FSDP2 gradient chunk-cat, one rank's full gradient -> group buffers (k_fsdp2_copy), Llama-1.3B units",
+        timed(chunk_cat), plan.numel, 2 * plan.numel + 2 * P, layout_launches)
+    launches += steps * layout_launches
+
+    def f2():
+        t[0] += 1
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, t[0], stream=stream)
+
+    row("FSDP2 layout fused step, Llama-1.3B units, N_d=8", timed(f2), plan.numel,
+        bytes_per_padded_element(n_d, "fused") * P, 1, padding=P - plan.numel)
+    launches += steps
+    row("FSDP2 copy-out, group buffers -> one rank's parameters (k_fsdp2_copy)", timed(copy_out), plan.numel,
+        2 * plan.numel * 2, layout_launches)
+    launches += steps * layout_launches
+    del master, m, v, grads, reps, params
+    torch.cuda.empty_cache()
+    clocks = sampler.stop()
+
+    head = next(r for r in rows if r["row"].startswith("FSDP2 layout fused step"))
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": ws * head["params_per_s"], "unit": "params/s", "n_gpus": ws, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": head["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "next-rows", "head": head["row"], "n_d": n_d,
+                       "l2": "every timed call moves >= 1 GB >> 129 MB L2, no flush",
+                       "naive_dp_state_bytes_per_rank": state_dp, "zero2_state_bytes_per_rank": state_zero},
+            "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": head["gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
+            "rows": rows, "gpu_launches": launches, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -682,12 +901,14 @@ def main():
     if args.warmup < 3 and args.impl == "ours" and not args.profile_case:
         log("note: fewer than 3 warm-up steps")
     if args.steps is None:
-        args.steps = 20 if "zero3" in args.workload else (10 if args.workload == "flat-sweep" else 200)
+        args.steps = 20 if "zero3" in args.workload else (10 if args.workload in ("flat-sweep", "next-rows") else 200)
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     if args.workload == "flat-sweep":
         return run_sweep(args, ws, rank, local)
+    if args.workload == "next-rows":
+        return run_next(args, ws, rank, local)
     return run_ours(args, ws, rank, local)
 
 

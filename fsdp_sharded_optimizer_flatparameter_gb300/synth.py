@@ -11,7 +11,9 @@ Shapes (random-initialised stand-ins; no weights or datasets are used):
                  n_ctx=1024, tied embeddings, LayerNorms with bias
                  (124,439,808).
 * ``llama-1.3b`` 24 layers, d=2048, SwiGLU ffn 5504, 16 heads (MHA), RMSNorm,
-                 vocab 32000, untied output (1,345,423,360).
+                 vocab 32000, untied output (1,345,423,360).  ``llama-1.3b-units``
+                 is the same list grouped one unit per layer plus a root unit
+                 (embedding, final norm, output), for ZeRO-3 and FSDP2 groups.
 * ``llama-7b``   32 layers, d=4096, ffn 11008, vocab 32000, untied
                  (6,738,415,616); one FSDP unit per layer plus a root unit
                  holding the embedding, final norm and output.
@@ -44,12 +46,16 @@ def workload_params(name):
             shapes += _layer_gpt2()
         shapes += [(768,), (768,)]
         return shapes, None
-    if name == "llama-1.3b":
-        shapes = [(32000, 2048)]
-        for _ in range(24):
-            shapes += _layer_llama(2048, 5504)
+    if name in ("llama-1.3b", "llama-1.3b-units"):
+        n_layers = 24
+        shapes, units = [(32000, 2048)], [n_layers]
+        for layer in range(n_layers):
+            ls = _layer_llama(2048, 5504)
+            shapes += ls
+            units += [layer] * len(ls)
         shapes += [(2048,), (32000, 2048)]
-        return shapes, None
+        units += [n_layers, n_layers]
+        return shapes, (units if name == "llama-1.3b-units" else None)
     if name == "llama-7b":
         n_layers = 32
         shapes, units = [(32000, 4096)], [n_layers]
