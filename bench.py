@@ -388,6 +388,7 @@ def run_sweep(args, ws, rank, local):
         return timed_on_stream(torch, fn, n, args.warmup, stream, dev, dist)
 
     points, launches = [], 0
+    side_bw = torch.cuda.Stream(dev)
     sampler = ClockSampler(local)
     sampler.start()
     for n_d in wl["sweep_n_d"]:
@@ -431,17 +432,19 @@ def run_sweep(args, ws, rank, local):
                 bp = zs.Plan(shapes, n_d, stage=2, bucket_bytes=mib << 20)
 
                 order = list(reversed(range(bp.n_buckets)))
+                for side in (None, side_bw):
 
-                def bucketwise(bp=bp, order=order):
-                    t[0] += 1
-                    zs.zs_fused_step_buckets(bp, order, grads, master, m, v, reps, hp, t[0], stream=stream)
+                    def bucketwise(bp=bp, order=order, side=side):
+                        t[0] += 1
+                        zs.zs_fused_step_buckets(bp, order, grads, master, m, v, reps, hp, t[0], stream=stream,
+                                                 side_stream=side)
 
-                ms = timed(bucketwise, steps)
-                launches += steps * bp.n_buckets
-                gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
-                points.append({"n_d": n_d, "bucket_mib": mib, "buckets": bp.n_buckets,
-                               "step": "fused, one launch per bucket (descending), zs_fused_step_buckets", "ms": ms,
-                               "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
+                    ms = timed(bucketwise, steps)
+                    launches += steps * bp.n_buckets
+                    gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
+                    points.append({"n_d": n_d, "bucket_mib": mib, "buckets": bp.n_buckets, "streams": 1 if side is None else 2,
+                                   "step": "fused, one launch per bucket (descending), zs_fused_step_buckets", "ms": ms,
+                                   "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
         del master, m, v, grads, reps
         torch.cuda.empty_cache()
     clocks = sampler.stop()

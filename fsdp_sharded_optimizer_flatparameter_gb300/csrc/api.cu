@@ -256,7 +256,8 @@ extern "C" int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* 
 
 extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buckets,
                                      const void* const* grads, float* master, float* m, float* v,
-                                     void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream) {
+                                     void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream,
+                                     void* side_stream) {
     static const char* fn = "zs_fused_step_buckets";
     zs::TraceRange trace_(fn);
     zs::clear_error();
@@ -281,13 +282,45 @@ extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const in
     for (int q = 0; q < nd; ++q)
         for (int j = 0; j < nd; ++j)
             if (replicas[q] == grads[j]) return fail(fn, "replicas must not be the gradient buffers");
-    for (int32_t i = 0; i < n_buckets; ++i) {
-        const auto& bk = plan->buckets[buckets[i]];
-        if (bk.end <= bk.begin) continue;
-        ZS_TRY(cuda_status(fn, zs::launch_fused(g, master, m, v, o, true, {bk.begin, bk.end, 0, 1}, s, nd,
-                                                as_stream(stream))));
+    std::vector<int32_t> todo;
+    for (int32_t i = 0; i < n_buckets; ++i)
+        if (plan->buckets[buckets[i]].end > plan->buckets[buckets[i]].begin) todo.push_back(buckets[i]);
+    if (todo.empty()) return ZS_OK;
+    // the same pointers serve every bucket: ask the runtime about them once
+    const zs::StagedPolicy pol =
+        zs::fused_ptrs_on_device(g, master, m, v, o, true, nd) ? zs::kStagedDeviceKnown : zs::kStagedNever;
+    cudaStream_t a = as_stream(stream);
+    cudaStream_t b = side_stream ? as_stream(side_stream) : a;
+    const bool two = b != a && todo.size() > 1;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    if (two) {
+        // buckets are disjoint, so consecutive ones may overlap: odd positions run on the side stream,
+        // which first waits for everything already enqueued on the caller's stream
+        ZS_TRY(cuda_status(fn, cudaEventCreateWithFlags(&fork, cudaEventDisableTiming)));
+        cudaError_t e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventRecord(fork, a);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(b, fork, 0);
+        if (e != cudaSuccess) {
+            cudaEventDestroy(fork);
+            if (join) cudaEventDestroy(join);
+            return cuda_status(fn, e);
+        }
     }
-    return ZS_OK;
+    cudaError_t err = cudaSuccess;
+    for (size_t i = 0; i < todo.size() && err == cudaSuccess; ++i) {
+        const auto& bk = plan->buckets[todo[i]];
+        err = zs::launch_fused(g, master, m, v, o, true, {bk.begin, bk.end, 0, 1}, s, nd, (two && (i & 1)) ? b : a,
+                               pol);
+    }
+    if (two) {
+        // join even after a failed launch, so later work on the caller's stream orders after the side stream
+        cudaError_t e = cudaEventRecord(join, b);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(a, join, 0);
+        if (err == cudaSuccess) err = e;
+        cudaEventDestroy(fork);
+        cudaEventDestroy(join);
+    }
+    return cuda_status(fn, err);
 }
 
 extern "C" int zs_fused_step_host(zs_plan_t plan, const void* const* host_grads, void* const* dev_grads,

@@ -420,24 +420,28 @@ static bool all_device(const void* const* ps, int n) {
     return true;
 }
 
+bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
+                          int nd) {
+    const void* ps[2 * ZS_MAX_RANKS + 3];
+    int n = 0;
+    for (int q = 0; q < nd; ++q) ps[n++] = g.ptr.p[q];
+    for (int q = 0; q < (broadcast ? nd : 1); ++q) ps[n++] = out.ptr.p[q];
+    ps[n++] = master;
+    ps[n++] = m;
+    ps[n++] = v;
+    return all_device(ps, n);
+}
+
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st, bool allow_staged) {
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st, StagedPolicy staged_policy) {
     const bool vec = aligned8(g.off) && aligned8(out.off);
     const Split sp = split_range(r.lo, r.hi, vec);
     const bool want_tma = g_fused_variant == ZS_FUSED_TMA ||
                           (g_fused_variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
-    bool staged = want_tma && sp.nvec > 0 && allow_staged &&
+    bool staged = want_tma && sp.nvec > 0 && staged_policy != kStagedNever &&
                   (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
-    if (staged) {                       // only a staged candidate pays for the pointer queries
-        const void* ps[2 * ZS_MAX_RANKS + 3];
-        int n = 0;
-        for (int q = 0; q < nd; ++q) ps[n++] = g.ptr.p[q];
-        for (int q = 0; q < (broadcast ? nd : 1); ++q) ps[n++] = out.ptr.p[q];
-        ps[n++] = master;
-        ps[n++] = m;
-        ps[n++] = v;
-        staged = all_device(ps, n);
-    }
+    // only a staged candidate pays for the pointer queries, and only when the caller has not
+    if (staged && staged_policy == kStagedIfDevice) staged = fused_ptrs_on_device(g, master, m, v, out, broadcast, nd);
     if (!staged) return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);
     // staged body, then the at most 14 fringe elements one by one
     const int64_t body_hi = sp.vlo + (sp.nvec << 3);

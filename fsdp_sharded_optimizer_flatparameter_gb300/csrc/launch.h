@@ -43,8 +43,14 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
                           const Range& r, int nd, cudaStream_t st);
 // The staged kernel runs only for 8-aligned ranges of supported rank counts whose buffers are all
 // device memory; allow_staged = false forces the register-streaming kernel.
+// Which fused kernel a launch may use.  kStagedIfDevice asks the runtime about every pointer;
+// kStagedDeviceKnown is for callers that already did (fused_ptrs_on_device) for the same pointers.
+enum StagedPolicy { kStagedNever = 0, kStagedIfDevice = 1, kStagedDeviceKnown = 2 };
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st, bool allow_staged = true);
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st,
+                         StagedPolicy staged_policy = kStagedIfDevice);
+// True when every pointer a fused launch over these views touches is device memory.
+bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast, int nd);
 
 // Bulk-copy staged fused kernel over the 8-aligned body [lo, lo + n); returns
 // cudaErrorNotSupported when no staged variant exists for this rank count.

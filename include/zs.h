@@ -329,12 +329,21 @@ int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int3
 /* zs_fused_step for a list of buckets (ZS_RANK_FULL gradients), one launch per
  * bucket in the order given - e.g. the buckets whose gradients became ready
  * together, last layer first.  Same results as calling zs_fused_step once per
- * bucket, with the argument checks and the per-call overhead paid once.
+ * bucket, with the argument checks, the pointer-kind queries and the per-call
+ * overhead paid once.  The update is element-wise and the buckets are disjoint,
+ * so their launches need no order among themselves: with a side_stream other
+ * than stream, the buckets at odd positions of the list run on side_stream
+ * (which first waits for all work enqueued on stream) and the next bucket's
+ * launch overlaps the end of the previous one; before returning, stream is
+ * made to wait for side_stream, so all of the step is ordered before later
+ * work on stream either way.  side_stream NULL or equal to stream: one stream.
+ * The call creates and releases two CUDA events (no device memory).
  * Errors: ZS_ERR_INVALID (bad or repeated bucket index, or any check of
  * zs_fused_step; nothing enqueued), ZS_ERR_CUDA. */
 int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buckets,
                           const void* const* grads, float* master, float* m, float* v,
-                          void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream);
+                          void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream,
+                          void* side_stream);
 
 /* zs_fused_step over the whole flat space with the gradients in HOST memory
  * (pinned for overlap): enqueues one host-to-device copy per rank into

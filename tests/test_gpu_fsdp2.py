@@ -30,6 +30,34 @@ def _bf16_param(rng, shape, scale):
     return numerics.bf16_rne((rng.standard_normal(n) * scale).astype(np.float32))
 
 
+@pytest.mark.parametrize("n_d", [3, 8])
+def test_chunk_cat_and_copy_out_large_pieces_and_many_params(n_d):
+    """Pieces spanning many 16K-element copy tasks, padding rows inside a task, rows of odd length
+    (element-wise path) and a group of more parameters than one launch takes (70 > 64)."""
+    big = [(1000, 33), (517, 64), (7,), (70000, 1), (4096, 8), ()]
+    small = [(rng_d0, 3) for rng_d0 in range(1, 65)]
+    shapes = big + small
+    units = [0] * len(big) + [1] * len(small)
+    plan = zs.Plan(shapes, n_d, unit_of_param=units, layout=zs.ZS_LAYOUT_FSDP2)
+    ref = fsdp2.make_plan(shapes, n_d, unit_of_param=units)
+    nrng = np.random.default_rng(n_d)
+    vals = [_bf16_param(nrng, s, 1.0) for s in shapes]
+    for u in range(plan.n_units):
+        members = [k for k in range(len(shapes)) if units[k] == u]
+        dev_params = [H.from_np_bf16(vals[k]).reshape(shapes[k]) for k in members]
+        flat = torch.full((plan.unit(u)["padded"],), -2.0, dtype=BF16, device=DEV)
+        zs.zs_fsdp2_chunk_cat(plan, u, dev_params, flat)
+        torch.cuda.synchronize()
+        want = fsdp2.chunk_cat(ref, u, vals)
+        assert np.array_equal(H.to_np_bf16(flat), want)
+        outs = [torch.full_like(x, 3.0) for x in dev_params]
+        zs.zs_fsdp2_copy_out(plan, u, flat, outs)
+        torch.cuda.synchronize()
+        back = fsdp2.copy_out(ref, u, want)
+        for x, k in zip(outs, members):
+            assert np.array_equal(H.to_np_bf16(x.reshape(-1)), back[k])
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_chunk_cat_and_copy_out_match_oracle(seed):
     rng = random.Random(seed)

@@ -624,24 +624,36 @@ def test_guard_zones_untouched_large_kernels():
         assert bool((raw[:g] == 0x5A).all()) and bool((raw[-g:] == 0x5A).all())
 
 
-def test_fused_step_buckets_equals_whole_range():
-    """zs_fused_step_buckets (all buckets, descending, one launch each) equals the whole-range step; a
-    repeated bucket is refused before anything runs."""
-    plan, _ = _plans([(3_000_011,)], 8, bucket_bytes=1 << 20)
+@pytest.mark.parametrize("bucket_bytes", [1 << 20, 4 << 20])
+@pytest.mark.parametrize("two_streams", [False, True])
+def test_fused_step_buckets_equals_whole_range(bucket_bytes, two_streams):
+    """zs_fused_step_buckets (all buckets, descending, one launch each; with a side stream the odd
+    positions overlap on it) equals the whole-range step; work enqueued on the caller's stream just
+    before the call is seen by both streams, and work enqueued right after it sees the whole step;
+    a repeated bucket is refused before anything runs."""
+    plan, _ = _plans([(3_000_011,)], 8, bucket_bytes=bucket_bytes)
     P, pads = plan.padded, plan.pad_ranges()
     master0 = synth.master_init(P, pads, seed=62, device=DEV)
     a, b = State(master0), State(master0)
     ra = synth.rank_buffers(8, P, BF16, DEV)[0]
     rb = synth.rank_buffers(8, P, BF16, DEV)[0]
-    grads, _ = synth.rank_grads(8, P, pads, seed=62, step=1, sigma=1e-3, device=DEV)
-    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *a.args(), ra, HP, 1)
-    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), grads, *b.args(), rb, HP, 1)
+    src, _ = synth.rank_grads(8, P, pads, seed=62, step=1, sigma=1e-3, device=DEV)
+    grads = synth.rank_buffers(8, P, BF16, DEV)[0]
+    side = torch.cuda.Stream() if two_streams else None
+    zs.zs_fused_step(plan, -1, src, zs.ZS_RANK_FULL, *a.args(), ra, HP, 1)
+    torch.cuda.synchronize()
+    for q in range(8):
+        grads[q].copy_(src[q])                      # on the caller's stream, still in flight at the call
+    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), grads, *b.args(), rb, HP, 1,
+                             side_stream=side)
+    after = [r.clone() for r in rb] + [x.clone() for x in b.args()]   # caller's stream, right after
     torch.cuda.synchronize()
     for x, y in zip(a.args(), b.args()):
         assert torch.equal(x, y)
     assert all(torch.equal(x, y) for x, y in zip(ra, rb))
+    assert all(torch.equal(x, y) for x, y in zip(ra + list(a.args()), after))
     before = b.master.clone()
     with pytest.raises(zs.ZsError):
-        zs.zs_fused_step_buckets(plan, [0, 1, 0], grads, *b.args(), rb, HP, 2)
+        zs.zs_fused_step_buckets(plan, [0, 1, 0], grads, *b.args(), rb, HP, 2, side_stream=side)
     torch.cuda.synchronize()
     assert torch.equal(b.master, before)
