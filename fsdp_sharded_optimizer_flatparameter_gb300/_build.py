@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzs.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "-I" + INCLUDE, "-I" + CSRC]
+COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall,-pthread", "-I" + INCLUDE, "-I" + CSRC]
 
 
 def cuda_home():
@@ -65,7 +65,7 @@ def build(verbose_ptxas=False, quiet=True):
                 sys.stderr.write(err)
     tmp = LIB + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-           "-Xlinker", "-rpath," + os.path.join(home, "lib64"), "-Xlinker", "--no-undefined"]
+           "-Xlinker", "-rpath," + os.path.join(home, "lib64"), "-Xlinker", "--no-undefined", "-lpthread"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), res.stderr))

@@ -19,15 +19,29 @@
 //                     the arrays and their element types
 //   rank-NNNNN.bin    rank r's shard of params (bf16), master, m, v (fp32), one after
 //                     another; each is the rank's piece of every unit, units in order
-// Both calls copy through a 64 MiB host buffer with cudaMemcpyAsync on the given
-// stream and synchronise that stream.
+// Transfers: both calls first wait for the caller's stream, then cut the data
+// into chunks of at most 16 MiB, each a contiguous byte range of one rank file
+// and of one device array, and share them out among worker threads (up to 16,
+// contiguous runs of chunks of equal total size, so each worker reads or writes
+// its files mostly sequentially).  A worker owns a non-blocking stream and two
+// pinned staging buffers: while it writes one chunk to its file with pwrite, the
+// device-to-host copy of its next chunk runs (save); while the host-to-device
+// copy of one chunk runs, it reads the next with pread (load).  The calls return
+// once every worker's copies have completed.
 #include <algorithm>
+#include <atomic>
 #include <cerrno>
 #include <cstdio>
 #include <cstring>
 #include <fstream>
+#include <mutex>
 #include <string>
+#include <thread>
 #include <vector>
+
+#include <fcntl.h>
+#include <sys/stat.h>
+#include <unistd.h>
 
 #include <cuda_runtime.h>
 
@@ -35,7 +49,8 @@
 
 namespace {
 
-constexpr size_t kChunk = size_t(64) << 20;            // host staging per copy
+constexpr size_t kChunk = size_t(16) << 20;            // bytes per transfer chunk (and per staging buffer)
+constexpr int kMaxWorkers = 16;
 const int kElemBytes[4] = {2, 4, 4, 4};
 
 int fail(const char* fn, const std::string& what, int code = ZS_ERR_INVALID) {
@@ -99,6 +114,172 @@ struct Layout {
     }
 };
 
+// One chunk: `bytes` bytes between file descriptor `fd` at `off` and device address `dev`.
+struct Xfer {
+    int fd;
+    int64_t off;
+    char* dev;
+    size_t bytes;
+};
+
+// Appends [off, off + bytes) <-> [dev, dev + bytes) as chunks of at most kChunk bytes, first
+// growing the last chunk when the range continues it on both sides.
+void add_chunks(std::vector<Xfer>& out, int fd, int64_t off, char* dev, size_t bytes) {
+    if (bytes && !out.empty()) {
+        Xfer& t = out.back();
+        if (t.fd == fd && t.off + (int64_t)t.bytes == off && t.dev + t.bytes == dev && t.bytes < kChunk) {
+            const size_t n = std::min(bytes, kChunk - t.bytes);
+            t.bytes += n;
+            off += (int64_t)n;
+            dev += n;
+            bytes -= n;
+        }
+    }
+    while (bytes) {
+        const size_t n = bytes < kChunk ? bytes : kChunk;
+        out.push_back({fd, off, dev, n});
+        off += (int64_t)n;
+        dev += n;
+        bytes -= n;
+    }
+}
+
+bool full_pwrite(int fd, const char* p, size_t n, int64_t off) {
+    while (n) {
+        const ssize_t w = ::pwrite(fd, p, n, (off_t)off);
+        if (w < 0 && errno == EINTR) continue;
+        if (w <= 0) return false;
+        p += w;
+        n -= (size_t)w;
+        off += w;
+    }
+    return true;
+}
+
+bool full_pread(int fd, char* p, size_t n, int64_t off) {
+    while (n) {
+        const ssize_t r = ::pread(fd, p, n, (off_t)off);
+        if (r < 0 && errno == EINTR) continue;
+        if (r <= 0) return false;
+        p += r;
+        n -= (size_t)r;
+        off += r;
+    }
+    return true;
+}
+
+struct Failure {
+    std::mutex mu;
+    std::atomic<bool> any{false};
+    std::string what;
+    int code = ZS_OK;
+    void set(const std::string& w, int c) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!any.load()) {
+            what = w;
+            code = c;
+            any.store(true);
+        }
+    }
+};
+
+// One worker: chunks [lo, hi) of `xs`, device <-> file through two pinned buffers on its own stream.
+void worker(const std::vector<Xfer>& xs, size_t lo, size_t hi, bool save, int device, Failure* fail) {
+    if (lo >= hi) return;
+    cudaStream_t st = nullptr;
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    char* buf[2] = {nullptr, nullptr};
+    auto cuda_fail = [&](cudaError_t e) { fail->set(cudaGetErrorString(e), ZS_ERR_CUDA); };
+    cudaError_t e = cudaSetDevice(device);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) e = cudaEventCreateWithFlags(&ev[b], cudaEventDisableTiming);
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) e = cudaHostAlloc((void**)&buf[b], kChunk, cudaHostAllocDefault);
+    if (e != cudaSuccess) cuda_fail(e);
+    if (save) {
+        // D2H of chunk i + 1 runs while chunk i is written out
+        if (e == cudaSuccess) e = cudaMemcpyAsync(buf[0], xs[lo].dev, xs[lo].bytes, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[0], st);
+        if (e != cudaSuccess && !fail->any.load()) cuda_fail(e);
+        for (size_t i = lo; i < hi && !fail->any.load(); ++i) {
+            const int b = (int)((i - lo) & 1);
+            if (i + 1 < hi) {
+                const int nb = b ^ 1;          // its last chunk was written out in the previous iteration
+                e = cudaMemcpyAsync(buf[nb], xs[i + 1].dev, xs[i + 1].bytes, cudaMemcpyDeviceToHost, st);
+                if (e == cudaSuccess) e = cudaEventRecord(ev[nb], st);
+                if (e != cudaSuccess) {
+                    cuda_fail(e);
+                    break;
+                }
+            }
+            e = cudaEventSynchronize(ev[b]);
+            if (e != cudaSuccess) {
+                cuda_fail(e);
+                break;
+            }
+            if (!full_pwrite(xs[i].fd, buf[b], xs[i].bytes, xs[i].off)) {
+                fail->set(std::string("write failed: ") + std::strerror(errno), ZS_ERR_INVALID);
+                break;
+            }
+        }
+    } else {
+        // pread of chunk i runs while the H2D copy of chunk i - 1 is in flight
+        for (size_t i = lo; i < hi && e == cudaSuccess && !fail->any.load(); ++i) {
+            const int b = (int)((i - lo) & 1);
+            if (i - lo >= 2) {                 // the copy out of this buffer two chunks ago must be done
+                e = cudaEventSynchronize(ev[b]);
+                if (e != cudaSuccess) {
+                    cuda_fail(e);
+                    break;
+                }
+            }
+            if (!full_pread(xs[i].fd, buf[b], xs[i].bytes, xs[i].off)) {
+                fail->set("short read from a rank file", ZS_ERR_INVALID);
+                break;
+            }
+            e = cudaMemcpyAsync(xs[i].dev, buf[b], xs[i].bytes, cudaMemcpyHostToDevice, st);
+            if (e == cudaSuccess) e = cudaEventRecord(ev[b], st);
+            if (e != cudaSuccess) cuda_fail(e);
+        }
+    }
+    // every copy of this worker has completed before its buffers go
+    if (st) {
+        cudaError_t se = cudaStreamSynchronize(st);
+        if (se != cudaSuccess) cuda_fail(se);
+    }
+    for (int b = 0; b < 2; ++b) {
+        if (buf[b]) cudaFreeHost(buf[b]);
+        if (ev[b]) cudaEventDestroy(ev[b]);
+    }
+    if (st) cudaStreamDestroy(st);
+}
+
+// Runs every chunk on up to kMaxWorkers threads; returns ZS_OK or the first failure (message set).
+int transfer(const char* fn, const std::vector<Xfer>& xs, bool save) {
+    if (xs.empty()) return ZS_OK;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
+    unsigned hw = std::thread::hardware_concurrency();
+    size_t W = std::min<size_t>({(size_t)kMaxWorkers, hw ? (size_t)hw : 1, xs.size()});
+    uint64_t total = 0;
+    for (const auto& x : xs) total += x.bytes;
+    // contiguous runs of chunks with about total / W bytes each
+    std::vector<size_t> cut(1, 0);
+    uint64_t acc = 0;
+    for (size_t i = 0; i < xs.size() && cut.size() < W; ++i) {
+        acc += xs[i].bytes;
+        if (acc * W >= total * cut.size()) cut.push_back(i + 1);
+    }
+    cut.push_back(xs.size());
+    Failure f;
+    std::vector<std::thread> threads;
+    for (size_t w = 0; w + 1 < cut.size(); ++w)
+        threads.emplace_back(worker, std::cref(xs), cut[w], cut[w + 1], save, device, &f);
+    for (auto& t : threads) t.join();
+    if (f.any.load()) return fail(fn, f.what, f.code);
+    return ZS_OK;
+}
+
 Layout layout_of(zs_plan_t p) {
     Layout L;
     L.n_d = p->n_d;
@@ -121,6 +302,10 @@ extern "C" int zs_checkpoint_save(zs_plan_t plan, const char* dir, const void* s
     cudaStream_t st = (cudaStream_t)stream;
     const std::string d(dir);
     {
+        cudaError_t e = cudaStreamSynchronize(st);   // the arrays as the caller's stream leaves them
+        if (e != cudaSuccess) return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
+    }
+    {
         std::ofstream meta(d + "/meta.txt");
         if (!meta) return fail(fn, "cannot write " + d + "/meta.txt: " + std::strerror(errno));
         meta << "zs-checkpoint 2\n";
@@ -136,34 +321,37 @@ extern "C" int zs_checkpoint_save(zs_plan_t plan, const char* dir, const void* s
         if (!meta) return fail(fn, "writing meta.txt failed");
     }
     const void* src[4] = {shards, master, m, v};
-    std::vector<char> buf(kChunk);
+    std::vector<int> fds(plan->n_d, -1);
+    auto close_all = [&]() {
+        bool ok = true;
+        for (int& fd : fds)
+            if (fd >= 0) {
+                ok = ::close(fd) == 0 && ok;
+                fd = -1;
+            }
+        return ok;
+    };
+    std::vector<Xfer> xs;
     for (int r = 0; r < plan->n_d; ++r) {
-        FILE* f = std::fopen(rank_file(d, r).c_str(), "wb");
-        if (!f) return fail(fn, "cannot write " + rank_file(d, r) + ": " + std::strerror(errno));
+        fds[r] = ::open(rank_file(d, r).c_str(), O_WRONLY | O_CREAT | O_TRUNC, 0644);
+        if (fds[r] < 0) {
+            const std::string why = std::strerror(errno);
+            close_all();
+            return fail(fn, "cannot write " + rank_file(d, r) + ": " + why);
+        }
+        int64_t off = 0;
         for (int a = 0; a < 4; ++a) {
             const int eb = kElemBytes[a];
             for (const auto& u : plan->units) {
-                const char* from = (const char*)src[a] + (size_t)(u.base + (int64_t)r * u.shard) * eb;
-                size_t left = (size_t)u.shard * eb;
-                while (left) {
-                    const size_t n = left < kChunk ? left : kChunk;
-                    cudaError_t e = cudaMemcpyAsync(buf.data(), from, n, cudaMemcpyDeviceToHost, st);
-                    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-                    if (e != cudaSuccess) {
-                        std::fclose(f);
-                        return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
-                    }
-                    if (std::fwrite(buf.data(), 1, n, f) != n) {
-                        std::fclose(f);
-                        return fail(fn, "short write to " + rank_file(d, r));
-                    }
-                    from += n;
-                    left -= n;
-                }
+                char* from = (char*)src[a] + (size_t)(u.base + (int64_t)r * u.shard) * eb;
+                add_chunks(xs, fds[r], off, from, (size_t)u.shard * eb);
+                off += u.shard * eb;
             }
         }
-        if (std::fclose(f) != 0) return fail(fn, "closing " + rank_file(d, r) + " failed");
     }
+    const int rc = transfer(fn, xs, true);
+    if (!close_all() && rc == ZS_OK) return fail(fn, "closing a rank file failed");
+    if (rc != ZS_OK) return rc;
     return ZS_OK;
 }
 
@@ -229,21 +417,24 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
     const Layout D = layout_of(plan);
 
     // ---- files
-    std::vector<FILE*> files(S.n_d, nullptr);
+    std::vector<int> fds(S.n_d, -1);
     auto close_all = [&]() {
-        for (auto f : files)
-            if (f) std::fclose(f);
+        for (int& fd : fds)
+            if (fd >= 0) {
+                ::close(fd);
+                fd = -1;
+            }
     };
     for (int r = 0; r < S.n_d; ++r) {
-        files[r] = std::fopen(rank_file(d, r).c_str(), "rb");
-        if (!files[r]) {
+        fds[r] = ::open(rank_file(d, r).c_str(), O_RDONLY);
+        if (fds[r] < 0) {
             close_all();
             return fail(fn, "cannot read " + rank_file(d, r));
         }
         int64_t want = 0;
         for (int a = 0; a < 4; ++a) want += saved_shard_total * kElemBytes[a];
-        std::fseek(files[r], 0, SEEK_END);
-        if ((int64_t)std::ftell(files[r]) != want) {
+        struct stat sb;
+        if (::fstat(fds[r], &sb) != 0 || (int64_t)sb.st_size != want) {
             close_all();
             return fail(fn, rank_file(d, r) + " has the wrong size");
         }
@@ -261,7 +452,14 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
         pad_b.resize(count);
         pad_e.resize(count);
     }
-    std::vector<char> buf(kChunk);
+    {
+        cudaError_t e = cudaStreamSynchronize(st);   // the caller's work on the arrays is done
+        if (e != cudaSuccess) {
+            close_all();
+            return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
+        }
+    }
+    std::vector<Xfer> xs;
     int64_t section = 0;                                   // byte offset of array a inside a rank file
     for (int a = 0; a < 4; ++a) {
         const int eb = kElemBytes[a];
@@ -278,35 +476,18 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
                 int64_t ps, pd, ls, ld;
                 S.locate(k, e0, &rs, &ps, &ls);
                 D.locate(k, e0, &rd, &pd, &ld);
-                int64_t len = std::min(ls, ld);
-                if (std::fseek(files[rs], (long)(section + ps * eb), SEEK_SET) != 0) {
-                    close_all();
-                    return fail(fn, "seek failed in " + rank_file(d, rs));
-                }
-                char* to = (char*)dst[a] + (size_t)D.global(k, rd, pd) * eb;
-                size_t left = (size_t)len * eb;
-                while (left) {
-                    const size_t n = left < kChunk ? left : kChunk;
-                    if (std::fread(buf.data(), 1, n, files[rs]) != n) {
-                        close_all();
-                        return fail(fn, "short read from " + rank_file(d, rs));
-                    }
-                    cudaError_t e = cudaMemcpyAsync(to, buf.data(), n, cudaMemcpyHostToDevice, st);
-                    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-                    if (e != cudaSuccess) {
-                        close_all();
-                        return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
-                    }
-                    to += n;
-                    left -= n;
-                }
+                const int64_t len = std::min(ls, ld);
+                add_chunks(xs, fds[rs], section + ps * eb, (char*)dst[a] + (size_t)D.global(k, rd, pd) * eb,
+                           (size_t)len * eb);
                 e0 += len;
             }
         }
         section += saved_shard_total * eb;
     }
+    const int rc = transfer(fn, xs, false);
     close_all();
-    cudaError_t e = cudaStreamSynchronize(st);
+    cudaError_t e = cudaStreamSynchronize(st);             // the padding memsets
+    if (rc != ZS_OK) return rc;
     if (e != cudaSuccess) return fail(fn, cudaGetErrorString(e), ZS_ERR_CUDA);
     if (step) *step = saved_step;
     return ZS_OK;

@@ -387,9 +387,11 @@ int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads
  * and dim-0 sizes) but may use another N_d, another unit grouping and the other
  * layout: every element keeps its place in its parameter, the target's padding is
  * zeroed.  `dir` must exist.  Arrays are ZS_SHARDED device arrays of plan's
- * padded_numel elements.  Both calls copy through a 64 MiB host buffer with
- * cudaMemcpyAsync on `stream` and synchronise it (they return after the data is
- * in place).
+ * padded_numel elements.  Both calls first synchronise `stream`, then move the
+ * data on up to 16 worker threads, each with its own non-blocking stream and two
+ * 16 MiB pinned host staging buffers (host memory, freed before returning; no
+ * device memory), overlapping file I/O with the copies; they return after the
+ * data is in place.
  * Errors: ZS_ERR_INVALID (NULL argument, I/O failure, a checkpoint of another
  * model or a malformed one: nothing is written to the device before the metadata
  * and file sizes are checked), ZS_ERR_CUDA. */
