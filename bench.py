@@ -84,14 +84,19 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("device.cuh", "launch.h", "kernels.cu", "kernels_tma.cu")
+# the files that define each profiled kernel: its code, its argument structs and its launch shape
+KERNEL_SOURCES = {
+    "k_fused_tma": ("device.cuh", "launch.h", "kernels_tma.cu"),
+    "k_gather_bulk": ("device.cuh", "launch.h", "kernels_tma.cu"),
+    "k_fused": ("device.cuh", "launch.h", "kernels.cu"),
+}
 
 
-def source_digest():
-    """Digest of the files that define the fused kernels (a profile is valid only for these sources)."""
+def source_digest(kernel_key):
+    """Digest of the files that define a kernel (a profile of it is valid only for these sources)."""
     csrc = os.path.join(ROOT, "fsdp_sharded_optimizer_flatparameter_gb300", "csrc")
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel_key]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -107,7 +112,7 @@ def profiled_traffic(workload, kernel_key):
                 if line.startswith("- ") and ":" in line:
                     k, v = line[2:].split(":", 1)
                     fields[k.strip()] = v.strip().strip("`")
-        if fields.get("source_digest") != source_digest():
+        if fields.get("source_digest") != source_digest(kernel_key):
             return None
         return float(fields["traffic_bytes_per_full_launch"])
     except Exception:
