@@ -520,18 +520,31 @@ struct DpStepOp {
 #pragma unroll
         for (int k = 0; k < VEC; ++k) acc[k] = mean_of_sum<ND>(acc[k], n, inv_nd);
         unpack(pack(acc), gr);                  // every rank receives the same bf16 mean
+        // and runs the same update on its own full state; two ranks per pass, both ranks' loads
+        // issued before either's stores (the stores may alias nothing the loads read, but the
+        // compiler cannot know that, so the order is written out)
 #pragma unroll 1
-        for (int q = 0; q < n; ++q) {           // and runs the same update on its own full state
-            float p[VEC], mm[VEC], vv[VEC];
-            ld_f32<VEC>(master.p[q] + i, p);
-            ld_f32<VEC>(m.p[q] + i, mm);
-            ld_f32<VEC>(v.p[q] + i, vv);
+        for (int q = 0; q < n; q += 2) {
+            const bool two = q + 1 < n;
+            float p[2][VEC], mm[2][VEC], vv[2][VEC];
+            ld_f32<VEC>(master.p[q] + i, p[0]);
+            ld_f32<VEC>(m.p[q] + i, mm[0]);
+            ld_f32<VEC>(v.p[q] + i, vv[0]);
+            if (two) {
+                ld_f32<VEC>(master.p[q + 1] + i, p[1]);
+                ld_f32<VEC>(m.p[q + 1] + i, mm[1]);
+                ld_f32<VEC>(v.p[q + 1] + i, vv[1]);
+            }
 #pragma unroll
-            for (int k = 0; k < VEC; ++k) adamw_elem(gr[k], p[k], mm[k], vv[k], s);
-            st_f32<VEC>(master.p[q] + i, p);
-            st_f32<VEC>(m.p[q] + i, mm);
-            st_f32<VEC>(v.p[q] + i, vv);
-            st_bf<VEC>(out.ptr.p[q] + (i - out.off), pack(p));
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !two) break;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) adamw_elem(gr[k], p[h][k], mm[h][k], vv[h][k], s);
+                st_f32<VEC>(master.p[q + h] + i, p[h]);
+                st_f32<VEC>(m.p[q + h] + i, mm[h]);
+                st_f32<VEC>(v.p[q + h] + i, vv[h]);
+                st_bf<VEC>(out.ptr.p[q + h] + (i - out.off), pack(p[h]));
+            }
         }
     }
 };

@@ -351,9 +351,10 @@ def test_staged_and_streaming_fused_kernels_agree_with_oracle(variant, n_d, nume
                 H.check_bf16(H.to_np_bf16(reps[v][q]), ref_reps[q], "variant %d replica %d" % (v, q))
 
 
-def test_staged_zero3_rs_step_matches_streaming(variant):
+@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
+def test_staged_zero3_rs_step_matches_streaming(variant, n_d):
+    """The single-output staged kernel (every rank count's own shape) equals the streaming kernel."""
     shapes, units = _tiny_llama(n_layers=2, d=256, ffn=704, vocab=1000)
-    n_d = 16
     plan, _ = _plans(shapes, n_d, units=units, stage=3)
     P, pads = plan.padded, plan.pad_ranges()
     master0 = synth.master_init(P, pads, seed=9, device=DEV)
