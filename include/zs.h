@@ -37,9 +37,12 @@
  *             master, m and v are always ZS_SHARDED fp32 arrays of
  *             padded_numel elements.
  * Ownership.  The caller owns all device memory and all streams.  The library
- *             never allocates device memory, never synchronises, and only
- *             enqueues work on the given stream (a cudaStream_t; NULL is the
- *             legacy default stream).  A plan owns host tables only.
+ *             never allocates device memory.  The step calls never
+ *             synchronise and enqueue work only on the streams they are given
+ *             (a cudaStream_t; NULL is the legacy default stream); calls that
+ *             use a second stream order it after the first with events.  The
+ *             checkpoint calls are the exception: they synchronise their stream
+ *             and return with the data in place.  A plan owns host tables only.
  * Alignment.  Every device pointer must be 16-byte aligned.
  * Aliasing.   Inputs and outputs must not overlap unless a call says so.
  * Step.       The AdamW step t is 1-based.
