@@ -13,6 +13,7 @@
 // parameter for the common powers of two so the rank loops unroll; other
 // counts use the runtime value.  Nothing here waits on anything, so no kernel
 // can hang.
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -296,7 +297,7 @@ static cudaError_t fused_impl(const BView& g, float* master, float* m, float* v,
 
 static bool aligned8(int64_t x) { return (x & 7) == 0; }
 static bool all_device(const void* const* ps, int n);
-static int g_fused_variant = ZS_FUSED_AUTO;
+static std::atomic<int> g_fused_variant{ZS_FUSED_AUTO};   // read by launches on any thread
 // Smallest body worth a persistent staged launch (below it the register-streaming kernel is as fast).
 constexpr int64_t kTmaMinElems = int64_t(1) << 20;
 
@@ -331,7 +332,7 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
     // reduced gradient and parameters both one array (ZeRO-2): the staged kernel with one rank is
     // exactly this update (the mean of one bf16 value is that value; a -0 gradient reads as +0,
     // which changes neither moment nor parameter)
-    if (!by_owner && (sp.nvec << 3) >= kTmaMinElems && g_fused_variant != ZS_FUSED_LDG) {
+    if (!by_owner && (sp.nvec << 3) >= kTmaMinElems && g_fused_variant.load() != ZS_FUSED_LDG) {
         const void* ps[5] = {grad.ptr.p[0], par.ptr.p[0], master, m, v};
         if (all_device(ps, 5)) {
             const int64_t body_hi = sp.vlo + (sp.nvec << 3);
@@ -389,8 +390,8 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
 #undef ZS_GA
 }
 
-void set_fused_variant(int v) { g_fused_variant = v; }
-int fused_variant() { return g_fused_variant; }
+void set_fused_variant(int v) { g_fused_variant.store(v); }
+int fused_variant() { return g_fused_variant.load(); }
 
 static cudaError_t launch_fused_ldg(const BView& g, float* master, float* m, float* v, const BView& out,
                                     bool broadcast, const Split& sp, const AdamScalars& s, int nd, cudaStream_t st) {
@@ -436,8 +437,8 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
                          const Range& r, const AdamScalars& s, int nd, cudaStream_t st, StagedPolicy staged_policy) {
     const bool vec = aligned8(g.off) && aligned8(out.off);
     const Split sp = split_range(r.lo, r.hi, vec);
-    const bool want_tma = g_fused_variant == ZS_FUSED_TMA ||
-                          (g_fused_variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
+    const int variant = g_fused_variant.load();
+    const bool want_tma = variant == ZS_FUSED_TMA || (variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
     bool staged = want_tma && sp.nvec > 0 && staged_policy != kStagedNever &&
                   (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
     // only a staged candidate pays for the pointer queries, and only when the caller has not
