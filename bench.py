@@ -507,9 +507,17 @@ def run_next(args, ws, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
 
+    # --profile-case: the same kernels on small shapes (a few GB on the device) for ncu captures
+    small = args.profile_case
+    unit_model = "llama-small-units" if small else "llama-1.3b-units"
+    unit_label = "Llama-small (profile case)" if small else "Llama-1.3B"
+    dp_label = "flat 2^24 (profile case)" if small else "GPT-2-small"
+
     # naive DP on GPT-2-small, N_d = 8: every rank holds and updates the whole fp32 state
     n_d = 8
     shapes, _ = synth.workload_params("gpt2-small")
+    if small:
+        shapes = [(1 << 24,)]
     plan = zs.Plan(shapes, n_d, stage=0)
     P, pads = plan.padded, plan.pad_ranges()
     grads, _ = synth.rank_buffers(n_d, P, bf16, dev)
@@ -525,14 +533,14 @@ def run_next(args, ws, rank, local):
         t[0] += 1
         zs.zs_dp_step(plan, grads, master, mm, vv, reps, hp, t[0], stream=stream)
 
-    row("naive DP step (k_dp_step: all-reduce-mean + replicated AdamW), GPT-2-small, N_d=8", timed(dp), plan.numel,
+    row("naive DP step (k_dp_step: all-reduce-mean + replicated AdamW), %s, N_d=8" % dp_label, timed(dp), plan.numel,
         28 * n_d * P, 1)
     launches += steps
 
     def ar():
         zs.zs_all_reduce_mean(plan, -1, grads, stream=stream)
 
-    row("naive DP all-reduce-mean alone (k_all_reduce_mean), GPT-2-small, N_d=8", timed(ar), plan.numel,
+    row("naive DP all-reduce-mean alone (k_all_reduce_mean), %s, N_d=8" % dp_label, timed(ar), plan.numel,
         4 * n_d * P, 1)
     launches += steps
     z_master, z_m, z_v = master0.clone(), torch.zeros_like(master0), torch.zeros_like(master0)
@@ -548,38 +556,42 @@ def run_next(args, ws, rank, local):
     del grads, reps, master, mm, vv, z_master, z_m, z_v
 
     # sharded checkpoint of GPT-2-small: save at N_d = 8, reload at N_d = 8 and (resharded) N_d = 4
-    plan8 = zs.Plan(shapes, 8, stage=1)
-    plan4 = zs.Plan(shapes, 4, stage=1)
-    sh = master0.to(bf16)
-    cm, cv = torch.zeros_like(master0), torch.zeros_like(master0)
-    tmp = tempfile.mkdtemp(prefix="zs_ckpt_")
-    try:
+    # (host I/O, so not part of the small case)
+    if not small:
+        plan8, plan4 = zs.Plan(shapes, 8, stage=1), zs.Plan(shapes, 4, stage=1)
+        sh = master0.to(bf16)
+        cm, cv = torch.zeros_like(master0), torch.zeros_like(master0)
+        P4 = plan4.padded
+        sh4 = torch.empty(P4, dtype=bf16, device=dev)
+        m4, c4m, c4v = (torch.empty(P4, dtype=torch.float32, device=dev) for _ in range(3))
+        ckpt_bytes = 14 * plan8.numel
+        tmp = tempfile.mkdtemp(prefix="zs_ckpt_")
+
         def wall(fn):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
             fn()
             torch.cuda.synchronize(dev)
             return (time.perf_counter() - t0) * 1e3
-        ckpt_bytes = 14 * plan8.numel
-        ms = min(wall(lambda: zs.zs_checkpoint_save(plan8, tmp, sh, master0, cm, cv, 7, stream=stream))
-                 for _ in range(3))
-        row("checkpoint save (N_d=8 shards -> files), GPT-2-small", ms, plan8.numel, ckpt_bytes, 0, timing="wall clock")
-        ms = min(wall(lambda: zs.zs_checkpoint_load(plan8, tmp, sh, master0, cm, cv, stream=stream))
-                 for _ in range(3))
-        row("checkpoint load, same N_d=8", ms, plan8.numel, ckpt_bytes, 0, timing="wall clock")
-        P4 = plan4.padded
-        sh4 = torch.empty(P4, dtype=bf16, device=dev)
-        m4, c4m, c4v = (torch.empty(P4, dtype=torch.float32, device=dev) for _ in range(3))
-        ms = min(wall(lambda: zs.zs_checkpoint_load(plan4, tmp, sh4, m4, c4m, c4v, stream=stream))
-                 for _ in range(3))
-        row("checkpoint load resharded to N_d=4", ms, plan4.numel, ckpt_bytes, 0, timing="wall clock")
-        del sh4, m4, c4m, c4v
-    finally:
-        shutil.rmtree(tmp, ignore_errors=True)
-    del sh, cm, cv, master0
+
+        try:
+            ms = min(wall(lambda: zs.zs_checkpoint_save(plan8, tmp, sh, master0, cm, cv, 7, stream=stream))
+                     for _ in range(3))
+            row("checkpoint save (N_d=8 shards -> files), GPT-2-small", ms, plan8.numel, ckpt_bytes, 0,
+                timing="wall clock")
+            ms = min(wall(lambda: zs.zs_checkpoint_load(plan8, tmp, sh, master0, cm, cv, stream=stream))
+                     for _ in range(3))
+            row("checkpoint load, same N_d=8", ms, plan8.numel, ckpt_bytes, 0, timing="wall clock")
+            ms = min(wall(lambda: zs.zs_checkpoint_load(plan4, tmp, sh4, m4, c4m, c4v, stream=stream))
+                     for _ in range(3))
+            row("checkpoint load resharded to N_d=4", ms, plan4.numel, ckpt_bytes, 0, timing="wall clock")
+        finally:
+            shutil.rmtree(tmp, ignore_errors=True)
+        del sh, cm, cv, sh4, m4, c4m, c4v
+    del master0
 
     # ZeRO-3 on Llama-1.3B (24 layer units + root), N_d = 8, with and without resharding after forward
-    shapes, units = synth.workload_params("llama-1.3b-units")
+    shapes, units = synth.workload_params(unit_model)
     plan = zs.Plan(shapes, n_d, stage=3, unit_of_param=units)
     P, U = plan.padded, plan.n_units
     biggest = max(plan.unit(u)["padded"] for u in range(U))
@@ -599,7 +611,7 @@ def run_next(args, ws, rank, local):
                              main_stream=stream, side_stream=side)
 
         gathers = 2 if reshard else 1
-        row("ZeRO-3 step, Llama-1.3B, N_d=8, reshard_after_forward=%s" % reshard, timed(z3), plan.numel,
+        row("ZeRO-3 step, %s, N_d=8, reshard_after_forward=%s" % (unit_label, reshard), timed(z3), plan.numel,
             P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), (gathers + 1) * U,
             comm_bytes_per_rank=plan.comm_bytes(3, reshard))
         launches += steps * (gathers + 1) * U
@@ -630,7 +642,7 @@ def run_next(args, ws, rank, local):
     for q in range(n_d):
         chunk_cat(q)
     layout_launches = sum((len(mem) + 63) // 64 for mem in members)
-    row("FSDP2 gradient chunk-cat, one rank's full gradient -> group buffers (k_fsdp2_copy), Llama-1.3B units",
+    row("FSDP2 gradient chunk-cat, one rank's full gradient -> group buffers (k_fsdp2_copy), %s units" % unit_label,
         timed(chunk_cat), plan.numel, 2 * plan.numel + 2 * P, layout_launches)
     launches += steps * layout_launches
 
@@ -638,7 +650,7 @@ def run_next(args, ws, rank, local):
         t[0] += 1
         zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, t[0], stream=stream)
 
-    row("FSDP2 layout fused step, Llama-1.3B units, N_d=8", timed(f2), plan.numel,
+    row("FSDP2 layout fused step, %s units, N_d=8" % unit_label, timed(f2), plan.numel,
         bytes_per_padded_element(n_d, "fused") * P, 1, padding=P - plan.numel)
     launches += steps
     row("FSDP2 copy-out, group buffers -> one rank's parameters (k_fsdp2_copy)", timed(copy_out), plan.numel,
@@ -654,7 +666,7 @@ def run_next(args, ws, rank, local):
             "metric": METRIC, "value": ws * head["params_per_s"], "unit": "params/s", "n_gpus": ws, "steps": steps,
             "warmup": args.warmup, "ms_per_step": head["ms"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "next-rows", "head": head["row"], "n_d": n_d,
+            "config": {"workload": "next-rows" + ("-profile-case" if small else ""), "head": head["row"], "n_d": n_d,
                        "l2": "every timed call moves >= 1 GB >> 129 MB L2, no flush",
                        "naive_dp_state_bytes_per_rank": state_dp, "zero2_state_bytes_per_rank": state_zero},
             "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": peak, "unit": "GB/s",

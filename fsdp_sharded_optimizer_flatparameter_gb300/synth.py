@@ -14,6 +14,9 @@ Shapes (random-initialised stand-ins; no weights or datasets are used):
                  vocab 32000, untied output (1,345,423,360).  ``llama-1.3b-units``
                  is the same list grouped one unit per layer plus a root unit
                  (embedding, final norm, output), for ZeRO-3 and FSDP2 groups.
+* ``llama-small-units`` 4 layers, d=1024, ffn 2816, vocab 32000, untied, one
+                 unit per layer plus the root unit (116,925,440): the same kernels as
+                 the Llama-1.3B grouping on a few GB, for profiler captures.
 * ``llama-7b``   32 layers, d=4096, ffn 11008, vocab 32000, untied
                  (6,738,415,616); one FSDP unit per layer plus a root unit
                  holding the embedding, final norm and output.
@@ -56,6 +59,16 @@ def workload_params(name):
         shapes += [(2048,), (32000, 2048)]
         units += [n_layers, n_layers]
         return shapes, (units if name == "llama-1.3b-units" else None)
+    if name == "llama-small-units":
+        n_layers = 4
+        shapes, units = [(32000, 1024)], [n_layers]
+        for layer in range(n_layers):
+            ls = _layer_llama(1024, 2816)
+            shapes += ls
+            units += [layer] * len(ls)
+        shapes += [(1024,), (32000, 1024)]
+        units += [n_layers, n_layers]
+        return shapes, units
     if name == "llama-7b":
         n_layers = 32
         shapes, units = [(32000, 4096)], [n_layers]
