@@ -372,8 +372,8 @@ def timed_on_stream(torch, fn, steps, warmup, stream, dev, dist):
 
 def run_sweep(args, ws, rank, local):
     """The 2^28+7-element flat buffer: the fused ZeRO-1/2 step and the ZeRO-3 step for every N_d of
-    the sweep, and the bucket-wise ZeRO-2 step (one fused launch per bucket, descending) for every
-    bucket size at N_d = 8."""
+    the sweep, and the bucket-wise ZeRO-2 step (every bucket, descending: walked by one launch, one
+    launch per bucket, and one launch per bucket on two streams) for every bucket size at N_d = 8."""
     import torch
 
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
@@ -437,18 +437,30 @@ def run_sweep(args, ws, rank, local):
                 bp = zs.Plan(shapes, n_d, stage=2, bucket_bytes=mib << 20)
 
                 order = list(reversed(range(bp.n_buckets)))
-                for side in (None, side_bw):
+                half = -(-bp.n_buckets // 2)
+                modes = (("one walk over the list (neighbours merge into one range)", zs.ZS_BUCKETS_ONE_WALK, None, 1),
+                         ("two walks: every other bucket, then the rest (disjoint runs, list kernel)",
+                          "alternate", None, 2 * -(-half // 128)),
+                         ("one launch per bucket", zs.ZS_BUCKETS_PER_BUCKET, None, bp.n_buckets),
+                         ("one launch per bucket, odd positions on a side stream", zs.ZS_BUCKETS_PER_BUCKET,
+                          side_bw, bp.n_buckets))
+                for label, lm, side, n_launch in modes:
 
-                    def bucketwise(bp=bp, order=order, side=side):
+                    def bucketwise(bp=bp, order=order, lm=lm, side=side):
                         t[0] += 1
-                        zs.zs_fused_step_buckets(bp, order, grads, master, m, v, reps, hp, t[0], stream=stream,
-                                                 side_stream=side)
+                        if lm == "alternate":
+                            for part in (order[0::2], order[1::2]):
+                                zs.zs_fused_step_buckets(bp, part, grads, master, m, v, reps, hp, t[0],
+                                                         launch_mode=zs.ZS_BUCKETS_ONE_WALK, stream=stream)
+                        else:
+                            zs.zs_fused_step_buckets(bp, order, grads, master, m, v, reps, hp, t[0], launch_mode=lm,
+                                                     stream=stream, side_stream=side)
 
                     ms = timed(bucketwise, steps)
-                    launches += steps * bp.n_buckets
+                    launches += steps * n_launch
                     gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
-                    points.append({"n_d": n_d, "bucket_mib": mib, "buckets": bp.n_buckets, "streams": 1 if side is None else 2,
-                                   "step": "fused, one launch per bucket (descending), zs_fused_step_buckets", "ms": ms,
+                    points.append({"n_d": n_d, "bucket_mib": mib, "buckets": bp.n_buckets, "mode": label,
+                                   "step": "fused over every bucket (descending), zs_fused_step_buckets", "ms": ms,
                                    "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
         del master, m, v, grads, reps
         torch.cuda.empty_cache()

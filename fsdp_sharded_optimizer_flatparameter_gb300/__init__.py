@@ -29,6 +29,7 @@ ZS_STAGE_DP, ZS_STAGE_ZERO1, ZS_STAGE_ZERO2, ZS_STAGE_ZERO3 = 0, 1, 2, 3
 ZS_RANK_FULL, ZS_SHARDED, ZS_RANK_BUCKET, ZS_RANK_UNIT = 0, 1, 2, 3
 ZS_MAX_RANKS = 64
 ZS_FUSED_AUTO, ZS_FUSED_LDG, ZS_FUSED_TMA = 0, 1, 2
+ZS_BUCKETS_ONE_WALK, ZS_BUCKETS_PER_BUCKET = 0, 1
 ZS_LAYOUT_FSDP1, ZS_LAYOUT_FSDP2 = 0, 1
 ZS_DEVERR_NONE, ZS_DEVERR_PRODUCER_WAIT, ZS_DEVERR_CONSUMER_WAIT, ZS_DEVERR_SELFTEST = 0, 1, 2, 3
 ZS_DEVERR_GATHER_WAIT = 4
@@ -96,7 +97,7 @@ _sig("zs_zero2_step_host_noalloc", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.P
 _sig("zs_all_reduce_mean", [c_vp, c_i32, c_vp, c_vp])
 _sig("zs_dp_step", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
 _sig("zs_fused_step_buckets", [c_vp, c_i32, P_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
-                               ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp])
+                               ctypes.POINTER(zs_adamw_hparams), c_i64, c_i32, c_vp, c_vp])
 _sig("zs_set_fused_variant", [c_i32])
 _sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
 _sig("zs_selftest_wait_timeout", [c_i64, c_vp])
@@ -511,17 +512,21 @@ def zs_fsdp2_copy_out(plan, unit, flat, params, stream=None):
                                          (c_vp * max(len(ptrs), 1))(*ptrs), _stream(stream)))
 
 
-def zs_fused_step_buckets(plan, buckets, grads, master, m, v, replicas, hp, step, stream=None, side_stream=None):
-    """buckets: bucket indices, launched one by one in this order (odd positions on side_stream if given)."""
+def zs_fused_step_buckets(plan, buckets, grads, master, m, v, replicas, hp, step, launch_mode=None, stream=None,
+                          side_stream=None):
+    """buckets: bucket indices in stepping order.  launch_mode: ZS_BUCKETS_ONE_WALK (default: one
+    persistent launch walks them) or ZS_BUCKETS_PER_BUCKET (one launch each; odd positions on
+    side_stream if given)."""
     _n_ptrs(ZS_RANK_FULL, grads, plan.n_d, "grads")
     _n_ptrs(ZS_RANK_FULL, replicas, plan.n_d, "replicas")
     n = plan.padded
     ids = (c_i32 * max(len(buckets), 1))(*[int(b) for b in buckets])
+    mode = ZS_BUCKETS_ONE_WALK if launch_mode is None else int(launch_mode)
     side = None if side_stream is None else _stream(side_stream)
     return _check(_lib.zs_fused_step_buckets(
         plan.handle, len(buckets), ids, _ptr_array(grads, n, 2, "grads"), _addr(master, n, 4, "master"),
         _addr(m, n, 4, "m"), _addr(v, n, 4, "v"), _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)),
-        int(step), _stream(stream), side))
+        int(step), mode, _stream(stream), side))
 
 
 def zs_set_fused_variant(variant):

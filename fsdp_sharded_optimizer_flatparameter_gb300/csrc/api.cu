@@ -256,13 +256,15 @@ extern "C" int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* 
 
 extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buckets,
                                      const void* const* grads, float* master, float* m, float* v,
-                                     void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream,
-                                     void* side_stream) {
+                                     void* const* replicas, const zs_adamw_hparams* hp, int64_t step,
+                                     int32_t launch_mode, void* stream, void* side_stream) {
     static const char* fn = "zs_fused_step_buckets";
     zs::TraceRange trace_(fn);
     zs::clear_error();
     ZS_TRY(check_plan(fn, plan));
     if (n_buckets < 0 || (n_buckets > 0 && !buckets)) return fail(fn, "bad bucket list");
+    if (launch_mode != ZS_BUCKETS_ONE_WALK && launch_mode != ZS_BUCKETS_PER_BUCKET)
+        return fail(fn, "launch_mode must be ZS_BUCKETS_ONE_WALK or ZS_BUCKETS_PER_BUCKET");
     std::vector<char> seen(plan->buckets.size(), 0);
     for (int32_t i = 0; i < n_buckets; ++i) {
         ZS_TRY(check_bucket(fn, plan, buckets[i], false));
@@ -290,6 +292,12 @@ extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const in
     const zs::StagedPolicy pol =
         zs::fused_ptrs_on_device(g, master, m, v, o, true, nd) ? zs::kStagedDeviceKnown : zs::kStagedNever;
     cudaStream_t a = as_stream(stream);
+    if (launch_mode == ZS_BUCKETS_ONE_WALK) {
+        std::vector<zs::Range> ranges;
+        ranges.reserve(todo.size());
+        for (int32_t b : todo) ranges.push_back({plan->buckets[b].begin, plan->buckets[b].end, 0, 1});
+        return cuda_status(fn, zs::launch_fused_ranges(g, master, m, v, o, ranges, s, nd, a, pol));
+    }
     cudaStream_t b = side_stream ? as_stream(side_stream) : a;
     const bool two = b != a && todo.size() > 1;
     cudaEvent_t fork = nullptr, join = nullptr;

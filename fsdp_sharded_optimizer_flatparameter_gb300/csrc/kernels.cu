@@ -13,6 +13,7 @@
 // parameter for the common powers of two so the rank loops unroll; other
 // counts use the runtime value.  Nothing here waits on anything, so no kernel
 // can hang.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <unordered_map>
@@ -454,6 +455,67 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
     }
     if (sp.hi > body_hi) e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(body_hi, sp.hi, false), s, nd, st);
     return e;
+}
+
+cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* v, const BView& out,
+                                const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
+                                StagedPolicy staged_policy) {
+    // Inside one launch the order of disjoint ranges is not observable, so ranges that touch are
+    // merged (a run of neighbouring buckets, in either order, becomes one range for the single-range
+    // kernels); only what stays disjoint goes through the list kernel.
+    std::vector<Range> merged;
+    for (const Range& r : ranges)
+        if (r.hi > r.lo) merged.push_back(r);
+    std::sort(merged.begin(), merged.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
+    size_t w = 0;
+    for (size_t i = 0; i < merged.size(); ++i) {
+        if (w > 0 && merged[w - 1].hi == merged[i].lo) merged[w - 1].hi = merged[i].hi;
+        else merged[w++] = merged[i];
+    }
+    merged.resize(w);
+    if (merged.empty()) return cudaSuccess;
+    if (merged.size() == 1) return launch_fused(g, master, m, v, out, true, merged[0], s, nd, st, staged_policy);
+    const bool vec = aligned8(g.off) && aligned8(out.off);
+    std::vector<Split> splits;
+    splits.reserve(merged.size());
+    int64_t body_total = 0;
+    for (const Range& r : merged) {
+        splits.push_back(split_range(r.lo, r.hi, vec));
+        body_total += splits.back().nvec << 3;
+    }
+    const int variant = g_fused_variant.load();
+    // the list is one launch, so the staged kernel's ramp is paid once for all of it
+    bool staged = body_total > 0 && staged_policy != kStagedNever &&
+                  (variant == ZS_FUSED_TMA || (variant == ZS_FUSED_AUTO && body_total >= kTmaMinElems)) &&
+                  (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
+    if (staged && staged_policy == kStagedIfDevice) staged = fused_ptrs_on_device(g, master, m, v, out, true, nd);
+    if (!staged) {
+        for (const Split& sp : splits) {
+            cudaError_t e = launch_fused_ldg(g, master, m, v, out, true, sp, s, nd, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    std::vector<std::pair<int64_t, int64_t>> bodies;
+    bodies.reserve(splits.size());
+    for (const Split& sp : splits)
+        if (sp.nvec > 0) bodies.emplace_back(sp.vlo, sp.nvec << 3);
+    cudaError_t e = launch_fused_tma_list(g, master, m, v, out, bodies, s, nd, st);
+    if (e != cudaSuccess) return e;
+    // fringes (ranges whose ends are off the 8-element grid): at most 14 elements per range
+    for (const Split& sp : splits) {
+        const int64_t body_hi = sp.nvec > 0 ? sp.vlo + (sp.nvec << 3) : sp.lo;
+        const int64_t head_hi = sp.nvec > 0 ? sp.vlo : sp.hi;
+        if (head_hi > sp.lo) {
+            e = launch_fused_ldg(g, master, m, v, out, true, split_range(sp.lo, head_hi, false), s, nd, st);
+            if (e != cudaSuccess) return e;
+        }
+        if (sp.nvec > 0 && sp.hi > body_hi) {
+            e = launch_fused_ldg(g, master, m, v, out, true, split_range(body_hi, sp.hi, false), s, nd, st);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
 }
 
 }  // namespace zs

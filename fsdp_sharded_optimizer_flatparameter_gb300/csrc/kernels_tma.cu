@@ -20,6 +20,11 @@
 // Every wait is bounded (clock64 budget).  A wait that runs out sets
 // g_zs_device_error, the CTA stops taking tiles, the producer waits (again
 // bounded) for the copies it still has in flight, and the kernel returns.
+#include <memory>
+#include <type_traits>
+#include <utility>
+#include <vector>
+
 #include "device.cuh"
 
 namespace zs {
@@ -134,6 +139,48 @@ struct TmaArgs {
     long long wait_limit; // cycles a wait may take before the kernel gives up
     long long drain_limit;// cycles to wait for copies still in flight after giving up
 };
+
+// A list of bodies stepped by one launch (the buckets of one call, in the caller's order): body r
+// is [lo[r], lo[r] + n[r]) with the same alignment rules as TmaArgs' body, and first[r] is the
+// number of tiles of the bodies before it (first[nr] = all tiles).  The kernel walks the
+// concatenation of the bodies' tiles, so a CTA's tiles follow the list order.
+constexpr int kTmaListMax = 128;   // bodies per launch (the table is staged in shared memory)
+struct TmaListArgs {
+    TmaArgs a;            // everything but lo and n
+    int nr;
+    int64_t total_tiles;  // first[nr]
+    int64_t lo[kTmaListMax];
+    int64_t n[kTmaListMax];
+    int32_t first[kTmaListMax + 1];
+};
+
+namespace {
+
+// A list launch copies the body table from the kernel parameter into shared memory once per CTA,
+// reading the parameter with compile-time indices only: indexing a __grid_constant__ parameter with
+// a run-time index turns every parameter access of the kernel into a generic load, which measured
+// ~4 % slower on GB300.  Each thread then walks its CTA's tiles in increasing order, keeping the
+// current body in registers and reading the shared table only when a tile lies past it.
+struct ListTable {
+    int64_t lo[kTmaListMax];
+    int64_t n[kTmaListMax];
+    int32_t first[kTmaListMax + 1];
+};
+constexpr int kListTableBytes = (int)((sizeof(ListTable) + 127) / 128 * 128);
+
+__device__ __forceinline__ void list_table_fill(const TmaListArgs& l, ListTable* t, int lane) {
+#pragma unroll
+    for (int q = 0; q < kTmaListMax; ++q) {
+        if ((q & 31) == lane) {
+            t->lo[q] = l.lo[q];
+            t->n[q] = l.n[q];
+            t->first[q] = l.first[q];
+        }
+    }
+    if (lane == 0) t->first[kTmaListMax] = l.first[kTmaListMax];
+}
+
+}  // namespace
 
 // Tile and ring geometry: T elements per tile, as many stages as fit in
 // BUDGET bytes of shared memory (at most MAXST), 256 bytes of barriers first.
@@ -279,6 +326,167 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
     }
 }
 
+// The broadcast step over a list of disjoint bodies in one launch (bodies that touch are merged
+// on the host, so this serves scattered subsets of buckets).  The producer walks the bodies in
+// table order, taking the tiles t of their concatenation with t = blockIdx.x mod gridDim.x, and
+// publishes each stage's tile (first element, length) in shared memory before arriving on the
+// stage's full barrier; after its last tile it publishes length 0 and arrives without data, which
+// ends the consumers' loop.  The consumers' per-tile work is that of k_fused_tma; they read the
+// tile from shared memory instead of computing it (the kernel stays a separate loop from
+// k_fused_tma's: folding both into one generic loop cost the single-range kernel ~3 % on GB300).
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_list(const __grid_constant__ TmaListArgs l) {
+    constexpr bool BROADCAST = true;
+    const TmaArgs& a = l.a;
+    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
+    constexpr int T = Sh::kT;
+    constexpr int S = Sh::kStages;
+    static_assert(2 * S * 8 + 12 * S <= 256, "barriers and the tile table share the first 256 bytes");
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + S;
+    int64_t* meta_i0 = reinterpret_cast<int64_t*>(smem + 2 * S * 8);
+    uint32_t* meta_len = reinterpret_cast<uint32_t*>(smem + 2 * S * 8 + 8 * S);
+    ListTable* table = reinterpret_cast<ListTable*>(smem + 256);
+    uint8_t* stages = smem + 256 + kListTableBytes;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCW * 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) list_table_fill(l, table, lane);
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            const uint64_t pol = evict_first_policy();
+            const int64_t G = gridDim.x;
+            int64_t j = 0;
+            bool ok = true;
+            for (int r = 0; r < l.nr && ok; ++r) {
+                const int64_t f0 = table->first[r], f1 = table->first[r + 1];
+                const int64_t blo = table->lo[r], bn = table->n[r];
+                for (int64_t k = ((int64_t)blockIdx.x - f0 % G + G) % G; f0 + k < f1; k += G, ++j) {
+                    const int s = (int)(j % S);
+                    if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), a.wait_limit)) {
+                        flag_error(ZS_DEVERR_PRODUCER_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    const int64_t i0 = blo + k * T;
+                    const int64_t rem = bn - k * T;
+                    const uint32_t len = (uint32_t)(rem < T ? rem : T);
+                    meta_i0[s] = i0;                     // ordered before the arrive below (release)
+                    meta_len[s] = len;
+                uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
+                mbar_expect_tx(&full[s], len * (2u * ND + 12u));
+#pragma unroll
+                for (int q = 0; q < ND; ++q)
+                    bulk_load(st + (size_t)q * T * 2, a.g.p[q] + (i0 - a.g_off), len * 2u, &full[s], pol);
+                float* sf = reinterpret_cast<float*>(st + (size_t)ND * T * 2);
+                bulk_load(sf, a.master + i0, len * 4u, &full[s], pol);
+                bulk_load(sf + T, a.m + i0, len * 4u, &full[s], pol);
+                bulk_load(sf + 2 * T, a.v + i0, len * 4u, &full[s], pol);
+                }
+            }
+            if (ok) {
+                // the end: a stage with length 0 and no data
+                const int s = (int)(j % S);
+                if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), a.wait_limit)) {
+                    flag_error(ZS_DEVERR_PRODUCER_WAIT);
+                    ok = false;
+                } else {
+                    meta_len[s] = 0;
+                    mbar_arrive(&full[s]);
+                }
+            }
+            if (!ok) {
+                // drain: wait (bounded) for the copies issued into stages not yet consumed
+                const int64_t issued = j;
+                for (int64_t k = issued > S ? issued - S : 0; k < issued; ++k)
+                    mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int ct = threadIdx.x - 32;                  // 0 .. NCW*32-1
+    const int e = ct * VPT;                           // this thread's first element in a tile
+    const int n = ND;
+    for (int64_t j = 0;; ++j) {
+        const int s = (int)(j % S);
+        if (!mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
+            flag_error(ZS_DEVERR_CONSUMER_WAIT);
+            return;
+        }
+        const int64_t i0 = meta_i0[s];
+        const int len = (int)meta_len[s];
+        if (len == 0) return;
+        if (e < len) {
+            const uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
+            const uint16_t* sg = reinterpret_cast<const uint16_t*>(st);
+            const float* sf = reinterpret_cast<const float*>(st + (size_t)ND * T * 2);
+            float acc[VPT];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) acc[k] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < n; ++q) {
+                float f[VPT];
+                lds_bf<VPT>(sg + (size_t)q * T + e, f);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+            }
+            float p[VPT], mm[VPT], vv[VPT];
+            lds_f32<VPT>(sf + e, p);
+            lds_f32<VPT>(sf + T + e, mm);
+            lds_f32<VPT>(sf + 2 * T + e, vv);
+            uint32_t gw[VPT / 2];
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2)
+                gw[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], n, a.inv_nd), mean_of_sum<ND>(acc[k + 1], n, a.inv_nd));
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2) {
+                adamw_elem(bf16_lo(gw[k / 2]), p[k], mm[k], vv[k], a.s);
+                adamw_elem(bf16_hi(gw[k / 2]), p[k + 1], mm[k + 1], vv[k + 1], a.s);
+            }
+            mbar_arrive(&empty[s]);                      // this thread is done with the stage
+            const int64_t i = i0 + e;
+            stg_f32<VPT>(a.master + i, p);
+            stg_f32<VPT>(a.m + i, mm);
+            stg_f32<VPT>(a.v + i, vv);
+            uint32_t pw[VPT / 2];
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2) pw[k / 2] = pack_bf16x2(p[k], p[k + 1]);
+            if constexpr (VPT == 8) {
+                const uint4 w = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                if constexpr (BROADCAST) {
+#pragma unroll
+                    for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint4*>(a.out.p[q] + (i - a.out_off)), w);
+                } else {
+                    __stcs(reinterpret_cast<uint4*>(a.out.p[0] + (i - a.out_off)), w);
+                }
+            } else {
+                const uint2 w = make_uint2(pw[0], pw[1]);
+                if constexpr (BROADCAST) {
+#pragma unroll
+                    for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint2*>(a.out.p[q] + (i - a.out_off)), w);
+                } else {
+                    __stcs(reinterpret_cast<uint2*>(a.out.p[0] + (i - a.out_off)), w);
+                }
+            }
+        } else {
+            mbar_arrive(&empty[s]);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ gather with bulk stores
 // One source, N_d destinations (the all-gather from shards and the ZeRO-3 unit gather:
 // "Infra: Data Parallel", ZeRO section).  Each CTA is one warp with a ring of S shared-memory
@@ -356,45 +564,46 @@ __global__ void __launch_bounds__(32) k_gather_bulk(const __grid_constant__ Gath
 
 namespace {
 
-template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
-cudaError_t tma_impl(const TmaArgs& a, cudaStream_t st) {
+int64_t host_tiles(const TmaArgs& a, int T) { return (a.n + T - 1) / T; }
+
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET>
+auto pick_kernel(const TmaArgs*) { return k_fused_tma<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>; }
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET>
+auto pick_kernel(const TmaListArgs*) {
+    static_assert(BROADCAST, "lists are stepped by the broadcast form only");
+    return k_fused_tma_list<ND, NCW, VPT, MAXST, BUDGET>;
+}
+int64_t host_tiles(const TmaListArgs& l, int) { return l.total_tiles; }
+
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET, class Args>
+cudaError_t tma_impl(const Args& a, cudaStream_t st) {
     using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
-    auto kern = k_fused_tma<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>;
+    constexpr int kSmem = Sh::kSmem + (std::is_same<Args, TmaListArgs>::value ? kListTableBytes : 0);
+    static_assert(kSmem <= 232448, "shared memory above the per-CTA limit");
+    auto kern = pick_kernel<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>(static_cast<const Args*>(nullptr));
     // set on every launch: the attribute belongs to the current device
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), Sh::kSmem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), kSmem);
     if (per_sm < 1) per_sm = 1;
-    const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
+    const int64_t ntiles = host_tiles(a, Sh::kT);
+    if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
     const int grid = (int)(ntiles < cap ? ntiles : cap);
-    kern<<<grid, 32 * (NCW + 1), Sh::kSmem, st>>>(a);
+    kern<<<grid, 32 * (NCW + 1), kSmem, st>>>(a);
     return cudaGetLastError();
 }
 
-}  // namespace
+template <int V>
+using IC = std::integral_constant<int, V>;
+template <bool V>
+using BC = std::integral_constant<bool, V>;
 
-// Returns cudaErrorNotSupported when no staged variant exists for this rank count.
-cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
-    TmaArgs a;
-    a.g = g.ptr;
-    a.g_off = g.off;
-    a.out = out.ptr;
-    a.out_off = out.off;
-    a.master = master;
-    a.m = m;
-    a.v = v;
-    a.s = s;
-    a.lo = lo;
-    a.n = n;
-    a.nd = nd;
-    a.inv_nd = 1.0f / (float)nd;
-    a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
-    a.drain_limit = 4000000000LL;
+// Calls f(ND, NCW, VPT, BROADCAST, MAXST, BUDGET) (as integral constants) with the measured shape for
+// this rank count and output form; cudaErrorNotSupported when there is none.
 // Shapes per rank count, chosen by measurement on GB300 (a grid of warps x elements per thread x
 // ring depth per rank count and output form, on 2^28-element buffers, then the leaders re-timed
 // three times interleaved): consumer warps, elements per thread, stage cap, shared-memory budget
@@ -402,8 +611,10 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
 // form (ZeRO-3 update, standalone AdamW with N_d = 1) is read-heavy: at N_d = 8 the broadcast
 // shape reaches only ~74 % there, while three small CTAs per SM (2 warps x 512, 4 stages) stream
 // at the copy rate.
+template <class F>
+cudaError_t with_shape(bool broadcast, int nd, F&& f) {
 #define ZS_TMA(ND_, NCW_, VPT_, MAXST_, BUDGET_, BROADCAST_) \
-    return tma_impl<ND_, NCW_, VPT_, BROADCAST_, MAXST_, BUDGET_>(a, st)
+    return f(IC<ND_>{}, IC<NCW_>{}, IC<VPT_>{}, BC<BROADCAST_>{}, IC<MAXST_>{}, IC<BUDGET_>{})
     if (broadcast) {
         switch (nd) {
             case 2: ZS_TMA(2, 8, 8, 4, 232448, true);     // T 2048, 4 stages, 1 CTA/SM
@@ -424,6 +635,91 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
         default: return cudaErrorNotSupported;
     }
 #undef ZS_TMA
+}
+
+TmaArgs make_args(const BView& g, float* master, float* m, float* v, const BView& out, const AdamScalars& s,
+                  int nd) {
+    TmaArgs a;
+    a.g = g.ptr;
+    a.g_off = g.off;
+    a.out = out.ptr;
+    a.out_off = out.off;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.s = s;
+    a.lo = 0;
+    a.n = 0;
+    a.nd = nd;
+    a.inv_nd = 1.0f / (float)nd;
+    a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
+    a.drain_limit = 4000000000LL;
+    return a;
+}
+
+}  // namespace
+
+// Returns cudaErrorNotSupported when no staged variant exists for this rank count.
+cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
+                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+    TmaArgs a = make_args(g, master, m, v, out, s, nd);
+    a.lo = lo;
+    a.n = n;
+    return with_shape(broadcast, nd, [&](auto ND, auto NCW, auto VPT, auto BR, auto MS, auto BU) {
+        return tma_impl<decltype(ND)::value, decltype(NCW)::value, decltype(VPT)::value, decltype(BR)::value,
+                        decltype(MS)::value, decltype(BU)::value>(a, st);
+    });
+}
+
+namespace {
+
+// Launches the list kernel over `bodies`, kTmaListMax bodies (and at most 2^31 - 1 tiles) per launch.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+cudaError_t tma_list_impl(TmaListArgs& l, const std::vector<std::pair<int64_t, int64_t>>& bodies, cudaStream_t st) {
+    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
+    size_t i = 0;
+    while (i < bodies.size()) {
+        int nr = 0;
+        int64_t tiles = 0;
+        l.first[0] = 0;
+        for (; i < bodies.size() && nr < kTmaListMax; ++i) {
+            const int64_t t = (bodies[i].second + Sh::kT - 1) / Sh::kT;
+            if (t < 1) continue;
+            if (tiles + t > 0x7fffffffLL) {                       // tile counts are 32-bit in the list
+                if (nr == 0) return cudaErrorInvalidValue;
+                break;
+            }
+            l.lo[nr] = bodies[i].first;
+            l.n[nr] = bodies[i].second;
+            tiles += t;
+            l.first[++nr] = (int32_t)tiles;
+        }
+        l.nr = nr;
+        l.total_tiles = tiles;
+        if (nr == 0) continue;
+        cudaError_t e = tma_impl<ND, NCW, VPT, true, MAXST, BUDGET>(l, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+// Broadcast form over a list of bodies in one launch per kTmaListMax bodies.
+cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float* v, const BView& out,
+                                  const std::vector<std::pair<int64_t, int64_t>>& bodies, const AdamScalars& s,
+                                  int nd, cudaStream_t st) {
+    if (bodies.empty()) return cudaSuccess;
+    // the argument block is ~11 KB: built on the heap
+    std::unique_ptr<TmaListArgs> l(new TmaListArgs());
+    l->a = make_args(g, master, m, v, out, s, nd);
+    return with_shape(true, nd, [&](auto ND, auto NCW, auto VPT, auto BR, auto MS, auto BU) -> cudaError_t {
+        if constexpr (decltype(BR)::value)
+            return tma_list_impl<decltype(ND)::value, decltype(NCW)::value, decltype(VPT)::value,
+                                 decltype(MS)::value, decltype(BU)::value>(*l, bodies, st);
+        else
+            return cudaErrorNotSupported;                     // only the broadcast form walks lists
+    });
 }
 
 // Self-test of the bounded wait: waits on an mbarrier nothing arrives at, with

@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+#include <vector>
+
 #include "zs.h"
 
 namespace zs {
@@ -56,6 +59,17 @@ bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, con
 // cudaErrorNotSupported when no staged variant exists for this rank count.
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                              int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
+// The broadcast staged kernel over a list of bodies ([lo, lo + n): the TMA alignment rules of
+// launch_fused_tma for each) in one launch per 512 bodies, tiles walked in list order.
+cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float* v, const BView& out,
+                                  const std::vector<std::pair<int64_t, int64_t>>& bodies, const AdamScalars& s,
+                                  int nd, cudaStream_t st);
+// The broadcast fused step over several disjoint ranges: with the staged kernel one walk over all of
+// them (bodies in one list launch, the few fringe elements by the streaming kernel), else one
+// streaming launch per range.
+cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* v, const BView& out,
+                                const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
+                                StagedPolicy staged_policy = kStagedIfDevice);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
 // One source to N_d destinations with bulk stores, over the 8-aligned body [lo, lo + n).
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,

@@ -329,24 +329,35 @@ int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int3
                   float* master, float* m, float* v, void* const* replicas,
                   const zs_adamw_hparams* hp, int64_t step, void* stream);
 
-/* zs_fused_step for a list of buckets (ZS_RANK_FULL gradients), one launch per
- * bucket in the order given - e.g. the buckets whose gradients became ready
- * together, last layer first.  Same results as calling zs_fused_step once per
- * bucket, with the argument checks, the pointer-kind queries and the per-call
- * overhead paid once.  The update is element-wise and the buckets are disjoint,
- * so their launches need no order among themselves: with a side_stream other
- * than stream, the buckets at odd positions of the list run on side_stream
- * (which first waits for all work enqueued on stream) and the next bucket's
- * launch overlaps the end of the previous one; before returning, stream is
- * made to wait for side_stream, so all of the step is ordered before later
- * work on stream either way.  side_stream NULL or equal to stream: one stream.
- * The call creates and releases two CUDA events (no device memory).
- * Errors: ZS_ERR_INVALID (bad or repeated bucket index, or any check of
- * zs_fused_step; nothing enqueued), ZS_ERR_CUDA. */
+/* zs_fused_step for a list of buckets (ZS_RANK_FULL gradients) in the order
+ * given - e.g. the buckets whose gradients became ready together, last layer
+ * first.  Same results as calling zs_fused_step once per bucket, with the
+ * argument checks, the pointer-kind queries and the per-call overhead paid
+ * once.  The update is element-wise and the buckets are disjoint, so the
+ * launches need no order among themselves.
+ *   launch_mode  ZS_BUCKETS_ONE_WALK: the staged kernel walks all listed
+ *                buckets in one persistent launch (per 512 buckets), each
+ *                CTA taking its tiles in list order, so a small bucket costs
+ *                no launch of its own; where only the streaming kernel
+ *                applies (host buffers, other rank counts, a total below
+ *                2^20 elements) one launch per bucket on `stream`.
+ *                ZS_BUCKETS_PER_BUCKET: one launch per bucket; with a
+ *                side_stream other than stream, the buckets at odd positions
+ *                run on side_stream (which first waits for all work enqueued
+ *                on stream) and each launch overlaps the end of the previous
+ *                one; before returning, stream is made to wait for
+ *                side_stream.  This mode creates and releases two CUDA events
+ *                (no device memory).
+ *   side_stream  used by ZS_BUCKETS_PER_BUCKET only; NULL or equal to stream:
+ *                one stream.
+ * Errors: ZS_ERR_INVALID (bad or repeated bucket index, unknown launch_mode,
+ * or any check of zs_fused_step; nothing enqueued), ZS_ERR_CUDA. */
+#define ZS_BUCKETS_ONE_WALK 0
+#define ZS_BUCKETS_PER_BUCKET 1
 int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buckets,
                           const void* const* grads, float* master, float* m, float* v,
-                          void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream,
-                          void* side_stream);
+                          void* const* replicas, const zs_adamw_hparams* hp, int64_t step,
+                          int32_t launch_mode, void* stream, void* side_stream);
 
 /* zs_fused_step over the whole flat space with the gradients in HOST memory
  * (pinned for overlap): enqueues one host-to-device copy per rank into

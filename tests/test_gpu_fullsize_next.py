@@ -1,7 +1,8 @@
 """Full-size parity for the widening rows, in the launch configurations the benchmark's
 widening leg times, sampled.
 
-* the bucket-list step with a side stream on the 2^28+7 buffer (1 MiB and 4 MiB buckets);
+* the bucket-list step on the 2^28+7 buffer (1 MiB and 4 MiB buckets), walked by one launch and
+  launched bucket by bucket on two streams;
 * naive DP (all-reduce-mean + replicated AdamW) on GPT-2-small at N_d = 8;
 * ZeRO-3 without resharding after forward on Llama-1.3B (24 layer units + root), N_d = 8;
 * the FSDP2 Shard(0) layout on the same grouping: gradients converted per rank, the fused step
@@ -63,10 +64,11 @@ def _check_chunks(chunks, before, master, m, v, reps, t, what):
             H.check_bf16(_np(r[lo:hi]), bits, "replica %d %s" % (q, w))
 
 
-@pytest.mark.parametrize("mib", [1, 4])
-def test_bucket_list_two_streams_full_size(mib):
-    """2^28+7 elements, N_d = 8: every bucket in descending order, odd positions on a side stream,
-    equals the whole-range step bit for bit, and the oracle on chunks around bucket edges."""
+@pytest.mark.parametrize("mib,mode", [(1, "walk"), (4, "walk"), (1, "two_streams"), (4, "two_streams")])
+def test_bucket_list_full_size(mib, mode):
+    """2^28+7 elements, N_d = 8: every bucket in descending order, walked by one launch or launched
+    one by one with the odd positions on a side stream, equals the whole-range step bit for bit,
+    and the oracle on chunks around bucket edges."""
     n_d = 8
     shapes = [(2 ** 28 + 7,)]
     whole = zs.Plan(shapes, n_d, stage=2)
@@ -85,14 +87,20 @@ def test_bucket_list_two_streams_full_size(mib):
     before = [([_np(g[lo:hi]) for g in grads], _np(b[0][lo:hi]), _np(b[1][lo:hi]), _np(b[2][lo:hi]))
               for lo, hi in chunks]
     zs.zs_fused_step(whole, -1, grads, zs.ZS_RANK_FULL, *a, ra, HP, 1)
-    side = torch.cuda.Stream()
-    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), grads, *b, rb, HP, 1, side_stream=side)
+    order = list(reversed(range(plan.n_buckets)))
+    if mode == "walk":
+        # two lists of disjoint buckets (all at once would merge into one range)
+        for part in (order[0::2], order[1::2]):
+            zs.zs_fused_step_buckets(plan, part, grads, *b, rb, HP, 1, launch_mode=zs.ZS_BUCKETS_ONE_WALK)
+    else:
+        zs.zs_fused_step_buckets(plan, order, grads, *b, rb, HP, 1, launch_mode=zs.ZS_BUCKETS_PER_BUCKET,
+                                 side_stream=torch.cuda.Stream())
     torch.cuda.synchronize()
     assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
     for x, y in zip(a, b):
         assert torch.equal(x, y)
     assert all(torch.equal(x, y) for x, y in zip(ra, rb))
-    _check_chunks(chunks, before, *b, [rb[0], rb[-1]], 1, "buckets %d MiB" % mib)
+    _check_chunks(chunks, before, *b, [rb[0], rb[-1]], 1, "buckets %d MiB %s" % (mib, mode))
 
 
 def test_naive_dp_gpt2_full_size():

@@ -625,13 +625,14 @@ def test_guard_zones_untouched_large_kernels():
         assert bool((raw[:g] == 0x5A).all()) and bool((raw[-g:] == 0x5A).all())
 
 
-@pytest.mark.parametrize("bucket_bytes", [1 << 20, 4 << 20])
-@pytest.mark.parametrize("two_streams", [False, True])
-def test_fused_step_buckets_equals_whole_range(bucket_bytes, two_streams):
-    """zs_fused_step_buckets (all buckets, descending, one launch each; with a side stream the odd
-    positions overlap on it) equals the whole-range step; work enqueued on the caller's stream just
-    before the call is seen by both streams, and work enqueued right after it sees the whole step;
-    a repeated bucket is refused before anything runs."""
+@pytest.mark.parametrize("bucket_bytes", [1 << 20, 4 << 20, 1000])
+@pytest.mark.parametrize("mode", ["walk", "per_bucket", "per_bucket_two_streams"])
+def test_fused_step_buckets_equals_whole_range(bucket_bytes, mode):
+    """zs_fused_step_buckets over all buckets, descending, equals the whole-range step: walked as two
+    lists of disjoint buckets, one launch per bucket, and one launch per bucket with the odd
+    positions on a side stream.  Work enqueued on the caller's stream just before the call is
+    seen, and work enqueued right after it sees the whole step; a repeated bucket is refused before
+    anything runs."""
     plan, _ = _plans([(3_000_011,)], 8, bucket_bytes=bucket_bytes)
     P, pads = plan.padded, plan.pad_ranges()
     master0 = synth.master_init(P, pads, seed=62, device=DEV)
@@ -640,21 +641,76 @@ def test_fused_step_buckets_equals_whole_range(bucket_bytes, two_streams):
     rb = synth.rank_buffers(8, P, BF16, DEV)[0]
     src, _ = synth.rank_grads(8, P, pads, seed=62, step=1, sigma=1e-3, device=DEV)
     grads = synth.rank_buffers(8, P, BF16, DEV)[0]
-    side = torch.cuda.Stream() if two_streams else None
+    side = torch.cuda.Stream() if mode == "per_bucket_two_streams" else None
+    lm = zs.ZS_BUCKETS_ONE_WALK if mode == "walk" else zs.ZS_BUCKETS_PER_BUCKET
     zs.zs_fused_step(plan, -1, src, zs.ZS_RANK_FULL, *a.args(), ra, HP, 1)
     torch.cuda.synchronize()
     for q in range(8):
         grads[q].copy_(src[q])                      # on the caller's stream, still in flight at the call
-    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), grads, *b.args(), rb, HP, 1,
-                             side_stream=side)
+    order = list(reversed(range(plan.n_buckets)))
+    if mode == "walk":
+        # every other bucket, then the rest: each call is a list of disjoint runs (the list kernel;
+        # 1000-byte buckets give 3,000 runs per call, several list launches and a streaming fringe
+        # at every run edge off the 8-element grid); all buckets at once would merge into one range
+        for part in (order[0::2], order[1::2]):
+            zs.zs_fused_step_buckets(plan, part, grads, *b.args(), rb, HP, 1, launch_mode=lm)
+    else:
+        zs.zs_fused_step_buckets(plan, order, grads, *b.args(), rb, HP, 1, launch_mode=lm, side_stream=side)
     after = [r.clone() for r in rb] + [x.clone() for x in b.args()]   # caller's stream, right after
     torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
     for x, y in zip(a.args(), b.args()):
         assert torch.equal(x, y)
     assert all(torch.equal(x, y) for x, y in zip(ra, rb))
     assert all(torch.equal(x, y) for x, y in zip(ra + list(a.args()), after))
     before = b.master.clone()
     with pytest.raises(zs.ZsError):
-        zs.zs_fused_step_buckets(plan, [0, 1, 0], grads, *b.args(), rb, HP, 2, side_stream=side)
+        zs.zs_fused_step_buckets(plan, [0, 1, 0], grads, *b.args(), rb, HP, 2, launch_mode=lm, side_stream=side)
+    with pytest.raises(zs.ZsError):
+        zs.zs_fused_step_buckets(plan, [0, 1], grads, *b.args(), rb, HP, 2, launch_mode=7)
     torch.cuda.synchronize()
     assert torch.equal(b.master, before)
+
+
+def test_fused_step_buckets_all_at_once_merge_into_one_range():
+    """All buckets of a plan in one walk (descending) touch each other, so they are stepped as one
+    range: the same values as the whole-range step."""
+    plan, _ = _plans([(2_500_003,)], 8, bucket_bytes=1 << 20)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=64, device=DEV)
+    a, b = State(master0), State(master0)
+    ra = synth.rank_buffers(8, P, BF16, DEV)[0]
+    rb = synth.rank_buffers(8, P, BF16, DEV)[0]
+    grads, _ = synth.rank_grads(8, P, pads, seed=64, step=1, sigma=1e-3, device=DEV)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *a.args(), ra, HP, 1)
+    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), grads, *b.args(), rb, HP, 1)
+    torch.cuda.synchronize()
+    for x, y in zip(a.args(), b.args()):
+        assert torch.equal(x, y)
+    assert all(torch.equal(x, y) for x, y in zip(ra, rb))
+
+
+@pytest.mark.parametrize("n_d", [2, 4, 16, 32])
+def test_fused_step_bucket_walk_every_rank_count(variant, n_d):
+    """The list walk of the staged kernel (forced, so even a small list takes it) for every rank count
+    with a staged shape, buckets in a shuffled order and a subset stepped first: equals stepping the
+    same buckets one by one with the streaming kernel."""
+    plan, _ = _plans([(700_001,)], n_d, bucket_bytes=2 * 40_000)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=63, device=DEV)
+    grads, _ = synth.rank_grads(n_d, P, pads, seed=63, step=1, sigma=1e-3, device=DEV)
+    order = list(np.random.default_rng(n_d).permutation(plan.n_buckets))
+    out = {}
+    for v, lm in ((zs.ZS_FUSED_TMA, zs.ZS_BUCKETS_ONE_WALK), (zs.ZS_FUSED_LDG, zs.ZS_BUCKETS_PER_BUCKET)):
+        variant(v)
+        st = State(master0)
+        reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+        zs.zs_fused_step_buckets(plan, order[:3], grads, *st.args(), reps, HP, 1, launch_mode=lm)
+        zs.zs_fused_step_buckets(plan, order[3:], grads, *st.args(), reps, HP, 1, launch_mode=lm)
+        torch.cuda.synchronize()
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+        out[v] = (st, reps)
+    (sa, ra), (sb, rb) = out[zs.ZS_FUSED_TMA], out[zs.ZS_FUSED_LDG]
+    for x, y in zip(sa.args(), sb.args()):
+        assert torch.equal(x, y)
+    assert all(torch.equal(x, y) for x, y in zip(ra, rb))
