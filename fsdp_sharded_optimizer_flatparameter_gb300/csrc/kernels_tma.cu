@@ -492,8 +492,12 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_list(const __grid_
 // "Infra: Data Parallel", ZeRO section).  Each CTA is one warp with a ring of S shared-memory
 // stages of T bf16 elements: lane 0 loads a tile with one bulk copy, then lanes 0..31 issue the
 // N_d bulk stores of that tile (shared -> each destination) in parallel; a stage is refilled once
-// every lane's stores have read it.  Many small CTAs per SM keep many store streams in flight,
-// which is what a write-heavy (1 read : N_d writes) stream needs.
+// every lane's stores have read it.  The tile shape was measured on GB300 (tiles of 4K-32K
+// elements, 2-6 stages, 1-16 CTAs per SM in the grid, every N_d): 16K-element tiles in a 4-stage
+// ring (128 KB, so one CTA resident per SM, up to 4 x 32 KB x N_d bytes of stores in flight) with a
+// grid of 16 CTAs per SM streamed at 99.6-107 % of the measured copy rate for N_d = 2..32, against
+// 94.5-100.7 % for 8K-element tiles in 2 stages; a read-light stream (1 read : N_d writes) can pass
+// a 1:1 copy's rate.
 
 struct GatherBulkArgs {
     const uint16_t* src;
@@ -751,10 +755,10 @@ cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs&
     a.lo = lo;
     a.n = n;
     a.nd = nd;
-    a.T = 8192;
+    a.T = 16384;
     a.wait_limit = 4000000000LL;
     a.drain_limit = 4000000000LL;
-    constexpr int S = 2;
+    constexpr int S = 4;
     const int smem = 128 + S * a.T * 2;
     cudaError_t e = cudaFuncSetAttribute(k_gather_bulk<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
