@@ -313,14 +313,41 @@ constexpr int64_t kTmaMinElems = int64_t(1) << 20;
         default: return CALL(0);            \
     }
 
+static cudaError_t rs_ldg(const BView& g, const BView& out, bool out_by_owner, const Range& r, int nd,
+                          const Split& sp, cudaStream_t st) {
+#define ZS_RS(N) rs_impl<N>(g, out, out_by_owner, r, nd, sp, st)
+    ZS_DISPATCH_ND(nd, ZS_RS)
+#undef ZS_RS
+}
+
 cudaError_t launch_rs_mean(const BView& g, const BView& out, bool out_by_owner, const Range& r, int nd,
                            cudaStream_t st) {
     const bool vec = aligned8(g.off) && aligned8(out.off) &&
                      (!out_by_owner || (aligned8(r.base) && aligned8(r.shard)));
     const Split sp = split_range(r.lo, r.hi, vec);
-#define ZS_RS(N) rs_impl<N>(g, out, out_by_owner, r, nd, sp, st)
-    ZS_DISPATCH_ND(nd, ZS_RS)
-#undef ZS_RS
+    // one output array (ZeRO-2/3 shard, a bucket's staging): the staged kernel for the 8-aligned
+    // body, all on device memory; the in-place ZeRO-1 form (each element to its owner's buffer) and
+    // host buffers keep the streaming kernel
+    if (!out_by_owner && (sp.nvec << 3) >= kTmaMinElems && g_fused_variant.load() != ZS_FUSED_LDG &&
+        (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32)) {
+        const void* ps[ZS_MAX_RANKS + 1];
+        for (int q = 0; q < nd; ++q) ps[q] = g.ptr.p[q];
+        ps[nd] = out.ptr.p[0];
+        if (all_device(ps, nd + 1)) {
+            const int64_t body_hi = sp.vlo + (sp.nvec << 3);
+            cudaError_t e = launch_rs_tma(g, out.ptr.p[0], out.off, sp.vlo, sp.nvec << 3, nd, st);
+            if (e != cudaErrorNotSupported) {
+                if (e != cudaSuccess) return e;
+                if (sp.vlo > sp.lo) {
+                    e = rs_ldg(g, out, false, r, nd, split_range(sp.lo, sp.vlo, false), st);
+                    if (e != cudaSuccess) return e;
+                }
+                if (sp.hi > body_hi) e = rs_ldg(g, out, false, r, nd, split_range(body_hi, sp.hi, false), st);
+                return e;
+            }
+        }
+    }
+    return rs_ldg(g, out, out_by_owner, r, nd, sp, st);
 }
 
 cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, float* m, float* v,

@@ -726,6 +726,180 @@ cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float
     });
 }
 
+// ------------------------------------------------------------------ staged reduce-scatter-mean
+// The reduce-scatter with averaging alone, into one output array ("Infra: Data Parallel", ZeRO
+// section): out[i] = bf16(fold over ranks of fp32 g_q[i], ascending from +0, times 1/N_d or divided
+// by N_d), the same arithmetic as the fused kernel's first half.  The ring of k_fused_tma without the
+// optimizer state: the producer stages every rank's bf16 tile with one bulk copy each, consumers fold
+// from shared memory and stream the 16-bit results out.
+
+struct RsTmaArgs {
+    Ptrs g;               // rank gradients; element i of rank q at g.p[q] + (i - g_off)
+    int64_t g_off;
+    uint16_t* out;        // element i at out + (i - out_off)
+    int64_t out_off;
+    int64_t lo, n;        // body [lo, lo + n): lo, n, lo - g_off and lo - out_off multiples of 8
+    int nd;
+    float inv_nd;
+    long long wait_limit, drain_limit;
+};
+
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
+struct RsShape {
+    static constexpr int kT = NCW * 32 * VPT;
+    static constexpr int kStageBytes = kT * 2 * ND;
+    static constexpr int kFit = (BUDGET - 256) / kStageBytes;
+    static constexpr int kStages = kFit > MAXST ? MAXST : kFit;
+    static constexpr int kSmem = 256 + kStages * kStageBytes;
+    static_assert(kStages >= 2, "tile too large for a 2-stage ring");
+    static_assert(2 * kStages * 8 <= 256, "barriers must fit in the first 256 bytes");
+};
+
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant__ RsTmaArgs a) {
+    using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
+    constexpr int T = Sh::kT;
+    constexpr int S = Sh::kStages;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + S;
+    uint8_t* stages = smem + 256;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCW * 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int64_t ntiles = (a.n + T - 1) / T;
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            const uint64_t pol = evict_first_policy();
+            int64_t j = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+                const int s = (int)(j % S);
+                if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), a.wait_limit)) {
+                    flag_error(ZS_DEVERR_PRODUCER_WAIT);
+                    ok = false;
+                    break;
+                }
+                const int64_t i0 = a.lo + tile * T;
+                const int64_t rem = a.n - tile * T;
+                const uint32_t len = (uint32_t)(rem < T ? rem : T);
+                uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
+                mbar_expect_tx(&full[s], len * 2u * ND);
+#pragma unroll
+                for (int q = 0; q < ND; ++q)
+                    bulk_load(st + (size_t)q * T * 2, a.g.p[q] + (i0 - a.g_off), len * 2u, &full[s], pol);
+            }
+            if (!ok) {
+                const int64_t issued = j;
+                for (int64_t k = issued > S ? issued - S : 0; k < issued; ++k)
+                    mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int ct = threadIdx.x - 32;
+    const int e = ct * VPT;
+    int64_t j = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        const int s = (int)(j % S);
+        if (!mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
+            flag_error(ZS_DEVERR_CONSUMER_WAIT);
+            return;
+        }
+        const int64_t i0 = a.lo + tile * T;
+        const int64_t rem = a.n - tile * T;
+        const int len = (int)(rem < T ? rem : T);
+        if (e < len) {
+            const uint16_t* sg = reinterpret_cast<const uint16_t*>(stages + (size_t)s * Sh::kStageBytes);
+            float acc[VPT];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) acc[k] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < ND; ++q) {
+                float f[VPT];
+                lds_bf<VPT>(sg + (size_t)q * T + e, f);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+            }
+            mbar_arrive(&empty[s]);
+            uint32_t w[VPT / 2];
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2)
+                w[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], ND, a.inv_nd), mean_of_sum<ND>(acc[k + 1], ND, a.inv_nd));
+            uint16_t* o = a.out + (i0 + e - a.out_off);
+            if constexpr (VPT == 8)
+                __stcs(reinterpret_cast<uint4*>(o), make_uint4(w[0], w[1], w[2], w[3]));
+            else
+                __stcs(reinterpret_cast<uint2*>(o), make_uint2(w[0], w[1]));
+        } else {
+            mbar_arrive(&empty[s]);
+        }
+    }
+}
+
+namespace {
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
+    using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
+    auto kern = k_rs_tma<ND, NCW, VPT, MAXST, BUDGET>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), Sh::kSmem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
+    if (ntiles < 1) return cudaSuccess;
+    const int64_t cap = (int64_t)sms * per_sm;
+    const int grid = (int)(ntiles < cap ? ntiles : cap);
+    kern<<<grid, 32 * (NCW + 1), Sh::kSmem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Returns cudaErrorNotSupported when no staged shape exists for this rank count.
+cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
+                          cudaStream_t st) {
+    RsTmaArgs a;
+    a.g = g.ptr;
+    a.g_off = g.off;
+    a.out = out;
+    a.out_off = out_off;
+    a.lo = lo;
+    a.n = n;
+    a.nd = nd;
+    a.inv_nd = 1.0f / (float)nd;
+    a.wait_limit = 4000000000LL;
+    a.drain_limit = 4000000000LL;
+    // shapes per rank count from a measured sweep on GB300 (consumer warps x elements per thread x
+    // ring depth, 2^27-element buffers): 96 / 99 / 100 / 102 / 102 % of the measured copy rate for
+    // N_d = 2 / 4 / 8 / 16 / 32, against ~94 % for the register-streaming kernel
+    switch (nd) {
+        case 2: return rs_tma_impl<2, 4, 8, 2, 232448>(a, st);     // T 1024, 2 stages, 12 CTAs/SM
+        case 4: return rs_tma_impl<4, 4, 4, 2, 232448>(a, st);     // T 512, 2 stages, 12 CTAs/SM
+        case 8: return rs_tma_impl<8, 8, 8, 2, 232448>(a, st);     // T 2048, 2 stages, 3 CTAs/SM
+        case 16: return rs_tma_impl<16, 8, 8, 2, 232448>(a, st);   // T 2048, 2 stages, 1 CTA/SM
+        case 32: return rs_tma_impl<32, 2, 4, 2, 232448>(a, st);   // T 256, 2 stages, 6 CTAs/SM
+        default: return cudaErrorNotSupported;
+    }
+}
+
 // Self-test of the bounded wait: waits on an mbarrier nothing arrives at, with
 // a budget of `limit` cycles, then records ZS_DEVERR_SELFTEST and returns.
 __global__ void k_wait_selftest(long long limit) {

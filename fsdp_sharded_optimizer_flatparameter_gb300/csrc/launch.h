@@ -72,6 +72,11 @@ cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* 
                                 StagedPolicy staged_policy = kStagedIfDevice);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
 // One source to N_d destinations with bulk stores, over the 8-aligned body [lo, lo + n).
+// Staged reduce-scatter-mean of the body [lo, lo + n) into one array (element i at out + (i -
+// out_off)); the TMA alignment rules of launch_fused_tma.  cudaErrorNotSupported for rank counts
+// without a staged shape.
+cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
+                          cudaStream_t st);
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
                                int64_t n, int nd, cudaStream_t st);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);

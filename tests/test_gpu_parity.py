@@ -352,6 +352,39 @@ def test_staged_and_streaming_fused_kernels_agree_with_oracle(variant, n_d, nume
 
 
 @pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
+def test_staged_reduce_scatter_matches_oracle(variant, n_d):
+    """The staged reduce-scatter-mean (forced, every rank count with a shape) into one array, over the
+    whole space and bucket by bucket from per-bucket staging buffers (offset views, bucket edges off
+    the 8-element grid, so the fringes take the streaming kernel): the oracle's mean, bit for bit;
+    the in-place ZeRO-1 form (streaming kernel) agrees on the owned slices."""
+    numel = 1_100_003
+    plan, ref = _plans([(numel,)], n_d, bucket_bytes=2 * 300_001, stage=2)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads, _ = synth.rank_grads(n_d, P, pads, seed=65, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)
+    want = steps.reduce_mean([H.to_np_bf16(g) for g in grads])
+    variant(zs.ZS_FUSED_TMA)
+    ghat = torch.full((P,), 7.0, dtype=BF16, device=DEV)
+    zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    H.check_bf16(H.to_np_bf16(ghat), want, "whole space n_d=%d" % n_d)
+    ghat2 = torch.full((P,), 7.0, dtype=BF16, device=DEV)
+    for b in reversed(range(plan.n_buckets)):
+        _, lo, hi = plan.bucket(b)
+        staging = [g[lo:hi].clone() for g in grads]
+        zs.zs_reduce_scatter_mean(plan, b, staging, zs.ZS_RANK_BUCKET, [ghat2], zs.ZS_SHARDED)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    assert torch.equal(ghat2, ghat)
+    inplace = [g.clone() for g in grads]
+    zs.zs_reduce_scatter_mean(plan, -1, inplace, zs.ZS_RANK_FULL, inplace, zs.ZS_RANK_FULL)
+    torch.cuda.synchronize()
+    S = plan.shard_per_rank
+    for q in (0, n_d - 1):
+        assert torch.equal(inplace[q][q * S:(q + 1) * S], ghat[q * S:(q + 1) * S])
+
+
+@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
 def test_staged_zero3_rs_step_matches_streaming(variant, n_d):
     """The single-output staged kernel (every rank count's own shape) equals the streaming kernel."""
     shapes, units = _tiny_llama(n_layers=2, d=256, ffn=704, vocab=1000)
