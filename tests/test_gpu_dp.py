@@ -36,6 +36,25 @@ def test_all_reduce_mean(n_d, numel, bucket_bytes):
         H.check_bf16(H.to_np_bf16(grads[q]), want, "rank %d" % q)
 
 
+@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
+def test_staged_all_reduce_mean(n_d):
+    """The staged in-place all-reduce (forced, every rank count with a shape; ragged tail on the
+    streaming kernel): every rank's buffer holds the oracle's mean, bit for bit."""
+    plan = zs.Plan([(1_100_003,)], n_d, stage=0)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads, _ = synth.rank_grads(n_d, P, pads, seed=53, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)
+    want = steps.reduce_mean([H.to_np_bf16(g) for g in grads])
+    zs.zs_set_fused_variant(zs.ZS_FUSED_TMA)
+    try:
+        zs.zs_all_reduce_mean(plan, -1, grads)
+        torch.cuda.synchronize()
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    for q in (0, n_d // 2, n_d - 1):
+        H.check_bf16(H.to_np_bf16(grads[q]), want, "rank %d" % q)
+
+
 @pytest.mark.parametrize("n_d", [1, 3, 4, 8])
 def test_dp_step_matches_oracle_and_zero(n_d):
     shapes = [(300, 96), (96,), (257, 96), (5,)]
