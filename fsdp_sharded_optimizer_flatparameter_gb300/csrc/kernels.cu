@@ -669,33 +669,12 @@ static cudaError_t dp_step_impl(const BView& g, const BView& out, float* const* 
     return cudaGetLastError();
 }
 
-static cudaError_t all_reduce_ldg(const BView& g, int nd, const Split& sp, cudaStream_t st) {
+cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st) {
+    // the register-streaming kernel: a staged variant of this 1:1 read/write stream measured no faster
+    const Split sp = split_range(r.lo, r.hi, aligned8(g.off));
 #define ZS_AR(N) all_reduce_impl<N>(g, nd, sp, st)
     ZS_DISPATCH_ND(nd, ZS_AR)
 #undef ZS_AR
-}
-
-cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st) {
-    const Split sp = split_range(r.lo, r.hi, aligned8(g.off));
-    if ((sp.nvec << 3) >= kTmaMinElems && g_fused_variant.load() != ZS_FUSED_LDG &&
-        (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32)) {
-        const void* ps[ZS_MAX_RANKS];
-        for (int q = 0; q < nd; ++q) ps[q] = g.ptr.p[q];
-        if (all_device(ps, nd)) {
-            const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-            cudaError_t e = launch_all_reduce_tma(g, sp.vlo, sp.nvec << 3, nd, st);
-            if (e != cudaErrorNotSupported) {
-                if (e != cudaSuccess) return e;
-                if (sp.vlo > sp.lo) {
-                    e = all_reduce_ldg(g, nd, split_range(sp.lo, sp.vlo, false), st);
-                    if (e != cudaSuccess) return e;
-                }
-                if (sp.hi > body_hi) e = all_reduce_ldg(g, nd, split_range(body_hi, sp.hi, false), st);
-                return e;
-            }
-        }
-    }
-    return all_reduce_ldg(g, nd, sp, st);
 }
 
 cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,

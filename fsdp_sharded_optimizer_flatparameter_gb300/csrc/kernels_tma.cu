@@ -384,15 +384,15 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_list(const __grid_
                     const uint32_t len = (uint32_t)(rem < T ? rem : T);
                     meta_i0[s] = i0;                     // ordered before the arrive below (release)
                     meta_len[s] = len;
-                uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
-                mbar_expect_tx(&full[s], len * (2u * ND + 12u));
+                    uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
+                    mbar_expect_tx(&full[s], len * (2u * ND + 12u));
 #pragma unroll
-                for (int q = 0; q < ND; ++q)
-                    bulk_load(st + (size_t)q * T * 2, a.g.p[q] + (i0 - a.g_off), len * 2u, &full[s], pol);
-                float* sf = reinterpret_cast<float*>(st + (size_t)ND * T * 2);
-                bulk_load(sf, a.master + i0, len * 4u, &full[s], pol);
-                bulk_load(sf + T, a.m + i0, len * 4u, &full[s], pol);
-                bulk_load(sf + 2 * T, a.v + i0, len * 4u, &full[s], pol);
+                    for (int q = 0; q < ND; ++q)
+                        bulk_load(st + (size_t)q * T * 2, a.g.p[q] + (i0 - a.g_off), len * 2u, &full[s], pol);
+                    float* sf = reinterpret_cast<float*>(st + (size_t)ND * T * 2);
+                    bulk_load(sf, a.master + i0, len * 4u, &full[s], pol);
+                    bulk_load(sf + T, a.m + i0, len * 4u, &full[s], pol);
+                    bulk_load(sf + 2 * T, a.v + i0, len * 4u, &full[s], pol);
                 }
             }
             if (ok) {
@@ -736,7 +736,7 @@ cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float
 struct RsTmaArgs {
     Ptrs g;               // rank gradients; element i of rank q at g.p[q] + (i - g_off)
     int64_t g_off;
-    Ptrs out;             // element i at out.p[0] + (i - out_off); broadcast form: every out.p[q]
+    uint16_t* out;        // element i at out + (i - out_off)
     int64_t out_off;
     int64_t lo, n;        // body [lo, lo + n): lo, n, lo - g_off and lo - out_off multiples of 8
     int nd;
@@ -755,7 +755,7 @@ struct RsShape {
     static_assert(2 * kStages * 8 <= 256, "barriers must fit in the first 256 bytes");
 };
 
-template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024, bool BROADCAST = false>
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant__ RsTmaArgs a) {
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
@@ -839,14 +839,11 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant
 #pragma unroll
             for (int k = 0; k < VPT; k += 2)
                 w[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], ND, a.inv_nd), mean_of_sum<ND>(acc[k + 1], ND, a.inv_nd));
-            const int64_t io = i0 + e - a.out_off;
-#pragma unroll
-            for (int q = 0; q < (BROADCAST ? ND : 1); ++q) {
-                if constexpr (VPT == 8)
-                    __stcs(reinterpret_cast<uint4*>(a.out.p[q] + io), make_uint4(w[0], w[1], w[2], w[3]));
-                else
-                    __stcs(reinterpret_cast<uint2*>(a.out.p[q] + io), make_uint2(w[0], w[1]));
-            }
+            uint16_t* o = a.out + (i0 + e - a.out_off);
+            if constexpr (VPT == 8)
+                __stcs(reinterpret_cast<uint4*>(o), make_uint4(w[0], w[1], w[2], w[3]));
+            else
+                __stcs(reinterpret_cast<uint2*>(o), make_uint2(w[0], w[1]));
         } else {
             mbar_arrive(&empty[s]);
         }
@@ -855,10 +852,10 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant
 
 namespace {
 
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool BROADCAST = false>
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
 cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
-    auto kern = k_rs_tma<ND, NCW, VPT, MAXST, BUDGET, BROADCAST>;
+    auto kern = k_rs_tma<ND, NCW, VPT, MAXST, BUDGET>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
@@ -881,8 +878,8 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
     RsTmaArgs a;
     a.g = g.ptr;
     a.g_off = g.off;
-    a.out = g.ptr;
-    a.out_off = g.off;
+    a.out = nullptr;
+    a.out_off = 0;
     a.lo = lo;
     a.n = n;
     a.nd = nd;
@@ -892,27 +889,10 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
     return a;
 }
 
-// The all-reduce with averaging in place: every rank's buffer gets the mean (the naive-DP collective,
-// "Infra: Data Parallel", section on naive data parallelism).  Staging a whole tile of every rank
-// before any result is written makes the in-place update safe.  Shapes from a measured sweep
-// (2^27 elements): 95.4 / 94.5 / 95.8 / 95.1 / 95.7 % of the copy rate for N_d = 2 .. 32, against
-// ~93.6 % for the register-streaming kernel at N_d = 8.
-cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd, cudaStream_t st) {
-    const RsTmaArgs a = rs_args(g, lo, n, nd);
-    switch (nd) {
-        case 2: return rs_tma_impl<2, 8, 4, 2, 232448, true>(a, st);     // T 1024, 2 stages
-        case 4: return rs_tma_impl<4, 8, 8, 4, 232448, true>(a, st);     // T 2048, 4 stages
-        case 8: return rs_tma_impl<8, 8, 8, 4, 232448, true>(a, st);     // T 2048, 4 stages, 1 CTA/SM
-        case 16: return rs_tma_impl<16, 8, 8, 2, 232448, true>(a, st);   // T 2048, 2 stages, 1 CTA/SM
-        case 32: return rs_tma_impl<32, 8, 4, 2, 232448, true>(a, st);   // T 1024, 2 stages, 1 CTA/SM
-        default: return cudaErrorNotSupported;
-    }
-}
-
 cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
                           cudaStream_t st) {
     RsTmaArgs a = rs_args(g, lo, n, nd);
-    a.out.p[0] = out;
+    a.out = out;
     a.out_off = out_off;
     // shapes per rank count from a measured sweep on GB300 (consumer warps x elements per thread x
     // ring depth, 2^27-element buffers): 96 / 99 / 100 / 102 / 102 % of the measured copy rate for

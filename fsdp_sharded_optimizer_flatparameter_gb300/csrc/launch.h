@@ -77,9 +77,6 @@ cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
 // without a staged shape.
 cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
                           cudaStream_t st);
-// Staged in-place all-reduce-mean of the body [lo, lo + n) of every rank's buffer g.ptr.p[q];
-// cudaErrorNotSupported for rank counts without a staged shape.
-cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd, cudaStream_t st);
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
                                int64_t n, int nd, cudaStream_t st);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);

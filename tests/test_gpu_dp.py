@@ -37,9 +37,10 @@ def test_all_reduce_mean(n_d, numel, bucket_bytes):
 
 
 @pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
-def test_staged_all_reduce_mean(n_d):
-    """The staged in-place all-reduce (forced, every rank count with a shape; ragged tail on the
-    streaming kernel): every rank's buffer holds the oracle's mean, bit for bit."""
+def test_all_reduce_mean_every_rank_count(n_d):
+    """The in-place all-reduce on a million-element buffer with a ragged tail, with the staged variant
+    requested (the all-reduce keeps its streaming kernel either way): every rank's buffer holds the
+    oracle's mean, bit for bit."""
     plan = zs.Plan([(1_100_003,)], n_d, stage=0)
     P, pads = plan.padded, plan.pad_ranges()
     grads, _ = synth.rank_grads(n_d, P, pads, seed=53, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)
