@@ -229,6 +229,76 @@ def time_oracle(n_d, sample_elems, sigma, outlier_p, seed, min_seconds, max_reps
     return el / done, done, plan.padded
 
 
+def time_oracle_rows(seconds=1.5):
+    """The oracle beside each widening row, each on a bounded sample (params or elements per second,
+    one host thread): naive-DP step, ZeRO-3 unit step, FSDP2 chunk-cat + copy-out, checkpoint save +
+    resharded load (in memory)."""
+    import numpy as np
+
+    from oracle import checkpoint as ock
+    from oracle import fsdp2 as ofs
+    from oracle import layout, steps
+
+    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+
+    def rate(fn, elems):
+        done, t0 = 0, time.perf_counter()
+        while True:
+            fn(done + 1)
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return elems * done / el, done
+
+    n_d, E = 8, 1 << 18
+    out = {}
+    g_np, master = oracle_sample(n_d, E, 1e-3, 0.0, 1)
+    st = {"p": master.copy(), "m": np.zeros(E, np.float32), "v": np.zeros(E, np.float32)}
+
+    def dp(t):
+        _, st["p"], st["m"], st["v"] = steps.dp_step(g_np, st["p"], st["m"], st["v"], synth.HPARAMS, t)
+    r, k = rate(dp, E)
+    out["naive_dp"] = {"params_per_s": r, "sample": "oracle naive-DP step, %d elements, N_d=%d, %d steps" % (E, n_d, k)}
+
+    plan = layout.make_plan([(E,)], n_d, unit_of_param=[0])
+    sh = [np.zeros(plan.shard_total, np.uint16) for _ in range(n_d)]
+    z = {"m": [steps.shard_of(plan, q, master) for q in range(n_d)],
+         "mm": [np.zeros(plan.shard_total, np.float32) for _ in range(n_d)],
+         "v": [np.zeros(plan.shard_total, np.float32) for _ in range(n_d)]}
+
+    def z3(t):
+        _, _, _, z["m"], z["mm"], z["v"] = steps.zero3_unit_step(plan, 0, sh, g_np, z["m"], z["mm"], z["v"],
+                                                                  synth.HPARAMS, t)
+    r, k = rate(z3, E)
+    out["zero3"] = {"params_per_s": r, "sample": "oracle ZeRO-3 unit step (2 gathers + RS + AdamW), %d elements, "
+                    "N_d=%d, %d steps" % (E, n_d, k)}
+
+    shapes = [(512, 256)] * 2 + [(256,)]
+    p2 = ofs.make_plan(shapes, n_d)
+    vals = [np.arange(int(np.prod(sh_)), dtype=np.uint16) for sh_ in shapes]
+    n2 = sum(int(np.prod(sh_)) for sh_ in shapes)
+
+    def f2(_):
+        ofs.copy_out(p2, 0, ofs.chunk_cat(p2, 0, vals))
+    r, k = rate(f2, n2)
+    out["fsdp2_copy"] = {"elements_per_s": r, "sample": "oracle chunk-cat + copy-out of %d elements, N_d=%d, %d rounds"
+                         % (n2, n_d, k)}
+
+    p8, p4 = layout.make_plan([(E,)], 8), layout.make_plan([(E,)], 4)
+    ranks = [{"params": np.zeros(p8.shard_total, np.uint16), "master": np.zeros(p8.shard_total, np.float32),
+              "m": np.zeros(p8.shard_total, np.float32), "v": np.zeros(p8.shard_total, np.float32)}
+             for _ in range(8)]
+
+    def ck(_):
+        saved = ock.save(p8, ranks)
+        for name in ("params", "master", "m", "v"):
+            ock.load(p4, saved, name)
+    r, k = rate(ck, E)
+    out["checkpoint"] = {"params_per_s": r, "sample": "oracle save at N_d=8 + load at N_d=4 (in memory), %d elements, "
+                         "%d rounds" % (E, k)}
+    return out
+
+
 def cpu_threads_used():
     # numpy element-wise ufuncs run on one thread
     return 1
@@ -673,6 +743,22 @@ def run_next(args, ws, rank, local):
     clocks = sampler.stop()
 
     head = next(r for r in rows if r["row"].startswith("FSDP2 layout fused step"))
+    cpu = None
+    if rank == 0 and not small and not args.no_cpu_baseline:
+        orc = time_oracle_rows()
+        for r in rows:
+            key = ("naive_dp" if r["row"].startswith("naive DP") else "zero3" if r["row"].startswith("ZeRO-3")
+                   else "fsdp2_copy" if "k_fsdp2_copy" in r["row"] else "checkpoint" if r["row"].startswith("checkpoint")
+                   else None)
+            if key:
+                r["cpu_oracle"] = orc[key]
+        sec, k, padded = time_oracle(n_d, 1 << 20, 5e-4, 1e-3, 2, min_seconds=5.0)
+        cpu = {"value": padded / sec, "unit": "params/s", "cores": cpu_threads_used(), "kind": "oracle",
+               "sample": "oracle ZeRO step (numpy fp32) on a %d-element flat sample, N_d=%d, %d steps in %.1f s"
+                         % (padded, n_d, k, sec * k)}
+        for r in rows:
+            if r["row"].startswith("FSDP2 layout fused step") or r["row"].startswith("ZeRO-1/2 fused step"):
+                r["cpu_oracle"] = {"params_per_s": cpu["value"], "sample": cpu["sample"]}
     if rank == 0:
         line = {
             "metric": METRIC, "value": ws * head["params_per_s"], "unit": "params/s", "n_gpus": ws, "steps": steps,
@@ -685,6 +771,8 @@ def run_next(args, ws, rank, local):
                          "frac": head["gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
             "rows": rows, "gpu_launches": launches, "clocks": clocks,
         }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

@@ -17,6 +17,7 @@
 #include <atomic>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "device.cuh"
 
@@ -679,6 +680,8 @@ cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaS
 
 cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,
                            const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
+    // the register-streaming kernel: a staged variant (every rank's state staged per tile, one rank's
+    // update after another from shared memory) measured slower, 88 % against 93 % at N_d = 8
     const Split sp = split_range(r.lo, r.hi, aligned8(g.off) && aligned8(out.off));
 #define ZS_DP(N) dp_step_impl<N>(g, out, master, m, v, s, nd, sp, st)
     ZS_DISPATCH_ND(nd, ZS_DP)

@@ -56,6 +56,36 @@ def test_all_reduce_mean_every_rank_count(n_d):
         H.check_bf16(H.to_np_bf16(grads[q]), want, "rank %d" % q)
 
 
+@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
+def test_dp_step_every_rank_count(n_d):
+    """The naive-DP step on a 600K-element buffer with a ragged tail, every power-of-two rank count
+    (the staged variant requested; the DP step keeps its streaming kernel either way), two steps:
+    every rank's state and replica equal the oracle's, bit for bit."""
+    plan = zs.Plan([(600_003,)], n_d, stage=0)
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=54, device=DEV)
+    dm = [master0.clone() for _ in range(n_d)]
+    dmm = [torch.zeros_like(master0) for _ in range(n_d)]
+    dv = [torch.zeros_like(master0) for _ in range(n_d)]
+    reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    om, omm, ov = H.to_np_f32(master0), np.zeros(P, np.float32), np.zeros(P, np.float32)
+    zs.zs_set_fused_variant(zs.ZS_FUSED_TMA)
+    try:
+        for t in (1, 2):
+            grads, _ = synth.rank_grads(n_d, P, pads, seed=54, step=t, sigma=1e-3, outlier_p=0.001, device=DEV)
+            reps_ref, om, omm, ov = steps.dp_step([H.to_np_bf16(g) for g in grads], om, omm, ov, HP, t)
+            zs.zs_dp_step(plan, grads, dm, dmm, dv, reps, HP, t)
+            torch.cuda.synchronize()
+            assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+            for q in (0, n_d - 1):
+                H.check_f32(H.to_np_f32(dm[q]), om, "master rank %d t=%d" % (q, t))
+                H.check_f32(H.to_np_f32(dmm[q]), omm, "m rank %d t=%d" % (q, t))
+                H.check_f32(H.to_np_f32(dv[q]), ov, "v rank %d t=%d" % (q, t))
+                H.check_bf16(H.to_np_bf16(reps[q]), reps_ref[q], "replica %d t=%d" % (q, t))
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+
+
 @pytest.mark.parametrize("n_d", [1, 3, 4, 8])
 def test_dp_step_matches_oracle_and_zero(n_d):
     shapes = [(300, 96), (96,), (257, 96), (5,)]
