@@ -77,6 +77,24 @@ cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
 // without a staged shape.
 cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
                           cudaStream_t st);
+// FSDP2 layout copies (csrc/fsdp2.cu): one launch covers up to kFsdp2PerLaunch parameters of a
+// group; every (parameter, rank) piece is cut into tasks of kFsdp2Task buffer elements, task t of
+// the launch belonging to the last piece j with first[j] <= t (rank = (t - first[j]) / tasks).
+constexpr int kFsdp2PerLaunch = 64;
+constexpr int64_t kFsdp2Task = 16384;
+struct Fsdp2Piece {
+    uint16_t* param;        // the parameter's own layout (d0 x row elements)
+    int64_t d0, row, chunk, off;
+    int64_t tasks;          // tasks per rank: ceil(chunk * row / kFsdp2Task)
+};
+struct Fsdp2CopyArgs {
+    Fsdp2Piece p[kFsdp2PerLaunch];
+    int64_t first[kFsdp2PerLaunch + 1];
+    int n;                  // pieces in this launch
+    uint16_t* flat;         // the group's buffer (N_d * shard elements)
+    int64_t shard;
+    int to_flat;            // 1: parameters -> buffer (zero padding rows), 0: buffer -> parameters
+};
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
                                int64_t n, int nd, cudaStream_t st);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);

@@ -62,6 +62,22 @@ def _compare_plans(shapes, n_d, units=None, bucket_bytes=0, stage=1, sample_para
     return ours, ref
 
 
+def test_python_constants_match_the_header():
+    """Every ZS_* integer constant of the binding has the value include/zs.h gives it."""
+    text = open(os.path.join(ROOT, "include", "zs.h")).read()
+    pairs = re.findall(r"#define\s+(ZS_[A-Z0-9_]+)\s+\(?(-?\d+)[uUlL]*\)?\s", text)
+    pairs += re.findall(r"\b(ZS_[A-Z0-9_]+)\s*=\s*(-?\d+)", text)
+    checked = 0
+    for name, value in pairs:
+        if hasattr(zs, name):
+            assert getattr(zs, name) == int(value), name
+            checked += 1
+    assert checked >= 20
+    names = {n for n, _ in pairs}
+    for n in ("ZS_DEVERR_GATHER_WAIT", "ZS_BUCKETS_ONE_WALK", "ZS_BUCKETS_PER_BUCKET", "ZS_FUSED_TMA"):
+        assert n in names and hasattr(zs, n), n
+
+
 def test_plan_matches_oracle_on_tiny_plans():
     rng = random.Random(5)
     for _ in range(150):

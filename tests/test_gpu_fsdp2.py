@@ -30,6 +30,34 @@ def _bf16_param(rng, shape, scale):
     return numerics.bf16_rne((rng.standard_normal(n) * scale).astype(np.float32))
 
 
+@pytest.mark.parametrize("n_d", [2, 8])
+def test_chunk_cat_and_copy_out_aligned_groups(n_d):
+    """Every piece of the first group 16-byte aligned in both layouts (the vector path throughout):
+    pieces of several 16K-element tasks, a last rank with fewer rows (zero padding rows), a
+    parameter with fewer rows than ranks; the second group has 5-element rows (element path)."""
+    shapes = [(4096, 64), (1003, 128), (4, 64), (64, 8), (40, 5)]
+    units = [0, 0, 0, 0, 1]
+    plan = zs.Plan(shapes, n_d, unit_of_param=units, layout=zs.ZS_LAYOUT_FSDP2)
+    ref = fsdp2.make_plan(shapes, n_d, unit_of_param=units)
+    nrng = np.random.default_rng(70 + n_d)
+    vals = [_bf16_param(nrng, s_, 1.0) for s_ in shapes]
+    for u in range(plan.n_units):
+        members = [k for k in range(len(shapes)) if units[k] == u]
+        dev_params = [H.from_np_bf16(vals[k]).reshape(shapes[k]) for k in members]
+        flat = torch.full((plan.unit(u)["padded"],), -3.0, dtype=BF16, device=DEV)
+        zs.zs_fsdp2_chunk_cat(plan, u, dev_params, flat)
+        torch.cuda.synchronize()
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+        want = fsdp2.chunk_cat(ref, u, vals)
+        assert np.array_equal(H.to_np_bf16(flat), want)
+        outs = [torch.full_like(x, 5.0) for x in dev_params]
+        zs.zs_fsdp2_copy_out(plan, u, flat, outs)
+        torch.cuda.synchronize()
+        back = fsdp2.copy_out(ref, u, want)
+        for x, k in zip(outs, members):
+            assert np.array_equal(H.to_np_bf16(x.reshape(-1)), back[k])
+
+
 @pytest.mark.parametrize("n_d", [3, 8])
 def test_chunk_cat_and_copy_out_large_pieces_and_many_params(n_d):
     """Pieces spanning many 16K-element copy tasks, padding rows inside a task, rows of odd length
