@@ -836,7 +836,7 @@ def run_ours(args, ws, rank, local):
 
     # the unfused path on the same buffers, for comparison (not part of value)
     unfused = None
-    if W.kind == "fused" and not args.profile_case and rank == 0 and args.unfused_steps > 0:
+    if W.kind == "fused" and rank == 0 and args.unfused_steps > 0:
         # the unfused ZeRO-2 step on the same buffers, each kernel timed on its own (not part of value)
         ghat = torch.empty(P, dtype=torch.bfloat16, device=dev)
         shards = torch.empty(P, dtype=torch.bfloat16, device=dev)
