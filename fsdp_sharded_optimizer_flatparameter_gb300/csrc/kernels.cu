@@ -12,7 +12,8 @@
 // runs element by element throughout.  The rank count N_d is a template
 // parameter for the common powers of two so the rank loops unroll; other
 // counts use the runtime value.  Nothing here waits on anything, so no kernel
-// can hang.
+// can hang.  The launchers below also choose, per call, the bulk-copy staged
+// kernels (kernels_tma.cu) for large bodies whose buffers are all device memory.
 #include <algorithm>
 #include <atomic>
 #include <mutex>

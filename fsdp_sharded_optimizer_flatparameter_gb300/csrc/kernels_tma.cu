@@ -1,9 +1,12 @@
-// Fused step with bulk-copy (TMA engine) staging of the inputs, sm_103a.
+// Kernels with bulk-copy (TMA engine) staging, sm_103a: the fused step over one range
+// (k_fused_tma) and over a list of ranges (k_fused_tma_list), the reduce-scatter-mean alone
+// (k_rs_tma), and the gather from one source into N_d destinations with bulk stores
+// (k_gather_bulk).
 //
-// Same arithmetic as the register-streaming fused kernel (reduce-mean over
+// The fused step: same arithmetic as the register-streaming fused kernel (reduce-mean over
 // ranks, AdamW, bf16 cast, store into every replica: "Infra: Data Parallel",
 // ZeRO section), different data movement.  The flat range is cut into tiles
-// of T elements.  Each CTA is persistent (one per SM) and owns a ring of
+// of T elements.  Each CTA is persistent (one wave of resident CTAs) and owns a ring of
 // STAGES shared-memory stages; a stage holds one tile of every rank's bf16
 // gradients and of the fp32 master, m and v.  One producer thread issues the
 // N_d + 3 one-dimensional bulk copies of a tile (cp.async.bulk, completion
@@ -12,10 +15,10 @@
 // elements from shared memory, streams its results straight to global memory
 // and releases the stage on its "empty" mbarrier.  With up to STAGES-1 tiles
 // in flight per CTA the loads keep up to ~200 KB of reads outstanding per SM
-// independent of register pressure.  The tile shape per rank count (warps,
-// elements per thread, ring depth, one or two CTAs per SM) was picked by
-// measurement; ring depth is not monotone in benefit on GB300 (for N_d = 8,
-// 8 stages of 1024 elements beat both 6-7 and 16 stages).
+// independent of register pressure.  The tile shape per rank count and output form (warps,
+// elements per thread, ring depth, CTAs per SM) was picked by measurement; ring depth is not
+// monotone in benefit on GB300 (for N_d = 8 broadcast, 8 stages of 1024 elements beat both 6-7
+// and 16 stages).
 //
 // Every wait is bounded (clock64 budget).  A wait that runs out sets
 // g_zs_device_error, the CTA stops taking tiles, the producer waits (again
