@@ -93,12 +93,16 @@ KERNEL_SOURCES = {
 
 
 def source_digest(kernel_key):
-    """Digest of the files that define a kernel (a profile of it is valid only for these sources)."""
+    """Digest of the code of the files that define a kernel (a profile of it is valid only for this
+    code); line comments and blank lines are left out, so editing a comment keeps a profile valid."""
+    import re
+
     csrc = os.path.join(ROOT, "fsdp_sharded_optimizer_flatparameter_gb300", "csrc")
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel_key]:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name)) as f:
+            code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in f.read().splitlines()]
+        h.update(name.encode() + b"\0" + "\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()[:16]
 
 
