@@ -70,7 +70,7 @@ extern "C" {
 #define ZS_ERR_INVALID     (-1)   /* bad argument: nothing was enqueued              */
 #define ZS_ERR_CUDA        (-2)   /* a CUDA runtime call or launch failed            */
 #define ZS_ERR_OOM_HOST    (-3)   /* host allocation for plan tables failed          */
-#define ZS_ERR_UNSUPPORTED (-5)   /* valid request this build does not implement     */
+#define ZS_ERR_UNSUPPORTED (-5)   /* valid request the library does not implement     */
 
 #define ZS_STAGE_DP     0         /* naive data parallel (no sharding)               */
 #define ZS_STAGE_ZERO1  1         /* optimizer state sharded                         */
