@@ -516,7 +516,7 @@ def zs_fused_step_buckets(plan, buckets, grads, master, m, v, replicas, hp, step
                           side_stream=None):
     """buckets: bucket indices in stepping order.  launch_mode: ZS_BUCKETS_ONE_WALK (default: one
     persistent launch walks them) or ZS_BUCKETS_PER_BUCKET (one launch each; odd positions on
-    side_stream if given)."""
+    side_stream if given).  Gradients and replicas may be pinned host memory, as for zs_fused_step."""
     _n_ptrs(ZS_RANK_FULL, grads, plan.n_d, "grads")
     _n_ptrs(ZS_RANK_FULL, replicas, plan.n_d, "replicas")
     n = plan.padded
@@ -524,9 +524,9 @@ def zs_fused_step_buckets(plan, buckets, grads, master, m, v, replicas, hp, step
     mode = ZS_BUCKETS_ONE_WALK if launch_mode is None else int(launch_mode)
     side = None if side_stream is None else _stream(side_stream)
     return _check(_lib.zs_fused_step_buckets(
-        plan.handle, len(buckets), ids, _ptr_array(grads, n, 2, "grads"), _addr(master, n, 4, "master"),
-        _addr(m, n, 4, "m"), _addr(v, n, 4, "v"), _ptr_array(replicas, n, 2, "replicas"), ctypes.byref(_hp(hp)),
-        int(step), mode, _stream(stream), side))
+        plan.handle, len(buckets), ids, _ptr_array(grads, n, 2, "grads", "pinned_ok"), _addr(master, n, 4, "master"),
+        _addr(m, n, 4, "m"), _addr(v, n, 4, "v"), _ptr_array(replicas, n, 2, "replicas", "pinned_ok"),
+        ctypes.byref(_hp(hp)), int(step), mode, _stream(stream), side))
 
 
 def zs_set_fused_variant(variant):

@@ -556,6 +556,33 @@ def test_fused_step_reads_and_writes_pinned_host_memory(variant):
         zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
 
 
+@pytest.mark.parametrize("variant", [zs.ZS_FUSED_AUTO, zs.ZS_FUSED_TMA])
+def test_bucket_walk_with_pinned_host_gradients(variant):
+    """A bucket walk (every other bucket, then the rest) whose gradients are pinned host memory runs
+    on the streaming kernel, range by range, and equals the all-device whole-range step."""
+    zs.zs_set_fused_variant(variant)
+    try:
+        plan, _ = _plans([(2_000_003,)], 4, bucket_bytes=1 << 20)
+        P, pads = plan.padded, plan.pad_ranges()
+        master0 = synth.master_init(P, pads, seed=15, device=DEV)
+        a, b = State(master0), State(master0)
+        reps_a = synth.rank_buffers(4, P, BF16, DEV)[0]
+        reps_b = synth.rank_buffers(4, P, BF16, DEV)[0]
+        grads, _ = synth.rank_grads(4, P, pads, seed=15, step=1, sigma=1e-3, device=DEV)
+        host = [g.cpu().pin_memory() for g in grads]
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *a.args(), reps_a, HP, 1)
+        order = list(reversed(range(plan.n_buckets)))
+        for part in (order[0::2], order[1::2]):
+            zs.zs_fused_step_buckets(plan, part, host, *b.args(), reps_b, HP, 1)
+        torch.cuda.synchronize()
+        for x, y in zip(a.args(), b.args()):
+            assert torch.equal(x, y)
+        assert all(torch.equal(x, y) for x, y in zip(reps_a, reps_b))
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+
+
 # ---------------------------------------------------------------- bulk-store gather
 
 @pytest.mark.parametrize("n_d,numel", [(2, 3_000_001), (3, 1_500_007), (8, 4_194_305), (16, 2_100_003), (64, 1_048_583)])
