@@ -303,6 +303,30 @@ def time_oracle_rows(seconds=1.5):
     return out
 
 
+def _oracle_worker(job):
+    """One host process of the all-cores oracle timing (module level, so a spawned process can run it)."""
+    n_d, sample, sigma, outlier_p, seed, seconds = job
+    per_step, done, padded = time_oracle(n_d, sample, sigma, outlier_p, seed, seconds)
+    return padded * done, per_step * done
+
+
+def time_oracle_all_cores(n_d, sample, sigma, outlier_p, seed, seconds, procs=None):
+    """The oracle's ZeRO step on every host core at once: the step is element-wise, so disjoint
+    samples in separate processes are the whole step's work split over cores.  Processes are
+    spawned (never forked from a process that has touched the GPU)."""
+    import multiprocessing as mp
+
+    procs = procs or max(1, os.cpu_count() or 1)
+    jobs = [(n_d, sample, sigma, outlier_p, seed + 7919 * k, seconds) for k in range(procs)]
+    t0 = time.perf_counter()
+    with mp.get_context("spawn").Pool(procs) as pool:          # leaving the block terminates the workers
+        results = pool.map_async(_oracle_worker, jobs).get(timeout=4 * seconds + 120)
+    wall = time.perf_counter() - t0
+    elems = sum(e for e, _ in results)
+    busy = max(t for _, t in results)
+    return elems / busy, procs, elems, busy, wall
+
+
 def cpu_threads_used():
     # numpy element-wise ufuncs run on one thread
     return 1
@@ -889,12 +913,21 @@ def run_ours(args, ws, rank, local):
             e2e = {"value": None, "unit": "params/s", "error": str(exc)[:200]}
             torch.cuda.synchronize(dev)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline and not args.profile_case:
         per_step, done, padded = time_oracle(n_d, 1 << 20, W.wl["sigma"], W.wl["outlier_p"], W.wl["seed"], 10.0)
         cpu = {"value": padded / per_step, "unit": "params/s", "cores": cpu_threads_used(), "kind": "oracle",
                "sample": "oracle ZeRO step (numpy fp32) on a %d-element sample of the %s flat buffer, N_d=%d, "
                          "%d steps in %.1f s" % (padded, W.wl["model"], n_d, done, per_step * done)}
+        try:
+            rate, procs, elems, busy, _ = time_oracle_all_cores(n_d, 1 << 20, W.wl["sigma"], W.wl["outlier_p"],
+                                                                W.wl["seed"], 5.0)
+            cpu_all = {"value": rate, "unit": "params/s", "cores": procs, "kind": "oracle",
+                       "sample": "the same oracle step in %d spawned processes on disjoint %d-element samples "
+                                 "(element-wise, so this is the step split over cores), %d elements in %.1f s"
+                                 % (procs, 1 << 20, elems, busy)}
+        except Exception as exc:                          # no process pool on this host: say so
+            cpu_all = {"value": None, "error": str(exc)[:200]}
 
     if rank == 0:
         staged = W.staged()
@@ -920,6 +953,7 @@ def run_ours(args, ws, rank, local):
                          "algorithmic_bytes_per_step": algo_bytes, "kernel": W.kernel_label(),
                          "kernel_ms": step_ms},
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all if cpu is not None else None,
             "e2e": e2e,
             "e2e_alt": e2e_alt,
             "gpu_launches": launches * steps,
