@@ -189,6 +189,56 @@ def test_device_calls_reject_bad_arguments_before_launch():
                              ctypes.c_int64(1), None) == zs.ZS_ERR_INVALID
 
 
+def test_list_zero3_and_dp_calls_reject_bad_arguments_before_launch():
+    """The bucket-list, ZeRO-3 and naive-DP entry points refuse bad arguments with ZS_ERR_INVALID before
+    anything is enqueued (placeholder addresses: no case may reach a launch)."""
+    lib = ctypes.CDLL(zs.LIB_PATH)
+    for name in ("zs_fused_step_buckets", "zs_zero3_step", "zs_dp_step"):
+        getattr(lib, name).restype = ctypes.c_int32
+    p = zs.Plan([(64,)], 4, stage=2, bucket_bytes=32)          # 4 buckets of 16 elements
+    hp = zs.zs_adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1)
+    good = [0x10000 * (q + 1) for q in range(4)]
+    reps = [0x100000 * (q + 1) for q in range(4)]
+    S = ctypes.c_void_p
+
+    def arr(xs):
+        return (ctypes.c_void_p * len(xs))(*xs)
+
+    def ids(xs):
+        return (ctypes.c_int32 * max(len(xs), 1))(*xs)
+
+    def walk(buckets, grads=good, mode=zs.ZS_BUCKETS_ONE_WALK, n=None):
+        return lib.zs_fused_step_buckets(p.handle, ctypes.c_int32(len(buckets) if n is None else n), ids(buckets),
+                                         arr(grads), S(0x90000), S(0xA0000), S(0xB0000), arr(reps),
+                                         ctypes.byref(hp), ctypes.c_int64(1), ctypes.c_int32(mode), S(0), S(0))
+
+    assert walk([0, 4]) == zs.ZS_ERR_INVALID                                   # no such bucket
+    assert walk([1, 2, 1]) == zs.ZS_ERR_INVALID                                # repeated bucket
+    assert "twice" in zs.zs_last_error()
+    assert walk([0], mode=7) == zs.ZS_ERR_INVALID                              # unknown launch mode
+    assert walk([0], n=-1) == zs.ZS_ERR_INVALID                                # negative count
+    assert walk([0], grads=[good[0], 0, good[2], good[3]]) == zs.ZS_ERR_INVALID  # missing rank
+    assert lib.zs_fused_step_buckets(p.handle, 2, None, arr(good), S(0x90000), S(0xA0000), S(0xB0000), arr(reps),
+                                     ctypes.byref(hp), ctypes.c_int64(1), 0, S(0), S(0)) == zs.ZS_ERR_INVALID
+
+    p3 = zs.Plan([(64,), (32,), (16,)], 4, stage=3, unit_of_param=[0, 1, 2])   # three units
+    ug = arr(good * 3)
+    pool1 = arr(reps)                                                          # one slot: too few
+    assert lib.zs_zero3_step(p3.handle, S(0xC0000), S(0x90000), S(0xA0000), S(0xB0000), ug, pool1, 1, 1,
+                             ctypes.byref(hp), ctypes.c_int64(1), S(0), S(0)) == zs.ZS_ERR_INVALID
+    assert lib.zs_zero3_step(p3.handle, S(0xC0000), S(0x90000), S(0xA0000), S(0xB0000), ug, arr(reps + reps), 2, 0,
+                             ctypes.byref(hp), ctypes.c_int64(1), S(0), S(0)) == zs.ZS_ERR_INVALID  # needs 3 slots
+    assert lib.zs_zero3_step(p3.handle, S(0xC0000), S(0x90000), S(0xA0000), S(0xB0000), ug, arr(reps + reps), 2, 1,
+                             ctypes.byref(hp), ctypes.c_int64(0), S(0), S(0)) == zs.ZS_ERR_INVALID  # 0-based step
+
+    pd = zs.Plan([(64,)], 4, stage=0)
+    st = arr([0x200000 * (q + 1) for q in range(4)])
+    assert lib.zs_dp_step(pd.handle, arr(good), st, st, st, arr(reps), ctypes.byref(hp), ctypes.c_int64(0),
+                          S(0)) == zs.ZS_ERR_INVALID                           # 0-based step
+    assert lib.zs_dp_step(pd.handle, arr([good[0] + 4] + good[1:]), st, st, st, arr(reps), ctypes.byref(hp),
+                          ctypes.c_int64(1), S(0)) == zs.ZS_ERR_INVALID          # misaligned gradient
+
+
 def test_fused_variant_switch_validates():
     assert zs.zs_set_fused_variant(zs.ZS_FUSED_LDG) == zs.ZS_OK
     assert zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO) == zs.ZS_OK
