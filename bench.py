@@ -862,6 +862,34 @@ def run_ours(args, ws, rank, local):
     achieved = algo_bytes / (step_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
 
+    # the accumulate + fused step's launches timed one by one (not part of value)
+    breakdown = None
+    if W.kind == "accumulate+fused" and rank == 0:
+        micro = W.wl["micro"]
+        acc_ms, fused_ms = [[] for _ in range(micro)], []
+        for k in range(5):
+            W.t += 1
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(micro + 2)]
+            evs[0].record(stream)
+            for j in range(micro):
+                zs.zs_accumulate_grad(plan, W.acc, W.grads, 1.0 / micro, first=(j == 0), stream=stream)
+                evs[j + 1].record(stream)
+            zs.zs_fused_step(plan, -1, W.acc, zs.ZS_RANK_FULL, W.master, W.m, W.v, W.reps, W.hp, W.t, stream=stream)
+            evs[micro + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            if k >= 2:
+                for j in range(micro):
+                    acc_ms[j].append(evs[j].elapsed_time(evs[j + 1]))
+                fused_ms.append(evs[micro].elapsed_time(evs[micro + 1]))
+
+        def entry(ms, nbytes):
+            gbs = nbytes / (ms / 1e3) / 1e9
+            return {"ms": ms, "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak}
+
+        breakdown = {"accumulate_first": entry(statistics.mean(acc_ms[0]), 4 * n_d * P),
+                     "accumulate": entry(statistics.mean(statistics.mean(a) for a in acc_ms[1:]), 6 * n_d * P),
+                     "fused": entry(statistics.mean(fused_ms), bytes_per_padded_element(n_d, "fused") * P)}
+
     # the unfused path on the same buffers, for comparison (not part of value)
     unfused = None
     if W.kind == "fused" and rank == 0 and args.unfused_steps > 0:
@@ -959,6 +987,7 @@ def run_ours(args, ws, rank, local):
             "gpu_launches": launches * steps,
             "clocks": clocks,
             "unfused": unfused,
+            "kernels": breakdown,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
