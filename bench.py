@@ -564,6 +564,39 @@ def run_sweep(args, ws, rank, local):
         torch.cuda.empty_cache()
     clocks = sampler.stop()
     head = next(p for p in points if p["n_d"] == 8 and p["step"] == "fused, whole buffer")
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle beside each point: its ZeRO step and its ZeRO-3 unit step, per N_d, one thread
+        import numpy as np
+
+        from oracle import layout as olayout
+        from oracle import steps as osteps
+
+        for n_d in wl["sweep_n_d"]:
+            sec, k, padded = time_oracle(n_d, 1 << 18, wl["sigma"], 0.0, wl["seed"], min_seconds=1.0)
+            for p in points:
+                if p["n_d"] == n_d and p.get("stage") is None:
+                    p["cpu_oracle"] = {"params_per_s": padded / sec, "sample": "oracle ZeRO step, %d elements, "
+                                       "N_d=%d, %d steps" % (padded, n_d, k)}
+            oplan = olayout.make_plan([(1 << 18,)], n_d, unit_of_param=[0])
+            g_np, master = oracle_sample(n_d, oplan.padded, wl["sigma"], 0.0, wl["seed"])
+            sh = [np.zeros(oplan.shard_total, np.uint16) for _ in range(n_d)]
+            st = [[osteps.shard_of(oplan, q, master) for q in range(n_d)],
+                  [np.zeros(oplan.shard_total, np.float32) for _ in range(n_d)],
+                  [np.zeros(oplan.shard_total, np.float32) for _ in range(n_d)]]
+            done, t0 = 0, time.perf_counter()
+            while time.perf_counter() - t0 < 1.0:
+                done += 1
+                _, _, _, st[0], st[1], st[2] = osteps.zero3_unit_step(oplan, 0, sh, g_np, st[0], st[1], st[2],
+                                                                     synth.HPARAMS, done)
+            rate = oplan.padded * done / (time.perf_counter() - t0)
+            for p in points:
+                if p["n_d"] == n_d and p.get("stage") == 3:
+                    p["cpu_oracle"] = {"params_per_s": rate, "sample": "oracle ZeRO-3 unit step, %d elements, "
+                                       "N_d=%d, %d steps" % (oplan.padded, n_d, done)}
+        ref = next(p for p in points if p["n_d"] == 8 and p.get("stage") is None)["cpu_oracle"]
+        cpu = {"value": ref["params_per_s"], "unit": "params/s", "cores": cpu_threads_used(), "kind": "oracle",
+               "sample": ref["sample"]}
     if rank == 0:
         line = {
             "metric": METRIC, "value": ws * head["params_per_s"], "unit": "params/s", "n_gpus": ws, "steps": steps,
@@ -575,6 +608,8 @@ def run_sweep(args, ws, rank, local):
                          "frac": head["gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
             "sweep": points, "gpu_launches": launches, "clocks": clocks,
         }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
