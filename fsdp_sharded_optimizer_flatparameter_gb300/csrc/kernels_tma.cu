@@ -339,7 +339,6 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
 // k_fused_tma's: folding both into one generic loop cost the single-range kernel ~3 % on GB300).
 template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_list(const __grid_constant__ TmaListArgs l) {
-    constexpr bool BROADCAST = true;
     const TmaArgs& a = l.a;
     using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
@@ -429,37 +428,40 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_list(const __grid_
             flag_error(ZS_DEVERR_CONSUMER_WAIT);
             return;
         }
+        // the stage's data is read and computed on before its tile record is needed (a thread past the
+        // tile's end works on stale values of the stage and stores nothing), so the shared-memory
+        // reads of the record and of the data are issued together
         const int64_t i0 = meta_i0[s];
         const int len = (int)meta_len[s];
-        if (len == 0) return;
+        const uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
+        const uint16_t* sg = reinterpret_cast<const uint16_t*>(st);
+        const float* sf = reinterpret_cast<const float*>(st + (size_t)ND * T * 2);
+        float acc[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) acc[k] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < n; ++q) {
+            float f[VPT];
+            lds_bf<VPT>(sg + (size_t)q * T + e, f);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+        }
+        float p[VPT], mm[VPT], vv[VPT];
+        lds_f32<VPT>(sf + e, p);
+        lds_f32<VPT>(sf + T + e, mm);
+        lds_f32<VPT>(sf + 2 * T + e, vv);
+        if (len == 0) return;                            // the closing stage
+        uint32_t gw[VPT / 2];
+#pragma unroll
+        for (int k = 0; k < VPT; k += 2)
+            gw[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], n, a.inv_nd), mean_of_sum<ND>(acc[k + 1], n, a.inv_nd));
+#pragma unroll
+        for (int k = 0; k < VPT; k += 2) {
+            adamw_elem(bf16_lo(gw[k / 2]), p[k], mm[k], vv[k], a.s);
+            adamw_elem(bf16_hi(gw[k / 2]), p[k + 1], mm[k + 1], vv[k + 1], a.s);
+        }
+        mbar_arrive(&empty[s]);                          // this thread is done with the stage
         if (e < len) {
-            const uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
-            const uint16_t* sg = reinterpret_cast<const uint16_t*>(st);
-            const float* sf = reinterpret_cast<const float*>(st + (size_t)ND * T * 2);
-            float acc[VPT];
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) acc[k] = 0.0f;
-#pragma unroll
-            for (int q = 0; q < n; ++q) {
-                float f[VPT];
-                lds_bf<VPT>(sg + (size_t)q * T + e, f);
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
-            }
-            float p[VPT], mm[VPT], vv[VPT];
-            lds_f32<VPT>(sf + e, p);
-            lds_f32<VPT>(sf + T + e, mm);
-            lds_f32<VPT>(sf + 2 * T + e, vv);
-            uint32_t gw[VPT / 2];
-#pragma unroll
-            for (int k = 0; k < VPT; k += 2)
-                gw[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], n, a.inv_nd), mean_of_sum<ND>(acc[k + 1], n, a.inv_nd));
-#pragma unroll
-            for (int k = 0; k < VPT; k += 2) {
-                adamw_elem(bf16_lo(gw[k / 2]), p[k], mm[k], vv[k], a.s);
-                adamw_elem(bf16_hi(gw[k / 2]), p[k + 1], mm[k + 1], vv[k + 1], a.s);
-            }
-            mbar_arrive(&empty[s]);                      // this thread is done with the stage
             const int64_t i = i0 + e;
             stg_f32<VPT>(a.master + i, p);
             stg_f32<VPT>(a.m + i, mm);
@@ -469,23 +471,13 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_list(const __grid_
             for (int k = 0; k < VPT; k += 2) pw[k / 2] = pack_bf16x2(p[k], p[k + 1]);
             if constexpr (VPT == 8) {
                 const uint4 w = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                if constexpr (BROADCAST) {
 #pragma unroll
-                    for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint4*>(a.out.p[q] + (i - a.out_off)), w);
-                } else {
-                    __stcs(reinterpret_cast<uint4*>(a.out.p[0] + (i - a.out_off)), w);
-                }
+                for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint4*>(a.out.p[q] + (i - a.out_off)), w);
             } else {
                 const uint2 w = make_uint2(pw[0], pw[1]);
-                if constexpr (BROADCAST) {
 #pragma unroll
-                    for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint2*>(a.out.p[q] + (i - a.out_off)), w);
-                } else {
-                    __stcs(reinterpret_cast<uint2*>(a.out.p[0] + (i - a.out_off)), w);
-                }
+                for (int q = 0; q < n; ++q) __stcs(reinterpret_cast<uint2*>(a.out.p[q] + (i - a.out_off)), w);
             }
-        } else {
-            mbar_arrive(&empty[s]);
         }
     }
 }
