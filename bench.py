@@ -678,8 +678,15 @@ def run_next(args, ws, rank, local):
         t[0] += 1
         zs.zs_dp_step(plan, grads, master, mm, vv, reps, hp, t[0], stream=stream)
 
-    row("naive DP step (k_dp_step: all-reduce-mean + replicated AdamW), %s, N_d=8" % dp_label, timed(dp), plan.numel,
+    row("naive DP step (k_dp_tma: all-reduce-mean + replicated AdamW), %s, N_d=8" % dp_label, timed(dp), plan.numel,
         28 * n_d * P, 1)
+    launches += steps
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
+    try:
+        row("naive DP step, register-streaming kernel (k_dp_step), for comparison", timed(dp), plan.numel,
+            28 * n_d * P, 1)
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
     launches += steps
 
     def ar():

@@ -679,14 +679,44 @@ cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaS
 #undef ZS_AR
 }
 
-cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,
-                           const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
-    // the register-streaming kernel: a staged variant (every rank's state staged per tile, one rank's
-    // update after another from shared memory) measured slower, 88 % against 93 % at N_d = 8
-    const Split sp = split_range(r.lo, r.hi, aligned8(g.off) && aligned8(out.off));
+static cudaError_t dp_step_ldg(const BView& g, const BView& out, float* const* master, float* const* m,
+                               float* const* v, const Split& sp, const AdamScalars& s, int nd, cudaStream_t st) {
 #define ZS_DP(N) dp_step_impl<N>(g, out, master, m, v, s, nd, sp, st)
     ZS_DISPATCH_ND(nd, ZS_DP)
 #undef ZS_DP
+}
+
+cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,
+                           const Range& r, const AdamScalars& s, int nd, cudaStream_t st) {
+    // The staged kernel streams one rank's state at a time through its ring (an earlier staged
+    // variant that held every rank's state of a tile at once measured 88 % of the copy rate at
+    // N_d = 8, the register-streaming kernel 92-93 %).  The fused-variant switch selects here too.
+    const Split sp = split_range(r.lo, r.hi, aligned8(g.off) && aligned8(out.off));
+    const int variant = g_fused_variant.load();
+    bool staged = sp.nvec > 0 && (variant == ZS_FUSED_TMA || (variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems)) &&
+                  (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
+    if (staged) {
+        const void* ps[5 * ZS_MAX_RANKS];
+        int n = 0;
+        for (int q = 0; q < nd; ++q) {
+            ps[n++] = g.ptr.p[q];
+            ps[n++] = out.ptr.p[q];
+            ps[n++] = master[q];
+            ps[n++] = m[q];
+            ps[n++] = v[q];
+        }
+        staged = all_device(ps, n);
+    }
+    if (!staged) return dp_step_ldg(g, out, master, m, v, sp, s, nd, st);
+    const int64_t body_hi = sp.vlo + (sp.nvec << 3);
+    cudaError_t e = launch_dp_tma(g, out, master, m, v, sp.vlo, sp.nvec << 3, s, nd, st);
+    if (e != cudaSuccess) return e;
+    if (sp.vlo > sp.lo) {
+        e = dp_step_ldg(g, out, master, m, v, split_range(sp.lo, sp.vlo, false), s, nd, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (sp.hi > body_hi) e = dp_step_ldg(g, out, master, m, v, split_range(body_hi, sp.hi, false), s, nd, st);
+    return e;
 }
 
 }  // namespace zs

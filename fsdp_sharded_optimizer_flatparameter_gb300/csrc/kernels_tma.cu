@@ -1,7 +1,7 @@
 // Kernels with bulk-copy (TMA engine) staging, sm_103a: the fused step over one range
 // (k_fused_tma) and over a list of ranges (k_fused_tma_list), the reduce-scatter-mean alone
-// (k_rs_tma), and the gather from one source into N_d destinations with bulk stores
-// (k_gather_bulk).
+// (k_rs_tma), the gather from one source into N_d destinations with bulk stores
+// (k_gather_bulk), and the naive-DP step over N_d full replicated states (k_dp_tma).
 //
 // The fused step: same arithmetic as the register-streaming fused kernel (reduce-mean over
 // ranks, AdamW, bf16 cast, store into every replica: "Infra: Data Parallel",
@@ -873,7 +873,6 @@ cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-// Returns cudaErrorNotSupported when no staged shape exists for this rank count.
 static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
     RsTmaArgs a;
     a.g = g.ptr;
@@ -889,6 +888,7 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
     return a;
 }
 
+// Returns cudaErrorNotSupported when no staged shape exists for this rank count.
 cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
                           cudaStream_t st) {
     RsTmaArgs a = rs_args(g, lo, n, nd);
@@ -903,6 +903,277 @@ cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_
         case 8: return rs_tma_impl<8, 8, 8, 2, 232448>(a, st);     // T 2048, 2 stages, 3 CTAs/SM
         case 16: return rs_tma_impl<16, 8, 8, 2, 232448>(a, st);   // T 2048, 2 stages, 1 CTA/SM
         case 32: return rs_tma_impl<32, 2, 4, 2, 232448>(a, st);   // T 256, 2 stages, 6 CTAs/SM
+        default: return cudaErrorNotSupported;
+    }
+}
+
+// ------------------------------------------------------------------ naive-DP step, staged
+// "Infra: Data Parallel", section "Naive Data Parallelism": every rank keeps the full fp32 state
+// and applies the same AdamW update with the all-reduced bf16 mean.  Per tile of T elements the
+// producer stages every rank's bf16 gradients (two grads buffers, so the next tile's arrive while
+// this one's ranks are updated), then each rank's master, m and v in turn through a ring of S
+// state stages.  Consumers fold the mean once per tile and keep it in registers as bf16, then
+// update each rank's state as that rank's stage arrives and stream the results (state, replica)
+// straight to global memory.  The arithmetic is the register-streaming naive-DP kernel's; the
+// state of N_d ranks is 96 of the 112 bytes read per element at N_d = 8, so the ring stages one
+// rank's state at a time instead of holding every rank's state of a tile at once.
+
+struct DpTmaArgs {
+    Ptrs g;               // rank gradients; element i of rank q at g.p[q] + (i - g_off)
+    int64_t g_off;
+    Ptrs out;             // rank replicas; element i of rank q at out.p[q] + (i - out_off)
+    int64_t out_off;
+    float* master[ZS_MAX_RANKS];     // rank q's full fp32 state, element i at master[q] + i
+    float* m[ZS_MAX_RANKS];
+    float* v[ZS_MAX_RANKS];
+    AdamScalars s;
+    int64_t lo, n;        // body [lo, lo + n): lo, n, lo - g_off and lo - out_off multiples of 8
+    int nd;
+    float inv_nd;
+    long long wait_limit, drain_limit;
+};
+
+// Consumers index the ranks at run time (one copy of the update code, not N_d): the rank pointers
+// are copied from the kernel parameter into shared memory once per CTA, with compile-time indices.
+template <int ND>
+struct DpTable {
+    uint16_t* out[ND];
+    float* master[ND];
+    float* m[ND];
+    float* v[ND];
+};
+
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
+struct DpShape {
+    static constexpr int kT = NCW * 32 * VPT;                               // elements per tile
+    static constexpr int kBarBytes = 512;
+    static constexpr int kHead = kBarBytes + (int)((sizeof(DpTable<ND>) + 127) / 128 * 128);
+    static constexpr int kGradBytes = kT * 2 * ND;                          // one grads buffer
+    static constexpr int kStageBytes = kT * 12;                             // one rank's master, m, v
+    static constexpr int kFit = (BUDGET - kHead - 2 * kGradBytes) / kStageBytes;
+    static constexpr int kStages = kFit > MAXST ? MAXST : kFit;
+    static constexpr int kSmem = kHead + 2 * kGradBytes + kStages * kStageBytes;
+    static_assert(kStages >= 2, "tile too large for a 2-stage ring");
+    static_assert((4 + 2 * kStages) * 8 <= kBarBytes, "barriers must fit in their block");
+};
+
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
+__global__ void __launch_bounds__(32 * (NCW + 1), 1) k_dp_tma(const __grid_constant__ DpTmaArgs a) {
+    using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
+    constexpr int T = Sh::kT;
+    constexpr int S = Sh::kStages;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* gfull = reinterpret_cast<uint64_t*>(smem);     // [2] grads buffer b loaded
+    uint64_t* gempty = gfull + 2;                            // [2] grads buffer b folded
+    uint64_t* full = gfull + 4;                              // [S] state stage s loaded
+    uint64_t* empty = full + S;                              // [S] state stage s consumed
+    DpTable<ND>* tab = reinterpret_cast<DpTable<ND>*>(smem + Sh::kBarBytes);
+    uint16_t* gbuf = reinterpret_cast<uint16_t*>(smem + Sh::kHead);
+    uint8_t* stages = smem + Sh::kHead + 2 * Sh::kGradBytes;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&gfull[b], 1);
+            mbar_init(&gempty[b], NCW * 32);
+        }
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCW * 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+#pragma unroll
+        for (int q = 0; q < ND; ++q) {
+            if ((q & 31) == lane) {
+                tab->out[q] = a.out.p[q];
+                tab->master[q] = a.master[q];
+                tab->m[q] = a.m[q];
+                tab->v[q] = a.v[q];
+            }
+        }
+    }
+    __syncthreads();
+
+    const int64_t ntiles = (a.n + T - 1) / T;
+
+    if (warp == 0) {
+        // ---------------- producer: grads of a tile, then each rank's state of the tile
+        if (lane == 0) {
+            const uint64_t pol = evict_first_policy();
+            int64_t j = 0;        // state stages issued
+            int64_t gi = 0;       // grads buffers issued (= tiles started)
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const int b = (int)(gi & 1);
+                if (gi >= 2 && !mbar_wait(&gempty[b], (uint32_t)(((gi >> 1) - 1) & 1), a.wait_limit)) {
+                    flag_error(ZS_DEVERR_PRODUCER_WAIT);
+                    ok = false;
+                    break;
+                }
+                const int64_t i0 = a.lo + tile * T;
+                const int64_t rem = a.n - tile * T;
+                const uint32_t len = (uint32_t)(rem < T ? rem : T);
+                uint16_t* gb = gbuf + (size_t)b * ND * T;
+                mbar_expect_tx(&gfull[b], len * 2u * ND);
+#pragma unroll
+                for (int q = 0; q < ND; ++q)
+                    bulk_load(gb + (size_t)q * T, a.g.p[q] + (i0 - a.g_off), len * 2u, &gfull[b], pol);
+                ++gi;
+#pragma unroll
+                for (int q = 0; q < ND; ++q, ++j) {
+                    const int s = (int)(j % S);
+                    if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), a.wait_limit)) {
+                        flag_error(ZS_DEVERR_PRODUCER_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    float* sf = reinterpret_cast<float*>(stages + (size_t)s * Sh::kStageBytes);
+                    mbar_expect_tx(&full[s], len * 12u);
+                    bulk_load(sf, a.master[q] + i0, len * 4u, &full[s], pol);
+                    bulk_load(sf + T, a.m[q] + i0, len * 4u, &full[s], pol);
+                    bulk_load(sf + 2 * T, a.v[q] + i0, len * 4u, &full[s], pol);
+                }
+            }
+            if (!ok) {
+                // drain: wait (bounded) for the copies issued into buffers not yet consumed
+                for (int64_t k = gi > 2 ? gi - 2 : 0; k < gi; ++k)
+                    mbar_wait(&gfull[k & 1], (uint32_t)((k >> 1) & 1), a.drain_limit);
+                for (int64_t k = j > S ? j - S : 0; k < j; ++k)
+                    mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int ct = threadIdx.x - 32;                  // 0 .. NCW*32-1
+    const int e = ct * VPT;                           // this thread's first element in a tile
+    int64_t j = 0, t = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++t) {
+        const int b = (int)(t & 1);
+        if (!mbar_wait(&gfull[b], (uint32_t)((t >> 1) & 1), a.wait_limit)) {
+            flag_error(ZS_DEVERR_CONSUMER_WAIT);
+            return;
+        }
+        const int64_t i0 = a.lo + tile * T;
+        const int64_t rem = a.n - tile * T;
+        const int len = (int)(rem < T ? rem : T);
+        uint32_t gw[VPT / 2] = {};                    // the tile's mean, bf16 pairs, kept for every rank
+        if (e < len) {
+            const uint16_t* gb = gbuf + (size_t)b * ND * T;
+            float acc[VPT];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) acc[k] = 0.0f;
+#pragma unroll
+            for (int q = 0; q < ND; ++q) {
+                float f[VPT];
+                lds_bf<VPT>(gb + (size_t)q * T + e, f);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; k += 2)
+                gw[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], ND, a.inv_nd), mean_of_sum<ND>(acc[k + 1], ND, a.inv_nd));
+        }
+        mbar_arrive(&gempty[b]);
+#pragma unroll 1
+        for (int q = 0; q < ND; ++q, ++j) {
+            const int s = (int)(j % S);
+            if (!mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
+                flag_error(ZS_DEVERR_CONSUMER_WAIT);
+                return;
+            }
+            if (e < len) {
+                const float* sf = reinterpret_cast<const float*>(stages + (size_t)s * Sh::kStageBytes);
+                float p[VPT], mm[VPT], vv[VPT];
+                lds_f32<VPT>(sf + e, p);
+                lds_f32<VPT>(sf + T + e, mm);
+                lds_f32<VPT>(sf + 2 * T + e, vv);
+#pragma unroll
+                for (int k = 0; k < VPT; k += 2) {
+                    adamw_elem(bf16_lo(gw[k / 2]), p[k], mm[k], vv[k], a.s);
+                    adamw_elem(bf16_hi(gw[k / 2]), p[k + 1], mm[k + 1], vv[k + 1], a.s);
+                }
+                mbar_arrive(&empty[s]);                  // this thread is done with the stage
+                const int64_t i = i0 + e;
+                stg_f32<VPT>(tab->master[q] + i, p);
+                stg_f32<VPT>(tab->m[q] + i, mm);
+                stg_f32<VPT>(tab->v[q] + i, vv);
+                uint32_t pw[VPT / 2];
+#pragma unroll
+                for (int k = 0; k < VPT; k += 2) pw[k / 2] = pack_bf16x2(p[k], p[k + 1]);
+                uint16_t* o = tab->out[q] + (i - a.out_off);
+                if constexpr (VPT == 8)
+                    __stcs(reinterpret_cast<uint4*>(o), make_uint4(pw[0], pw[1], pw[2], pw[3]));
+                else
+                    __stcs(reinterpret_cast<uint2*>(o), make_uint2(pw[0], pw[1]));
+            } else {
+                mbar_arrive(&empty[s]);
+            }
+        }
+    }
+}
+
+namespace {
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
+    using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
+    static_assert(Sh::kSmem <= 232448, "shared memory above the per-CTA limit");
+    auto kern = k_dp_tma<ND, NCW, VPT, MAXST, BUDGET>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), Sh::kSmem);
+    if (per_sm < 1) per_sm = 1;
+    const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
+    if (ntiles < 1) return cudaSuccess;
+    const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
+    const int grid = (int)(ntiles < cap ? ntiles : cap);
+    kern<<<grid, 32 * (NCW + 1), Sh::kSmem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Staged naive-DP step over the 8-aligned body [lo, lo + n); cudaErrorNotSupported for rank
+// counts without a staged shape.
+cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master, float* const* m,
+                          float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+    DpTmaArgs a{};
+    a.g = g.ptr;
+    a.g_off = g.off;
+    a.out = out.ptr;
+    a.out_off = out.off;
+    for (int q = 0; q < nd && q < ZS_MAX_RANKS; ++q) {
+        a.master[q] = master[q];
+        a.m[q] = m[q];
+        a.v[q] = v[q];
+    }
+    a.s = s;
+    a.lo = lo;
+    a.n = n;
+    a.nd = nd;
+    a.inv_nd = 1.0f / (float)nd;
+    a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
+    a.drain_limit = 4000000000LL;
+    // Shapes per rank count from a measured sweep on GB300 (GPT-2-small buffers, 124.4 M elements;
+    // consumer warps x elements per thread x ring depth x CTAs per SM).  The update is ALU-heavy
+    // here (one AdamW per 28 bytes moved, twice the fused step's density), so the consumers set the
+    // pace: 4 consumer warps per SM reached only 53 % at N_d = 8, 8 warps 97 %.  Of the measured copy
+    // rate, staged / streaming: N_d = 2: 90 / 89 %, 4: 97 / 95 %, 8: 97-98 / 92 %, 16: 95 / 91 %,
+    // 32: 94 / 91 %.
+    switch (nd) {
+        case 2: return dp_tma_impl<2, 16, 8, 16, 232448>(a, st);   // T 4096, 4 stages, 1 CTA/SM
+        case 4: return dp_tma_impl<4, 8, 8, 16, 232448>(a, st);    // T 2048, 8 stages, 1 CTA/SM
+        case 8: return dp_tma_impl<8, 8, 8, 16, 232448>(a, st);    // T 2048, 6 stages, 1 CTA/SM
+        case 16: return dp_tma_impl<16, 8, 8, 16, 232448>(a, st);  // T 2048, 4 stages, 1 CTA/SM
+        case 32: return dp_tma_impl<32, 8, 4, 16, 232448>(a, st);  // T 1024, 8 stages, 1 CTA/SM
         default: return cudaErrorNotSupported;
     }
 }
@@ -924,8 +1195,9 @@ cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// Bulk-store gather over the 8-aligned body [lo, lo + n): tiles of 8192 elements, a 2-stage ring
-// (32.9 KB) per one-warp CTA, about 16 CTAs per SM (chosen by measurement on GB300).
+// Bulk-store gather over the 8-aligned body [lo, lo + n): tiles of 16384 elements in a 4-stage ring
+// (131 KB, so one one-warp CTA resident per SM), a grid of 16 CTAs per SM (chosen by measurement on
+// GB300).
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
                                int64_t n, int nd, cudaStream_t st) {
     GatherBulkArgs a{};

@@ -44,8 +44,8 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
                          cudaStream_t st);
 cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
                           const Range& r, int nd, cudaStream_t st);
-// The staged kernel runs only for 8-aligned ranges of supported rank counts whose buffers are all
-// device memory; allow_staged = false forces the register-streaming kernel.
+// The fused step over r.  The staged kernel runs only for the 8-aligned body of a range of a
+// supported rank count whose buffers are all device memory; elsewhere the register-streaming kernel.
 // Which fused kernel a launch may use.  kStagedIfDevice asks the runtime about every pointer;
 // kStagedDeviceKnown is for callers that already did (fused_ptrs_on_device) for the same pointers.
 enum StagedPolicy { kStagedNever = 0, kStagedIfDevice = 1, kStagedDeviceKnown = 2 };
@@ -60,7 +60,7 @@ bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, con
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                              int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
 // The broadcast staged kernel over a list of bodies ([lo, lo + n): the TMA alignment rules of
-// launch_fused_tma for each) in one launch per 512 bodies, tiles walked in list order.
+// launch_fused_tma for each) in one launch per kTmaListMax (128) bodies, tiles walked in list order.
 cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float* v, const BView& out,
                                   const std::vector<std::pair<int64_t, int64_t>>& bodies, const AdamScalars& s,
                                   int nd, cudaStream_t st);
@@ -71,7 +71,6 @@ cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* 
                                 const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
                                 StagedPolicy staged_policy = kStagedIfDevice);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
-// One source to N_d destinations with bulk stores, over the 8-aligned body [lo, lo + n).
 // Staged reduce-scatter-mean of the body [lo, lo + n) into one array (element i at out + (i -
 // out_off)); the TMA alignment rules of launch_fused_tma.  cudaErrorNotSupported for rank counts
 // without a staged shape.
@@ -95,9 +94,17 @@ struct Fsdp2CopyArgs {
     int64_t shard;
     int to_flat;            // 1: parameters -> buffer (zero padding rows), 0: buffer -> parameters
 };
+// One source to N_d destinations with bulk stores, over the 8-aligned body [lo, lo + n).
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
                                int64_t n, int nd, cudaStream_t st);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);
+// Staged naive-DP step over the 8-aligned body [lo, lo + n) (the TMA alignment rules of
+// launch_fused_tma; every rank's master, m and v 16-byte aligned); cudaErrorNotSupported for rank
+// counts without a staged shape.
+cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master, float* const* m,
+                          float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
+// The naive-DP step over r: the staged kernel for the 8-aligned body of a large range whose buffers
+// are all device memory (the few fringe elements, and everything else, by the streaming kernel).
 cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,
                            const Range& r, const AdamScalars& s, int nd, cudaStream_t st);
 cudaError_t read_device_error(unsigned int* out, bool clear);

@@ -205,8 +205,9 @@ int zs_adamw_scalars(const zs_adamw_hparams* hp, int64_t step, float* out8);
 /* Message for the last non-OK return on this thread ("" if none). */
 const char* zs_last_error(void);
 
-/* Selects the kernel behind zs_fused_step and zs_zero3_rs_step_unit for the
- * whole process (ZS_FUSED_AUTO, ZS_FUSED_LDG or ZS_FUSED_TMA).  Every variant
+/* Selects the kernel behind zs_fused_step, zs_fused_step_buckets,
+ * zs_zero3_rs_step_unit and zs_dp_step for the whole process (ZS_FUSED_AUTO,
+ * ZS_FUSED_LDG or ZS_FUSED_TMA).  Every variant
  * computes bit-identical results; they differ in how data reaches the SMs.  The
  * staged kernel exists for N_d in {2, 4, 8, 16, 32} and needs the range's buffers
  * on the 8-element grid; elsewhere the streaming kernel runs.  Set it before
