@@ -781,15 +781,25 @@ def run_next(args, ws, rank, local):
     unit_base = [plan.unit(u)["base"] for u in range(plan.n_units)]
     unit_pad = [plan.unit(u)["padded"] for u in range(plan.n_units)]
 
-    def chunk_cat(q=0):
+    def chunk_cat(q=0, st=None):
         for u in range(plan.n_units):
             zs.zs_fsdp2_chunk_cat(plan, u, [params[k] for k in members[u]],
-                                  grads[q][unit_base[u]:unit_base[u] + unit_pad[u]], stream=stream)
+                                  grads[q][unit_base[u]:unit_base[u] + unit_pad[u]], stream=st or stream)
 
-    def copy_out(q=0):
+    def copy_out(q=0, st=None):
         for u in range(plan.n_units):
             zs.zs_fsdp2_copy_out(plan, u, reps[q][unit_base[u]:unit_base[u] + unit_pad[u]],
-                                 [params[k] for k in members[u]], stream=stream)
+                                 [params[k] for k in members[u]], stream=st or stream)
+
+    def graphed(body):
+        # the per-group calls of one step captured once and replayed: one launch per group as before,
+        # without the host's ~30 us per call between them (the library's calls are capturable: no
+        # synchronisation, no allocation)
+        g, cs = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+        with torch.cuda.graph(g, stream=cs):
+            body(st=cs)
+        torch.cuda.synchronize(dev)
+        return g
 
     for q in range(n_d):
         chunk_cat(q)
@@ -797,6 +807,11 @@ def run_next(args, ws, rank, local):
     row("FSDP2 gradient chunk-cat, one rank's full gradient -> group buffers (k_fsdp2_copy), %s units" % unit_label,
         timed(chunk_cat), plan.numel, 2 * plan.numel + 2 * P, layout_launches)
     launches += steps * layout_launches
+    g_cc = graphed(chunk_cat)
+    row("FSDP2 gradient chunk-cat, the same calls replayed from a CUDA graph (k_fsdp2_copy)", timed(g_cc.replay),
+        plan.numel, 2 * plan.numel + 2 * P, layout_launches)
+    launches += steps * layout_launches
+    del g_cc
 
     def f2():
         t[0] += 1
@@ -808,6 +823,11 @@ def run_next(args, ws, rank, local):
     row("FSDP2 copy-out, group buffers -> one rank's parameters (k_fsdp2_copy)", timed(copy_out), plan.numel,
         2 * plan.numel * 2, layout_launches)
     launches += steps * layout_launches
+    g_co = graphed(copy_out)
+    row("FSDP2 copy-out, the same calls replayed from a CUDA graph (k_fsdp2_copy)", timed(g_co.replay), plan.numel,
+        2 * plan.numel * 2, layout_launches)
+    launches += steps * layout_launches
+    del g_co
     del master, m, v, grads, reps, params
     torch.cuda.empty_cache()
     clocks = sampler.stop()

@@ -55,6 +55,13 @@
  * Threads.    A plan is immutable after creation and may be shared by
  *             threads; calls on different streams may run concurrently when
  *             their buffers do not overlap.
+ * Graphs.     Because the step calls only enqueue work, a sequence of them
+ *             (including the two-stream ones) may be captured into a CUDA
+ *             graph and replayed, which removes the host's per-call time
+ *             between short kernels (e.g. per-group FSDP2 conversions).  The
+ *             step number, hyper-parameters and pointers are kernel arguments:
+ *             a replay repeats the values it was captured with.  The
+ *             checkpoint calls synchronise and cannot be captured.
  */
 #ifndef ZS_H
 #define ZS_H

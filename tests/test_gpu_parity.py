@@ -647,8 +647,9 @@ def test_staged_adamw_on_sharded_buffers(variant, n_d, numel):
 
 
 def test_guard_zones_untouched_large_kernels():
-    """Sentinels around every buffer of the large-range kernels (staged fused step, staged AdamW,
-    bulk-store gathers, FSDP2 copies): nothing is written outside the buffers."""
+    """Sentinels around every buffer of the large-range kernels (staged fused step over one range
+    and over a scattered bucket list, staged AdamW, bulk-store gathers, staged naive-DP step and the
+    in-place all-reduce, FSDP2 copies): nothing is written outside the buffers."""
     n_d, numel = 8, 2_097_165
     plan, _ = _plans([(numel,)], n_d, stage=3)
     P = plan.padded
@@ -673,6 +674,14 @@ def test_guard_zones_untouched_large_kernels():
     zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, master, m, v, [shards], zs.ZS_SHARDED, HP, 3)
     zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps)                               # bulk gather
     zs.zs_zero3_gather_unit(plan, 0, shards, full)                                      # bulk gather
+    bp = zs.Plan([(numel,)], n_d, stage=2, bucket_bytes=1 << 20)
+    assert bp.n_buckets >= 4
+    zs.zs_fused_step_buckets(bp, list(range(0, bp.n_buckets, 2)), grads, master, m, v, reps, HP, 4)  # list kernel
+    dp = zs.Plan([(numel,)], n_d, stage=0)
+    assert dp.padded == P
+    dm, dmm, dv = ([mk(P, torch.float32) for _ in range(n_d)] for _ in range(3))
+    zs.zs_dp_step(dp, grads, dm, dmm, dv, full, HP, 1)                                  # staged naive DP
+    zs.zs_all_reduce_mean(dp, -1, grads)                                                # in place
     p2 = zs.Plan([(1023, 2048), (5,)], n_d, layout=zs.ZS_LAYOUT_FSDP2)
     params = [mk(1023 * 2048, BF16), mk(5, BF16)]
     params[0].normal_()
