@@ -767,6 +767,16 @@ def run_next(args, ws, rank, local):
             P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), (gathers + 1) * U,
             comm_bytes_per_rank=plan.comm_bytes(3, reshard))
         launches += steps * (gathers + 1) * U
+        # the same step captured once (both streams) and replayed; the replay repeats its step number
+        g3, cs = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+        with torch.cuda.graph(g3, stream=cs):
+            zs.zs_zero3_step(plan, shards, master, m, v, [ugrads] * U, slots, reshard, hp, t[0] + 1,
+                             main_stream=cs, side_stream=side)
+        torch.cuda.synchronize(dev)
+        row("ZeRO-3 step, reshard_after_forward=%s, replayed from a CUDA graph" % reshard, timed(g3.replay),
+            plan.numel, P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), (gathers + 1) * U)
+        launches += steps * (gathers + 1) * U
+        del g3
     del master, m, v, shards, ugrads, pool
 
     # FSDP2 Shard(0) layout on the same grouping: per rank gradient chunk-cat, fused step, copy-out
