@@ -133,6 +133,7 @@ class Plan:
     def __init__(self, shapes, n_d, stage=ZS_STAGE_ZERO1, bucket_bytes=0, unit_of_param=None, layout=ZS_LAYOUT_FSDP1):
         self._h = None
         self._members = self._param_numel = None
+        self._units, self._buckets = {}, {}      # query results, kept: the plan is immutable
         self.shapes = [tuple(int(d) for d in s) for s in shapes]
         shapes = [tuple(int(d) for d in s) for s in shapes]
         n = len(shapes)
@@ -174,14 +175,28 @@ class Plan:
                 "n_buckets": e.value, "n_d": f.value, "stage": g.value}
 
     def unit(self, u):
-        a, b, c, d = c_i64(), c_i64(), c_i64(), c_i64()
-        _check(_lib.zs_plan_unit(self._h, int(u), *(ctypes.byref(x) for x in (a, b, c, d))))
-        return {"base": a.value, "numel": b.value, "padded": c.value, "shard": d.value}
+        u = int(u)
+        got = self._units.get(u)
+        if got is None:
+            a, b, c, d = c_i64(), c_i64(), c_i64(), c_i64()
+            _check(_lib.zs_plan_unit(self._h, u, *(ctypes.byref(x) for x in (a, b, c, d))))
+            got = self._units[u] = (a.value, b.value, c.value, d.value)
+        return {"base": got[0], "numel": got[1], "padded": got[2], "shard": got[3]}
+
+    def unit_padded(self, u):
+        """padded_u of unit u (the size of its ZS_RANK_UNIT buffers)."""
+        u = int(u)
+        got = self._units.get(u)
+        return got[2] if got is not None else self.unit(u)["padded"]
 
     def bucket(self, b):
-        u, lo, hi = c_i32(), c_i64(), c_i64()
-        _check(_lib.zs_plan_bucket(self._h, int(b), ctypes.byref(u), ctypes.byref(lo), ctypes.byref(hi)))
-        return u.value, lo.value, hi.value
+        b = int(b)
+        got = self._buckets.get(b)
+        if got is None:
+            u, lo, hi = c_i32(), c_i64(), c_i64()
+            _check(_lib.zs_plan_bucket(self._h, b, ctypes.byref(u), ctypes.byref(lo), ctypes.byref(hi)))
+            got = self._buckets[b] = (u.value, lo.value, hi.value)
+        return got
 
     def bucket_rank_slice(self, b, rank):
         lo, hi = c_i64(), c_i64()
@@ -260,6 +275,11 @@ def _hp(hp):
                             float(hp["weight_decay"]))
 
 
+def _name(what):
+    """An argument's name for a message: a string, or (name, index) formatted only when needed."""
+    return what if isinstance(what, str) else "%s[%d]" % what
+
+
 def _addr(x, min_elems=None, elem_size=None, what="buffer", device=True):
     """Address of a tensor (size-checked) or an integer address (unchecked).
 
@@ -271,23 +291,23 @@ def _addr(x, min_elems=None, elem_size=None, what="buffer", device=True):
     if hasattr(x, "data_ptr"):
         if device == "pinned_ok":
             if not (x.is_cuda or x.is_pinned()):
-                raise ValueError("%s must be a CUDA tensor or pinned host memory" % what)
+                raise ValueError("%s must be a CUDA tensor or pinned host memory" % _name(what))
         elif device and not x.is_cuda:
-            raise ValueError("%s must be a CUDA tensor" % what)
+            raise ValueError("%s must be a CUDA tensor" % _name(what))
         if not x.is_contiguous():
-            raise ValueError("%s must be contiguous" % what)
+            raise ValueError("%s must be contiguous" % _name(what))
         if elem_size is not None and x.element_size() != elem_size:
-            raise ValueError("%s must have %d-byte elements" % (what, elem_size))
+            raise ValueError("%s must have %d-byte elements" % (_name(what), elem_size))
         if min_elems is not None and x.numel() < min_elems:
-            raise ValueError("%s holds %d elements, the call touches %d" % (what, x.numel(), min_elems))
+            raise ValueError("%s holds %d elements, the call touches %d" % (_name(what), x.numel(), min_elems))
         return x.data_ptr()
-    raise TypeError("%s: expected a tensor or an integer address" % what)
+    raise TypeError("%s: expected a tensor or an integer address" % _name(what))
 
 
 def _ptr_array(xs, min_elems, elem_size, what, device=True):
     if xs is None:
         return None
-    vals = [_addr(x, min_elems, elem_size, "%s[%d]" % (what, i), device) for i, x in enumerate(xs)]
+    vals = [_addr(x, min_elems, elem_size, (what, i), device) for i, x in enumerate(xs)]
     return (c_vp * max(len(vals), 1))(*vals)
 
 
@@ -307,14 +327,14 @@ def _bf16_elems(plan, kind, bucket=-1, unit=0):
         _, lo, hi = plan.bucket(bucket)
         return hi - lo
     if kind == ZS_RANK_UNIT:
-        return plan.unit(unit)["padded"]
+        return plan.unit_padded(unit)
     raise ValueError("unknown buffer kind %r" % (kind,))
 
 
 def _n_ptrs(kind, xs, n_d, what):
     want = 1 if kind == ZS_SHARDED else n_d
     if xs is not None and len(xs) != want:
-        raise ValueError("%s: expected %d pointer(s), got %d" % (what, want, len(xs)))
+        raise ValueError("%s: expected %d pointer(s), got %d" % (_name(what), want, len(xs)))
 
 
 # ------------------------------------------------------------------ device operations
@@ -382,7 +402,7 @@ def zs_fused_step_host(plan, host_grads, dev_grads, master, m, v, replicas, hp, 
 
 def zs_zero3_gather_unit(plan, unit, shards, full, stream=None):
     _n_ptrs(ZS_RANK_UNIT, full, plan.n_d, "full")
-    nu = plan.unit(unit)["padded"]
+    nu = plan.unit_padded(unit)
     return _check(_lib.zs_zero3_gather_unit(plan.handle, int(unit), _addr(shards, plan.padded, 2, "shards"),
                                             _ptr_array(full, nu, 2, "full"), _stream(stream)))
 
@@ -390,7 +410,7 @@ def zs_zero3_gather_unit(plan, unit, shards, full, stream=None):
 def zs_zero3_rs_step_unit(plan, unit, grads, master, m, v, shards, hp, step, stream=None):
     _n_ptrs(ZS_RANK_UNIT, grads, plan.n_d, "grads")
     n = plan.padded
-    nu = plan.unit(unit)["padded"]
+    nu = plan.unit_padded(unit)
     return _check(_lib.zs_zero3_rs_step_unit(
         plan.handle, int(unit), _ptr_array(grads, nu, 2, "grads"),
         _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
@@ -403,15 +423,16 @@ def zs_zero3_step(plan, shards, master, m, v, unit_grads, pool, reshard_after_fo
     n, nd = plan.padded, plan.n_d
     if len(unit_grads) != plan.n_units:
         raise ValueError("unit_grads needs one list of N_d buffers per unit")
-    biggest = max(plan.unit(u)["padded"] for u in range(plan.n_units))
+    biggest = max(plan.unit_padded(u) for u in range(plan.n_units))
     flat_g = []
     for u, per_rank in enumerate(unit_grads):
-        _n_ptrs(ZS_RANK_UNIT, per_rank, nd, "unit_grads[%d]" % u)
-        flat_g += [_addr(x, plan.unit(u)["padded"], 2, "unit_grads[%d]" % u) for x in per_rank]
+        _n_ptrs(ZS_RANK_UNIT, per_rank, nd, ("unit_grads", u))
+        n_u = plan.unit_padded(u)
+        flat_g += [_addr(x, n_u, 2, ("unit_grads", u)) for x in per_rank]
     flat_p = []
     for k, per_rank in enumerate(pool):
-        _n_ptrs(ZS_RANK_UNIT, per_rank, nd, "pool[%d]" % k)
-        flat_p += [_addr(x, biggest, 2, "pool[%d]" % k) for x in per_rank]
+        _n_ptrs(ZS_RANK_UNIT, per_rank, nd, ("pool", k))
+        flat_p += [_addr(x, biggest, 2, ("pool", k)) for x in per_rank]
     main = _stream(main_stream)
     side = main if side_stream is None else _stream(side_stream)
     return _check(_lib.zs_zero3_step(
@@ -430,8 +451,8 @@ def zs_zero2_step_host(plan, host_grads, staging, master, m, v, replicas, hp, st
     biggest = max(hi - lo for _, lo, hi in (plan.bucket(b) for b in range(plan.n_buckets)))
     flat_s = []
     for k, per_rank in enumerate(staging):
-        _n_ptrs(ZS_RANK_BUCKET, per_rank, nd, "staging[%d]" % k)
-        flat_s += [_addr(x, biggest, 2, "staging[%d]" % k) for x in per_rank]
+        _n_ptrs(ZS_RANK_BUCKET, per_rank, nd, ("staging", k))
+        flat_s += [_addr(x, biggest, 2, ("staging", k)) for x in per_rank]
     main = _stream(stream)
     cp = _stream(copy_stream) if copy_stream is not None else main
     d2 = _stream(d2h_stream) if d2h_stream is not None else None
@@ -498,17 +519,17 @@ def zs_fsdp2_chunk_cat(plan, unit, params, flat, stream=None):
     members = _unit_params(plan, unit)
     if len(params) != len(members):
         raise ValueError("expected %d parameters for unit %d" % (len(members), unit))
-    ptrs = [_addr(x, plan.param_numel(k), 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
+    ptrs = [_addr(x, plan.param_numel(k), 2, ("params", i)) for i, (x, k) in enumerate(zip(params, members))]
     return _check(_lib.zs_fsdp2_chunk_cat(plan.handle, int(unit), (c_vp * max(len(ptrs), 1))(*ptrs),
-                                          _addr(flat, plan.unit(unit)["padded"], 2, "flat"), _stream(stream)))
+                                          _addr(flat, plan.unit_padded(unit), 2, "flat"), _stream(stream)))
 
 
 def zs_fsdp2_copy_out(plan, unit, flat, params, stream=None):
     members = _unit_params(plan, unit)
     if len(params) != len(members):
         raise ValueError("expected %d parameters for unit %d" % (len(members), unit))
-    ptrs = [_addr(x, plan.param_numel(k), 2, "params[%d]" % i) for i, (x, k) in enumerate(zip(params, members))]
-    return _check(_lib.zs_fsdp2_copy_out(plan.handle, int(unit), _addr(flat, plan.unit(unit)["padded"], 2, "flat"),
+    ptrs = [_addr(x, plan.param_numel(k), 2, ("params", i)) for i, (x, k) in enumerate(zip(params, members))]
+    return _check(_lib.zs_fsdp2_copy_out(plan.handle, int(unit), _addr(flat, plan.unit_padded(unit), 2, "flat"),
                                          (c_vp * max(len(ptrs), 1))(*ptrs), _stream(stream)))
 
 
