@@ -99,6 +99,7 @@ _sig("zs_dp_step", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.POINTER(zs_adamw_
 _sig("zs_fused_step_buckets", [c_vp, c_i32, P_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                ctypes.POINTER(zs_adamw_hparams), c_i64, c_i32, c_vp, c_vp])
 _sig("zs_set_fused_variant", [c_i32])
+_sig("zs_set_dependent_launch", [c_i32])
 _sig("zs_device_status", [ctypes.POINTER(ctypes.c_uint32), c_i32])
 _sig("zs_selftest_wait_timeout", [c_i64, c_vp])
 
@@ -111,7 +112,7 @@ EXPORTED = [
     "zs_device_status", "zs_selftest_wait_timeout", "zs_zero3_step", "zs_zero2_step_host",
     "zs_checkpoint_save", "zs_checkpoint_load", "zs_zero2_step_host_noalloc", "zs_all_reduce_mean",
     "zs_dp_step", "zs_plan_create_fsdp2", "zs_plan_layout", "zs_plan_param_rows", "zs_plan_pad_ranges",
-    "zs_fsdp2_chunk_cat", "zs_fsdp2_copy_out", "zs_fused_step_buckets",
+    "zs_fsdp2_chunk_cat", "zs_fsdp2_copy_out", "zs_fused_step_buckets", "zs_set_dependent_launch",
 ]
 
 
@@ -552,6 +553,11 @@ def zs_fused_step_buckets(plan, buckets, grads, master, m, v, replicas, hp, step
 
 def zs_set_fused_variant(variant):
     return _check(_lib.zs_set_fused_variant(int(variant)))
+
+
+def zs_set_dependent_launch(enable):
+    """Programmatic dependent launch for every kernel of the library (on by default)."""
+    return _check(_lib.zs_set_dependent_launch(1 if enable else 0))
 
 
 def zs_device_status(clear=False):

@@ -409,6 +409,12 @@ extern "C" int zs_set_fused_variant(int32_t variant) {
     return ZS_OK;
 }
 
+extern "C" int zs_set_dependent_launch(int32_t enable) {
+    zs::clear_error();
+    zs::set_dependent_launch(enable != 0);
+    return ZS_OK;
+}
+
 extern "C" int zs_device_status(uint32_t* code, int32_t clear) {
     static const char* fn = "zs_device_status";
     zs::clear_error();

@@ -123,6 +123,18 @@ __device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v
     p = __fsub_rn(pd, __fmul_rn(s.step_size, __fdiv_rn(m, den)));
 }
 
+// Programmatic dependent launch (sm_90 and later).  The library launches its kernels with
+// programmatic stream serialization allowed: the next kernel on a stream may be scheduled once
+// every CTA of the current one has started, so its CTAs are resident when the current one ends
+// instead of being launched after it.  Each kernel therefore first lets its successor launch and
+// then waits (griddepcontrol.wait: until every prerequisite grid has completed and its memory
+// operations are visible) before it touches global memory, which keeps stream order for every
+// byte.  Launched without the attribute, both instructions do nothing.
+__device__ __forceinline__ void dependent_launch_prologue() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Grid-stride loop helpers.
 __device__ __forceinline__ int64_t gtid() { return (int64_t)blockIdx.x * blockDim.x + threadIdx.x; }
 __device__ __forceinline__ int64_t gstride() { return (int64_t)gridDim.x * blockDim.x; }

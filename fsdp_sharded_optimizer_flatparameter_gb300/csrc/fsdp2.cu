@@ -28,7 +28,7 @@
 // and the ring's fill and drain do not pay for themselves.)
 #include <string>
 
-#include "launch.h"
+#include "device.cuh"
 #include "plan.h"
 
 namespace zs {
@@ -75,6 +75,7 @@ __device__ __forceinline__ void zero_run(uint16_t* dst, int64_t n, int t, int st
 }
 
 __global__ void __launch_bounds__(kCopyThreads) k_fsdp2_copy(const __grid_constant__ CopyArgs a) {
+    dependent_launch_prologue();
     const int64_t task = blockIdx.x;
     int lo = 0, hi = a.n - 1;                                 // last j with first[j] <= task
     while (lo < hi) {
@@ -141,8 +142,7 @@ int fsdp2_copy(const char* fn, zs_plan_t plan, int32_t unit, void* const* params
         a.to_flat = to_flat;
         const int64_t total = a.first[cnt];
         if (total > 0x7fffffffLL) return fail(fn, "unit too large for one launch");
-        k_fsdp2_copy<<<(unsigned)total, kCopyThreads, 0, st>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_kernel(k_fsdp2_copy, dim3((unsigned)total), dim3(kCopyThreads), 0, st, a);
         if (e != cudaSuccess) {
             set_error(std::string(fn) + ": " + cudaGetErrorString(e));
             return ZS_ERR_CUDA;

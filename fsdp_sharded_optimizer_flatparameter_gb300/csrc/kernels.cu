@@ -77,6 +77,7 @@ static Split split_range(int64_t lo, int64_t hi, bool vec_ok) {
 // Runs op.template run<8>(i) over the body and op.template run<1>(i) over the fringe.
 template <class Op>
 __device__ __forceinline__ void for_range(const Split& sp, const Op& op) {
+    dependent_launch_prologue();
     if (sp.nvec > 0) {
         for (int64_t t = gtid(); t < sp.nvec; t += gstride()) op.template run<8>(sp.vlo + (t << 3));
         const int64_t nhead = sp.vlo - sp.lo;
@@ -133,8 +134,7 @@ cudaError_t launch_accumulate(const Ptrs& acc, const Ptrs& micro, int nd, int64_
     AccumArgs a{acc, micro, scale, first};
     Split sp = split_range(0, n, true);
     dim3 grid(grid_for((const void*)k_accumulate, sp.nvec > 0 ? sp.nvec : n), nd);
-    k_accumulate<<<grid, kThreads, 0, st>>>(a, sp);
-    return cudaGetLastError();
+    return launch_kernel(k_accumulate, grid, dim3(kThreads), 0, st, a, sp);
 }
 
 // ------------------------------------------------------------------ reduce-scatter with averaging
@@ -174,8 +174,7 @@ static cudaError_t rs_impl(const BView& g, const BView& out, bool by_owner, cons
                            cudaStream_t st) {
     RsOp<ND> op{g, out, by_owner ? 1 : 0, nd, 1.0f / (float)nd, r.base, r.shard};
     const int grid = grid_for((const void*)k_rs_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
-    k_rs_mean<ND><<<grid, kThreads, 0, st>>>(op, sp);
-    return cudaGetLastError();
+    return launch_kernel(k_rs_mean<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
 // ------------------------------------------------------------------ AdamW on a shard
@@ -234,8 +233,7 @@ static cudaError_t gather_impl(const BView& src, bool src_by_owner, const BView&
                                const Range& r, int nd, Split sp, cudaStream_t st) {
     GatherOp<ND> op{src, dst, src_by_owner ? 1 : 0, skip_owner ? 1 : 0, nd, r.base, r.shard};
     const int grid = grid_for((const void*)k_gather<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
-    k_gather<ND><<<grid, kThreads, 0, st>>>(op, sp);
-    return cudaGetLastError();
+    return launch_kernel(k_gather<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
 // ------------------------------------------------------------------ fused: reduce-mean + AdamW + scatter
@@ -292,8 +290,7 @@ static cudaError_t fused_impl(const BView& g, float* master, float* m, float* v,
                               const AdamScalars& s, int nd, Split sp, cudaStream_t st) {
     FusedOp<ND, BROADCAST> op{g, out, master, m, v, s, nd, 1.0f / (float)nd};
     const int grid = grid_for((const void*)k_fused<ND, BROADCAST>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
-    k_fused<ND, BROADCAST><<<grid, kThreads, 0, st>>>(op, sp);
-    return cudaGetLastError();
+    return launch_kernel(k_fused<ND, BROADCAST>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
 // ------------------------------------------------------------------ dispatch
@@ -373,8 +370,8 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
                 Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
                 for (const Split& f : rest) {
                     if (f.hi <= f.lo) continue;
-                    k_adamw<<<grid_for((const void*)k_adamw, f.hi - f.lo), kThreads, 0, st>>>(op, f);
-                    e = cudaGetLastError();
+                    e = launch_kernel(k_adamw, dim3(grid_for((const void*)k_adamw, f.hi - f.lo)), dim3(kThreads), 0, st,
+                                      op, f);
                     if (e != cudaSuccess) return e;
                 }
                 return cudaSuccess;
@@ -383,8 +380,7 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
     }
     AdamOp op{grad, par, grad_by_owner ? 1 : 0, par_by_owner ? 1 : 0, master, m, v, s, r.base, r.shard};
     const int grid = grid_for((const void*)k_adamw, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
-    k_adamw<<<grid, kThreads, 0, st>>>(op, sp);
-    return cudaGetLastError();
+    return launch_kernel(k_adamw, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
 constexpr int64_t kBulkGatherMinElems = int64_t(1) << 20;
@@ -422,6 +418,10 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
 
 void set_fused_variant(int v) { g_fused_variant.store(v); }
 int fused_variant() { return g_fused_variant.load(); }
+
+static std::atomic<int> g_dependent_launch{1};
+void set_dependent_launch(int on) { g_dependent_launch.store(on ? 1 : 0); }
+int dependent_launch() { return g_dependent_launch.load(); }
 
 static cudaError_t launch_fused_ldg(const BView& g, float* master, float* m, float* v, const BView& out,
                                     bool broadcast, const Split& sp, const AdamScalars& s, int nd, cudaStream_t st) {
@@ -648,8 +648,7 @@ template <int ND>
 static cudaError_t all_reduce_impl(const BView& g, int nd, Split sp, cudaStream_t st) {
     AllReduceOp<ND> op{g, nd, 1.0f / (float)nd};
     const int grid = grid_for((const void*)k_all_reduce_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
-    k_all_reduce_mean<ND><<<grid, kThreads, 0, st>>>(op, sp);
-    return cudaGetLastError();
+    return launch_kernel(k_all_reduce_mean<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
 template <int ND>
@@ -667,8 +666,7 @@ static cudaError_t dp_step_impl(const BView& g, const BView& out, float* const* 
     op.nd = nd;
     op.inv_nd = 1.0f / (float)nd;
     const int grid = grid_for((const void*)k_dp_step<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
-    k_dp_step<ND><<<grid, kThreads, 0, st>>>(op, sp);
-    return cudaGetLastError();
+    return launch_kernel(k_dp_step<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st) {

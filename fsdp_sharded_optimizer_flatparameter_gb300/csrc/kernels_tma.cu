@@ -200,6 +200,7 @@ struct TmaShape {
 
 template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_constant__ TmaArgs a) {
+    dependent_launch_prologue();
     using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
@@ -339,6 +340,7 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
 // k_fused_tma's: folding both into one generic loop cost the single-range kernel ~3 % on GB300).
 template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_list(const __grid_constant__ TmaListArgs l) {
+    dependent_launch_prologue();
     const TmaArgs& a = l.a;
     using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
@@ -507,6 +509,7 @@ struct GatherBulkArgs {
 
 template <int S>
 __global__ void __launch_bounds__(32) k_gather_bulk(const __grid_constant__ GatherBulkArgs a) {
+    dependent_launch_prologue();
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     uint16_t* buf = reinterpret_cast<uint16_t*>(smem + 128);
@@ -592,8 +595,7 @@ cudaError_t tma_impl(const Args& a, cudaStream_t st) {
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
     const int grid = (int)(ntiles < cap ? ntiles : cap);
-    kern<<<grid, 32 * (NCW + 1), kSmem, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(32 * (NCW + 1)), kSmem, st, a);
 }
 
 template <int V>
@@ -757,6 +759,7 @@ struct RsShape {
 
 template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant__ RsTmaArgs a) {
+    dependent_launch_prologue();
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
@@ -867,8 +870,7 @@ cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;
     const int grid = (int)(ntiles < cap ? ntiles : cap);
-    kern<<<grid, 32 * (NCW + 1), Sh::kSmem, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(32 * (NCW + 1)), Sh::kSmem, st, a);
 }
 
 }  // namespace
@@ -959,6 +961,7 @@ struct DpShape {
 
 template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
 __global__ void __launch_bounds__(32 * (NCW + 1), 1) k_dp_tma(const __grid_constant__ DpTmaArgs a) {
+    dependent_launch_prologue();
     using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
@@ -1135,8 +1138,7 @@ cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
     const int grid = (int)(ntiles < cap ? ntiles : cap);
-    kern<<<grid, 32 * (NCW + 1), Sh::kSmem, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(32 * (NCW + 1)), Sh::kSmem, st, a);
 }
 
 }  // namespace
@@ -1181,6 +1183,7 @@ cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master
 // Self-test of the bounded wait: waits on an mbarrier nothing arrives at, with
 // a budget of `limit` cycles, then records ZS_DEVERR_SELFTEST and returns.
 __global__ void k_wait_selftest(long long limit) {
+    dependent_launch_prologue();
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
@@ -1191,8 +1194,7 @@ __global__ void k_wait_selftest(long long limit) {
 }
 
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
-    k_wait_selftest<<<1, 32, 0, st>>>(limit_cycles);
-    return cudaGetLastError();
+    return launch_kernel(k_wait_selftest, dim3(1), dim3(32), 0, st, limit_cycles);
 }
 
 // Bulk-store gather over the 8-aligned body [lo, lo + n): tiles of 16384 elements in a 4-stage ring
@@ -1221,8 +1223,7 @@ cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs&
     const int64_t ntiles = (n + a.T - 1) / a.T;
     const int64_t cap = (int64_t)sms * 16;
     const int grid = (int)(ntiles < cap ? ntiles : cap);
-    k_gather_bulk<S><<<grid, 32, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_gather_bulk<S>, dim3(grid), dim3(32), smem, st, a);
 }
 
 cudaError_t read_device_error(unsigned int* out, bool clear) {

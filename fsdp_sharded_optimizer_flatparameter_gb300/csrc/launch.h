@@ -113,4 +113,29 @@ cudaError_t read_device_error(unsigned int* out, bool clear);
 void set_fused_variant(int v);
 int fused_variant();
 
+// Whether launches allow programmatic dependent launch (see dependent_launch_prologue).
+void set_dependent_launch(int on);
+int dependent_launch();
+
+// Launches kern<<<grid, block, smem, st>>>(args...) with programmatic stream serialization allowed
+// when dependent launch is on; a failed launch is returned and cleared from the runtime's last-error
+// state, as cudaGetLastError after <<<>>> did.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = dependent_launch() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
+}
+
 }  // namespace zs

@@ -221,6 +221,16 @@ const char* zs_last_error(void);
  * enqueueing work from other threads.  Errors: ZS_ERR_INVALID for an unknown value. */
 int zs_set_fused_variant(int32_t variant);
 
+/* Programmatic dependent launch (sm_90 and later) for every kernel of the
+ * library, for the whole process: enable != 0 (the default) launches each kernel
+ * so that it may be scheduled while the previous kernel on its stream drains;
+ * the kernel waits for that kernel to complete, with its memory visible, before
+ * it touches global memory, so stream order holds for every byte and results
+ * are identical either way.  It shortens the gap between back-to-back launches
+ * (bucket-by-bucket steps, per-group calls).  enable = 0 launches plainly.
+ * Set it before enqueueing work from other threads.  Never fails (ZS_OK). */
+int zs_set_dependent_launch(int32_t enable);
+
 /* Device-side status of the current device (ZS_DEVERR_*): a staged kernel whose
  * bounded wait ran out records a code here, stops, waits (bounded) for its
  * copies in flight and returns, leaving the context usable.  This call copies

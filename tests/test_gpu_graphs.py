@@ -6,6 +6,7 @@ launch-bound loop of short calls (per-group FSDP2 conversions, per-unit ZeRO-3 w
 without the host's per-call overhead between kernels.  Each test runs the same calls directly and
 from a captured graph, from identical states, and requires bit-identical results.  The step
 number is a kernel argument, so a replayed graph repeats the step number it was captured with.
+The last test runs a chain of dependent launches with programmatic dependent launch on and off.
 """
 
 import pytest
@@ -46,7 +47,7 @@ def _assert_same(a, b):
     for k in a:
         xs, ys = (a[k], b[k]) if isinstance(a[k], list) else ([a[k]], [b[k]])
         for i, (x, y) in enumerate(zip(xs, ys)):
-            assert torch.equal(x, y), "%s[%d] differs between direct calls and graph replay" % (k, i)
+            assert torch.equal(x, y), "%s[%d] differs between the two runs" % (k, i)
 
 
 @pytest.mark.parametrize("n_d,numel", [(8, 1_500_007), (3, 70_001)])
@@ -169,3 +170,43 @@ def test_naive_dp_and_fsdp2_conversions_replay():
     _assert_same(a, b)
     for k in range(len(shapes)):
         assert torch.equal(a["back"][k], params[k])
+
+
+def test_dependent_launch_on_and_off_agree():
+    """A chain of back-to-back launches in which each reads what the previous wrote (accumulations,
+    bucket-by-bucket fused steps, the in-place all-reduce of their replicas, a naive-DP step on the
+    result, a gather from the shards), run with programmatic dependent launch on and off: every
+    buffer ends bit-identical."""
+    n_d = 8
+    plan = zs.Plan([(2_100_003,)], n_d, stage=2, bucket_bytes=1 << 20)
+    P, pads = plan.padded, plan.pad_ranges()
+    micro = [synth.rank_grads(n_d, P, pads, seed=80, step=j + 1, sigma=1e-3, device=DEV)[0] for j in range(4)]
+    master0 = synth.master_init(P, pads, seed=81, device=DEV)
+    dp = zs.Plan([(2_100_003,)], n_d, stage=0)
+    assert dp.padded == P
+
+    def run(enable):
+        zs.zs_set_dependent_launch(enable)
+        try:
+            st = {"acc": synth.rank_buffers(n_d, P, BF16, DEV)[0], "reps": synth.rank_buffers(n_d, P, BF16, DEV)[0],
+                  "master": master0.clone(), "m": torch.zeros_like(master0), "v": torch.zeros_like(master0),
+                  "dm": [master0.clone() for _ in range(n_d)], "dmm": [torch.zeros_like(master0) for _ in range(n_d)],
+                  "dv": [torch.zeros_like(master0) for _ in range(n_d)], "out": synth.rank_buffers(n_d, P, BF16, DEV)[0]}
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for t in (1, 2):
+                    for j in range(4):
+                        zs.zs_accumulate_grad(plan, st["acc"], micro[j], 0.25, j == 0, stream=s)
+                    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), st["acc"], st["master"],
+                                             st["m"], st["v"], st["reps"], HP, t, launch_mode=zs.ZS_BUCKETS_PER_BUCKET,
+                                             stream=s)
+                    zs.zs_all_reduce_mean(dp, -1, st["reps"], stream=s)
+                    zs.zs_dp_step(dp, st["reps"], st["dm"], st["dmm"], st["dv"], st["out"], HP, t, stream=s)
+                    zs.zs_all_gather(plan, [st["out"][0]], zs.ZS_SHARDED, st["acc"], stream=s)
+            torch.cuda.synchronize()
+            assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+            return st
+        finally:
+            zs.zs_set_dependent_launch(True)
+
+    _assert_same(run(False), run(True))
