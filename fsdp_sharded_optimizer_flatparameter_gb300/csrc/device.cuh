@@ -129,7 +129,8 @@ __device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v
 // instead of being launched after it.  Each kernel therefore first lets its successor launch and
 // then waits (griddepcontrol.wait: until every prerequisite grid has completed and its memory
 // operations are visible) before it touches global memory, which keeps stream order for every
-// byte.  Launched without the attribute, both instructions do nothing.
+// byte; it waits no longer than plain stream order would.  Launched without the attribute, both
+// instructions do nothing.
 __device__ __forceinline__ void dependent_launch_prologue() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
