@@ -244,3 +244,9 @@ def test_fused_variant_switch_validates():
     assert zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO) == zs.ZS_OK
     with pytest.raises(zs.ZsError):
         zs.zs_set_fused_variant(3)
+
+
+def test_dependent_launch_switch():
+    """The programmatic-dependent-launch switch is process-wide and never fails (no CUDA call)."""
+    assert zs.zs_set_dependent_launch(False) == zs.ZS_OK
+    assert zs.zs_set_dependent_launch(True) == zs.ZS_OK
