@@ -119,3 +119,35 @@ def test_bucket_list_and_sharded_adamw():
                                zs.ZS_SHARDED, HP, 3)
 
     _run_both(make_state, body)
+
+
+@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
+def test_reduce_scatter_into_one_array(n_d):
+    """The staged reduce-scatter-mean (every rank's tile staged, the mean streamed to one array)."""
+    plan = zs.Plan([((1 << 25) + 7,)], n_d, stage=2)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads = synth.rank_grads(n_d, P, pads, seed=99, step=1, sigma=1e-3, device=DEV)[0]
+
+    def make_state():
+        return {"out": torch.zeros(P, dtype=BF16, device=DEV)}
+
+    def body(st):
+        zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [st["out"]], zs.ZS_SHARDED)
+
+    _run_both(make_state, body)
+
+
+@pytest.mark.parametrize("n_d", [2, 8, 16, 64])
+def test_bulk_store_gather_copies_every_element(n_d):
+    """The bulk-store gather (one source, N_d destinations): every destination equals the source on
+    every element (the gather has no streaming twin behind the variant switch: it is a copy)."""
+    plan = zs.Plan([((1 << 25) + 9,)], n_d, stage=2)
+    P = plan.padded
+    src = torch.empty(P, dtype=BF16, device=DEV).normal_(0, 1e-2)
+    reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    torch.cuda.synchronize()
+    zs.zs_all_gather(plan, [src], zs.ZS_SHARDED, reps)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    for q in range(n_d):
+        assert torch.equal(reps[q], src), "replica %d differs from the source" % q
