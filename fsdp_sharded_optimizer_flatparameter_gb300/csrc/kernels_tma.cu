@@ -323,11 +323,12 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
                     __stcs(reinterpret_cast<uint2*>(a.out.p[0] + (i - a.out_off)), w);
                 }
             }
-            // The stage is released after the stores, not as soon as it has been read: master, m and v
-            // are read from and written back to the same addresses, and an in-place staged kernel
-            // that released its stage before its stores gave wrong results on GB300 (a staged
-            // all-reduce at N_d = 2, up to 6 elements in 10^5, cause not found; releasing after the
-            // stores removed them).  Measured cost here: none (11.27 against 11.30 ms per step).
+            // The stage is released after the stores, which consume what was read from it, not right
+            // after the shared-memory loads: on GB300 the arrive on the empty barrier can take effect
+            // before those loads have returned their data, and the producer's refill of the stage then
+            // lands under them (a staged all-reduce that released early read, for a few elements in
+            // 10^5, the values of the tile S positions later in the same stage).  Measured cost here:
+            // none (11.27 against 11.30 ms per step).
             mbar_arrive(&empty[s]);
         } else {
             mbar_arrive(&empty[s]);
@@ -842,7 +843,6 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
             }
-            mbar_arrive(&empty[s]);
             uint32_t w[VPT / 2];
 #pragma unroll
             for (int k = 0; k < VPT; k += 2)
@@ -852,6 +852,7 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant
                 __stcs(reinterpret_cast<uint4*>(o), make_uint4(w[0], w[1], w[2], w[3]));
             else
                 __stcs(reinterpret_cast<uint2*>(o), make_uint2(w[0], w[1]));
+            mbar_arrive(&empty[s]);                      // after the store: see k_fused_tma
         } else {
             mbar_arrive(&empty[s]);
         }
@@ -1086,7 +1087,6 @@ __global__ void __launch_bounds__(32 * (NCW + 1), 1) k_dp_tma(const __grid_const
             for (int k = 0; k < VPT; k += 2)
                 gw[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], ND, a.inv_nd), mean_of_sum<ND>(acc[k + 1], ND, a.inv_nd));
         }
-        mbar_arrive(&gempty[b]);
 #pragma unroll 1
         for (int q = 0; q < ND; ++q, ++j) {
             const int s = (int)(j % S);
@@ -1122,6 +1122,8 @@ __global__ void __launch_bounds__(32 * (NCW + 1), 1) k_dp_tma(const __grid_const
                 mbar_arrive(&empty[s]);
             }
         }
+        // the grads buffer too is released only after stores that used what was read from it
+        mbar_arrive(&gempty[b]);
     }
 }
 
