@@ -525,12 +525,28 @@ cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* 
         }
         return cudaSuccess;
     }
+    // Large disjoint ranges go one launch each to the single-range kernel (with dependent launch its
+    // CTAs are resident as the previous launch drains; the list kernel streams ~5 % slower per tile),
+    // the rest through one list launch.  Measured on 2^28 elements at N_d = 8, two walks of every
+    // other bucket: one launch per 64 MiB bucket 95.5 % of the copy rate against 92.3 % for the
+    // list kernel; at 16 MiB the list kernel leads (92.2 % against 88.5 %).
+    constexpr int64_t kOwnLaunchElems = int64_t(1) << 25;
     std::vector<std::pair<int64_t, int64_t>> bodies;
     bodies.reserve(splits.size());
-    for (const Split& sp : splits)
-        if (sp.nvec > 0) bodies.emplace_back(sp.vlo, sp.nvec << 3);
-    cudaError_t e = launch_fused_tma_list(g, master, m, v, out, bodies, s, nd, st);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    for (const Split& sp : splits) {
+        if (sp.nvec <= 0) continue;
+        if ((sp.nvec << 3) >= kOwnLaunchElems) {
+            e = launch_fused_tma(g, master, m, v, out, true, sp.vlo, sp.nvec << 3, s, nd, st);
+            if (e != cudaSuccess) return e;
+        } else {
+            bodies.emplace_back(sp.vlo, sp.nvec << 3);
+        }
+    }
+    if (!bodies.empty()) {
+        e = launch_fused_tma_list(g, master, m, v, out, bodies, s, nd, st);
+        if (e != cudaSuccess) return e;
+    }
     // fringes (ranges whose ends are off the 8-element grid): at most 14 elements per range
     for (const Split& sp : splits) {
         const int64_t body_hi = sp.nvec > 0 ? sp.vlo + (sp.nvec << 3) : sp.lo;

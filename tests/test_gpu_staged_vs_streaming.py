@@ -151,3 +151,24 @@ def test_bulk_store_gather_copies_every_element(n_d):
     assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
     for q in range(n_d):
         assert torch.equal(reps[q], src), "replica %d differs from the source" % q
+
+
+def test_bucket_walk_large_scattered_buckets():
+    """Every other 64 MiB bucket of a 2^27+7-element buffer: the two large bodies take one
+    single-range launch each, the short last bucket the list kernel; against the streaming kernel."""
+    n_d = 8
+    plan = zs.Plan([((1 << 27) + 7,)], n_d, stage=2, bucket_bytes=64 << 20)
+    P, pads = plan.padded, plan.pad_ranges()
+    assert plan.n_buckets == 5
+    m0 = synth.master_init(P, pads, seed=100, device=DEV)
+    grads = synth.rank_grads(n_d, P, pads, seed=101, step=1, sigma=1e-3, device=DEV)[0]
+
+    def make_state():
+        return {"master": m0.clone(), "m": torch.zeros_like(m0), "v": torch.zeros_like(m0),
+                "reps": synth.rank_buffers(n_d, P, BF16, DEV)[0]}
+
+    def body(st):
+        for t in (1, 2):
+            zs.zs_fused_step_buckets(plan, [4, 2, 0], grads, st["master"], st["m"], st["v"], st["reps"], HP, t)
+
+    _run_both(make_state, body)
