@@ -11,8 +11,9 @@
 // units (a bucket or unit base, or an owner boundary, off the 8-element grid)
 // runs element by element throughout.  The rank count N_d is a template
 // parameter for the common powers of two so the rank loops unroll; other
-// counts use the runtime value.  Nothing here waits on anything, so no kernel
-// can hang.  The launchers below also choose, per call, the bulk-copy staged
+// counts use the runtime value.  Nothing here waits on anything but the preceding
+// kernel on the stream (the dependent-launch wait, no longer than stream order), so
+// no kernel can hang.  The launchers below also choose, per call, the bulk-copy staged
 // kernels (kernels_tma.cu) for large bodies whose buffers are all device memory.
 #include <algorithm>
 #include <atomic>
