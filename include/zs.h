@@ -353,12 +353,15 @@ int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int3
  * argument checks, the pointer-kind queries and the per-call overhead paid
  * once.  The update is element-wise and the buckets are disjoint, so the
  * launches need no order among themselves.
- *   launch_mode  ZS_BUCKETS_ONE_WALK: the staged kernel walks all listed
- *                buckets in one persistent launch (per 512 buckets), each
+ *   launch_mode  ZS_BUCKETS_ONE_WALK: listed buckets that touch are merged
+ *                into one range (a run of neighbours, in either order); a
+ *                merged range of at least 2^25 elements gets a launch of the
+ *                single-range staged kernel of its own, and all the others
+ *                are walked by one persistent launch (per 128 ranges), each
  *                CTA taking its tiles in list order, so a small bucket costs
  *                no launch of its own; where only the streaming kernel
  *                applies (host buffers, other rank counts, a total below
- *                2^20 elements) one launch per bucket on `stream`.
+ *                2^20 elements) one launch per range on `stream`.
  *                ZS_BUCKETS_PER_BUCKET: one launch per bucket; with a
  *                side_stream other than stream, the buckets at odd positions
  *                run on side_stream (which first waits for all work enqueued
