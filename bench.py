@@ -183,6 +183,32 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
 
 
+# ------------------------------------------------------------------ device status
+
+class DeviceStatusError(RuntimeError):
+    """A kernel recorded a device status code during a timed region: its time is not a valid number."""
+
+
+def check_device_status(read_status, where, ok_code=0):
+    """Reads (and clears) the library's device status word after a timed region.  A staged kernel
+    whose bounded wait runs out records a code there and returns early without finishing its
+    work, so the region's time would be too short: raise instead of reporting it."""
+    code = int(read_status())
+    if code != ok_code:
+        raise DeviceStatusError("device status %d after %s: a kernel gave up waiting, so no value is "
+                                "reported" % (code, where))
+    return code
+
+
+def library_mapped(name="libzs.so"):
+    """True when this process has the library mapped (Linux /proc maps)."""
+    try:
+        with open("/proc/self/maps") as f:
+            return any(line.rstrip().endswith("/" + name) for line in f)
+    except OSError:
+        return False
+
+
 # ------------------------------------------------------------------ workloads
 
 def bytes_per_padded_element(n_d, kernel):
@@ -199,7 +225,7 @@ def oracle_sample(n_d, sample_elems, sigma, outlier_p, seed):
     import numpy as np
     import torch
 
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+    import synth
 
     grads, _ = synth.rank_grads(n_d, sample_elems, [], seed=seed, step=1, sigma=sigma, outlier_p=outlier_p)
     g_np = [g.contiguous().view(torch.int16).numpy().view(np.uint16).copy() for g in grads]
@@ -214,7 +240,7 @@ def time_oracle(n_d, sample_elems, sigma, outlier_p, seed, min_seconds, max_reps
 
     from oracle import layout, steps
 
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+    import synth
 
     plan = layout.make_plan([(sample_elems,)], n_d, bucket_bytes=25 << 20)
     g_np, master = oracle_sample(n_d, plan.padded, sigma, outlier_p, seed)
@@ -243,7 +269,7 @@ def time_oracle_rows(seconds=1.5):
     from oracle import fsdp2 as ofs
     from oracle import layout, steps
 
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+    import synth
 
     def rate(fn, elems):
         done, t0 = 0, time.perf_counter()
@@ -337,7 +363,7 @@ def cpu_threads_used():
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+    import synth
 
     wl = synth.WORKLOADS[args.workload]
     n_d = wl["n_d"]
@@ -357,6 +383,10 @@ def run_reference(args, ws, rank):
                          "sample": desc},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    # the oracle arm must not have the library it judges in its address space
+    if library_mapped():
+        log("bench.py --impl reference: libzs.so is mapped in the oracle process")
+        return 4
     print(json.dumps(line), flush=True)
     return 0
 
@@ -370,7 +400,7 @@ class Workload:
         import torch
 
         import fsdp_sharded_optimizer_flatparameter_gb300 as zs
-        from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+        import synth
 
         self.zs, self.torch = zs, torch
         self.args, self.dev, self.stream = args, dev, stream
@@ -454,8 +484,9 @@ class Workload:
                              main_stream=st, side_stream=self.side)
 
 
-def timed_on_stream(torch, fn, steps, warmup, stream, dev, dist):
-    """Mean ms per call over `steps` calls after `warmup`, CUDA events on `stream`, max over ranks."""
+def timed_on_stream(torch, fn, steps, warmup, stream, dev, dist, status=None, where="a timed region"):
+    """Mean ms per call over `steps` calls after `warmup`, CUDA events on `stream`, max over ranks;
+    status(where), when given, checks the device status word after the region."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(dev)
@@ -465,6 +496,8 @@ def timed_on_stream(torch, fn, steps, warmup, stream, dev, dist):
         fn()
     b.record(stream)
     torch.cuda.synchronize(dev)
+    if status is not None:
+        status(where)
     return max_over_ranks(dist, a.elapsed_time(b) / steps, dev)
 
 
@@ -475,7 +508,7 @@ def run_sweep(args, ws, rank, local):
     import torch
 
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+    import synth
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -487,8 +520,13 @@ def run_sweep(args, ws, rank, local):
     peak, peak_kind = hbm_peak()
     steps = max(3, args.steps)
 
+    def status(where):
+        return check_device_status(lambda: zs.zs_device_status(clear=True), where)
+
+    status("setup")
+
     def timed(fn, n):
-        return timed_on_stream(torch, fn, n, args.warmup, stream, dev, dist)
+        return timed_on_stream(torch, fn, n, args.warmup, stream, dev, dist, status, "a flat-sweep point")
 
     points, launches = [], 0
     side_bw = torch.cuda.Stream(dev)
@@ -606,7 +644,7 @@ def run_sweep(args, ws, rank, local):
                        "l2": "every step moves >= 10 GB >> 129 MB L2, no flush"},
             "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": head["gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
-            "sweep": points, "gpu_launches": launches, "clocks": clocks,
+            "sweep": points, "gpu_launches": launches, "clocks": clocks, "device_status": status("the sweep"),
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
@@ -629,7 +667,7 @@ def run_next(args, ws, rank, local):
     import torch
 
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+    import synth
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -641,8 +679,13 @@ def run_next(args, ws, rank, local):
     bf16 = torch.bfloat16
     rows, launches = [], 0
 
+    def status(where):
+        return check_device_status(lambda: zs.zs_device_status(clear=True), where)
+
+    status("setup")
+
     def timed(fn):
-        return timed_on_stream(torch, fn, steps, args.warmup, stream, dev, dist)
+        return timed_on_stream(torch, fn, steps, args.warmup, stream, dev, dist, status, "a widening row")
 
     def row(name, ms, numel, nbytes, n_launch, **extra):
         gbs = nbytes / (ms / 1e3) / 1e9
@@ -869,7 +912,7 @@ def run_next(args, ws, rank, local):
                        "naive_dp_state_bytes_per_rank": state_dp, "zero2_state_bytes_per_rank": state_zero},
             "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": head["gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
-            "rows": rows, "gpu_launches": launches, "clocks": clocks,
+            "rows": rows, "gpu_launches": launches, "clocks": clocks, "device_status": status("the widening rows"),
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
@@ -895,6 +938,11 @@ def run_ours(args, ws, rank, local):
     zs.fused_variant_setting = variant
 
     stream = torch.cuda.current_stream(dev)
+
+    def status(where):
+        return check_device_status(lambda: zs.zs_device_status(clear=True), where)
+
+    status("start")
     t_setup = time.perf_counter()
     W = Workload(args, dev, stream)
     plan, n_d, P = W.plan, W.n_d, W.P
@@ -905,6 +953,7 @@ def run_ours(args, ws, rank, local):
     for _ in range(args.warmup):
         W.step()
     torch.cuda.synchronize(dev)
+    status("the warm-up steps")
 
     steps = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -923,6 +972,7 @@ def run_ours(args, ws, rank, local):
         ev[k][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    status("the timed steps")
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
@@ -958,6 +1008,7 @@ def run_ours(args, ws, rank, local):
             gbs = nbytes / (ms / 1e3) / 1e9
             return {"ms": ms, "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak}
 
+        status("the per-launch breakdown")
         breakdown = {"accumulate_first": entry(statistics.mean(acc_ms[0]), 4 * n_d * P),
                      "accumulate": entry(statistics.mean(statistics.mean(a) for a in acc_ms[1:]), 6 * n_d * P),
                      "fused": entry(statistics.mean(fused_ms), bytes_per_padded_element(n_d, "fused") * P)}
@@ -987,6 +1038,7 @@ def run_ours(args, ws, rank, local):
                 for j, name in enumerate(names):
                     per[name].append(evs[j].elapsed_time(evs[j + 1]))
                 total.append(evs[0].elapsed_time(evs[3]))
+        status("the unfused steps")
         ums = statistics.mean(total)
         kb = {"reduce_scatter_mean": 2 * n_d + 2, "adamw_shard_step": 28, "all_gather": 2 + 2 * n_d}
         unfused = {"ms_per_step": ums, "params_per_s": plan.numel / (ums / 1e3),
@@ -1008,7 +1060,9 @@ def run_ours(args, ws, rank, local):
     e2e = e2e_alt = None
     if W.kind == "fused" and not args.no_e2e and not args.profile_case:
         try:
-            e2e, e2e_alt = measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws)
+            e2e, e2e_alt = measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws, status)
+        except DeviceStatusError:
+            raise
         except (RuntimeError, MemoryError) as exc:        # e.g. pinned host memory exhausted
             e2e = {"value": None, "unit": "params/s", "error": str(exc)[:200]}
             torch.cuda.synchronize(dev)
@@ -1060,6 +1114,7 @@ def run_ours(args, ws, rank, local):
             "clocks": clocks,
             "unfused": unfused,
             "kernels": breakdown,
+            "device_status": status("the benchmark"),
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -1079,7 +1134,7 @@ def all_ranks_ok(dist, ok, device):
     return t.item() > 0.5
 
 
-def measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws):
+def measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws, status):
     """Both host-fed paths; returns (faster, other)."""
     try:
         host_g = torch.empty((n_d, P), dtype=torch.bfloat16, pin_memory=True)
@@ -1104,6 +1159,7 @@ def measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws):
             fn()
         b.record(stream)
         torch.cuda.synchronize(dev)
+        status("an end-to-end leg")
         return max_over_ranks(dist, a.elapsed_time(b) / n_e2e, dev)
 
     zc_ms = timed(lambda: zs.zs_fused_step(plan, -1, hrows, zs.ZS_RANK_FULL, W.master, W.m, W.v,
@@ -1137,7 +1193,7 @@ def measure_e2e(torch, zs, W, plan, n_d, P, steps, stream, dev, dist, ws):
 def zs_synth_buffers(n_d, n, dev):
     import torch
 
-    from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+    import synth
 
     return synth.rank_buffers(n_d, n, torch.bfloat16, dev)[0]
 
@@ -1164,11 +1220,15 @@ def main():
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, ws, rank)
-    if args.workload == "flat-sweep":
-        return run_sweep(args, ws, rank, local)
-    if args.workload == "next-rows":
-        return run_next(args, ws, rank, local)
-    return run_ours(args, ws, rank, local)
+    try:
+        if args.workload == "flat-sweep":
+            return run_sweep(args, ws, rank, local)
+        if args.workload == "next-rows":
+            return run_next(args, ws, rank, local)
+        return run_ours(args, ws, rank, local)
+    except DeviceStatusError as exc:
+        log("bench.py: %s" % exc)
+        return 3
 
 
 if __name__ == "__main__":

@@ -299,6 +299,7 @@ extern "C" int zs_checkpoint_save(zs_plan_t plan, const char* dir, const void* s
     static const char* fn = "zs_checkpoint_save";
     zs::clear_error();
     if (!plan || !dir || !shards || !master || !m || !v) return fail(fn, "NULL argument");
+    if (step < 0) return fail(fn, "step must be >= 0 (the number of optimizer steps taken)");
     cudaStream_t st = (cudaStream_t)stream;
     const std::string d(dir);
     {
@@ -376,7 +377,7 @@ extern "C" int zs_checkpoint_load(zs_plan_t plan, const char* dir, void* shards,
     meta >> key >> S.n_d;
     if (key != "n_d" || S.n_d < 1 || S.n_d > ZS_MAX_RANKS) return fail(fn, "bad n_d in meta.txt");
     meta >> key >> saved_step;
-    if (key != "step") return fail(fn, "bad step in meta.txt");
+    if (key != "step" || !meta || saved_step < 0) return fail(fn, "bad step in meta.txt");
     meta >> key >> S.layout;
     if (key != "layout" || (S.layout != ZS_LAYOUT_FSDP1 && S.layout != ZS_LAYOUT_FSDP2)) return fail(fn, "bad layout in meta.txt");
     meta >> key >> n_params;

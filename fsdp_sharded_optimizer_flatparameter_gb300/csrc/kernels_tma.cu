@@ -24,7 +24,9 @@
 // g_zs_device_error, the CTA stops taking tiles, the producer waits (again
 // bounded) for the copies it still has in flight, and the kernel returns.
 #include <memory>
+#include <mutex>
 #include <type_traits>
+#include <unordered_map>
 #include <utility>
 #include <vector>
 
@@ -35,6 +37,40 @@ namespace zs {
 __device__ unsigned int g_zs_device_error;   // 0 = fine; otherwise a ZS_DEVERR_* code
 
 namespace {
+
+// Launch geometry of a staged kernel on the current device: the SM count and how many CTAs of
+// `threads` threads and `smem` bytes of dynamic shared memory fit on one SM.  The first launch of a
+// kernel on a device raises its dynamic shared-memory limit (an attribute held per device) and asks
+// the runtime; the answer is cached per (device, kernel), so later launches make none of these
+// calls (the bucket-by-bucket and per-group paths launch many short kernels back to back).  Every
+// runtime error is returned.
+cudaError_t staged_geometry(const void* kern, int threads, int smem, int* sms, int* per_sm) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, std::pair<int, int>> cache;   // (device, kernel) -> (sms, per_sm)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t key = ((uint64_t)(uintptr_t)kern) ^ ((uint64_t)(uint32_t)dev << 56);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+        *sms = it->second.first;
+        *per_sm = it->second.second;
+        return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int n_sm = 0, occ = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (n_sm < 1 || occ < 1) return cudaErrorInvalidConfiguration;     // the kernel does not fit on an SM
+    cache.emplace(key, std::make_pair(n_sm, occ));
+    *sms = n_sm;
+    *per_sm = occ;
+    return cudaSuccess;
+}
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -589,14 +625,9 @@ cudaError_t tma_impl(const Args& a, cudaStream_t st) {
     constexpr int kSmem = Sh::kSmem + (std::is_same<Args, TmaListArgs>::value ? kListTableBytes : 0);
     static_assert(kSmem <= 232448, "shared memory above the per-CTA limit");
     auto kern = pick_kernel<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>(static_cast<const Args*>(nullptr));
-    // set on every launch: the attribute belongs to the current device
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    int sms = 0, per_sm = 0;
+    cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), kSmem);
-    if (per_sm < 1) per_sm = 1;
     const int64_t ntiles = host_tiles(a, Sh::kT);
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
@@ -867,13 +898,9 @@ template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
 cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
     auto kern = k_rs_tma<ND, NCW, VPT, MAXST, BUDGET>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    int sms = 0, per_sm = 0;
+    cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), Sh::kSmem);
-    if (per_sm < 1) per_sm = 1;
     const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;
@@ -1136,13 +1163,9 @@ cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
     using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
     static_assert(Sh::kSmem <= 232448, "shared memory above the per-CTA limit");
     auto kern = k_dp_tma<ND, NCW, VPT, MAXST, BUDGET>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmem);
+    int sms = 0, per_sm = 0;
+    cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (NCW + 1), Sh::kSmem);
-    if (per_sm < 1) per_sm = 1;
     const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
@@ -1224,11 +1247,9 @@ cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs&
     a.drain_limit = 4000000000LL;
     constexpr int S = 4;
     const int smem = 128 + S * a.T * 2;
-    cudaError_t e = cudaFuncSetAttribute(k_gather_bulk<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int sms = 0, per_sm = 0;
+    cudaError_t e = staged_geometry((const void*)k_gather_bulk<S>, 32, smem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t ntiles = (n + a.T - 1) / a.T;
     const int64_t cap = (int64_t)sms * 16;
     const int grid = (int)(ntiles < cap ? ntiles : cap);

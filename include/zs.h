@@ -421,7 +421,9 @@ int zs_zero3_rs_step_unit(zs_plan_t plan, int32_t unit, const void* const* grads
  * ZS_SHARDED arrays of `plan`, which must list the same parameters (element counts
  * and dim-0 sizes) but may use another N_d, another unit grouping and the other
  * layout: every element keeps its place in its parameter, the target's padding is
- * zeroed.  `dir` must exist.  Arrays are ZS_SHARDED device arrays of plan's
+ * zeroed.  `dir` must exist.  `step` is the number of optimizer steps taken
+ * (>= 0); load returns the saved count and rejects a meta.txt whose step is
+ * missing or negative.  Arrays are ZS_SHARDED device arrays of plan's
  * padded_numel elements.  Both calls first synchronise `stream`, then move the
  * data on up to 16 worker threads, each with its own non-blocking stream and two
  * 16 MiB pinned host staging buffers (host memory, freed before returning; no

@@ -2,7 +2,10 @@
 
 This module holds none of the method's arithmetic: it only names parameter
 shapes and draws random tensors.  Both the CUDA path (bench, tests) and the
-oracle side of the tests take their inputs from here.
+oracle side of the tests take their inputs from here.  It stands apart from
+the library package and imports nothing but torch, so a process that feeds
+the oracle from it (the CPU baseline, the oracle tests) never loads the
+library it checks.
 
 Shapes (random-initialised stand-ins; no weights or datasets are used):
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import fsdp_sharded_optimizer_flatparameter_gb300 as zs
-from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+import synth
 from oracle import accounting, layout, steps
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -250,3 +250,22 @@ def test_dependent_launch_switch():
     """The programmatic-dependent-launch switch is process-wide and never fails (no CUDA call)."""
     assert zs.zs_set_dependent_launch(False) == zs.ZS_OK
     assert zs.zs_set_dependent_launch(True) == zs.ZS_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="passes placeholder addresses; the GPU tests cover this with real buffers")
+def test_checkpoint_step_is_validated(tmp_path):
+    """A save with a negative step count and a meta.txt whose step is negative or missing are refused
+    before any device memory is touched (placeholder addresses: no case may reach a copy)."""
+    lib = ctypes.CDLL(zs.LIB_PATH)
+    lib.zs_checkpoint_save.restype = ctypes.c_int32
+    lib.zs_checkpoint_load.restype = ctypes.c_int32
+    p = zs.Plan([(64,)], 4, stage=1)
+    a = [ctypes.c_void_p(0x10000 * (k + 1)) for k in range(4)]
+    d = os.fsencode(str(tmp_path))
+    assert lib.zs_checkpoint_save(p.handle, d, *a, ctypes.c_int64(-1), None) == zs.ZS_ERR_INVALID
+    assert "step" in zs.zs_last_error()
+    step = ctypes.c_int64(0)
+    for bad in ("step -5\n", "step\n", "steps 3\n"):
+        (tmp_path / "meta.txt").write_text("zs-checkpoint 2\nn_d 4\n" + bad + "layout 0\nparams 1\n")
+        assert lib.zs_checkpoint_load(p.handle, d, *a, ctypes.byref(step), None) == zs.ZS_ERR_INVALID
+        assert "bad step" in zs.zs_last_error(), bad

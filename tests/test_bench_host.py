@@ -1,0 +1,89 @@
+"""Host-side behaviour of bench.py (no GPU).
+
+* A timed region after which the library's device status word is not zero
+  (a staged kernel whose bounded wait ran out, recorded a code and returned
+  early) yields no value: the bench raises, prints no JSON line and exits
+  with a non-zero code.
+* The reference arm (the CPU oracle) runs without the library in its
+  address space and prints its JSON line.
+"""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_check_device_status_passes_zero_and_refuses_a_code():
+    assert bench.check_device_status(lambda: 0, "a region") == 0
+    with pytest.raises(bench.DeviceStatusError) as e:
+        bench.check_device_status(lambda: 2, "the timed steps")
+    assert "2" in str(e.value) and "the timed steps" in str(e.value)
+
+
+class _FakeEvent:
+    def __init__(self, enable_timing=False):
+        pass
+
+    def record(self, stream=None):
+        pass
+
+    def elapsed_time(self, other):
+        return 1.0
+
+
+class _FakeCuda:
+    Event = _FakeEvent
+
+    @staticmethod
+    def synchronize(dev=None):
+        pass
+
+
+class _FakeTorch:
+    cuda = _FakeCuda
+
+
+def test_timed_region_with_a_device_code_yields_no_time():
+    calls = []
+    codes = iter([3])
+
+    def status(where):
+        return bench.check_device_status(lambda: next(codes), where)
+
+    with pytest.raises(bench.DeviceStatusError):
+        bench.timed_on_stream(_FakeTorch, lambda: calls.append(1), 2, 1, None, None, None, status, "a point")
+    assert len(calls) == 3                        # the region ran; its time was refused
+
+
+def test_main_prints_no_line_and_fails_when_the_status_is_set(monkeypatch, capsys):
+    def fake_run(args, ws, rank, local):
+        bench.check_device_status(lambda: 1, "the timed steps")
+        print(json.dumps({"value": 1.0}))         # never reached
+        return 0
+
+    monkeypatch.setattr(bench, "run_ours", fake_run)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "1", "--warmup", "3"])
+    rc = bench.main()
+    out = capsys.readouterr()
+    assert rc != 0
+    assert out.out.strip() == ""
+    assert "device status 1" in out.err
+
+
+def test_reference_arm_runs_without_the_library():
+    proc = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                           "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert proc.returncode == 0, proc.stderr[-3000:]
+    lines = [ln for ln in proc.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle"

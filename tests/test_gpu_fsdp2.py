@@ -15,7 +15,7 @@ import torch
 
 import fsdp_sharded_optimizer_flatparameter_gb300 as zs
 import gpu_helpers as H
-from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+import synth
 from oracle import fsdp2, numerics, steps
 
 pytestmark = pytest.mark.gpu

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import fsdp_sharded_optimizer_flatparameter_gb300 as zs
-from fsdp_sharded_optimizer_flatparameter_gb300 import synth
+import synth
 
 pytestmark = pytest.mark.gpu
 
