@@ -314,11 +314,19 @@ extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const in
             return cuda_status(fn, e);
         }
     }
+    // The buckets of the list are distinct (checked above), hence disjoint, so on each stream the
+    // launches after the first need not wait for their predecessor before they start: each streams
+    // its own bucket while the previous one drains, and waits for it only before exiting.  The first
+    // launch on each stream waits for everything enqueued before the call (zs::LaunchSync).
     cudaError_t err = cudaSuccess;
+    bool first_a = true, first_b = true;
     for (size_t i = 0; i < todo.size() && err == cudaSuccess; ++i) {
         const auto& bk = plan->buckets[todo[i]];
-        err = zs::launch_fused(g, master, m, v, o, true, {bk.begin, bk.end, 0, 1}, s, nd, (two && (i & 1)) ? b : a,
-                               pol);
+        const bool on_b = two && (i & 1);
+        bool& first = on_b ? first_b : first_a;
+        const int sync = first ? zs::kSyncWalkFirst : zs::kSyncWalkNext;
+        first = false;
+        err = zs::launch_fused(g, master, m, v, o, true, {bk.begin, bk.end, 0, 1}, s, nd, on_b ? b : a, pol, sync);
     }
     if (two) {
         // join even after a failed launch, so later work on the caller's stream orders after the side stream

@@ -131,9 +131,27 @@ __device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v
 // operations are visible) before it touches global memory, which keeps stream order for every
 // byte; it waits no longer than plain stream order would.  Launched without the attribute, both
 // instructions do nothing.
-__device__ __forceinline__ void dependent_launch_prologue() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+// A walk over disjoint ranges (the launches of one bucket-by-bucket call) relaxes this with the
+// modes of LaunchSync: its first launch waits before it lets the next one launch, and its later
+// staged launches start on their own ranges at once and wait only before they exit
+// (dependent_launch_epilogue), so a launch's CTAs stream while its predecessor drains and the walk
+// still completes in order.  The wait never deadlocks: a kernel is launched early only after every
+// CTA of its predecessor has started, so the grid it waits for needs no further resources.
+__device__ __forceinline__ void dependent_launch_prologue(int sync = kSyncStream) {
+    if (sync == kSyncWalkFirst) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    } else if (sync == kSyncWalkNext) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    } else {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
+}
+
+// Every thread of a kSyncWalkNext launch waits for the predecessor before it exits.
+__device__ __forceinline__ void dependent_launch_epilogue(int sync) {
+    if (sync == kSyncWalkNext) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Grid-stride loop helpers.

@@ -61,10 +61,11 @@ struct Split {
     int64_t lo, hi;      // whole range
     int64_t vlo;         // first element of the vector body
     int64_t nvec;        // vectors of 8 in the body (0: run everything one by one)
+    int sync;            // LaunchSync (kSyncStream or kSyncWalkFirst: these kernels read through L1)
 };
 
 static Split split_range(int64_t lo, int64_t hi, bool vec_ok) {
-    Split s{lo, hi, lo, 0};
+    Split s{lo, hi, lo, 0, kSyncStream};
     if (!vec_ok) return s;
     const int64_t vlo = (lo + 7) & ~int64_t(7);
     const int64_t vhi = hi & ~int64_t(7);
@@ -78,7 +79,7 @@ static Split split_range(int64_t lo, int64_t hi, bool vec_ok) {
 // Runs op.template run<8>(i) over the body and op.template run<1>(i) over the fringe.
 template <class Op>
 __device__ __forceinline__ void for_range(const Split& sp, const Op& op) {
-    dependent_launch_prologue();
+    dependent_launch_prologue(sp.sync);
     if (sp.nvec > 0) {
         for (int64_t t = gtid(); t < sp.nvec; t += gstride()) op.template run<8>(sp.vlo + (t << 3));
         const int64_t nhead = sp.vlo - sp.lo;
@@ -91,6 +92,7 @@ __device__ __forceinline__ void for_range(const Split& sp, const Op& op) {
     } else {
         for (int64_t i = sp.lo + gtid(); i < sp.hi; i += gstride()) op.template run<1>(i);
     }
+    dependent_launch_epilogue(sp.sync);
 }
 
 __device__ __forceinline__ int owner_of(int64_t i, int64_t base, int64_t shard) { return (int)((i - base) / shard); }
@@ -301,6 +303,9 @@ static bool all_device(const void* const* ps, int n);
 static std::atomic<int> g_fused_variant{ZS_FUSED_AUTO};   // read by launches on any thread
 // Smallest body worth a persistent staged launch (below it the register-streaming kernel is as fast).
 constexpr int64_t kTmaMinElems = int64_t(1) << 20;
+// Within a walk over disjoint buckets a staged launch overlaps its predecessor (kSyncWalkNext), so
+// the staged kernel pays off for smaller bodies there.
+constexpr int64_t kTmaWalkMinElems = int64_t(1) << 16;
 
 #define ZS_DISPATCH_ND(nd, CALL)            \
     switch (nd) {                           \
@@ -465,19 +470,25 @@ bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, con
 }
 
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st, StagedPolicy staged_policy) {
+                         const Range& r, const AdamScalars& s, int nd, cudaStream_t st, StagedPolicy staged_policy,
+                         int sync) {
     const bool vec = aligned8(g.off) && aligned8(out.off);
-    const Split sp = split_range(r.lo, r.hi, vec);
+    Split sp = split_range(r.lo, r.hi, vec);
     const int variant = g_fused_variant.load();
-    const bool want_tma = variant == ZS_FUSED_TMA || (variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= kTmaMinElems);
+    const int64_t min_staged = sync == kSyncStream ? kTmaMinElems : kTmaWalkMinElems;
+    const bool want_tma = variant == ZS_FUSED_TMA || (variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= min_staged);
     bool staged = want_tma && sp.nvec > 0 && staged_policy != kStagedNever &&
                   (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
     // only a staged candidate pays for the pointer queries, and only when the caller has not
     if (staged && staged_policy == kStagedIfDevice) staged = fused_ptrs_on_device(g, master, m, v, out, broadcast, nd);
-    if (!staged) return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);
+    if (!staged) {
+        // the streaming kernel reads through L1, so it never starts before its predecessor completes
+        sp.sync = sync == kSyncWalkFirst ? kSyncWalkFirst : kSyncStream;
+        return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);
+    }
     // staged body, then the at most 14 fringe elements one by one
     const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-    cudaError_t e = launch_fused_tma(g, master, m, v, out, broadcast, sp.vlo, sp.nvec << 3, s, nd, st);
+    cudaError_t e = launch_fused_tma(g, master, m, v, out, broadcast, sp.vlo, sp.nvec << 3, s, nd, st, sync);
     if (e != cudaSuccess) return e;
     if (sp.vlo > sp.lo) {
         e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(sp.lo, sp.vlo, false), s, nd, st);

@@ -23,6 +23,29 @@
 // Every wait is bounded (clock64 budget).  A wait that runs out sets
 // g_zs_device_error, the CTA stops taking tiles, the producer waits (again
 // bounded) for the copies it still has in flight, and the kernel returns.
+//
+// Stage reuse (every staged kernel here).  A consumer thread reads a stage with ordinary
+// shared-memory loads (the generic proxy), then arrives on the stage's "empty" barrier
+// (mbarrier.arrive.release.cta).  The producer's acquire wait on that barrier sees the phase
+// complete once every consumer has arrived, and only then refills the stage with bulk copies,
+// which write through the async proxy.  Two rules of the PTX memory model bear on whether a refill
+// can land under a consumer's loads:
+//   (1) the arrive's release orders the thread's earlier memory accesses before the arrive, for a
+//       thread that acquires the barrier's phase, within the generic proxy;
+//   (2) accesses to one location through different proxies are ordered only across a proxy fence
+//       (fence.proxy.async); a bulk copy's own completion carries one, but nothing orders a
+//       generic-proxy read before a later async-proxy write to the same shared memory.
+// So release/acquire alone does not promise that a consumer's loads have returned before the
+// refill writes the stage, and on GB300 they did not always: a staged all-reduce whose consumers
+// arrived right after their loads read, for a few elements in 10^5, the data of the tile S
+// positions later in the same stage.  The protocol these kernels rely on is therefore a data
+// dependency, not the memory model: a consumer arrives on an empty barrier only after
+// instructions that consume every value it loaded from that stage (the global stores of its
+// results; a thread that loaded nothing, past the end of a tile, arrives at once, and a thread
+// of the list kernel past the end of a tile discards what it loaded).  The arrive cannot issue
+// before the loads it depends on have delivered their data, whatever the proxies.  A change that
+// moves an arrive above the consuming stores (releasing after the state stores only, say) must
+// keep that dependency; tests/test_stage_release.py checks the source for it.
 #include <memory>
 #include <mutex>
 #include <type_traits>
@@ -79,18 +102,20 @@ __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
 }
 
+// The arrive and the wait spell out the semantics PTX gives them by default (release and acquire
+// at CTA scope), so what the stage protocol below rests on is visible at the call.
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(su32(b)), "r"(parity)
@@ -177,6 +202,7 @@ struct TmaArgs {
     float inv_nd;
     long long wait_limit; // cycles a wait may take before the kernel gives up
     long long drain_limit;// cycles to wait for copies still in flight after giving up
+    int sync;             // LaunchSync: order against the previous kernel on the stream
 };
 
 // A list of bodies stepped by one launch (the buckets of one call, in the caller's order): body r
@@ -234,9 +260,8 @@ struct TmaShape {
     static_assert(2 * kStages * 8 <= 256, "barriers must fit in the first 256 bytes");
 };
 
-template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
-__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_constant__ TmaArgs a) {
-    dependent_launch_prologue();
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET>
+__device__ __forceinline__ void fused_tma_body(const TmaArgs& a) {
     using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
@@ -359,17 +384,23 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
                     __stcs(reinterpret_cast<uint2*>(a.out.p[0] + (i - a.out_off)), w);
                 }
             }
-            // The stage is released after the stores, which consume what was read from it, not right
-            // after the shared-memory loads: on GB300 the arrive on the empty barrier can take effect
-            // before those loads have returned their data, and the producer's refill of the stage then
-            // lands under them (a staged all-reduce that released early read, for a few elements in
-            // 10^5, the values of the tile S positions later in the same stage).  Measured cost here:
-            // none (11.27 against 11.30 ms per step).
+            // The stage is released after the stores, which consume everything read from it (the
+            // stage reuse protocol at the top of this file); measured cost: none (11.27 against
+            // 11.30 ms per step).
             mbar_arrive(&empty[s]);
         } else {
             mbar_arrive(&empty[s]);
         }
     }
+}
+
+// The step over one range; the body returns early (producer lanes, a wait that ran out) into the
+// launch-order epilogue, which a kSyncWalkNext launch needs on every exit path.
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_constant__ TmaArgs a) {
+    dependent_launch_prologue(a.sync);
+    fused_tma_body<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>(a);
+    dependent_launch_epilogue(a.sync);
 }
 
 // The broadcast step over a list of disjoint bodies in one launch (bodies that touch are merged
@@ -699,6 +730,7 @@ TmaArgs make_args(const BView& g, float* master, float* m, float* v, const BView
     a.inv_nd = 1.0f / (float)nd;
     a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
     a.drain_limit = 4000000000LL;
+    a.sync = kSyncStream;
     return a;
 }
 
@@ -706,10 +738,11 @@ TmaArgs make_args(const BView& g, float* master, float* m, float* v, const BView
 
 // Returns cudaErrorNotSupported when no staged variant exists for this rank count.
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st, int sync) {
     TmaArgs a = make_args(g, master, m, v, out, s, nd);
     a.lo = lo;
     a.n = n;
+    a.sync = sync;
     return with_shape(broadcast, nd, [&](auto ND, auto NCW, auto VPT, auto BR, auto MS, auto BU) {
         return tma_impl<decltype(ND)::value, decltype(NCW)::value, decltype(VPT)::value, decltype(BR)::value,
                         decltype(MS)::value, decltype(BU)::value>(a, st);

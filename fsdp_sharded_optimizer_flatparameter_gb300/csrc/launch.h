@@ -29,6 +29,20 @@ struct AdamScalars {
     float beta1, beta2, eps, decay, c1, c2, step_size, sqrt_bc2;
 };
 
+// How a kernel orders itself against the previous kernel on its stream under programmatic
+// dependent launch (see dependent_launch_prologue in device.cuh).
+//   kSyncStream    every launch by default: let the successor launch, then wait for the
+//                  predecessor before touching global memory (plain stream order for every byte).
+//   kSyncWalkFirst the first launch of a walk over disjoint ranges: wait for the predecessor,
+//                  then let the successor launch, so no later launch of the walk starts before
+//                  everything enqueued ahead of the walk has completed.
+//   kSyncWalkNext  a later staged launch of such a walk: let the successor launch at once and read
+//                  and write its own range without waiting, then wait for the predecessor before
+//                  exiting, so it completes after every launch before it.  Valid only when the
+//                  kernel touches no byte that an earlier launch of the walk touches, and it reads
+//                  global memory only through bulk copies (which read L2, never a stale L1 line).
+enum LaunchSync : int { kSyncStream = 0, kSyncWalkFirst = 1, kSyncWalkNext = 2 };
+
 // A global range [lo, hi) inside one unit (base, shard); owner(i) = (i - base) / shard.
 struct Range {
     int64_t lo, hi;
@@ -49,16 +63,20 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
 // Which fused kernel a launch may use.  kStagedIfDevice asks the runtime about every pointer;
 // kStagedDeviceKnown is for callers that already did (fused_ptrs_on_device) for the same pointers.
 enum StagedPolicy { kStagedNever = 0, kStagedIfDevice = 1, kStagedDeviceKnown = 2 };
+// `sync` (LaunchSync) orders the launch against its predecessor; a walk over disjoint buckets passes
+// kSyncWalkFirst for its first launch on a stream and kSyncWalkNext for later ones, and then also
+// takes the staged kernel for bodies down to kTmaWalkMinElems.
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                          const Range& r, const AdamScalars& s, int nd, cudaStream_t st,
-                         StagedPolicy staged_policy = kStagedIfDevice);
+                         StagedPolicy staged_policy = kStagedIfDevice, int sync = kSyncStream);
 // True when every pointer a fused launch over these views touches is device memory.
 bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast, int nd);
 
 // Bulk-copy staged fused kernel over the 8-aligned body [lo, lo + n); returns
 // cudaErrorNotSupported when no staged variant exists for this rank count.
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
+                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st,
+                             int sync = kSyncStream);
 // The broadcast staged kernel over a list of bodies ([lo, lo + n): the TMA alignment rules of
 // launch_fused_tma for each) in one launch per kTmaListMax (128) bodies, tiles walked in list order.
 cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float* v, const BView& out,

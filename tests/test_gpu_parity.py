@@ -694,14 +694,17 @@ def test_guard_zones_untouched_large_kernels():
         assert bool((raw[:g] == 0x5A).all()) and bool((raw[-g:] == 0x5A).all())
 
 
-@pytest.mark.parametrize("bucket_bytes", [1 << 20, 4 << 20, 1000])
+@pytest.mark.parametrize("bucket_bytes", [1 << 20, 4 << 20, 1000, 2 * 65544])
 @pytest.mark.parametrize("mode", ["walk", "per_bucket", "per_bucket_two_streams"])
 def test_fused_step_buckets_equals_whole_range(bucket_bytes, mode):
     """zs_fused_step_buckets over all buckets, descending, equals the whole-range step: walked as two
     lists of disjoint buckets, one launch per bucket, and one launch per bucket with the odd
     positions on a side stream.  Work enqueued on the caller's stream just before the call is
-    seen, and work enqueued right after it sees the whole step; a repeated bucket is refused before
-    anything runs."""
+    seen, and work enqueued right after it sees the whole step (one launch per bucket lets a
+    bucket's launch start before the previous bucket's ends; only the first launch on each stream
+    waits for what came before the call); a repeated bucket is refused before anything runs.
+    65,544-element buckets make the walk start with a short last bucket on the streaming kernel and
+    go on with staged launches."""
     plan, _ = _plans([(3_000_011,)], 8, bucket_bytes=bucket_bytes)
     P, pads = plan.padded, plan.pad_ranges()
     master0 = synth.master_init(P, pads, seed=62, device=DEV)
