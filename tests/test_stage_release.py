@@ -18,7 +18,8 @@ import re
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "fsdp_sharded_optimizer_flatparameter_gb300", "csrc", "kernels_tma.cu")
 
-KERNELS = ("k_fused_tma", "k_fused_tma_list", "k_rs_tma", "k_dp_tma")
+# the staged kernels' consumer code (k_fused_tma's lives in fused_tma_body, which the kernel calls)
+KERNELS = ("fused_tma_body", "k_fused_tma_list", "k_rs_tma", "k_dp_tma")
 LOAD = re.compile(r"\blds_(?:bf|f32)<")
 STORE = re.compile(r"\b__stcs\(|\bstg_f32<")
 # consumer releases: empty[...] pairs with full[...], gempty[...] with gfull[...]
@@ -32,7 +33,7 @@ def _strip_comments(text):
 
 
 def _kernel_body(text, name):
-    m = re.search(r"__global__ void[^\n]*\b%s\(" % re.escape(name), text)
+    m = re.search(r"(?:__global__|__device__)[^\n]*\bvoid[^\n]*\b%s\(" % re.escape(name), text)
     assert m, "kernel %s not found" % name
     start = text.index("{", m.end())
     depth, i = 0, start
@@ -83,6 +84,7 @@ def test_every_consumer_arrive_follows_the_stores_that_consume_the_stage():
                 % (name, a.group(1)))
             checked += 1
     assert checked >= 6
+    assert "fused_tma_body<" in _kernel_body(text, "k_fused_tma")
 
 
 def test_barrier_semantics_are_explicit():
