@@ -241,8 +241,9 @@ static int fused_common(const char* fn, zs_plan_t plan, int32_t bucket, const vo
         r = {0, plan->padded, 0, 1};       // the fused step needs no owner: one pass over the flat space
     }
     if (r.hi <= r.lo) return ZS_OK;
-    // gradients or replicas may be pinned host memory: launch_fused then keeps to the streaming kernel
-    return cuda_status(fn, zs::launch_fused(g, master, m, v, o, true, r, s, nd, st));
+    // gradients or replicas may be pinned host memory: launch_fused then keeps to the streaming kernel.
+    // The range is walked in chunks whose launches overlap (zs::launch_fused_walk).
+    return cuda_status(fn, zs::launch_fused_walk(g, master, m, v, o, {r}, s, nd, st, zs::kStagedIfDevice));
 }
 
 extern "C" int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
@@ -314,20 +315,17 @@ extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const in
             return cuda_status(fn, e);
         }
     }
-    // The buckets of the list are distinct (checked above), hence disjoint, so on each stream the
-    // launches after the first need not wait for their predecessor before they start: each streams
-    // its own bucket while the previous one drains, and waits for it only before exiting.  The first
-    // launch on each stream waits for everything enqueued before the call (zs::LaunchSync).
-    cudaError_t err = cudaSuccess;
-    bool first_a = true, first_b = true;
-    for (size_t i = 0; i < todo.size() && err == cudaSuccess; ++i) {
+    // The buckets of the list are distinct (checked above), hence disjoint, so on each stream they are
+    // walked (zs::launch_fused_walk): the launches after the first need not wait for their predecessor
+    // before they start; each streams its own bucket while the previous one drains, and completes
+    // after it.  The first launch on each stream waits for everything enqueued before the call.
+    std::vector<zs::Range> on_a, on_b;
+    for (size_t i = 0; i < todo.size(); ++i) {
         const auto& bk = plan->buckets[todo[i]];
-        const bool on_b = two && (i & 1);
-        bool& first = on_b ? first_b : first_a;
-        const int sync = first ? zs::kSyncWalkFirst : zs::kSyncWalkNext;
-        first = false;
-        err = zs::launch_fused(g, master, m, v, o, true, {bk.begin, bk.end, 0, 1}, s, nd, on_b ? b : a, pol, sync);
+        ((two && (i & 1)) ? on_b : on_a).push_back({bk.begin, bk.end, 0, 1});
     }
+    cudaError_t err = zs::launch_fused_walk(g, master, m, v, o, on_a, s, nd, a, pol);
+    if (err == cudaSuccess && !on_b.empty()) err = zs::launch_fused_walk(g, master, m, v, o, on_b, s, nd, b, pol);
     if (two) {
         // join even after a failed launch, so later work on the caller's stream orders after the side stream
         cudaError_t e = cudaEventRecord(join, b);

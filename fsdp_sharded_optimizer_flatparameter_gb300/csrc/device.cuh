@@ -133,7 +133,7 @@ __device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v
 // instructions do nothing.
 // A walk over disjoint ranges (the launches of one bucket-by-bucket call) relaxes this with the
 // modes of LaunchSync: its first launch waits before it lets the next one launch, and its later
-// staged launches start on their own ranges at once and wait only before they exit
+// staged launches start on their own ranges at once and wait only before their CTA 0 exits
 // (dependent_launch_epilogue), so a launch's CTAs stream while its predecessor drains and the walk
 // still completes in order.  The wait never deadlocks: a kernel is launched early only after every
 // CTA of its predecessor has started, so the grid it waits for needs no further resources.
@@ -149,9 +149,12 @@ __device__ __forceinline__ void dependent_launch_prologue(int sync = kSyncStream
     }
 }
 
-// Every thread of a kSyncWalkNext launch waits for the predecessor before it exits.
+// A kSyncWalkNext launch completes only after its predecessor: CTA 0 waits for the predecessor
+// before it exits, and a grid completes when its last CTA exits.  The other CTAs exit as soon as
+// their work is done, so a CTA that drew fewer tiles frees its SM for the next launch at once.
 __device__ __forceinline__ void dependent_launch_epilogue(int sync) {
-    if (sync == kSyncWalkNext) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (sync == kSyncWalkNext && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Grid-stride loop helpers.

@@ -498,6 +498,32 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
     return e;
 }
 
+cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v, const BView& out,
+                              const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
+                              StagedPolicy staged_policy) {
+    // Cut points are multiples of the chunk (8-aligned, so a range's pieces keep its own fringes
+    // only), none closer than a quarter chunk to a range end, so no piece is a sliver.
+    const bool chunked = fused_walk_shape(nd);
+    constexpr int64_t C = kFusedWalkChunk;
+    bool first = true;
+    for (const Range& r : ranges) {
+        int64_t lo = r.lo;
+        while (lo < r.hi) {
+            int64_t hi = r.hi;
+            if (chunked) {
+                const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
+                if (cut < r.hi - C / 4) hi = cut;
+            }
+            const cudaError_t e = launch_fused(g, master, m, v, out, true, {lo, hi, r.base, r.shard}, s, nd, st,
+                                               staged_policy, first ? kSyncWalkFirst : kSyncWalkNext);
+            if (e != cudaSuccess) return e;
+            first = false;
+            lo = hi;
+        }
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* v, const BView& out,
                                 const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
                                 StagedPolicy staged_policy) {
@@ -515,7 +541,10 @@ cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* 
     }
     merged.resize(w);
     if (merged.empty()) return cudaSuccess;
-    if (merged.size() == 1) return launch_fused(g, master, m, v, out, true, merged[0], s, nd, st, staged_policy);
+    // with a walk shape, disjoint ranges are walked one launch each (the launches overlap); the list
+    // kernel below serves the rank counts without one
+    if (merged.size() == 1 || fused_walk_shape(nd))
+        return launch_fused_walk(g, master, m, v, out, merged, s, nd, st, staged_policy);
     const bool vec = aligned8(g.off) && aligned8(out.off);
     std::vector<Split> splits;
     splits.reserve(merged.size());

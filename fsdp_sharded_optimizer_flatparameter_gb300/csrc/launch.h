@@ -37,8 +37,8 @@ struct AdamScalars {
 //                  then let the successor launch, so no later launch of the walk starts before
 //                  everything enqueued ahead of the walk has completed.
 //   kSyncWalkNext  a later staged launch of such a walk: let the successor launch at once and read
-//                  and write its own range without waiting, then wait for the predecessor before
-//                  exiting, so it completes after every launch before it.  Valid only when the
+//                  and write its own range without waiting; CTA 0 waits for the predecessor before
+//                  exiting, so the launch completes after every launch before it.  Valid only when the
 //                  kernel touches no byte that an earlier launch of the walk touches, and it reads
 //                  global memory only through bulk copies (which read L2, never a stale L1 line).
 enum LaunchSync : int { kSyncStream = 0, kSyncWalkFirst = 1, kSyncWalkNext = 2 };
@@ -72,6 +72,17 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
 // True when every pointer a fused launch over these views touches is device memory.
 bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast, int nd);
 
+// Whether the broadcast staged kernel has a walk shape for this rank count: a shape whose launches
+// share each SM with the next launch of a walk, for kSyncWalkFirst / kSyncWalkNext launches.
+bool fused_walk_shape(int nd);
+// The broadcast fused step over disjoint ranges as a walk: ranges longer than kFusedWalkChunk are cut
+// at multiples of it, each piece is one launch, the first on the stream kSyncWalkFirst and the others
+// kSyncWalkNext, so every launch streams its piece while the previous one drains.  Without a walk
+// shape for nd, one launch per range in stream order.
+constexpr int64_t kFusedWalkChunk = int64_t(1) << 22;
+cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v, const BView& out,
+                              const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
+                              StagedPolicy staged_policy);
 // Bulk-copy staged fused kernel over the 8-aligned body [lo, lo + n); returns
 // cudaErrorNotSupported when no staged variant exists for this rank count.
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
