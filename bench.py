@@ -211,6 +211,41 @@ def library_mapped(name="libzs.so"):
 
 # ------------------------------------------------------------------ workloads
 
+# The launches of a walked fused step (the rule of launch_fused_walk in csrc/kernels.cu): ranges longer
+# than the chunk are cut at multiples of it, none closer than a quarter chunk to a range end; each
+# piece is one launch of the staged kernel (plus one per fringe off the 8-element grid), or one
+# streaming launch when its body is below the walk's staged threshold.
+WALK_CHUNK = 1 << 22           # kFusedWalkChunk
+WALK_MIN_STAGED = 1 << 16      # kTmaWalkMinElems
+WALK_SHAPE_ND = (2, 4, 8, 16, 32)  # rank counts with a walk shape (fused_walk_shape)
+STAGED_ND = (2, 4, 8, 16, 32)
+
+
+def walk_pieces(ranges, n_d):
+    out, C = [], WALK_CHUNK
+    for lo, hi in ranges:
+        while lo < hi:
+            end = hi
+            if n_d in WALK_SHAPE_ND:
+                cut = (lo + C // 4 + C) // C * C
+                if cut < hi - C // 4:
+                    end = cut
+            out.append((lo, end))
+            lo = end
+    return out
+
+
+def walk_launches(ranges, n_d, staged_ok=True):
+    n = 0
+    for lo, hi in walk_pieces(ranges, n_d):
+        vlo, vhi = (lo + 7) // 8 * 8, hi // 8 * 8
+        if staged_ok and n_d in STAGED_ND and vhi - vlo >= WALK_MIN_STAGED:
+            n += 1 + (vlo > lo) + (hi > vhi)
+        else:
+            n += 1
+    return n
+
+
 def bytes_per_padded_element(n_d, kernel):
     """Algorithmic HBM bytes per padded element of one launch (each byte crosses HBM once)."""
     if kernel == "fused":          # read N_d bf16 grads + master/m/v; write master/m/v + N_d bf16 replicas
@@ -442,23 +477,27 @@ class Workload:
     # algorithmic HBM bytes of one step and the kernel launches it makes
     def step_bytes(self):
         n_d, P = self.n_d, self.P
+        walk = walk_launches([(0, P)], n_d, self.staged())
         if self.kind == "fused":
-            return bytes_per_padded_element(n_d, "fused") * P, 1
+            return bytes_per_padded_element(n_d, "fused") * P, walk
         if self.kind == "accumulate+fused":
             micro = self.wl["micro"]
             acc = n_d * P * (4 + 6 * (micro - 1))       # first: read micro, write acc; then read both, write acc
-            return acc + bytes_per_padded_element(n_d, "fused") * P, micro + 1
+            return acc + bytes_per_padded_element(n_d, "fused") * P, micro + walk
         # zero3: per unit two gathers (read shard, write N_d copies) + reduce-scatter with update
         return P * (2 * (2 + 2 * n_d) + (2 * n_d + 12 + 12 + 2)), 3 * self.plan.n_units
 
     def staged(self):
         zs = self.zs
         v = zs.fused_variant_setting
-        big = (self.P >= (1 << 20)) if self.kind != "zero3" else True
+        big = (self.P >= WALK_MIN_STAGED) if self.kind != "zero3" else True
         return self.n_d in (2, 4, 8, 16, 32) and (v == zs.ZS_FUSED_TMA or (v == zs.ZS_FUSED_AUTO and big))
 
     def kernel_label(self):
         fused = ("k_fused_tma<%d>" if self.staged() else "k_fused<%d>") % self.n_d
+        pieces = len(walk_pieces([(0, self.P)], self.n_d))
+        if pieces > 1:
+            fused += " walked in %d overlapping launches" % pieces
         if self.kind == "fused":
             return fused
         if self.kind == "accumulate+fused":
@@ -1050,6 +1089,39 @@ def run_ours(args, ws, rank, local):
                                for name in names}}
         del ghat, shards
 
+    # ZeRO-2 as the buckets become ready (config 2's bucket-wise flow): every bucket of the plan, last
+    # first, stepped bucket by bucket (no launch spans two buckets), on one stream and with the odd
+    # positions on a side stream; and the same list as one walk (touching buckets merge).  Not part of
+    # value.
+    bucketwise = None
+    if W.kind == "fused" and rank == 0 and not args.profile_case and args.bucketwise_steps > 0:
+        order = list(reversed(range(plan.n_buckets)))
+        branges = [plan.bucket(b)[1:] for b in order]
+        side_bw = torch.cuda.Stream(dev)
+        recs = []
+        for label, lm, sd, nl in (
+                ("bucket by bucket, one stream", zs.ZS_BUCKETS_PER_BUCKET, None,
+                 walk_launches(branges, n_d, W.staged())),
+                ("bucket by bucket, odd positions on a side stream", zs.ZS_BUCKETS_PER_BUCKET, side_bw,
+                 walk_launches(branges[0::2], n_d, W.staged()) + walk_launches(branges[1::2], n_d, W.staged())),
+                ("one walk over the list (touching buckets merge)", zs.ZS_BUCKETS_ONE_WALK, None,
+                 walk_launches([(0, P)], n_d, W.staged()))):
+
+            def bw(lm=lm, sd=sd):
+                W.t += 1
+                zs.zs_fused_step_buckets(plan, order, W.grads, W.master, W.m, W.v, W.reps, W.hp, W.t, launch_mode=lm,
+                                         stream=stream, side_stream=sd)
+
+            ms = timed_on_stream(torch, bw, args.bucketwise_steps, 3, stream, dev, None, status,
+                                 "the bucket-wise steps")
+            gbs = algo_bytes / (ms / 1e3) / 1e9
+            recs.append({"mode": label, "ms_per_step": ms, "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs,
+                         "frac": gbs / peak, "launches_per_step": nl})
+        bucketwise = {"buckets": plan.n_buckets, "bucket_bytes": W.wl["bucket_bytes"],
+                      "order": "descending (the last bucket first, as backward makes them ready)",
+                      "step": "zs_fused_step_buckets: reduce-scatter-mean + AdamW + all-gather per bucket",
+                      "modes": recs}
+
     # end to end through the C ABI with host buffers, all inside the timed region, two ways:
     #  (a) zero-copy: zs_fused_step reads every rank's gradients from pinned host memory and writes
     #      rank 0's updated replica to pinned host memory over the host link, in the kernel itself;
@@ -1105,7 +1177,10 @@ def run_ours(args, ws, rank, local):
                          "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
                          "algorithmic_bytes_per_launch": algo_bytes if launches == 1 else None,
                          "algorithmic_bytes_per_step": algo_bytes, "kernel": W.kernel_label(),
-                         "kernel_ms": step_ms},
+                         "launches_per_step": launches, "kernel_ms": step_ms,
+                         "timing": ("CUDA events around each step on the launching stream; the step's "
+                                    "launches overlap (each starts while the previous drains), so "
+                                    "achieved = algorithmic bytes per step / step span")},
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all if cpu is not None else None,
             "e2e": e2e,
@@ -1113,6 +1188,7 @@ def run_ours(args, ws, rank, local):
             "gpu_launches": launches * steps,
             "clocks": clocks,
             "unfused": unfused,
+            "bucketwise": bucketwise,
             "kernels": breakdown,
             "device_status": status("the benchmark"),
         }
@@ -1210,6 +1286,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused-steps", type=int, default=10)
+    ap.add_argument("--bucketwise-steps", type=int, default=10)
     ap.add_argument("--fused-variant", choices=["auto", "ldg", "tma"], default="auto",
                     help="kernel behind the fused step (all variants compute identical results)")
     args = ap.parse_args()

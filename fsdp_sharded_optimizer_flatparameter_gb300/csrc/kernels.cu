@@ -527,9 +527,9 @@ cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v,
 cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* v, const BView& out,
                                 const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
                                 StagedPolicy staged_policy) {
-    // Inside one launch the order of disjoint ranges is not observable, so ranges that touch are
-    // merged (a run of neighbouring buckets, in either order, becomes one range for the single-range
-    // kernels); only what stays disjoint goes through the list kernel.
+    // The order of disjoint ranges is not observable, so ranges that touch are merged (a run of
+    // neighbouring buckets, in either order, becomes one range, walked); what stays disjoint is walked
+    // range by range, except short runs, which share list launches.
     std::vector<Range> merged;
     for (const Range& r : ranges)
         if (r.hi > r.lo) merged.push_back(r);
@@ -541,10 +541,7 @@ cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* 
     }
     merged.resize(w);
     if (merged.empty()) return cudaSuccess;
-    // with a walk shape, disjoint ranges are walked one launch each (the launches overlap); the list
-    // kernel below serves the rank counts without one
-    if (merged.size() == 1 || fused_walk_shape(nd))
-        return launch_fused_walk(g, master, m, v, out, merged, s, nd, st, staged_policy);
+    if (merged.size() == 1) return launch_fused_walk(g, master, m, v, out, merged, s, nd, st, staged_policy);
     const bool vec = aligned8(g.off) && aligned8(out.off);
     std::vector<Split> splits;
     splits.reserve(merged.size());
@@ -566,30 +563,32 @@ cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* 
         }
         return cudaSuccess;
     }
-    // Large disjoint ranges go one launch each to the single-range kernel (with dependent launch its
-    // CTAs are resident as the previous launch drains; the list kernel streams ~5 % slower per tile),
-    // the rest through one list launch.  Measured on 2^28 elements at N_d = 8, two walks of every
-    // other bucket: one launch per 64 MiB bucket 95.5 % of the copy rate against 92.3 % for the
-    // list kernel; at 16 MiB the list kernel leads (92.2 % against 88.5 %).
-    constexpr int64_t kOwnLaunchElems = int64_t(1) << 25;
+    // Ranges with a body of at least kTmaWalkMinElems are walked (one or more launches each, which
+    // overlap: the walk shape streams them at the copy rate, 1 MiB buckets included); the short runs
+    // left go through one list launch per kTmaListMax bodies, which pays one ramp for all of them
+    // instead of one launch each.
+    std::vector<Range> walked;
     std::vector<std::pair<int64_t, int64_t>> bodies;
     bodies.reserve(splits.size());
     cudaError_t e = cudaSuccess;
-    for (const Split& sp : splits) {
-        if (sp.nvec <= 0) continue;
-        if ((sp.nvec << 3) >= kOwnLaunchElems) {
-            e = launch_fused_tma(g, master, m, v, out, true, sp.vlo, sp.nvec << 3, s, nd, st);
-            if (e != cudaSuccess) return e;
-        } else {
-            bodies.emplace_back(sp.vlo, sp.nvec << 3);
-        }
+    for (size_t k = 0; k < splits.size(); ++k) {
+        const Split& sp = splits[k];
+        if ((sp.nvec << 3) >= kTmaWalkMinElems && fused_walk_shape(nd)) walked.push_back(merged[k]);
+        else if (sp.nvec > 0) bodies.emplace_back(sp.vlo, sp.nvec << 3);
+    }
+    if (!walked.empty()) {
+        e = launch_fused_walk(g, master, m, v, out, walked, s, nd, st, kStagedDeviceKnown);
+        if (e != cudaSuccess) return e;
     }
     if (!bodies.empty()) {
         e = launch_fused_tma_list(g, master, m, v, out, bodies, s, nd, st);
         if (e != cudaSuccess) return e;
     }
-    // fringes (ranges whose ends are off the 8-element grid): at most 14 elements per range
-    for (const Split& sp : splits) {
+    // fringes of the listed runs (ends off the 8-element grid): at most 14 elements per range; the
+    // walked ranges' fringes were launched by the walk
+    for (size_t k = 0; k < splits.size(); ++k) {
+        const Split& sp = splits[k];
+        if ((sp.nvec << 3) >= kTmaWalkMinElems && fused_walk_shape(nd)) continue;
         const int64_t body_hi = sp.nvec > 0 ? sp.vlo + (sp.nvec << 3) : sp.lo;
         const int64_t head_hi = sp.nvec > 0 ? sp.vlo : sp.hi;
         if (head_hi > sp.lo) {

@@ -720,17 +720,27 @@ cudaError_t with_shape(bool broadcast, int nd, F&& f) {
 }
 
 // The broadcast shape for the launches of a walk (kSyncWalkFirst / kSyncWalkNext), where consecutive
-// launches overlap: half an SM's shared memory per CTA, so a launch's CTAs share each SM with the
-// next launch's.  N_d = 8: 8 consumer warps x 8 elements, T = 2048, 2 stages (114,944 B, two CTAs per
-// SM).  Measured on GB300 (Llama-1.3B buffer, N_d = 8, the step walked in 4 Mi-element launches):
-// 103.5 % of the copy rate, against 98.5 % for one persistent launch of the whole-range shape over
-// the same bytes and 95 % for this shape in one persistent launch; among walk shapes (T = 1024 with
-// 3-4 stages, T = 512 with 4-8 stages, 4 or 8 consumer warps) it led for every bucket size from
-// 1 to 64 MiB.  cudaErrorNotSupported where no walk shape exists (other rank counts).
+// launches overlap: a two-stage ring in under half an SM's shared memory, so a launch's CTAs share
+// each SM with the next launch's.  N_d = 8: 8 consumer warps x 8 elements, T = 2048 (114,944 B).
+// Measured on GB300 (Llama-1.3B buffer, N_d = 8, the step walked in 4 Mi-element launches): 103.5 %
+// of the copy rate, against 98.5 % for one persistent launch of the whole-range shape over the same
+// bytes and 95 % for this shape in one persistent launch; among walk shapes (T = 1024 with 3-4
+// stages, T = 512 with 4-8 stages, 4 or 8 consumer warps) it led for every bucket size from 1 to
+// 64 MiB.  The other rank counts, on the 2^28+7 buffer (whole step walked / one launch per 1, 4,
+// 16 MiB bucket, of the copy rate; the whole-range shape's single launch in brackets):
+//   N_d = 2:  8 warps x 8, T 2048, 2 stages: 102.9 / 97.5 / 99.4 / 102.6 %  (98.2 %)
+//   N_d = 4:  8 warps x 8, T 2048, 2 stages: 102.4 / 87.8 / 97.8 / 102.3 %  (100.5 %)
+//   N_d = 16: 8 warps x 4, T 1024, 2 stages: 101.1 / 97.6 / 101.6 / 101.2 % (94.4 %)
+//   N_d = 32: 4 warps x 4, T 512, 2 stages:  99.7 / 99.4 / 99.2 / 99.8 %    (93.6 %)
+// each the best of four candidates (2-4 stages, 2-8 consumer warps) at its rank count.
 template <class F>
 cudaError_t with_walk_shape(int nd, F&& f) {
     switch (nd) {
+        case 2: return f(IC<2>{}, IC<8>{}, IC<8>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        case 4: return f(IC<4>{}, IC<8>{}, IC<8>{}, BC<true>{}, IC<2>{}, IC<115712>{});
         case 8: return f(IC<8>{}, IC<8>{}, IC<8>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        case 16: return f(IC<16>{}, IC<8>{}, IC<4>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        case 32: return f(IC<32>{}, IC<4>{}, IC<4>{}, BC<true>{}, IC<2>{}, IC<115712>{});
         default: return cudaErrorNotSupported;
     }
 }
@@ -777,7 +787,7 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
     });
 }
 
-bool fused_walk_shape(int nd) { return nd == 8; }
+bool fused_walk_shape(int nd) { return nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32; }
 
 namespace {
 

@@ -93,9 +93,10 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
 cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float* v, const BView& out,
                                   const std::vector<std::pair<int64_t, int64_t>>& bodies, const AdamScalars& s,
                                   int nd, cudaStream_t st);
-// The broadcast fused step over several disjoint ranges: with the staged kernel one walk over all of
-// them (bodies in one list launch, the few fringe elements by the streaming kernel), else one
-// streaming launch per range.
+// The broadcast fused step over several ranges: touching ranges merge; with the staged kernel each
+// range with a body of at least kTmaWalkMinElems is walked (launch_fused_walk) and the short runs
+// share list launches (their fringe elements by the streaming kernel); else one streaming launch per
+// range.
 cudaError_t launch_fused_ranges(const BView& g, float* master, float* m, float* v, const BView& out,
                                 const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
                                 StagedPolicy staged_policy = kStagedIfDevice);
