@@ -586,7 +586,7 @@ def run_sweep(args, ws, rank, local):
             zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, t[0], stream=stream)
 
         ms = timed(fused, steps)
-        launches += steps
+        launches += steps * walk_launches([(0, P)], n_d)
         gbs = bytes_per_padded_element(n_d, "fused") * P / (ms / 1e3) / 1e9
         points.append({"n_d": n_d, "padding": P - plan.numel, "step": "fused, whole buffer", "ms": ms,
                        "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
@@ -612,13 +612,15 @@ def run_sweep(args, ws, rank, local):
                 bp = zs.Plan(shapes, n_d, stage=2, bucket_bytes=mib << 20)
 
                 order = list(reversed(range(bp.n_buckets)))
-                half = -(-bp.n_buckets // 2)
-                modes = (("one walk over the list (neighbours merge into one range)", zs.ZS_BUCKETS_ONE_WALK, None, 1),
-                         ("two walks: every other bucket, then the rest (disjoint runs, list kernel)",
-                          "alternate", None, 2 * -(-half // 128)),
-                         ("one launch per bucket", zs.ZS_BUCKETS_PER_BUCKET, None, bp.n_buckets),
-                         ("one launch per bucket, odd positions on a side stream", zs.ZS_BUCKETS_PER_BUCKET,
-                          side_bw, bp.n_buckets))
+                br = [bp.bucket(b)[1:] for b in order]
+                modes = (("one walk over the list (neighbours merge into one range)", zs.ZS_BUCKETS_ONE_WALK, None,
+                          walk_launches([(0, P)], n_d)),
+                         ("two walks: every other bucket, then the rest (disjoint ranges)",
+                          "alternate", None, walk_launches(sorted(br[0::2]), n_d) + walk_launches(sorted(br[1::2]), n_d)),
+                         ("bucket by bucket (no launch spans two buckets)", zs.ZS_BUCKETS_PER_BUCKET, None,
+                          walk_launches(br, n_d)),
+                         ("bucket by bucket, odd positions on a side stream", zs.ZS_BUCKETS_PER_BUCKET,
+                          side_bw, walk_launches(br[0::2], n_d) + walk_launches(br[1::2], n_d)))
                 for label, lm, side, n_launch in modes:
 
                     def bucketwise(bp=bp, order=order, lm=lm, side=side):
@@ -784,8 +786,8 @@ def run_next(args, ws, rank, local):
         zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, z_master, z_m, z_v, reps, hp, t[0], stream=stream)
 
     row("ZeRO-1/2 fused step on the same buffers, for comparison", timed(zero), plan.numel,
-        bytes_per_padded_element(n_d, "fused") * P, 1)
-    launches += steps
+        bytes_per_padded_element(n_d, "fused") * P, walk_launches([(0, P)], n_d))
+    launches += steps * walk_launches([(0, P)], n_d)
     state_dp, state_zero = plan.memory_bytes(0), plan.memory_bytes(2)
     del grads, reps, master, mm, vv, z_master, z_m, z_v
 
@@ -910,8 +912,8 @@ def run_next(args, ws, rank, local):
         zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, hp, t[0], stream=stream)
 
     row("FSDP2 layout fused step, %s units, N_d=8" % unit_label, timed(f2), plan.numel,
-        bytes_per_padded_element(n_d, "fused") * P, 1, padding=P - plan.numel)
-    launches += steps
+        bytes_per_padded_element(n_d, "fused") * P, walk_launches([(0, P)], n_d), padding=P - plan.numel)
+    launches += steps * walk_launches([(0, P)], n_d)
     row("FSDP2 copy-out, group buffers -> one rank's parameters (k_fsdp2_copy)", timed(copy_out), plan.numel,
         2 * plan.numel * 2, layout_launches)
     launches += steps * layout_launches

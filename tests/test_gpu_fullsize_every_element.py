@@ -1,0 +1,161 @@
+"""Every-element oracle parity at the benchmarked sizes (GPU).
+
+The sampled full-size tests check chunks of the flat space; a race that hits
+one element in 10^5 would slip through them.  Here the benchmarked call runs
+once on the full workload, then the whole flat space is walked in chunks and
+every element of every output is compared with the oracle, bit for bit:
+
+* the Llama-1.3B ZeRO-2 step at N_d = 8 (1,345,423,360 elements), exactly
+  the call the benchmark times (zs_fused_step over the whole flat space, the
+  launches walked), at step 2 so the moments going in are not zero;
+* the whole Llama-7B ZeRO-3 step at N_d = 16 (zs_zero3_step, both streams,
+  the 2-slot pool), at step 2, on its largest unit (the root unit: embedding,
+  final norm and output, 262,148,096 elements) with the parameter shards.
+
+Every step is element-wise, so the oracle on a chunk needs only that chunk's
+inputs.  Chunks are checked by a pool of host threads (numpy releases the GIL
+in its array operations), each copying its chunk from the device, running
+the oracle's reduce-mean and AdamW on it and comparing.
+"""
+
+import concurrent.futures as cf
+import gc
+import os
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+import gpu_helpers as H
+import synth
+from oracle import steps
+
+pytestmark = pytest.mark.gpu
+
+HP = synth.HPARAMS
+DEV = "cuda"
+BF16 = torch.bfloat16
+CHUNK = 1 << 23
+THREADS = max(2, min(16, os.cpu_count() or 2))
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _bits16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _f32(t):
+    return t.detach().cpu().contiguous().numpy()
+
+
+def _first_diff(got, want):
+    bad = np.flatnonzero(got != want)
+    return None if bad.size == 0 else (int(bad.size), int(bad[0]))
+
+
+def _verify(n, job, label):
+    """Runs job(lo, hi) -> list of (name, count, first index) over [0, n) in chunks on a thread pool."""
+    t0 = time.perf_counter()
+    spans = [(lo, min(n, lo + CHUNK)) for lo in range(0, n, CHUNK)]
+    bad = []
+    with cf.ThreadPoolExecutor(THREADS) as ex:
+        for (lo, hi), res in zip(spans, ex.map(lambda s: job(*s), spans)):
+            bad += ["%s [%d,%d): %d values differ, first at %d" % (name, lo, hi, cnt, lo + first)
+                    for name, cnt, first in res]
+    print("%s: %d elements checked in %d chunks on %d threads, %.1f s"
+          % (label, n, len(spans), THREADS, time.perf_counter() - t0))
+    assert not bad, "\n".join(bad[:20])
+
+
+def test_llama13b_zero2_step_every_element():
+    wl = synth.WORKLOADS["llama-1.3b-zero2"]
+    shapes, _ = synth.workload_params(wl["model"])
+    n_d = wl["n_d"]
+    plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"])
+    P, pads = plan.padded, plan.pad_ranges()
+    assert plan.numel == 1_345_423_360
+    master = synth.master_init(P, pads, wl["seed"], device=DEV)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    reps, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    grads, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    synth.fill_grads(grads, pads, wl["seed"], 1, wl["sigma"], wl["outlier_p"])
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    synth.fill_grads(grads, pads, wl["seed"], 2, wl["sigma"], wl["outlier_p"])
+    torch.cuda.synchronize()
+    p0, m0, v0 = _f32(master), _f32(m), _f32(v)           # the state going into step 2
+    zs.zs_device_status(clear=True)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 2)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+
+    def job(lo, hi):
+        g = [_bits16(grads[q][lo:hi]) for q in range(n_d)]
+        ghat = steps.reduce_mean(g)
+        p, m1, v1, bits = steps.adamw(p0[lo:hi], m0[lo:hi], v0[lo:hi], ghat, HP, 2)
+        out = []
+        for name, dev_t, want in (("master", master, p), ("m", m, m1), ("v", v, v1)):
+            d = _first_diff(_f32(dev_t[lo:hi]).view(np.uint32), want.view(np.uint32))
+            if d:
+                out.append((name,) + d)
+        d = _first_diff(_bits16(reps[0][lo:hi]), bits)
+        if d:
+            out.append(("replica 0",) + d)
+        for q in range(1, n_d):
+            if not torch.equal(reps[q][lo:hi], reps[0][lo:hi]):
+                out.append(("replica %d vs replica 0" % q, -1, 0))
+        return out
+
+    _verify(P, job, "Llama-1.3B ZeRO-2 step, N_d=8")
+
+
+def test_llama7b_zero3_step_root_unit_every_element():
+    wl = synth.WORKLOADS["llama-7b-zero3"]
+    shapes, units = synth.workload_params(wl["model"])
+    n_d = wl["n_d"]
+    plan = zs.Plan(shapes, n_d, stage=3, unit_of_param=units)
+    P, pads = plan.padded, plan.pad_ranges()
+    sizes = [plan.unit(u)["padded"] for u in range(plan.n_units)]
+    root = int(np.argmax(sizes))
+    ud = plan.unit(root)
+    base, up = ud["base"], ud["padded"]
+    assert up == 262_148_096 and up == ud["numel"]                # no padding in this unit
+    master = synth.master_init(P, pads, wl["seed"], device=DEV)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    shards = master.to(BF16)
+    biggest = max(sizes)
+    ugrads, _ = synth.rank_buffers(n_d, biggest, BF16, DEV)
+    synth.fill_grads(ugrads, [], wl["seed"], 1, wl["sigma"])
+    pool = [synth.rank_buffers(n_d, biggest, BF16, DEV)[0] for _ in range(2)]
+    side = torch.cuda.Stream()
+    zs.zs_zero3_step(plan, shards, master, m, v, [ugrads] * plan.n_units, pool, True, HP, 1, side_stream=side)
+    synth.fill_grads(ugrads, [], wl["seed"], 2, wl["sigma"])
+    torch.cuda.synchronize()
+    p0, m0, v0 = (_f32(x[base:base + up]) for x in (master, m, v))
+    zs.zs_device_status(clear=True)
+    zs.zs_zero3_step(plan, shards, master, m, v, [ugrads] * plan.n_units, pool, True, HP, 2, side_stream=side)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+
+    def job(lo, hi):
+        g = [_bits16(ugrads[q][lo:hi]) for q in range(n_d)]
+        ghat = steps.reduce_mean(g)
+        p, m1, v1, bits = steps.adamw(p0[lo:hi], m0[lo:hi], v0[lo:hi], ghat, HP, 2)
+        out = []
+        for name, dev_t, want in (("master", master, p), ("m", m, m1), ("v", v, v1)):
+            d = _first_diff(_f32(dev_t[base + lo:base + hi]).view(np.uint32), want.view(np.uint32))
+            if d:
+                out.append((name,) + d)
+        d = _first_diff(_bits16(shards[base + lo:base + hi]), bits)
+        if d:
+            out.append(("shards",) + d)
+        return out
+
+    _verify(up, job, "Llama-7B ZeRO-3 step, N_d=16, root unit")

@@ -1,16 +1,19 @@
-"""zs_zero2_step_host_noalloc against zs_zero2_step_host (GPU).
+"""zs_zero2_step_host_noalloc against the oracle and against zs_zero2_step_host (GPU).
 
 The no-allocation entry point serves callers that cannot allocate device
 memory when they step the optimizer; it stages gradients in a fixed array
 inside the library instead of a caller-provided ring.  Its results must equal
-the staged entry point's on two calls in a row (the second call reuses the
-array the first one left behind).  This file is collected last so that a run
+the oracle's step (reduce-mean over ranks, then AdamW, on the whole flat
+space) and the staged entry point's, bit for bit, on two calls in a row (the
+second call reuses the array the first one left behind), with the device
+status word clear after each pair.  This file is collected last so that a run
 stopping at the first failure has already run every other test; it also
 passes on its own in a fresh process.
 """
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
@@ -33,11 +36,14 @@ def _run_pair(plan, steps=(1, 2)):
     reps_b = synth.rank_buffers(n_d, P, torch.bfloat16, DEV)[0]
     biggest = max(hi - lo for _, lo, hi in (plan.bucket(k) for k in range(plan.n_buckets)))
     staging = [synth.rank_buffers(n_d, biggest, torch.bfloat16, DEV)[0] for _ in range(2)]
+    # the oracle's state, stepped beside the device (every step is element-wise over the flat space)
+    o_p, o_m, o_v = H.to_np_f32(master0), np.zeros(P, np.float32), np.zeros(P, np.float32)
     for t in steps:
         grads, _ = synth.rank_grads(n_d, P, pads, seed=32, step=t, sigma=1e-3, outlier_p=0.001, device=DEV)
         host = [g.cpu().pin_memory() for g in grads]
         out_a = torch.empty(P, dtype=torch.bfloat16).pin_memory()
         out_b = torch.empty(P, dtype=torch.bfloat16).pin_memory()
+        zs.zs_device_status(clear=True)
         zs.zs_zero2_step_host(plan, host, staging, *a, reps_a, HP, t, host_replica0=out_a)
         # through the C ABI directly: plain pointers, nothing allocated by the call
         lib = ctypes.CDLL(zs.LIB_PATH)
@@ -50,6 +56,13 @@ def _run_pair(plan, steps=(1, 2)):
                 ctypes.c_void_p(out_b.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert rc == zs.ZS_OK, zs.zs_last_error()
         torch.cuda.synchronize()
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+        _, o_p, o_m, o_v, o_bits = H.chunk_oracle([H.to_np_bf16(g) for g in host], o_p, o_m, o_v, HP, t)
+        for y, want, name in zip(b, (o_p, o_m, o_v), ("master", "m", "v")):
+            H.check_f32(H.to_np_f32(y), want, "no-alloc %s vs oracle t=%d" % (name, t))
+        for q in range(n_d):
+            H.check_bf16(H.to_np_bf16(reps_b[q]), o_bits, "no-alloc replica %d vs oracle t=%d" % (q, t))
+        H.check_bf16(H.to_np_bf16(out_b), o_bits, "no-alloc host replica vs oracle t=%d" % t)
         for x, y, name in zip(a, b, ("master", "m", "v")):
             H.check_f32(H.to_np_f32(y), H.to_np_f32(x), "%s t=%d" % (name, t))
         for q in range(n_d):
