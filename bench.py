@@ -221,12 +221,12 @@ WALK_SHAPE_ND = (2, 4, 8, 16, 32)  # rank counts with a walk shape (fused_walk_s
 STAGED_ND = (2, 4, 8, 16, 32)
 
 
-def walk_pieces(ranges, n_d):
+def walk_pieces(ranges, n_d, staged_ok=True):
     out, C = [], WALK_CHUNK
     for lo, hi in ranges:
         while lo < hi:
             end = hi
-            if n_d in WALK_SHAPE_ND:
+            if n_d in WALK_SHAPE_ND and staged_ok:
                 cut = (lo + C // 4 + C) // C * C
                 if cut < hi - C // 4:
                     end = cut
@@ -237,7 +237,7 @@ def walk_pieces(ranges, n_d):
 
 def walk_launches(ranges, n_d, staged_ok=True):
     n = 0
-    for lo, hi in walk_pieces(ranges, n_d):
+    for lo, hi in walk_pieces(ranges, n_d, staged_ok):
         vlo, vhi = (lo + 7) // 8 * 8, hi // 8 * 8
         if staged_ok and n_d in STAGED_ND and vhi - vlo >= WALK_MIN_STAGED:
             n += 1 + (vlo > lo) + (hi > vhi)
@@ -495,7 +495,7 @@ class Workload:
 
     def kernel_label(self):
         fused = ("k_fused_tma<%d>" if self.staged() else "k_fused<%d>") % self.n_d
-        pieces = len(walk_pieces([(0, self.P)], self.n_d))
+        pieces = len(walk_pieces([(0, self.P)], self.n_d, self.staged()))
         if pieces > 1:
             fused += " walked in %d overlapping launches" % pieces
         if self.kind == "fused":

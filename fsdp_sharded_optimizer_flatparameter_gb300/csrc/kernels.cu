@@ -502,8 +502,13 @@ cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v,
                               const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
                               StagedPolicy staged_policy) {
     // Cut points are multiples of the chunk (8-aligned, so a range's pieces keep its own fringes
-    // only), none closer than a quarter chunk to a range end, so no piece is a sliver.
-    const bool chunked = fused_walk_shape(nd);
+    // only), none closer than a quarter chunk to a range end, so no piece is a sliver.  Only staged
+    // launches overlap: buffers the staged kernel may not touch (pinned host memory) or the streaming
+    // variant leave every range whole.
+    if (staged_policy == kStagedIfDevice)
+        staged_policy = fused_ptrs_on_device(g, master, m, v, out, true, nd) ? kStagedDeviceKnown : kStagedNever;
+    const bool chunked = fused_walk_shape(nd) && staged_policy != kStagedNever &&
+                         g_fused_variant.load() != ZS_FUSED_LDG;
     constexpr int64_t C = kFusedWalkChunk;
     bool first = true;
     for (const Range& r : ranges) {
