@@ -442,8 +442,9 @@ class Workload:
         wl = self.wl = dict(synth.WORKLOADS[args.workload])
         shapes, units = synth.workload_params(wl["model"])
         if args.profile_case:
-            # the same kernel on a smaller flat buffer (32 Mi elements, 1.9 GB at N_d = 8): for ncu captures
-            shapes, units = [(32 << 20,)], None
+            # the same kernels on a smaller flat buffer (by default 32 Mi elements, 1.9 GB at N_d = 8): for
+            # ncu captures
+            shapes, units = [(args.profile_elems,)], None
         self.n_d = n_d = wl["n_d"]
         self.plan = plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"],
                                    unit_of_param=units)
@@ -1285,6 +1286,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-1.3b-zero2")
     ap.add_argument("--profile-case", action="store_true")
+    ap.add_argument("--profile-elems", type=int, default=32 << 20,
+                    help="elements of the --profile-case flat buffer")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused-steps", type=int, default=10)
