@@ -107,7 +107,8 @@ def source_digest(kernel_key):
 
 
 def profiled_traffic(workload, kernel_key):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the current sources."""
+    """DRAM bytes per step from the committed ncu summary (every launch of a step, steady state), if it
+    was taken on the current sources."""
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel_key, workload))
     try:
         fields = {}
@@ -118,7 +119,7 @@ def profiled_traffic(workload, kernel_key):
                     fields[k.strip()] = v.strip().strip("`")
         if fields.get("source_digest") != source_digest(kernel_key):
             return None
-        return float(fields["traffic_bytes_per_full_launch"])
+        return float(fields["traffic_bytes_per_step"])
     except Exception:
         return None
 
@@ -1178,6 +1179,8 @@ def run_ours(args, ws, rank, local):
             "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                         "traffic_unit": "bytes per step (every launch of a step, ncu, steady state)",
+                         "traffic_vs_algorithmic": (traffic / algo_bytes) if traffic else None,
                          "algorithmic_bytes_per_launch": algo_bytes if launches == 1 else None,
                          "algorithmic_bytes_per_step": algo_bytes, "kernel": W.kernel_label(),
                          "launches_per_step": launches, "kernel_ms": step_ms,
