@@ -497,7 +497,7 @@ class Workload:
 
     def kernel_label(self):
         fused = ("k_fused_tma<%d>" if self.staged() else "k_fused<%d>") % self.n_d
-        pieces = len(walk_pieces([(0, self.P)], self.n_d, self.staged()))
+        pieces = len(walk_pieces([(0, self.P)], self.n_d, self.staged())) if self.kind != "zero3" else 1
         if pieces > 1:
             fused += " walked in %d overlapping launches" % pieces
         if self.kind == "fused":
