@@ -86,6 +86,8 @@ _sig("zs_fused_step_host", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
 _sig("zs_zero3_gather_unit", [c_vp, c_i32, c_vp, c_vp, c_vp])
 _sig("zs_zero3_rs_step_unit", [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
+_sig("zs_rank_shard_step", [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                            ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
 _sig("zs_zero3_step", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                        ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp])
 _sig("zs_zero2_step_host", [c_vp, c_vp, c_vp, c_i64, c_vp, c_vp, c_vp, c_vp,
@@ -113,6 +115,7 @@ EXPORTED = [
     "zs_checkpoint_save", "zs_checkpoint_load", "zs_zero2_step_host_noalloc", "zs_all_reduce_mean",
     "zs_dp_step", "zs_plan_create_fsdp2", "zs_plan_layout", "zs_plan_param_rows", "zs_plan_pad_ranges",
     "zs_fsdp2_chunk_cat", "zs_fsdp2_copy_out", "zs_fused_step_buckets", "zs_set_dependent_launch",
+    "zs_rank_shard_step",
 ]
 
 
@@ -203,6 +206,19 @@ class Plan:
         lo, hi = c_i64(), c_i64()
         _check(_lib.zs_plan_bucket_rank_slice(self._h, int(b), int(rank), ctypes.byref(lo), ctypes.byref(hi)))
         return lo.value, hi.value
+
+    def unit_local_offset(self, u):
+        """Offset of unit u's shard in a rank's local layout (the units' shards back to back)."""
+        return sum(self.unit(k)["shard"] for k in range(int(u)))
+
+    def rank_bucket_part(self, rank, b):
+        """Rank `rank`'s part of bucket b: (global begin, end, offset in the rank's local layout)."""
+        lo, hi = self.bucket_rank_slice(b, rank)
+        u = self.bucket(b)[0]
+        ud = self.unit(u)
+        s_lo = ud["base"] + int(rank) * ud["shard"]
+        local = self.unit_local_offset(u) + (lo - s_lo) if hi > lo else self.unit_local_offset(u)
+        return lo, hi, local
 
     def param(self, k):
         u, off, n = c_i32(), c_i64(), c_i64()
@@ -416,6 +432,24 @@ def zs_zero3_rs_step_unit(plan, unit, grads, master, m, v, shards, hp, step, str
         plan.handle, int(unit), _ptr_array(grads, nu, 2, "grads"),
         _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
         _addr(shards, n, 2, "shards"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+def zs_rank_shard_step(plan, rank, bucket, slices, master, m, v, param_shard, hp, step, stream=None):
+    """Rank `rank`'s local part of the step when every rank is its own process and GPU: slices are the
+    N_d received gradient slices of its part of `bucket` (-1: of its whole shard); master, m, v and
+    param_shard are the rank's own shard arrays in its local layout."""
+    if bucket >= 0:
+        lo, hi, _ = plan.rank_bucket_part(rank, bucket)
+        n = hi - lo
+    else:
+        n = plan.shard_per_rank
+    if len(slices) != plan.n_d:
+        raise ValueError("slices must hold N_d = %d entries" % plan.n_d)
+    ns = plan.shard_per_rank
+    return _check(_lib.zs_rank_shard_step(
+        plan.handle, int(rank), int(bucket), _ptr_array(slices, n, 2, "slices"),
+        _addr(master, ns, 4, "master"), _addr(m, ns, 4, "m"), _addr(v, ns, 4, "v"),
+        _addr(param_shard, ns, 2, "param_shard"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
 
 
 def zs_zero3_step(plan, shards, master, m, v, unit_grads, pool, reshard_after_forward, hp, step,

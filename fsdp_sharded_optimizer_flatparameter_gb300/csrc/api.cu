@@ -337,6 +337,94 @@ extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const in
     return cuda_status(fn, err);
 }
 
+extern "C" int zs_rank_shard_step(zs_plan_t plan, int32_t rank, int32_t bucket, const void* const* slices,
+                                  float* master, float* m, float* v, void* param_shard,
+                                  const zs_adamw_hparams* hp, int64_t step, void* stream) {
+    static const char* fn = "zs_rank_shard_step";
+    zs::TraceRange trace_(fn);
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    const int nd = plan->n_d;
+    if (rank < 0 || rank >= nd) return fail(fn, "rank out of range");
+    ZS_TRY(check_bucket(fn, plan, bucket, true));
+    ZS_TRY(check_ptrs(fn, "slices", slices, nd));
+    ZS_TRY(check_one(fn, "master", master));
+    ZS_TRY(check_one(fn, "m", m));
+    ZS_TRY(check_one(fn, "v", v));
+    ZS_TRY(check_one(fn, "param_shard", param_shard));
+    zs::AdamScalars s;
+    ZS_TRY(check_hp(fn, hp, step, &s));
+    // the pieces of rank r's part: global [lo, hi), offset in the rank's local layout, offset in the slices
+    struct Piece {
+        int64_t lo, hi, local, in_slice;
+    };
+    std::vector<Piece> pieces;
+    std::vector<int64_t> local_of_unit(plan->units.size());
+    int64_t acc = 0;
+    for (size_t u = 0; u < plan->units.size(); ++u) {
+        local_of_unit[u] = acc;
+        acc += plan->units[u].shard;
+    }
+    auto own = [&](size_t u, int64_t lo, int64_t hi, int64_t in_slice) {
+        const auto& un = plan->units[u];
+        const int64_t s_lo = un.base + (int64_t)rank * un.shard;
+        const int64_t a = lo > s_lo ? lo : s_lo, b = hi < s_lo + un.shard ? hi : s_lo + un.shard;
+        if (b > a) pieces.push_back({a, b, local_of_unit[u] + (a - s_lo), in_slice});
+        return b > a ? b - a : 0;
+    };
+    if (bucket >= 0) {
+        const auto& bk = plan->buckets[bucket];
+        own(bk.unit, bk.begin, bk.end, 0);
+    } else {
+        int64_t off = 0;
+        for (size_t u = 0; u < plan->units.size(); ++u) off += own(u, plan->units[u].base,
+                                                                   plan->units[u].base + plan->units[u].padded, off);
+    }
+    if (pieces.empty()) return ZS_OK;
+    cudaStream_t st = as_stream(stream);
+    // the kernels address element i of the state as base + i: hand them bases shifted so that global
+    // index lo lands on the piece's local offset (integer arithmetic; only in-range addresses are formed)
+    auto shift = [](void* p, int64_t elems, size_t esize) {
+        return (void*)((uintptr_t)p + (uintptr_t)(elems * (int64_t)esize));
+    };
+    BView g, o;
+    {
+        const void* sp[1] = {param_shard};
+        ZS_TRY(make_view(fn, "param_shard", sp, ZS_SHARDED, nd, 0, 0, &o));
+    }
+    // ask the runtime once whether every buffer is device memory (the staged kernel's bulk copies are
+    // pointed at device memory only)
+    const void* real[ZS_MAX_RANKS + 4];
+    int nreal = 0;
+    for (int q = 0; q < nd; ++q) real[nreal++] = slices[q];
+    real[nreal++] = master;
+    real[nreal++] = m;
+    real[nreal++] = v;
+    real[nreal++] = param_shard;
+    bool on_device = true;
+    for (int k = 0; k < nreal && on_device; ++k) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, real[k]) != cudaSuccess) {
+            cudaGetLastError();
+            on_device = false;
+        } else if (at.type != cudaMemoryTypeDevice) {
+            on_device = false;
+        }
+    }
+    const zs::StagedPolicy pol = on_device ? zs::kStagedDeviceKnown : zs::kStagedNever;
+    for (const Piece& pc : pieces) {
+        for (int q = 0; q < ZS_MAX_RANKS; ++q)
+            g.ptr.p[q] = q < nd ? (uint16_t*)slices[q] + pc.in_slice : nullptr;
+        g.off = pc.lo;
+        o.off = pc.lo - pc.local;
+        const int64_t d = pc.local - pc.lo;
+        ZS_TRY(cuda_status(fn, zs::launch_fused(g, (float*)shift(master, d, 4), (float*)shift(m, d, 4),
+                                                (float*)shift(v, d, 4), o, false, {pc.lo, pc.hi, 0, 1}, s, nd, st,
+                                                pol)));
+    }
+    return ZS_OK;
+}
+
 extern "C" int zs_fused_step_host(zs_plan_t plan, const void* const* host_grads, void* const* dev_grads,
                                   float* master, float* m, float* v, void* const* replicas,
                                   const zs_adamw_hparams* hp, int64_t step, void* host_replica0, void* stream) {

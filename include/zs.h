@@ -341,6 +341,10 @@ int zs_dp_step(zs_plan_t plan, const void* const* grads, float* const* master, f
  *   bucket      -1 = the whole flat space, else one bucket (the update is
  *               element-wise, so a bucket can be stepped as soon as its
  *               gradients are complete).
+ * The range is stepped as a walk: cut at multiples of 4 Mi elements, one
+ * launch per piece; the launches after the first start on their own pieces
+ * while the previous one drains and complete after it, so stream order holds
+ * at the call's end (pinned host buffers: one launch, nothing cut).
  *   grads_kind  ZS_RANK_FULL, or ZS_RANK_BUCKET (bucket >= 0; ZeRO-2 staging).
  *   replicas    ZS_RANK_FULL; must not overlap grads. */
 int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
@@ -352,23 +356,25 @@ int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int3
  * first.  Same results as calling zs_fused_step once per bucket, with the
  * argument checks, the pointer-kind queries and the per-call overhead paid
  * once.  The update is element-wise and the buckets are disjoint, so the
- * launches need no order among themselves.
+ * launches need no order among themselves: the list is walked as in
+ * zs_fused_step (pieces of at most ~4 Mi elements, each launch starting while
+ * the previous one drains; the first waits for everything enqueued before the
+ * call, and the call's work completes in stream order).
  *   launch_mode  ZS_BUCKETS_ONE_WALK: listed buckets that touch are merged
- *                into one range (a run of neighbours, in either order); a
- *                merged range of at least 2^25 elements gets a launch of the
- *                single-range staged kernel of its own, and all the others
- *                are walked by one persistent launch (per 128 ranges), each
- *                CTA taking its tiles in list order, so a small bucket costs
- *                no launch of its own; where only the streaming kernel
- *                applies (host buffers, other rank counts, a total below
- *                2^20 elements) one launch per range on `stream`.
- *                ZS_BUCKETS_PER_BUCKET: one launch per bucket; with a
- *                side_stream other than stream, the buckets at odd positions
- *                run on side_stream (which first waits for all work enqueued
- *                on stream) and each launch overlaps the end of the previous
- *                one; before returning, stream is made to wait for
- *                side_stream.  This mode creates and releases two CUDA events
- *                (no device memory).
+ *                into one range (a run of neighbours, in either order) before
+ *                the walk; disjoint runs shorter than 2^16 elements share
+ *                persistent launches of a list kernel (128 runs per launch)
+ *                instead of a launch each; where only the streaming kernel
+ *                applies (host buffers, other rank counts) one launch per
+ *                range.
+ *                ZS_BUCKETS_PER_BUCKET: the buckets are walked one after
+ *                another in the order given, no launch spanning two buckets,
+ *                as when each is stepped as soon as backward has made it
+ *                ready; with a side_stream other than stream, the buckets at
+ *                odd positions are walked on side_stream (which first waits
+ *                for all work enqueued on stream); before returning, stream
+ *                is made to wait for side_stream.  The two-stream form creates
+ *                and releases two CUDA events (no device memory).
  *   side_stream  used by ZS_BUCKETS_PER_BUCKET only; NULL or equal to stream:
  *                one stream.
  * Errors: ZS_ERR_INVALID (bad or repeated bucket index, unknown launch_mode,
@@ -379,6 +385,41 @@ int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buck
                           const void* const* grads, float* master, float* m, float* v,
                           void* const* replicas, const zs_adamw_hparams* hp, int64_t step,
                           int32_t launch_mode, void* stream, void* side_stream);
+
+/* One rank's local share of the ZeRO-1/2 step when every data-parallel rank is
+ * its own process on its own GPU ("Infra: Data Parallel", ZeRO section,
+ * communication paragraphs and ZeRO-1/2 flow figures: the reduce-scatter hands
+ * rank r every rank's gradients for the part of the bucket it owns, rank r
+ * averages them and updates its own shard of the optimizer state, and the
+ * all-gather then spreads the updated shards).  The exchanges are the caller's
+ * collectives (an all-to-all of each bucket before this call, an all-gather of
+ * the parameter shards after it); this call is the part between them: over
+ * rank r's part of `bucket`, fold the N_d received gradient slices in
+ * ascending rank order from +0, average, round to bf16, run AdamW on the
+ * rank's own fp32 state and write the rank's bf16 parameter shard.  Results
+ * equal rank r's shard of zs_fused_step bit for bit.
+ *   rank         0 .. N_d-1, the calling rank.
+ *   bucket       a bucket index, or -1 for the rank's whole shard (every unit).
+ *   slices       N_d device pointers (16-byte aligned); slices[q] holds rank
+ *                q's bf16 gradients for the elements rank r owns in the bucket,
+ *                contiguous, in flat-index order: the receive buffer of an
+ *                all-to-all in which every rank sends its bucket
+ *                [begin, end), split by owner (zs_plan_bucket_rank_slice gives
+ *                each owner's part).  For bucket -1: rank r's pieces of every
+ *                unit back to back, in unit order.
+ *   master, m, v rank r's own fp32 state, in its local layout: its shard of
+ *                every unit, units in order (shard_numel_per_rank elements);
+ *                the bucket's part starts at the unit's offset in that layout
+ *                (sum of the earlier units' shard sizes) plus the part's offset
+ *                in the rank's shard of the unit.
+ *   param_shard  rank r's bf16 parameters in the same local layout (written).
+ * Runs on `stream` (the staged kernel when the local offsets keep 16-byte
+ * alignment, else the streaming kernel; the values are the same).
+ * Errors: ZS_ERR_INVALID (bad plan, rank or bucket, a NULL or misaligned
+ * pointer, bad hyper-parameters or step; nothing enqueued), ZS_ERR_CUDA. */
+int zs_rank_shard_step(zs_plan_t plan, int32_t rank, int32_t bucket, const void* const* slices,
+                       float* master, float* m, float* v, void* param_shard,
+                       const zs_adamw_hparams* hp, int64_t step, void* stream);
 
 /* zs_fused_step over the whole flat space with the gradients in HOST memory
  * (pinned for overlap): enqueues one host-to-device copy per rank into

@@ -1,0 +1,101 @@
+"""zs_rank_shard_step against the oracle (GPU): the local part of a rank's step when every rank is its
+own process.
+
+The ranks are simulated in one process (no rank waits on another): for each rank r the slices an
+all-to-all would deliver are cut from every rank's gradient buffer with torch, and the call updates
+rank r's own shard state (local layout) from them.  The results must equal the oracle's simulated
+step (steps.zero_step) bit for bit, bucket by bucket and for the whole shard at once, on plans whose
+local offsets keep 16-byte alignment (the staged kernel for parts of 2^20 elements and more) and on
+plans whose offsets do not (the streaming kernel element by element).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+import gpu_helpers as H
+import synth
+from oracle import layout, steps
+
+pytestmark = pytest.mark.gpu
+
+HP = synth.HPARAMS
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+CASES = {
+    # S = 2 Mi elements per rank: most bucket parts take the staged kernel
+    "aligned-n8": dict(shapes=[(1 << 24,)], units=None, n_d=8, bucket_bytes=25 << 20),
+    # ragged: 1,000,003 elements padded to N_d = 8, 128 Ki-element buckets
+    "ragged-n8": dict(shapes=[(1_000_003,)], units=None, n_d=8, bucket_bytes=1 << 18),
+    # several units, N_d = 3: odd local offsets, element by element
+    "units-n3": dict(shapes=[(64, 48), (48,), (100, 30), (30,), (7, 5)], units=[0, 0, 1, 1, 2], n_d=3,
+                     bucket_bytes=2_000),
+}
+
+
+def _part_slices(grads, lo, hi):
+    """What an all-to-all delivers to the owner of [lo, hi): every rank's gradients there."""
+    return [g[lo:hi].contiguous() for g in grads]
+
+
+@pytest.mark.parametrize("whole", [False, True])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_rank_shard_step_matches_the_oracle(case, whole):
+    cfg = CASES[case]
+    n_d = cfg["n_d"]
+    plan = zs.Plan(cfg["shapes"], n_d, stage=2, bucket_bytes=cfg["bucket_bytes"], unit_of_param=cfg["units"])
+    oplan = layout.make_plan(cfg["shapes"], n_d, unit_of_param=cfg["units"], bucket_bytes=cfg["bucket_bytes"])
+    P, pads, S = plan.padded, plan.pad_ranges(), plan.shard_per_rank
+    master_full = synth.master_init(P, pads, seed=51, device=DEV)
+    mf = H.to_np_f32(master_full)
+    state = [[torch.from_numpy(steps.shard_of(oplan, r, mf).copy()).to(DEV), torch.zeros(S, device=DEV),
+              torch.zeros(S, device=DEV)] for r in range(n_d)]
+    shards = [torch.zeros(S, dtype=BF16, device=DEV) for _ in range(n_d)]
+    o_m = [steps.shard_of(oplan, r, mf) for r in range(n_d)]
+    o_mm = [np.zeros(S, np.float32) for _ in range(n_d)]
+    o_v = [np.zeros(S, np.float32) for _ in range(n_d)]
+    zs.zs_device_status(clear=True)
+    for t in (1, 2):
+        grads, _ = synth.rank_grads(n_d, P, pads, seed=52, step=t, sigma=1e-3, outlier_p=0.001, device=DEV)
+        for r in range(n_d):
+            if whole:
+                # the rank's pieces of every unit, back to back in unit order
+                pieces = []
+                for u in range(plan.n_units):
+                    ud = plan.unit(u)
+                    lo = ud["base"] + r * ud["shard"]
+                    pieces.append(_part_slices(grads, lo, lo + ud["shard"]))
+                slices = [torch.cat([p[q] for p in pieces]) for q in range(n_d)]
+                zs.zs_rank_shard_step(plan, r, -1, slices, *state[r], shards[r], HP, t)
+            else:
+                for b in reversed(range(plan.n_buckets)):
+                    lo, hi, _ = plan.rank_bucket_part(r, b)
+                    if hi > lo:
+                        zs.zs_rank_shard_step(plan, r, b, _part_slices(grads, lo, hi), *state[r], shards[r], HP, t)
+        torch.cuda.synchronize()
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+        reps, o_m, o_mm, o_v = steps.zero_step(oplan, [H.to_np_bf16(g) for g in grads], o_m, o_mm, o_v, HP, t)
+        for r in range(n_d):
+            what = "%s rank %d t=%d" % (case, r, t)
+            H.check_f32(H.to_np_f32(state[r][0]), o_m[r], "master " + what)
+            H.check_f32(H.to_np_f32(state[r][1]), o_mm[r], "m " + what)
+            H.check_f32(H.to_np_f32(state[r][2]), o_v[r], "v " + what)
+            H.check_bf16(H.to_np_bf16(shards[r]), steps.shard_of(oplan, r, reps[r]), "shard " + what)
+
+
+def test_rank_shard_step_rejects_bad_arguments():
+    plan = zs.Plan([(1 << 12,)], 4, stage=2, bucket_bytes=1 << 10)
+    S = plan.shard_per_rank
+    st = [torch.zeros(S, device=DEV) for _ in range(3)]
+    sh = torch.zeros(S, dtype=BF16, device=DEV)
+    lo, hi, _ = plan.rank_bucket_part(0, 0)
+    sl = [torch.zeros(max(1, hi - lo), dtype=BF16, device=DEV) for _ in range(4)]
+    for rank, bucket in ((4, 0), (-1, 0), (0, plan.n_buckets)):
+        with pytest.raises(zs.ZsError):
+            zs.zs_rank_shard_step(plan, rank, bucket, sl, *st, sh, HP, 1)
+    with pytest.raises(zs.ZsError):
+        zs.zs_rank_shard_step(plan, 0, 0, sl, *st, sh, HP, 0)             # 0-based step
+    with pytest.raises(ValueError):
+        zs.zs_rank_shard_step(plan, 0, 0, sl[:3], *st, sh, HP, 1)         # a missing rank
