@@ -67,7 +67,15 @@ class ZeroRank:
         recv = torch.empty(self.n_d * mine, dtype=grads.dtype, device=grads.device)
         dist.all_to_all_single(recv, send, [mine] * self.n_d, lens, group=self.group)
         self.bytes_sent += 2 * (sum(lens) - lens[self.rank])
-        return [recv[q * mine:(q + 1) * mine] for q in range(self.n_d)]
+        if mine % 8 == 0:
+            return [recv[q * mine:(q + 1) * mine] for q in range(self.n_d)]
+        # the library takes 16-byte-aligned slices: a part that is not a multiple of 8 elements is laid
+        # out again in rows of a multiple of 8 (one copy of the part; plans whose bucket parts are
+        # multiples of 8 elements never take this path)
+        stride = (mine + 7) // 8 * 8
+        rows = torch.empty((self.n_d, stride), dtype=grads.dtype, device=grads.device)
+        rows[:, :mine].copy_(recv.view(self.n_d, mine))
+        return [rows[q, :mine] for q in range(self.n_d)]
 
     def reduce_scatter_update(self, bucket, grads, master, m, v, param_shard, hp, step, grads_base=0):
         """Exchange one bucket, then average and apply AdamW to this rank's part of it."""

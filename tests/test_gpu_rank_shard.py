@@ -36,8 +36,9 @@ CASES = {
 
 
 def _part_slices(grads, lo, hi):
-    """What an all-to-all delivers to the owner of [lo, hi): every rank's gradients there."""
-    return [g[lo:hi].contiguous() for g in grads]
+    """What an all-to-all delivers to the owner of [lo, hi): every rank's gradients there, each in a
+    buffer of its own (16-byte aligned, as the call requires)."""
+    return [g[lo:hi].clone() for g in grads]
 
 
 @pytest.mark.parametrize("whole", [False, True])
@@ -99,3 +100,40 @@ def test_rank_shard_step_rejects_bad_arguments():
         zs.zs_rank_shard_step(plan, 0, 0, sl, *st, sh, HP, 0)             # 0-based step
     with pytest.raises(ValueError):
         zs.zs_rank_shard_step(plan, 0, 0, sl[:3], *st, sh, HP, 1)         # a missing rank
+
+
+def test_zero_rank_over_nccl_with_one_rank():
+    """ZeroRank end to end on the GPU: an NCCL group of one process (the all-to-all, the all-gather
+    and the library's local update on device buffers), two ZeRO-2 steps against the oracle."""
+    import socket
+
+    import torch.distributed as dist
+
+    from fsdp_sharded_optimizer_flatparameter_gb300.zero_rank import ZeroRank
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0, world_size=1)
+    try:
+        shapes = [(300, 96), (96,), (257, 96)]
+        plan = zs.Plan(shapes, 1, stage=2, bucket_bytes=10_000)
+        oplan = layout.make_plan(shapes, 1, bucket_bytes=10_000)
+        P, pads = plan.padded, plan.pad_ranges()
+        master0 = synth.master_init(P, pads, seed=53, device=DEV)
+        master, m, v = master0.clone(), torch.zeros_like(master0), torch.zeros_like(master0)
+        shard = torch.zeros(P, dtype=BF16, device=DEV)
+        replica = torch.zeros(P, dtype=BF16, device=DEV)
+        zr = ZeroRank(plan)
+        o = [[H.to_np_f32(master0)], [np.zeros(P, np.float32)], [np.zeros(P, np.float32)]]
+        for t in (1, 2):
+            grads, _ = synth.rank_grads(1, P, pads, seed=54, step=t, sigma=1e-3, device=DEV)
+            zr.step(grads[0], master, m, v, shard, replica, HP, t)
+            torch.cuda.synchronize()
+            reps, o[0], o[1], o[2] = steps.zero_step(oplan, [H.to_np_bf16(grads[0])], o[0], o[1], o[2], HP, t)
+            H.check_f32(H.to_np_f32(master), o[0][0], "master t=%d" % t)
+            H.check_f32(H.to_np_f32(v), o[2][0], "v t=%d" % t)
+            H.check_bf16(H.to_np_bf16(replica), reps[0], "replica t=%d" % t)
+        assert zr.bytes_sent == 0                     # one rank sends nothing
+    finally:
+        dist.destroy_process_group()
