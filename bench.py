@@ -447,8 +447,11 @@ class Workload:
             # ncu captures
             shapes, units = [(args.profile_elems,)], None
         self.n_d = n_d = wl["n_d"]
+        if args.bucket_bytes is not None:
+            wl["bucket_bytes"] = args.bucket_bytes
         self.plan = plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"],
                                    unit_of_param=units)
+        self.order = list(reversed(range(plan.n_buckets)))     # bucket-wise modes: last bucket first
         P, pads = plan.padded, plan.pad_ranges()
         self.P, self.pads = P, pads
         self.hp = synth.HPARAMS
@@ -471,6 +474,7 @@ class Workload:
             self.grads, self._gb = synth.rank_buffers(n_d, P, bf16, dev)
             synth.fill_grads(self.grads, pads, wl["seed"], 1, wl["sigma"], wl["outlier_p"])
             self.reps, self._rb = synth.rank_buffers(n_d, P, bf16, dev)
+            self.side = torch.cuda.Stream(dev) if args.step_mode == "per-bucket-2s" else None
             self.resident = 12 * P + 2 * 2 * n_d * P
             if self.kind == "accumulate+fused":
                 self.acc, self._ab = synth.rank_buffers(n_d, P, bf16, dev)
@@ -480,6 +484,12 @@ class Workload:
     def step_bytes(self):
         n_d, P = self.n_d, self.P
         walk = walk_launches([(0, P)], n_d, self.staged())
+        if self.kind == "fused" and self.args.step_mode != "whole":
+            br = [self.plan.bucket(b)[1:] for b in self.order]
+            if self.args.step_mode == "per-bucket-2s":
+                walk = walk_launches(br[0::2], n_d, self.staged()) + walk_launches(br[1::2], n_d, self.staged())
+            else:
+                walk = walk_launches(br, n_d, self.staged())
         if self.kind == "fused":
             return bytes_per_padded_element(n_d, "fused") * P, walk
         if self.kind == "accumulate+fused":
@@ -510,7 +520,12 @@ class Workload:
         zs, plan, hp = self.zs, self.plan, self.hp
         self.t += 1
         t, st = self.t, self.stream
-        if self.kind == "fused":
+        if self.kind == "fused" and self.args.step_mode != "whole":
+            # the step as backward makes buckets ready: every bucket, last first, bucket by bucket
+            zs.zs_fused_step_buckets(plan, self.order, self.grads, self.master, self.m, self.v, self.reps, hp, t,
+                                     launch_mode=zs.ZS_BUCKETS_PER_BUCKET, stream=st,
+                                     side_stream=self.side if self.args.step_mode == "per-bucket-2s" else None)
+        elif self.kind == "fused":
             zs.zs_fused_step(plan, -1, self.grads, zs.ZS_RANK_FULL, self.master, self.m, self.v, self.reps, hp, t,
                              stream=st)
         elif self.kind == "accumulate+fused":
@@ -1171,7 +1186,7 @@ def run_ours(args, ws, rank, local):
             "config": {"workload": args.workload + ("-profile-case" if args.profile_case else ""),
                        "fused_variant": args.fused_variant, "model_shape": W.wl["model"], "params": plan.numel,
                        "padded": P, "n_d": n_d, "stage": "zero%d" % W.wl["stage"],
-                       "bucket_bytes": W.wl["bucket_bytes"], "step": W.kind,
+                       "bucket_bytes": W.wl["bucket_bytes"], "step": W.kind, "step_mode": args.step_mode,
                        "storage": "bf16 params/grads, fp32 master/m/v",
                        "l2": "step moves %.0f GB >> 129 MB L2, no flush" % (algo_bytes / 1e9),
                        "parallelism": "replicas" if ws > 1 else "1 GPU, %d simulated ranks" % n_d},
@@ -1295,6 +1310,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused-steps", type=int, default=10)
     ap.add_argument("--bucketwise-steps", type=int, default=10)
+    ap.add_argument("--step-mode", choices=["whole", "per-bucket", "per-bucket-2s"], default="whole",
+                    help="fused workloads: one call over the whole flat space (default), or every bucket stepped "
+                         "bucket by bucket, last first (one stream / two streams)")
+    ap.add_argument("--bucket-bytes", type=int, default=None, help="override the workload's bucket size")
     ap.add_argument("--fused-variant", choices=["auto", "ldg", "tma"], default="auto",
                     help="kernel behind the fused step (all variants compute identical results)")
     args = ap.parse_args()

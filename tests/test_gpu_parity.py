@@ -786,3 +786,43 @@ def test_fused_step_bucket_walk_every_rank_count(variant, n_d):
     for x, y in zip(sa.args(), sb.args()):
         assert torch.equal(x, y)
     assert all(torch.equal(x, y) for x, y in zip(ra, rb))
+
+
+@pytest.mark.parametrize("mode", ["walk", "per_bucket", "per_bucket_two_streams", "single_bucket_calls"])
+def test_walk_of_unaligned_long_buckets(mode):
+    """Buckets of 4,194,307 elements (longer than a walk piece, odd, so every bucket edge is off the
+    8-element grid): each bucket is walked as staged pieces plus streaming fringes, the later staged
+    launches not waiting before they start.  Equals the whole-range step bit for bit, with the
+    gradients' copy enqueued just before the call and the results read just after it."""
+    n = 3 * 4_194_307 + 5
+    plan, _ = _plans([(n,)], 8, bucket_bytes=2 * 4_194_307)
+    assert plan.n_buckets == 4
+    P, pads = plan.padded, plan.pad_ranges()
+    master0 = synth.master_init(P, pads, seed=65, device=DEV)
+    a, b = State(master0), State(master0)
+    ra = synth.rank_buffers(8, P, BF16, DEV)[0]
+    rb = synth.rank_buffers(8, P, BF16, DEV)[0]
+    src, _ = synth.rank_grads(8, P, pads, seed=65, step=1, sigma=1e-3, device=DEV)
+    grads = synth.rank_buffers(8, P, BF16, DEV)[0]
+    zs.zs_fused_step(plan, -1, src, zs.ZS_RANK_FULL, *a.args(), ra, HP, 1)
+    torch.cuda.synchronize()
+    for q in range(8):
+        grads[q].copy_(src[q])
+    order = list(reversed(range(plan.n_buckets)))
+    if mode == "single_bucket_calls":
+        for bk in order:
+            zs.zs_fused_step(plan, bk, grads, zs.ZS_RANK_FULL, *b.args(), rb, HP, 1)
+    elif mode == "walk":
+        for part in (order[0::2], order[1::2]):
+            zs.zs_fused_step_buckets(plan, part, grads, *b.args(), rb, HP, 1, launch_mode=zs.ZS_BUCKETS_ONE_WALK)
+    else:
+        side = torch.cuda.Stream() if mode == "per_bucket_two_streams" else None
+        zs.zs_fused_step_buckets(plan, order, grads, *b.args(), rb, HP, 1, launch_mode=zs.ZS_BUCKETS_PER_BUCKET,
+                                 side_stream=side)
+    after = [r.clone() for r in rb] + [x.clone() for x in b.args()]
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    for x, y in zip(a.args(), b.args()):
+        assert torch.equal(x, y)
+    assert all(torch.equal(x, y) for x, y in zip(ra, rb))
+    assert all(torch.equal(x, y) for x, y in zip(ra + list(a.args()), after))
