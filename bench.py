@@ -1184,7 +1184,7 @@ def run_ours(args, ws, rank, local):
             "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": args.workload + ("-profile-case" if args.profile_case else ""),
-                       "fused_variant": args.fused_variant, "model_shape": W.wl["model"], "params": plan.numel,
+                       "fused_variant": args.fused_variant, "params": plan.numel,
                        "padded": P, "n_d": n_d, "stage": "zero%d" % W.wl["stage"],
                        "bucket_bytes": W.wl["bucket_bytes"], "step": W.kind, "step_mode": args.step_mode,
                        "storage": "bf16 params/grads, fp32 master/m/v",
