@@ -3,8 +3,11 @@
 
 One step = one pass of the hot path over one batch of synthetic gradients:
 reduce-scatter with averaging over N_d simulated ranks, AdamW on every rank's
-shard, all-gather of the bf16 parameters into every rank's replica - the
-fused single-launch kernel over the whole flat space (zs_fused_step).
+shard, all-gather of the bf16 parameters into every rank's replica - one
+zs_fused_step call over the whole flat space, which the library walks in
+overlapping launches of the fused kernel (each byte crosses HBM once).
+--step-mode per-bucket steps the same buckets one by one instead, last first,
+as backward makes them ready.
 
 Default workload: Llama-style 1.3B flat buffer (24 layers, d 2048, SwiGLU
 5504, vocab 32000, untied), N_d = 8 simulated ranks, ZeRO-2, 25 MiB buckets,
@@ -12,7 +15,9 @@ bf16 grads N(0, 5e-4) with 0.1% entries x100, fp32 master/m/v.  Inputs are
 59 GB, far larger than the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--profile-case] [--no-e2e] [--no-cpu-baseline]
+                  [--workload NAME] [--profile-case [--profile-elems N]] [--no-e2e]
+                  [--no-cpu-baseline] [--step-mode whole|per-bucket|per-bucket-2s]
+                  [--bucket-bytes B]
 
 With --gpus N > 1 (launched by torchrun) every rank runs an independent
 replica of the workload on its own GPU (the simulated ranks live inside one
@@ -559,8 +564,9 @@ def timed_on_stream(torch, fn, steps, warmup, stream, dev, dist, status=None, wh
 
 def run_sweep(args, ws, rank, local):
     """The 2^28+7-element flat buffer: the fused ZeRO-1/2 step and the ZeRO-3 step for every N_d of
-    the sweep, and the bucket-wise ZeRO-2 step (every bucket, descending: walked by one launch, one
-    launch per bucket, and one launch per bucket on two streams) for every bucket size at N_d = 8."""
+    the sweep, and the bucket-wise ZeRO-2 step (every bucket, descending: as one merged walk, as two
+    walks of every other bucket, bucket by bucket on one stream and on two) for every bucket size
+    at N_d = 8."""
     import torch
 
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
