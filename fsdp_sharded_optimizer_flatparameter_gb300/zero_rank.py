@@ -21,7 +21,9 @@ Device buffers of one rank (all on its own GPU):
   param_shard  its bf16 parameter shard, same layout;
   replica      its full bf16 parameters (ZeRO-1/2), refreshed by the all-gather.
 The collectives run on the process group's backend (NCCL between GPUs); with the default local
-update the step's arithmetic runs in the library's kernels on the current stream.
+update the step's arithmetic runs in the library's kernels on the current stream.  A step issues
+every bucket's exchange before the first update, so the exchanges stream on the collective's side
+while the updates follow bucket by bucket, each after its own exchange.
 """
 
 import torch
@@ -56,17 +58,17 @@ class ZeroRank:
     def _library_update(self, bucket, slices, master, m, v, param_shard, hp, step):
         zs_rank_shard_step(self.plan, self.rank, bucket, slices, master, m, v, param_shard, hp, step)
 
-    def exchange(self, bucket, grads, grads_base=0):
-        """The reduce-scatter's data movement for one bucket: an all-to-all in which every rank sends
-        each owner its part of the bucket.  Returns N_d slices, slice q holding rank q's gradients for
-        this rank's part.  grads: element i of this rank's gradients at grads[i - grads_base]."""
+    def _exchange_start(self, bucket, grads, grads_base, async_op):
         lens = self._lens[bucket]
         _, lo, hi = self.plan.bucket(bucket)
         send = grads[lo - grads_base:hi - grads_base]
         mine = lens[self.rank]
         recv = torch.empty(self.n_d * mine, dtype=grads.dtype, device=grads.device)
-        dist.all_to_all_single(recv, send, [mine] * self.n_d, lens, group=self.group)
+        work = dist.all_to_all_single(recv, send, [mine] * self.n_d, lens, group=self.group, async_op=async_op)
         self.bytes_sent += 2 * (sum(lens) - lens[self.rank])
+        return work, recv, mine
+
+    def _slices(self, recv, mine, grads):
         if mine % 8 == 0:
             return [recv[q * mine:(q + 1) * mine] for q in range(self.n_d)]
         # the library takes 16-byte-aligned slices: a part that is not a multiple of 8 elements is laid
@@ -77,11 +79,28 @@ class ZeroRank:
         rows[:, :mine].copy_(recv.view(self.n_d, mine))
         return [rows[q, :mine] for q in range(self.n_d)]
 
+    def exchange(self, bucket, grads, grads_base=0):
+        """The reduce-scatter's data movement for one bucket: an all-to-all in which every rank sends
+        each owner its part of the bucket.  Returns N_d slices, slice q holding rank q's gradients for
+        this rank's part.  grads: element i of this rank's gradients at grads[i - grads_base]."""
+        _, recv, mine = self._exchange_start(bucket, grads, grads_base, False)
+        return self._slices(recv, mine, grads)
+
     def reduce_scatter_update(self, bucket, grads, master, m, v, param_shard, hp, step, grads_base=0):
         """Exchange one bucket, then average and apply AdamW to this rank's part of it."""
-        slices = self.exchange(bucket, grads, grads_base)
-        if slices[0].numel() > 0:
-            self._update(bucket, slices, master, m, v, param_shard, hp, step)
+        self._buckets_update([bucket], grads, master, m, v, param_shard, hp, step, grads_base)
+
+    def _buckets_update(self, buckets, grads, master, m, v, param_shard, hp, step, grads_base=0):
+        # Every listed bucket's exchange is issued before the first update: an exchange only reads the
+        # gradients and writes its own receive buffer, so the exchanges run on the collective's stream
+        # while the updates follow one by one on the current stream, each after its own exchange.
+        # The receive buffers alive at once hold N_d times this rank's part of the listed buckets (at
+        # most one gradient buffer's worth for a whole step).
+        pending = [(b, self._exchange_start(b, grads, grads_base, True)) for b in buckets]
+        for b, (work, recv, mine) in pending:
+            work.wait()
+            if mine > 0:
+                self._update(b, self._slices(recv, mine, grads), master, m, v, param_shard, hp, step)
 
     def all_gather(self, param_shard, replica):
         """Every rank's updated shard of every unit into this rank's full bf16 replica."""
@@ -95,8 +114,7 @@ class ZeroRank:
         """One ZeRO-1/2 step: each bucket (default: all, last first, as backward makes them ready)
         exchanged and applied, then the all-gather of the parameter shards."""
         order = list(buckets) if buckets is not None else list(reversed(range(self.plan.n_buckets)))
-        for b in order:
-            self.reduce_scatter_update(b, grads, master, m, v, param_shard, hp, step)
+        self._buckets_update(order, grads, master, m, v, param_shard, hp, step)
         self.all_gather(param_shard, replica)
 
     def gather_unit(self, unit, param_shard, full):
@@ -109,5 +127,5 @@ class ZeroRank:
         """ZeRO-3: the unit's gradients (unit-local buffer) exchanged bucket by bucket and applied to
         this rank's shard of the unit; nothing is gathered afterwards."""
         base = self.plan.unit(unit)["base"]
-        for b in reversed(self._unit_buckets[unit]):
-            self.reduce_scatter_update(b, unit_grads, master, m, v, param_shard, hp, step, grads_base=base)
+        self._buckets_update(list(reversed(self._unit_buckets[unit])), unit_grads, master, m, v, param_shard, hp,
+                             step, grads_base=base)
