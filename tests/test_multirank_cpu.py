@@ -44,7 +44,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_gloo_world_size_2():
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     out = manager.dict()
     mp.start_processes(_worker, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
     assert dict(out) == {0: (15.0, (True, False)), 1: (15.0, (True, False))}

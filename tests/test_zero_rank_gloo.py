@@ -131,7 +131,7 @@ def _worker(rank, world, port, case, stage, out):
 @pytest.mark.parametrize("case,stage", [("flat", 2), ("units", 2), ("units", 3)])
 def test_zero_rank_exchanges_match_the_oracle(world, case, stage):
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.start_processes(_worker, args=(world, port, case, stage, out), nprocs=world, join=True,
                        start_method="spawn")
     assert sorted(out.keys()) == list(range(world))
