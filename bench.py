@@ -1323,6 +1323,12 @@ def main():
     ap.add_argument("--fused-variant", choices=["auto", "ldg", "tma"], default="auto",
                     help="kernel behind the fused step (all variants compute identical results)")
     args = ap.parse_args()
+    if args.step_mode != "whole" and args.impl == "ours":
+        import synth
+
+        wl = synth.WORKLOADS.get(args.workload, {})
+        if wl.get("stage") == 3 or wl.get("micro", 1) > 1 or args.workload in ("flat-sweep", "next-rows"):
+            ap.error("--step-mode applies to the fused ZeRO-1/2 workloads without accumulation")
     if args.warmup < 3 and args.impl == "ours" and not args.profile_case:
         log("note: fewer than 3 warm-up steps")
     if args.steps is None:

@@ -392,26 +392,11 @@ extern "C" int zs_rank_shard_step(zs_plan_t plan, int32_t rank, int32_t bucket, 
         const void* sp[1] = {param_shard};
         ZS_TRY(make_view(fn, "param_shard", sp, ZS_SHARDED, nd, 0, 0, &o));
     }
-    // ask the runtime once whether every buffer is device memory (the staged kernel's bulk copies are
-    // pointed at device memory only)
-    const void* real[ZS_MAX_RANKS + 4];
-    int nreal = 0;
-    for (int q = 0; q < nd; ++q) real[nreal++] = slices[q];
-    real[nreal++] = master;
-    real[nreal++] = m;
-    real[nreal++] = v;
-    real[nreal++] = param_shard;
-    bool on_device = true;
-    for (int k = 0; k < nreal && on_device; ++k) {
-        cudaPointerAttributes at;
-        if (cudaPointerGetAttributes(&at, real[k]) != cudaSuccess) {
-            cudaGetLastError();
-            on_device = false;
-        } else if (at.type != cudaMemoryTypeDevice) {
-            on_device = false;
-        }
-    }
-    const zs::StagedPolicy pol = on_device ? zs::kStagedDeviceKnown : zs::kStagedNever;
+    // ask the runtime once, about the real pointers, whether every buffer is device memory (the staged
+    // kernel's bulk copies are pointed at device memory only)
+    for (int q = 0; q < ZS_MAX_RANKS; ++q) g.ptr.p[q] = q < nd ? (uint16_t*)slices[q] : nullptr;
+    const zs::StagedPolicy pol =
+        zs::fused_ptrs_on_device(g, master, m, v, o, false, nd) ? zs::kStagedDeviceKnown : zs::kStagedNever;
     for (const Piece& pc : pieces) {
         for (int q = 0; q < ZS_MAX_RANKS; ++q)
             g.ptr.p[q] = q < nd ? (uint16_t*)slices[q] + pc.in_slice : nullptr;
