@@ -10,7 +10,10 @@ every element of every output is compared with the oracle, bit for bit:
   launches walked), at step 2 so the moments going in are not zero;
 * the whole Llama-7B ZeRO-3 step at N_d = 16 (zs_zero3_step, both streams,
   the 2-slot pool), at step 2, on its largest unit (the root unit: embedding,
-  final norm and output, 262,148,096 elements) with the parameter shards.
+  final norm and output, 262,148,096 elements) with the parameter shards;
+* the GPT-2-small step with four accumulated micro-batches at N_d = 8 (every
+  accumulated gradient too);
+* the 2^28+7-element flat buffer at N_d = 32 (padding, the widest rank count).
 
 Every step is element-wise, so the oracle on a chunk needs only that chunk's
 inputs.  Chunks are checked by a pool of host threads (numpy releases the GIL
@@ -159,3 +162,92 @@ def test_llama7b_zero3_step_root_unit_every_element():
         return out
 
     _verify(up, job, "Llama-7B ZeRO-3 step, N_d=16, root unit")
+
+
+def test_gpt2_small_accumulate_and_step_every_element():
+    """GPT-2-small, N_d = 8: four micro-batches accumulated with the 1/4 loss scale, then the walked
+    fused step; every accumulated gradient and every output element against the oracle."""
+    wl = synth.WORKLOADS["gpt2-small-zero1"]
+    shapes, _ = synth.workload_params(wl["model"])
+    n_d, micro_n = wl["n_d"], wl["micro"]
+    plan = zs.Plan(shapes, n_d, stage=wl["stage"], bucket_bytes=wl["bucket_bytes"])
+    P, pads = plan.padded, plan.pad_ranges()
+    acc, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    micro = [synth.rank_buffers(n_d, P, BF16, DEV)[0] for _ in range(micro_n)]
+    for j in range(micro_n):
+        synth.fill_grads(micro[j], pads, wl["seed"], 100 + j, wl["sigma"])
+        zs.zs_accumulate_grad(plan, acc, micro[j], 1.0 / micro_n, first=(j == 0))
+    master = synth.master_init(P, pads, wl["seed"], device=DEV)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    reps, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    torch.cuda.synchronize()
+    p0 = _f32(master)
+    zs.zs_device_status(clear=True)
+    zs.zs_fused_step(plan, -1, acc, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+
+    def job(lo, hi):
+        out = []
+        accs = []
+        for q in range(n_d):
+            a = None
+            for j in range(micro_n):
+                a = steps.accumulate(a, _bits16(micro[j][q][lo:hi]), 1.0 / micro_n, first=(j == 0))
+            d = _first_diff(_bits16(acc[q][lo:hi]), a)
+            if d:
+                out.append(("accumulated gradient of rank %d" % q,) + d)
+            accs.append(a)
+        ghat = steps.reduce_mean(accs)
+        z = np.zeros(hi - lo, np.float32)
+        p, m1, v1, bits = steps.adamw(p0[lo:hi], z, z, ghat, HP, 1)
+        for name, dev_t, want in (("master", master, p), ("m", m, m1), ("v", v, v1)):
+            d = _first_diff(_f32(dev_t[lo:hi]).view(np.uint32), want.view(np.uint32))
+            if d:
+                out.append((name,) + d)
+        for q in range(n_d):
+            d = _first_diff(_bits16(reps[q][lo:hi]), bits)
+            if d:
+                out.append(("replica %d" % q,) + d)
+        return out
+
+    _verify(P, job, "GPT-2-small 4 x accumulate + ZeRO-1 step, N_d=8")
+
+
+def test_flat_sweep_n32_step_every_element():
+    """The 2^28+7-element flat buffer at N_d = 32 (25 padding elements, the widest walk shape's rank
+    count): the walked fused step, every element of every output against the oracle."""
+    n_d = 32
+    plan = zs.Plan([(2 ** 28 + 7,)], n_d, stage=2)
+    P, pads = plan.padded, plan.pad_ranges()
+    assert P - plan.numel == 25
+    master = synth.master_init(P, pads, 4, device=DEV)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    grads, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    synth.fill_grads(grads, pads, 4, 1, 1e-3)
+    reps, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    p0 = _f32(master)
+    zs.zs_device_status(clear=True)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+
+    def job(lo, hi):
+        g = [_bits16(grads[q][lo:hi]) for q in range(n_d)]
+        ghat = steps.reduce_mean(g)
+        z = np.zeros(hi - lo, np.float32)
+        p, m1, v1, bits = steps.adamw(p0[lo:hi], z, z, ghat, HP, 1)
+        out = []
+        for name, dev_t, want in (("master", master, p), ("m", m, m1), ("v", v, v1)):
+            d = _first_diff(_f32(dev_t[lo:hi]).view(np.uint32), want.view(np.uint32))
+            if d:
+                out.append((name,) + d)
+        d = _first_diff(_bits16(reps[0][lo:hi]), bits)
+        if d:
+            out.append(("replica 0",) + d)
+        for q in range(1, n_d):
+            if not torch.equal(reps[q][lo:hi], reps[0][lo:hi]):
+                out.append(("replica %d vs replica 0" % q, -1, 0))
+        return out
+
+    _verify(P, job, "flat 2^28+7 fused step, N_d=32")
