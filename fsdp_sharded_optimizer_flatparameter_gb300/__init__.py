@@ -571,9 +571,10 @@ def zs_fsdp2_copy_out(plan, unit, flat, params, stream=None):
 def zs_fused_step_buckets(plan, buckets, grads, master, m, v, replicas, hp, step, launch_mode=None, stream=None,
                           side_stream=None):
     """buckets: bucket indices in stepping order.  launch_mode: ZS_BUCKETS_ONE_WALK (default:
-    touching buckets merge, ranges of 2^25+ elements get a launch each, one persistent launch walks
-    the rest) or ZS_BUCKETS_PER_BUCKET (one launch each; odd positions on side_stream if given).
-    Gradients and replicas may be pinned host memory, as for zs_fused_step."""
+    touching buckets merge, the ranges are walked in overlapping launches, runs under 2^16 elements
+    share list launches) or ZS_BUCKETS_PER_BUCKET (the buckets walked one after another, no launch
+    spanning two; odd positions on side_stream if given).  Gradients and replicas may be pinned host
+    memory, as for zs_fused_step."""
     _n_ptrs(ZS_RANK_FULL, grads, plan.n_d, "grads")
     _n_ptrs(ZS_RANK_FULL, replicas, plan.n_d, "replicas")
     n = plan.padded
