@@ -32,6 +32,10 @@ CASES = {
     # several units, N_d = 3: odd local offsets, element by element
     "units-n3": dict(shapes=[(64, 48), (48,), (100, 30), (30,), (7, 5)], units=[0, 0, 1, 1, 2], n_d=3,
                      bucket_bytes=2_000),
+    # more ranks than elements, one-element buckets: most parts empty
+    "tiny-n8": dict(shapes=[(3,), (4,)], units=None, n_d=8, bucket_bytes=2),
+    # one rank: the rank's part is the whole bucket
+    "one-rank": dict(shapes=[(1,), (70_001,)], units=[0, 1], n_d=1, bucket_bytes=1 << 12),
 }
 
 

@@ -26,6 +26,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CASES = {
     "flat": dict(shapes=[(300, 96), (96,), (257, 96)], units=None, bucket_bytes=10_000),
     "units": dict(shapes=[(64, 48), (48,), (100, 30), (30,), (7, 5)], units=[0, 0, 1, 1, 2], bucket_bytes=2_000),
+    # fewer elements than ranks have room for: one-element buckets, most parts empty
+    "tiny": dict(shapes=[(3,), (2,)], units=None, bucket_bytes=2),
 }
 
 
@@ -128,7 +130,7 @@ def _worker(rank, world, port, case, stage, out):
 
 
 @pytest.mark.parametrize("world", [2, 3])
-@pytest.mark.parametrize("case,stage", [("flat", 2), ("units", 2), ("units", 3)])
+@pytest.mark.parametrize("case,stage", [("flat", 2), ("units", 2), ("units", 3), ("tiny", 2)])
 def test_zero_rank_exchanges_match_the_oracle(world, case, stage):
     port = _free_port()
     out = mp.get_context("spawn").Manager().dict()
