@@ -269,3 +269,32 @@ def test_checkpoint_step_is_validated(tmp_path):
         (tmp_path / "meta.txt").write_text("zs-checkpoint 2\nn_d 4\n" + bad + "layout 0\nparams 1\n")
         assert lib.zs_checkpoint_load(p.handle, d, *a, ctypes.byref(step), None) == zs.ZS_ERR_INVALID
         assert "bad step" in zs.zs_last_error(), bad
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="passes placeholder addresses; the GPU tests cover this with real buffers")
+def test_rank_shard_step_rejects_bad_arguments_before_launch():
+    """zs_rank_shard_step (one rank's local update) refuses bad arguments with ZS_ERR_INVALID before it
+    looks at any buffer (placeholder addresses: no case may reach a launch)."""
+    lib = ctypes.CDLL(zs.LIB_PATH)
+    lib.zs_rank_shard_step.restype = ctypes.c_int32
+    p = zs.Plan([(64,)], 4, stage=2, bucket_bytes=32)
+    hp = zs.zs_adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.1)
+    good = [0x10000 * (q + 1) for q in range(4)]
+
+    def call(rank=0, bucket=0, slices=good, master=0x90000, step=1, hpp=hp):
+        arr = (ctypes.c_void_p * len(slices))(*slices)
+        return lib.zs_rank_shard_step(p.handle, ctypes.c_int32(rank), ctypes.c_int32(bucket), arr,
+                                      ctypes.c_void_p(master), ctypes.c_void_p(0xA0000), ctypes.c_void_p(0xB0000),
+                                      ctypes.c_void_p(0xC0000), ctypes.byref(hpp), ctypes.c_int64(step),
+                                      ctypes.c_void_p(0))
+
+    assert call(rank=4) == zs.ZS_ERR_INVALID and "rank" in zs.zs_last_error()
+    assert call(rank=-1) == zs.ZS_ERR_INVALID
+    assert call(bucket=p.n_buckets) == zs.ZS_ERR_INVALID and "bucket" in zs.zs_last_error()
+    assert call(bucket=-2) == zs.ZS_ERR_INVALID
+    assert call(slices=[good[0], 0, good[2], good[3]]) == zs.ZS_ERR_INVALID
+    assert "missing rank" in zs.zs_last_error()
+    assert call(slices=[good[0] + 2] + good[1:]) == zs.ZS_ERR_INVALID                # misaligned slice
+    assert call(master=0x90004) == zs.ZS_ERR_INVALID                                 # misaligned state
+    assert call(step=0) == zs.ZS_ERR_INVALID
+    assert call(hpp=zs.zs_adamw_hparams(1e-3, 1.0, 0.95, 1e-8, 0.1)) == zs.ZS_ERR_INVALID
