@@ -33,20 +33,15 @@ from . import zs_rank_shard_step
 
 
 class ZeroRank:
-    """One rank of N_d, each its own process: exchange, local update, gather.
+    """One rank of N_d, each its own process: exchange, local update (the library's
+    zs_rank_shard_step, in local_update), gather."""
 
-    local_update(bucket, slices, master, m, v, param_shard, hp, step) replaces the library's
-    zs_rank_shard_step; it exists so the exchanges can be exercised on CPU process groups, where
-    the library's kernels cannot run.
-    """
-
-    def __init__(self, plan, group=None, local_update=None):
+    def __init__(self, plan, group=None):
         self.plan, self.group = plan, group
         self.rank = dist.get_rank(group)
         self.n_d = dist.get_world_size(group)
         if self.n_d != plan.n_d:
             raise ValueError("the process group has %d ranks, the plan N_d = %d" % (self.n_d, plan.n_d))
-        self._update = local_update or self._library_update
         self.bytes_sent = 0
         # every owner's part of every bucket: the all-to-all's split sizes
         self._lens = [[hi - lo for lo, hi in (plan.bucket_rank_slice(b, q) for q in range(self.n_d))]
@@ -55,7 +50,8 @@ class ZeroRank:
         for b in range(plan.n_buckets):
             self._unit_buckets[plan.bucket(b)[0]].append(b)
 
-    def _library_update(self, bucket, slices, master, m, v, param_shard, hp, step):
+    def local_update(self, bucket, slices, master, m, v, param_shard, hp, step):
+        """This rank's part of `bucket`: fold the received slices, AdamW on its own shard state."""
         zs_rank_shard_step(self.plan, self.rank, bucket, slices, master, m, v, param_shard, hp, step)
 
     def _exchange_start(self, bucket, grads, grads_base, async_op):
@@ -100,7 +96,7 @@ class ZeroRank:
         for b, (work, recv, mine) in pending:
             work.wait()
             if mine > 0:
-                self._update(b, self._slices(recv, mine, grads), master, m, v, param_shard, hp, step)
+                self.local_update(b, self._slices(recv, mine, grads), master, m, v, param_shard, hp, step)
 
     def all_gather(self, param_shard, replica):
         """Every rank's updated shard of every unit into this rank's full bf16 replica."""

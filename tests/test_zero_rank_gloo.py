@@ -3,8 +3,8 @@
 Each process is one rank: it holds only its own gradients, its own shard of the fp32 state and of the
 bf16 parameters, and a full replica.  The all-to-all of every bucket, the all-gather of the shards
 and the ZeRO-3 unit gathers run over torch.distributed (gloo here, NCCL between GPUs).  The library's
-kernels cannot run on a CPU group, so each rank's local update is the oracle's reduce-mean and AdamW
-on the slices the exchange delivered; the GPU test of zs_rank_shard_step checks the kernel side of
+kernels cannot run on a CPU group, so each rank's local update (ZeroRank.local_update, overridden
+here) is the oracle's reduce-mean and AdamW on the slices the exchange delivered; the GPU test of zs_rank_shard_step checks the kernel side of
 the same update.  Every rank's results must equal the oracle's simulated step (steps.zero_step,
 steps.zero3_unit_step) bit for bit, and the bytes each rank sent must equal the plan's
 communication count.
@@ -45,21 +45,27 @@ def _from_bits(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
 
 
-def _oracle_update(plan, rank, steps):
-    """This rank's local update computed by the oracle from the exchanged slices (CPU groups only)."""
+def _oracle_rank_class(ZeroRank, steps):
+    """ZeroRank whose local update is the oracle's, on the exchanged slices (CPU groups, where the
+    library's kernels cannot run); the exchanges and gathers are ZeroRank's own."""
 
-    def update(bucket, slices, master, m, v, param_shard, hp, t):
-        lo, hi, local = plan.rank_bucket_part(rank, bucket)
-        n = hi - lo
-        ghat = steps.reduce_mean([_bits(s) for s in slices])
-        p, m1, v1, bits = steps.adamw(master[local:local + n].numpy(), m[local:local + n].numpy(),
-                                      v[local:local + n].numpy(), ghat, hp, t)
-        master[local:local + n] = torch.from_numpy(p)
-        m[local:local + n] = torch.from_numpy(m1)
-        v[local:local + n] = torch.from_numpy(v1)
-        param_shard[local:local + n] = _from_bits(bits)
+    class OracleRank(ZeroRank):
+        def local_update(self, bucket, slices, master, m, v, param_shard, hp, t):
+            _oracle_update(self.plan, self.rank, steps, bucket, slices, master, m, v, param_shard, hp, t)
 
-    return update
+    return OracleRank
+
+
+def _oracle_update(plan, rank, steps, bucket, slices, master, m, v, param_shard, hp, t):
+    lo, hi, local = plan.rank_bucket_part(rank, bucket)
+    n = hi - lo
+    ghat = steps.reduce_mean([_bits(s) for s in slices])
+    p, m1, v1, bits = steps.adamw(master[local:local + n].numpy(), m[local:local + n].numpy(),
+                                  v[local:local + n].numpy(), ghat, hp, t)
+    master[local:local + n] = torch.from_numpy(p)
+    m[local:local + n] = torch.from_numpy(m1)
+    v[local:local + n] = torch.from_numpy(v1)
+    param_shard[local:local + n] = _from_bits(bits)
 
 
 def _worker(rank, world, port, case, stage, out):
@@ -84,7 +90,7 @@ def _worker(rank, world, port, case, stage, out):
         mine = steps.shard_of(oplan, rank, master_full.numpy())
         master, m, v = torch.from_numpy(mine.copy()), torch.zeros(S), torch.zeros(S)
         param_shard = _from_bits(np.zeros(S, np.uint16))
-        zr = ZeroRank(plan, local_update=_oracle_update(plan, rank, steps))
+        zr = _oracle_rank_class(ZeroRank, steps)(plan)
         o_m = [steps.shard_of(oplan, r, master_full.numpy()) for r in range(world)]
         o_mm = [np.zeros(oplan.shard_total, np.float32) for _ in range(world)]
         o_v = [np.zeros(oplan.shard_total, np.float32) for _ in range(world)]
