@@ -210,3 +210,47 @@ def test_dependent_launch_on_and_off_agree():
             zs.zs_set_dependent_launch(True)
 
     _assert_same(run(False), run(True))
+
+
+def test_overlapping_walks_repeat_the_serialised_result():
+    """Race check of the walk's overlapping launches: the bucket-by-bucket step over 128 buckets of
+    1 MiB (every later launch starts before its predecessor ends), on one stream and on two, and the
+    whole-range walk, repeated 20 times each from the same state, must equal bit for bit the same
+    step run with programmatic dependent launch off (every launch waiting for the previous one)."""
+    n_d = 8
+    plan = zs.Plan([(1 << 26,)], n_d, stage=2, bucket_bytes=1 << 20)
+    assert plan.n_buckets == 128
+    P, pads = plan.padded, plan.pad_ranges()
+    grads = synth.rank_grads(n_d, P, pads, seed=90, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)[0]
+    master0 = synth.master_init(P, pads, seed=91, device=DEV)
+    m0 = torch.rand_like(master0) * 1e-3                 # moments going in are not zero
+    v0 = torch.rand_like(master0) * 1e-6
+    order = list(reversed(range(plan.n_buckets)))
+    side = torch.cuda.Stream()
+
+    def fresh():
+        return [master0.clone(), m0.clone(), v0.clone()], synth.rank_buffers(n_d, P, BF16, DEV)[0]
+
+    def run(mode, st, reps):
+        if mode == "whole":
+            zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *st, reps, HP, 3)
+        else:
+            zs.zs_fused_step_buckets(plan, order, grads, *st, reps, HP, 3, launch_mode=zs.ZS_BUCKETS_PER_BUCKET,
+                                     side_stream=side if mode == "two_streams" else None)
+
+    zs.zs_set_dependent_launch(False)
+    try:
+        ref_st, ref_reps = fresh()
+        run("per_bucket", ref_st, ref_reps)
+        torch.cuda.synchronize()
+    finally:
+        zs.zs_set_dependent_launch(True)
+    zs.zs_device_status(clear=True)
+    for mode in ("per_bucket", "two_streams", "whole"):
+        for k in range(20):
+            st, reps = fresh()
+            run(mode, st, reps)
+            torch.cuda.synchronize()
+            assert all(torch.equal(x, y) for x, y in zip(st, ref_st)), "%s run %d: state differs" % (mode, k)
+            assert all(torch.equal(x, y) for x, y in zip(reps, ref_reps)), "%s run %d: replicas differ" % (mode, k)
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
