@@ -34,8 +34,10 @@
  *                  its own piece)
  *   ZS_RANK_BUCKET N_d pointers; ptrs[q][i - bucket_begin] (one bucket)
  *   ZS_RANK_UNIT   N_d pointers; ptrs[q][i - unit_base]    (one unit)
- *             master, m and v are always ZS_SHARDED fp32 arrays of
- *             padded_numel elements.
+ *             master, m and v are ZS_SHARDED fp32 arrays of padded_numel
+ *             elements, except in zs_rank_shard_step, which takes one rank's
+ *             own state in that rank's local layout (its shard of every unit,
+ *             back to back) for the mode with one rank per process and GPU.
  * Ownership.  The caller owns all device memory and all streams.  The library
  *             never allocates device memory.  The step calls never
  *             synchronise and enqueue work only on the streams they are given
