@@ -1323,6 +1323,11 @@ def main():
     ap.add_argument("--fused-variant", choices=["auto", "ldg", "tma"], default="auto",
                     help="kernel behind the fused step (all variants compute identical results)")
     args = ap.parse_args()
+    if args.impl == "reference":
+        import synth
+
+        if args.workload not in synth.WORKLOADS:
+            ap.error("--impl reference times the oracle on one of the workloads %s" % sorted(synth.WORKLOADS))
     if args.step_mode != "whole" and args.impl == "ours":
         import synth
 
