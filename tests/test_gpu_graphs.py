@@ -50,10 +50,11 @@ def _assert_same(a, b):
             assert torch.equal(x, y), "%s[%d] differs between the two runs" % (k, i)
 
 
-@pytest.mark.parametrize("n_d,numel", [(8, 1_500_007), (3, 70_001)])
+@pytest.mark.parametrize("n_d,numel", [(8, 1_500_007), (3, 70_001), (8, 10_000_007)])
 def test_accumulate_and_fused_step_replay(n_d, numel):
     """ZeRO-1 with four micro-batches: four accumulations then the fused step (staged at the larger
-    size, streaming at the smaller), captured and replayed twice."""
+    sizes, streaming at the smallest; at 10 M elements the step is walked in three overlapping
+    launches, captured as programmatic edges), captured and replayed twice."""
     plan = zs.Plan([(numel,)], n_d, stage=1)
     P, pads = plan.padded, plan.pad_ranges()
     micro = [synth.rank_grads(n_d, P, pads, seed=70, step=j + 1, sigma=1e-3, device=DEV)[0] for j in range(4)]
