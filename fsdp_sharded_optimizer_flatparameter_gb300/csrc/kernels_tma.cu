@@ -95,6 +95,19 @@ cudaError_t staged_geometry(const void* kern, int threads, int smem, int* sms, i
     return cudaSuccess;
 }
 
+// Host-side guard of the bulk-copy rules before a staged launch: a one-dimensional bulk copy must
+// start at a 16-byte-aligned address and move a multiple of 16 bytes.  The staged kernels copy tiles
+// of whole 8-element groups starting at body start + k * T (T a multiple of 8), so it suffices that
+// the body [lo, lo + n) has lo and n multiples of 8 and that element lo of every array the kernel
+// touches is 16-byte aligned.  The callers guarantee this; a launch that would break it is refused
+// (cudaErrorMisalignedAddress) instead of faulting the GPU.
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+bool body_ok(int64_t lo, int64_t n) { return (lo & 7) == 0 && (n & 7) == 0 && n > 0; }
+template <class T>
+bool at_ok(const T* base, int64_t elems) {
+    return aligned16((const void*)((uintptr_t)base + (uintptr_t)(elems * (int64_t)sizeof(T))));
+}
+
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
@@ -771,6 +784,10 @@ TmaArgs make_args(const BView& g, float* master, float* m, float* v, const BView
 // Returns cudaErrorNotSupported when no staged variant exists for this rank count.
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                              int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st, int sync) {
+    bool ok = body_ok(lo, n) && at_ok(master, lo) && at_ok(m, lo) && at_ok(v, lo);
+    for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off);
+    for (int q = 0; q < (broadcast ? nd : 1) && ok; ++q) ok = at_ok(out.ptr.p[q], lo - out.off);
+    if (!ok) return cudaErrorMisalignedAddress;
     TmaArgs a = make_args(g, master, m, v, out, s, nd);
     a.lo = lo;
     a.n = n;
@@ -828,6 +845,12 @@ cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float
                                   const std::vector<std::pair<int64_t, int64_t>>& bodies, const AdamScalars& s,
                                   int nd, cudaStream_t st) {
     if (bodies.empty()) return cudaSuccess;
+    for (const auto& b : bodies) {
+        bool ok = body_ok(b.first, b.second) && at_ok(master, b.first) && at_ok(m, b.first) && at_ok(v, b.first);
+        for (int q = 0; q < nd && ok; ++q)
+            ok = at_ok(g.ptr.p[q], b.first - g.off) && at_ok(out.ptr.p[q], b.first - out.off);
+        if (!ok) return cudaErrorMisalignedAddress;
+    }
     // the argument block is ~11 KB: built on the heap
     std::unique_ptr<TmaListArgs> l(new TmaListArgs());
     l->a = make_args(g, master, m, v, out, s, nd);
@@ -1001,6 +1024,9 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
 // Returns cudaErrorNotSupported when no staged shape exists for this rank count.
 cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
                           cudaStream_t st) {
+    bool ok = body_ok(lo, n) && at_ok(out, lo - out_off);
+    for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off);
+    if (!ok) return cudaErrorMisalignedAddress;
     RsTmaArgs a = rs_args(g, lo, n, nd);
     a.out = out;
     a.out_off = out_off;
@@ -1252,6 +1278,11 @@ cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
 // counts without a staged shape.
 cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master, float* const* m,
                           float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+    bool ok = body_ok(lo, n);
+    for (int q = 0; q < nd && ok; ++q)
+        ok = at_ok(g.ptr.p[q], lo - g.off) && at_ok(out.ptr.p[q], lo - out.off) && at_ok(master[q], lo) &&
+             at_ok(m[q], lo) && at_ok(v[q], lo);
+    if (!ok) return cudaErrorMisalignedAddress;
     DpTmaArgs a{};
     a.g = g.ptr;
     a.g_off = g.off;
@@ -1307,6 +1338,9 @@ cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
 // GB300).
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
                                int64_t n, int nd, cudaStream_t st) {
+    bool ok = body_ok(lo, n) && at_ok(src, lo - src_off);
+    for (int q = 0; q < nd && ok; ++q) ok = at_ok(dst.p[q], lo - dst_off);
+    if (!ok) return cudaErrorMisalignedAddress;
     GatherBulkArgs a{};
     a.src = src;
     a.src_off = src_off;
