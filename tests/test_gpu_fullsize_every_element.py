@@ -13,7 +13,11 @@ every element of every output is compared with the oracle, bit for bit:
   final norm and output, 262,148,096 elements) with the parameter shards;
 * the GPT-2-small step with four accumulated micro-batches at N_d = 8 (every
   accumulated gradient too);
-* the 2^28+7-element flat buffer at N_d = 32 (padding, the widest rank count).
+* the 2^28+7-element flat buffer at N_d = 32 (padding, the widest rank count);
+* a flat buffer past 2^32 elements at N_d = 2 (element offsets, tile counts
+  and walk pieces that overflow 32-bit integers): the walked fused step
+  against the oracle, then the bucket-by-bucket walk and the unfused calls
+  against that result on the device.
 
 Every step is element-wise, so the oracle on a chunk needs only that chunk's
 inputs.  Chunks are checked by a pool of host threads (numpy releases the GIL
@@ -251,3 +255,89 @@ def test_flat_sweep_n32_step_every_element():
         return out
 
     _verify(P, job, "flat 2^28+7 fused step, N_d=32")
+
+
+def test_flat_buffer_past_2p32_elements():
+    """One flat tensor of 2^32 + 2^22 + 3 elements at N_d = 2 (one padding element): every offset
+    past 2^31 and 2^32 that a 32-bit index would wrap.  The walked fused step is checked against the
+    oracle on every element; the same step bucket by bucket (25 MiB buckets, last first) and the
+    unfused ZeRO-2 calls (reduce-scatter into a sharded staging buffer, update, all-gather) run on
+    copies of the initial state and must reproduce it bit for bit."""
+    n_d = 2
+    numel = 2 ** 32 + 2 ** 22 + 3
+    plan = zs.Plan([(numel,)], n_d, stage=2, bucket_bytes=25 << 20)
+    P, pads = plan.padded, plan.pad_ranges()
+    assert P == numel + 1 and plan.n_buckets > 300
+    free, _ = torch.cuda.mem_get_info()
+    # at the peak: grads, replicas and fp32 state twice over (2 n_d + 2 n_d + 12 + 12 + 2 n_d B per
+    # element) plus the initial master (4 B), later the staging and shard buffers (2 + 2 B)
+    need = P * (6 * n_d + 24 + 4) + (4 << 30)
+    if free < need:
+        pytest.skip("needs %.0f GB of free device memory, %.0f GB free" % (need / 1e9, free / 1e9))
+    master = synth.master_init(P, pads, 4, device=DEV)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    grads, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    synth.fill_grads(grads, pads, 4, 1, 1e-3)
+    reps, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    p0 = _f32(master)
+    master2 = master.clone()
+    m2, v2 = torch.zeros_like(master), torch.zeros_like(master)
+    reps2, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+    zs.zs_device_status(clear=True)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+
+    def job(lo, hi):
+        g = [_bits16(grads[q][lo:hi]) for q in range(n_d)]
+        ghat = steps.reduce_mean(g)
+        z = np.zeros(hi - lo, np.float32)
+        p, m1, v1, bits = steps.adamw(p0[lo:hi], z, z, ghat, HP, 1)
+        out = []
+        for name, dev_t, want in (("master", master, p), ("m", m, m1), ("v", v, v1)):
+            d = _first_diff(_f32(dev_t[lo:hi]).view(np.uint32), want.view(np.uint32))
+            if d:
+                out.append((name,) + d)
+        d = _first_diff(_bits16(reps[0][lo:hi]), bits)
+        if d:
+            out.append(("replica 0",) + d)
+        if not torch.equal(reps[1][lo:hi], reps[0][lo:hi]):
+            out.append(("replica 1 vs replica 0", -1, 0))
+        return out
+
+    _verify(P, job, "flat 2^32+2^22+3 fused step, N_d=2")
+    del p0
+    gc.collect()
+
+    def same_as_fused(label):
+        for name, got, want in (("master", master2, master), ("m", m2, m), ("v", v2, v),
+                                ("replica 0", reps2[0], reps[0]), ("replica 1", reps2[1], reps[1])):
+            for lo in range(0, P, 1 << 30):
+                hi = min(P, lo + (1 << 30))
+                assert torch.equal(got[lo:hi], want[lo:hi]), "%s: %s differs in [%d, %d)" % (label, name, lo, hi)
+
+    def reset_state(init):
+        master2.copy_(init)
+        m2.zero_()
+        v2.zero_()
+        for r in reps2:
+            r.zero_()
+
+    init = master2.clone()
+    zs.zs_fused_step_buckets(plan, list(reversed(range(plan.n_buckets))), grads, master2, m2, v2, reps2, HP, 1,
+                             launch_mode=zs.ZS_BUCKETS_PER_BUCKET)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    same_as_fused("bucket by bucket")
+
+    reset_state(init)
+    del init
+    ghat = torch.zeros(P, dtype=BF16, device=DEV)
+    shards = torch.zeros(P, dtype=BF16, device=DEV)
+    for b in reversed(range(plan.n_buckets)):
+        zs.zs_reduce_scatter_mean(plan, b, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED)
+    zs.zs_adamw_shard_step(plan, -1, [ghat], zs.ZS_SHARDED, master2, m2, v2, [shards], zs.ZS_SHARDED, HP, 1)
+    zs.zs_all_gather(plan, [shards], zs.ZS_SHARDED, reps2)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    same_as_fused("unfused reduce-scatter, update, all-gather")
