@@ -29,23 +29,28 @@ constexpr int kThreads = 256;
 
 // ------------------------------------------------------------------ launch geometry
 
-// Blocks for a grid-stride kernel: enough to cover the work, at most one
-// full wave of resident blocks on the current device.
-static int grid_for(const void* kernel, int64_t items) {
+// Blocks for a grid-stride kernel: enough to cover the work, at most one full wave of resident
+// blocks on the current device.  The wave is cached per (device, kernel) once the queries succeed; a
+// failed query is returned to the caller and not cached.
+static cudaError_t grid_for(const void* kernel, int64_t items, int* grid) {
     static std::mutex mu;
     static std::unordered_map<uint64_t, int> cap_cache;     // (device, kernel) -> resident blocks
     int dev = 0;
-    cudaGetDevice(&dev);
-    const uint64_t key = ((uint64_t)(uintptr_t)kernel) ^ ((uint64_t)dev << 56);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t key = ((uint64_t)(uintptr_t)kernel) ^ ((uint64_t)(uint32_t)dev << 56);
     int cap;
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cap_cache.find(key);
         if (it == cap_cache.end()) {
             int sms = 0, occ = 0;
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
-            cap = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+            if (e != cudaSuccess) return e;
+            if (sms < 1 || occ < 1) return cudaErrorInvalidConfiguration;
+            cap = sms * occ;
             cap_cache.emplace(key, cap);
         } else {
             cap = it->second;
@@ -53,7 +58,8 @@ static int grid_for(const void* kernel, int64_t items) {
     }
     int64_t want = (items + kThreads - 1) / kThreads;
     if (want < 1) want = 1;
-    return (int)(want < cap ? want : cap);
+    *grid = (int)(want < cap ? want : cap);
+    return cudaSuccess;
 }
 
 // Split [lo, hi) into an 8-aligned vector body and a scalar fringe.
@@ -136,8 +142,10 @@ cudaError_t launch_accumulate(const Ptrs& acc, const Ptrs& micro, int nd, int64_
                               cudaStream_t st) {
     AccumArgs a{acc, micro, scale, first};
     Split sp = split_range(0, n, true);
-    dim3 grid(grid_for((const void*)k_accumulate, sp.nvec > 0 ? sp.nvec : n), nd);
-    return launch_kernel(k_accumulate, grid, dim3(kThreads), 0, st, a, sp);
+    int gx = 0;
+    cudaError_t e = grid_for((const void*)k_accumulate, sp.nvec > 0 ? sp.nvec : n, &gx);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k_accumulate, dim3(gx, nd), dim3(kThreads), 0, st, a, sp);
 }
 
 // ------------------------------------------------------------------ reduce-scatter with averaging
@@ -176,7 +184,9 @@ template <int ND>
 static cudaError_t rs_impl(const BView& g, const BView& out, bool by_owner, const Range& r, int nd, Split sp,
                            cudaStream_t st) {
     RsOp<ND> op{g, out, by_owner ? 1 : 0, nd, 1.0f / (float)nd, r.base, r.shard};
-    const int grid = grid_for((const void*)k_rs_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    int grid = 0;
+    cudaError_t ge = grid_for((const void*)k_rs_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
+    if (ge != cudaSuccess) return ge;
     return launch_kernel(k_rs_mean<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
@@ -235,7 +245,9 @@ template <int ND>
 static cudaError_t gather_impl(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
                                const Range& r, int nd, Split sp, cudaStream_t st) {
     GatherOp<ND> op{src, dst, src_by_owner ? 1 : 0, skip_owner ? 1 : 0, nd, r.base, r.shard};
-    const int grid = grid_for((const void*)k_gather<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    int grid = 0;
+    cudaError_t ge = grid_for((const void*)k_gather<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
+    if (ge != cudaSuccess) return ge;
     return launch_kernel(k_gather<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
@@ -292,7 +304,9 @@ template <int ND, bool BROADCAST>
 static cudaError_t fused_impl(const BView& g, float* master, float* m, float* v, const BView& out,
                               const AdamScalars& s, int nd, Split sp, cudaStream_t st) {
     FusedOp<ND, BROADCAST> op{g, out, master, m, v, s, nd, 1.0f / (float)nd};
-    const int grid = grid_for((const void*)k_fused<ND, BROADCAST>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    int grid = 0;
+    cudaError_t ge = grid_for((const void*)k_fused<ND, BROADCAST>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
+    if (ge != cudaSuccess) return ge;
     return launch_kernel(k_fused<ND, BROADCAST>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
@@ -376,8 +390,10 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
                 Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
                 for (const Split& f : rest) {
                     if (f.hi <= f.lo) continue;
-                    e = launch_kernel(k_adamw, dim3(grid_for((const void*)k_adamw, f.hi - f.lo)), dim3(kThreads), 0, st,
-                                      op, f);
+                    int grid = 0;
+                    e = grid_for((const void*)k_adamw, f.hi - f.lo, &grid);
+                    if (e != cudaSuccess) return e;
+                    e = launch_kernel(k_adamw, dim3(grid), dim3(kThreads), 0, st, op, f);
                     if (e != cudaSuccess) return e;
                 }
                 return cudaSuccess;
@@ -385,7 +401,9 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
         }
     }
     AdamOp op{grad, par, grad_by_owner ? 1 : 0, par_by_owner ? 1 : 0, master, m, v, s, r.base, r.shard};
-    const int grid = grid_for((const void*)k_adamw, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    int grid = 0;
+    cudaError_t ge = grid_for((const void*)k_adamw, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
+    if (ge != cudaSuccess) return ge;
     return launch_kernel(k_adamw, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
@@ -708,7 +726,9 @@ __global__ void __launch_bounds__(kThreads) k_dp_step(DpStepOp<ND> op, Split sp)
 template <int ND>
 static cudaError_t all_reduce_impl(const BView& g, int nd, Split sp, cudaStream_t st) {
     AllReduceOp<ND> op{g, nd, 1.0f / (float)nd};
-    const int grid = grid_for((const void*)k_all_reduce_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    int grid = 0;
+    cudaError_t ge = grid_for((const void*)k_all_reduce_mean<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
+    if (ge != cudaSuccess) return ge;
     return launch_kernel(k_all_reduce_mean<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
@@ -726,7 +746,9 @@ static cudaError_t dp_step_impl(const BView& g, const BView& out, float* const* 
     op.s = s;
     op.nd = nd;
     op.inv_nd = 1.0f / (float)nd;
-    const int grid = grid_for((const void*)k_dp_step<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo);
+    int grid = 0;
+    cudaError_t ge = grid_for((const void*)k_dp_step<ND>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
+    if (ge != cudaSuccess) return ge;
     return launch_kernel(k_dp_step<ND>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 

@@ -214,6 +214,7 @@ def _mutant_scalars(kind):
 
 @pytest.mark.parametrize("kind", ["no_bias_correction", "betas_swapped", "decay_sign", "eps_dropped",
                                   "t_off_by_one"])
+@pytest.mark.filterwarnings("ignore:invalid value encountered in divide:RuntimeWarning")   # eps_dropped: 0 / 0
 def test_planted_adamw_mistakes_are_caught(kind, monkeypatch):
     monkeypatch.setattr(steps, "adamw_scalars", _mutant_scalars(kind))
     failures = 0
