@@ -256,6 +256,8 @@ def bytes_per_padded_element(n_d, kernel):
     """Algorithmic HBM bytes per padded element of one launch (each byte crosses HBM once)."""
     if kernel == "fused":          # read N_d bf16 grads + master/m/v; write master/m/v + N_d bf16 replicas
         return 2 * n_d + 12 + 12 + 2 * n_d
+    if kernel == "fused_accumulate":   # the fused step forming each gradient from acc + micro: N_d more reads,
+        return 2 * n_d + 2 * n_d + 12 + 12 + 2 * n_d    # no gradient written
     if kernel == "unfused":        # RS (N_d reads, 1 write) + AdamW (2 + 12 read, 12 + 2 write) + AG (2 read, N_d writes)
         return (2 * n_d + 2) + (14 + 14) + (2 + 2 * n_d)
     raise ValueError(kernel)
@@ -499,8 +501,12 @@ class Workload:
             return bytes_per_padded_element(n_d, "fused") * P, walk
         if self.kind == "accumulate+fused":
             micro = self.wl["micro"]
-            acc = n_d * P * (4 + 6 * (micro - 1))       # first: read micro, write acc; then read both, write acc
-            return acc + bytes_per_padded_element(n_d, "fused") * P, micro + walk
+            if self.args.accumulate_mode == "separate":
+                acc = n_d * P * (4 + 6 * (micro - 1))   # first: read micro, write acc; then read both, write acc
+                return acc + bytes_per_padded_element(n_d, "fused") * P, micro + walk
+            # the last micro-batch inside the step: it reads acc and micro, writes no gradient
+            acc = n_d * P * (4 + 6 * (micro - 2))
+            return acc + bytes_per_padded_element(n_d, "fused_accumulate") * P, micro - 1 + walk
         # zero3: per unit two gathers (read shard, write N_d copies) + reduce-scatter with update
         return P * (2 * (2 + 2 * n_d) + (2 * n_d + 12 + 12 + 2)), 3 * self.plan.n_units
 
@@ -518,7 +524,10 @@ class Workload:
         if self.kind == "fused":
             return fused
         if self.kind == "accumulate+fused":
-            return "%d x k_accumulate + %s" % (self.wl["micro"], fused)
+            if self.args.accumulate_mode == "separate":
+                return "%d x k_accumulate + %s" % (self.wl["micro"], fused)
+            return "%d x k_accumulate + %s" % (self.wl["micro"] - 1, fused.replace("k_fused_tma<", "k_fused_tma_acc<")
+                                                .replace("k_fused<", "k_fused<acc "))
         return "2 x k_gather<%d> + %s per unit" % (self.n_d, fused)
 
     def step(self):
@@ -534,15 +543,32 @@ class Workload:
             zs.zs_fused_step(plan, -1, self.grads, zs.ZS_RANK_FULL, self.master, self.m, self.v, self.reps, hp, t,
                              stream=st)
         elif self.kind == "accumulate+fused":
-            micro = self.wl["micro"]
-            for j in range(micro):
-                zs.zs_accumulate_grad(plan, self.acc, self.grads, 1.0 / micro, first=(j == 0), stream=st)
-            zs.zs_fused_step(plan, -1, self.acc, zs.ZS_RANK_FULL, self.master, self.m, self.v, self.reps, hp, t,
-                             stream=st)
+            self.accumulate_step(t, st, self.args.accumulate_mode)
         else:
             ug = [self.ugrads] * plan.n_units
             zs.zs_zero3_step(plan, self.shards, self.master, self.m, self.v, ug, self.pool, True, hp, t,
                              main_stream=st, side_stream=self.side)
+
+
+    def accumulate_step(self, t, st, mode, events=None):
+        """The micro-batches accumulated and the step (config with micro > 1).  mode "fused-last": the
+        last micro-batch's accumulation inside the step (zs_fused_step_accumulate); "separate": every
+        micro-batch accumulated, then zs_fused_step.  events: recorded after every launch call."""
+        zs, plan, hp = self.zs, self.plan, self.hp
+        micro = self.wl["micro"]
+        n_acc = micro if mode == "separate" else micro - 1
+        for j in range(n_acc):
+            zs.zs_accumulate_grad(plan, self.acc, self.grads, 1.0 / micro, first=(j == 0), stream=st)
+            if events:
+                events[j].record(st)
+        if mode == "separate":
+            zs.zs_fused_step(plan, -1, self.acc, zs.ZS_RANK_FULL, self.master, self.m, self.v, self.reps, hp, t,
+                             stream=st)
+        else:
+            zs.zs_fused_step_accumulate(plan, -1, self.acc, self.grads, zs.ZS_RANK_FULL, 1.0 / micro, self.master,
+                                        self.m, self.v, self.reps, hp, t, stream=st)
+        if events:
+            events[n_acc].record(st)
 
 
 def timed_on_stream(torch, fn, steps, warmup, stream, dev, dist, status=None, where="a timed region"):
@@ -1051,31 +1077,39 @@ def run_ours(args, ws, rank, local):
     # the accumulate + fused step's launches timed one by one (not part of value)
     breakdown = None
     if W.kind == "accumulate+fused" and rank == 0:
+        # both forms of the step, alternately, each launch call timed (events after every call)
         micro = W.wl["micro"]
-        acc_ms, fused_ms = [[] for _ in range(micro)], []
-        for k in range(5):
-            W.t += 1
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(micro + 2)]
-            evs[0].record(stream)
-            for j in range(micro):
-                zs.zs_accumulate_grad(plan, W.acc, W.grads, 1.0 / micro, first=(j == 0), stream=stream)
-                evs[j + 1].record(stream)
-            zs.zs_fused_step(plan, -1, W.acc, zs.ZS_RANK_FULL, W.master, W.m, W.v, W.reps, W.hp, W.t, stream=stream)
-            evs[micro + 1].record(stream)
-            torch.cuda.synchronize(dev)
-            if k >= 2:
-                for j in range(micro):
-                    acc_ms[j].append(evs[j].elapsed_time(evs[j + 1]))
-                fused_ms.append(evs[micro].elapsed_time(evs[micro + 1]))
+        # per form: one list per launch call (index j), the whole step at index micro + 1
+        ms = {mode: [[] for _ in range(micro + 2)] for mode in ("fused-last", "separate")}
+        for k in range(12):
+            for mode in ("fused-last", "separate"):
+                W.t += 1
+                n_calls = micro if mode == "fused-last" else micro + 1
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 1)]
+                evs[0].record(stream)
+                W.accumulate_step(W.t, stream, mode, events=evs[1:])
+                torch.cuda.synchronize(dev)
+                if k >= 2:
+                    for j in range(n_calls):
+                        ms[mode][j].append(evs[j].elapsed_time(evs[j + 1]))
+                    ms[mode][micro + 1].append(evs[0].elapsed_time(evs[n_calls]))
 
-        def entry(ms, nbytes):
-            gbs = nbytes / (ms / 1e3) / 1e9
-            return {"ms": ms, "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak}
+        def entry(t_ms, nbytes):
+            gbs = nbytes / (t_ms / 1e3) / 1e9
+            return {"ms": t_ms, "algorithmic_bytes": nbytes, "gbs": gbs, "frac_of_peak": gbs / peak}
 
         status("the per-launch breakdown")
-        breakdown = {"accumulate_first": entry(statistics.mean(acc_ms[0]), 4 * n_d * P),
-                     "accumulate": entry(statistics.mean(statistics.mean(a) for a in acc_ms[1:]), 6 * n_d * P),
-                     "fused": entry(statistics.mean(fused_ms), bytes_per_padded_element(n_d, "fused") * P)}
+        fl, sp = ms["fused-last"], ms["separate"]
+        mean = statistics.mean
+        breakdown = {"accumulate_first": entry(mean(fl[0] + sp[0]), 4 * n_d * P),
+                     "accumulate": entry(mean([x for a in fl[1:micro - 1] + sp[1:micro] for x in a]), 6 * n_d * P),
+                     "fused_accumulate": entry(mean(fl[micro - 1]),
+                                               bytes_per_padded_element(n_d, "fused_accumulate") * P),
+                     "fused": entry(mean(sp[micro]), bytes_per_padded_element(n_d, "fused") * P),
+                     "step_fused_last_ms": mean(fl[micro + 1]),
+                     "step_separate_ms": mean(sp[micro + 1]),
+                     "timing": "launch calls timed one by one with events between them, after 2 untimed rounds; "
+                               "both forms alternate"}
 
     # the unfused path on the same buffers, for comparison (not part of value)
     unfused = None
@@ -1193,6 +1227,8 @@ def run_ours(args, ws, rank, local):
                        "fused_variant": args.fused_variant, "params": plan.numel,
                        "padded": P, "n_d": n_d, "stage": "zero%d" % W.wl["stage"],
                        "bucket_bytes": W.wl["bucket_bytes"], "step": W.kind, "step_mode": args.step_mode,
+                       **({"micro_batches": W.wl["micro"], "accumulate_mode": args.accumulate_mode}
+                          if W.kind == "accumulate+fused" else {}),
                        "storage": "bf16 params/grads, fp32 master/m/v",
                        "l2": "step moves %.0f GB >> 129 MB L2, no flush" % (algo_bytes / 1e9),
                        "parallelism": "replicas" if ws > 1 else "1 GPU, %d simulated ranks" % n_d},
@@ -1320,6 +1356,9 @@ def main():
                     help="fused workloads: one call over the whole flat space (default), or every bucket stepped "
                          "bucket by bucket, last first (one stream / two streams)")
     ap.add_argument("--bucket-bytes", type=int, default=None, help="override the workload's bucket size")
+    ap.add_argument("--accumulate-mode", choices=["fused-last", "separate"], default="fused-last",
+                    help="workloads with micro-batches: the last micro-batch's accumulation inside the step, or "
+                         "every micro-batch accumulated before it")
     ap.add_argument("--fused-variant", choices=["auto", "ldg", "tma"], default="auto",
                     help="kernel behind the fused step (all variants compute identical results)")
     args = ap.parse_args()

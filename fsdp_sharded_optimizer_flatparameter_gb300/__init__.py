@@ -81,6 +81,8 @@ _sig("zs_adamw_shard_step", [c_vp, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c
 _sig("zs_all_gather", [c_vp, c_vp, c_i32, c_vp, c_vp])
 _sig("zs_fused_step", [c_vp, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
                        ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
+_sig("zs_fused_step_accumulate", [c_vp, c_i32, c_vp, c_vp, c_i32, c_f32, c_vp, c_vp, c_vp, c_vp,
+                                  ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp])
 _sig("zs_fused_step_host", [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                             ctypes.POINTER(zs_adamw_hparams), c_i64, c_vp, c_vp])
 _sig("zs_zero3_gather_unit", [c_vp, c_i32, c_vp, c_vp, c_vp])
@@ -115,7 +117,7 @@ EXPORTED = [
     "zs_checkpoint_save", "zs_checkpoint_load", "zs_zero2_step_host_noalloc", "zs_all_reduce_mean",
     "zs_dp_step", "zs_plan_create_fsdp2", "zs_plan_layout", "zs_plan_param_rows", "zs_plan_pad_ranges",
     "zs_fsdp2_chunk_cat", "zs_fsdp2_copy_out", "zs_fused_step_buckets", "zs_set_dependent_launch",
-    "zs_rank_shard_step",
+    "zs_rank_shard_step", "zs_fused_step_accumulate",
 ]
 
 
@@ -400,6 +402,22 @@ def zs_fused_step(plan, bucket, grads, grads_kind, master, m, v, replicas, hp, s
     # gradients and replicas may be pinned host memory (read / written by the kernel over the host link)
     return _check(_lib.zs_fused_step(
         plan.handle, int(bucket), _ptr_array(grads, ng, 2, "grads", "pinned_ok"), int(grads_kind),
+        _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
+        _ptr_array(replicas, n, 2, "replicas", "pinned_ok"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
+
+
+def zs_fused_step_accumulate(plan, bucket, acc, micro, grads_kind, scale, master, m, v, replicas, hp, step,
+                             stream=None):
+    """zs_fused_step on the gradients bf16(acc[q] + micro[q] * scale): the last micro-batch's
+    accumulation inside the step (acc and micro are only read)."""
+    _n_ptrs(grads_kind, acc, plan.n_d, "acc")
+    _n_ptrs(grads_kind, micro, plan.n_d, "micro")
+    _n_ptrs(ZS_RANK_FULL, replicas, plan.n_d, "replicas")
+    n = plan.padded
+    ng = _bf16_elems(plan, grads_kind, bucket)
+    return _check(_lib.zs_fused_step_accumulate(
+        plan.handle, int(bucket), _ptr_array(acc, ng, 2, "acc", "pinned_ok"),
+        _ptr_array(micro, ng, 2, "micro", "pinned_ok"), int(grads_kind), float(scale),
         _addr(master, n, 4, "master"), _addr(m, n, 4, "m"), _addr(v, n, 4, "v"),
         _ptr_array(replicas, n, 2, "replicas", "pinned_ok"), ctypes.byref(_hp(hp)), int(step), _stream(stream)))
 

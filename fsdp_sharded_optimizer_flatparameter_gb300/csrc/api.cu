@@ -255,6 +255,43 @@ extern "C" int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* 
                         as_stream(stream));
 }
 
+extern "C" int zs_fused_step_accumulate(zs_plan_t plan, int32_t bucket, const void* const* acc,
+                                        const void* const* micro, int32_t grads_kind, float scale, float* master,
+                                        float* m, float* v, void* const* replicas, const zs_adamw_hparams* hp,
+                                        int64_t step, void* stream) {
+    static const char* fn = "zs_fused_step_accumulate";
+    zs::TraceRange trace_(fn);
+    zs::clear_error();
+    ZS_TRY(check_plan(fn, plan));
+    ZS_TRY(check_bucket(fn, plan, bucket, true));
+    if (grads_kind != ZS_RANK_FULL && grads_kind != ZS_RANK_BUCKET) return fail(fn, "grads_kind must be RANK_FULL or RANK_BUCKET");
+    if (grads_kind == ZS_RANK_BUCKET && bucket < 0) return fail(fn, "RANK_BUCKET gradients need a bucket index");
+    if (!std::isfinite(scale)) return fail(fn, "scale must be finite");
+    const int nd = plan->n_d;
+    ZS_TRY(check_one(fn, "master", master));
+    ZS_TRY(check_one(fn, "m", m));
+    ZS_TRY(check_one(fn, "v", v));
+    zs::AdamScalars s;
+    ZS_TRY(check_hp(fn, hp, step, &s));
+    const int64_t bbeg = bucket >= 0 ? plan->buckets[bucket].begin : 0;
+    BView a, o;
+    zs::AccumIn in;
+    in.scale = scale;
+    ZS_TRY(make_view(fn, "acc", acc, grads_kind, nd, bbeg, 0, &a));
+    ZS_TRY(make_view(fn, "micro", micro, grads_kind, nd, bbeg, 0, &in.micro));
+    ZS_TRY(make_view(fn, "replicas", (const void* const*)replicas, ZS_RANK_FULL, nd, 0, 0, &o));
+    for (int q = 0; q < nd; ++q)
+        for (int j = 0; j < nd; ++j)
+            if (replicas[q] == acc[j] || replicas[q] == micro[j])
+                return fail(fn, "replicas must not be the accumulator or micro-batch buffers");
+    Range r = bucket >= 0 ? Range{plan->buckets[bucket].begin, plan->buckets[bucket].end, 0, 1}
+                          : Range{0, plan->padded, 0, 1};
+    if (r.hi <= r.lo) return ZS_OK;
+    // walked like zs_fused_step; pinned host buffers keep to the streaming kernel
+    return cuda_status(fn, zs::launch_fused_walk(a, master, m, v, o, {r}, s, nd, as_stream(stream),
+                                                 zs::kStagedIfDevice, &in));
+}
+
 extern "C" int zs_fused_step_buckets(zs_plan_t plan, int32_t n_buckets, const int32_t* buckets,
                                      const void* const* grads, float* master, float* m, float* v,
                                      void* const* replicas, const zs_adamw_hparams* hp, int64_t step,

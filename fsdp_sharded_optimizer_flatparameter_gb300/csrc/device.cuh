@@ -113,6 +113,13 @@ __device__ __forceinline__ float mean_of_sum(float sum, int nd, float inv_nd) {
     }
 }
 
+// Gradient accumulation of one element: the running sum plus the micro-batch's gradient times the
+// scale, each operation rounded in fp32 ("Infra: Data Parallel", gradient accumulation); the caller
+// stores the result as bf16 (or, folded into a step, rounds it to bf16 before use).
+__device__ __forceinline__ float accumulate_elem(float acc, float micro, float scale) {
+    return __fadd_rn(acc, __fmul_rn(micro, scale));
+}
+
 // AdamW on one element (decoupled weight decay, bias corrections folded into
 // step_size and sqrt_bc2); g is the fp32 value of the bf16 reduced gradient.
 __device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v, const AdamScalars& s) {

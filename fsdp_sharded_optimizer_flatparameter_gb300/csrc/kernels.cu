@@ -128,7 +128,7 @@ struct AccumOp {
             unpack(ld_bf<VEC>(acc + i), prev);
         }
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) prev[k] = __fadd_rn(prev[k], __fmul_rn(g[k], scale));
+        for (int k = 0; k < VEC; ++k) prev[k] = accumulate_elem(prev[k], g[k], scale);
         st_bf<VEC>(acc + i, pack(prev));
     }
 };
@@ -253,8 +253,18 @@ static cudaError_t gather_impl(const BView& src, bool src_by_owner, const BView&
 
 // ------------------------------------------------------------------ fused: reduce-mean + AdamW + scatter
 
-template <int ND, bool BROADCAST>
-struct FusedOp {
+// The micro-batch operand of the accumulating form (ACC): present only there, so the plain form's
+// kernel parameter stays as small as before.
+template <bool ACC>
+struct FusedMicro {};
+template <>
+struct FusedMicro<true> {
+    BView micro;
+    float scale;
+};
+
+template <int ND, bool BROADCAST, bool ACC = false>
+struct FusedOp : FusedMicro<ACC> {
     BView g, out;
     float *master, *m, *v;
     AdamScalars s;
@@ -270,6 +280,15 @@ struct FusedOp {
         for (int q = 0; q < n; ++q) {
             float f[VEC];
             unpack(ld_bf<VEC>(g.ptr.p[q] + (i - g.off)), f);
+            if constexpr (ACC) {
+                // rank q's gradient: its accumulator plus the last micro-batch, rounded to bf16 as the
+                // accumulation stores it
+                float b[VEC];
+                unpack(ld_bf<VEC>(this->micro.ptr.p[q] + (i - this->micro.off)), b);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) f[k] = accumulate_elem(f[k], b[k], this->scale);
+                unpack(pack(f), f);
+            }
 #pragma unroll
             for (int k = 0; k < VEC; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
         }
@@ -297,17 +316,29 @@ struct FusedOp {
     }
 };
 
-template <int ND, bool BROADCAST>
-__global__ void __launch_bounds__(kThreads) k_fused(FusedOp<ND, BROADCAST> op, Split sp) { for_range(sp, op); }
+template <int ND, bool BROADCAST, bool ACC>
+__global__ void __launch_bounds__(kThreads) k_fused(FusedOp<ND, BROADCAST, ACC> op, Split sp) { for_range(sp, op); }
 
-template <int ND, bool BROADCAST>
+template <int ND, bool BROADCAST, bool ACC = false>
 static cudaError_t fused_impl(const BView& g, float* master, float* m, float* v, const BView& out,
-                              const AdamScalars& s, int nd, Split sp, cudaStream_t st) {
-    FusedOp<ND, BROADCAST> op{g, out, master, m, v, s, nd, 1.0f / (float)nd};
+                              const AdamScalars& s, int nd, Split sp, cudaStream_t st, const AccumIn* acc = nullptr) {
+    FusedOp<ND, BROADCAST, ACC> op;
+    op.g = g;
+    op.out = out;
+    op.master = master;
+    op.m = m;
+    op.v = v;
+    op.s = s;
+    op.nd = nd;
+    op.inv_nd = 1.0f / (float)nd;
+    if constexpr (ACC) {
+        op.micro = acc->micro;
+        op.scale = acc->scale;
+    }
     int grid = 0;
-    cudaError_t ge = grid_for((const void*)k_fused<ND, BROADCAST>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
+    cudaError_t ge = grid_for((const void*)k_fused<ND, BROADCAST, ACC>, sp.nvec > 0 ? sp.nvec : sp.hi - sp.lo, &grid);
     if (ge != cudaSuccess) return ge;
-    return launch_kernel(k_fused<ND, BROADCAST>, dim3(grid), dim3(kThreads), 0, st, op, sp);
+    return launch_kernel(k_fused<ND, BROADCAST, ACC>, dim3(grid), dim3(kThreads), 0, st, op, sp);
 }
 
 // ------------------------------------------------------------------ dispatch
@@ -448,7 +479,14 @@ void set_dependent_launch(int on) { g_dependent_launch.store(on ? 1 : 0); }
 int dependent_launch() { return g_dependent_launch.load(); }
 
 static cudaError_t launch_fused_ldg(const BView& g, float* master, float* m, float* v, const BView& out,
-                                    bool broadcast, const Split& sp, const AdamScalars& s, int nd, cudaStream_t st) {
+                                    bool broadcast, const Split& sp, const AdamScalars& s, int nd, cudaStream_t st,
+                                    const AccumIn* acc = nullptr) {
+    if (acc) {
+        if (!broadcast) return cudaErrorNotSupported;
+#define ZS_FA(N) fused_impl<N, true, true>(g, master, m, v, out, s, nd, sp, st, acc)
+        ZS_DISPATCH_ND(nd, ZS_FA)
+#undef ZS_FA
+    }
     if (broadcast) {
 #define ZS_FB(N) fused_impl<N, true>(g, master, m, v, out, s, nd, sp, st)
         ZS_DISPATCH_ND(nd, ZS_FB)
@@ -476,10 +514,12 @@ static bool all_device(const void* const* ps, int n) {
 }
 
 bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                          int nd) {
-    const void* ps[2 * ZS_MAX_RANKS + 3];
+                          int nd, const AccumIn* acc) {
+    const void* ps[3 * ZS_MAX_RANKS + 3];
     int n = 0;
     for (int q = 0; q < nd; ++q) ps[n++] = g.ptr.p[q];
+    if (acc)
+        for (int q = 0; q < nd; ++q) ps[n++] = acc->micro.ptr.p[q];
     for (int q = 0; q < (broadcast ? nd : 1); ++q) ps[n++] = out.ptr.p[q];
     ps[n++] = master;
     ps[n++] = m;
@@ -489,43 +529,46 @@ bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, con
 
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                          const Range& r, const AdamScalars& s, int nd, cudaStream_t st, StagedPolicy staged_policy,
-                         int sync) {
-    const bool vec = aligned8(g.off) && aligned8(out.off);
+                         int sync, const AccumIn* acc) {
+    if (acc && !broadcast) return cudaErrorNotSupported;
+    const bool vec = aligned8(g.off) && aligned8(out.off) && (!acc || aligned8(acc->micro.off));
     Split sp = split_range(r.lo, r.hi, vec);
     const int variant = g_fused_variant.load();
     const int64_t min_staged = sync == kSyncStream ? kTmaMinElems : kTmaWalkMinElems;
     const bool want_tma = variant == ZS_FUSED_TMA || (variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= min_staged);
     bool staged = want_tma && sp.nvec > 0 && staged_policy != kStagedNever &&
-                  (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32);
+                  (acc ? fused_walk_shape(nd, true) : (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32));
     // only a staged candidate pays for the pointer queries, and only when the caller has not
-    if (staged && staged_policy == kStagedIfDevice) staged = fused_ptrs_on_device(g, master, m, v, out, broadcast, nd);
+    if (staged && staged_policy == kStagedIfDevice)
+        staged = fused_ptrs_on_device(g, master, m, v, out, broadcast, nd, acc);
     if (!staged) {
         // the streaming kernel reads through L1, so it never starts before its predecessor completes
         sp.sync = sync == kSyncWalkFirst ? kSyncWalkFirst : kSyncStream;
-        return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st);
+        return launch_fused_ldg(g, master, m, v, out, broadcast, sp, s, nd, st, acc);
     }
     // staged body, then the at most 14 fringe elements one by one
     const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-    cudaError_t e = launch_fused_tma(g, master, m, v, out, broadcast, sp.vlo, sp.nvec << 3, s, nd, st, sync);
+    cudaError_t e = launch_fused_tma(g, master, m, v, out, broadcast, sp.vlo, sp.nvec << 3, s, nd, st, sync, acc);
     if (e != cudaSuccess) return e;
     if (sp.vlo > sp.lo) {
-        e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(sp.lo, sp.vlo, false), s, nd, st);
+        e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(sp.lo, sp.vlo, false), s, nd, st, acc);
         if (e != cudaSuccess) return e;
     }
-    if (sp.hi > body_hi) e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(body_hi, sp.hi, false), s, nd, st);
+    if (sp.hi > body_hi)
+        e = launch_fused_ldg(g, master, m, v, out, broadcast, split_range(body_hi, sp.hi, false), s, nd, st, acc);
     return e;
 }
 
 cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v, const BView& out,
                               const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
-                              StagedPolicy staged_policy) {
+                              StagedPolicy staged_policy, const AccumIn* acc) {
     // Cut points are multiples of the chunk (8-aligned, so a range's pieces keep its own fringes
     // only), none closer than a quarter chunk to a range end, so no piece is a sliver.  Only staged
     // launches overlap: buffers the staged kernel may not touch (pinned host memory) or the streaming
     // variant leave every range whole.
     if (staged_policy == kStagedIfDevice)
-        staged_policy = fused_ptrs_on_device(g, master, m, v, out, true, nd) ? kStagedDeviceKnown : kStagedNever;
-    const bool chunked = fused_walk_shape(nd) && staged_policy != kStagedNever &&
+        staged_policy = fused_ptrs_on_device(g, master, m, v, out, true, nd, acc) ? kStagedDeviceKnown : kStagedNever;
+    const bool chunked = fused_walk_shape(nd, acc != nullptr) && staged_policy != kStagedNever &&
                          g_fused_variant.load() != ZS_FUSED_LDG;
     constexpr int64_t C = kFusedWalkChunk;
     bool first = true;
@@ -538,7 +581,7 @@ cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v,
                 if (cut < r.hi - C / 4) hi = cut;
             }
             const cudaError_t e = launch_fused(g, master, m, v, out, true, {lo, hi, r.base, r.shard}, s, nd, st,
-                                               staged_policy, first ? kSyncWalkFirst : kSyncWalkNext);
+                                               staged_policy, first ? kSyncWalkFirst : kSyncWalkNext, acc);
             if (e != cudaSuccess) return e;
             first = false;
             lo = hi;

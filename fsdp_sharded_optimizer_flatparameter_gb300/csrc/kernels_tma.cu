@@ -218,6 +218,15 @@ struct TmaArgs {
     int sync;             // LaunchSync: order against the previous kernel on the stream
 };
 
+// The fused step with the last micro-batch's accumulation folded in (AccumIn): `a.g` holds the
+// accumulators, `micro` the micro-batch gradients; rank q's gradient is bf16(acc_q + micro_q * scale).
+struct TmaAccArgs {
+    TmaArgs a;
+    Ptrs micro;           // element i of rank q at micro.p[q] + (i - micro_off); lo - micro_off a multiple of 8
+    int64_t micro_off;
+    float scale;
+};
+
 // A list of bodies stepped by one launch (the buckets of one call, in the caller's order): body r
 // is [lo[r], lo[r] + n[r]) with the same alignment rules as TmaArgs' body, and first[r] is the
 // number of tiles of the bodies before it (first[nr] = all tiles).  The kernel walks the
@@ -273,9 +282,12 @@ struct TmaShape {
     static_assert(2 * kStages * 8 <= 256, "barriers must fit in the first 256 bytes");
 };
 
-template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET>
-__device__ __forceinline__ void fused_tma_body(const TmaArgs& a) {
-    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
+// ACC: every rank's gradient tile is formed from two staged tiles, its accumulator (a.g) and the
+// last micro-batch (micro), so a stage holds 2 N_d bf16 tiles ahead of the fp32 state.
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET, bool ACC = false>
+__device__ __forceinline__ void fused_tma_body(const TmaArgs& a, const Ptrs& micro, int64_t micro_off, float scale) {
+    constexpr int NG = ACC ? 2 * ND : ND;                 // bf16 tiles per stage
+    using Sh = TmaShape<NG, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -313,11 +325,16 @@ __device__ __forceinline__ void fused_tma_body(const TmaArgs& a) {
                 const int64_t rem = a.n - tile * T;
                 const uint32_t len = (uint32_t)(rem < T ? rem : T);
                 uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
-                mbar_expect_tx(&full[s], len * (2u * ND + 12u));
+                mbar_expect_tx(&full[s], len * (2u * NG + 12u));
 #pragma unroll
                 for (int q = 0; q < ND; ++q)
                     bulk_load(st + (size_t)q * T * 2, a.g.p[q] + (i0 - a.g_off), len * 2u, &full[s], pol);
-                float* sf = reinterpret_cast<float*>(st + (size_t)ND * T * 2);
+                if constexpr (ACC) {
+#pragma unroll
+                    for (int q = 0; q < ND; ++q)
+                        bulk_load(st + (size_t)(ND + q) * T * 2, micro.p[q] + (i0 - micro_off), len * 2u, &full[s], pol);
+                }
+                float* sf = reinterpret_cast<float*>(st + (size_t)NG * T * 2);
                 bulk_load(sf, a.master + i0, len * 4u, &full[s], pol);
                 bulk_load(sf + T, a.m + i0, len * 4u, &full[s], pol);
                 bulk_load(sf + 2 * T, a.v + i0, len * 4u, &full[s], pol);
@@ -349,7 +366,7 @@ __device__ __forceinline__ void fused_tma_body(const TmaArgs& a) {
         if (e < len) {
             const uint8_t* st = stages + (size_t)s * Sh::kStageBytes;
             const uint16_t* sg = reinterpret_cast<const uint16_t*>(st);
-            const float* sf = reinterpret_cast<const float*>(st + (size_t)ND * T * 2);
+            const float* sf = reinterpret_cast<const float*>(st + (size_t)NG * T * 2);
             float acc[VPT];
 #pragma unroll
             for (int k = 0; k < VPT; ++k) acc[k] = 0.0f;
@@ -357,6 +374,13 @@ __device__ __forceinline__ void fused_tma_body(const TmaArgs& a) {
             for (int q = 0; q < n; ++q) {
                 float f[VPT];
                 lds_bf<VPT>(sg + (size_t)q * T + e, f);
+                if constexpr (ACC) {
+                    // rank q's gradient: accumulator plus micro-batch, rounded to bf16 as stored
+                    float b[VPT];
+                    lds_bf<VPT>(sg + (size_t)(ND + q) * T + e, b);
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) f[k] = bf16_to_f32(f32_to_bf16(accumulate_elem(f[k], b[k], scale)));
+                }
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) acc[k] = __fadd_rn(acc[k], f[k]);
             }
@@ -412,8 +436,16 @@ __device__ __forceinline__ void fused_tma_body(const TmaArgs& a) {
 template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST = 16, int BUDGET = 227 * 1024>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_constant__ TmaArgs a) {
     dependent_launch_prologue(a.sync);
-    fused_tma_body<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>(a);
+    fused_tma_body<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>(a, a.g, 0, 0.0f);
     dependent_launch_epilogue(a.sync);
+}
+
+// The broadcast step with the last micro-batch's accumulation folded in (TmaAccArgs).
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_acc(const __grid_constant__ TmaAccArgs x) {
+    dependent_launch_prologue(x.a.sync);
+    fused_tma_body<ND, NCW, VPT, true, MAXST, BUDGET, true>(x.a, x.micro, x.micro_off, x.scale);
+    dependent_launch_epilogue(x.a.sync);
 }
 
 // The broadcast step over a list of disjoint bodies in one launch (bodies that touch are merged
@@ -662,6 +694,12 @@ auto pick_kernel(const TmaListArgs*) {
     return k_fused_tma_list<ND, NCW, VPT, MAXST, BUDGET>;
 }
 int64_t host_tiles(const TmaListArgs& l, int) { return l.total_tiles; }
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET>
+auto pick_kernel(const TmaAccArgs*) {
+    static_assert(BROADCAST, "the accumulating step has the broadcast form only");
+    return k_fused_tma_acc<ND, NCW, VPT, MAXST, BUDGET>;
+}
+int64_t host_tiles(const TmaAccArgs& x, int T) { return (x.a.n + T - 1) / T; }
 
 // walk: a launch of a walk over disjoint ranges whose CTAs leave room for the next launch's.  A body
 // of at most one tile per resident CTA then takes one CTA per SM, so the next launch of the walk
@@ -670,7 +708,7 @@ int64_t host_tiles(const TmaListArgs& l, int) { return l.total_tiles; }
 // fill every slot.
 template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET, class Args>
 cudaError_t tma_impl(const Args& a, cudaStream_t st, bool walk = false) {
-    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
+    using Sh = TmaShape<std::is_same<Args, TmaAccArgs>::value ? 2 * ND : ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int kSmem = Sh::kSmem + (std::is_same<Args, TmaListArgs>::value ? kListTableBytes : 0);
     static_assert(kSmem <= 232448, "shared memory above the per-CTA limit");
     auto kern = pick_kernel<ND, NCW, VPT, BROADCAST, MAXST, BUDGET>(static_cast<const Args*>(nullptr));
@@ -758,6 +796,22 @@ cudaError_t with_walk_shape(int nd, F&& f) {
     }
 }
 
+// The walk shapes of the accumulating step (k_fused_tma_acc): a stage holds 2 N_d bf16 tiles, so
+// each rank count takes the tile of the plain walk shape with twice its rank count (two-stage ring
+// under half an SM's shared memory): N_d = 2, 4: 8 warps x 8 (T 2048); 8: 8 x 4 (T 1024); 16: 4 x 4
+// (T 512); 32: 2 x 4 (T 256).
+template <class F>
+cudaError_t with_acc_walk_shape(int nd, F&& f) {
+    switch (nd) {
+        case 2: return f(IC<2>{}, IC<8>{}, IC<8>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        case 4: return f(IC<4>{}, IC<8>{}, IC<8>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        case 8: return f(IC<8>{}, IC<8>{}, IC<4>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        case 16: return f(IC<16>{}, IC<4>{}, IC<4>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        case 32: return f(IC<32>{}, IC<2>{}, IC<4>{}, BC<true>{}, IC<2>{}, IC<115712>{});
+        default: return cudaErrorNotSupported;
+    }
+}
+
 TmaArgs make_args(const BView& g, float* master, float* m, float* v, const BView& out, const AdamScalars& s,
                   int nd) {
     TmaArgs a;
@@ -783,15 +837,31 @@ TmaArgs make_args(const BView& g, float* master, float* m, float* v, const BView
 
 // Returns cudaErrorNotSupported when no staged variant exists for this rank count.
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
-                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st, int sync) {
+                             int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st, int sync,
+                             const AccumIn* acc) {
+    if (acc && !broadcast) return cudaErrorNotSupported;
     bool ok = body_ok(lo, n) && at_ok(master, lo) && at_ok(m, lo) && at_ok(v, lo);
     for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off);
     for (int q = 0; q < (broadcast ? nd : 1) && ok; ++q) ok = at_ok(out.ptr.p[q], lo - out.off);
+    for (int q = 0; acc && q < nd && ok; ++q) ok = at_ok(acc->micro.ptr.p[q], lo - acc->micro.off);
     if (!ok) return cudaErrorMisalignedAddress;
     TmaArgs a = make_args(g, master, m, v, out, s, nd);
     a.lo = lo;
     a.n = n;
     a.sync = sync;
+    if (acc) {
+        TmaAccArgs x;
+        x.a = a;
+        x.micro = acc->micro.ptr;
+        x.micro_off = acc->micro.off;
+        x.scale = acc->scale;
+        // one shape per rank count, walked or not: a single launch of it over a whole range runs one
+        // wave of resident CTAs
+        return with_acc_walk_shape(nd, [&](auto ND, auto NCW, auto VPT, auto BR, auto MS, auto BU) {
+            return tma_impl<decltype(ND)::value, decltype(NCW)::value, decltype(VPT)::value, decltype(BR)::value,
+                            decltype(MS)::value, decltype(BU)::value>(x, st, sync != kSyncStream);
+        });
+    }
     if (broadcast && sync != kSyncStream && fused_walk_shape(nd)) {
         return with_walk_shape(nd, [&](auto ND, auto NCW, auto VPT, auto BR, auto MS, auto BU) {
             return tma_impl<decltype(ND)::value, decltype(NCW)::value, decltype(VPT)::value, decltype(BR)::value,
@@ -804,7 +874,9 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
     });
 }
 
-bool fused_walk_shape(int nd) { return nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32; }
+bool fused_walk_shape(int nd, bool /*acc: the same rank counts*/) {
+    return nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32;
+}
 
 namespace {
 

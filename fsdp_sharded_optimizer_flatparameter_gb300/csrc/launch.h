@@ -58,8 +58,17 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
                          cudaStream_t st);
 cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
                           const Range& r, int nd, cudaStream_t st);
+// The last micro-batch's accumulation folded into the broadcast fused step: rank q's gradient is
+// bf16(acc_q[i] + micro_q[i] * scale) (the accumulation rule, computed in the kernel and not stored),
+// where the fused launch's gradient view holds the accumulators acc_q and `micro` the micro-batch.
+struct AccumIn {
+    BView micro;
+    float scale;
+};
+
 // The fused step over r.  The staged kernel runs only for the 8-aligned body of a range of a
 // supported rank count whose buffers are all device memory; elsewhere the register-streaming kernel.
+// With `acc` (broadcast only) the gradients are formed from accumulators and a micro-batch.
 // Which fused kernel a launch may use.  kStagedIfDevice asks the runtime about every pointer;
 // kStagedDeviceKnown is for callers that already did (fused_ptrs_on_device) for the same pointers.
 enum StagedPolicy { kStagedNever = 0, kStagedIfDevice = 1, kStagedDeviceKnown = 2 };
@@ -68,13 +77,15 @@ enum StagedPolicy { kStagedNever = 0, kStagedIfDevice = 1, kStagedDeviceKnown = 
 // takes the staged kernel for bodies down to kTmaWalkMinElems.
 cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                          const Range& r, const AdamScalars& s, int nd, cudaStream_t st,
-                         StagedPolicy staged_policy = kStagedIfDevice, int sync = kSyncStream);
+                         StagedPolicy staged_policy = kStagedIfDevice, int sync = kSyncStream,
+                         const AccumIn* acc = nullptr);
 // True when every pointer a fused launch over these views touches is device memory.
-bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast, int nd);
+bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast, int nd,
+                          const AccumIn* acc = nullptr);
 
 // Whether the broadcast staged kernel has a walk shape for this rank count: a shape whose launches
 // share each SM with the next launch of a walk, for kSyncWalkFirst / kSyncWalkNext launches.
-bool fused_walk_shape(int nd);
+bool fused_walk_shape(int nd, bool acc = false);
 // The broadcast fused step over disjoint ranges as a walk: ranges longer than kFusedWalkChunk are cut
 // at multiples of it, each piece is one launch, the first on the stream kSyncWalkFirst and the others
 // kSyncWalkNext, so every launch streams its piece while the previous one drains.  Without a walk
@@ -82,12 +93,12 @@ bool fused_walk_shape(int nd);
 constexpr int64_t kFusedWalkChunk = int64_t(1) << 22;
 cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v, const BView& out,
                               const std::vector<Range>& ranges, const AdamScalars& s, int nd, cudaStream_t st,
-                              StagedPolicy staged_policy);
+                              StagedPolicy staged_policy, const AccumIn* acc = nullptr);
 // Bulk-copy staged fused kernel over the 8-aligned body [lo, lo + n); returns
 // cudaErrorNotSupported when no staged variant exists for this rank count.
 cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, const BView& out, bool broadcast,
                              int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st,
-                             int sync = kSyncStream);
+                             int sync = kSyncStream, const AccumIn* acc = nullptr);
 // The broadcast staged kernel over a list of bodies ([lo, lo + n): the TMA alignment rules of
 // launch_fused_tma for each) in one launch per kTmaListMax (128) bodies, tiles walked in list order.
 cudaError_t launch_fused_tma_list(const BView& g, float* master, float* m, float* v, const BView& out,

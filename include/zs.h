@@ -353,6 +353,31 @@ int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int3
                   float* master, float* m, float* v, void* const* replicas,
                   const zs_adamw_hparams* hp, int64_t step, void* stream);
 
+/* zs_fused_step with the last micro-batch's gradient accumulation done inside
+ * the step ("Infra: Data Parallel", section "Naive Data Parallelism",
+ * gradient-accumulation paragraph: the micro-batch gradients are summed, each
+ * scaled, before the data-parallel reduction; ZeRO section for the rest).  For every element i of the range and
+ * every rank q, rank q's gradient is
+ *     g_q[i] = bf16( fp32(acc[q][i]) + fp32(micro[q][i]) * scale )
+ * - exactly what zs_accumulate_grad(acc, micro, scale, first = 0) would store -
+ * and the step then runs on g_q as zs_fused_step does.  The results (master, m,
+ * v, replicas) are bit-identical to zs_accumulate_grad followed by
+ * zs_fused_step on acc; acc and micro are only read (the accumulated gradient is
+ * consumed by the step, not stored), which saves writing and re-reading it:
+ * 24 + 6 N_d bytes per element against 24 + 10 N_d for the two calls.
+ *   acc, micro  N_d pointers each, both of kind grads_kind (ZS_RANK_FULL, or
+ *               ZS_RANK_BUCKET with bucket >= 0); acc holds the earlier
+ *               micro-batches' sum (zs_accumulate_grad), micro the last
+ *               micro-batch's gradients; either may be pinned host memory (the
+ *               streaming kernel then runs, as in zs_fused_step).
+ *   scale       finite; 1/n_micro for n_micro equal micro-batches.
+ *   bucket, master, m, v, replicas, hp, step as in zs_fused_step; replicas must
+ *               not overlap acc or micro.  Walked as zs_fused_step.
+ * Errors: ZS_ERR_INVALID (nothing enqueued), ZS_ERR_CUDA. */
+int zs_fused_step_accumulate(zs_plan_t plan, int32_t bucket, const void* const* acc, const void* const* micro,
+                             int32_t grads_kind, float scale, float* master, float* m, float* v,
+                             void* const* replicas, const zs_adamw_hparams* hp, int64_t step, void* stream);
+
 /* zs_fused_step for a list of buckets (ZS_RANK_FULL gradients) in the order
  * given - e.g. the buckets whose gradients became ready together, last layer
  * first.  Same results as calling zs_fused_step once per bucket, with the

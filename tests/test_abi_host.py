@@ -188,6 +188,26 @@ def test_device_calls_reject_bad_arguments_before_launch():
     assert lib.zs_fused_step(None, -1, arr(good), 0, None, None, None, arr(reps), ctypes.byref(hp),
                              ctypes.c_int64(1), None) == zs.ZS_ERR_INVALID
 
+    # the accumulating step: the same checks plus its own operands
+    lib.zs_fused_step_accumulate.restype = ctypes.c_int32
+    micro = [0x200000 * (q + 1) for q in range(4)]
+
+    def fused_acc(acc, mic, replicas, scale=0.25, kind=zs.ZS_RANK_FULL, bucket=-1, step=1):
+        return lib.zs_fused_step_accumulate(p.handle, ctypes.c_int32(bucket), arr(acc), arr(mic), ctypes.c_int32(kind),
+                                            ctypes.c_float(scale), ctypes.c_void_p(0x90000), ctypes.c_void_p(0xA0000),
+                                            ctypes.c_void_p(0xB0000), arr(replicas), ctypes.byref(hp),
+                                            ctypes.c_int64(step), ctypes.c_void_p(0))
+
+    assert fused_acc(good, [micro[0], 0] + micro[2:], reps) == zs.ZS_ERR_INVALID    # missing micro rank
+    assert "micro" in zs.zs_last_error()
+    assert fused_acc(good, [micro[0] + 8] + micro[1:], reps) == zs.ZS_ERR_INVALID   # misaligned micro
+    assert fused_acc(good, micro, reps, scale=float("nan")) == zs.ZS_ERR_INVALID    # scale not finite
+    assert fused_acc(good, micro, micro) == zs.ZS_ERR_INVALID                       # replicas alias micro
+    assert fused_acc(good, micro, good) == zs.ZS_ERR_INVALID                        # replicas alias acc
+    assert fused_acc(good, micro, reps, kind=zs.ZS_RANK_BUCKET) == zs.ZS_ERR_INVALID
+    assert fused_acc(good, micro, reps, step=0) == zs.ZS_ERR_INVALID
+    assert fused_acc(good, micro, reps, bucket=3) == zs.ZS_ERR_INVALID              # no such bucket
+
 
 def test_list_zero3_and_dp_calls_reject_bad_arguments_before_launch():
     """The bucket-list, ZeRO-3 and naive-DP entry points refuse bad arguments with ZS_ERR_INVALID before

@@ -11,8 +11,9 @@ every element of every output is compared with the oracle, bit for bit:
 * the whole Llama-7B ZeRO-3 step at N_d = 16 (zs_zero3_step, both streams,
   the 2-slot pool), at step 2, on its largest unit (the root unit: embedding,
   final norm and output, 262,148,096 elements) with the parameter shards;
-* the GPT-2-small step with four accumulated micro-batches at N_d = 8 (every
-  accumulated gradient too);
+* the GPT-2-small step with four micro-batches at N_d = 8, the last one
+  accumulated inside the step (as benchmarked) and all four before it (every
+  stored accumulated gradient too);
 * the 2^28+7-element flat buffer at N_d = 32 (padding, the widest rank count);
 * a flat buffer past 2^32 elements at N_d = 2 (element offsets, tile counts
   and walk pieces that overflow 32-bit integers): the walked fused step
@@ -168,9 +169,13 @@ def test_llama7b_zero3_step_root_unit_every_element():
     _verify(up, job, "Llama-7B ZeRO-3 step, N_d=16, root unit")
 
 
-def test_gpt2_small_accumulate_and_step_every_element():
-    """GPT-2-small, N_d = 8: four micro-batches accumulated with the 1/4 loss scale, then the walked
-    fused step; every accumulated gradient and every output element against the oracle."""
+@pytest.mark.parametrize("mode", ["fused-last", "separate"])
+def test_gpt2_small_accumulate_and_step_every_element(mode):
+    """GPT-2-small, N_d = 8, four micro-batches with the 1/4 loss scale, as the benchmark steps them:
+    "fused-last" accumulates three with zs_accumulate_grad and hands the fourth to
+    zs_fused_step_accumulate (the benchmark's default); "separate" accumulates all four, then the
+    walked zs_fused_step.  Every stored accumulated gradient and every output element against the
+    oracle."""
     wl = synth.WORKLOADS["gpt2-small-zero1"]
     shapes, _ = synth.workload_params(wl["model"])
     n_d, micro_n = wl["n_d"], wl["micro"]
@@ -178,16 +183,22 @@ def test_gpt2_small_accumulate_and_step_every_element():
     P, pads = plan.padded, plan.pad_ranges()
     acc, _ = synth.rank_buffers(n_d, P, BF16, DEV)
     micro = [synth.rank_buffers(n_d, P, BF16, DEV)[0] for _ in range(micro_n)]
+    stored = micro_n if mode == "separate" else micro_n - 1        # micro-batches accumulated into acc
     for j in range(micro_n):
         synth.fill_grads(micro[j], pads, wl["seed"], 100 + j, wl["sigma"])
-        zs.zs_accumulate_grad(plan, acc, micro[j], 1.0 / micro_n, first=(j == 0))
+        if j < stored:
+            zs.zs_accumulate_grad(plan, acc, micro[j], 1.0 / micro_n, first=(j == 0))
     master = synth.master_init(P, pads, wl["seed"], device=DEV)
     m, v = torch.zeros_like(master), torch.zeros_like(master)
     reps, _ = synth.rank_buffers(n_d, P, BF16, DEV)
     torch.cuda.synchronize()
     p0 = _f32(master)
     zs.zs_device_status(clear=True)
-    zs.zs_fused_step(plan, -1, acc, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    if mode == "separate":
+        zs.zs_fused_step(plan, -1, acc, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    else:
+        zs.zs_fused_step_accumulate(plan, -1, acc, micro[-1], zs.ZS_RANK_FULL, 1.0 / micro_n, master, m, v, reps,
+                                    HP, 1)
     torch.cuda.synchronize()
     assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
 
@@ -198,9 +209,10 @@ def test_gpt2_small_accumulate_and_step_every_element():
             a = None
             for j in range(micro_n):
                 a = steps.accumulate(a, _bits16(micro[j][q][lo:hi]), 1.0 / micro_n, first=(j == 0))
-            d = _first_diff(_bits16(acc[q][lo:hi]), a)
-            if d:
-                out.append(("accumulated gradient of rank %d" % q,) + d)
+                if j == stored - 1:
+                    d = _first_diff(_bits16(acc[q][lo:hi]), a)
+                    if d:
+                        out.append(("accumulated gradient of rank %d" % q,) + d)
             accs.append(a)
         ghat = steps.reduce_mean(accs)
         z = np.zeros(hi - lo, np.float32)
@@ -215,7 +227,7 @@ def test_gpt2_small_accumulate_and_step_every_element():
                 out.append(("replica %d" % q,) + d)
         return out
 
-    _verify(P, job, "GPT-2-small 4 x accumulate + ZeRO-1 step, N_d=8")
+    _verify(P, job, "GPT-2-small 4 micro-batches + ZeRO-1 step (%s), N_d=8" % mode)
 
 
 def test_flat_sweep_n32_step_every_element():
