@@ -400,6 +400,28 @@ cudaError_t launch_rs_mean(const BView& g, const BView& out, bool out_by_owner, 
     return rs_ldg(g, out, out_by_owner, r, nd, sp, st);
 }
 
+// The staged AdamW over the 8-aligned body [lo, hi) of one-array buffers as a walk: pieces cut as in
+// launch_fused_walk (multiples of kFusedWalkChunk, none shorter than a quarter of it), one launch each,
+// the first waiting for the stream's predecessor and the others streaming their pieces while the
+// previous one drains (the launch-order modes of launch.h: the pieces are disjoint and the kernel
+// reads global memory through bulk copies only).
+static cudaError_t adamw_tma_walk(const BView& grad, float* master, float* m, float* v, const BView& par, int64_t lo,
+                                  int64_t hi, const AdamScalars& s, cudaStream_t st) {
+    constexpr int64_t C = kFusedWalkChunk;
+    bool first = true;
+    while (lo < hi) {
+        int64_t end = hi;
+        const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
+        if (cut < hi - C / 4) end = cut;
+        const cudaError_t e = launch_fused_tma(grad, master, m, v, par, false, lo, end - lo, s, 1, st,
+                                               first ? kSyncWalkFirst : kSyncWalkNext);
+        if (e != cudaSuccess) return e;
+        first = false;
+        lo = end;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, float* m, float* v,
                          const BView& par, bool par_by_owner, const Range& r, const AdamScalars& s,
                          cudaStream_t st) {
@@ -414,7 +436,7 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
         const void* ps[5] = {grad.ptr.p[0], par.ptr.p[0], master, m, v};
         if (all_device(ps, 5)) {
             const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-            cudaError_t e = launch_fused_tma(grad, master, m, v, par, false, sp.vlo, sp.nvec << 3, s, 1, st);
+            cudaError_t e = adamw_tma_walk(grad, master, m, v, par, sp.vlo, body_hi, s, st);
             if (e != cudaErrorNotSupported) {
                 if (e != cudaSuccess) return e;
                 AdamOp op{grad, par, 0, 0, master, m, v, s, r.base, r.shard};
