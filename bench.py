@@ -252,6 +252,27 @@ def walk_launches(ranges, n_d, staged_ok=True):
     return n
 
 
+def adamw_launches(ranges):
+    """Launches of zs_adamw_shard_step on one-array buffers: per unit range, a body of at least 2^20
+    8-aligned elements is walked in pieces (cut like the fused walk) plus one launch per ragged end;
+    a shorter range is one streaming launch."""
+    n, C = 0, WALK_CHUNK
+    for lo, hi in ranges:
+        vlo, vhi = (lo + 7) // 8 * 8, hi // 8 * 8
+        if vhi - vlo < (1 << 20):
+            n += 1 if hi > lo else 0
+            continue
+        n += (vlo > lo) + (hi > vhi)
+        while vlo < vhi:
+            end = vhi
+            cut = (vlo + C // 4 + C) // C * C
+            if cut < vhi - C // 4:
+                end = cut
+            n += 1
+            vlo = end
+    return n
+
+
 def bytes_per_padded_element(n_d, kernel):
     """Algorithmic HBM bytes per padded element of one launch (each byte crosses HBM once)."""
     if kernel == "fused":          # read N_d bf16 grads + master/m/v; write master/m/v + N_d bf16 replicas
@@ -1141,7 +1162,9 @@ def run_ours(args, ws, rank, local):
         kb = {"reduce_scatter_mean": 2 * n_d + 2, "adamw_shard_step": 28, "all_gather": 2 + 2 * n_d}
         unfused = {"ms_per_step": ums, "params_per_s": plan.numel / (ums / 1e3),
                    "algorithmic_gbs": bytes_per_padded_element(n_d, "unfused") * P / (ums / 1e3) / 1e9,
-                   "launches_per_step": 3,
+                   "launches_per_step": 2 + adamw_launches([(plan.unit(u)["base"], plan.unit(u)["base"]
+                                                                 + plan.unit(u)["padded"])
+                                                                for u in range(plan.n_units)]),
                    "kernels": {name: {"ms": statistics.mean(per[name]), "bytes_per_element": kb[name],
                                       "gbs": kb[name] * P / (statistics.mean(per[name]) / 1e3) / 1e9,
                                       "frac_of_peak": kb[name] * P / (statistics.mean(per[name]) / 1e3) / 1e9 / peak}

@@ -141,6 +141,39 @@ def test_accumulation_in_place_and_equal_microbatches():
         assert torch.equal(same[q], g[q])
 
 
+@pytest.mark.parametrize("n_d,numel", [(2, 3 * (1 << 22) + 13), (8, (1 << 22) + (1 << 20) + 3), (3, (1 << 20) + 8)])
+@pytest.mark.parametrize("mode", ["auto", "ldg"])
+def test_accumulation_large_buffers_match_oracle(n_d, numel, mode):
+    """Accumulation over buffers of a million elements and more (3 x 2^22 + 13 elements, padded to
+    3 x 2^22 + 14: a ragged end of 6 elements past the 16-byte vectors), four micro-batches at scale
+    1/4 with outliers, then in place (the micro-batch buffer as its own accumulator): equal to the
+    oracle bit for bit, with the default and the forced register-streaming (ldg) fused variant."""
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG if mode == "ldg" else zs.ZS_FUSED_AUTO)
+    try:
+        plan, _ = _plans([(numel,)], n_d)
+        P, pads = plan.padded, plan.pad_ranges()
+        acc, _ = synth.rank_buffers(n_d, P, BF16, DEV)
+        ref_acc = [None] * n_d
+        last = None
+        for j in range(4):
+            micro, _ = synth.rank_grads(n_d, P, pads, seed=17, step=j, sigma=1e-3, outlier_p=0.001, device=DEV)
+            zs.zs_accumulate_grad(plan, acc, micro, 0.25, first=(j == 0))
+            for q in range(n_d):
+                ref_acc[q] = steps.accumulate(ref_acc[q], H.to_np_bf16(micro[q]), 0.25, first=(j == 0))
+            last = micro
+        # in place: the micro-batch buffer is its own accumulator
+        last_np = [H.to_np_bf16(x) for x in last]
+        zs.zs_accumulate_grad(plan, last, last, 0.5, first=False)
+        torch.cuda.synchronize()
+        assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+        for q in range(n_d):
+            H.check_bf16(H.to_np_bf16(acc[q]), ref_acc[q], "acc rank %d (%s)" % (q, mode))
+            m = last_np[q]
+            H.check_bf16(H.to_np_bf16(last[q]), steps.accumulate(m, m, 0.5, first=False), "in place rank %d" % q)
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+
+
 # ---------------------------------------------------------------- ZeRO-3 per unit
 
 def _tiny_llama(n_layers=3, d=64, ffn=176, vocab=100):
@@ -648,9 +681,9 @@ def test_staged_adamw_on_sharded_buffers(variant, n_d, numel):
 
 
 def test_guard_zones_untouched_large_kernels():
-    """Sentinels around every buffer of the large-range kernels (staged fused step over one range
-    and over a scattered bucket list, staged AdamW, bulk-store gathers, staged naive-DP step and the
-    in-place all-reduce, FSDP2 copies): nothing is written outside the buffers."""
+    """Sentinels around every buffer of the large-range kernels (accumulation, staged fused step over
+    one range and over a scattered bucket list, staged AdamW, bulk-store gathers, staged naive-DP step
+    and the in-place all-reduce, FSDP2 copies): nothing is written outside the buffers."""
     n_d, numel = 8, 2_097_165
     plan, _ = _plans([(numel,)], n_d, stage=3)
     P = plan.padded
@@ -669,6 +702,8 @@ def test_guard_zones_untouched_large_kernels():
     full = [mk(P, BF16) for _ in range(n_d)]
     master, m, v = mk(P, torch.float32), mk(P, torch.float32), mk(P, torch.float32)
     ghat, shards = mk(P, BF16), mk(P, BF16)
+    zs.zs_accumulate_grad(plan, reps, grads, 0.25, first=True)                           # accumulation
+    zs.zs_accumulate_grad(plan, reps, grads, 0.25, first=False)
     zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)        # staged, broadcast
     zs.zs_zero3_rs_step_unit(plan, 0, grads, master, m, v, shards, HP, 2)               # staged, single output
     zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED)
