@@ -133,20 +133,30 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
         if (reshard_after_forward) slot_free[slot] = ev(u, 1);
     }
 
-    // backward, reverse unit order
+    // backward, reverse unit order.  With resharding, each unit's gather goes into its slot once main
+    // has released the slot's previous user, and the gather of the next unit (u - 1) is issued before
+    // the reduce-scatter/update of unit u (backward prefetch): the side stream streams that gather
+    // while main runs backward(u), instead of idling until backward(u) is done.
+    auto backward_gather = [&](int u) {
+        zs::TraceRange r_("zero3 backward gather unit %lld", (long long)u);
+        const zs::Unit& un = plan->units[u];
+        const int slot = u & 1;
+        if (slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
+        check(zs::launch_gather(shard_view, false, slot_view(slot, un), false,
+                                zs::Range{un.base, un.base + un.padded, un.base, un.shard}, nd, sideS));
+        check(cudaEventRecord(ev(u, 2), sideS));
+    };
+    if (reshard_after_forward && U > 0 && err == cudaSuccess) backward_gather(U - 1);
     for (int u = U - 1; u >= 0 && err == cudaSuccess; --u) {
-        zs::TraceRange r_("zero3 backward gather + reduce-scatter/update unit %lld", (long long)u);
+        zs::TraceRange r_("zero3 backward reduce-scatter/update unit %lld", (long long)u);
         const zs::Unit& un = plan->units[u];
         const zs::Range r{un.base, un.base + un.padded, un.base, un.shard};
         if (reshard_after_forward) {
-            const int slot = u & 1;
-            if (slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
-            check(zs::launch_gather(shard_view, false, slot_view(slot, un), false, r, nd, sideS));
-            check(cudaEventRecord(ev(u, 2), sideS));
             check(cudaStreamWaitEvent(mainS, ev(u, 2), 0));
             // backward(u) runs here on main and produces unit_grads[u]; then the slot is released
             check(cudaEventRecord(ev(u, 4), mainS));
-            slot_free[slot] = ev(u, 4);
+            slot_free[u & 1] = ev(u, 4);
+            if (u > 0) backward_gather(u - 1);
         } else {
             check(cudaStreamWaitEvent(mainS, ev(u, 0), 0));   // still gathered from forward
         }

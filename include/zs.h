@@ -561,7 +561,9 @@ int zs_zero2_step_host_noalloc(zs_plan_t plan, const void* const* host_grads, fl
  * (zs_zero3_rs_step_unit).  Gathers and updates run on side_stream; main_stream
  * (the compute stream, where a model's forward/backward would run) only waits
  * for each gather and releases the slot, and at the end waits for the last
- * update.  With two slots the next unit's gather overlaps the current unit's use.
+ * update.  With two slots the next unit's gather overlaps the current unit's use;
+ * in backward the next unit's gather is issued before the current unit's
+ * reduce-scatter and update (backward prefetch).
  * side_stream may equal main_stream (everything serialised; same results).
  *   shards       ZS_SHARDED bf16 parameter shards (updated in place).
  *   master,m,v   ZS_SHARDED fp32.
