@@ -273,6 +273,34 @@ def adamw_launches(ranges):
     return n
 
 
+ZERO3_WALK_CHUNK = 1 << 23     # the ZeRO-3 step's walk chunk (zero3.cu)
+
+
+def zero3_launches(plan, n_d, reshard=True):
+    """Launches of one zs_zero3_step on device buffers: each unit's gathers and its reduce-scatter +
+    update are walks cut like the fused walk (8 Mi-element chunk).  A piece takes the staged kernel
+    (bulk-store gather for bodies of at least 2^20 elements; single-output update for rank counts with
+    a staged shape, bodies of at least 2^16) plus one streaming launch per ragged end, else one
+    streaming launch; a unit whose base is off the 8-element grid streams every piece."""
+    n, C = 0, ZERO3_WALK_CHUNK
+    for u in range(plan.n_units):
+        base, padded = plan.unit(u)["base"], plan.unit(u)["padded"]
+        lo, hi = base, base + padded
+        while lo < hi:
+            end = hi
+            cut = (lo + C // 4 + C) // C * C
+            if cut < hi - C // 4:
+                end = cut
+            vlo, vhi = (lo + 7) // 8 * 8, end // 8 * 8
+            fringes = (vlo > lo) + (end > vhi)
+            vec = base % 8 == 0
+            g = 1 + fringes if vec and vhi - vlo >= (1 << 20) else 1
+            upd = 1 + fringes if vec and n_d in STAGED_ND and vhi - vlo >= WALK_MIN_STAGED else 1
+            n += (2 if reshard else 1) * g + upd
+            lo = end
+    return n
+
+
 def bytes_per_padded_element(n_d, kernel):
     """Algorithmic HBM bytes per padded element of one launch (each byte crosses HBM once)."""
     if kernel == "fused":          # read N_d bf16 grads + master/m/v; write master/m/v + N_d bf16 replicas
@@ -529,7 +557,7 @@ class Workload:
             acc = n_d * P * (4 + 6 * (micro - 2))
             return acc + bytes_per_padded_element(n_d, "fused_accumulate") * P, micro - 1 + walk
         # zero3: per unit two gathers (read shard, write N_d copies) + reduce-scatter with update
-        return P * (2 * (2 + 2 * n_d) + (2 * n_d + 12 + 12 + 2)), 3 * self.plan.n_units
+        return P * (2 * (2 + 2 * n_d) + (2 * n_d + 12 + 12 + 2)), zero3_launches(self.plan, n_d)
 
     def staged(self):
         zs = self.zs
@@ -549,7 +577,8 @@ class Workload:
                 return "%d x k_accumulate + %s" % (self.wl["micro"], fused)
             return "%d x k_accumulate + %s" % (self.wl["micro"] - 1, fused.replace("k_fused_tma<", "k_fused_tma_acc<")
                                                 .replace("k_fused<", "k_fused<acc "))
-        return "2 x k_gather<%d> + %s per unit" % (self.n_d, fused)
+        return ("2 x k_gather_bulk + k_fused_tma<%d> single output per unit, each walked in launches of 8 Mi elements "
+                "(%d launches per step)" % (self.n_d, zero3_launches(self.plan, self.n_d)))
 
     def step(self):
         zs, plan, hp = self.zs, self.plan, self.hp
@@ -672,7 +701,7 @@ def run_sweep(args, ws, rank, local):
                              main_stream=stream, side_stream=side)
 
         ms = timed(zero3, steps)
-        launches += 3 * steps
+        launches += zero3_launches(p3, n_d) * steps
         gbs = P * (2 * (2 + 2 * n_d) + (2 * n_d + 26)) / (ms / 1e3) / 1e9
         points.append({"n_d": n_d, "stage": 3, "step": "ZeRO-3: 2 gathers + reduce-scatter/update (one unit)",
                        "ms": ms, "params_per_s": plan.numel / (ms / 1e3), "gbs": gbs, "frac": gbs / peak})
@@ -917,10 +946,11 @@ def run_next(args, ws, rank, local):
                              main_stream=stream, side_stream=side)
 
         gathers = 2 if reshard else 1
+        z3n = zero3_launches(plan, n_d, reshard)
         row("ZeRO-3 step, %s, N_d=8, reshard_after_forward=%s" % (unit_label, reshard), timed(z3), plan.numel,
-            P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), (gathers + 1) * U,
+            P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), z3n,
             comm_bytes_per_rank=plan.comm_bytes(3, reshard))
-        launches += steps * (gathers + 1) * U
+        launches += steps * z3n
         # the same step captured once (both streams) and replayed; the replay repeats its step number
         g3, cs = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
         with torch.cuda.graph(g3, stream=cs):
@@ -928,8 +958,8 @@ def run_next(args, ws, rank, local):
                              main_stream=cs, side_stream=side)
         torch.cuda.synchronize(dev)
         row("ZeRO-3 step, reshard_after_forward=%s, replayed from a CUDA graph" % reshard, timed(g3.replay),
-            plan.numel, P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), (gathers + 1) * U)
-        launches += steps * (gathers + 1) * U
+            plan.numel, P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), z3n)
+        launches += steps * z3n
         del g3
     del master, m, v, shards, ugrads, pool
 

@@ -463,7 +463,7 @@ cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, f
 constexpr int64_t kBulkGatherMinElems = int64_t(1) << 20;
 
 cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
-                          const Range& r, int nd, cudaStream_t st) {
+                          const Range& r, int nd, cudaStream_t st, int sync) {
     const bool by_owner = src_by_owner || skip_owner;
     const bool vec = aligned8(src.off) && aligned8(dst.off) &&
                      (!by_owner || (aligned8(r.base) && aligned8(r.shard)));
@@ -475,7 +475,8 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
         for (int q = 0; q < nd; ++q) ps[q + 1] = dst.ptr.p[q];
         if (all_device(ps, nd + 1)) {
             const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-            cudaError_t e = launch_gather_bulk(src.ptr.p[0], src.off, dst.ptr, dst.off, sp.vlo, sp.nvec << 3, nd, st);
+            cudaError_t e = launch_gather_bulk(src.ptr.p[0], src.off, dst.ptr, dst.off, sp.vlo, sp.nvec << 3, nd, st,
+                                               sync);
             if (e != cudaSuccess) return e;
             Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
             for (const Split& f : rest) {
@@ -488,7 +489,11 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
             return cudaSuccess;
         }
     }
-#define ZS_GA(N) gather_impl<N>(src, src_by_owner, dst, skip_owner, r, nd, sp, st)
+    // the streaming kernel reads through L1, so it never starts before its predecessor completes; as
+    // the first launch of a walk it also waits before letting its successor launch
+    Split ss = sp;
+    ss.sync = sync == kSyncWalkFirst ? kSyncWalkFirst : kSyncStream;
+#define ZS_GA(N) gather_impl<N>(src, src_by_owner, dst, skip_owner, r, nd, ss, st)
     ZS_DISPATCH_ND(nd, ZS_GA)
 #undef ZS_GA
 }

@@ -623,11 +623,12 @@ struct GatherBulkArgs {
     int nd;
     int T;                // elements per tile (multiple of 8)
     long long wait_limit, drain_limit;
+    int sync;             // LaunchSync: the loads are bulk copies, so a later launch of a walk may stream at once
 };
 
 template <int S>
 __global__ void __launch_bounds__(32) k_gather_bulk(const __grid_constant__ GatherBulkArgs a) {
-    dependent_launch_prologue();
+    dependent_launch_prologue(a.sync);
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
     uint16_t* buf = reinterpret_cast<uint16_t*>(smem + 128);
@@ -680,6 +681,7 @@ __global__ void __launch_bounds__(32) k_gather_bulk(const __grid_constant__ Gath
     if (!ok && lane == 0)                                // loads still in flight into the ring
         for (int64_t k = j; k < issued; ++k) mbar_wait(&bar[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
     bulk_wait_all();
+    dependent_launch_epilogue(a.sync);
 }
 
 namespace {
@@ -796,6 +798,21 @@ cudaError_t with_walk_shape(int nd, F&& f) {
     }
 }
 
+// The single-output walk shapes (the ZeRO-3 reduce-scatter + update of one unit, walked in launches of
+// 8 Mi elements): two-stage rings in under half an SM's shared memory, the broadcast walk shapes'
+// tiles (N_d = 2, 4, 8: 8 warps x 8, T 2048; 16: 8 x 4, T 1024; 32: 4 x 4, T 512).
+template <class F>
+cudaError_t with_single_walk_shape(int nd, F&& f) {
+    switch (nd) {
+        case 2: return f(IC<2>{}, IC<8>{}, IC<8>{}, BC<false>{}, IC<2>{}, IC<115712>{});
+        case 4: return f(IC<4>{}, IC<8>{}, IC<8>{}, BC<false>{}, IC<2>{}, IC<115712>{});
+        case 8: return f(IC<8>{}, IC<8>{}, IC<8>{}, BC<false>{}, IC<2>{}, IC<115712>{});
+        case 16: return f(IC<16>{}, IC<8>{}, IC<4>{}, BC<false>{}, IC<2>{}, IC<115712>{});
+        case 32: return f(IC<32>{}, IC<4>{}, IC<4>{}, BC<false>{}, IC<2>{}, IC<115712>{});
+        default: return cudaErrorNotSupported;
+    }
+}
+
 // The walk shapes of the accumulating step (k_fused_tma_acc): a stage holds 2 N_d bf16 tiles, so
 // each rank count takes the tile of the plain walk shape with twice its rank count (two-stage ring
 // under half an SM's shared memory): N_d = 2, 4: 8 warps x 8 (T 2048); 8: 8 x 4 (T 1024); 16: 4 x 4
@@ -870,6 +887,12 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
     // shape walked; T 2048 with 3 or 4 stages 102.4 / 101.9 %, three T 1024 shapes 101.5-101.6 %,
     // 16 warps x 8 with 2 stages 101.7 %; pieces of 2 Mi elements 89.8 %, of 8 Mi 101.9 %.
     if (!broadcast && nd == 1 && sync != kSyncStream) return tma_impl<1, 8, 8, false, 2, 115712>(a, st, true);
+    if (!broadcast && sync != kSyncStream && fused_walk_shape(nd)) {
+        return with_single_walk_shape(nd, [&](auto ND, auto NCW, auto VPT, auto BR, auto MS, auto BU) {
+            return tma_impl<decltype(ND)::value, decltype(NCW)::value, decltype(VPT)::value, decltype(BR)::value,
+                            decltype(MS)::value, decltype(BU)::value>(a, st, true);
+        });
+    }
     if (broadcast && sync != kSyncStream && fused_walk_shape(nd)) {
         return with_walk_shape(nd, [&](auto ND, auto NCW, auto VPT, auto BR, auto MS, auto BU) {
             return tma_impl<decltype(ND)::value, decltype(NCW)::value, decltype(VPT)::value, decltype(BR)::value,
@@ -1417,7 +1440,7 @@ cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
 // (131 KB, so one one-warp CTA resident per SM), a grid of 16 CTAs per SM (chosen by measurement on
 // GB300).
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
-                               int64_t n, int nd, cudaStream_t st) {
+                               int64_t n, int nd, cudaStream_t st, int sync) {
     bool ok = body_ok(lo, n) && at_ok(src, lo - src_off);
     for (int q = 0; q < nd && ok; ++q) ok = at_ok(dst.p[q], lo - dst_off);
     if (!ok) return cudaErrorMisalignedAddress;
@@ -1432,6 +1455,20 @@ cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs&
     a.T = 16384;
     a.wait_limit = 4000000000LL;
     a.drain_limit = 4000000000LL;
+    a.sync = sync;
+    if (sync != kSyncStream) {
+        // a launch of a walk: a 2-stage ring (65,664 B, three CTAs per SM) and one wave of resident
+        // CTAs, so a launch's CTAs share each SM with the next launch's
+        constexpr int S2 = 2;
+        const int smem2 = 128 + S2 * a.T * 2;
+        int sms = 0, per_sm = 0;
+        cudaError_t e = staged_geometry((const void*)k_gather_bulk<S2>, 32, smem2, &sms, &per_sm);
+        if (e != cudaSuccess) return e;
+        const int64_t ntiles = (n + a.T - 1) / a.T;
+        const int64_t cap = (int64_t)sms * per_sm;
+        const int grid = (int)(ntiles < cap ? ntiles : cap);
+        return launch_kernel(k_gather_bulk<S2>, dim3(grid), dim3(32), smem2, st, a);
+    }
     constexpr int S = 4;
     const int smem = 128 + S * a.T * 2;
     int sms = 0, per_sm = 0;

@@ -56,8 +56,11 @@ cudaError_t launch_rs_mean(const BView& g, const BView& out, bool out_by_owner, 
 cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, float* m, float* v,
                          const BView& par, bool par_by_owner, const Range& r, const AdamScalars& s,
                          cudaStream_t st);
+// `sync`: a launch-order mode of a walk over disjoint ranges (kSyncWalkFirst / kSyncWalkNext) for the
+// bulk-store kernel; the streaming kernel keeps stream order (a first launch of a walk still waits
+// before it lets its successor launch).
 cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst, bool skip_owner,
-                          const Range& r, int nd, cudaStream_t st);
+                          const Range& r, int nd, cudaStream_t st, int sync = kSyncStream);
 // The last micro-batch's accumulation folded into the broadcast fused step: rank q's gradient is
 // bf16(acc_q[i] + micro_q[i] * scale) (the accumulation rule, computed in the kernel and not stored),
 // where the fused launch's gradient view holds the accumulators acc_q and `micro` the micro-batch.
@@ -135,9 +138,10 @@ struct Fsdp2CopyArgs {
     int64_t shard;
     int to_flat;            // 1: parameters -> buffer (zero padding rows), 0: buffer -> parameters
 };
-// One source to N_d destinations with bulk stores, over the 8-aligned body [lo, lo + n).
+// One source to N_d destinations with bulk stores, over the 8-aligned body [lo, lo + n); `sync` as for
+// the fused kernel (the kernel reads through bulk copies only, so it may be a later launch of a walk).
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
-                               int64_t n, int nd, cudaStream_t st);
+                               int64_t n, int nd, cudaStream_t st, int sync = kSyncStream);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);
 // Staged naive-DP step over the 8-aligned body [lo, lo + n) (the TMA alignment rules of
 // launch_fused_tma; every rank's master, m and v 16-byte aligned); cudaErrorNotSupported for rank

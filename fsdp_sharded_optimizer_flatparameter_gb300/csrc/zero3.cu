@@ -111,6 +111,30 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
     auto check = [&](cudaError_t e) {
         if (e != cudaSuccess && err == cudaSuccess) err = e;
     };
+    // A unit's gather and its reduce-scatter + update are each a walk over the unit's range: pieces cut
+    // at multiples of kWalkChunk (none shorter than a quarter of it), one launch each, the first
+    // waiting for everything before it on the stream, the others streaming their pieces while the
+    // previous one drains (the launch-order modes of launch.h; the pieces are disjoint and the staged
+    // kernels read global memory through bulk copies only).
+    constexpr int64_t kWalkChunk = int64_t(1) << 23;
+    auto walk = [&](const zs::Unit& un, auto&& launch) {
+        int64_t lo = un.base;
+        const int64_t hi = un.base + un.padded;
+        bool first = true;
+        while (lo < hi && err == cudaSuccess) {
+            int64_t end = hi;
+            const int64_t cut = (lo + kWalkChunk / 4 + kWalkChunk) / kWalkChunk * kWalkChunk;
+            if (cut < hi - kWalkChunk / 4) end = cut;
+            check(launch(zs::Range{lo, end, un.base, un.shard}, first ? zs::kSyncWalkFirst : zs::kSyncWalkNext));
+            first = false;
+            lo = end;
+        }
+    };
+    auto gather = [&](int slot, const zs::Unit& un) {
+        walk(un, [&](const zs::Range& r, int sync) {
+            return zs::launch_gather(shard_view, false, slot_view(slot, un), false, r, nd, sideS, sync);
+        });
+    };
 
     // the side stream starts after everything already enqueued on main
     check(cudaEventRecord(start, mainS));
@@ -124,8 +148,7 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
         const zs::Unit& un = plan->units[u];
         const int slot = reshard_after_forward ? (u & 1) : u;
         if (reshard_after_forward && slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
-        const zs::Range r{un.base, un.base + un.padded, un.base, un.shard};
-        check(zs::launch_gather(shard_view, false, slot_view(slot, un), false, r, nd, sideS));
+        gather(slot, un);
         check(cudaEventRecord(ev(u, 0), sideS));
         check(cudaStreamWaitEvent(mainS, ev(u, 0), 0));
         // forward(u) runs here on main; afterwards the gathered parameters are released
@@ -142,15 +165,13 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
         const zs::Unit& un = plan->units[u];
         const int slot = u & 1;
         if (slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
-        check(zs::launch_gather(shard_view, false, slot_view(slot, un), false,
-                                zs::Range{un.base, un.base + un.padded, un.base, un.shard}, nd, sideS));
+        gather(slot, un);
         check(cudaEventRecord(ev(u, 2), sideS));
     };
     if (reshard_after_forward && U > 0 && err == cudaSuccess) backward_gather(U - 1);
     for (int u = U - 1; u >= 0 && err == cudaSuccess; --u) {
         zs::TraceRange r_("zero3 backward reduce-scatter/update unit %lld", (long long)u);
         const zs::Unit& un = plan->units[u];
-        const zs::Range r{un.base, un.base + un.padded, un.base, un.shard};
         if (reshard_after_forward) {
             check(cudaStreamWaitEvent(mainS, ev(u, 2), 0));
             // backward(u) runs here on main and produces unit_grads[u]; then the slot is released
@@ -162,7 +183,10 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
         }
         check(cudaEventRecord(ev(u, 3), mainS));             // backward(u) done: its gradients exist
         check(cudaStreamWaitEvent(sideS, ev(u, 3), 0));
-        check(zs::launch_fused(grad_view(u), master, m, v, shard_view, false, r, s, nd, sideS));
+        walk(un, [&](const zs::Range& r, int sync) {
+            return zs::launch_fused(grad_view(u), master, m, v, shard_view, false, r, s, nd, sideS,
+                                    zs::kStagedIfDevice, sync);
+        });
     }
     // main continues (the next step's forward) only after the last update
     check(cudaEventRecord(done, sideS));

@@ -459,12 +459,18 @@ def test_bounded_wait_times_out_and_reports():
 
 # ---------------------------------------------------------------- ZeRO-3 step on two streams
 
-@pytest.mark.parametrize("n_d,reshard", [(16, True), (5, True), (4, False), (2, True)])
-def test_zero3_step_two_streams_matches_oracle(n_d, reshard):
+@pytest.mark.parametrize("n_d,reshard,size", [(16, True, "tiny"), (5, True, "tiny"), (4, False, "tiny"), (2, True, "tiny"),
+                                               (8, True, "walked"), (5, True, "walked"), (16, False, "walked")])
+def test_zero3_step_two_streams_matches_oracle(n_d, reshard, size):
     """The whole ZeRO-3 step (forward gathers, backward gathers, reduce-scatter + update per
     unit) with communication on a side stream equals the oracle, and equals the same step
-    with everything serialised on one stream, bit for bit."""
-    shapes, units = _tiny_llama(n_layers=3, d=96, ffn=256, vocab=300)
+    with everything serialised on one stream, bit for bit.  "walked": layer units of 3.2 M
+    elements and a root unit of 32.8 M (unit bases off the 8-element grid for N_d = 5), so
+    the root unit's gathers and update are each walked in four overlapping launches."""
+    if size == "tiny":
+        shapes, units = _tiny_llama(n_layers=3, d=96, ffn=256, vocab=300)
+    else:
+        shapes, units = _tiny_llama(n_layers=2, d=512, ffn=1408, vocab=32000)
     plan, ref = _plans(shapes, n_d, units=units, stage=3)
     P, pads = plan.padded, plan.pad_ranges()
     U = plan.n_units
