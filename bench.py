@@ -252,10 +252,11 @@ def walk_launches(ranges, n_d, staged_ok=True):
     return n
 
 
-def adamw_launches(ranges):
-    """Launches of zs_adamw_shard_step on one-array buffers: per unit range, a body of at least 2^20
-    8-aligned elements is walked in pieces (cut like the fused walk) plus one launch per ragged end;
-    a shorter range is one streaming launch."""
+def staged_walk_launches(ranges):
+    """Launches of a call that walks each range's 8-aligned body of at least 2^20 elements with a staged
+    kernel in pieces (cut like the fused walk) plus one streaming launch per ragged end, and gives a
+    shorter range one streaming launch: zs_adamw_shard_step on one-array buffers (per unit range) and
+    zs_all_reduce_mean on device buffers at a rank count with a staged shape."""
     n, C = 0, WALK_CHUNK
     for lo, hi in ranges:
         vlo, vhi = (lo + 7) // 8 * 8, hi // 8 * 8
@@ -875,9 +876,10 @@ def run_next(args, ws, rank, local):
     def ar():
         zs.zs_all_reduce_mean(plan, -1, grads, stream=stream)
 
-    row("naive DP all-reduce-mean alone (k_all_reduce_mean), %s, N_d=8" % dp_label, timed(ar), plan.numel,
-        4 * n_d * P, 1)
-    launches += steps
+    n_ar = staged_walk_launches([(0, P)])
+    row("naive DP all-reduce-mean alone (k_ar_tma, walked), %s, N_d=8" % dp_label, timed(ar), plan.numel,
+        4 * n_d * P, n_ar)
+    launches += steps * n_ar
     z_master, z_m, z_v = master0.clone(), torch.zeros_like(master0), torch.zeros_like(master0)
 
     def zero():
@@ -1192,7 +1194,7 @@ def run_ours(args, ws, rank, local):
         kb = {"reduce_scatter_mean": 2 * n_d + 2, "adamw_shard_step": 28, "all_gather": 2 + 2 * n_d}
         unfused = {"ms_per_step": ums, "params_per_s": plan.numel / (ums / 1e3),
                    "algorithmic_gbs": bytes_per_padded_element(n_d, "unfused") * P / (ums / 1e3) / 1e9,
-                   "launches_per_step": 2 + adamw_launches([(plan.unit(u)["base"], plan.unit(u)["base"]
+                   "launches_per_step": 2 + staged_walk_launches([(plan.unit(u)["base"], plan.unit(u)["base"]
                                                                  + plan.unit(u)["padded"])
                                                                 for u in range(plan.n_units)]),
                    "kernels": {name: {"ms": statistics.mean(per[name]), "bytes_per_element": kb[name],

@@ -823,8 +823,36 @@ static cudaError_t dp_step_impl(const BView& g, const BView& out, float* const* 
 }
 
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st) {
-    // the register-streaming kernel: a staged variant of this 1:1 read/write stream measured no faster
     const Split sp = split_range(r.lo, r.hi, aligned8(g.off));
+    // a body of at least kTmaMinElems in device memory: the staged kernel, walked (pieces cut as in
+    // launch_fused_walk, the first waiting for the stream's predecessor, the others streaming while the
+    // previous one drains); fringes, short ranges, host memory and other rank counts stream
+    const int64_t body = sp.nvec << 3;
+    if (body >= kTmaMinElems && g_fused_variant.load() != ZS_FUSED_LDG &&
+        (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32)) {
+        const void* ps[ZS_MAX_RANKS];
+        for (int q = 0; q < nd; ++q) ps[q] = g.ptr.p[q];
+        if (all_device(ps, nd)) {
+            constexpr int64_t C = kFusedWalkChunk;
+            const int64_t body_hi = sp.vlo + body;
+            cudaError_t e = cudaSuccess;
+            for (int64_t lo = sp.vlo; lo < body_hi && e == cudaSuccess;) {
+                int64_t end = body_hi;
+                const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
+                if (cut < body_hi - C / 4) end = cut;
+                e = launch_all_reduce_tma(g, lo, end - lo, nd, st, lo == sp.vlo ? kSyncWalkFirst : kSyncWalkNext);
+                lo = end;
+            }
+            Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
+            for (const Split& f : rest) {
+                if (e != cudaSuccess || f.hi <= f.lo) continue;
+#define ZS_ARF(N) all_reduce_impl<N>(g, nd, f, st)
+                e = [&]() -> cudaError_t { ZS_DISPATCH_ND(nd, ZS_ARF) }();
+#undef ZS_ARF
+            }
+            return e;
+        }
+    }
 #define ZS_AR(N) all_reduce_impl<N>(g, nd, sp, st)
     ZS_DISPATCH_ND(nd, ZS_AR)
 #undef ZS_AR

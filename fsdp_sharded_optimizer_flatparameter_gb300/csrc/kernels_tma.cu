@@ -982,6 +982,7 @@ struct RsTmaArgs {
     int nd;
     float inv_nd;
     long long wait_limit, drain_limit;
+    int sync;             // LaunchSync (the in-place all-reduce's walk; the reduce-scatter keeps stream order)
 };
 
 template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
@@ -995,9 +996,12 @@ struct RsShape {
     static_assert(2 * kStages * 8 <= 256, "barriers must fit in the first 256 bytes");
 };
 
-template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
-__global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant__ RsTmaArgs a) {
-    dependent_launch_prologue();
+// ALL: the in-place all-reduce with averaging of naive DP ("Infra: Data Parallel", Naive Data
+// Parallelism): the mean goes back into every rank's own buffer (a.g) instead of one output array.  A
+// tile's copies into shared memory complete before any consumer stores into it, and tiles are
+// disjoint, so in place is safe.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL>
+__device__ __forceinline__ void rs_tma_body(const RsTmaArgs& a) {
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
@@ -1079,24 +1083,58 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant
 #pragma unroll
             for (int k = 0; k < VPT; k += 2)
                 w[k / 2] = pack_bf16x2(mean_of_sum<ND>(acc[k], ND, a.inv_nd), mean_of_sum<ND>(acc[k + 1], ND, a.inv_nd));
-            uint16_t* o = a.out + (i0 + e - a.out_off);
-            if constexpr (VPT == 8)
-                __stcs(reinterpret_cast<uint4*>(o), make_uint4(w[0], w[1], w[2], w[3]));
-            else
-                __stcs(reinterpret_cast<uint2*>(o), make_uint2(w[0], w[1]));
-            mbar_arrive(&empty[s]);                      // after the store: see k_fused_tma
+            if constexpr (ALL) {
+#pragma unroll
+                for (int q = 0; q < ND; ++q) {
+                    uint16_t* o = a.g.p[q] + (i0 + e - a.g_off);
+                    if constexpr (VPT == 8)
+                        __stcs(reinterpret_cast<uint4*>(o), make_uint4(w[0], w[1], w[2], w[3]));
+                    else
+                        __stcs(reinterpret_cast<uint2*>(o), make_uint2(w[0], w[1]));
+                }
+            } else {
+                uint16_t* o = a.out + (i0 + e - a.out_off);
+                if constexpr (VPT == 8)
+                    __stcs(reinterpret_cast<uint4*>(o), make_uint4(w[0], w[1], w[2], w[3]));
+                else
+                    __stcs(reinterpret_cast<uint2*>(o), make_uint2(w[0], w[1]));
+            }
+            mbar_arrive(&empty[s]);                      // after the stores: see k_fused_tma
         } else {
             mbar_arrive(&empty[s]);
         }
     }
 }
 
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma(const __grid_constant__ RsTmaArgs a) {
+    dependent_launch_prologue();
+    rs_tma_body<ND, NCW, VPT, MAXST, BUDGET, false>(a);
+}
+
+// The in-place all-reduce, launched as the pieces of a walk (a.sync); the body returns early
+// (producer lanes, a wait that ran out) into the launch-order epilogue.
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_ar_tma(const __grid_constant__ RsTmaArgs a) {
+    dependent_launch_prologue(a.sync);
+    rs_tma_body<ND, NCW, VPT, MAXST, BUDGET, true>(a);
+    dependent_launch_epilogue(a.sync);
+}
+
 namespace {
 
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL>
+auto rs_kernel() {
+    if constexpr (ALL)
+        return k_ar_tma<ND, NCW, VPT, MAXST, BUDGET>;
+    else
+        return k_rs_tma<ND, NCW, VPT, MAXST, BUDGET>;
+}
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL = false>
 cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
-    auto kern = k_rs_tma<ND, NCW, VPT, MAXST, BUDGET>;
+    auto kern = rs_kernel<ND, NCW, VPT, MAXST, BUDGET, ALL>();
     int sms = 0, per_sm = 0;
     cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
@@ -1121,6 +1159,7 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
     a.inv_nd = 1.0f / (float)nd;
     a.wait_limit = 4000000000LL;
     a.drain_limit = 4000000000LL;
+    a.sync = kSyncStream;
     return a;
 }
 
@@ -1142,6 +1181,30 @@ cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_
         case 8: return rs_tma_impl<8, 8, 8, 2, 232448>(a, st);     // T 2048, 2 stages, 3 CTAs/SM
         case 16: return rs_tma_impl<16, 8, 8, 2, 232448>(a, st);   // T 2048, 2 stages, 1 CTA/SM
         case 32: return rs_tma_impl<32, 2, 4, 2, 232448>(a, st);   // T 256, 2 stages, 6 CTAs/SM
+        default: return cudaErrorNotSupported;
+    }
+}
+
+// The in-place all-reduce with averaging over the 8-aligned body [lo, lo + n) of every rank's buffer, as
+// one launch of a walk (`sync`); cudaErrorNotSupported when no staged shape exists for this rank
+// count.  Two-stage rings with at least two CTAs per SM, so a launch's CTAs run beside the next
+// launch's.  Measured on GB300 (GPT-2-small buffers, 124,439,808 elements per rank, walked in 4 Mi-element
+// launches; of the measured copy rate, the register-streaming kernel in brackets): N_d = 2, 4 with 8
+// warps x 8 (T 2048): 101.4 / 98.0 % (92.0 / 93.3 %; the reduce-scatter's smaller tiles 90.7 / 95.6 %,
+// five other shapes 89.5-101.2 / 94.2-97.5 %); N_d = 8, 16, 32 with the reduce-scatter's tiles (T 2048,
+// 8 x 4 at T 1024 for 16, T 256): 102.1 / 101.1 / 100.2 % (93.6 / 94.4 / 98.3 %).
+cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd, cudaStream_t st, int sync) {
+    bool ok = body_ok(lo, n);
+    for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off);
+    if (!ok) return cudaErrorMisalignedAddress;
+    RsTmaArgs a = rs_args(g, lo, n, nd);
+    a.sync = sync;
+    switch (nd) {
+        case 2: return rs_tma_impl<2, 8, 8, 2, 232448, true>(a, st);
+        case 4: return rs_tma_impl<4, 8, 8, 2, 232448, true>(a, st);
+        case 8: return rs_tma_impl<8, 8, 8, 2, 232448, true>(a, st);
+        case 16: return rs_tma_impl<16, 8, 4, 2, 232448, true>(a, st);
+        case 32: return rs_tma_impl<32, 2, 4, 2, 232448, true>(a, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -143,6 +143,9 @@ struct Fsdp2CopyArgs {
 cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
                                int64_t n, int nd, cudaStream_t st, int sync = kSyncStream);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);
+// Bulk-copy staged in-place all-reduce over the 8-aligned body [lo, lo + n) of every rank's buffer
+// (device memory), one launch of a walk (`sync`); cudaErrorNotSupported without a staged shape.
+cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd, cudaStream_t st, int sync);
 // Staged naive-DP step over the 8-aligned body [lo, lo + n) (the TMA alignment rules of
 // launch_fused_tma; every rank's master, m and v 16-byte aligned); cudaErrorNotSupported for rank
 // counts without a staged shape.

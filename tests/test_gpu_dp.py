@@ -36,23 +36,27 @@ def test_all_reduce_mean(n_d, numel, bucket_bytes):
         H.check_bf16(H.to_np_bf16(grads[q]), want, "rank %d" % q)
 
 
-@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
-def test_all_reduce_mean_every_rank_count(n_d):
-    """The in-place all-reduce on a million-element buffer with a ragged tail, with the staged variant
-    requested (the all-reduce keeps its streaming kernel either way): every rank's buffer holds the
-    oracle's mean, bit for bit."""
-    plan = zs.Plan([(1_100_003,)], n_d, stage=0)
+@pytest.mark.parametrize("variant", ["auto", "ldg"])
+@pytest.mark.parametrize("n_d,numel", [(2, 1_100_003), (4, 1_100_003), (8, 1_100_003), (16, 1_100_003),
+                                       (32, 1_100_003), (8, 3 * (1 << 22) + 5), (2, 3 * (1 << 22) + 5)])
+def test_all_reduce_mean_every_rank_count(n_d, numel, variant):
+    """The in-place all-reduce on buffers of a million elements and more with a ragged tail: the
+    bulk-copy staged kernel (3 x 2^22 + 5 elements: walked in three overlapping launches, the ragged
+    end streamed) and the register-streaming kernel (ldg) leave the oracle's mean in every rank's
+    buffer, bit for bit."""
+    plan = zs.Plan([(numel,)], n_d, stage=0)
     P, pads = plan.padded, plan.pad_ranges()
     grads, _ = synth.rank_grads(n_d, P, pads, seed=53, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)
     want = steps.reduce_mean([H.to_np_bf16(g) for g in grads])
-    zs.zs_set_fused_variant(zs.ZS_FUSED_TMA)
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG if variant == "ldg" else zs.ZS_FUSED_AUTO)
     try:
+        zs.zs_device_status(clear=True)
         zs.zs_all_reduce_mean(plan, -1, grads)
         torch.cuda.synchronize()
     finally:
         zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
     assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
-    for q in (0, n_d // 2, n_d - 1):
+    for q in range(n_d):
         H.check_bf16(H.to_np_bf16(grads[q]), want, "rank %d" % q)
 
 

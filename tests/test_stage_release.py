@@ -18,8 +18,9 @@ import re
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "fsdp_sharded_optimizer_flatparameter_gb300", "csrc", "kernels_tma.cu")
 
-# the staged kernels' consumer code (k_fused_tma's lives in fused_tma_body, which the kernel calls)
-KERNELS = ("fused_tma_body", "k_fused_tma_list", "k_rs_tma", "k_dp_tma")
+# the staged kernels' consumer code (k_fused_tma's lives in fused_tma_body and k_rs_tma's / k_ar_tma's
+# in rs_tma_body, which the kernels call)
+KERNELS = ("fused_tma_body", "k_fused_tma_list", "rs_tma_body", "k_dp_tma")
 LOAD = re.compile(r"\blds_(?:bf|f32)<")
 STORE = re.compile(r"\b__stcs\(|\bstg_f32<")
 # consumer releases: empty[...] pairs with full[...], gempty[...] with gfull[...]
@@ -85,6 +86,7 @@ def test_every_consumer_arrive_follows_the_stores_that_consume_the_stage():
             checked += 1
     assert checked >= 6
     assert "fused_tma_body<" in _kernel_body(text, "k_fused_tma")
+    assert "rs_tma_body<" in _kernel_body(text, "k_rs_tma") and "rs_tma_body<" in _kernel_body(text, "k_ar_tma")
 
 
 def test_barrier_semantics_are_explicit():
@@ -98,7 +100,7 @@ def test_barrier_semantics_are_explicit():
 def test_the_check_catches_an_early_release():
     """A planted early release (arrive right after the loads) must fail the rule above."""
     body = _strip_comments(open(SRC).read())
-    cons = _consumer_part(_kernel_body(body, "k_rs_tma"))
+    cons = _consumer_part(_kernel_body(body, "rs_tma_body"))
     early = cons.replace("lds_bf<VPT>(sg + (size_t)q * T + e, f);",
                          "lds_bf<VPT>(sg + (size_t)q * T + e, f); mbar_arrive(&empty[s]);", 1)
     assert early != cons
