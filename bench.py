@@ -255,8 +255,8 @@ def walk_launches(ranges, n_d, staged_ok=True):
 def staged_walk_launches(ranges):
     """Launches of a call that walks each range's 8-aligned body of at least 2^20 elements with a staged
     kernel in pieces (cut like the fused walk) plus one streaming launch per ragged end, and gives a
-    shorter range one streaming launch: zs_adamw_shard_step on one-array buffers (per unit range) and
-    zs_all_reduce_mean on device buffers at a rank count with a staged shape."""
+    shorter range one streaming launch: zs_adamw_shard_step on one-array buffers (per unit range), and
+    zs_all_reduce_mean and zs_dp_step on device buffers at a rank count with a walk shape."""
     n, C = 0, WALK_CHUNK
     for lo, hi in ranges:
         vlo, vhi = (lo + 7) // 8 * 8, hi // 8 * 8
@@ -862,9 +862,10 @@ def run_next(args, ws, rank, local):
         t[0] += 1
         zs.zs_dp_step(plan, grads, master, mm, vv, reps, hp, t[0], stream=stream)
 
-    row("naive DP step (k_dp_tma: all-reduce-mean + replicated AdamW), %s, N_d=8" % dp_label, timed(dp), plan.numel,
-        28 * n_d * P, 1)
-    launches += steps
+    n_dp = staged_walk_launches([(0, P)])          # walked at N_d = 8
+    row("naive DP step (k_dp_tma walked: all-reduce-mean + replicated AdamW), %s, N_d=8" % dp_label, timed(dp),
+        plan.numel, 28 * n_d * P, n_dp)
+    launches += steps * n_dp
     zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
     try:
         row("naive DP step, register-streaming kernel (k_dp_step), for comparison", timed(dp), plan.numel,

@@ -887,8 +887,24 @@ cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* maste
         staged = all_device(ps, n);
     }
     if (!staged) return dp_step_ldg(g, out, master, m, v, sp, s, nd, st);
+    // the body walked where the rank count has a walk shape (pieces cut as in launch_fused_walk, the first
+    // waiting for the stream's predecessor, the others streaming while the previous one drains), else
+    // one launch; then the fringes
     const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-    cudaError_t e = launch_dp_tma(g, out, master, m, v, sp.vlo, sp.nvec << 3, s, nd, st);
+    cudaError_t e = cudaSuccess;
+    if (dp_walk_shape(nd)) {
+        constexpr int64_t C = kFusedWalkChunk;
+        for (int64_t lo = sp.vlo; lo < body_hi && e == cudaSuccess;) {
+            int64_t end = body_hi;
+            const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
+            if (cut < body_hi - C / 4) end = cut;
+            e = launch_dp_tma(g, out, master, m, v, lo, end - lo, s, nd, st,
+                              lo == sp.vlo ? kSyncWalkFirst : kSyncWalkNext);
+            lo = end;
+        }
+    } else {
+        e = launch_dp_tma(g, out, master, m, v, sp.vlo, sp.nvec << 3, s, nd, st);
+    }
     if (e != cudaSuccess) return e;
     if (sp.vlo > sp.lo) {
         e = dp_step_ldg(g, out, master, m, v, split_range(sp.lo, sp.vlo, false), s, nd, st);

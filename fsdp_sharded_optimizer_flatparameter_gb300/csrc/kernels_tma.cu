@@ -1233,6 +1233,7 @@ struct DpTmaArgs {
     int nd;
     float inv_nd;
     long long wait_limit, drain_limit;
+    int sync;             // LaunchSync: the loads are bulk copies, so a later launch of a walk may stream at once
 };
 
 // Consumers index the ranks at run time (one copy of the update code, not N_d): the rank pointers
@@ -1259,9 +1260,8 @@ struct DpShape {
     static_assert((4 + 2 * kStages) * 8 <= kBarBytes, "barriers must fit in their block");
 };
 
-template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
-__global__ void __launch_bounds__(32 * (NCW + 1), 1) k_dp_tma(const __grid_constant__ DpTmaArgs a) {
-    dependent_launch_prologue();
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+__device__ __forceinline__ void dp_tma_body(const DpTmaArgs& a) {
     using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
@@ -1421,13 +1421,23 @@ __global__ void __launch_bounds__(32 * (NCW + 1), 1) k_dp_tma(const __grid_const
     }
 }
 
+// The naive-DP step over one range; MINB CTAs per SM at least (a walk shape runs two, so a launch's
+// CTAs share each SM with the next launch's).  The body returns early (producer lanes, a wait that
+// ran out) into the launch-order epilogue.
+template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024, int MINB = 1>
+__global__ void __launch_bounds__(32 * (NCW + 1), MINB) k_dp_tma(const __grid_constant__ DpTmaArgs a) {
+    dependent_launch_prologue(a.sync);
+    dp_tma_body<ND, NCW, VPT, MAXST, BUDGET>(a);
+    dependent_launch_epilogue(a.sync);
+}
+
 namespace {
 
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, int MINB = 1>
 cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
     using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
     static_assert(Sh::kSmem <= 232448, "shared memory above the per-CTA limit");
-    auto kern = k_dp_tma<ND, NCW, VPT, MAXST, BUDGET>;
+    auto kern = k_dp_tma<ND, NCW, VPT, MAXST, BUDGET, MINB>;
     int sms = 0, per_sm = 0;
     cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
@@ -1443,7 +1453,8 @@ cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
 // Staged naive-DP step over the 8-aligned body [lo, lo + n); cudaErrorNotSupported for rank
 // counts without a staged shape.
 cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master, float* const* m,
-                          float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+                          float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st,
+                          int sync) {
     bool ok = body_ok(lo, n);
     for (int q = 0; q < nd && ok; ++q)
         ok = at_ok(g.ptr.p[q], lo - g.off) && at_ok(out.ptr.p[q], lo - out.off) && at_ok(master[q], lo) &&
@@ -1466,6 +1477,22 @@ cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master
     a.inv_nd = 1.0f / (float)nd;
     a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
     a.drain_limit = 4000000000LL;
+    a.sync = sync;
+    if (sync != kSyncStream) {
+        // The launches of a walk: two CTAs per SM, each with half an SM's shared memory, 8 consumer
+        // warps each.  Measured on GB300 (GPT-2-small buffers walked in 4 Mi-element launches, of the
+        // measured copy rate; the whole-range shapes' single launch in brackets): N_d = 2: 8 x 8, T 2048,
+        // 4 stages: 101.5 % (90.5 %); 4: 8 x 8, 3 stages: 100.8 % (96.7 %); 8: 8 x 4, T 1024, 6 stages:
+        // 99.9 % (98.2 %); 16: 8 x 4, 4 stages: 99.3 % (97.8 %).  N_d = 32 (4 x 4, T 512, 7 stages:
+        // 90.2 % against 94.1 %) keeps its single launch (dp_walk_shape).
+        switch (nd) {
+            case 2: return dp_tma_impl<2, 8, 8, 16, 115712, 2>(a, st);
+            case 4: return dp_tma_impl<4, 8, 8, 16, 115712, 2>(a, st);
+            case 8: return dp_tma_impl<8, 8, 4, 16, 115712, 2>(a, st);
+            case 16: return dp_tma_impl<16, 8, 4, 16, 115712, 2>(a, st);
+            default: return cudaErrorNotSupported;
+        }
+    }
     // Shapes per rank count from a measured sweep on GB300 (GPT-2-small buffers, 124.4 M elements;
     // consumer warps x elements per thread x ring depth x CTAs per SM).  The update is ALU-heavy
     // here (one AdamW per 28 bytes moved, twice the fused step's density), so the consumers set the
@@ -1481,6 +1508,8 @@ cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master
         default: return cudaErrorNotSupported;
     }
 }
+
+bool dp_walk_shape(int nd) { return nd == 2 || nd == 4 || nd == 8 || nd == 16; }
 
 // Self-test of the bounded wait: waits on an mbarrier nothing arrives at, with
 // a budget of `limit` cycles, then records ZS_DEVERR_SELFTEST and returns.

@@ -148,9 +148,12 @@ cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaS
 cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd, cudaStream_t st, int sync);
 // Staged naive-DP step over the 8-aligned body [lo, lo + n) (the TMA alignment rules of
 // launch_fused_tma; every rank's master, m and v 16-byte aligned); cudaErrorNotSupported for rank
-// counts without a staged shape.
+// counts without a staged shape.  `sync` as for the fused kernel (the kernel reads through bulk copies
+// only, so it may be a later launch of a walk); walk launches need a walk shape (dp_walk_shape).
+bool dp_walk_shape(int nd);
 cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master, float* const* m,
-                          float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
+                          float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st,
+                          int sync = kSyncStream);
 // The naive-DP step over r: the staged kernel for the 8-aligned body of a large range whose buffers
 // are all device memory (the few fringe elements, and everything else, by the streaming kernel).
 cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* master, float* const* m, float* const* v,

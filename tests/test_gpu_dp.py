@@ -61,13 +61,15 @@ def test_all_reduce_mean_every_rank_count(n_d, numel, variant):
 
 
 @pytest.mark.parametrize("variant", ["tma", "ldg"])
-@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 32])
-def test_dp_step_every_rank_count(n_d, variant):
-    """The naive-DP step on a 600K-element buffer with a ragged tail, every power-of-two rank count,
-    with the staged kernel (grads of a tile, then one rank's state after another through the ring;
-    the tail's few elements by the streaming kernel) and with the streaming kernel alone, two steps:
-    every rank's state and replica equal the oracle's, bit for bit."""
-    plan = zs.Plan([(600_003,)], n_d, stage=0)
+@pytest.mark.parametrize("n_d,numel", [(2, 600_003), (4, 600_003), (8, 600_003), (16, 600_003), (32, 600_003),
+                                       (8, 3 * (1 << 22) + 5), (16, (1 << 22) + (1 << 20) + 3), (32, 3_000_005)])
+def test_dp_step_every_rank_count(n_d, numel, variant):
+    """The naive-DP step on buffers with a ragged tail, every power-of-two rank count, with the staged
+    kernel (grads of a tile, then one rank's state after another through the ring; walked in
+    overlapping 4 Mi-element launches where the rank count has a walk shape: 3 x 2^22 + 5 elements
+    at N_d = 8 are three launches; the tail's few elements by the streaming kernel) and with the
+    streaming kernel alone, two steps: every rank's state and replica equal the oracle's, bit for bit."""
+    plan = zs.Plan([(numel,)], n_d, stage=0)
     P, pads = plan.padded, plan.pad_ranges()
     master0 = synth.master_init(P, pads, seed=54, device=DEV)
     dm = [master0.clone() for _ in range(n_d)]

@@ -18,9 +18,9 @@ import re
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "fsdp_sharded_optimizer_flatparameter_gb300", "csrc", "kernels_tma.cu")
 
-# the staged kernels' consumer code (k_fused_tma's lives in fused_tma_body and k_rs_tma's / k_ar_tma's
-# in rs_tma_body, which the kernels call)
-KERNELS = ("fused_tma_body", "k_fused_tma_list", "rs_tma_body", "k_dp_tma")
+# the staged kernels' consumer code (k_fused_tma's lives in fused_tma_body, k_rs_tma's / k_ar_tma's in
+# rs_tma_body and k_dp_tma's in dp_tma_body, which the kernels call)
+KERNELS = ("fused_tma_body", "k_fused_tma_list", "rs_tma_body", "dp_tma_body")
 LOAD = re.compile(r"\blds_(?:bf|f32)<")
 STORE = re.compile(r"\b__stcs\(|\bstg_f32<")
 # consumer releases: empty[...] pairs with full[...], gempty[...] with gfull[...]
@@ -87,6 +87,7 @@ def test_every_consumer_arrive_follows_the_stores_that_consume_the_stage():
     assert checked >= 6
     assert "fused_tma_body<" in _kernel_body(text, "k_fused_tma")
     assert "rs_tma_body<" in _kernel_body(text, "k_rs_tma") and "rs_tma_body<" in _kernel_body(text, "k_ar_tma")
+    assert "dp_tma_body<" in _kernel_body(text, "k_dp_tma")
 
 
 def test_barrier_semantics_are_explicit():
