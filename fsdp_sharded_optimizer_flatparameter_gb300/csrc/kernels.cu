@@ -22,6 +22,7 @@
 #include <vector>
 
 #include "device.cuh"
+#include "walk.h"
 
 namespace zs {
 
@@ -407,19 +408,9 @@ cudaError_t launch_rs_mean(const BView& g, const BView& out, bool out_by_owner, 
 // reads global memory through bulk copies only).
 static cudaError_t adamw_tma_walk(const BView& grad, float* master, float* m, float* v, const BView& par, int64_t lo,
                                   int64_t hi, const AdamScalars& s, cudaStream_t st) {
-    constexpr int64_t C = kFusedWalkChunk;
-    bool first = true;
-    while (lo < hi) {
-        int64_t end = hi;
-        const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
-        if (cut < hi - C / 4) end = cut;
-        const cudaError_t e = launch_fused_tma(grad, master, m, v, par, false, lo, end - lo, s, 1, st,
-                                               first ? kSyncWalkFirst : kSyncWalkNext);
-        if (e != cudaSuccess) return e;
-        first = false;
-        lo = end;
-    }
-    return cudaSuccess;
+    return walk_range(lo, hi, kFusedWalkChunk, [&](int64_t a, int64_t b, int sync) {
+        return launch_fused_tma(grad, master, m, v, par, false, a, b - a, s, 1, st, sync);
+    });
 }
 
 cudaError_t launch_adamw(const BView& grad, bool grad_by_owner, float* master, float* m, float* v,
@@ -597,22 +588,14 @@ cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v,
         staged_policy = fused_ptrs_on_device(g, master, m, v, out, true, nd, acc) ? kStagedDeviceKnown : kStagedNever;
     const bool chunked = fused_walk_shape(nd, acc != nullptr) && staged_policy != kStagedNever &&
                          g_fused_variant.load() != ZS_FUSED_LDG;
-    constexpr int64_t C = kFusedWalkChunk;
     bool first = true;
     for (const Range& r : ranges) {
-        int64_t lo = r.lo;
-        while (lo < r.hi) {
-            int64_t hi = r.hi;
-            if (chunked) {
-                const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
-                if (cut < r.hi - C / 4) hi = cut;
-            }
-            const cudaError_t e = launch_fused(g, master, m, v, out, true, {lo, hi, r.base, r.shard}, s, nd, st,
-                                               staged_policy, first ? kSyncWalkFirst : kSyncWalkNext, acc);
-            if (e != cudaSuccess) return e;
-            first = false;
-            lo = hi;
-        }
+        if (r.hi <= r.lo) continue;
+        const cudaError_t e = walk_range(r.lo, r.hi, chunked ? kFusedWalkChunk : 0, [&](int64_t a, int64_t b, int sync) {
+            return launch_fused(g, master, m, v, out, true, {a, b, r.base, r.shard}, s, nd, st, staged_policy, sync, acc);
+        }, first ? (int)kSyncWalkFirst : (int)kSyncWalkNext);
+        if (e != cudaSuccess) return e;
+        first = false;
     }
     return cudaSuccess;
 }
@@ -833,16 +816,10 @@ cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaS
         const void* ps[ZS_MAX_RANKS];
         for (int q = 0; q < nd; ++q) ps[q] = g.ptr.p[q];
         if (all_device(ps, nd)) {
-            constexpr int64_t C = kFusedWalkChunk;
             const int64_t body_hi = sp.vlo + body;
-            cudaError_t e = cudaSuccess;
-            for (int64_t lo = sp.vlo; lo < body_hi && e == cudaSuccess;) {
-                int64_t end = body_hi;
-                const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
-                if (cut < body_hi - C / 4) end = cut;
-                e = launch_all_reduce_tma(g, lo, end - lo, nd, st, lo == sp.vlo ? kSyncWalkFirst : kSyncWalkNext);
-                lo = end;
-            }
+            cudaError_t e = walk_range(sp.vlo, body_hi, kFusedWalkChunk, [&](int64_t a, int64_t b, int sync) {
+                return launch_all_reduce_tma(g, a, b - a, nd, st, sync);
+            });
             Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
             for (const Split& f : rest) {
                 if (e != cudaSuccess || f.hi <= f.lo) continue;
@@ -893,15 +870,9 @@ cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* maste
     const int64_t body_hi = sp.vlo + (sp.nvec << 3);
     cudaError_t e = cudaSuccess;
     if (dp_walk_shape(nd)) {
-        constexpr int64_t C = kFusedWalkChunk;
-        for (int64_t lo = sp.vlo; lo < body_hi && e == cudaSuccess;) {
-            int64_t end = body_hi;
-            const int64_t cut = (lo + C / 4 + C) / C * C;    // first multiple of C past lo + C/4
-            if (cut < body_hi - C / 4) end = cut;
-            e = launch_dp_tma(g, out, master, m, v, lo, end - lo, s, nd, st,
-                              lo == sp.vlo ? kSyncWalkFirst : kSyncWalkNext);
-            lo = end;
-        }
+        e = walk_range(sp.vlo, body_hi, kFusedWalkChunk, [&](int64_t a, int64_t b, int sync) {
+            return launch_dp_tma(g, out, master, m, v, a, b - a, s, nd, st, sync);
+        });
     } else {
         e = launch_dp_tma(g, out, master, m, v, sp.vlo, sp.nvec << 3, s, nd, st);
     }

@@ -22,6 +22,7 @@
 #include "launch.h"
 #include "plan.h"
 #include "trace.h"
+#include "walk.h"
 
 namespace {
 
@@ -118,17 +119,10 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
     // kernels read global memory through bulk copies only).
     constexpr int64_t kWalkChunk = int64_t(1) << 23;
     auto walk = [&](const zs::Unit& un, auto&& launch) {
-        int64_t lo = un.base;
-        const int64_t hi = un.base + un.padded;
-        bool first = true;
-        while (lo < hi && err == cudaSuccess) {
-            int64_t end = hi;
-            const int64_t cut = (lo + kWalkChunk / 4 + kWalkChunk) / kWalkChunk * kWalkChunk;
-            if (cut < hi - kWalkChunk / 4) end = cut;
-            check(launch(zs::Range{lo, end, un.base, un.shard}, first ? zs::kSyncWalkFirst : zs::kSyncWalkNext));
-            first = false;
-            lo = end;
-        }
+        if (err != cudaSuccess) return;
+        check(zs::walk_range(un.base, un.base + un.padded, kWalkChunk, [&](int64_t a, int64_t b, int sync) {
+            return launch(zs::Range{a, b, un.base, un.shard}, sync);
+        }));
     };
     auto gather = [&](int slot, const zs::Unit& un) {
         walk(un, [&](const zs::Range& r, int sync) {
