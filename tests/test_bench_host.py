@@ -87,3 +87,24 @@ def test_reference_arm_runs_without_the_library():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_walk_launch_counts_match_the_recorded_launch_lists():
+    """The launch counts bench.py reports for walked calls follow the library's piece cutting; pinned
+    to the counts ncu's launch lists of the benchmarked steps show (profiles/launches_*.md): 321 fused
+    launches per Llama-1.3B ZeRO-2 step, 1,640 gathers + 820 updates per Llama-7B ZeRO-3 step."""
+    import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+    import synth
+
+    shapes, _ = synth.workload_params("llama-1.3b")
+    P = zs.Plan(shapes, 8, stage=2).padded
+    assert bench.walk_launches([(0, P)], 8) == 321
+    assert bench.staged_walk_launches([(0, P)]) == 321
+    shapes, units = synth.workload_params("llama-7b")
+    plan = zs.Plan(shapes, 16, stage=3, unit_of_param=units)
+    assert bench.zero3_launches(plan, 16) == 2460
+    assert bench.zero3_launches(plan, 16, reshard=False) == 1640
+    # short, ragged and unaligned ranges
+    assert bench.staged_walk_launches([(0, 1000)]) == 1
+    assert bench.staged_walk_launches([(3, (1 << 21) + 5)]) == 3          # body plus two ragged ends
+    assert bench.staged_walk_launches([(0, 3 * (1 << 22) + 8)]) == 3
