@@ -92,6 +92,7 @@ def hbm_peak():
 # the files that define each profiled kernel: its code, its argument structs and its launch shape
 KERNEL_SOURCES = {
     "k_fused_tma": ("device.cuh", "launch.h", "kernels_tma.cu"),
+    "k_fused_tma_dyn": ("device.cuh", "launch.h", "kernels_tma.cu"),
     "k_gather_bulk": ("device.cuh", "launch.h", "kernels_tma.cu"),
     "k_fused": ("device.cuh", "launch.h", "kernels.cu"),
 }
@@ -241,7 +242,23 @@ def walk_pieces(ranges, n_d, staged_ok=True):
     return out
 
 
+DYN_ND = (2, 4, 8, 16, 32)       # rank counts with a dynamic-order shape (fused_dyn_shape)
+DYN_MIN = 1 << 24                # kDynMinElems
+
+
+def dyn_range(ranges, n_d, staged_ok=True):
+    """True when a fused call over these ranges is one dynamic-order launch (one range whose 8-aligned
+    body has at least 2^24 elements, a rank count with a dynamic-order shape, device buffers)."""
+    if not staged_ok or n_d not in DYN_ND or len(ranges) != 1:
+        return False
+    lo, hi = ranges[0]
+    return hi // 8 * 8 - (lo + 7) // 8 * 8 >= DYN_MIN
+
+
 def walk_launches(ranges, n_d, staged_ok=True):
+    if dyn_range(ranges, n_d, staged_ok):
+        lo, hi = ranges[0]
+        return 1 + ((lo + 7) // 8 * 8 > lo) + (hi > hi // 8 * 8)
     n = 0
     for lo, hi in walk_pieces(ranges, n_d, staged_ok):
         vlo, vhi = (lo + 7) // 8 * 8, hi // 8 * 8
@@ -566,10 +583,17 @@ class Workload:
         big = (self.P >= WALK_MIN_STAGED) if self.kind != "zero3" else True
         return self.n_d in (2, 4, 8, 16, 32) and (v == zs.ZS_FUSED_TMA or (v == zs.ZS_FUSED_AUTO and big))
 
+    def dynamic_order(self):
+        """The fused step runs as one dynamic-order launch (kind fused, whole flat space)."""
+        return (self.kind == "fused" and self.args.step_mode == "whole"
+                and dyn_range([(0, self.P)], self.n_d, self.staged()))
+
     def kernel_label(self):
         fused = ("k_fused_tma<%d>" if self.staged() else "k_fused<%d>") % self.n_d
         pieces = len(walk_pieces([(0, self.P)], self.n_d, self.staged())) if self.kind != "zero3" else 1
-        if pieces > 1:
+        if self.dynamic_order():
+            fused = "k_fused_tma_dyn<%d> (one launch, tiles taken in dynamic order)" % self.n_d
+        elif pieces > 1:
             fused += " walked in %d overlapping launches" % pieces
         if self.kind == "fused":
             return fused
@@ -1274,7 +1298,8 @@ def run_ours(args, ws, rank, local):
         staged = W.staged()
         traffic = None
         if W.kind == "fused" and not args.profile_case:
-            traffic = profiled_traffic(args.workload, "k_fused_tma" if staged else "k_fused")
+            traffic = profiled_traffic(args.workload, "k_fused_tma_dyn" if W.dynamic_order()
+                                       else ("k_fused_tma" if staged else "k_fused"))
         line = {
             "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": steps,
             "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,

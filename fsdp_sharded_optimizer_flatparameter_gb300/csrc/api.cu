@@ -242,7 +242,8 @@ static int fused_common(const char* fn, zs_plan_t plan, int32_t bucket, const vo
     }
     if (r.hi <= r.lo) return ZS_OK;
     // gradients or replicas may be pinned host memory: launch_fused then keeps to the streaming kernel.
-    // The range is walked in chunks whose launches overlap (zs::launch_fused_walk).
+    // zs::launch_fused_walk runs a long range as one launch that takes its tiles in dynamic order and
+    // walks a shorter one in chunks whose launches overlap.
     return cuda_status(fn, zs::launch_fused_walk(g, master, m, v, o, {r}, s, nd, st, zs::kStagedIfDevice));
 }
 

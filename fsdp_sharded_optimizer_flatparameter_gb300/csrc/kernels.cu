@@ -588,6 +588,21 @@ cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v,
         staged_policy = fused_ptrs_on_device(g, master, m, v, out, true, nd, acc) ? kStagedDeviceKnown : kStagedNever;
     const bool chunked = fused_walk_shape(nd, acc != nullptr) && staged_policy != kStagedNever &&
                          g_fused_variant.load() != ZS_FUSED_LDG;
+    // One long range (the whole flat space, or touching buckets merged): one launch that takes its tiles
+    // in dynamic order, then the fringes off the 8-element grid.
+    if (chunked && !acc && ranges.size() == 1 && fused_dyn_shape(nd)) {
+        const Range& r = ranges[0];
+        const Split sp = split_range(r.lo, r.hi, aligned8(g.off) && aligned8(out.off));
+        if ((sp.nvec << 3) >= kDynMinElems) {
+            const int64_t body_hi = sp.vlo + (sp.nvec << 3);
+            cudaError_t e = launch_fused_tma_dyn(g, master, m, v, out, sp.vlo, sp.nvec << 3, s, nd, st);
+            if (e == cudaSuccess && sp.vlo > sp.lo)
+                e = launch_fused_ldg(g, master, m, v, out, true, split_range(sp.lo, sp.vlo, false), s, nd, st);
+            if (e == cudaSuccess && sp.hi > body_hi)
+                e = launch_fused_ldg(g, master, m, v, out, true, split_range(body_hi, sp.hi, false), s, nd, st);
+            return e;
+        }
+    }
     bool first = true;
     for (const Range& r : ranges) {
         if (r.hi <= r.lo) continue;

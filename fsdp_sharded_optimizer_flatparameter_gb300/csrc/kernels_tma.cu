@@ -46,6 +46,7 @@
 // before the loads it depends on have delivered their data, whatever the proxies.  A change that
 // moves an arrive above the consuming stores (releasing after the state stores only, say) must
 // keep that dependency; tests/test_stage_release.py checks the source for it.
+#include <atomic>
 #include <memory>
 #include <mutex>
 #include <type_traits>
@@ -216,6 +217,8 @@ struct TmaArgs {
     long long wait_limit; // cycles a wait may take before the kernel gives up
     long long drain_limit;// cycles to wait for copies still in flight after giving up
     int sync;             // LaunchSync: order against the previous kernel on the stream
+    unsigned int* order;  // dynamic tile order (k_fused_tma_dyn): the launch's tile counter and finish
+                          // counter, order[0] and order[1]; null for the static order
 };
 
 // The fused step with the last micro-batch's accumulation folded in (AccumIn): `a.g` holds the
@@ -284,15 +287,22 @@ struct TmaShape {
 
 // ACC: every rank's gradient tile is formed from two staged tiles, its accumulator (a.g) and the
 // last micro-batch (micro), so a stage holds 2 N_d bf16 tiles ahead of the fp32 state.
-template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET, bool ACC = false>
+//
+// DYN: the tiles are taken in dynamic order.  The producer takes its next tile from the launch's tile
+// counter (a.order[0], an atomic add, so the whole grid works through the range front to back and
+// its accesses stay close together) and publishes the tile index in the stage's record before the
+// stage's copies; a record past the last tile tells the consumers that the CTA is done.
+template <int ND, int NCW, int VPT, bool BROADCAST, int MAXST, int BUDGET, bool ACC = false, bool DYN = false>
 __device__ __forceinline__ void fused_tma_body(const TmaArgs& a, const Ptrs& micro, int64_t micro_off, float scale) {
     constexpr int NG = ACC ? 2 * ND : ND;                 // bf16 tiles per stage
     using Sh = TmaShape<NG, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
+    static_assert(!DYN || S <= 8, "the dynamic order's stage records sit behind the barriers");
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + S;
+    int64_t* rec = reinterpret_cast<int64_t*>(smem + 128);   // DYN: the tile of each stage
     uint8_t* stages = smem + 256;
 
     const int warp = threadIdx.x >> 5;
@@ -314,12 +324,20 @@ __device__ __forceinline__ void fused_tma_body(const TmaArgs& a, const Ptrs& mic
             const uint64_t pol = evict_first_policy();
             int64_t j = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            for (int64_t tile = DYN ? 0 : blockIdx.x; DYN || tile < ntiles; tile += gridDim.x, ++j) {
                 const int s = (int)(j % S);
                 if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), a.wait_limit)) {
                     flag_error(ZS_DEVERR_PRODUCER_WAIT);
                     ok = false;
                     break;
+                }
+                if constexpr (DYN) {
+                    tile = (int64_t)atomicAdd(a.order, 1u);
+                    rec[s] = tile;                        // published by the arrive below (release)
+                    if (tile >= ntiles) {
+                        mbar_arrive(&full[s]);            // no copies: the consumers read the end mark
+                        break;
+                    }
                 }
                 const int64_t i0 = a.lo + tile * T;
                 const int64_t rem = a.n - tile * T;
@@ -354,11 +372,15 @@ __device__ __forceinline__ void fused_tma_body(const TmaArgs& a, const Ptrs& mic
     const int e = ct * VPT;                           // this thread's first element in a tile
     const int n = ND;
     int64_t j = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+    for (int64_t tile = DYN ? 0 : blockIdx.x; DYN || tile < ntiles; tile += gridDim.x, ++j) {
         const int s = (int)(j % S);
         if (!mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
             flag_error(ZS_DEVERR_CONSUMER_WAIT);
             return;
+        }
+        if constexpr (DYN) {
+            tile = rec[s];
+            if (tile >= ntiles) return;                   // the producer's end mark
         }
         const int64_t i0 = a.lo + tile * T;
         const int64_t rem = a.n - tile * T;
@@ -441,6 +463,24 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
 }
 
 // The broadcast step with the last micro-batch's accumulation folded in (TmaAccArgs).
+// The broadcast step over one range in one persistent launch that takes its tiles in dynamic order
+// (DYN in the body).  The launch's counters, order[0] (tiles handed out) and order[1] (CTAs
+// finished), start at zero; the last CTA to finish sets both back to zero for the next launch that
+// draws the same pair.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_dyn(const __grid_constant__ TmaArgs a) {
+    dependent_launch_prologue(kSyncStream);
+    fused_tma_body<ND, NCW, VPT, true, MAXST, BUDGET, false, true>(a, a.g, 0, 0.0f);
+    __syncthreads();                                      // every thread of the CTA is past the body
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.order + 1, 1u) == gridDim.x - 1) {   // the last CTA: no producer draws any more
+            atomicExch(a.order, 0u);
+            atomicExch(a.order + 1, 0u);
+        }
+    }
+}
+
 template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_acc(const __grid_constant__ TmaAccArgs x) {
     dependent_launch_prologue(x.a.sync);
@@ -847,6 +887,7 @@ TmaArgs make_args(const BView& g, float* master, float* m, float* v, const BView
     a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
     a.drain_limit = 4000000000LL;
     a.sync = kSyncStream;
+    a.order = nullptr;
     return a;
 }
 
@@ -907,6 +948,84 @@ cudaError_t launch_fused_tma(const BView& g, float* master, float* m, float* v, 
 
 bool fused_walk_shape(int nd, bool /*acc: the same rank counts*/) {
     return nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32;
+}
+
+// ------------------------------------------------------------------ dynamic tile order
+// Counter pairs of the dynamic-order launches, one pair per launch in flight: launches draw pairs in
+// turn, so up to kDynOrderSlots of them may run at once on a device, on any streams.  Module memory,
+// zero at load (every device that loads the library holds its own array).
+constexpr unsigned int kDynOrderSlots = 1024;
+__device__ unsigned int g_zs_dyn_order[2 * kDynOrderSlots];
+
+namespace {
+
+// The next counter pair on the current device (its address looked up once per device).
+cudaError_t dyn_order_pair(unsigned int** out) {
+    static std::mutex mu;
+    static std::unordered_map<int, unsigned int*> base;
+    static std::atomic<unsigned int> next{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    unsigned int* b = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = base.find(dev);
+        if (it == base.end()) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_zs_dyn_order);
+            if (e != cudaSuccess) return e;
+            it = base.emplace(dev, static_cast<unsigned int*>(p)).first;
+        }
+        b = it->second;
+    }
+    *out = b + 2 * (next.fetch_add(1u) % kDynOrderSlots);
+    return cudaSuccess;
+}
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+cudaError_t dyn_impl(TmaArgs a, cudaStream_t st) {
+    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
+    auto kern = k_fused_tma_dyn<ND, NCW, VPT, MAXST, BUDGET>;
+    int sms = 0, per_sm = 0;
+    cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
+    if (ntiles < 1) return cudaSuccess;
+    const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
+    const int grid = (int)(ntiles < cap ? ntiles : cap);
+    e = dyn_order_pair(&a.order);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, dim3(grid), dim3(32 * (NCW + 1)), Sh::kSmem, st, a);
+}
+
+}  // namespace
+
+bool fused_dyn_shape(int nd) { return nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32; }
+
+// The broadcast fused step over the 8-aligned body [lo, lo + n) in one dynamic-order launch.  Shapes from
+// a measured comparison on GB300 (the 2^28+7-element buffer, against the walk of 4 Mi-element launches
+// on the same box, of the measured copy rate): N_d = 2, 4: 4 consumer warps x 8 (T 1024), 4 stages:
+// 103.3 / 103.0 % (walk 101.9 / 101.2 %); N_d = 8: 4 x 8, 4 stages: 102.0 % (100.5 %; on the
+// Llama-1.3B buffer 103.4-103.8 % against 101.7-101.9 %); N_d = 16: 8 x 4 (T 1024), 2 stages: 102.0 %
+// (99.4 %); N_d = 32: 4 x 4 (T 512), 2 stages: 102.0 % (97.5 %).  Rings of at most half an SM's shared
+// memory, two CTAs per SM.
+cudaError_t launch_fused_tma_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
+                                 int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+    bool ok = body_ok(lo, n) && at_ok(master, lo) && at_ok(m, lo) && at_ok(v, lo);
+    for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off) && at_ok(out.ptr.p[q], lo - out.off);
+    if (!ok) return cudaErrorMisalignedAddress;
+    TmaArgs a = make_args(g, master, m, v, out, s, nd);
+    a.lo = lo;
+    a.n = n;
+    switch (nd) {
+        case 2: return dyn_impl<2, 4, 8, 4, 115712>(a, st);
+        case 4: return dyn_impl<4, 4, 8, 4, 115712>(a, st);
+        case 8: return dyn_impl<8, 4, 8, 4, 115712>(a, st);
+        case 16: return dyn_impl<16, 8, 4, 4, 115712>(a, st);
+        case 32: return dyn_impl<32, 4, 4, 4, 115712>(a, st);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 namespace {

@@ -89,6 +89,12 @@ bool fused_ptrs_on_device(const BView& g, float* master, float* m, float* v, con
 // Whether the broadcast staged kernel has a walk shape for this rank count: a shape whose launches
 // share each SM with the next launch of a walk, for kSyncWalkFirst / kSyncWalkNext launches.
 bool fused_walk_shape(int nd, bool acc = false);
+// Whether the broadcast staged kernel has a dynamic-order shape for this rank count: one persistent
+// launch whose CTAs take tiles from a counter, for one range of at least kDynMinElems elements.
+bool fused_dyn_shape(int nd);
+constexpr int64_t kDynMinElems = int64_t(1) << 24;
+cudaError_t launch_fused_tma_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
+                                 int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
 // The broadcast fused step over disjoint ranges as a walk: ranges longer than kFusedWalkChunk are cut
 // at multiples of it, each piece is one launch, the first on the stream kSyncWalkFirst and the others
 // kSyncWalkNext, so every launch streams its piece while the previous one drains.  Without a walk

@@ -91,15 +91,20 @@ def test_reference_arm_runs_without_the_library():
 
 def test_walk_launch_counts_match_the_recorded_launch_lists():
     """The launch counts bench.py reports for walked calls follow the library's piece cutting; pinned
-    to the counts ncu's launch lists of the benchmarked steps show (profiles/launches_*.md): 321 fused
-    launches per Llama-1.3B ZeRO-2 step, 1,640 gathers + 820 updates per Llama-7B ZeRO-3 step."""
+    to the counts ncu's launch lists of the benchmarked steps show (profiles/launches_*.md): one
+    dynamic-order launch per Llama-1.3B ZeRO-2 step (321 walked launches for the update on its shard
+    arrays, 360 for the step bucket by bucket over its 103 buckets), 1,640 gathers + 820 updates per
+    Llama-7B ZeRO-3 step."""
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
     import synth
 
     shapes, _ = synth.workload_params("llama-1.3b")
-    P = zs.Plan(shapes, 8, stage=2).padded
-    assert bench.walk_launches([(0, P)], 8) == 321
+    plan13 = zs.Plan(shapes, 8, stage=2, bucket_bytes=25 << 20)
+    P = plan13.padded
+    assert bench.walk_launches([(0, P)], 8) == 1
     assert bench.staged_walk_launches([(0, P)]) == 321
+    br = [plan13.bucket(b)[1:] for b in reversed(range(plan13.n_buckets))]
+    assert plan13.n_buckets == 103 and bench.walk_launches(br, 8) == 360
     shapes, units = synth.workload_params("llama-7b")
     plan = zs.Plan(shapes, 16, stage=3, unit_of_param=units)
     assert bench.zero3_launches(plan, 16) == 2460

@@ -1,0 +1,152 @@
+"""The fused step over one long range in one dynamic-order launch (GPU).
+
+A broadcast fused step over one range of at least 2^24 elements (the whole flat space, or touching
+buckets merged) runs as one persistent launch whose CTAs take their tiles from a counter pair in
+module memory: the tile counter hands out tiles front to back, the last CTA to finish sets both
+counters back to zero, and launches draw the pairs in turn (1024 of them), so launches in flight on
+several streams use different pairs.  These tests check that path against the oracle and the
+register-streaming kernel, with ragged ends, on two concurrent streams, after the pairs have all
+been used (the counters came back to zero), from a CUDA graph, and inside guard zones.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fsdp_sharded_optimizer_flatparameter_gb300 as zs
+import gpu_helpers as H
+import synth
+from oracle import layout, steps
+
+pytestmark = pytest.mark.gpu
+
+HP = synth.HPARAMS
+DEV = "cuda"
+BF16 = torch.bfloat16
+
+
+def _setup(n_d, numel, seed):
+    plan = zs.Plan([(numel,)], n_d, stage=2)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads = synth.rank_grads(n_d, P, pads, seed=seed, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)[0]
+    master = synth.master_init(P, pads, seed=seed + 1, device=DEV)
+    state = [master, torch.rand_like(master) * 1e-3, torch.rand_like(master) * 1e-6]
+    return plan, P, grads, state
+
+
+def _fresh(state, n_d, P):
+    return [x.clone() for x in state], synth.rank_buffers(n_d, P, BF16, DEV)[0]
+
+
+@pytest.mark.parametrize("n_d,numel", [(8, (1 << 24) + 13), (2, (1 << 24) + (1 << 20) + 1), (32, (1 << 24) + 5)])
+def test_dynamic_order_step_matches_the_oracle_and_streaming(n_d, numel):
+    """Every element of master, m, v and every replica: the one-launch dynamic-order step (with the
+    streaming kernel for the ragged end) equals the oracle's ZeRO step and the register-streaming
+    kernel, bit for bit."""
+    plan, P, grads, state = _setup(n_d, numel, 70)
+    ref = layout.make_plan([(numel,)], n_d)
+    st, reps = _fresh(state, n_d, P)
+    zs.zs_device_status(clear=True)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *st, reps, HP, 3)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
+    try:
+        st2, reps2 = _fresh(state, n_d, P)
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *st2, reps2, HP, 3)
+        torch.cuda.synchronize()
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+    assert all(torch.equal(x, y) for x, y in zip(st, st2))
+    assert all(torch.equal(x, y) for x, y in zip(reps, reps2))
+    g_np = [H.to_np_bf16(g) for g in grads]
+    om, omm, ov = (H.reshard(ref, H.to_np_f32(x)) for x in state)
+    want_reps, om, omm, ov = steps.zero_step(ref, g_np, om, omm, ov, HP, 3)
+    H.check_f32(H.to_np_f32(st[0]), H.unshard(ref, om), "master")
+    H.check_f32(H.to_np_f32(st[1]), H.unshard(ref, omm), "m")
+    H.check_f32(H.to_np_f32(st[2]), H.unshard(ref, ov), "v")
+    for q in range(n_d):
+        H.check_bf16(H.to_np_bf16(reps[q]), want_reps[q], "replica %d" % q)
+
+
+def test_concurrent_launches_on_two_streams_and_every_counter_pair():
+    """Two dynamic-order steps on disjoint buffers run at once on two streams, 600 steps each (1,200
+    launches: every counter pair is drawn at least once, and the first 176 twice, so they must have
+    come back to zero), and the final states equal the same 600 steps run by the register-streaming
+    kernel, bit for bit."""
+    n_d, numel = 8, (1 << 24) + 8
+    runs = [_setup(n_d, numel, 80 + 10 * k) for k in range(2)]
+    plan, P = runs[0][0], runs[0][1]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for (_, _, grads, state), s in zip(runs, streams):
+        outs.append(_fresh(state, n_d, P))
+    torch.cuda.synchronize()
+    zs.zs_device_status(clear=True)
+    for t in range(1, 601):
+        for k in range(2):
+            st, reps = outs[k]
+            zs.zs_fused_step(plan, -1, runs[k][2], zs.ZS_RANK_FULL, *st, reps, HP, t, stream=streams[k])
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
+    try:
+        for k in range(2):
+            st, reps = outs[k]
+            want = _fresh(runs[k][3], n_d, P)
+            for t in range(1, 601):
+                zs.zs_fused_step(plan, -1, runs[k][2], zs.ZS_RANK_FULL, *want[0], want[1], HP, t)
+            torch.cuda.synchronize()
+            assert all(torch.equal(x, y) for x, y in zip(st, want[0])), "stream %d: state differs" % k
+            assert all(torch.equal(x, y) for x, y in zip(reps, want[1])), "stream %d: replicas differ" % k
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+
+
+def test_dynamic_order_step_replays_from_a_graph():
+    n_d, numel = 4, (1 << 24) + 3
+    plan, P, grads, state = _setup(n_d, numel, 90)
+    direct, graphed = _fresh(state, n_d, P), _fresh(state, n_d, P)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *direct[0], direct[1], HP, 2, stream=s)
+    torch.cuda.synchronize()
+    g, cs = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=cs):
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *graphed[0], graphed[1], HP, 2, stream=cs)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    assert all(torch.equal(x, y) for x, y in zip(direct[0], graphed[0]))
+    assert all(torch.equal(x, y) for x, y in zip(direct[1], graphed[1]))
+
+
+def test_dynamic_order_step_stays_inside_its_buffers():
+    """Sentinel bytes around every buffer of a dynamic-order step survive it."""
+    n_d, numel = 8, (1 << 24) + 21
+    plan = zs.Plan([(numel,)], n_d, stage=2)
+    P = plan.padded
+    guard, fill = 2048, 0x5A
+    raws = []
+
+    def mk(n, dtype):
+        esz = torch.tensor([], dtype=dtype).element_size()
+        raw = torch.full(((n + 2 * guard) * esz,), fill, dtype=torch.uint8, device=DEV)
+        raws.append((raw, guard * esz))
+        t = raw.view(dtype)[guard:guard + n]
+        t.zero_()
+        return t
+
+    grads = [mk(P, BF16) for _ in range(n_d)]
+    for g in grads:
+        g.normal_(0, 1e-3)
+    reps = [mk(P, BF16) for _ in range(n_d)]
+    master, m, v = mk(P, torch.float32), mk(P, torch.float32), mk(P, torch.float32)
+    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    torch.cuda.synchronize()
+    for raw, gb in raws:
+        head, tail = raw[:gb].cpu().numpy(), raw[raw.numel() - gb:].cpu().numpy()
+        assert np.all(head == fill) and np.all(tail == fill)

@@ -7,7 +7,8 @@ every element of every output is compared with the oracle, bit for bit:
 
 * the Llama-1.3B ZeRO-2 step at N_d = 8 (1,345,423,360 elements), exactly
   the call the benchmark times (zs_fused_step over the whole flat space, the
-  launches walked), at step 2 so the moments going in are not zero;
+  whole range in one launch that takes its tiles in dynamic order), at step 2 so the moments going
+  in are not zero;
 * the whole Llama-7B ZeRO-3 step at N_d = 16 (zs_zero3_step, both streams,
   the 2-slot pool), at step 2, on its largest unit (the root unit: embedding,
   final norm and output, 262,148,096 elements) with the parameter shards;
@@ -16,8 +17,8 @@ every element of every output is compared with the oracle, bit for bit:
   stored accumulated gradient too);
 * the 2^28+7-element flat buffer at N_d = 32 (padding, the widest rank count);
 * a flat buffer past 2^32 elements at N_d = 2 (element offsets, tile counts
-  and walk pieces that overflow 32-bit integers): the walked fused step
-  against the oracle, then the bucket-by-bucket walk and the unfused calls
+  and tile indices that overflow 32-bit integers): the fused step (one
+  dynamic-order launch) against the oracle, then the bucket-by-bucket walk and the unfused calls
   against that result on the device.
 
 Every step is element-wise, so the oracle on a chunk needs only that chunk's
@@ -232,7 +233,7 @@ def test_gpt2_small_accumulate_and_step_every_element(mode):
 
 def test_flat_sweep_n32_step_every_element():
     """The 2^28+7-element flat buffer at N_d = 32 (25 padding elements, the widest walk shape's rank
-    count): the walked fused step, every element of every output against the oracle."""
+    count): the fused step (one dynamic-order launch), every element of every output against the oracle."""
     n_d = 32
     plan = zs.Plan([(2 ** 28 + 7,)], n_d, stage=2)
     P, pads = plan.padded, plan.pad_ranges()
@@ -271,7 +272,7 @@ def test_flat_sweep_n32_step_every_element():
 
 def test_flat_buffer_past_2p32_elements():
     """One flat tensor of 2^32 + 2^22 + 3 elements at N_d = 2 (one padding element): every offset
-    past 2^31 and 2^32 that a 32-bit index would wrap.  The walked fused step is checked against the
+    past 2^31 and 2^32 that a 32-bit index would wrap.  The fused step (one dynamic-order launch) is checked against the
     oracle on every element; the same step bucket by bucket (25 MiB buckets, last first) and the
     unfused ZeRO-2 calls (reduce-scatter into a sharded staging buffer, update, all-gather) run on
     copies of the initial state and must reproduce it bit for bit."""

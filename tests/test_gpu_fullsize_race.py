@@ -1,15 +1,16 @@
 """Race checks of the overlapping launches at the benchmarked sizes (GPU).
 
-A walk lets each launch stream its piece while its predecessor drains, and the ZeRO-3 step walks its
-gathers and updates on a side stream as well.  A race there would show as a run-to-run difference,
-so each step below runs repeatedly from the same state and must equal, bit for bit, the same step
-with programmatic dependent launch off (every launch waiting for the previous one to complete) and,
-for ZeRO-3, with everything on one stream:
+The benchmarked fused step is one launch whose CTAs take their tiles in dynamic order from a
+counter, and the ZeRO-3 step walks its gathers and updates (each launch streaming its piece while its
+predecessor drains) on a side stream.  A race there would show as a run-to-run difference,
+so each step below runs repeatedly from the same state and must equal, bit for bit, a reference run
+of the same step:
 
-* the Llama-1.3B ZeRO-2 step at N_d = 8, the call the benchmark times (321 overlapping launches),
-  ten times (1.3e10 element-steps);
+* the Llama-1.3B ZeRO-2 step at N_d = 8, the call the benchmark times (one dynamic-order launch),
+  ten times (1.3e10 element-steps), against the register-streaming kernel;
 * the ZeRO-3 step on the Llama-1.3B units at N_d = 8 (25 units, each unit's gathers and update
-  walked, two streams, the 2-slot pool), five times.
+  walked, two streams, the 2-slot pool), five times, against the same step with programmatic
+  dependent launch off (every launch waiting for the previous one to complete) on one stream.
 
 The oracle itself is not needed here: every-element oracle parity of these calls is in
 test_gpu_fullsize_every_element.py.
@@ -44,7 +45,7 @@ def _need(nbytes):
         pytest.skip("needs %.0f GB of free device memory, %.0f GB free" % (nbytes / 1e9, free / 1e9))
 
 
-def test_llama13b_zero2_walk_repeats_the_serialised_step():
+def test_llama13b_zero2_step_repeats_the_streaming_result():
     wl = synth.WORKLOADS["llama-1.3b-zero2"]
     shapes, _ = synth.workload_params(wl["model"])
     n_d = wl["n_d"]
@@ -57,10 +58,12 @@ def test_llama13b_zero2_walk_repeats_the_serialised_step():
     state0 += [torch.rand_like(state0[0]) * 1e-3, torch.rand_like(state0[0]) * 1e-6]   # moments not zero
     ref_st = [x.clone() for x in state0]
     ref_reps, _ = synth.rank_buffers(n_d, P, BF16, DEV)
-    zs.zs_set_dependent_launch(False)
-    zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *ref_st, ref_reps, HP, 2)
-    torch.cuda.synchronize()
-    zs.zs_set_dependent_launch(True)
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
+    try:
+        zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, *ref_st, ref_reps, HP, 2)
+        torch.cuda.synchronize()
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
     st = [x.clone() for x in state0]
     reps, _ = synth.rank_buffers(n_d, P, BF16, DEV)
     zs.zs_device_status(clear=True)

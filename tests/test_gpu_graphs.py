@@ -214,10 +214,11 @@ def test_dependent_launch_on_and_off_agree():
 
 
 def test_overlapping_walks_repeat_the_serialised_result():
-    """Race check of the walk's overlapping launches: the bucket-by-bucket step over 128 buckets of
+    """Race check of the overlapping launches: the bucket-by-bucket step over 128 buckets of
     1 MiB (every later launch starts before its predecessor ends), on one stream and on two, and the
-    whole-range walk, repeated 20 times each from the same state, must equal bit for bit the same
-    step run with programmatic dependent launch off (every launch waiting for the previous one)."""
+    whole-range step (one dynamic-order launch), repeated 20 times each from the same state, must
+    equal bit for bit the same step run with programmatic dependent launch off (every launch waiting
+    for the previous one)."""
     n_d = 8
     plan = zs.Plan([(1 << 26,)], n_d, stage=2, bucket_bytes=1 << 20)
     assert plan.n_buckets == 128
