@@ -39,7 +39,12 @@
  *             own state in that rank's local layout (its shard of every unit,
  *             back to back) for the mode with one rank per process and GPU.
  * Ownership.  The caller owns all device memory and all streams.  The library
- *             never allocates device memory.  The step calls never
+ *             never allocates device memory; its module memory holds a status
+ *             word (zs_device_status), 1024 counter pairs for the fused step's
+ *             dynamic tile order (one pair per such launch in flight, drawn in
+ *             turn, so at most 1024 of those launches may run at once on a
+ *             device) and the staging array of zs_zero2_step_host_noalloc.
+ *             The step calls never
  *             synchronise and enqueue work only on the streams they are given
  *             (a cudaStream_t; NULL is the legacy default stream); calls that
  *             use a second stream order it after the first with events.  The
@@ -343,10 +348,13 @@ int zs_dp_step(zs_plan_t plan, const void* const* grads, float* const* master, f
  *   bucket      -1 = the whole flat space, else one bucket (the update is
  *               element-wise, so a bucket can be stepped as soon as its
  *               gradients are complete).
- * The range is stepped as a walk: cut at multiples of 4 Mi elements, one
- * launch per piece; the launches after the first start on their own pieces
- * while the previous one drains and complete after it, so stream order holds
- * at the call's end (pinned host buffers: one launch, nothing cut).
+ * A range of at least 2^24 elements (device buffers, N_d of 2, 4, 8, 16 or
+ * 32) is stepped by one persistent launch whose CTAs take their tiles in
+ * order from a counter; a shorter range is stepped as a walk: cut at
+ * multiples of 4 Mi elements, one launch per piece; the launches after the
+ * first start on their own pieces while the previous one drains and complete
+ * after it, so stream order holds at the call's end (pinned host buffers: one
+ * launch, nothing cut).
  *   grads_kind  ZS_RANK_FULL, or ZS_RANK_BUCKET (bucket >= 0; ZeRO-2 staging).
  *   replicas    ZS_RANK_FULL; must not overlap grads. */
 int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int32_t grads_kind,
@@ -372,7 +380,8 @@ int zs_fused_step(zs_plan_t plan, int32_t bucket, const void* const* grads, int3
  *               streaming kernel then runs, as in zs_fused_step).
  *   scale       finite; 1/n_micro for n_micro equal micro-batches.
  *   bucket, master, m, v, replicas, hp, step as in zs_fused_step; replicas must
- *               not overlap acc or micro.  Walked as zs_fused_step.
+ *               not overlap acc or micro.  Walked as zs_fused_step walks a short
+ *               range, at every length.
  * Errors: ZS_ERR_INVALID (nothing enqueued), ZS_ERR_CUDA. */
 int zs_fused_step_accumulate(zs_plan_t plan, int32_t bucket, const void* const* acc, const void* const* micro,
                              int32_t grads_kind, float scale, float* master, float* m, float* v,
@@ -389,13 +398,16 @@ int zs_fused_step_accumulate(zs_plan_t plan, int32_t bucket, const void* const* 
  * call, and the call's work completes in stream order).
  *   launch_mode  ZS_BUCKETS_ONE_WALK: listed buckets that touch are merged
  *                into one range (a run of neighbours, in either order) before
- *                the walk; disjoint runs shorter than 2^16 elements share
+ *                the walk (when they merge into one range of at least 2^24
+ *                elements, it is stepped as zs_fused_step steps a long range:
+ *                one dynamic-order launch); disjoint runs shorter than 2^16 elements share
  *                persistent launches of a list kernel (128 runs per launch)
  *                instead of a launch each; where only the streaming kernel
  *                applies (host buffers, other rank counts) one launch per
  *                range.
  *                ZS_BUCKETS_PER_BUCKET: the buckets are walked one after
- *                another in the order given, no launch spanning two buckets,
+ *                another in the order given (a list of one bucket of at least
+ *                2^24 elements: one dynamic-order launch), no launch spanning two buckets,
  *                as when each is stepped as soon as backward has made it
  *                ready; with a side_stream other than stream, the buckets at
  *                odd positions are walked on side_stream (which first waits
