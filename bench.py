@@ -295,7 +295,8 @@ ZERO3_WALK_CHUNK = 1 << 23     # the ZeRO-3 step's walk chunk (zero3.cu)
 
 
 def zero3_launches(plan, n_d, reshard=True):
-    """Launches of one zs_zero3_step on device buffers: each unit's gathers and its reduce-scatter +
+    """Launches of one zs_zero3_step on device buffers: a unit of at least 2^24 elements at N_d <= 16 takes
+    one dynamic-order launch per gather and for its reduce-scatter + update; other units' gathers and
     update are walks cut like the fused walk (8 Mi-element chunk).  A piece takes the staged kernel
     (bulk-store gather for bodies of at least 2^20 elements; single-output update for rank counts with
     a staged shape, bodies of at least 2^16) plus one streaming launch per ragged end, else one
@@ -307,7 +308,7 @@ def zero3_launches(plan, n_d, reshard=True):
         while lo < hi:
             end = hi
             cut = (lo + C // 4 + C) // C * C
-            if cut < hi - C // 4:
+            if cut < hi - C // 4 and (padded < DYN_MIN or n_d > 16):   # a long unit at N_d <= 16: one dynamic-order launch per phase
                 end = cut
             vlo, vhi = (lo + 7) // 8 * 8, end // 8 * 8
             fringes = (vlo > lo) + (end > vhi)
@@ -584,15 +585,17 @@ class Workload:
         return self.n_d in (2, 4, 8, 16, 32) and (v == zs.ZS_FUSED_TMA or (v == zs.ZS_FUSED_AUTO and big))
 
     def dynamic_order(self):
-        """The fused step runs as one dynamic-order launch (kind fused, whole flat space)."""
-        return (self.kind == "fused" and self.args.step_mode == "whole"
+        """The fused step (plain or with the last micro-batch inside) runs as one dynamic-order launch
+        over the whole flat space."""
+        return (self.kind in ("fused", "accumulate+fused") and self.args.step_mode == "whole"
                 and dyn_range([(0, self.P)], self.n_d, self.staged()))
 
     def kernel_label(self):
         fused = ("k_fused_tma<%d>" if self.staged() else "k_fused<%d>") % self.n_d
         pieces = len(walk_pieces([(0, self.P)], self.n_d, self.staged())) if self.kind != "zero3" else 1
+        dyn = " (one launch, tiles taken in dynamic order)"
         if self.dynamic_order():
-            fused = "k_fused_tma_dyn<%d> (one launch, tiles taken in dynamic order)" % self.n_d
+            fused = "k_fused_tma_dyn<%d>" % self.n_d + dyn
         elif pieces > 1:
             fused += " walked in %d overlapping launches" % pieces
         if self.kind == "fused":
@@ -600,8 +603,12 @@ class Workload:
         if self.kind == "accumulate+fused":
             if self.args.accumulate_mode == "separate":
                 return "%d x k_accumulate + %s" % (self.wl["micro"], fused)
-            return "%d x k_accumulate + %s" % (self.wl["micro"] - 1, fused.replace("k_fused_tma<", "k_fused_tma_acc<")
+            return "%d x k_accumulate + %s" % (self.wl["micro"] - 1, fused.replace("k_fused_tma_dyn<", "k_fused_tma_acc_dyn<")
+                                                .replace("k_fused_tma<", "k_fused_tma_acc<")
                                                 .replace("k_fused<", "k_fused<acc "))
+        if self.n_d <= 16:
+            return ("2 x k_gather_bulk_dyn + k_fused_tma_single_dyn<%d> per unit, one dynamic-order launch each "
+                    "(%d launches per step)" % (self.n_d, zero3_launches(self.plan, self.n_d)))
         return ("2 x k_gather_bulk + k_fused_tma<%d> single output per unit, each walked in launches of 8 Mi elements "
                 "(%d launches per step)" % (self.n_d, zero3_launches(self.plan, self.n_d)))
 

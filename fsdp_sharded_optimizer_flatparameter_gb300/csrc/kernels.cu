@@ -466,8 +466,10 @@ cudaError_t launch_gather(const BView& src, bool src_by_owner, const BView& dst,
         for (int q = 0; q < nd; ++q) ps[q + 1] = dst.ptr.p[q];
         if (all_device(ps, nd + 1)) {
             const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-            cudaError_t e = launch_gather_bulk(src.ptr.p[0], src.off, dst.ptr, dst.off, sp.vlo, sp.nvec << 3, nd, st,
-                                               sync);
+            cudaError_t e = sync == kSyncDynamic && (sp.nvec << 3) >= kDynMinElems
+                                ? launch_gather_bulk_dyn(src.ptr.p[0], src.off, dst.ptr, dst.off, sp.vlo, sp.nvec << 3, nd, st)
+                                : launch_gather_bulk(src.ptr.p[0], src.off, dst.ptr, dst.off, sp.vlo, sp.nvec << 3, nd, st,
+                                                     sync == kSyncDynamic ? (int)kSyncStream : sync);
             if (e != cudaSuccess) return e;
             Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
             for (const Split& f : rest) {
@@ -551,6 +553,22 @@ cudaError_t launch_fused(const BView& g, float* master, float* m, float* v, cons
     if (acc && !broadcast) return cudaErrorNotSupported;
     const bool vec = aligned8(g.off) && aligned8(out.off) && (!acc || aligned8(acc->micro.off));
     Split sp = split_range(r.lo, r.hi, vec);
+    if (sync == kSyncDynamic) {
+        // one output (the ZeRO-3 update): a long body in one dynamic-order launch, then the fringes;
+        // anything else in plain stream order
+        sync = kSyncStream;
+        const int64_t body_hi = sp.vlo + (sp.nvec << 3);
+        if (!broadcast && !acc && (sp.nvec << 3) >= kDynMinElems && fused_dyn_shape(nd) &&
+            g_fused_variant.load() != ZS_FUSED_LDG && staged_policy != kStagedNever &&
+            (staged_policy == kStagedDeviceKnown || fused_ptrs_on_device(g, master, m, v, out, false, nd))) {
+            cudaError_t e = launch_fused_single_dyn(g, master, m, v, out, sp.vlo, sp.nvec << 3, s, nd, st);
+            if (e == cudaSuccess && sp.vlo > sp.lo)
+                e = launch_fused_ldg(g, master, m, v, out, false, split_range(sp.lo, sp.vlo, false), s, nd, st);
+            if (e == cudaSuccess && sp.hi > body_hi)
+                e = launch_fused_ldg(g, master, m, v, out, false, split_range(body_hi, sp.hi, false), s, nd, st);
+            return e;
+        }
+    }
     const int variant = g_fused_variant.load();
     const int64_t min_staged = sync == kSyncStream ? kTmaMinElems : kTmaWalkMinElems;
     const bool want_tma = variant == ZS_FUSED_TMA || (variant == ZS_FUSED_AUTO && (sp.nvec << 3) >= min_staged);
@@ -590,16 +608,16 @@ cudaError_t launch_fused_walk(const BView& g, float* master, float* m, float* v,
                          g_fused_variant.load() != ZS_FUSED_LDG;
     // One long range (the whole flat space, or touching buckets merged): one launch that takes its tiles
     // in dynamic order, then the fringes off the 8-element grid.
-    if (chunked && !acc && ranges.size() == 1 && fused_dyn_shape(nd)) {
+    if (chunked && ranges.size() == 1 && fused_dyn_shape(nd)) {
         const Range& r = ranges[0];
-        const Split sp = split_range(r.lo, r.hi, aligned8(g.off) && aligned8(out.off));
+        const Split sp = split_range(r.lo, r.hi, aligned8(g.off) && aligned8(out.off) && (!acc || aligned8(acc->micro.off)));
         if ((sp.nvec << 3) >= kDynMinElems) {
             const int64_t body_hi = sp.vlo + (sp.nvec << 3);
-            cudaError_t e = launch_fused_tma_dyn(g, master, m, v, out, sp.vlo, sp.nvec << 3, s, nd, st);
+            cudaError_t e = launch_fused_tma_dyn(g, master, m, v, out, sp.vlo, sp.nvec << 3, s, nd, st, acc);
             if (e == cudaSuccess && sp.vlo > sp.lo)
-                e = launch_fused_ldg(g, master, m, v, out, true, split_range(sp.lo, sp.vlo, false), s, nd, st);
+                e = launch_fused_ldg(g, master, m, v, out, true, split_range(sp.lo, sp.vlo, false), s, nd, st, acc);
             if (e == cudaSuccess && sp.hi > body_hi)
-                e = launch_fused_ldg(g, master, m, v, out, true, split_range(body_hi, sp.hi, false), s, nd, st);
+                e = launch_fused_ldg(g, master, m, v, out, true, split_range(body_hi, sp.hi, false), s, nd, st, acc);
             return e;
         }
     }

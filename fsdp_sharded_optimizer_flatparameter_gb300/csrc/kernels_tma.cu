@@ -467,18 +467,38 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma(const __grid_const
 // (DYN in the body).  The launch's counters, order[0] (tiles handed out) and order[1] (CTAs
 // finished), start at zero; the last CTA to finish sets both back to zero for the next launch that
 // draws the same pair.
+__device__ __forceinline__ void dyn_order_finish(unsigned int* order) {
+    __syncthreads();                                      // every thread of the CTA is past the body
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(order + 1, 1u) == gridDim.x - 1) {  // the last CTA: no producer draws any more
+            atomicExch(order, 0u);
+            atomicExch(order + 1, 0u);
+        }
+    }
+}
+
 template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
 __global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_dyn(const __grid_constant__ TmaArgs a) {
     dependent_launch_prologue(kSyncStream);
     fused_tma_body<ND, NCW, VPT, true, MAXST, BUDGET, false, true>(a, a.g, 0, 0.0f);
-    __syncthreads();                                      // every thread of the CTA is past the body
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(a.order + 1, 1u) == gridDim.x - 1) {   // the last CTA: no producer draws any more
-            atomicExch(a.order, 0u);
-            atomicExch(a.order + 1, 0u);
-        }
-    }
+    dyn_order_finish(a.order);
+}
+
+// The same with the last micro-batch's accumulation folded in (as k_fused_tma_acc).
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_acc_dyn(const __grid_constant__ TmaAccArgs x) {
+    dependent_launch_prologue(kSyncStream);
+    fused_tma_body<ND, NCW, VPT, true, MAXST, BUDGET, true, true>(x.a, x.micro, x.micro_off, x.scale);
+    dyn_order_finish(x.a.order);
+}
+
+// The single-output step (the ZeRO-3 reduce-scatter + update of one unit) in one dynamic-order launch.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_fused_tma_single_dyn(const __grid_constant__ TmaArgs a) {
+    dependent_launch_prologue(kSyncStream);
+    fused_tma_body<ND, NCW, VPT, false, MAXST, BUDGET, false, true>(a, a.g, 0, 0.0f);
+    dyn_order_finish(a.order);
 }
 
 template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
@@ -664,6 +684,7 @@ struct GatherBulkArgs {
     int T;                // elements per tile (multiple of 8)
     long long wait_limit, drain_limit;
     int sync;             // LaunchSync: the loads are bulk copies, so a later launch of a walk may stream at once
+    unsigned int* order;  // k_gather_bulk_dyn: the launch's tile and finish counters
 };
 
 template <int S>
@@ -722,6 +743,71 @@ __global__ void __launch_bounds__(32) k_gather_bulk(const __grid_constant__ Gath
         for (int64_t k = j; k < issued; ++k) mbar_wait(&bar[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
     bulk_wait_all();
     dependent_launch_epilogue(a.sync);
+}
+
+// The gather in one dynamic-order launch: lane 0 takes each next tile from the launch's tile counter
+// (a.order[0]) and records it in the stage (rec[s]) before the stage's bulk load; the warp reads the
+// record after a __syncwarp.  A record past the last tile ends the CTA; the last CTA to finish sets
+// the counters back to zero (dyn_order_finish).
+template <int S>
+__global__ void __launch_bounds__(32) k_gather_bulk_dyn(const __grid_constant__ GatherBulkArgs a) {
+    static_assert(S <= 8, "barriers and records share the first 128 bytes");
+    dependent_launch_prologue(kSyncStream);
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    int64_t* rec = reinterpret_cast<int64_t*>(smem + 64);
+    uint16_t* buf = reinterpret_cast<uint16_t*>(smem + 128);
+    const int lane = threadIdx.x;
+    const int T = a.T;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const int64_t ntiles = (a.n + T - 1) / T;
+    auto take = [&](int s) {                             // lane 0: the next tile into stage s
+        const int64_t tl = (int64_t)atomicAdd(a.order, 1u);
+        rec[s] = tl;
+        if (tl < ntiles) {
+            const int64_t rem = a.n - tl * T;
+            const uint32_t len = (uint32_t)(rem < T ? rem : T);
+            mbar_expect_tx(&bar[s], len * 2u);
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             su32(buf + (size_t)s * T)),
+                         "l"(a.src + (a.lo + tl * T - a.src_off)), "r"(len * 2u), "r"(su32(&bar[s]))
+                         : "memory");
+        }
+    };
+    if (lane == 0)
+        for (int s = 0; s < S; ++s) take(s);
+    __syncwarp();
+    int64_t j = 0;
+    bool ok = true;
+    for (;; ++j) {
+        const int s = (int)(j % S);
+        const int64_t tl = rec[s];
+        if (tl >= ntiles) break;
+        if (!mbar_wait(&bar[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
+            flag_error(ZS_DEVERR_GATHER_WAIT);
+            ok = false;
+            break;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const int64_t i = a.lo + tl * T;
+        const int64_t rem = a.n - tl * T;
+        const uint32_t bytes = (uint32_t)(rem < T ? rem : T) * 2u;
+        for (int q = lane; q < a.nd; q += 32) bulk_store(a.dst.p[q] + (i - a.dst_off), buf + (size_t)s * T, bytes);
+        bulk_commit();
+        bulk_wait_read_all();                            // every lane's stores have read the stage
+        __syncwarp();
+        if (lane == 0) take(s);
+        __syncwarp();
+    }
+    if (!ok && lane == 0)                                // loads still in flight into the ring
+        for (int64_t k = j; k < j + S; ++k)
+            if (rec[k % S] < ntiles) mbar_wait(&bar[k % S], (uint32_t)((k / S) & 1), a.drain_limit);
+    bulk_wait_all();
+    dyn_order_finish(a.order);
 }
 
 namespace {
@@ -983,18 +1069,34 @@ cudaError_t dyn_order_pair(unsigned int** out) {
     return cudaSuccess;
 }
 
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
-cudaError_t dyn_impl(TmaArgs a, cudaStream_t st) {
-    using Sh = TmaShape<ND, NCW, VPT, MAXST, BUDGET>;
-    auto kern = k_fused_tma_dyn<ND, NCW, VPT, MAXST, BUDGET>;
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool BROADCAST>
+auto dyn_kernel(const TmaArgs*) {
+    if constexpr (BROADCAST)
+        return k_fused_tma_dyn<ND, NCW, VPT, MAXST, BUDGET>;
+    else
+        return k_fused_tma_single_dyn<ND, NCW, VPT, MAXST, BUDGET>;
+}
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool BROADCAST>
+auto dyn_kernel(const TmaAccArgs*) {
+    static_assert(BROADCAST, "the accumulating step has the broadcast form only");
+    return k_fused_tma_acc_dyn<ND, NCW, VPT, MAXST, BUDGET>;
+}
+TmaArgs& base_args(TmaArgs& a) { return a; }
+TmaArgs& base_args(TmaAccArgs& x) { return x.a; }
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool BROADCAST = true, class Args>
+cudaError_t dyn_impl(Args a, cudaStream_t st) {
+    using Sh = TmaShape<std::is_same<Args, TmaAccArgs>::value ? 2 * ND : ND, NCW, VPT, MAXST, BUDGET>;
+    auto kern = dyn_kernel<ND, NCW, VPT, MAXST, BUDGET, BROADCAST>(static_cast<const Args*>(nullptr));
     int sms = 0, per_sm = 0;
     cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
-    const int64_t ntiles = (a.n + Sh::kT - 1) / Sh::kT;
+    TmaArgs& b = base_args(a);
+    const int64_t ntiles = (b.n + Sh::kT - 1) / Sh::kT;
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
     const int grid = (int)(ntiles < cap ? ntiles : cap);
-    e = dyn_order_pair(&a.order);
+    e = dyn_order_pair(&b.order);
     if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(grid), dim3(32 * (NCW + 1)), Sh::kSmem, st, a);
 }
@@ -1002,6 +1104,27 @@ cudaError_t dyn_impl(TmaArgs a, cudaStream_t st) {
 }  // namespace
 
 bool fused_dyn_shape(int nd) { return nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32; }
+
+// The single-output step (ZeRO-3 reduce-scatter + update; out.p[0] the shard array) over the 8-aligned
+// body [lo, lo + n) in one dynamic-order launch, with the single-output walk shapes' tiles and rings
+// (two-stage rings under half an SM).
+cudaError_t launch_fused_single_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
+                                    int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+    bool ok = body_ok(lo, n) && at_ok(master, lo) && at_ok(m, lo) && at_ok(v, lo) && at_ok(out.ptr.p[0], lo - out.off);
+    for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off);
+    if (!ok) return cudaErrorMisalignedAddress;
+    TmaArgs a = make_args(g, master, m, v, out, s, nd);
+    a.lo = lo;
+    a.n = n;
+    switch (nd) {
+        case 2: return dyn_impl<2, 8, 8, 2, 115712, false>(a, st);
+        case 4: return dyn_impl<4, 8, 8, 2, 115712, false>(a, st);
+        case 8: return dyn_impl<8, 8, 8, 2, 115712, false>(a, st);
+        case 16: return dyn_impl<16, 8, 4, 2, 115712, false>(a, st);
+        case 32: return dyn_impl<32, 4, 4, 2, 115712, false>(a, st);
+        default: return cudaErrorNotSupported;
+    }
+}
 
 // The broadcast fused step over the 8-aligned body [lo, lo + n) in one dynamic-order launch.  Shapes from
 // a measured comparison on GB300 (the 2^28+7-element buffer, against the walk of 4 Mi-element launches
@@ -1011,13 +1134,33 @@ bool fused_dyn_shape(int nd) { return nd == 2 || nd == 4 || nd == 8 || nd == 16 
 // (99.4 %); N_d = 32: 4 x 4 (T 512), 2 stages: 102.0 % (97.5 %).  Rings of at most half an SM's shared
 // memory, two CTAs per SM.
 cudaError_t launch_fused_tma_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
-                                 int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
+                                 int64_t n, const AdamScalars& s, int nd, cudaStream_t st, const AccumIn* acc) {
     bool ok = body_ok(lo, n) && at_ok(master, lo) && at_ok(m, lo) && at_ok(v, lo);
     for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off) && at_ok(out.ptr.p[q], lo - out.off);
+    for (int q = 0; acc && q < nd && ok; ++q) ok = at_ok(acc->micro.ptr.p[q], lo - acc->micro.off);
     if (!ok) return cudaErrorMisalignedAddress;
     TmaArgs a = make_args(g, master, m, v, out, s, nd);
     a.lo = lo;
     a.n = n;
+    if (acc) {
+        TmaAccArgs x;
+        x.a = a;
+        x.micro = acc->micro.ptr;
+        x.micro_off = acc->micro.off;
+        x.scale = acc->scale;
+        // A stage holds 2 N_d bf16 tiles: rings under half an SM.  N_d = 8 measured on GB300 (GPT-2-small,
+        // the accumulating step alone, of the measured copy rate): 8 warps x 4 (T 1024), 2 stages 103.2 %,
+        // 4 x 8 102.8 %, T 512 with 4 stages 101.5 %, T 2048 in a whole SM 101.3 %, against 101.0 % for
+        // the walk on the same box; the other rank counts take tiles of the same bytes per stage.
+        switch (nd) {
+            case 2: return dyn_impl<2, 4, 8, 4, 115712>(x, st);
+            case 4: return dyn_impl<4, 4, 8, 4, 115712>(x, st);
+            case 8: return dyn_impl<8, 8, 4, 4, 115712>(x, st);
+            case 16: return dyn_impl<16, 4, 4, 4, 115712>(x, st);
+            case 32: return dyn_impl<32, 2, 4, 4, 115712>(x, st);
+            default: return cudaErrorNotSupported;
+        }
+    }
     switch (nd) {
         case 2: return dyn_impl<2, 4, 8, 4, 115712>(a, st);
         case 4: return dyn_impl<4, 4, 8, 4, 115712>(a, st);
@@ -1689,6 +1832,38 @@ cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs&
     const int64_t cap = (int64_t)sms * 16;
     const int grid = (int)(ntiles < cap ? ntiles : cap);
     return launch_kernel(k_gather_bulk<S>, dim3(grid), dim3(32), smem, st, a);
+}
+
+// The single-source gather over the 8-aligned body [lo, lo + n) in one dynamic-order launch: 16,384-element
+// tiles in a 2-stage ring (65,664 B, three CTAs per SM), one wave of resident CTAs.
+cudaError_t launch_gather_bulk_dyn(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
+                                   int64_t n, int nd, cudaStream_t st) {
+    bool ok = body_ok(lo, n) && at_ok(src, lo - src_off);
+    for (int q = 0; q < nd && ok; ++q) ok = at_ok(dst.p[q], lo - dst_off);
+    if (!ok) return cudaErrorMisalignedAddress;
+    GatherBulkArgs a{};
+    a.src = src;
+    a.src_off = src_off;
+    a.dst = dst;
+    a.dst_off = dst_off;
+    a.lo = lo;
+    a.n = n;
+    a.nd = nd;
+    a.T = 16384;
+    a.wait_limit = 4000000000LL;
+    a.drain_limit = 4000000000LL;
+    a.sync = kSyncStream;
+    constexpr int S = 2;
+    const int smem = 128 + S * a.T * 2;
+    int sms = 0, per_sm = 0;
+    cudaError_t e = staged_geometry((const void*)k_gather_bulk_dyn<S>, 32, smem, &sms, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (n + a.T - 1) / a.T;
+    const int64_t cap = (int64_t)sms * per_sm;
+    const int grid = (int)(ntiles < cap ? ntiles : cap);
+    e = dyn_order_pair(&a.order);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k_gather_bulk_dyn<S>, dim3(grid), dim3(32), smem, st, a);
 }
 
 cudaError_t read_device_error(unsigned int* out, bool clear) {

@@ -41,7 +41,10 @@ struct AdamScalars {
 //                  exiting, so the launch completes after every launch before it.  Valid only when the
 //                  kernel touches no byte that an earlier launch of the walk touches, and it reads
 //                  global memory only through bulk copies (which read L2, never a stale L1 line).
-enum LaunchSync : int { kSyncStream = 0, kSyncWalkFirst = 1, kSyncWalkNext = 2 };
+//   kSyncDynamic   (launch_fused with one output, launch_gather) one launch over the whole range whose
+//                  CTAs take their tiles in dynamic order from a counter pair (kDynMinElems and more
+//                  elements on device buffers, else plain stream order); in stream order otherwise.
+enum LaunchSync : int { kSyncStream = 0, kSyncWalkFirst = 1, kSyncWalkNext = 2, kSyncDynamic = 3 };
 
 // A global range [lo, hi) inside one unit (base, shard); owner(i) = (i - base) / shard.
 struct Range {
@@ -94,7 +97,12 @@ bool fused_walk_shape(int nd, bool acc = false);
 bool fused_dyn_shape(int nd);
 constexpr int64_t kDynMinElems = int64_t(1) << 24;
 cudaError_t launch_fused_tma_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
-                                 int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
+                                 int64_t n, const AdamScalars& s, int nd, cudaStream_t st,
+                                 const AccumIn* acc = nullptr);
+cudaError_t launch_fused_single_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
+                                    int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
+cudaError_t launch_gather_bulk_dyn(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
+                                   int64_t n, int nd, cudaStream_t st);
 // The broadcast fused step over disjoint ranges as a walk: ranges longer than kFusedWalkChunk are cut
 // at multiples of it, each piece is one launch, the first on the stream kSyncWalkFirst and the others
 // kSyncWalkNext, so every launch streams its piece while the previous one drains.  Without a walk

@@ -93,8 +93,8 @@ def test_walk_launch_counts_match_the_recorded_launch_lists():
     """The launch counts bench.py reports for walked calls follow the library's piece cutting; pinned
     to the counts ncu's launch lists of the benchmarked steps show (profiles/launches_*.md): one
     dynamic-order launch per Llama-1.3B ZeRO-2 step (321 walked launches for the update on its shard
-    arrays, 360 for the step bucket by bucket over its 103 buckets), 1,640 gathers + 820 updates per
-    Llama-7B ZeRO-3 step."""
+    arrays, 360 for the step bucket by bucket over its 103 buckets), 66 gathers + 33 updates per
+    Llama-7B ZeRO-3 step (one dynamic-order launch per unit and phase)."""
     import fsdp_sharded_optimizer_flatparameter_gb300 as zs
     import synth
 
@@ -107,8 +107,10 @@ def test_walk_launch_counts_match_the_recorded_launch_lists():
     assert plan13.n_buckets == 103 and bench.walk_launches(br, 8) == 360
     shapes, units = synth.workload_params("llama-7b")
     plan = zs.Plan(shapes, 16, stage=3, unit_of_param=units)
-    assert bench.zero3_launches(plan, 16) == 2460
-    assert bench.zero3_launches(plan, 16, reshard=False) == 1640
+    assert bench.zero3_launches(plan, 16) == 99
+    assert bench.zero3_launches(plan, 16, reshard=False) == 66
+    flat32 = zs.Plan([((1 << 28) + 7,)], 32, stage=3)                 # N_d = 32 keeps the walk
+    assert bench.zero3_launches(flat32, 32) == 32 * 3
     # short, ragged and unaligned ranges
     assert bench.staged_walk_launches([(0, 1000)]) == 1
     assert bench.staged_walk_launches([(3, (1 << 21) + 5)]) == 3          # body plus two ragged ends

@@ -67,10 +67,12 @@ def _oracle_step(accs, p0, m0, v0, t):
 
 @pytest.mark.parametrize("variant", ["auto", "ldg"])
 @pytest.mark.parametrize("n_d,numel", [(1, 4099), (2, 3 * (1 << 22) + 13), (3, 100_003), (4, 5_000_011),
-                                       (8, 2 * (1 << 22) + 4099), (8, 1001), (16, 1_048_583), (32, 600_007)])
+                                       (8, 2 * (1 << 22) + 4099), (8, 1001), (16, 1_048_583), (32, 600_007),
+                                       (8, (1 << 24) + 4099), (2, (1 << 24) + 11)])
 def test_fused_step_accumulate_matches_oracle(variant, n_d, numel):
     """Two steps (the second with non-zero moments): every element of master, m, v and of every
-    replica against the oracle; the accumulators and micro-batch buffers are left as they were."""
+    replica against the oracle; the accumulators and micro-batch buffers are left as they were.
+    Buffers of 2^24 elements and more run as one dynamic-order launch (plus the ragged end)."""
     if variant == "ldg":
         zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
     plan, micro, acc, master, m, v, reps = _setup(n_d, [(numel,)], seed=30 + n_d)
