@@ -1,15 +1,15 @@
 """Race checks of the overlapping launches at the benchmarked sizes (GPU).
 
 The benchmarked fused step is one launch whose CTAs take their tiles in dynamic order from a
-counter, and the ZeRO-3 step walks its gathers and updates (each launch streaming its piece while its
-predecessor drains) on a side stream.  A race there would show as a run-to-run difference,
+counter, and the ZeRO-3 step runs its gathers and updates on two streams, each unit's phase one such
+launch (units of 2^24 elements and more) or walked in overlapping launches.  A race there would show as a run-to-run difference,
 so each step below runs repeatedly from the same state and must equal, bit for bit, a reference run
 of the same step:
 
 * the Llama-1.3B ZeRO-2 step at N_d = 8, the call the benchmark times (one dynamic-order launch),
   ten times (1.3e10 element-steps), against the register-streaming kernel;
-* the ZeRO-3 step on the Llama-1.3B units at N_d = 8 (25 units, each unit's gathers and update
-  walked, two streams, the 2-slot pool), five times, against the same step with programmatic
+* the ZeRO-3 step on the Llama-1.3B units at N_d = 8 (25 units of ~50 M elements, each unit's gathers
+  and update one dynamic-order launch, two streams, the 2-slot pool), five times, against the same step with programmatic
   dependent launch off (every launch waiting for the previous one to complete) on one stream.
 
 The oracle itself is not needed here: every-element oracle parity of these calls is in
