@@ -270,10 +270,11 @@ def walk_launches(ranges, n_d, staged_ok=True):
 
 
 def staged_walk_launches(ranges):
-    """Launches of a call that walks each range's 8-aligned body of at least 2^20 elements with a staged
-    kernel in pieces (cut like the fused walk) plus one streaming launch per ragged end, and gives a
-    shorter range one streaming launch: zs_adamw_shard_step on one-array buffers (per unit range), and
-    zs_all_reduce_mean and zs_dp_step on device buffers at a rank count with a walk shape."""
+    """Launches of a call that gives each range's 8-aligned body of at least 2^24 elements one
+    dynamic-order launch, walks a body of at least 2^20 elements with a staged kernel in pieces (cut like
+    the fused walk), adds one streaming launch per ragged end, and gives a shorter range one streaming
+    launch: zs_adamw_shard_step on one-array buffers (per unit range), and zs_all_reduce_mean and
+    zs_dp_step on device buffers at N_d = 4, 8 or 16 (rank counts with both forms)."""
     n, C = 0, WALK_CHUNK
     for lo, hi in ranges:
         vlo, vhi = (lo + 7) // 8 * 8, hi // 8 * 8
@@ -281,6 +282,9 @@ def staged_walk_launches(ranges):
             n += 1 if hi > lo else 0
             continue
         n += (vlo > lo) + (hi > vhi)
+        if vhi - vlo >= DYN_MIN:
+            n += 1
+            continue
         while vlo < vhi:
             end = vhi
             cut = (vlo + C // 4 + C) // C * C
@@ -893,8 +897,9 @@ def run_next(args, ws, rank, local):
         t[0] += 1
         zs.zs_dp_step(plan, grads, master, mm, vv, reps, hp, t[0], stream=stream)
 
-    n_dp = staged_walk_launches([(0, P)])          # walked at N_d = 8
-    row("naive DP step (k_dp_tma walked: all-reduce-mean + replicated AdamW), %s, N_d=8" % dp_label, timed(dp),
+    n_dp = staged_walk_launches([(0, P)])          # one dynamic-order launch (walked below 2^24 elements)
+    row("naive DP step (k_dp_tma_dyn, one dynamic-order launch: all-reduce-mean + replicated AdamW), %s, N_d=8"
+        % dp_label, timed(dp),
         plan.numel, 28 * n_d * P, n_dp)
     launches += steps * n_dp
     zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
@@ -909,7 +914,8 @@ def run_next(args, ws, rank, local):
         zs.zs_all_reduce_mean(plan, -1, grads, stream=stream)
 
     n_ar = staged_walk_launches([(0, P)])
-    row("naive DP all-reduce-mean alone (k_ar_tma, walked), %s, N_d=8" % dp_label, timed(ar), plan.numel,
+    row("naive DP all-reduce-mean alone (k_ar_tma_dyn, one dynamic-order launch), %s, N_d=8" % dp_label, timed(ar),
+        plan.numel,
         4 * n_d * P, n_ar)
     launches += steps * n_ar
     z_master, z_m, z_v = master0.clone(), torch.zeros_like(master0), torch.zeros_like(master0)

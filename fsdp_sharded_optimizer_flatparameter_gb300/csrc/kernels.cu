@@ -408,6 +408,8 @@ cudaError_t launch_rs_mean(const BView& g, const BView& out, bool out_by_owner, 
 // reads global memory through bulk copies only).
 static cudaError_t adamw_tma_walk(const BView& grad, float* master, float* m, float* v, const BView& par, int64_t lo,
                                   int64_t hi, const AdamScalars& s, cudaStream_t st) {
+    if (hi - lo >= kDynMinElems)      // one launch, tiles in dynamic order
+        return launch_fused_single_dyn(grad, master, m, v, par, lo, hi - lo, s, 1, st);
     return walk_range(lo, hi, kFusedWalkChunk, [&](int64_t a, int64_t b, int sync) {
         return launch_fused_tma(grad, master, m, v, par, false, a, b - a, s, 1, st, sync);
     });
@@ -840,9 +842,10 @@ static cudaError_t dp_step_impl(const BView& g, const BView& out, float* const* 
 
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st) {
     const Split sp = split_range(r.lo, r.hi, aligned8(g.off));
-    // a body of at least kTmaMinElems in device memory: the staged kernel, walked (pieces cut as in
-    // launch_fused_walk, the first waiting for the stream's predecessor, the others streaming while the
-    // previous one drains); fringes, short ranges, host memory and other rank counts stream
+    // a body of at least kTmaMinElems in device memory: the staged kernel, in one dynamic-order launch
+    // from kDynMinElems on where the rank count has a dynamic-order shape, else walked (pieces cut as in launch_fused_walk, the first waiting for the
+    // stream's predecessor, the others streaming while the previous one drains); fringes, short
+    // ranges, host memory and other rank counts stream
     const int64_t body = sp.nvec << 3;
     if (body >= kTmaMinElems && g_fused_variant.load() != ZS_FUSED_LDG &&
         (nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32)) {
@@ -850,9 +853,11 @@ cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaS
         for (int q = 0; q < nd; ++q) ps[q] = g.ptr.p[q];
         if (all_device(ps, nd)) {
             const int64_t body_hi = sp.vlo + body;
-            cudaError_t e = walk_range(sp.vlo, body_hi, kFusedWalkChunk, [&](int64_t a, int64_t b, int sync) {
-                return launch_all_reduce_tma(g, a, b - a, nd, st, sync);
-            });
+            cudaError_t e = body >= kDynMinElems && ar_dyn_shape(nd)
+                                ? launch_all_reduce_tma(g, sp.vlo, body, nd, st, kSyncDynamic)
+                                : walk_range(sp.vlo, body_hi, kFusedWalkChunk, [&](int64_t a, int64_t b, int sync) {
+                                      return launch_all_reduce_tma(g, a, b - a, nd, st, sync);
+                                  });
             Split rest[2] = {split_range(sp.lo, sp.vlo, false), split_range(body_hi, sp.hi, false)};
             for (const Split& f : rest) {
                 if (e != cudaSuccess || f.hi <= f.lo) continue;
@@ -897,12 +902,14 @@ cudaError_t launch_dp_step(const BView& g, const BView& out, float* const* maste
         staged = all_device(ps, n);
     }
     if (!staged) return dp_step_ldg(g, out, master, m, v, sp, s, nd, st);
-    // the body walked where the rank count has a walk shape (pieces cut as in launch_fused_walk, the first
-    // waiting for the stream's predecessor, the others streaming while the previous one drains), else
-    // one launch; then the fringes
+    // where the rank count has a walk shape, a body of kDynMinElems or more in one dynamic-order launch
+    // (the walk's shapes), a shorter one walked (pieces cut as in launch_fused_walk, the first waiting for the stream's
+    // predecessor, the others streaming while the previous one drains), else one launch; then the fringes
     const int64_t body_hi = sp.vlo + (sp.nvec << 3);
     cudaError_t e = cudaSuccess;
-    if (dp_walk_shape(nd)) {
+    if ((sp.nvec << 3) >= kDynMinElems && dp_walk_shape(nd)) {
+        e = launch_dp_tma(g, out, master, m, v, sp.vlo, sp.nvec << 3, s, nd, st, kSyncDynamic);
+    } else if (dp_walk_shape(nd)) {
         e = walk_range(sp.vlo, body_hi, kFusedWalkChunk, [&](int64_t a, int64_t b, int sync) {
             return launch_dp_tma(g, out, master, m, v, a, b - a, s, nd, st, sync);
         });

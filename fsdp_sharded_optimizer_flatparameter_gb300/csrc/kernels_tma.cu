@@ -1105,9 +1105,9 @@ cudaError_t dyn_impl(Args a, cudaStream_t st) {
 
 bool fused_dyn_shape(int nd) { return nd == 2 || nd == 4 || nd == 8 || nd == 16 || nd == 32; }
 
-// The single-output step (ZeRO-3 reduce-scatter + update; out.p[0] the shard array) over the 8-aligned
-// body [lo, lo + n) in one dynamic-order launch, with the single-output walk shapes' tiles and rings
-// (two-stage rings under half an SM).
+// The single-output step (ZeRO-3 reduce-scatter + update; out.p[0] the shard array; with one rank, the
+// update alone on a reduced gradient) over the 8-aligned body [lo, lo + n) in one dynamic-order launch,
+// with the single-output walk shapes' tiles and rings (two-stage rings under half an SM).
 cudaError_t launch_fused_single_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
                                     int64_t n, const AdamScalars& s, int nd, cudaStream_t st) {
     bool ok = body_ok(lo, n) && at_ok(master, lo) && at_ok(m, lo) && at_ok(v, lo) && at_ok(out.ptr.p[0], lo - out.off);
@@ -1117,6 +1117,9 @@ cudaError_t launch_fused_single_dyn(const BView& g, float* master, float* m, flo
     a.lo = lo;
     a.n = n;
     switch (nd) {
+        // the update alone, in the walk's shape: 104.9 / 103.0 % of the measured copy rate on the
+        // Llama-1.3B / GPT-2-small buffers against 102.9-103.0 / 101.0-101.1 % walked (GB300)
+        case 1: return dyn_impl<1, 8, 8, 2, 115712, false>(a, st);
         case 2: return dyn_impl<2, 8, 8, 2, 115712, false>(a, st);
         case 4: return dyn_impl<4, 8, 8, 2, 115712, false>(a, st);
         case 8: return dyn_impl<8, 8, 8, 2, 115712, false>(a, st);
@@ -1245,6 +1248,7 @@ struct RsTmaArgs {
     float inv_nd;
     long long wait_limit, drain_limit;
     int sync;             // LaunchSync (the in-place all-reduce's walk; the reduce-scatter keeps stream order)
+    unsigned int* order;  // the dynamic-order launch's counter pair (k_ar_tma_dyn), else unused
 };
 
 template <int ND, int NCW, int VPT, int MAXST = 16, int BUDGET = 227 * 1024>
@@ -1261,15 +1265,17 @@ struct RsShape {
 // ALL: the in-place all-reduce with averaging of naive DP ("Infra: Data Parallel", Naive Data
 // Parallelism): the mean goes back into every rank's own buffer (a.g) instead of one output array.  A
 // tile's copies into shared memory complete before any consumer stores into it, and tiles are
-// disjoint, so in place is safe.
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL>
+// disjoint, so in place is safe.  DYN: tiles in dynamic order, as in fused_tma_body.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL, bool DYN = false>
 __device__ __forceinline__ void rs_tma_body(const RsTmaArgs& a) {
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
     constexpr int S = Sh::kStages;
+    static_assert(!DYN || S <= 8, "the dynamic order's stage records sit behind the barriers");
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + S;
+    int64_t* rec = reinterpret_cast<int64_t*>(smem + 128);   // DYN: the tile of each stage
     uint8_t* stages = smem + 256;
 
     const int warp = threadIdx.x >> 5;
@@ -1291,12 +1297,20 @@ __device__ __forceinline__ void rs_tma_body(const RsTmaArgs& a) {
             const uint64_t pol = evict_first_policy();
             int64_t j = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+            for (int64_t tile = DYN ? 0 : blockIdx.x; DYN || tile < ntiles; tile += gridDim.x, ++j) {
                 const int s = (int)(j % S);
                 if (j >= S && !mbar_wait(&empty[s], (uint32_t)(((j / S) - 1) & 1), a.wait_limit)) {
                     flag_error(ZS_DEVERR_PRODUCER_WAIT);
                     ok = false;
                     break;
+                }
+                if constexpr (DYN) {
+                    tile = (int64_t)atomicAdd(a.order, 1u);
+                    rec[s] = tile;                        // published by the arrive below (release)
+                    if (tile >= ntiles) {
+                        mbar_arrive(&full[s]);            // no copies: the consumers read the end mark
+                        break;
+                    }
                 }
                 const int64_t i0 = a.lo + tile * T;
                 const int64_t rem = a.n - tile * T;
@@ -1320,11 +1334,15 @@ __device__ __forceinline__ void rs_tma_body(const RsTmaArgs& a) {
     const int ct = threadIdx.x - 32;
     const int e = ct * VPT;
     int64_t j = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+    for (int64_t tile = DYN ? 0 : blockIdx.x; DYN || tile < ntiles; tile += gridDim.x, ++j) {
         const int s = (int)(j % S);
         if (!mbar_wait(&full[s], (uint32_t)((j / S) & 1), a.wait_limit)) {
             flag_error(ZS_DEVERR_CONSUMER_WAIT);
             return;
+        }
+        if constexpr (DYN) {
+            tile = rec[s];
+            if (tile >= ntiles) return;                   // the producer's end mark
         }
         const int64_t i0 = a.lo + tile * T;
         const int64_t rem = a.n - tile * T;
@@ -1383,20 +1401,32 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_ar_tma(const __grid_constant
     dependent_launch_epilogue(a.sync);
 }
 
-namespace {
-
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL>
-auto rs_kernel() {
-    if constexpr (ALL)
-        return k_ar_tma<ND, NCW, VPT, MAXST, BUDGET>;
-    else
-        return k_rs_tma<ND, NCW, VPT, MAXST, BUDGET>;
+// The in-place all-reduce over one range in one persistent launch taking its tiles in dynamic order.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_ar_tma_dyn(const __grid_constant__ RsTmaArgs a) {
+    dependent_launch_prologue(kSyncStream);
+    rs_tma_body<ND, NCW, VPT, MAXST, BUDGET, true, true>(a);
+    dyn_order_finish(a.order);
 }
 
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL = false>
-cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
+namespace {
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL, bool DYN>
+auto rs_kernel() {
+    if constexpr (DYN) {
+        static_assert(ALL, "the reduce-scatter has no dynamic-order form");
+        return k_ar_tma_dyn<ND, NCW, VPT, MAXST, BUDGET>;
+    } else if constexpr (ALL) {
+        return k_ar_tma<ND, NCW, VPT, MAXST, BUDGET>;
+    } else {
+        return k_rs_tma<ND, NCW, VPT, MAXST, BUDGET>;
+    }
+}
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL = false, bool DYN = false>
+cudaError_t rs_tma_impl(RsTmaArgs a, cudaStream_t st) {
     using Sh = RsShape<ND, NCW, VPT, MAXST, BUDGET>;
-    auto kern = rs_kernel<ND, NCW, VPT, MAXST, BUDGET, ALL>();
+    auto kern = rs_kernel<ND, NCW, VPT, MAXST, BUDGET, ALL, DYN>();
     int sms = 0, per_sm = 0;
     cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
@@ -1404,6 +1434,10 @@ cudaError_t rs_tma_impl(const RsTmaArgs& a, cudaStream_t st) {
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;
     const int grid = (int)(ntiles < cap ? ntiles : cap);
+    if constexpr (DYN) {
+        e = dyn_order_pair(&a.order);
+        if (e != cudaSuccess) return e;
+    }
     return launch_kernel(kern, dim3(grid), dim3(32 * (NCW + 1)), Sh::kSmem, st, a);
 }
 
@@ -1422,6 +1456,7 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
     a.wait_limit = 4000000000LL;
     a.drain_limit = 4000000000LL;
     a.sync = kSyncStream;
+    a.order = nullptr;
     return a;
 }
 
@@ -1460,6 +1495,19 @@ cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd,
     for (int q = 0; q < nd && ok; ++q) ok = at_ok(g.ptr.p[q], lo - g.off);
     if (!ok) return cudaErrorMisalignedAddress;
     RsTmaArgs a = rs_args(g, lo, n, nd);
+    if (sync == kSyncDynamic) {
+        // One launch over the whole range, tiles in dynamic order, with the walk's tiles and rings.
+        // Measured on GB300 against the walk (GPT-2-small buffers, of the measured copy rate): N_d = 4 /
+        // 8 / 16 / 32: 102.3 / 103.2 / 103.1 / 102.5 % (walk 98.1-98.4 / 101.8-101.9 / 101.1-101.2 /
+        // 100.2 %); N_d = 2: 100.8 % against 101.1-101.3 %, so that rank count keeps the walk.
+        switch (nd) {
+            case 4: return rs_tma_impl<4, 8, 8, 2, 232448, true, true>(a, st);
+            case 8: return rs_tma_impl<8, 8, 8, 2, 232448, true, true>(a, st);
+            case 16: return rs_tma_impl<16, 8, 4, 2, 232448, true, true>(a, st);
+            case 32: return rs_tma_impl<32, 2, 4, 2, 232448, true, true>(a, st);
+            default: return cudaErrorNotSupported;
+        }
+    }
     a.sync = sync;
     switch (nd) {
         case 2: return rs_tma_impl<2, 8, 8, 2, 232448, true>(a, st);
@@ -1470,6 +1518,8 @@ cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd,
         default: return cudaErrorNotSupported;
     }
 }
+
+bool ar_dyn_shape(int nd) { return nd == 4 || nd == 8 || nd == 16 || nd == 32; }
 
 // ------------------------------------------------------------------ naive-DP step, staged
 // "Infra: Data Parallel", section "Naive Data Parallelism": every rank keeps the full fp32 state
@@ -1496,6 +1546,7 @@ struct DpTmaArgs {
     float inv_nd;
     long long wait_limit, drain_limit;
     int sync;             // LaunchSync: the loads are bulk copies, so a later launch of a walk may stream at once
+    unsigned int* order;  // the dynamic-order launch's counter pair (k_dp_tma_dyn), else unused
 };
 
 // Consumers index the ranks at run time (one copy of the update code, not N_d): the rank pointers
@@ -1519,10 +1570,12 @@ struct DpShape {
     static constexpr int kStages = kFit > MAXST ? MAXST : kFit;
     static constexpr int kSmem = kHead + 2 * kGradBytes + kStages * kStageBytes;
     static_assert(kStages >= 2, "tile too large for a 2-stage ring");
-    static_assert((4 + 2 * kStages) * 8 <= kBarBytes, "barriers must fit in their block");
+    static_assert((4 + 2 * kStages) * 8 + 16 <= kBarBytes, "barriers and tile records must fit in their block");
 };
 
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+// DYN: tiles in dynamic order, as in fused_tma_body; the producer draws a tile per grads buffer and
+// publishes it in the buffer's record, which the buffer's full barrier releases to the consumers.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool DYN = false>
 __device__ __forceinline__ void dp_tma_body(const DpTmaArgs& a) {
     using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
     constexpr int T = Sh::kT;
@@ -1532,6 +1585,7 @@ __device__ __forceinline__ void dp_tma_body(const DpTmaArgs& a) {
     uint64_t* gempty = gfull + 2;                            // [2] grads buffer b folded
     uint64_t* full = gfull + 4;                              // [S] state stage s loaded
     uint64_t* empty = full + S;                              // [S] state stage s consumed
+    int64_t* rec = reinterpret_cast<int64_t*>(smem + Sh::kBarBytes - 16);   // [2] DYN: grads buffer b's tile
     DpTable<ND>* tab = reinterpret_cast<DpTable<ND>*>(smem + Sh::kBarBytes);
     uint16_t* gbuf = reinterpret_cast<uint16_t*>(smem + Sh::kHead);
     uint8_t* stages = smem + Sh::kHead + 2 * Sh::kGradBytes;
@@ -1571,12 +1625,20 @@ __device__ __forceinline__ void dp_tma_body(const DpTmaArgs& a) {
             int64_t j = 0;        // state stages issued
             int64_t gi = 0;       // grads buffers issued (= tiles started)
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            for (int64_t tile = DYN ? 0 : blockIdx.x; (DYN || tile < ntiles) && ok; tile += gridDim.x) {
                 const int b = (int)(gi & 1);
                 if (gi >= 2 && !mbar_wait(&gempty[b], (uint32_t)(((gi >> 1) - 1) & 1), a.wait_limit)) {
                     flag_error(ZS_DEVERR_PRODUCER_WAIT);
                     ok = false;
                     break;
+                }
+                if constexpr (DYN) {
+                    tile = (int64_t)atomicAdd(a.order, 1u);
+                    rec[b] = tile;                        // published by the arrive below (release)
+                    if (tile >= ntiles) {
+                        mbar_arrive(&gfull[b]);           // no copies: the consumers read the end mark
+                        break;
+                    }
                 }
                 const int64_t i0 = a.lo + tile * T;
                 const int64_t rem = a.n - tile * T;
@@ -1617,11 +1679,15 @@ __device__ __forceinline__ void dp_tma_body(const DpTmaArgs& a) {
     const int ct = threadIdx.x - 32;                  // 0 .. NCW*32-1
     const int e = ct * VPT;                           // this thread's first element in a tile
     int64_t j = 0, t = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++t) {
+    for (int64_t tile = DYN ? 0 : blockIdx.x; DYN || tile < ntiles; tile += gridDim.x, ++t) {
         const int b = (int)(t & 1);
         if (!mbar_wait(&gfull[b], (uint32_t)((t >> 1) & 1), a.wait_limit)) {
             flag_error(ZS_DEVERR_CONSUMER_WAIT);
             return;
+        }
+        if constexpr (DYN) {
+            tile = rec[b];
+            if (tile >= ntiles) return;                   // the producer's end mark
         }
         const int64_t i0 = a.lo + tile * T;
         const int64_t rem = a.n - tile * T;
@@ -1693,13 +1759,29 @@ __global__ void __launch_bounds__(32 * (NCW + 1), MINB) k_dp_tma(const __grid_co
     dependent_launch_epilogue(a.sync);
 }
 
+// The naive-DP step over one range in one persistent launch taking its tiles in dynamic order.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, int MINB>
+__global__ void __launch_bounds__(32 * (NCW + 1), MINB) k_dp_tma_dyn(const __grid_constant__ DpTmaArgs a) {
+    dependent_launch_prologue(kSyncStream);
+    dp_tma_body<ND, NCW, VPT, MAXST, BUDGET, true>(a);
+    dyn_order_finish(a.order);
+}
+
 namespace {
 
-template <int ND, int NCW, int VPT, int MAXST, int BUDGET, int MINB = 1>
-cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, int MINB, bool DYN>
+auto dp_kernel() {
+    if constexpr (DYN)
+        return k_dp_tma_dyn<ND, NCW, VPT, MAXST, BUDGET, MINB>;
+    else
+        return k_dp_tma<ND, NCW, VPT, MAXST, BUDGET, MINB>;
+}
+
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET, int MINB = 1, bool DYN = false>
+cudaError_t dp_tma_impl(DpTmaArgs a, cudaStream_t st) {
     using Sh = DpShape<ND, NCW, VPT, MAXST, BUDGET>;
     static_assert(Sh::kSmem <= 232448, "shared memory above the per-CTA limit");
-    auto kern = k_dp_tma<ND, NCW, VPT, MAXST, BUDGET, MINB>;
+    auto kern = dp_kernel<ND, NCW, VPT, MAXST, BUDGET, MINB, DYN>();
     int sms = 0, per_sm = 0;
     cudaError_t e = staged_geometry((const void*)kern, 32 * (NCW + 1), Sh::kSmem, &sms, &per_sm);
     if (e != cudaSuccess) return e;
@@ -1707,6 +1789,10 @@ cudaError_t dp_tma_impl(const DpTmaArgs& a, cudaStream_t st) {
     if (ntiles < 1) return cudaSuccess;
     const int64_t cap = (int64_t)sms * per_sm;          // persistent: one wave of resident CTAs
     const int grid = (int)(ntiles < cap ? ntiles : cap);
+    if constexpr (DYN) {
+        e = dyn_order_pair(&a.order);
+        if (e != cudaSuccess) return e;
+    }
     return launch_kernel(kern, dim3(grid), dim3(32 * (NCW + 1)), Sh::kSmem, st, a);
 }
 
@@ -1740,6 +1826,20 @@ cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master
     a.wait_limit = 4000000000LL;                     // ~2 s at the 2.07 GHz maximum SM clock
     a.drain_limit = 4000000000LL;
     a.sync = sync;
+    if (sync == kSyncDynamic) {
+        // One launch over the whole range, tiles in dynamic order, in the walk's shapes (two CTAs per
+        // SM).  Measured on GB300 against the walk (GPT-2-small buffers, of the measured copy rate):
+        // N_d = 2 / 4 / 8 / 16: 103.8 / 103.6 / 103.7 / 103.1 % (walk 101.5-101.6 / 100.1-100.7 / 99.7 /
+        // 99.4 %).  N_d = 32 in its whole-range shape: 90.3 % against 93.1 % for the statically ordered
+        // launch, so that rank count keeps it (dp_walk_shape).
+        switch (nd) {
+            case 2: return dp_tma_impl<2, 8, 8, 16, 115712, 2, true>(a, st);
+            case 4: return dp_tma_impl<4, 8, 8, 16, 115712, 2, true>(a, st);
+            case 8: return dp_tma_impl<8, 8, 4, 16, 115712, 2, true>(a, st);
+            case 16: return dp_tma_impl<16, 8, 4, 16, 115712, 2, true>(a, st);
+            default: return cudaErrorNotSupported;
+        }
+    }
     if (sync != kSyncStream) {
         // The launches of a walk: two CTAs per SM, each with half an SM's shared memory, 8 consumer
         // warps each.  Measured on GB300 (GPT-2-small buffers walked in 4 Mi-element launches, of the

@@ -99,6 +99,7 @@ constexpr int64_t kDynMinElems = int64_t(1) << 24;
 cudaError_t launch_fused_tma_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
                                  int64_t n, const AdamScalars& s, int nd, cudaStream_t st,
                                  const AccumIn* acc = nullptr);
+// The single-output form (one output array; nd = 1: the update alone) in one dynamic-order launch.
 cudaError_t launch_fused_single_dyn(const BView& g, float* master, float* m, float* v, const BView& out, int64_t lo,
                                     int64_t n, const AdamScalars& s, int nd, cudaStream_t st);
 cudaError_t launch_gather_bulk_dyn(const uint16_t* src, int64_t src_off, const Ptrs& dst, int64_t dst_off, int64_t lo,
@@ -158,12 +159,17 @@ cudaError_t launch_gather_bulk(const uint16_t* src, int64_t src_off, const Ptrs&
                                int64_t n, int nd, cudaStream_t st, int sync = kSyncStream);
 cudaError_t launch_all_reduce_mean(const BView& g, const Range& r, int nd, cudaStream_t st);
 // Bulk-copy staged in-place all-reduce over the 8-aligned body [lo, lo + n) of every rank's buffer
-// (device memory), one launch of a walk (`sync`); cudaErrorNotSupported without a staged shape.
+// (device memory), one launch of a walk (`sync`), or with kSyncDynamic one launch over the whole body
+// taking its tiles in dynamic order (rank counts with ar_dyn_shape); cudaErrorNotSupported without a
+// staged shape.
+bool ar_dyn_shape(int nd);
 cudaError_t launch_all_reduce_tma(const BView& g, int64_t lo, int64_t n, int nd, cudaStream_t st, int sync);
 // Staged naive-DP step over the 8-aligned body [lo, lo + n) (the TMA alignment rules of
 // launch_fused_tma; every rank's master, m and v 16-byte aligned); cudaErrorNotSupported for rank
 // counts without a staged shape.  `sync` as for the fused kernel (the kernel reads through bulk copies
-// only, so it may be a later launch of a walk); walk launches need a walk shape (dp_walk_shape).
+// only, so it may be a later launch of a walk); walk launches need a walk shape (dp_walk_shape).  With
+// kSyncDynamic, one launch over the whole body taking its tiles in dynamic order (rank counts with a walk
+// shape).
 bool dp_walk_shape(int nd);
 cudaError_t launch_dp_tma(const BView& g, const BView& out, float* const* master, float* const* m,
                           float* const* v, int64_t lo, int64_t n, const AdamScalars& s, int nd, cudaStream_t st,

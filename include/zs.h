@@ -40,10 +40,12 @@
  *             back to back) for the mode with one rank per process and GPU.
  * Ownership.  The caller owns all device memory and all streams.  The library
  *             never allocates device memory; its module memory holds a status
- *             word (zs_device_status), 1024 counter pairs for the fused step's
- *             dynamic tile order (one pair per such launch in flight, drawn in
- *             turn, so at most 1024 of those launches may run at once on a
- *             device) and the staging array of zs_zero2_step_host_noalloc.
+ *             word (zs_device_status), 1024 counter pairs for the dynamic tile
+ *             order of the launches over ranges of 2^24 elements and more (the
+ *             fused steps, the ZeRO-3 gathers and updates, the update alone, the
+ *             naive-DP all-reduce and step: one pair per such launch in flight,
+ *             drawn in turn, so at most 1024 of those launches may run at once
+ *             on a device) and the staging array of zs_zero2_step_host_noalloc.
  *             The step calls never
  *             synchronise and enqueue work only on the streams they are given
  *             (a cudaStream_t; NULL is the legacy default stream); calls that

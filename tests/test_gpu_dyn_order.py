@@ -6,7 +6,8 @@ module memory: the tile counter hands out tiles front to back, the last CTA to f
 counters back to zero, and launches draw the pairs in turn (1024 of them), so launches in flight on
 several streams use different pairs.  These tests check that path against the oracle and the
 register-streaming kernel, with ragged ends, on two concurrent streams, after the pairs have all
-been used (the counters came back to zero), from a CUDA graph, and inside guard zones.
+been used (the counters came back to zero), from a CUDA graph, and inside guard zones.  The
+naive-DP all-reduce and step, and the update alone, take the same order on such buffers.
 """
 
 import numpy as np
@@ -125,7 +126,8 @@ def test_dynamic_order_step_replays_from_a_graph():
 
 
 def test_dynamic_order_step_stays_inside_its_buffers():
-    """Sentinel bytes around every buffer of a dynamic-order step survive it."""
+    """Sentinel bytes around every buffer of the dynamic-order launches (the fused step, the naive-DP
+    all-reduce and step, the update alone) survive them."""
     n_d, numel = 8, (1 << 24) + 21
     plan = zs.Plan([(numel,)], n_d, stage=2)
     P = plan.padded
@@ -146,7 +148,54 @@ def test_dynamic_order_step_stays_inside_its_buffers():
     reps = [mk(P, BF16) for _ in range(n_d)]
     master, m, v = mk(P, torch.float32), mk(P, torch.float32), mk(P, torch.float32)
     zs.zs_fused_step(plan, -1, grads, zs.ZS_RANK_FULL, master, m, v, reps, HP, 1)
+    dm = [mk(P, torch.float32) for _ in range(n_d)]
+    dmm = [mk(P, torch.float32) for _ in range(n_d)]
+    dv = [mk(P, torch.float32) for _ in range(n_d)]
+    zs.zs_dp_step(plan, grads, dm, dmm, dv, reps, HP, 1)
+    zs.zs_all_reduce_mean(plan, -1, grads)
+    zs.zs_adamw_shard_step(plan, -1, [grads[0]], zs.ZS_SHARDED, master, m, v, [reps[0]], zs.ZS_SHARDED, HP, 2)
     torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
     for raw, gb in raws:
         head, tail = raw[:gb].cpu().numpy(), raw[raw.numel() - gb:].cpu().numpy()
         assert np.all(head == fill) and np.all(tail == fill)
+
+
+@pytest.mark.parametrize("n_d,numel", [(8, (1 << 24) + 13), (2, (1 << 24) + (1 << 20) + 1), (32, (1 << 24) + 5)])
+def test_dynamic_order_all_reduce_and_dp_step_match_the_oracle(n_d, numel):
+    """Naive DP on a buffer of 2^24 elements and more: the in-place all-reduce with averaging (N_d = 4 to
+    32) and the replicated step (N_d = 2 to 16) each run as one dynamic-order launch, the ragged end
+    streamed; at N_d = 2 the all-reduce is walked and at N_d = 32 the step is one statically ordered
+    launch.  Rank 0's mean, state and replica equal the oracle's bit for bit, and every other rank's
+    equal rank 0's."""
+    plan = zs.Plan([(numel,)], n_d, stage=0)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads = synth.rank_grads(n_d, P, pads, seed=95, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)[0]
+    g_np = [H.to_np_bf16(g) for g in grads]
+    zs.zs_device_status(clear=True)
+
+    reduced = [g.clone() for g in grads]
+    zs.zs_all_reduce_mean(plan, -1, reduced)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    H.check_bf16(H.to_np_bf16(reduced[0]), steps.reduce_mean(g_np), "all-reduce rank 0")
+    assert all(torch.equal(r, reduced[0]) for r in reduced[1:]), "the ranks' means differ"
+    del reduced
+
+    master0 = synth.master_init(P, pads, seed=96, device=DEV)
+    m0, v0 = torch.rand_like(master0) * 1e-3, torch.rand_like(master0) * 1e-6
+    dm = [master0.clone() for _ in range(n_d)]
+    dmm = [m0.clone() for _ in range(n_d)]
+    dv = [v0.clone() for _ in range(n_d)]
+    reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    zs.zs_dp_step(plan, grads, dm, dmm, dv, reps, HP, 3)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    want_reps, om, omm, ov = steps.dp_step(g_np, H.to_np_f32(master0), H.to_np_f32(m0), H.to_np_f32(v0), HP, 3)
+    H.check_f32(H.to_np_f32(dm[0]), om, "master rank 0")
+    H.check_f32(H.to_np_f32(dmm[0]), omm, "m rank 0")
+    H.check_f32(H.to_np_f32(dv[0]), ov, "v rank 0")
+    H.check_bf16(H.to_np_bf16(reps[0]), want_reps[0], "replica 0")
+    for q in range(1, n_d):
+        assert torch.equal(dm[q], dm[0]) and torch.equal(dmm[q], dmm[0]) and torch.equal(dv[q], dv[0]), q
+        assert torch.equal(reps[q], reps[0]), q

@@ -652,12 +652,14 @@ def test_bulk_store_gathers_match_oracle(n_d, numel):
             assert np.array_equal(H.to_np_bf16(full_units[u][q]), want_u[q])
 
 
-@pytest.mark.parametrize("n_d,numel", [(8, 3_000_005), (3, 2_500_001), (8, 3 * (1 << 22) + 5)])
+@pytest.mark.parametrize("n_d,numel", [(8, 3_000_005), (3, 2_500_001), (8, 3 * (1 << 22) + 5), (2, (1 << 24) + 13)])
 def test_staged_adamw_on_sharded_buffers(variant, n_d, numel):
     """zs_adamw_shard_step with the reduced gradient and the parameters in ZS_SHARDED arrays runs
     through the staged kernel with one rank, walked in overlapping launches (3 x 2^22 + 5 elements:
-    three launches, the later two streaming while their predecessor drains); whole-unit and per-rank
-    calls (ragged shard bounds) equal the oracle and the streaming kernel bit for bit."""
+    three launches, the later two streaming while their predecessor drains), or from 2^24 elements on
+    in one dynamic-order launch (the whole-buffer call at 2^24 + 13; its per-rank calls are walked);
+    whole-unit and per-rank calls (ragged shard bounds) equal the oracle and the streaming kernel bit
+    for bit."""
     plan, ref = _plans([(numel,)], n_d)
     P, pads = plan.padded, plan.pad_ranges()
     master0 = synth.master_init(P, pads, seed=61, device=DEV)
