@@ -199,3 +199,48 @@ def test_dynamic_order_all_reduce_and_dp_step_match_the_oracle(n_d, numel):
     for q in range(1, n_d):
         assert torch.equal(dm[q], dm[0]) and torch.equal(dmm[q], dmm[0]) and torch.equal(dv[q], dv[0]), q
         assert torch.equal(reps[q], reps[0]), q
+
+
+def test_different_dynamic_order_kernels_share_the_counter_pairs():
+    """Dynamic-order launches of different kernels draw from the same 1024 counter pairs: the naive-DP
+    step on one stream, the in-place all-reduce and the update alone on another, 400 rounds each
+    (1,200 launches, so every pair is drawn by more than one kernel), equal the same rounds run by the
+    register-streaming kernels one stream at a time, bit for bit."""
+    n_d, numel = 4, (1 << 24) + 3
+    plan = zs.Plan([(numel,)], n_d, stage=0)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads = synth.rank_grads(n_d, P, pads, seed=97, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)[0]
+    master0 = synth.master_init(P, pads, seed=98, device=DEV)
+
+    def fresh():
+        dp = ([master0.clone() for _ in range(n_d)], [torch.zeros_like(master0) for _ in range(n_d)],
+              [torch.zeros_like(master0) for _ in range(n_d)], synth.rank_buffers(n_d, P, BF16, DEV)[0])
+        ar = [g.clone() for g in grads]
+        up = (master0.clone(), torch.zeros_like(master0), torch.zeros_like(master0),
+              torch.zeros(P, dtype=BF16, device=DEV))
+        return dp, ar, up
+
+    def run(bufs, streams):
+        dp, ar, up = bufs
+        for t in range(1, 401):
+            zs.zs_dp_step(plan, grads, *dp, HP, t, stream=streams[0])
+            zs.zs_all_reduce_mean(plan, -1, ar, stream=streams[1])
+            zs.zs_adamw_shard_step(plan, -1, [ar[0]], zs.ZS_SHARDED, *up[:3], [up[3]], zs.ZS_SHARDED, HP, t,
+                                   stream=streams[1])
+        torch.cuda.synchronize()
+
+    got = fresh()
+    zs.zs_device_status(clear=True)
+    run(got, [torch.cuda.Stream(), torch.cuda.Stream()])
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    want = fresh()
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
+    try:
+        s = torch.cuda.current_stream()
+        run(want, [s, s])
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+    for a, b in zip(got[0], want[0]):
+        assert all(torch.equal(x, y) for x, y in zip(a, b)), "naive-DP step differs"
+    assert all(torch.equal(x, y) for x, y in zip(got[1], want[1])), "all-reduce differs"
+    assert all(torch.equal(x, y) for x, y in zip(got[2], want[2])), "update differs"
