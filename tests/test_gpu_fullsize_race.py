@@ -2,18 +2,21 @@
 
 The benchmarked fused step is one launch whose CTAs take their tiles in dynamic order from a
 counter, and the ZeRO-3 step runs its gathers and updates on two streams, each unit's phase one such
-launch (units of 2^24 elements and more) or walked in overlapping launches.  A race there would show as a run-to-run difference,
-so each step below runs repeatedly from the same state and must equal, bit for bit, a reference run
-of the same step:
+launch (units of 2^24 elements and more) or walked in overlapping launches.  A race there would show
+as a run-to-run difference, so each step below runs repeatedly from the same state and must equal,
+bit for bit, a reference run of the same step:
 
 * the Llama-1.3B ZeRO-2 step at N_d = 8, the call the benchmark times (one dynamic-order launch),
   ten times (1.3e10 element-steps), against the register-streaming kernel;
-* the ZeRO-3 step on the Llama-1.3B units at N_d = 8 (25 units of ~50 M elements, each unit's gathers
-  and update one dynamic-order launch, two streams, the 2-slot pool), five times, against the same step with programmatic
-  dependent launch off (every launch waiting for the previous one to complete) on one stream.
+* the ZeRO-3 step on the Llama-1.3B units at N_d = 8 (25 units of ~50 M elements, each unit's
+  gathers and update one dynamic-order launch, two streams, the 2-slot pool), five times, against
+  the same step with programmatic dependent launch off (every launch waiting for the previous one
+  to complete) on one stream;
+* the naive-DP step and the in-place all-reduce on the GPT-2-small buffers at N_d = 8 (one
+  dynamic-order launch each), against the register-streaming kernels.
 
-The oracle itself is not needed here: every-element oracle parity of these calls is in
-test_gpu_fullsize_every_element.py.
+The oracle itself is not needed here: every-element oracle parity of the headline call is in
+test_gpu_fullsize_every_element.py, and of the naive-DP forms in test_gpu_dyn_order.py.
 """
 
 import gc
@@ -110,4 +113,45 @@ def test_llama13b_units_zero3_walk_repeats_the_serialised_step():
         torch.cuda.synchronize()
         assert all(torch.equal(x, y) for x, y in zip(st, ref_st)), "run %d: state differs" % k
         assert torch.equal(sh, ref_sh), "run %d: shards differ" % k
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+
+
+def test_gpt2_naive_dp_step_repeats_the_streaming_result():
+    """The naive-DP step on the GPT-2-small buffers at N_d = 8 (one dynamic-order launch over 124 M
+    elements, every rank's full state), five times from the same state, and the in-place all-reduce
+    on the same gradients: bit for bit the register-streaming kernels' results."""
+    n_d = 8
+    shapes, _ = synth.workload_params("gpt2-small")
+    plan = zs.Plan(shapes, n_d, stage=0)
+    P, pads = plan.padded, plan.pad_ranges()
+    _need(P * (2 * n_d * 4 + 12 * n_d * 3 + 12) + (4 << 30))
+    grads, _ = synth.rank_grads(n_d, P, pads, seed=11, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)
+    master0 = synth.master_init(P, pads, 12, device=DEV)
+    m0, v0 = torch.rand_like(master0) * 1e-3, torch.rand_like(master0) * 1e-6
+
+    def state():
+        return ([master0.clone() for _ in range(n_d)], [m0.clone() for _ in range(n_d)],
+                [v0.clone() for _ in range(n_d)], synth.rank_buffers(n_d, P, BF16, DEV)[0])
+
+    ref = state()
+    ref_ar = [g.clone() for g in grads]
+    zs.zs_set_fused_variant(zs.ZS_FUSED_LDG)
+    try:
+        zs.zs_dp_step(plan, grads, *ref, HP, 2)
+        zs.zs_all_reduce_mean(plan, -1, ref_ar)
+        torch.cuda.synchronize()
+    finally:
+        zs.zs_set_fused_variant(zs.ZS_FUSED_AUTO)
+    zs.zs_device_status(clear=True)
+    for k in range(5):
+        got = state()
+        zs.zs_dp_step(plan, grads, *got, HP, 2)
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert all(torch.equal(x, y) for x, y in zip(a, b)), "run %d: the naive-DP step differs" % k
+        del got
+    ar = [g.clone() for g in grads]
+    zs.zs_all_reduce_mean(plan, -1, ar)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(ar, ref_ar)), "the all-reduce differs"
     assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
