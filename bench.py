@@ -991,6 +991,16 @@ def run_next(args, ws, rank, local):
             P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), z3n,
             comm_bytes_per_rank=plan.comm_bytes(3, reshard))
         launches += steps * z3n
+
+        # the same step on one stream (side_stream = main_stream: stream order, no events)
+        def z3_one(slots=slots, reshard=reshard):
+            t[0] += 1
+            zs.zs_zero3_step(plan, shards, master, m, v, [ugrads] * U, slots, reshard, hp, t[0],
+                             main_stream=stream, side_stream=stream)
+
+        row("ZeRO-3 step, reshard_after_forward=%s, one stream (no events)" % reshard, timed(z3_one), plan.numel,
+            P * (gathers * (2 + 2 * n_d) + (2 * n_d + 26)), z3n)
+        launches += steps * z3n
         # the same step captured once (both streams) and replayed; the replay repeats its step number
         g3, cs = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
         with torch.cuda.graph(g3, stream=cs):

@@ -83,16 +83,19 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
     const zs::AdamScalars s{sc[0], sc[1], sc[2], sc[3], sc[4], sc[5], sc[6], sc[7]};
 
     cudaStream_t mainS = (cudaStream_t)main_stream, sideS = (cudaStream_t)side_stream;
+    // On one stream (main_stream == side_stream) stream order already gives every dependency below, so
+    // no event is created, recorded or waited on, and each launch follows the previous one directly.
+    const bool one = mainS == sideS;
     Events E;
     // per unit: gathered (fwd), released (fwd), gathered (bwd), backward done, released (bwd)
-    cudaError_t err = E.make((size_t)U * 5 + 2);
+    cudaError_t err = one ? cudaSuccess : E.make((size_t)U * 5 + 2);
     if (err != cudaSuccess) {
         zs::set_error(std::string(fn) + ": " + cudaGetErrorString(err));
         return ZS_ERR_CUDA;
     }
-    auto ev = [&](int u, int k) { return E.ev[(size_t)u * 5 + k]; };
-    cudaEvent_t start = E.ev[(size_t)U * 5];
-    cudaEvent_t done = E.ev[(size_t)U * 5 + 1];
+    auto ev = [&](int u, int k) { return one ? nullptr : E.ev[(size_t)u * 5 + k]; };
+    cudaEvent_t start = one ? nullptr : E.ev[(size_t)U * 5];
+    cudaEvent_t done = one ? nullptr : E.ev[(size_t)U * 5 + 1];
 
     zs::BView shard_view;
     for (int q = 0; q < ZS_MAX_RANKS; ++q) shard_view.ptr.p[q] = (uint16_t*)shards;
@@ -111,6 +114,12 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
     };
     auto check = [&](cudaError_t e) {
         if (e != cudaSuccess && err == cudaSuccess) err = e;
+    };
+    auto record = [&](cudaEvent_t e, cudaStream_t on) {
+        if (!one) check(cudaEventRecord(e, on));
+    };
+    auto wait = [&](cudaStream_t on, cudaEvent_t e) {
+        if (!one && e) check(cudaStreamWaitEvent(on, e, 0));
     };
     // A unit's gather and its reduce-scatter + update are each a walk over the unit's range: pieces cut
     // at multiples of kWalkChunk (none shorter than a quarter of it), one launch each, the first
@@ -141,8 +150,8 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
     };
 
     // the side stream starts after everything already enqueued on main
-    check(cudaEventRecord(start, mainS));
-    check(cudaStreamWaitEvent(sideS, start, 0));
+    record(start, mainS);
+    wait(sideS, start);
 
     zs::TraceRange step_range("zs_zero3_step");
     // forward, unit order
@@ -151,12 +160,12 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
         zs::TraceRange r_("zero3 forward gather unit %lld", (long long)u);
         const zs::Unit& un = plan->units[u];
         const int slot = reshard_after_forward ? (u & 1) : u;
-        if (reshard_after_forward && slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
+        if (reshard_after_forward) wait(sideS, slot_free[slot]);
         gather(slot, un);
-        check(cudaEventRecord(ev(u, 0), sideS));
-        check(cudaStreamWaitEvent(mainS, ev(u, 0), 0));
+        record(ev(u, 0), sideS);
+        wait(mainS, ev(u, 0));
         // forward(u) runs here on main; afterwards the gathered parameters are released
-        check(cudaEventRecord(ev(u, 1), mainS));
+        record(ev(u, 1), mainS);
         if (reshard_after_forward) slot_free[slot] = ev(u, 1);
     }
 
@@ -168,33 +177,33 @@ extern "C" int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float*
         zs::TraceRange r_("zero3 backward gather unit %lld", (long long)u);
         const zs::Unit& un = plan->units[u];
         const int slot = u & 1;
-        if (slot_free[slot]) check(cudaStreamWaitEvent(sideS, slot_free[slot], 0));
+        wait(sideS, slot_free[slot]);
         gather(slot, un);
-        check(cudaEventRecord(ev(u, 2), sideS));
+        record(ev(u, 2), sideS);
     };
     if (reshard_after_forward && U > 0 && err == cudaSuccess) backward_gather(U - 1);
     for (int u = U - 1; u >= 0 && err == cudaSuccess; --u) {
         zs::TraceRange r_("zero3 backward reduce-scatter/update unit %lld", (long long)u);
         const zs::Unit& un = plan->units[u];
         if (reshard_after_forward) {
-            check(cudaStreamWaitEvent(mainS, ev(u, 2), 0));
+            wait(mainS, ev(u, 2));
             // backward(u) runs here on main and produces unit_grads[u]; then the slot is released
-            check(cudaEventRecord(ev(u, 4), mainS));
+            record(ev(u, 4), mainS);
             slot_free[u & 1] = ev(u, 4);
             if (u > 0) backward_gather(u - 1);
         } else {
-            check(cudaStreamWaitEvent(mainS, ev(u, 0), 0));   // still gathered from forward
+            wait(mainS, ev(u, 0));                           // still gathered from forward
         }
-        check(cudaEventRecord(ev(u, 3), mainS));             // backward(u) done: its gradients exist
-        check(cudaStreamWaitEvent(sideS, ev(u, 3), 0));
+        record(ev(u, 3), mainS);                             // backward(u) done: its gradients exist
+        wait(sideS, ev(u, 3));
         walk(un, [&](const zs::Range& r, int sync) {
             return zs::launch_fused(grad_view(u), master, m, v, shard_view, false, r, s, nd, sideS,
                                     zs::kStagedIfDevice, sync);
         });
     }
     // main continues (the next step's forward) only after the last update
-    check(cudaEventRecord(done, sideS));
-    check(cudaStreamWaitEvent(mainS, done, 0));
+    record(done, sideS);
+    wait(mainS, done);
     if (err != cudaSuccess) {
         zs::set_error(std::string(fn) + ": " + cudaGetErrorString(err));
         return ZS_ERR_CUDA;

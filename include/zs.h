@@ -578,7 +578,8 @@ int zs_zero2_step_host_noalloc(zs_plan_t plan, const void* const* host_grads, fl
  * update.  With two slots the next unit's gather overlaps the current unit's use;
  * in backward the next unit's gather is issued before the current unit's
  * reduce-scatter and update (backward prefetch).
- * side_stream may equal main_stream (everything serialised; same results).
+ * side_stream may equal main_stream (everything serialised in stream order, no
+ * event used; same results).
  *   shards       ZS_SHARDED bf16 parameter shards (updated in place).
  *   master,m,v   ZS_SHARDED fp32.
  *   unit_grads   n_units * N_d pointers; unit u, rank q at [u*N_d + q], each
@@ -587,7 +588,7 @@ int zs_zero2_step_host_noalloc(zs_plan_t plan, const void* const* host_grads, fl
  *                at least the largest unit's padded size.  pool_slots >= 2 (1 for
  *                a single unit) with reshard_after_forward, >= n_units without;
  *                afterwards each slot holds the last unit gathered into it.
- * The call creates and releases CUDA events (no device memory).
+ * With two streams the call creates and releases CUDA events (no device memory).
  * Errors: ZS_ERR_INVALID (checked before anything is enqueued), ZS_ERR_CUDA. */
 int zs_zero3_step(zs_plan_t plan, void* shards, float* master, float* m, float* v,
                   const void* const* unit_grads, void* const* pool, int32_t pool_slots,
