@@ -1409,13 +1409,22 @@ __global__ void __launch_bounds__(32 * (NCW + 1)) k_ar_tma_dyn(const __grid_cons
     dyn_order_finish(a.order);
 }
 
+// The reduce-scatter into one array over one range in one persistent launch, dynamic tile order.
+template <int ND, int NCW, int VPT, int MAXST, int BUDGET>
+__global__ void __launch_bounds__(32 * (NCW + 1)) k_rs_tma_dyn(const __grid_constant__ RsTmaArgs a) {
+    dependent_launch_prologue(kSyncStream);
+    rs_tma_body<ND, NCW, VPT, MAXST, BUDGET, false, true>(a);
+    dyn_order_finish(a.order);
+}
+
 namespace {
 
 template <int ND, int NCW, int VPT, int MAXST, int BUDGET, bool ALL, bool DYN>
 auto rs_kernel() {
-    if constexpr (DYN) {
-        static_assert(ALL, "the reduce-scatter has no dynamic-order form");
+    if constexpr (DYN && ALL) {
         return k_ar_tma_dyn<ND, NCW, VPT, MAXST, BUDGET>;
+    } else if constexpr (DYN) {
+        return k_rs_tma_dyn<ND, NCW, VPT, MAXST, BUDGET>;
     } else if constexpr (ALL) {
         return k_ar_tma<ND, NCW, VPT, MAXST, BUDGET>;
     } else {
@@ -1460,7 +1469,12 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
     return a;
 }
 
-// Returns cudaErrorNotSupported when no staged shape exists for this rank count.
+// Returns cudaErrorNotSupported when no staged shape exists for this rank count.  At N_d = 8, 16 and
+// 32 a body of kDynMinElems or more is one launch taking its tiles in dynamic order, in the same
+// shapes: measured on GB300 (of the measured copy rate) 101.9 -> 106.5 % on the Llama-1.3B buffer at
+// N_d = 8, 100.8 -> 102.1 / 93.7 -> 103.0 % on the 2^28+7 buffer at N_d = 16 / 32.  At N_d = 2 and 4
+// the tiles carry 6-10 KB each, too little per draw from the one tile counter (38.5 / 34.7 % against
+// 97.1-97.6 / 98.4-98.6 %), so those keep the static order.
 cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
                           cudaStream_t st) {
     bool ok = body_ok(lo, n) && at_ok(out, lo - out_off);
@@ -1469,6 +1483,14 @@ cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_
     RsTmaArgs a = rs_args(g, lo, n, nd);
     a.out = out;
     a.out_off = out_off;
+    if (n >= kDynMinElems && nd >= 8) {
+        switch (nd) {
+            case 8: return rs_tma_impl<8, 8, 8, 2, 232448, false, true>(a, st);
+            case 16: return rs_tma_impl<16, 8, 8, 2, 232448, false, true>(a, st);
+            case 32: return rs_tma_impl<32, 2, 4, 2, 232448, false, true>(a, st);
+            default: return cudaErrorNotSupported;
+        }
+    }
     // shapes per rank count from a measured sweep on GB300 (consumer warps x elements per thread x
     // ring depth, 2^27-element buffers): 96 / 99 / 100 / 102 / 102 % of the measured copy rate for
     // N_d = 2 / 4 / 8 / 16 / 32, against ~94 % for the register-streaming kernel

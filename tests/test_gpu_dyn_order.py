@@ -7,7 +7,8 @@ counters back to zero, and launches draw the pairs in turn (1024 of them), so la
 several streams use different pairs.  These tests check that path against the oracle and the
 register-streaming kernel, with ragged ends, on two concurrent streams, after the pairs have all
 been used (the counters came back to zero), from a CUDA graph, and inside guard zones.  The
-naive-DP all-reduce and step, and the update alone, take the same order on such buffers.
+naive-DP all-reduce and step, the update alone, and the unfused reduce-scatter and all-gather take
+the same order on such buffers.
 """
 
 import numpy as np
@@ -244,3 +245,24 @@ def test_different_dynamic_order_kernels_share_the_counter_pairs():
         assert all(torch.equal(x, y) for x, y in zip(a, b)), "naive-DP step differs"
     assert all(torch.equal(x, y) for x, y in zip(got[1], want[1])), "all-reduce differs"
     assert all(torch.equal(x, y) for x, y in zip(got[2], want[2])), "update differs"
+
+
+@pytest.mark.parametrize("n_d,numel", [(8, (1 << 24) + 13), (2, (1 << 24) + (1 << 20) + 1), (32, (1 << 24) + 5)])
+def test_dynamic_order_reduce_scatter_and_all_gather_match_the_oracle(n_d, numel):
+    """The unfused ZeRO-2 reduce-scatter with averaging into the sharded array and the all-gather from
+    it, each one dynamic-order launch over a unit of 2^24 elements and more (the ragged end
+    streamed): the reduced gradient equals the oracle's mean bit for bit, every replica equals the
+    sharded source."""
+    plan = zs.Plan([(numel,)], n_d, stage=2)
+    P, pads = plan.padded, plan.pad_ranges()
+    grads = synth.rank_grads(n_d, P, pads, seed=99, step=1, sigma=1e-3, outlier_p=0.001, device=DEV)[0]
+    ghat = torch.zeros(P, dtype=BF16, device=DEV)
+    reps = synth.rank_buffers(n_d, P, BF16, DEV)[0]
+    zs.zs_device_status(clear=True)
+    zs.zs_reduce_scatter_mean(plan, -1, grads, zs.ZS_RANK_FULL, [ghat], zs.ZS_SHARDED)
+    zs.zs_all_gather(plan, [ghat], zs.ZS_SHARDED, reps)
+    torch.cuda.synchronize()
+    assert zs.zs_device_status() == zs.ZS_DEVERR_NONE
+    H.check_bf16(H.to_np_bf16(ghat), steps.reduce_mean([H.to_np_bf16(g) for g in grads]), "reduced gradient")
+    for q in range(n_d):
+        assert torch.equal(reps[q], ghat), "replica %d" % q
