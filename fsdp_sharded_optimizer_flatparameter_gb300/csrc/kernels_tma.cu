@@ -1473,7 +1473,7 @@ static RsTmaArgs rs_args(const BView& g, int64_t lo, int64_t n, int nd) {
 // 32 a body of kDynMinElems or more is one launch taking its tiles in dynamic order, in the same
 // shapes: measured on GB300 (of the measured copy rate) 101.9 -> 106.5 % on the Llama-1.3B buffer at
 // N_d = 8, 100.8 -> 102.1 / 93.7 -> 103.0 % on the 2^28+7 buffer at N_d = 16 / 32.  At N_d = 2 and 4
-// the tiles carry 6-10 KB each, too little per draw from the one tile counter (38.5 / 34.7 % against
+// the tiles carry 5-6 KB each, too little per draw from the one tile counter (38.5 / 34.7 % against
 // 97.1-97.6 / 98.4-98.6 %), so those keep the static order.
 cudaError_t launch_rs_tma(const BView& g, uint16_t* out, int64_t out_off, int64_t lo, int64_t n, int nd,
                           cudaStream_t st) {
